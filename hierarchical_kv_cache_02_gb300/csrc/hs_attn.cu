@@ -1,0 +1,488 @@
+// Sparse attention over resolved slots (HiSparse summary §3 step (4): the physical slots
+// published by RESOLVE go to the sparse-attention backend, which gathers exactly those records).
+//
+// CUDA-core variant, used when few query heads share a KV block (GQA, 4 heads per KV head) and
+// as the MLA fallback.  Design:
+//   * grid (split, request, head group); a split is a fixed range of top-k entries, so the
+//     reduction order depends only on the top-k order and never on which slot holds a record
+//     (cold, warm and fully-resident runs are bit-identical);
+//   * one producer warp gathers whole records HBM -> shared memory with cp.async.bulk into a
+//     3-stage ring guarded by mbarriers (bounded waits); consumer warps own one KV block each;
+//   * per stage, a warp holds G heads x T tokens = 32 logits per lane and reduces them with a
+//     transposed butterfly (31 shuffles for 32 sums), then an online softmax in base 2;
+//   * the last CTA of a (request, head group) to finish combines the split partials in split
+//     order (atomic ticket, no waiting).
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "hs_internal.cuh"
+
+namespace {
+
+constexpr int kStages = 3;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct AttnArgs {
+  const uint16_t* q;     // [R][Hq][DK] bf16
+  const int32_t* locs;   // [R][k]
+  const uint8_t* kv;     // row base: row (r, loc) at kv + (r * rows + loc) * rec
+  float* out;            // [R][Hq][DV]
+  float* part;           // [R][S][Hq][DV]
+  float* ml;             // [R][S][Hq][2]
+  uint32_t* ticket;      // [R][groups]
+  uint32_t* err;
+  int64_t rows, rec;
+  int64_t kstride, vdelta;  // K of KV block g at g * kstride, V at K + vdelta (bytes)
+  float qscale;             // scale * log2(e)
+  int R, Hq, k, S, chunk, groups;
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for phase `parity` of `bar`; give up after ~1 s or when another warp raised *abort.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile uint32_t* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0u) {
+      if (*abort) return false;
+      if (global_ns() - t0 > 1000000000ull) return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// 32 partial sums per lane -> lane l holds the warp-wide sum of value l.
+__device__ __forceinline__ float reduce32_transposed(float (&v)[32], int lane) {
+#pragma unroll
+  for (int step = 0; step < 5; ++step) {
+    const int off = 16 >> step;
+    const int n = 32 >> step;
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      const float send = upper ? v[i] : v[i + n / 2];
+      const float keep = upper ? v[i + n / 2] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+  }
+  return v[0];
+}
+
+template <int DK, int DV, int G, int NW>
+struct AttnCfg {
+  static constexpr int T = 32 / G;      // tokens per stage
+  static constexpr int DKW = DK / 64;   // bf16 pairs per lane of a K row
+  static constexpr int DVW = DV / 64;   // bf16 pairs per lane of a V row
+  static constexpr int THREADS = (NW + 1) * 32;
+  static_assert(G * T == 32, "G must divide 32");
+  static_assert(DK % 64 == 0 && DV % 64 == 0, "head dims must be multiples of 64");
+};
+
+template <int DK, int DV, int G, int NW>
+__global__ void __launch_bounds__(AttnCfg<DK, DV, G, NW>::THREADS) k_attn_cc(AttnArgs a) {
+  using C = AttnCfg<DK, DV, G, NW>;
+  constexpr int T = C::T, DKW = C::DKW, DVW = C::DVW;
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t full_bar[kStages];
+  __shared__ __align__(8) uint64_t empty_bar[kStages];
+  __shared__ uint32_t tok_mask[kStages];
+  __shared__ uint32_t abort_flag;
+  __shared__ uint32_t is_last;
+
+  const int split = blockIdx.x, r = blockIdx.y, grp = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t0 = split * a.chunk;
+  const int t1 = min(a.k, t0 + a.chunk);
+  const int nst = (t1 - t0 + T - 1) / T;
+  const int64_t rec = a.rec;
+  const int32_t* locs = a.locs + (int64_t)r * a.k;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full_bar[s], 1u);
+      mbar_init(&empty_bar[s], (uint32_t)NW);
+    }
+    abort_flag = 0u;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+
+  float m_run[G], l_run[G], o[G][DVW][2];
+  const int g = grp * NW + warp;  // KV block of this consumer warp
+
+  if (warp == NW) {
+    // ---------------- producer: gather records into the ring ----------------
+    if (lane == 0) {
+      uint32_t bad = 0u;
+      int issued = 0;
+      for (int st = 0; st < nst; ++st) {
+        const int b = st % kStages;
+        if (st >= kStages) {
+          if (!mbar_wait_bounded(&empty_bar[b], (uint32_t)((st / kStages - 1) & 1), &abort_flag)) {
+            *(volatile uint32_t*)&abort_flag = 1u;
+            atomicOr(a.err, (uint32_t)HS_DEVERR_TIMEOUT);
+            break;
+          }
+        }
+        uint32_t mask = 0u, nvalid = 0u;
+        int32_t lc[T];
+#pragma unroll
+        for (int j = 0; j < T; ++j) {
+          const int idx = t0 + st * T + j;
+          int32_t loc = idx < t1 ? locs[idx] : -1;
+          if (loc < -1 || (int64_t)loc >= a.rows) {
+            bad = 1u;
+            loc = -1;
+          }
+          lc[j] = loc;
+          if (loc >= 0) {
+            mask |= 1u << j;
+            ++nvalid;
+          }
+        }
+        tok_mask[b] = mask;
+        mbar_arrive_expect_tx(&full_bar[b], nvalid * (uint32_t)rec);
+        uint8_t* dst = smem + (size_t)b * T * rec;
+#pragma unroll
+        for (int j = 0; j < T; ++j) {
+          if (lc[j] >= 0)
+            bulk_g2s(dst + (size_t)j * rec, a.kv + ((int64_t)r * a.rows + lc[j]) * rec, (uint32_t)rec, &full_bar[b]);
+        }
+        issued = st + 1;
+      }
+      if (bad) atomicOr(a.err, (uint32_t)HS_DEVERR_LOC);
+      if (abort_flag) {
+        // let copies already issued land before the CTA can retire
+        for (int st = max(0, issued - kStages); st < issued; ++st) {
+          volatile uint32_t never = 0u;
+          mbar_wait_bounded(&full_bar[st % kStages], (uint32_t)((st / kStages) & 1), &never);
+        }
+      }
+    }
+  } else {
+    // ---------------- consumers: one KV block, G query heads ----------------
+    float qf[G][DKW][2];
+    const int hbase = g * G;
+#pragma unroll
+    for (int x = 0; x < G; ++x) {
+      const uint32_t* qw = (const uint32_t*)(a.q + ((int64_t)r * a.Hq + hbase + x) * DK);
+#pragma unroll
+      for (int u = 0; u < DKW; ++u) {
+        const uint32_t w = qw[lane + 32 * u];
+        qf[x][u][0] = bf_lo(w) * a.qscale;
+        qf[x][u][1] = bf_hi(w) * a.qscale;
+      }
+      m_run[x] = -INFINITY;
+      l_run[x] = 0.f;
+#pragma unroll
+      for (int u = 0; u < DVW; ++u) o[x][u][0] = o[x][u][1] = 0.f;
+    }
+    const int64_t koff = (int64_t)g * a.kstride;
+    const int64_t voff = koff + a.vdelta;
+    const int my_x = lane / T, my_j = lane % T;
+    for (int st = 0; st < nst; ++st) {
+      const int b = st % kStages;
+      if (!mbar_wait_bounded(&full_bar[b], (uint32_t)((st / kStages) & 1), &abort_flag)) {
+        *(volatile uint32_t*)&abort_flag = 1u;
+        atomicOr(a.err, (uint32_t)HS_DEVERR_TIMEOUT);
+        break;
+      }
+      const uint32_t mask = tok_mask[b];
+      const uint8_t* stage = smem + (size_t)b * T * rec;
+      float s[32];
+#pragma unroll
+      for (int j = 0; j < T; ++j) {
+        const uint32_t* kw = (const uint32_t*)(stage + j * rec + koff);
+        uint32_t w[DKW];
+#pragma unroll
+        for (int u = 0; u < DKW; ++u) w[u] = kw[lane + 32 * u];
+#pragma unroll
+        for (int x = 0; x < G; ++x) {
+          float acc = 0.f;
+#pragma unroll
+          for (int u = 0; u < DKW; ++u) {
+            acc = fmaf(qf[x][u][0], bf_lo(w[u]), acc);
+            acc = fmaf(qf[x][u][1], bf_hi(w[u]), acc);
+          }
+          s[x * T + j] = acc;
+        }
+      }
+      float logit = reduce32_transposed(s, lane);
+      if (!((mask >> my_j) & 1u)) logit = -INFINITY;
+      float smax = logit;
+#pragma unroll
+      for (int off = T / 2; off > 0; off >>= 1) smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, off));
+      float mnew_mine = fmaxf(m_run[my_x], smax);
+      const float p = mnew_mine == -INFINITY ? 0.f : exp2f(logit - mnew_mine);
+      float psum = p;
+#pragma unroll
+      for (int off = T / 2; off > 0; off >>= 1) psum += __shfl_xor_sync(0xffffffffu, psum, off);
+#pragma unroll
+      for (int x = 0; x < G; ++x) {
+        const float mnew = __shfl_sync(0xffffffffu, mnew_mine, x * T);
+        const float ps = __shfl_sync(0xffffffffu, psum, x * T);
+        const float alpha = mnew == -INFINITY ? 1.f : exp2f(m_run[x] - mnew);
+        m_run[x] = mnew;
+        l_run[x] = l_run[x] * alpha + ps;
+#pragma unroll
+        for (int u = 0; u < DVW; ++u) {
+          o[x][u][0] *= alpha;
+          o[x][u][1] *= alpha;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < T; ++j) {
+        if (!((mask >> j) & 1u)) continue;
+        const uint32_t* vw = (const uint32_t*)(stage + j * rec + voff);
+        uint32_t w[DVW];
+#pragma unroll
+        for (int u = 0; u < DVW; ++u) w[u] = vw[lane + 32 * u];
+#pragma unroll
+        for (int x = 0; x < G; ++x) {
+          const float pj = __shfl_sync(0xffffffffu, p, x * T + j);
+#pragma unroll
+          for (int u = 0; u < DVW; ++u) {
+            o[x][u][0] = fmaf(pj, bf_lo(w[u]), o[x][u][0]);
+            o[x][u][1] = fmaf(pj, bf_hi(w[u]), o[x][u][1]);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[b]);
+    }
+    if (!abort_flag) {
+      // split partial: unnormalised o, running max (base 2) and sum
+#pragma unroll
+      for (int x = 0; x < G; ++x) {
+        const int64_t ph = ((int64_t)r * a.S + split) * a.Hq + hbase + x;
+        float2* po = (float2*)(a.part + ph * DV);
+#pragma unroll
+        for (int u = 0; u < DVW; ++u) po[lane + 32 * u] = make_float2(o[x][u][0], o[x][u][1]);
+        if (lane == 0) {
+          a.ml[ph * 2 + 0] = m_run[x];
+          a.ml[ph * 2 + 1] = l_run[x];
+        }
+      }
+    }
+  }
+  __threadfence();  // every writer publishes its partials before the ticket
+  __syncthreads();
+  if (abort_flag) return;
+  if (threadIdx.x == 0) {
+    const uint32_t t = atomicAdd(&a.ticket[(int64_t)r * a.groups + grp], 1u);
+    is_last = (t == (uint32_t)(a.S - 1)) ? 1u : 0u;
+  }
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  if (warp < NW) {
+    const int hbase = g * G;
+#pragma unroll 1
+    for (int x = 0; x < G; ++x) {
+      const int h = hbase + x;
+      float M = -INFINITY;
+      for (int s2 = 0; s2 < a.S; ++s2) M = fmaxf(M, __ldcg(&a.ml[(((int64_t)r * a.S + s2) * a.Hq + h) * 2]));
+      float acc[DVW][2];
+#pragma unroll
+      for (int u = 0; u < DVW; ++u) acc[u][0] = acc[u][1] = 0.f;
+      float den = 0.f;
+      if (M != -INFINITY) {
+        for (int s2 = 0; s2 < a.S; ++s2) {
+          const int64_t ph = ((int64_t)r * a.S + s2) * a.Hq + h;
+          const float ms = __ldcg(&a.ml[ph * 2]);
+          const float w = ms == -INFINITY ? 0.f : exp2f(ms - M);
+          den += w * __ldcg(&a.ml[ph * 2 + 1]);
+          const float2* po = (const float2*)(a.part + ph * DV);
+#pragma unroll
+          for (int u = 0; u < DVW; ++u) {
+            const float2 v = __ldcg(&po[lane + 32 * u]);
+            acc[u][0] = fmaf(w, v.x, acc[u][0]);
+            acc[u][1] = fmaf(w, v.y, acc[u][1]);
+          }
+        }
+      }
+      const float inv = den > 0.f ? 1.f / den : 0.f;
+      float2* out = (float2*)(a.out + ((int64_t)r * a.Hq + h) * DV);
+#pragma unroll
+      for (int u = 0; u < DVW; ++u) out[lane + 32 * u] = make_float2(acc[u][0] * inv, acc[u][1] * inv);
+    }
+  }
+  if (threadIdx.x == 0) a.ticket[(int64_t)r * a.groups + grp] = 0u;
+}
+
+// ---- dispatch ----------------------------------------------------------------
+
+struct Plan {
+  int NW, G, T, groups, S, chunk;
+  size_t smem;
+};
+
+bool plan_for(const hs_config* c, int num_sms, Plan* pl) {
+  const int64_t rec = hs_record_bytes(c);
+  if (c->layout == HS_LAYOUT_GQA) {
+    if (c->head_dim_qk != 128 || c->head_dim_v != 128) return false;
+    const int G = c->num_q_heads / c->num_kv_heads;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return false;
+    int NW = c->num_kv_heads;
+    if (NW > 8) {
+      if (NW % 8 != 0) return false;
+      NW = 8;
+    }
+    pl->NW = NW;
+    pl->G = G;
+    pl->groups = c->num_kv_heads / NW;
+  } else {
+    if (c->head_dim_qk != 576 || c->head_dim_v != 512) return false;
+    if (c->num_q_heads % 8 != 0) return false;
+    pl->NW = 8;
+    pl->G = 1;
+    pl->groups = c->num_q_heads / 8;
+  }
+  pl->T = 32 / pl->G;
+  pl->smem = (size_t)kStages * pl->T * (size_t)rec;
+  if (pl->smem > 200 * 1024) return false;
+  const int per_split = c->num_requests * pl->groups;
+  int S = (2 * num_sms + per_split - 1) / per_split;
+  const int max_s = (c->top_k + pl->T - 1) / pl->T;
+  S = S < 1 ? 1 : (S > max_s ? max_s : S);
+  int chunk = (c->top_k + S - 1) / S;
+  chunk = (chunk + pl->T - 1) / pl->T * pl->T;
+  pl->chunk = chunk;
+  pl->S = (c->top_k + chunk - 1) / chunk;
+  return true;
+}
+
+template <int DK, int DV, int G, int NW>
+cudaError_t launch_cc(const AttnArgs* a, const Plan& pl, cudaStream_t st) {
+  auto kern = k_attn_cc<DK, DV, G, NW>;
+  if (a == nullptr)  // preparation: raise the dynamic shared-memory limit once
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+  dim3 grid(pl.S, a->R, pl.groups);
+  kern<<<grid, AttnCfg<DK, DV, G, NW>::THREADS, pl.smem, st>>>(*a);
+  return cudaGetLastError();
+}
+
+template <int G>
+cudaError_t launch_gqa_nw(const AttnArgs* a, const Plan& pl, cudaStream_t st) {
+  switch (pl.NW) {
+    case 1: return launch_cc<128, 128, G, 1>(a, pl, st);
+    case 2: return launch_cc<128, 128, G, 2>(a, pl, st);
+    case 4: return launch_cc<128, 128, G, 4>(a, pl, st);
+    case 8: return launch_cc<128, 128, G, 8>(a, pl, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t dispatch(const hs_config& c, const AttnArgs* a, const Plan& pl, cudaStream_t st) {
+  if (c.layout == HS_LAYOUT_MLA) return launch_cc<576, 512, 1, 8>(a, pl, st);
+  switch (pl.G) {
+    case 1: return launch_gqa_nw<1>(a, pl, st);
+    case 2: return launch_gqa_nw<2>(a, pl, st);
+    case 4: return launch_gqa_nw<4>(a, pl, st);
+    default: return launch_gqa_nw<8>(a, pl, st);
+  }
+}
+
+}  // namespace
+
+bool hs_attn_supported(const hs_config* c) {
+  Plan pl;
+  if (!plan_for(c, 152, &pl)) return false;
+  if (c->layout == HS_LAYOUT_GQA && pl.NW != 1 && pl.NW != 2 && pl.NW != 4 && pl.NW != 8) return false;
+  return true;
+}
+
+void hs_attn_workspace(const hs_config* c, int num_sms, size_t* floats, int* max_splits, int* max_groups) {
+  Plan pl;
+  plan_for(c, num_sms, &pl);
+  *max_splits = pl.S;
+  *max_groups = pl.groups;
+  *floats = (size_t)c->num_requests * pl.S * c->num_q_heads * ((size_t)c->head_dim_v + 2);
+}
+
+int hs_launch_attn(hs_pool* p, int layer, const void* d_q, const int32_t* d_locs, const void* kv_base,
+                   int64_t kv_rows, float scale, float* d_out, cudaStream_t st) {
+  const hs_config& c = p->cfg;
+  Plan pl;
+  if (!plan_for(&c, p->num_sms, &pl)) return HS_ERR_CONFIG;
+  if (kv_base != nullptr && ((uintptr_t)kv_base & 15u) != 0) return HS_ERR_ARG;
+  AttnArgs a;
+  a.q = (const uint16_t*)d_q;
+  a.locs = d_locs;
+  if (kv_base == nullptr) {
+    a.kv = p->buf + (int64_t)layer * c.num_requests * c.buffer_slots * p->rec;
+    a.rows = c.buffer_slots;
+  } else {
+    a.kv = (const uint8_t*)kv_base;
+    a.rows = kv_rows;
+  }
+  a.out = d_out;
+  a.part = p->attn_part;
+  a.ml = p->attn_part + (size_t)c.num_requests * pl.S * c.num_q_heads * c.head_dim_v;
+  a.ticket = p->attn_ticket;
+  a.err = p->err_global;
+  a.rec = p->rec;
+  if (c.layout == HS_LAYOUT_GQA) {
+    a.kstride = 2 * (int64_t)(c.head_dim_qk + c.head_dim_v);
+    a.vdelta = 2 * (int64_t)c.head_dim_qk;
+  } else {
+    a.kstride = 0;
+    a.vdelta = 0;
+  }
+  a.qscale = scale * kLog2e;
+  a.R = c.num_requests;
+  a.Hq = c.num_q_heads;
+  a.k = c.top_k;
+  a.S = pl.S;
+  a.chunk = pl.chunk;
+  a.groups = pl.groups;
+  return dispatch(c, &a, pl, st) == cudaSuccess ? HS_OK : HS_ERR_CUDA;
+}
+
+int hs_attn_prepare(const hs_config* c, int num_sms) {
+  Plan pl;
+  if (!plan_for(c, num_sms, &pl)) return HS_ERR_CONFIG;
+  return dispatch(*c, nullptr, pl, 0) == cudaSuccess ? HS_OK : HS_ERR_CUDA;
+}

@@ -1,0 +1,86 @@
+// Internal declarations shared by the translation units of libhisparse.
+// Layouts (all row-major):
+//   host history   shared [L][P0][rec] and private [R][L][C - P0][rec]   (pinned, device-mapped)
+//   hot buffer     [L][R][B][rec]                                        (HBM)
+//   tag / stamp    [L][R][B]  int32 (-1 empty) / uint32 (0 empty)
+//   state          [L][R]     {clock, nres, err, pad}
+//   counters       [L][R][4]  uint64 hits, misses, appends, host_bytes
+//   step log       [log_steps][L][R] uint32
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "hisparse.h"
+
+struct hs_rl_state {
+  uint32_t clock;  // next stamp; starts at 1, 0 marks an empty slot
+  uint32_t nres;   // resolves done: the step counter of the random key
+  uint32_t err;    // hs_device_error bits
+  uint32_t pad;
+};
+
+struct hs_pool {
+  hs_config cfg;
+  int device;
+  int num_sms;
+  int64_t rec;          // record bytes
+  int64_t priv_tokens;  // capacity - shared_prefix
+  uint8_t* host_shared;  // host pointers (cudaHostAlloc, mapped)
+  uint8_t* host_priv;
+  uint8_t* dmap_shared;  // device aliases of the same memory
+  uint8_t* dmap_priv;
+  uint8_t* buf;
+  int32_t* tag;
+  uint32_t* stamp;
+  hs_rl_state* state;
+  unsigned long long* counters;
+  uint32_t* step_log;
+  uint32_t* err_global;  // attention-side error bits
+  float* attn_part;      // split partials
+  uint32_t* attn_ticket; // [R][attn_max_groups]
+  int attn_max_splits;
+  int attn_max_groups;
+  size_t attn_part_floats;
+};
+
+// ---- small device helpers -------------------------------------------------
+
+// splitmix64 output function at counter n (Steele, Lea, Flood 2014): mix(seed + n * gamma)
+__device__ __forceinline__ uint64_t hs_splitmix_at(uint64_t seed, uint64_t n) {
+  uint64_t z = seed + n * 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+// eviction key of a slot; smaller keys are evicted first, ties by lower slot
+__device__ __forceinline__ uint32_t hs_evict_key(int policy, int32_t tag, uint32_t stamp, uint64_t seed,
+                                                 uint32_t nres, int R, int r, int L, int l, int B, int j) {
+  if (policy == HS_POLICY_RANDOM) {
+    if (tag < 0) return 0u;
+    uint64_t n = (((uint64_t)nres * (uint64_t)R + (uint64_t)r) * (uint64_t)L + (uint64_t)l) * (uint64_t)B + (uint64_t)j;
+    return 1u + (uint32_t)(hs_splitmix_at(seed, n) >> 33);
+  }
+  return stamp;
+}
+
+// device address of position p of (r, l) in the mapped host history
+__device__ __forceinline__ const uint8_t* hs_hist_addr(const uint8_t* shared, const uint8_t* priv, int64_t P0,
+                                                       int64_t priv_tokens, int64_t rec, int L, int r, int l,
+                                                       int64_t p) {
+  if (p < P0) return shared + ((int64_t)l * P0 + p) * rec;
+  return priv + (((int64_t)r * L + l) * priv_tokens + (p - P0)) * rec;
+}
+
+// ---- launchers (defined in the kernel translation units) -------------------
+int hs_launch_resolve(hs_pool* pool, int layer, const int32_t* d_topk, int32_t* d_locs, cudaStream_t st);
+int hs_launch_append(hs_pool* pool, int layer, const int64_t* d_pos, const void* d_rec, cudaStream_t st);
+int hs_launch_attn(hs_pool* pool, int layer, const void* d_q, const int32_t* d_locs, const void* kv_base,
+                   int64_t kv_rows, float scale, float* d_out, cudaStream_t st);
+// attention workspace requirement for a configuration (floats, splits, groups)
+void hs_attn_workspace(const hs_config* cfg, int num_sms, size_t* floats, int* max_splits, int* max_groups);
+bool hs_attn_supported(const hs_config* cfg);
+int hs_attn_prepare(const hs_config* cfg, int num_sms);
+int hs_resolve_prepare(const hs_config* cfg);
+size_t hs_resolve_smem_bytes(const hs_config* cfg);

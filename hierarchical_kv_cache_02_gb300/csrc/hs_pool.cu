@@ -1,0 +1,363 @@
+// Host side of the C ABI: configuration checks, pool memory, prefill, stats and inspection.
+// The memory layer follows the HiSparse summary §3 and §8: a pinned host pool holds the
+// authoritative KV history; HBM holds only B slots per (request, layer) plus metadata.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <algorithm>
+#include <vector>
+
+#include "hs_internal.cuh"
+
+namespace {
+
+bool fault_requested(const char* what) {
+  const char* f = getenv("HS_FAULT");
+  return f != nullptr && strstr(f, what) != nullptr;
+}
+
+bool is_pow2(int64_t v) { return v > 0 && (v & (v - 1)) == 0; }
+
+int check_config(const hs_config* c) {
+  if (c == nullptr) return HS_ERR_ARG;
+  if (c->num_requests < 1 || c->num_layers < 1) return HS_ERR_CONFIG;
+  if (c->capacity < 1 || c->capacity > (int64_t)INT32_MAX) return HS_ERR_CONFIG;
+  if (c->shared_prefix < 0 || c->shared_prefix > c->capacity) return HS_ERR_CONFIG;
+  if (c->layout != HS_LAYOUT_MLA && c->layout != HS_LAYOUT_GQA) return HS_ERR_CONFIG;
+  if (c->num_q_heads < 1 || c->num_kv_heads < 1 || c->head_dim_qk < 1 || c->head_dim_v < 1) return HS_ERR_CONFIG;
+  if (c->layout == HS_LAYOUT_MLA && (c->num_kv_heads != 1 || c->head_dim_v > c->head_dim_qk)) return HS_ERR_CONFIG;
+  if (c->num_q_heads % c->num_kv_heads != 0) return HS_ERR_CONFIG;
+  if (c->top_k < 1 || c->top_k > c->buffer_slots || c->buffer_slots > 16384) return HS_ERR_CONFIG;
+  if (c->policy < HS_POLICY_LRU || c->policy > HS_POLICY_SWAP_VANILLA) return HS_ERR_CONFIG;
+  if (c->log_steps < 0) return HS_ERR_CONFIG;
+  int64_t rec = hs_record_bytes(c);
+  if (rec <= 0 || rec % 16 != 0) return HS_ERR_CONFIG;
+  if (!is_pow2(c->io_chunk_bytes) || c->io_chunk_bytes < 16 || c->io_chunk_bytes > 128 || rec % c->io_chunk_bytes != 0)
+    return HS_ERR_CONFIG;
+  if (!hs_attn_supported(c)) return HS_ERR_CONFIG;
+  if (hs_resolve_smem_bytes(c) > 200 * 1024) return HS_ERR_CONFIG;
+  return HS_OK;
+}
+
+template <typename T>
+int dev_alloc(T** p, size_t count) {
+  *p = nullptr;
+  if (count == 0) return HS_OK;
+  if (fault_requested("alloc_dev")) return HS_ERR_ALLOC_DEV;
+  if (cudaMalloc((void**)p, count * sizeof(T)) != cudaSuccess) {
+    *p = nullptr;
+    cudaGetLastError();
+    return HS_ERR_ALLOC_DEV;
+  }
+  return HS_OK;
+}
+
+int host_alloc(uint8_t** h, uint8_t** d, size_t bytes) {
+  *h = nullptr;
+  *d = nullptr;
+  if (bytes == 0) return HS_OK;
+  if (fault_requested("alloc_host")) return HS_ERR_ALLOC_HOST;
+  if (cudaHostAlloc((void**)h, bytes, cudaHostAllocMapped | cudaHostAllocPortable) != cudaSuccess) {
+    *h = nullptr;
+    cudaGetLastError();
+    return HS_ERR_ALLOC_HOST;
+  }
+  if (cudaHostGetDevicePointer((void**)d, *h, 0) != cudaSuccess) {
+    cudaGetLastError();
+    return HS_ERR_CUDA;
+  }
+  return HS_OK;
+}
+
+void free_pool(hs_pool* p) {
+  if (p == nullptr) return;
+  if (p->host_shared) cudaFreeHost(p->host_shared);
+  if (p->host_priv) cudaFreeHost(p->host_priv);
+  cudaFree(p->buf);
+  cudaFree(p->tag);
+  cudaFree(p->stamp);
+  cudaFree(p->state);
+  cudaFree(p->counters);
+  cudaFree(p->step_log);
+  cudaFree(p->err_global);
+  cudaFree(p->attn_part);
+  cudaFree(p->attn_ticket);
+  delete p;
+}
+
+__global__ void k_reset(int32_t* tag, uint32_t* stamp, size_t nslots, hs_rl_state* state, size_t nrl) {
+  size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t j = i; j < nslots; j += stride) {
+    tag[j] = -1;
+    stamp[j] = 0u;
+  }
+  for (size_t j = i; j < nrl; j += stride) {
+    hs_rl_state s;
+    s.clock = 1u;
+    s.nres = 0u;
+    s.err = 0u;
+    s.pad = 0u;
+    state[j] = s;
+  }
+}
+
+size_t slots_total(const hs_pool* p) {
+  return (size_t)p->cfg.num_layers * p->cfg.num_requests * p->cfg.buffer_slots;
+}
+
+size_t rl_total(const hs_pool* p) { return (size_t)p->cfg.num_layers * p->cfg.num_requests; }
+
+int do_reset(hs_pool* p, cudaStream_t st) {
+  size_t ns = slots_total(p), nrl = rl_total(p);
+  int blocks = (int)std::min<size_t>((ns + 255) / 256, (size_t)p->num_sms * 8);
+  k_reset<<<blocks, 256, 0, st>>>(p->tag, p->stamp, ns, p->state, nrl);
+  if (cudaMemsetAsync(p->counters, 0, nrl * 4 * sizeof(unsigned long long), st) != cudaSuccess) return HS_ERR_CUDA;
+  if (p->step_log && cudaMemsetAsync(p->step_log, 0, (size_t)p->cfg.log_steps * nrl * sizeof(uint32_t), st) != cudaSuccess)
+    return HS_ERR_CUDA;
+  if (cudaMemsetAsync(p->err_global, 0, sizeof(uint32_t), st) != cudaSuccess) return HS_ERR_CUDA;
+  if (cudaMemsetAsync(p->attn_ticket, 0, (size_t)p->cfg.num_requests * p->attn_max_groups * sizeof(uint32_t), st) !=
+      cudaSuccess)
+    return HS_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? HS_OK : HS_ERR_CUDA;
+}
+
+struct DeviceGuard {
+  int prev = -1;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    if (prev != dev) cudaSetDevice(dev);
+  }
+  ~DeviceGuard() {
+    if (prev >= 0) cudaSetDevice(prev);
+  }
+};
+
+}  // namespace
+
+extern "C" int64_t hs_record_bytes(const hs_config* c) {
+  if (c == nullptr) return -1;
+  if (c->layout == HS_LAYOUT_MLA) return 2 * (int64_t)c->head_dim_qk;
+  return 2 * (int64_t)c->num_kv_heads * ((int64_t)c->head_dim_qk + c->head_dim_v);
+}
+
+extern "C" int hs_pool_create(const hs_config* cfg, int cuda_device, hs_pool** out) {
+  if (out == nullptr) return HS_ERR_ARG;
+  *out = nullptr;
+  int rc = check_config(cfg);
+  if (rc != HS_OK) return rc;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || cuda_device < 0 || cuda_device >= ndev) {
+    cudaGetLastError();
+    return HS_ERR_CUDA;
+  }
+  DeviceGuard guard(cuda_device);
+  hs_pool* p = new hs_pool();
+  memset(p, 0, sizeof(*p));
+  p->cfg = *cfg;
+  p->device = cuda_device;
+  cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, cuda_device);
+  p->rec = hs_record_bytes(cfg);
+  p->priv_tokens = cfg->capacity - cfg->shared_prefix;
+  const size_t R = cfg->num_requests, L = cfg->num_layers, B = cfg->buffer_slots;
+  const size_t rec = (size_t)p->rec;
+
+  rc = host_alloc(&p->host_shared, &p->dmap_shared, L * (size_t)cfg->shared_prefix * rec);
+  if (rc == HS_OK) rc = host_alloc(&p->host_priv, &p->dmap_priv, R * L * (size_t)p->priv_tokens * rec);
+  if (rc == HS_OK) rc = dev_alloc(&p->buf, L * R * B * rec);
+  if (rc == HS_OK) rc = dev_alloc(&p->tag, L * R * B);
+  if (rc == HS_OK) rc = dev_alloc(&p->stamp, L * R * B);
+  if (rc == HS_OK) rc = dev_alloc(&p->state, L * R);
+  if (rc == HS_OK) rc = dev_alloc(&p->counters, L * R * 4);
+  if (rc == HS_OK) rc = dev_alloc(&p->step_log, (size_t)cfg->log_steps * L * R);
+  if (rc == HS_OK) rc = dev_alloc(&p->err_global, 1);
+  if (rc == HS_OK) {
+    hs_attn_workspace(cfg, p->num_sms, &p->attn_part_floats, &p->attn_max_splits, &p->attn_max_groups);
+    rc = dev_alloc(&p->attn_part, p->attn_part_floats);
+  }
+  if (rc == HS_OK) rc = dev_alloc(&p->attn_ticket, R * (size_t)p->attn_max_groups);
+  if (rc == HS_OK) rc = hs_resolve_prepare(cfg);
+  if (rc == HS_OK) rc = hs_attn_prepare(cfg, p->num_sms);
+  if (rc == HS_OK) rc = do_reset(p, 0);
+  if (rc == HS_OK && cudaDeviceSynchronize() != cudaSuccess) rc = HS_ERR_CUDA;
+  if (rc != HS_OK) {
+    cudaGetLastError();
+    free_pool(p);
+    return rc;
+  }
+  *out = p;
+  return HS_OK;
+}
+
+extern "C" int hs_pool_destroy(hs_pool* pool) {
+  if (pool == nullptr) return HS_OK;
+  DeviceGuard guard(pool->device);
+  cudaDeviceSynchronize();
+  free_pool(pool);
+  return HS_OK;
+}
+
+extern "C" int hs_pool_reset(hs_pool* pool, void* stream) {
+  if (pool == nullptr) return HS_ERR_ARG;
+  DeviceGuard guard(pool->device);
+  return do_reset(pool, (cudaStream_t)stream);
+}
+
+extern "C" int hs_prefill_write(hs_pool* pool, int req, int layer, int64_t pos0, int64_t n, const void* src,
+                                void* stream) {
+  if (pool == nullptr || src == nullptr) return HS_ERR_ARG;
+  const hs_config& c = pool->cfg;
+  if (req < 0 || req >= c.num_requests || layer < 0 || layer >= c.num_layers) return HS_ERR_ARG;
+  if (pos0 < 0 || n < 0 || pos0 + n > c.capacity) return HS_ERR_ARG;
+  if (n == 0) return HS_OK;
+  DeviceGuard guard(pool->device);
+  const int64_t P0 = c.shared_prefix, rec = pool->rec;
+  const uint8_t* s = (const uint8_t*)src;
+  cudaStream_t st = (cudaStream_t)stream;
+  int64_t a = pos0, end = pos0 + n;
+  if (a < P0) {  // shared part
+    int64_t b = std::min(end, P0);
+    uint8_t* dst = pool->host_shared + ((int64_t)layer * P0 + a) * rec;
+    if (cudaMemcpyAsync(dst, s, (size_t)((b - a) * rec), cudaMemcpyDefault, st) != cudaSuccess) return HS_ERR_CUDA;
+    s += (b - a) * rec;
+    a = b;
+  }
+  if (a < end) {
+    uint8_t* dst = pool->host_priv + (((int64_t)req * c.num_layers + layer) * pool->priv_tokens + (a - P0)) * rec;
+    if (cudaMemcpyAsync(dst, s, (size_t)((end - a) * rec), cudaMemcpyDefault, st) != cudaSuccess) return HS_ERR_CUDA;
+  }
+  return HS_OK;
+}
+
+extern "C" int hs_append_writethrough(hs_pool* pool, int layer, const int64_t* d_pos, const void* d_rec,
+                                      void* stream) {
+  if (pool == nullptr || d_pos == nullptr || d_rec == nullptr) return HS_ERR_ARG;
+  if (layer < 0 || layer >= pool->cfg.num_layers) return HS_ERR_ARG;
+  DeviceGuard guard(pool->device);
+  return hs_launch_append(pool, layer, d_pos, d_rec, (cudaStream_t)stream);
+}
+
+extern "C" int hs_resolve(hs_pool* pool, int layer, const int32_t* d_topk, int32_t* d_locs, void* stream) {
+  if (pool == nullptr || d_topk == nullptr || d_locs == nullptr) return HS_ERR_ARG;
+  if (layer < 0 || layer >= pool->cfg.num_layers) return HS_ERR_ARG;
+  DeviceGuard guard(pool->device);
+  return hs_launch_resolve(pool, layer, d_topk, d_locs, (cudaStream_t)stream);
+}
+
+extern "C" int hs_sparse_attn(hs_pool* pool, int layer, const void* d_q, const int32_t* d_locs,
+                              const void* kv_base, int64_t kv_rows, float scale, float* d_out, void* stream) {
+  if (pool == nullptr || d_q == nullptr || d_locs == nullptr || d_out == nullptr) return HS_ERR_ARG;
+  if (layer < 0 || layer >= pool->cfg.num_layers) return HS_ERR_ARG;
+  if (kv_base != nullptr && (kv_rows < 1 || kv_rows > (int64_t)INT32_MAX)) return HS_ERR_ARG;
+  DeviceGuard guard(pool->device);
+  return hs_launch_attn(pool, layer, d_q, d_locs, kv_base, kv_rows, scale, d_out, (cudaStream_t)stream);
+}
+
+extern "C" int hs_stats(hs_pool* pool, hs_totals* totals, uint64_t* h_counters, uint32_t* h_errors,
+                        uint32_t* h_step_log, int reset) {
+  if (pool == nullptr) return HS_ERR_ARG;
+  DeviceGuard guard(pool->device);
+  const int R = pool->cfg.num_requests, L = pool->cfg.num_layers;
+  const size_t nrl = (size_t)R * L;
+  if (cudaDeviceSynchronize() != cudaSuccess) return HS_ERR_CUDA;
+  std::vector<unsigned long long> cnt(nrl * 4);
+  std::vector<hs_rl_state> st(nrl);
+  std::vector<uint32_t> log((size_t)pool->cfg.log_steps * nrl);
+  uint32_t eg = 0;
+  if (cudaMemcpy(cnt.data(), pool->counters, cnt.size() * sizeof(unsigned long long), cudaMemcpyDeviceToHost) !=
+          cudaSuccess ||
+      cudaMemcpy(st.data(), pool->state, st.size() * sizeof(hs_rl_state), cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemcpy(&eg, pool->err_global, sizeof(uint32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return HS_ERR_CUDA;
+  if (!log.empty() && cudaMemcpy(log.data(), pool->step_log, log.size() * sizeof(uint32_t), cudaMemcpyDeviceToHost) !=
+                          cudaSuccess)
+    return HS_ERR_CUDA;
+  hs_totals t;
+  memset(&t, 0, sizeof t);
+  t.error_bits = eg;
+  // device layout [L][R]; the API layout is [R][L]
+  for (int r = 0; r < R; ++r) {
+    for (int l = 0; l < L; ++l) {
+      size_t d = (size_t)l * R + r, a = (size_t)r * L + l;
+      t.hits += cnt[d * 4 + 0];
+      t.misses += cnt[d * 4 + 1];
+      t.appends += cnt[d * 4 + 2];
+      t.host_bytes += cnt[d * 4 + 3];
+      t.error_bits |= st[d].err;
+      if (h_counters)
+        for (int x = 0; x < 4; ++x) h_counters[a * 4 + x] = cnt[d * 4 + x];
+      if (h_errors) h_errors[a] = st[d].err;
+      if (h_step_log)
+        for (int s = 0; s < pool->cfg.log_steps; ++s) h_step_log[(size_t)s * nrl + a] = log[(size_t)s * nrl + d];
+    }
+  }
+  t.resolves = st[0].nres;
+  if (totals) *totals = t;
+  if (reset) {
+    cudaMemset(pool->counters, 0, nrl * 4 * sizeof(unsigned long long));
+    if (!log.empty()) cudaMemset(pool->step_log, 0, log.size() * sizeof(uint32_t));
+    cudaMemset(pool->err_global, 0, sizeof(uint32_t));
+    for (auto& s : st) s.err = 0;
+    cudaMemcpy(pool->state, st.data(), st.size() * sizeof(hs_rl_state), cudaMemcpyHostToDevice);
+    if (cudaDeviceSynchronize() != cudaSuccess) return HS_ERR_CUDA;
+  }
+  return t.error_bits ? HS_ERR_DEVICE_FLAG : HS_OK;
+}
+
+extern "C" int hs_read_state(hs_pool* pool, int layer, int32_t* h_tag, uint32_t* h_stamp, uint32_t* h_clock) {
+  if (pool == nullptr || layer < 0 || layer >= pool->cfg.num_layers) return HS_ERR_ARG;
+  DeviceGuard guard(pool->device);
+  const size_t R = pool->cfg.num_requests, B = pool->cfg.buffer_slots;
+  if (cudaDeviceSynchronize() != cudaSuccess) return HS_ERR_CUDA;
+  const size_t off = (size_t)layer * R * B;
+  if (h_tag && cudaMemcpy(h_tag, pool->tag + off, R * B * sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return HS_ERR_CUDA;
+  if (h_stamp && cudaMemcpy(h_stamp, pool->stamp + off, R * B * sizeof(uint32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return HS_ERR_CUDA;
+  if (h_clock) {
+    std::vector<hs_rl_state> st(R);
+    if (cudaMemcpy(st.data(), pool->state + (size_t)layer * R, R * sizeof(hs_rl_state), cudaMemcpyDeviceToHost) !=
+        cudaSuccess)
+      return HS_ERR_CUDA;
+    for (size_t r = 0; r < R; ++r) h_clock[r] = st[r].clock;
+  }
+  return HS_OK;
+}
+
+extern "C" int hs_read_buffer(hs_pool* pool, int req, int layer, void* dst) {
+  if (pool == nullptr || dst == nullptr) return HS_ERR_ARG;
+  if (req < 0 || req >= pool->cfg.num_requests || layer < 0 || layer >= pool->cfg.num_layers) return HS_ERR_ARG;
+  DeviceGuard guard(pool->device);
+  const size_t R = pool->cfg.num_requests, B = pool->cfg.buffer_slots, rec = pool->rec;
+  if (cudaDeviceSynchronize() != cudaSuccess) return HS_ERR_CUDA;
+  const uint8_t* src = pool->buf + ((size_t)layer * R + req) * B * rec;
+  return cudaMemcpy(dst, src, B * rec, cudaMemcpyDeviceToHost) == cudaSuccess ? HS_OK : HS_ERR_CUDA;
+}
+
+extern "C" int hs_read_history(hs_pool* pool, int req, int layer, int64_t pos0, int64_t n, void* dst) {
+  if (pool == nullptr || dst == nullptr) return HS_ERR_ARG;
+  const hs_config& c = pool->cfg;
+  if (req < 0 || req >= c.num_requests || layer < 0 || layer >= c.num_layers) return HS_ERR_ARG;
+  if (pos0 < 0 || n < 0 || pos0 + n > c.capacity) return HS_ERR_ARG;
+  DeviceGuard guard(pool->device);
+  if (cudaDeviceSynchronize() != cudaSuccess) return HS_ERR_CUDA;
+  const int64_t P0 = c.shared_prefix, rec = pool->rec;
+  uint8_t* d = (uint8_t*)dst;
+  for (int64_t p = pos0; p < pos0 + n;) {
+    if (p < P0) {
+      int64_t b = std::min(pos0 + n, P0);
+      memcpy(d, pool->host_shared + ((int64_t)layer * P0 + p) * rec, (size_t)((b - p) * rec));
+      d += (b - p) * rec;
+      p = b;
+    } else {
+      int64_t b = pos0 + n;
+      memcpy(d, pool->host_priv + (((int64_t)req * c.num_layers + layer) * pool->priv_tokens + (p - P0)) * rec,
+             (size_t)((b - p) * rec));
+      d += (b - p) * rec;
+      p = b;
+    }
+  }
+  return HS_OK;
+}

@@ -1,0 +1,197 @@
+/*
+ * hisparse.h -- C ABI of a GB300 (sm_103a) library for the decode hot path of
+ * HiSparse ("HiSparse: Scaling Sparse-Attention Decoding with Hierarchical KV
+ * Cache Management", as summarised on marsggbo.github.io, 2026-09-23).
+ *
+ * The method (summary §3): every request keeps its full per-layer KV history in
+ * a host-DRAM pool (pinned; the authoritative copy).  The GPU holds only a
+ * fixed B-slot hot buffer per (request, layer) with page-table and recency
+ * metadata.  Each decode layer: the indexer hands over k logical positions;
+ * RESOLVE looks them up in the hot buffer, fetches the misses from the host
+ * pool into evicted slots and publishes the physical slot of every selected
+ * position (§5); sparse attention reads exactly those slots (§3 step (4));
+ * the new token's KV is written through to the host pool (§3 step (5)).
+ *
+ * Conventions for every call:
+ *   - Pointers named d_* are device pointers (or device-visible managed memory)
+ *     owned by the caller; the library never frees them.  Host pointers are
+ *     named h_* or src/dst with the rule stated at the call.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   - Calls marked CAPTURABLE only enqueue kernels on `stream`: no allocation,
+ *     no host synchronisation, no read of device data by the host.  They may be
+ *     captured in a CUDA graph and replayed.  A pool is used from one stream at
+ *     a time.
+ *   - Return value: HS_OK (0) or a negative hs_status.  Argument errors found on
+ *     the host return at once and enqueue nothing.  Errors that only the device
+ *     can see (a bad position in a top-k list, an append out of range, a timed
+ *     out wait) set bits in the pool's device error word; the kernel skips the
+ *     offending entry; hs_stats reports them and returns HS_ERR_DEVICE_FLAG.
+ */
+#ifndef HISPARSE_H
+#define HISPARSE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct hs_pool hs_pool; /* opaque; owns all pool, buffer and metadata memory */
+
+enum hs_status {
+  HS_OK = 0,
+  HS_ERR_CONFIG = -1,      /* hs_config rejected (see hs_pool_create) */
+  HS_ERR_ALLOC_HOST = -2,  /* pinned host allocation failed */
+  HS_ERR_ALLOC_DEV = -3,   /* device allocation failed */
+  HS_ERR_ARG = -4,         /* a call argument is out of range or NULL */
+  HS_ERR_CUDA = -5,        /* a CUDA runtime call failed */
+  HS_ERR_DEVICE_FLAG = -6  /* hs_stats: a kernel recorded an error bit */
+};
+
+enum hs_policy {
+  HS_POLICY_LRU = 0,          /* summary §4-§5: evict the least recently used, update in place */
+  HS_POLICY_FIFO = 1,         /* §4: evict the earliest inserted */
+  HS_POLICY_RANDOM = 2,       /* §4: evict at random (counter-based hash, reproducible) */
+  HS_POLICY_SWAP_VANILLA = 3  /* §4: keep only the current top-k, no hot set */
+};
+
+enum hs_layout {
+  HS_LAYOUT_MLA = 0, /* one shared latent of head_dim_qk bf16 per token; V = its first head_dim_v values */
+  HS_LAYOUT_GQA = 1  /* per token num_kv_heads blocks of [K (head_dim_qk) | V (head_dim_v)] bf16 */
+};
+
+/* bits of the device error word */
+enum hs_device_error {
+  HS_DEVERR_RANGE = 1,    /* a top-k entry outside [0, capacity) other than -1 */
+  HS_DEVERR_DUP = 2,      /* a top-k entry repeating an earlier one in the same list */
+  HS_DEVERR_CLOCK = 4,    /* the 32-bit recency clock of a (request, layer) would wrap */
+  HS_DEVERR_APPEND = 8,   /* an append position outside [shared_prefix, capacity) */
+  HS_DEVERR_LOC = 16,     /* an attention slot index outside [0, rows) */
+  HS_DEVERR_TIMEOUT = 32  /* a bounded wait inside a kernel gave up */
+};
+
+typedef struct {
+  int32_t num_requests;   /* R >= 1 */
+  int32_t num_layers;     /* L >= 1 */
+  int64_t capacity;       /* C: positions per (request, layer), prefill plus appends */
+  int64_t shared_prefix;  /* positions [0, shared_prefix) are ONE history shared by all requests
+                             (read-only for appends); 0 = every request owns its whole history */
+  int32_t layout;         /* hs_layout */
+  int32_t num_q_heads;    /* Hq */
+  int32_t num_kv_heads;   /* GQA: KV heads per token (Hq % num_kv_heads == 0); MLA: 1 */
+  int32_t head_dim_qk;    /* MLA 576, GQA 128 */
+  int32_t head_dim_v;     /* MLA 512, GQA 128 */
+  int32_t top_k;          /* k, 1 <= k <= buffer_slots, k <= 4096 (shared-memory hash) */
+  int32_t buffer_slots;   /* B: hot-buffer slots per (request, layer), <= 16384 */
+  int32_t policy;         /* hs_policy */
+  uint64_t seed;          /* key of HS_POLICY_RANDOM */
+  int32_t io_chunk_bytes; /* bytes one thread moves per batch of loads in a miss fetch:
+                             16..128, a power of two dividing the record size (summary §5: the
+                             per-thread transfer size of the swap-in is a tuned knob) */
+  int32_t log_steps;      /* >0: keep per-step miss counts of the first log_steps resolves */
+} hs_config;
+
+/* Record size in bytes for a configuration (MLA: 2*head_dim_qk; GQA: 2*kv_heads*(qk+v)). */
+int64_t hs_record_bytes(const hs_config* cfg);
+
+/*
+ * Create a pool on `cuda_device` (summary §3, §8 "memory layer"): pinned, device-mapped host
+ * history [L][shared_prefix][rec] + [R][L][capacity - shared_prefix][rec], hot buffer
+ * [L][R][B][rec] in HBM, tags (-1 = empty), stamps (0 = empty), per-(request, layer) clock
+ * (starts at 1), counters and attention workspace.  All slots start empty.  Synchronous,
+ * not capturable.  Errors: HS_ERR_CONFIG, HS_ERR_ALLOC_HOST, HS_ERR_ALLOC_DEV, HS_ERR_CUDA.
+ * Environment HS_FAULT=alloc_host|alloc_dev makes the named allocation fail (for tests).
+ */
+int hs_pool_create(const hs_config* cfg, int cuda_device, hs_pool** out);
+
+/* Free everything the pool owns.  Synchronises the device.  NULL is accepted. */
+int hs_pool_destroy(hs_pool* pool);
+
+/* Cold start: empty every slot, reset clocks, counters, error word and step log.  CAPTURABLE. */
+int hs_pool_reset(hs_pool* pool, void* stream);
+
+/*
+ * Prefill write (summary §3 step (1)): copy n records from `src` (host or device memory,
+ * [n][rec] bytes) into the host history of (req, layer) at positions [pos0, pos0 + n).
+ * Positions below shared_prefix go to the shared history whatever `req` is.  Writes only the
+ * host pool; the hot buffer is filled on demand by hs_resolve.  Enqueued on `stream`; the
+ * caller keeps `src` alive until the stream reaches this point.  Errors: HS_ERR_ARG.
+ */
+int hs_prefill_write(hs_pool* pool, int req, int layer, int64_t pos0, int64_t n, const void* src,
+                     void* stream);
+
+/*
+ * Write-through append (summary §3 step (5)): for every request r, record d_rec[r] (bf16,
+ * [R][rec] bytes, device) becomes position d_pos[r] (int64 [R], device) of (r, layer): it is
+ * stored to the host history (16-byte stores through the device mapping) and into the hot
+ * buffer -- in the slot already holding d_pos[r] if any, else the slot the policy would evict
+ * first over all B slots -- with stamp = clock, clock += 1.  Positions outside
+ * [shared_prefix, capacity) set HS_DEVERR_APPEND and are skipped.  CAPTURABLE.
+ */
+int hs_append_writethrough(hs_pool* pool, int layer, const int64_t* d_pos, const void* d_rec, void* stream);
+
+/*
+ * Fused RESOLVE (summary §5), one CTA per request: hash the k positions of d_topk[r]
+ * (int32 [R][k], device; -1 = padding) in shared memory, probe all B slots for hits, choose
+ * the m victims among the slots holding no selected position (smallest eviction key, then
+ * lowest slot; victims in ascending slot order take the misses in top-k order), update the
+ * recency stamps in place (hits to MRU in top-k order, misses after the hits), fetch each
+ * missing record from the pinned host history with 16-byte loads straight into its slot,
+ * and write d_locs[r][i] = slot of d_topk[r][i] (-1 for padding or invalid entries; int32
+ * [R][k], device).  Updates hits/misses/host-byte counters.  CAPTURABLE.
+ */
+int hs_resolve(hs_pool* pool, int layer, const int32_t* d_topk, int32_t* d_locs, void* stream);
+
+/*
+ * Sparse attention over resolved slots (summary §3 step (4)): for request r and query head h,
+ *   out[r][h] = sum_i softmax_i(scale * <q[r][h], K(row_i)>) V(row_i)
+ * over the entries i with d_locs[r][i] >= 0, in top-k order, with K/V taken from the record
+ * layout (MLA: K = the latent, V = its first head_dim_v values; GQA: KV head h/(Hq/Hkv)).
+ * d_q: bf16 [R][Hq][head_dim_qk]; d_out: fp32 [R][Hq][head_dim_v]; both device.
+ * kv_base == NULL: rows are the hot-buffer slots of `layer` (kv_rows ignored).  Otherwise
+ * kv_base is a caller-owned device array [R][kv_rows][rec] and d_locs index its rows
+ * (fully resident KV: used to check the exactness property).  A request with no valid entry
+ * gets zeros.  Entries >= rows set HS_DEVERR_LOC and are skipped.  The reduction order
+ * depends only on the top-k order, so the result is bit-identical whichever slots hold the
+ * records.  CAPTURABLE.
+ */
+int hs_sparse_attn(hs_pool* pool, int layer, const void* d_q, const int32_t* d_locs, const void* kv_base,
+                   int64_t kv_rows, float scale, float* d_out, void* stream);
+
+typedef struct {
+  uint64_t hits;
+  uint64_t misses;
+  uint64_t appends;
+  uint64_t host_bytes;  /* bytes fetched from the host history by hs_resolve */
+  uint32_t error_bits;  /* OR of all hs_device_error bits */
+  uint32_t resolves;    /* hs_resolve calls counted on (request 0, layer 0) */
+} hs_totals;
+
+/*
+ * Read the device counters (synchronises the device; not capturable).  Any output may be NULL.
+ *   h_counters : uint64 [R][L][4]  (hits, misses, appends, host_bytes) per (request, layer)
+ *   h_errors   : uint32 [R][L]     error bits per (request, layer)
+ *   h_step_log : uint32 [log_steps][R][L] misses of the t-th resolve of (r, l)
+ * reset != 0 zeroes the counters, error bits and step log afterwards (not the cache state).
+ * Returns HS_ERR_DEVICE_FLAG when any error bit is set, after filling the outputs.
+ */
+int hs_stats(hs_pool* pool, hs_totals* totals, uint64_t* h_counters, uint32_t* h_errors, uint32_t* h_step_log,
+             int reset);
+
+/*
+ * Inspection (synchronous, not capturable): copy the metadata of `layer` to host memory.
+ *   h_tag: int32 [R][B]; h_stamp: uint32 [R][B]; h_clock: uint32 [R]; any may be NULL.
+ */
+int hs_read_state(hs_pool* pool, int layer, int32_t* h_tag, uint32_t* h_stamp, uint32_t* h_clock);
+
+/* Inspection: copy the hot buffer of (req, layer), [B][rec] bytes, to host memory `dst`. */
+int hs_read_buffer(hs_pool* pool, int req, int layer, void* dst);
+
+/* Inspection: copy n records of the host history of (req, layer) from position pos0 to `dst`. */
+int hs_read_history(hs_pool* pool, int req, int layer, int64_t pos0, int64_t n, void* dst);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HISPARSE_H */

@@ -1,0 +1,268 @@
+"""GPU parity: the CUDA library against the oracle, element by element, through the C ABI.
+
+Bit-exact: slot of every selected position (locs), tags, stamps, clocks, per-step misses,
+hit/miss/append/host-byte counters, hot-buffer contents and the written-through history.
+Attention: max-abs <= 2e-2 and mean-abs <= 2e-3 against fp64 (and within the fp32 bound).
+"""
+import numpy as np
+import pytest
+
+from harness import OracleRun, Scenario, assert_attn_close, bf16_tensor, gpu_step, prefill
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+from hierarchical_kv_cache_02_gb300 import (DEVERR_APPEND, DEVERR_DUP, DEVERR_LOC, DEVERR_RANGE, LAYOUT_GQA,
+                                             LAYOUT_MLA, HsConfig, HsPool)
+
+
+def _gqa(R, L, C, k, B, policy=0, kvh=8, G=4, io=64, log=0, P0=0, seed=3):
+    return HsConfig(num_requests=R, num_layers=L, capacity=C, layout=LAYOUT_GQA, num_q_heads=kvh * G,
+                    num_kv_heads=kvh, head_dim_qk=128, head_dim_v=128, top_k=k, buffer_slots=B, policy=policy,
+                    seed=seed, io_chunk_bytes=io, log_steps=log, shared_prefix=P0)
+
+
+def _mla(R, L, C, k, B, Hq=16, policy=0, io=64, log=0, P0=0):
+    return HsConfig(num_requests=R, num_layers=L, capacity=C, layout=LAYOUT_MLA, num_q_heads=Hq, num_kv_heads=1,
+                    head_dim_qk=576, head_dim_v=512, top_k=k, buffer_slots=B, policy=policy, seed=11,
+                    io_chunk_bytes=io, log_steps=log, shared_prefix=P0)
+
+
+def run_and_compare(sc: Scenario, attn_every=1, check_state=True):
+    cfg = sc.cfg
+    pool = HsPool(cfg)
+    prefill(pool, sc)
+    orc = OracleRun(sc)
+    worst = 0.0
+    for t in range(sc.steps):
+        res = gpu_step(pool, sc, t, attn=(t % attn_every == 0))
+        ref = orc.step(t)
+        for l in range(cfg.num_layers):
+            locs, out = res[l]
+            for r in range(cfg.num_requests):
+                m, rlocs = ref[(r, l)]
+                assert np.array_equal(locs[r], rlocs), (t, r, l)
+                if out is not None:
+                    worst = max(worst, assert_attn_close(out[r], orc.attention(t, r, l), (t, r, l)))
+            if check_state:
+                tag, stamp, clock = pool.read_state(l)
+                for r in range(cfg.num_requests):
+                    otag, ostamp = orc.caches[(r, l)].slots()
+                    assert np.array_equal(tag[r], otag), (t, r, l)
+                    assert np.array_equal(stamp[r], ostamp), (t, r, l)
+                    assert clock[r] == orc.caches[(r, l)].counters()["clock"]
+    st = pool.stats()
+    tot = {"hits": 0, "misses": 0, "appends": 0}
+    for (r, l), cache in orc.caches.items():
+        cnt = cache.counters()
+        assert list(st["per_rl"][r, l, :3]) == [cnt["hits"], cnt["misses"], cnt["appends"]], (r, l)
+        assert st["per_rl"][r, l, 3] == cnt["misses"] * cfg.record_bytes
+        for key in tot:
+            tot[key] += cnt[key]
+    assert st["error_bits"] == 0 and st["status"] == 0
+    # hot buffer holds exactly the history record of every tagged slot; appended history written through
+    for l in range(cfg.num_layers):
+        tag, _, _ = pool.read_state(l)
+        for r in range(cfg.num_requests):
+            buf = pool.read_buffer(r, l)
+            occ = np.nonzero(tag[r] >= 0)[0]
+            assert np.array_equal(buf[occ], sc.hist[(r, l)][tag[r][occ]]), (r, l)
+            if sc.appends:
+                n = sc.steps
+                assert np.array_equal(pool.read_history(r, l, sc.ctx0, n), sc.hist[(r, l)][sc.ctx0:sc.ctx0 + n])
+    pool.close()
+    return worst
+
+
+def test_tiny_single_request_mla():
+    """1 request, 1 layer, 4096-token context, 576-dim latent, 16 heads, k=256, B=512, LRU,
+    64 steps with write-through append; drift keep 90%, recency mean 512."""
+    sc = Scenario(_mla(1, 1, 4096 + 64, 256, 512, log=64), ctx0=4096, steps=64, appends=True, keep=0.9,
+                  recency_mean=512, seed=1)
+    run_and_compare(sc)
+
+
+@pytest.mark.parametrize("policy", [0, 1, 2, 3])
+def test_gqa_policies_ragged(policy):
+    """3 requests x 2 layers, k=300 (not a multiple of the stage), B=640, every policy."""
+    B = 300 if policy == 3 else 640
+    sc = Scenario(_gqa(3, 2, 3000 + 12, 300, B, policy=policy), ctx0=3000, steps=12, appends=True, keep=0.8,
+                  recency_mean=200, seed=policy + 1)
+    run_and_compare(sc)
+
+
+@pytest.mark.parametrize("policy", [0, 2])
+def test_mla_64_heads_no_append(policy):
+    sc = Scenario(_mla(2, 1, 6000, 512, 1024, Hq=64, policy=policy), ctx0=6000, steps=8, appends=False, keep=0.85,
+                  recency_mean=600, seed=5)
+    run_and_compare(sc)
+
+
+@pytest.mark.parametrize("io", [16, 32, 128])
+def test_io_chunk_sizes(io):
+    sc = Scenario(_gqa(2, 1, 2000 + 6, 128, 256, kvh=2, G=4, io=io), ctx0=2000, steps=6, appends=True, seed=9)
+    run_and_compare(sc)
+
+
+@pytest.mark.parametrize("G", [1, 2, 8])
+def test_gqa_group_sizes(G):
+    sc = Scenario(_gqa(2, 1, 1500, 96, 200, kvh=4, G=G), ctx0=1500, steps=5, appends=False, seed=G)
+    run_and_compare(sc)
+
+
+def test_shared_prefix_history():
+    """Requests share one prefilled history (read-only); appended tokens are private."""
+    sc = Scenario(_gqa(3, 2, 2500 + 8, 200, 400, P0=2500), ctx0=2500, steps=8, appends=True, seed=21)
+    run_and_compare(sc)
+
+
+def test_buffer_as_large_as_context_no_misses_after_warmup():
+    cfg = _gqa(1, 1, 300, 64, 320, kvh=2, log=20)
+    sc = Scenario(cfg, ctx0=300, steps=20, appends=False, keep=0.7, recency_mean=50, seed=4)
+    run_and_compare(sc)
+
+
+def test_small_k_and_b_equal_k():
+    for policy in (0, 3):
+        sc = Scenario(_gqa(2, 1, 500, 1, 1, kvh=1, G=4, policy=policy), ctx0=500, steps=10, appends=False, seed=7)
+        run_and_compare(sc)
+        sc = Scenario(_gqa(2, 1, 500, 5, 5, kvh=1, G=4, policy=policy), ctx0=500, steps=10, appends=False, seed=8)
+        run_and_compare(sc)
+
+
+def test_padding_duplicates_and_out_of_range():
+    """Invalid entries are skipped like padding, flagged, and attention ignores them."""
+    cfg = _gqa(2, 1, 400, 16, 32, kvh=2)
+    sc = Scenario(cfg, ctx0=400, steps=3, appends=False, seed=12)
+    bad = sc.trace.copy()
+    bad[1, 0, 0, 3] = -1
+    bad[1, 0, 0, 5] = bad[1, 0, 0, 4]          # duplicate of an earlier entry
+    bad[2, 0, 1, 0] = 400                      # out of range
+    bad[2, 0, 1, 1] = -7                       # negative, not padding
+    sc.trace = bad
+    pool = HsPool(cfg)
+    prefill(pool, sc)
+    orc = OracleRun(sc)
+    for t in range(3):
+        res = gpu_step(pool, sc, t)
+        ref = orc.step(t)
+        for r in range(2):
+            assert np.array_equal(res[0][0][r], ref[(r, 0)][1])
+            assert_attn_close(res[0][1][r], orc.attention(t, r, 0))
+    st = pool.stats()
+    assert st["status"] == -6
+    assert st["errors"][0, 0] == DEVERR_DUP and st["errors"][1, 0] == DEVERR_RANGE
+    assert orc.caches[(0, 0)].counters()["err"] == DEVERR_DUP
+    pool.stats(reset=True)
+    assert pool.stats()["error_bits"] == 0
+    pool.close()
+
+
+def test_append_out_of_range_flags():
+    cfg = _gqa(2, 1, 100, 4, 8, kvh=1, P0=50)
+    pool = HsPool(cfg)
+    pos = torch.tensor([10, 100], dtype=torch.int64, device="cuda")  # below the shared prefix / past capacity
+    rec = torch.zeros((2, cfg.record_elems), dtype=torch.bfloat16, device="cuda")
+    pool.append(0, pos, rec)
+    st = pool.stats()
+    assert list(st["errors"][:, 0]) == [DEVERR_APPEND, DEVERR_APPEND] and st["appends"] == 0
+    pool.close()
+
+
+def test_exactness_cold_warm_resident_bit_identical():
+    """Summary §3: the output over the hot buffer equals the output over fully resident KV,
+    bit for bit, whatever the cache held before."""
+    for cfg in (_gqa(3, 1, 5000, 512, 1024), _mla(2, 1, 5000, 512, 1024, Hq=32)):
+        sc = Scenario(cfg, ctx0=5000, steps=10, appends=False, keep=0.85, recency_mean=300, seed=2)
+        warm = HsPool(cfg)
+        prefill(warm, sc)
+        for t in range(9):
+            gpu_step(warm, sc, t, attn=False)
+        out_warm = gpu_step(warm, sc, 9)[0][1]
+        cold = HsPool(cfg)
+        prefill(cold, sc)
+        out_cold = gpu_step(cold, sc, 9)[0][1]
+        kv = torch.stack([bf16_tensor(sc.hist[(r, 0)]) for r in range(cfg.num_requests)]).cuda()
+        q = bf16_tensor(sc.q[9, 0], "cuda")
+        locs = torch.from_numpy(sc.trace[9, 0]).cuda()
+        out_res = warm.sparse_attn(0, q, locs, scale=sc.scale, kv=kv).cpu().numpy()
+        assert warm.stats()["hits"] > 0  # the warm pool served hits
+        assert np.array_equal(out_warm, out_cold)
+        assert np.array_equal(out_warm, out_res)
+        orc = OracleRun(sc)
+        for r in range(cfg.num_requests):
+            assert_attn_close(out_res[r], orc.attention(9, r, 0))
+        warm.close()
+        cold.close()
+
+
+def test_resident_kv_bad_rows_flagged():
+    cfg = _gqa(1, 1, 64, 8, 16, kvh=1)
+    pool = HsPool(cfg)
+    kv = torch.zeros((1, 10, cfg.record_elems), dtype=torch.bfloat16, device="cuda")
+    locs = torch.tensor([[0, 1, 2, 10, -1, 3, 4, 5]], dtype=torch.int32, device="cuda")
+    q = torch.zeros((1, 4, 128), dtype=torch.bfloat16, device="cuda")
+    out = pool.sparse_attn(0, q, locs, kv=kv)
+    torch.cuda.synchronize()
+    assert pool.stats()["error_bits"] == DEVERR_LOC
+    assert torch.count_nonzero(out) == 0
+    pool.close()
+
+
+def test_cuda_graph_replay_matches_eager():
+    """All calls are capturable: one decode step (append, resolve, attention for every layer)
+    captured once and replayed gives the eager results bit for bit."""
+    cfg = _gqa(2, 2, 3000 + 6, 256, 512)
+    sc = Scenario(cfg, ctx0=3000, steps=6, appends=True, seed=14)
+    eager = HsPool(cfg)
+    prefill(eager, sc)
+    graphed = HsPool(cfg)
+    prefill(graphed, sc)
+    R, L = cfg.num_requests, cfg.num_layers
+    s_pos = torch.zeros((R,), dtype=torch.int64, device="cuda")
+    s_rec = [torch.zeros((R, cfg.record_elems), dtype=torch.bfloat16, device="cuda") for _ in range(L)]
+    s_topk = [torch.zeros((R, cfg.top_k), dtype=torch.int32, device="cuda") for _ in range(L)]
+    s_q = [torch.zeros((R, cfg.num_q_heads, 128), dtype=torch.bfloat16, device="cuda") for _ in range(L)]
+    s_locs = [torch.zeros((R, cfg.top_k), dtype=torch.int32, device="cuda") for _ in range(L)]
+    s_out = [torch.zeros((R, cfg.num_q_heads, 128), dtype=torch.float32, device="cuda") for _ in range(L)]
+    stream = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            for l in range(L):
+                graphed.append(l, s_pos, s_rec[l], stream=stream)
+                graphed.resolve(l, s_topk[l], s_locs[l], stream=stream)
+                graphed.sparse_attn(l, s_q[l], s_locs[l], s_out[l], scale=sc.scale, stream=stream)
+    graphed.reset()  # capture does not execute; start both pools cold
+    torch.cuda.synchronize()
+    for t in range(sc.steps):
+        s_pos.fill_(sc.ctx0 + t)
+        for l in range(L):
+            s_rec[l].copy_(bf16_tensor(np.stack([sc.hist[(r, l)][sc.ctx0 + t] for r in range(R)])))
+            s_topk[l].copy_(torch.from_numpy(sc.trace[t, l]))
+            s_q[l].copy_(bf16_tensor(sc.q[t, l]))
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        ref = gpu_step(eager, sc, t)
+        for l in range(L):
+            assert np.array_equal(s_locs[l].cpu().numpy(), ref[l][0])
+            assert np.array_equal(s_out[l].cpu().numpy(), ref[l][1])
+    for l in range(L):
+        a, b = eager.read_state(l), graphed.read_state(l)
+        assert all(np.array_equal(x, y) for x, y in zip(a, b))
+    eager.close()
+    graphed.close()
+
+
+def test_fault_injection_allocations(monkeypatch):
+    cfg = _gqa(1, 1, 64, 8, 16, kvh=1)
+    from hierarchical_kv_cache_02_gb300 import HsError
+
+    for what, code in (("alloc_host", -2), ("alloc_dev", -3)):
+        monkeypatch.setenv("HS_FAULT", what)
+        with pytest.raises(HsError) as e:
+            HsPool(cfg)
+        assert e.value.status == code
+    monkeypatch.delenv("HS_FAULT")
+    HsPool(cfg).close()
