@@ -1,0 +1,468 @@
+"""Benchmark of the HiSparse decode hot path on one GB300 (or N independent replicas).
+
+One step = one decode step over every layer of the workload: per layer, write-through append
+of the new token, fused resolve of the layer's top-k, sparse attention over the resolved slots.
+Default workload (GQA, 32 layers): batch 16, 8 KV heads x (128 K + 128 V) bf16 per token,
+32 query heads, context 131072, k = 2048, B = 4096 slots per (request, layer), LRU, drift
+traces keeping 88% per step (recency mean 2048).  The 16 requests share one prefilled
+131072-token history per layer (17 GB of pinned host memory); appended tokens are private.
+
+Printed: one JSON line (rank 0).  `value` = decode layer-steps/s (one layer for the whole
+batch) with every input resident in HBM; `e2e` = the same with per-step inputs copied from
+pinned host memory and outputs copied back inside the timed region.
+`--impl reference` times the CPU oracle (test infrastructure, single-threaded) on a bounded
+sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "resolve+sparse-attn µs/layer and decode layer-steps/s; HBM & host-link GB/s"
+
+WORKLOADS = {
+    # batch 16, 32 layers, GQA 8 x (128 | 128), 32 q heads, ctx 131072, k 2048, B 4096, keep 88%
+    "gqa_b16_l32": dict(R=16, L=32, ctx0=131072, layout=1, Hq=32, Hkv=8, Dqk=128, Dv=128, k=2048, B=4096,
+                        keep=0.88, mu=2048.0, burst=0, shared=True, steps=64),
+    # batch 8, 1 layer, MLA 576-dim latent, 64 heads, ctx 32768, k 2048, B 4096, keep 88%
+    "mla_b8": dict(R=8, L=1, ctx0=32768, layout=0, Hq=64, Hkv=1, Dqk=576, Dv=512, k=2048, B=4096,
+                   keep=0.88, mu=2048.0, burst=0, shared=False, steps=128),
+    # stress: batch 16, 4 layers, MLA, ctx 262144, k 2048, B 8192, bursts every 32 steps
+    "stress_b16_l4": dict(R=16, L=4, ctx0=262144, layout=0, Hq=64, Hkv=1, Dqk=576, Dv=512, k=2048, B=8192,
+                          keep=0.88, mu=2048.0, burst=32, shared=False, steps=128),
+    # tiny: 1 request, 1 layer, MLA 16 heads, ctx 4096, k 256, B 512, keep 90%, recency 512
+    "tiny": dict(R=1, L=1, ctx0=4096, layout=0, Hq=16, Hkv=1, Dqk=576, Dv=512, k=256, B=512,
+                 keep=0.9, mu=512.0, burst=0, shared=False, steps=64),
+}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def record_bytes(w):
+    return 2 * w["Dqk"] if w["layout"] == 0 else 2 * w["Hkv"] * (w["Dqk"] + w["Dv"])
+
+
+def attn_bytes_per_launch(w):
+    """Algorithmic bytes of one attention launch (one layer, all requests): the k gathered
+    records, q, the fp32 output and the slot list."""
+    return w["R"] * (w["k"] * record_bytes(w) + w["Hq"] * w["Dqk"] * 2 + w["Hq"] * w["Dv"] * 4 + w["k"] * 4)
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.device_index = device_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.device_index), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def reduce_max(value, world):
+    """Max over ranks (gloo or NCCL); the identity for one process."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(value)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# --------------------------------------------------------------------------------------------
+class Workload:
+    """Seeded synthetic inputs of one replica, resident on the GPU."""
+
+    def __init__(self, w, steps, device, seed):
+        import torch
+
+        from hierarchical_kv_cache_02_gb300 import HsConfig, inputs
+
+        self.w, self.steps, self.device = w, steps, device
+        R, L, k = w["R"], w["L"], w["k"]
+        self.cfg = HsConfig(num_requests=R, num_layers=L, capacity=w["ctx0"] + steps, layout=w["layout"],
+                            num_q_heads=w["Hq"], num_kv_heads=w["Hkv"], head_dim_qk=w["Dqk"], head_dim_v=w["Dv"],
+                            top_k=k, buffer_slots=w["B"], policy=0, seed=seed, io_chunk_bytes=64,
+                            shared_prefix=w["ctx0"] if w["shared"] else 0)
+        spec = inputs.TraceSpec(ctx0=w["ctx0"], k=k, steps=steps, keep=w["keep"], recency_mean=w["mu"],
+                                appends=True, burst_every=w["burst"], far_gap=int(8 * w["mu"]))
+        t0 = time.time()
+        self.trace_host = inputs.drift_traces(spec, R, L, seed=seed)            # [S][L][R][k]
+        self.trace_secs = time.time() - t0
+        self.topk = torch.from_numpy(self.trace_host).to(device)
+        E = self.cfg.record_elems
+        self.q = inputs.normal_bf16((steps, L, R, w["Hq"], w["Dqk"]), seed=seed + 1, device=device)
+        self.app = inputs.normal_bf16((steps, L, R, E), seed=seed + 2, device=device)
+        self.pos = (torch.arange(steps, dtype=torch.int64, device=device) + w["ctx0"]).view(steps, 1).expand(
+            steps, R).contiguous()
+        self.hist_seed = seed + 3
+
+    def history_layer(self, l, r=0):
+        """The prefilled records of (r, l): regenerated from its seed (no copy kept)."""
+        from hierarchical_kv_cache_02_gb300 import inputs
+
+        w = self.w
+        s = self.hist_seed + 7919 * l + (0 if w["shared"] else 104729 * (r + 1))
+        return inputs.normal_bf16((w["ctx0"], self.cfg.record_elems), seed=s, device=self.device)
+
+    def prefill(self, pool):
+        w = self.w
+        for l in range(w["L"]):
+            for r in range(1 if w["shared"] else w["R"]):
+                pool.prefill(r, l, 0, self.history_layer(l, r))
+
+
+def run_ours(args, w, world, rank, local):
+    import torch
+
+    from hierarchical_kv_cache_02_gb300 import HsPool, _lib
+
+    torch.cuda.set_device(local)
+    device = f"cuda:{local}"
+    _lib.load()
+    W, K = args.warmup, args.steps
+    S = W + K
+    t_setup = time.time()
+    wl = Workload(w, S, device, seed=1000 + 17 * rank)
+    pool = HsPool(wl.cfg, device=local)
+    wl.prefill(pool)
+    torch.cuda.synchronize()
+    setup_secs = time.time() - t_setup
+    R, L, k = w["R"], w["L"], w["k"]
+    scale = wl.cfg.default_scale
+    locs = [torch.empty((R, k), dtype=torch.int32, device=device) for _ in range(L)]
+    outs = [torch.empty((R, w["Hq"], w["Dv"]), dtype=torch.float32, device=device) for _ in range(L)]
+    stream = torch.cuda.current_stream()
+
+    def step(t, ev=None):
+        for l in range(L):
+            if ev is not None:
+                ev[l][0].record(stream)
+            pool.append(l, wl.pos[t], wl.app[t, l])
+            if ev is not None:
+                ev[l][1].record(stream)
+            pool.resolve(l, wl.topk[t, l], locs[l])
+            if ev is not None:
+                ev[l][2].record(stream)
+            pool.sparse_attn(l, wl.q[t, l], locs[l], outs[l], scale=scale)
+            if ev is not None:
+                ev[l][3].record(stream)
+
+    for t in range(W):
+        step(t)
+    torch.cuda.synchronize()
+    pool.stats(reset=True)
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(L)] for _ in range(K)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for i in range(K):
+        step(W + i, evs[i])
+    stop.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    elapsed = start.elapsed_time(stop) / 1e3
+    st = pool.stats()
+    app_ms = np.array([[e[l][0].elapsed_time(e[l][1]) for l in range(L)] for e in evs])
+    res_ms = np.array([[e[l][1].elapsed_time(e[l][2]) for l in range(L)] for e in evs])
+    att_ms = np.array([[e[l][2].elapsed_time(e[l][3]) for l in range(L)] for e in evs])
+    max_elapsed = reduce_max(elapsed, world)
+    units = world * K * L
+    value = units / max_elapsed
+
+    # ---- end to end through the public API: inputs from pinned host memory, outputs back -----
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(pool, wl, W, K, world, locs, outs, scale)
+
+    # ---- host-link peak on this machine: pinned H2D copy, best of 5 ----
+    h2d = measure_h2d(device)
+    peaks = load_peaks()
+    attn_us = float(att_ms.mean() * 1e3)
+    achieved = attn_bytes_per_launch(w) / (attn_us * 1e-6) / 1e9
+    rec = record_bytes(w)
+    miss_bytes = float(st["host_bytes"])
+    res_total_s = float(res_ms.sum() / 1e3)
+    out = {
+        "metric": METRIC, "value": value, "unit": "layer-steps/s", "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": max_elapsed / K * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "requests": R, "layers": L, "context": w["ctx0"], "top_k": k,
+                   "buffer_slots": w["B"], "layout": "gqa" if w["layout"] == 1 else "mla", "q_heads": w["Hq"],
+                   "kv_heads": w["Hkv"], "record_bytes": rec, "policy": "lru", "keep": w["keep"],
+                   "recency_mean": w["mu"], "burst_every": w["burst"], "shared_history": w["shared"],
+                   "append": True, "parallelism": f"replicas{world}",
+                   "l2": "inputs larger than L2 (each attention launch gathers "
+                         f"{attn_bytes_per_launch(w) / 1e6:.0f} MB; a step touches {L} layers)"},
+        "us_per_layer": {"total": max_elapsed / (K * L) * 1e6, "resolve": float(res_ms.mean() * 1e3),
+                         "sparse_attn": attn_us, "append": float(app_ms.mean() * 1e3),
+                         "resolve_plus_attn": float((res_ms + att_ms).mean() * 1e3)},
+        "miss_rate": float(st["misses"]) / max(1.0, float(st["hits"] + st["misses"])),
+        "roofline": {"kernel": "sparse_attn", "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": args.traffic,
+                     "peak_source": peaks["source"],
+                     "bytes_per_launch": attn_bytes_per_launch(w)},
+        "host_link": {"kernel": "resolve", "miss_bytes_per_layer": miss_bytes / (K * L),
+                      "achieved_gbs": miss_bytes / res_total_s / 1e9 if res_total_s > 0 else None,
+                      "h2d_copy_peak_gbs": h2d,
+                      "frac": (miss_bytes / res_total_s / 1e9) / h2d if res_total_s > 0 and h2d else None},
+        "gpu_launches": K * L * 3,
+        "clocks": clk,
+        "setup_s": setup_secs,
+        "errors": int(st["error_bits"]),
+    }
+    if e2e is not None:
+        out["e2e"] = e2e
+    pool.close()
+    return out
+
+
+def run_e2e(pool, wl, W, K, world, locs, outs, scale):
+    """Same steps after a cold reset, with this step's top-k, queries and new records copied
+    from pinned host memory and the attention outputs copied back inside the timed region."""
+    import torch
+
+    w = wl.w
+    R, L, k = w["R"], w["L"], w["k"]
+    S = W + K
+    h_topk = torch.from_numpy(wl.trace_host).pin_memory()
+    h_q = wl.q.cpu().pin_memory()
+    h_app = wl.app.cpu().pin_memory()
+    h_pos = wl.pos.cpu().pin_memory()
+    h_out = torch.empty((S, L, R, w["Hq"], w["Dv"]), dtype=torch.float32).pin_memory()
+    d_topk = torch.empty((L, R, k), dtype=torch.int32, device=wl.device)
+    d_q = torch.empty((L, R, w["Hq"], w["Dqk"]), dtype=torch.bfloat16, device=wl.device)
+    d_app = torch.empty((L, R, wl.cfg.record_elems), dtype=torch.bfloat16, device=wl.device)
+    d_pos = torch.empty((R,), dtype=torch.int64, device=wl.device)
+    stream = torch.cuda.current_stream()
+
+    def step(t):
+        d_topk.copy_(h_topk[t], non_blocking=True)
+        d_q.copy_(h_q[t], non_blocking=True)
+        d_app.copy_(h_app[t], non_blocking=True)
+        d_pos.copy_(h_pos[t], non_blocking=True)
+        for l in range(L):
+            pool.append(l, d_pos, d_app[l])
+            pool.resolve(l, d_topk[l], locs[l])
+            pool.sparse_attn(l, d_q[l], locs[l], outs[l], scale=scale)
+            h_out[t, l].copy_(outs[l], non_blocking=True)
+
+    pool.reset()
+    for t in range(W):
+        step(t)
+    torch.cuda.synchronize()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for i in range(K):
+        step(W + i)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    el = reduce_max(start.elapsed_time(stop) / 1e3, world)
+    h2d_bytes = (h_topk[0].numel() * 4 + h_q[0].numel() * 2 + h_app[0].numel() * 2 + h_pos[0].numel() * 8)
+    d2h_bytes = L * R * w["Hq"] * w["Dv"] * 4
+    return {"value": world * K * L / el, "unit": "layer-steps/s", "h2d_bytes_per_step": int(h2d_bytes),
+            "d2h_bytes_per_step": int(d2h_bytes), "ms_per_step": el / K * 1e3}
+
+
+def measure_h2d(device):
+    import torch
+
+    n = 1 << 30
+    h = torch.empty(n, dtype=torch.uint8).pin_memory()
+    d = torch.empty(n, dtype=torch.uint8, device=device)
+    best = float("inf")
+    for _ in range(5):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        d.copy_(h, non_blocking=True)
+        e.record()
+        torch.cuda.synchronize()
+        best = min(best, s.elapsed_time(e) / 1e3)
+    del h, d
+    return n / best / 1e9
+
+
+# --------------------------------------------------------------------------------------------
+def oracle_sample(w, steps, seed, budget_s, pairs_max=64):
+    """Time the CPU oracle on (request, layer) pairs of the workload: each pair replays its own
+    top-k trace from step 0 (append, resolve) with fp64 attention every step, until the time
+    budget is spent.  Returns seconds per (request, layer)-step and a description."""
+    import torch
+
+    import oracle
+    from hierarchical_kv_cache_02_gb300 import inputs
+
+    R, L, k = w["R"], w["L"], w["k"]
+    spec = inputs.TraceSpec(ctx0=w["ctx0"], k=k, steps=steps, keep=w["keep"], recency_mean=w["mu"], appends=True,
+                            burst_every=w["burst"], far_gap=int(8 * w["mu"]))
+    E = record_bytes(w) // 2
+    kvh = 0 if w["layout"] == 0 else w["Hkv"]
+    scale = float(np.float32(1.0 / math.sqrt(w["Dqk"])))
+    # one history stands in for every sampled pair: the oracle's cost does not depend on the values
+    hist = inputs.normal_bf16((w["ctx0"] + steps, E), seed=seed).view(torch.int16).numpy().view(np.uint16)
+    total_t, n_rl_steps, pairs = 0.0, 0, 0
+    for p in range(pairs_max):
+        r, l = p % R, (p * 7) % L
+        # the trace of (r, l) in a batch seeded `seed` is the single trace seeded seed + r*65536 + l
+        tr = inputs.drift_traces(spec, 1, 1, seed=seed + r * 65536 + l)[:, 0, 0]
+        q = inputs.normal_bf16((steps, w["Hq"], w["Dqk"]), seed=seed + 1 + p).view(torch.int16).numpy().view(np.uint16)
+        cache = oracle.Cache(w["B"], k, "lru", R=R, L=L, r=r, l=l, C=w["ctx0"] + steps)
+        t0 = time.perf_counter()
+        for t in range(steps):
+            cache.append(w["ctx0"] + t)
+            cache.resolve(tr[t])
+            oracle.attention(q[t], hist, tr[t], scale, kvh, w["Dqk"], w["Dv"])
+            n_rl_steps += 1
+            if total_t + time.perf_counter() - t0 > budget_s:
+                break
+        total_t += time.perf_counter() - t0
+        pairs += 1
+        if total_t > budget_s:
+            break
+    per = total_t / max(1, n_rl_steps)
+    desc = (f"{n_rl_steps} (request, layer)-steps of {pairs} pairs, each replayed from step 0 (append, resolve, "
+            f"fp64 attention), {total_t:.1f} s on 1 core; layer-steps/s = 1 / ({R} x s per (request, layer)-step)")
+    return per, desc, n_rl_steps
+
+
+def run_reference(args, w, world, rank):
+    """CPU oracle on the host cores, bounded sample per step (rank 0 only)."""
+    if rank != 0:
+        return None
+    K, W = args.steps, args.warmup
+    budget_per_step = float(os.environ.get("HS_REF_STEP_SECONDS", "1.0"))
+    per, desc, n = oracle_sample(w, steps=min(W + K, w["steps"]), seed=99, budget_s=budget_per_step * (K + W))
+    value = 1.0 / (w["R"] * per)
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "layer-steps/s", "n_gpus": world,
+            "steps": K, "warmup": W, "ms_per_step": w["L"] / value * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "requests": w["R"], "layers": w["L"], "context": w["ctx0"],
+                       "top_k": w["k"], "buffer_slots": w["B"]},
+            "cpu_baseline": {"value": value, "unit": "layer-steps/s", "cores": 1, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": "layer-steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=56)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="gqa_b16_l32")
+    ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling runs)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per attention launch from an ncu capture of the same kernel")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    w = dict(WORKLOADS[args.workload])
+    if args.layers:
+        w["L"] = args.layers
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        out = run_reference(args, w, world, rank)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return
+    out = run_ours(args, w, world, rank, local)
+    if rank == 0 and not args.no_cpu_baseline:
+        per, desc, n = oracle_sample(w, steps=min(16, args.warmup + args.steps), seed=99, budget_s=args.cpu_seconds)
+        out["cpu_baseline"] = {"value": 1.0 / (w["R"] * per), "unit": "layer-steps/s", "cores": 1, "kind": "oracle",
+                               "sample": desc}
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -352,15 +352,292 @@ __global__ void __launch_bounds__(AttnCfg<DK, DV, G, NW>::THREADS) k_attn_cc(Att
   if (threadIdx.x == 0) a.ticket[(int64_t)r * a.groups + grp] = 0u;
 }
 
+// ---- tensor-core variant for GQA records ----------------------------------------
+//
+// A KV block (one KV head) serves G <= 8 query heads.  Per 16-token tile a consumer warp runs
+//   S[16 x 8] = Q[16 x 128] . K^T          (rows 0..G-1 are the heads, the rest zero padding)
+//   O[16 x 128] += P[16 x 16] . V[16 x 128]
+// on mma.sync m16n8k16 (bf16 in, fp32 accumulate).  K and V fragments come from the staged
+// records with ldmatrix (non-transposed for K, transposed for V); each staged record is padded
+// by 16 bytes so the eight rows of every 8x8 matrix fall in distinct banks.  P is split into a
+// bf16 high part and a bf16 remainder, two MMAs, so the probabilities keep ~16 mantissa bits.
+
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ float bf16_lo_f(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi_f(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+constexpr int kMmaTile = 16;  // tokens per stage
+
+template <int G, int NW, int NSTAGE>
+__global__ void __launch_bounds__((NW + 1) * 32, 1) k_attn_gqa_mma(AttnArgs a) {
+  constexpr int T = kMmaTile;
+  constexpr int D = 128;  // head_dim_qk == head_dim_v
+  static_assert(G >= 1 && G <= 8, "up to 8 query heads per KV head");
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t full_bar[NSTAGE];
+  __shared__ __align__(8) uint64_t empty_bar[NSTAGE];
+  __shared__ uint32_t tok_mask[NSTAGE];
+  __shared__ uint32_t abort_flag;
+  __shared__ uint32_t is_last;
+
+  const int split = blockIdx.x, r = blockIdx.y, grp = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t0 = split * a.chunk;
+  const int t1 = min(a.k, t0 + a.chunk);
+  const int nst = (t1 - t0 + T - 1) / T;
+  const int64_t rec = a.rec;
+  const uint32_t rs = (uint32_t)rec + 16u;  // padded row stride in shared memory
+  const int32_t* locs = a.locs + (int64_t)r * a.k;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NSTAGE; ++s) {
+      mbar_init(&full_bar[s], 1u);
+      mbar_init(&empty_bar[s], (uint32_t)NW);
+    }
+    abort_flag = 0u;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+
+  const int g = grp * NW + warp;  // KV head of this consumer warp
+  const int grow = lane >> 2, tig = lane & 3;
+  float o[16][4];
+  float m_run = -INFINITY, l_run = 0.f;
+
+  if (warp == NW) {
+    if (lane == 0) {
+      uint32_t bad = 0u;
+      int issued = 0;
+      for (int st = 0; st < nst; ++st) {
+        const int b = st % NSTAGE;
+        if (st >= NSTAGE) {
+          if (!mbar_wait_bounded(&empty_bar[b], (uint32_t)((st / NSTAGE - 1) & 1), &abort_flag)) {
+            *(volatile uint32_t*)&abort_flag = 1u;
+            atomicOr(a.err, (uint32_t)HS_DEVERR_TIMEOUT);
+            break;
+          }
+        }
+        uint32_t mask = 0u, nvalid = 0u;
+        for (int j = 0; j < T; ++j) {
+          const int idx = t0 + st * T + j;
+          int32_t loc = idx < t1 ? locs[idx] : -1;
+          if (loc < -1 || (int64_t)loc >= a.rows) {
+            bad = 1u;
+            loc = -1;
+          }
+          if (loc >= 0) {
+            mask |= 1u << j;
+            ++nvalid;
+          }
+        }
+        tok_mask[b] = mask;
+        mbar_arrive_expect_tx(&full_bar[b], nvalid * (uint32_t)rec);
+        uint8_t* dst = smem + (size_t)b * T * rs;
+        for (int j = 0; j < T; ++j) {
+          if ((mask >> j) & 1u) {
+            const int32_t loc = locs[t0 + st * T + j];
+            bulk_g2s(dst + (size_t)j * rs, a.kv + ((int64_t)r * a.rows + loc) * rec, (uint32_t)rec, &full_bar[b]);
+          }
+        }
+        issued = st + 1;
+      }
+      if (bad) atomicOr(a.err, (uint32_t)HS_DEVERR_LOC);
+      if (abort_flag) {
+        for (int st = max(0, issued - NSTAGE); st < issued; ++st) {
+          volatile uint32_t never = 0u;
+          mbar_wait_bounded(&full_bar[st % NSTAGE], (uint32_t)((st / NSTAGE) & 1), &never);
+        }
+      }
+    }
+  } else {
+    // query fragments (A operand, rows = heads): only rows 0..G-1 are non-zero
+    uint32_t qa[8][2];
+    {
+      const uint32_t* qw = (const uint32_t*)(a.q + ((int64_t)r * a.Hq + (int64_t)g * G + (grow < G ? grow : 0)) * D);
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        qa[s][0] = grow < G ? qw[s * 8 + tig] : 0u;
+        qa[s][1] = grow < G ? qw[s * 8 + 4 + tig] : 0u;
+      }
+    }
+#pragma unroll
+    for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    const uint32_t koff = (uint32_t)(g * a.kstride);
+    const uint32_t voff = koff + (uint32_t)a.vdelta;
+    // ldmatrix row addresses: K (non-transposed) and V (transposed) patterns
+    const uint32_t k_tok = (uint32_t)((lane & 7) + ((lane >> 4) << 3));
+    const uint32_t k_col = (uint32_t)(((lane >> 3) & 1) * 16);
+    const uint32_t v_tok = (uint32_t)((lane & 7) + (((lane >> 3) & 1) << 3));
+    const uint32_t v_col = (uint32_t)((lane >> 4) * 16);
+    const uint32_t sbase = smem_u32(smem);
+    for (int st = 0; st < nst; ++st) {
+      const int b = st % NSTAGE;
+      if (!mbar_wait_bounded(&full_bar[b], (uint32_t)((st / NSTAGE) & 1), &abort_flag)) {
+        *(volatile uint32_t*)&abort_flag = 1u;
+        atomicOr(a.err, (uint32_t)HS_DEVERR_TIMEOUT);
+        break;
+      }
+      const uint32_t mask = tok_mask[b];
+      const uint32_t stage = sbase + (uint32_t)b * T * rs;
+      // S = Q K^T for tokens 0-7 (s0) and 8-15 (s1)
+      float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint32_t kaddr = stage + k_tok * rs + koff + k_col;
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kaddr + s * 32, b0, b1, b2, b3);
+        mma_bf16(s0, qa[s][0], 0u, qa[s][1], 0u, b0, b1);
+        mma_bf16(s1, qa[s][0], 0u, qa[s][1], 0u, b2, b3);
+      }
+      // online softmax on rows grow (< G): this lane holds tokens 2 tig, 2 tig + 1 (+8)
+      const int ta = 2 * tig;
+      float x0 = ((mask >> ta) & 1u) ? s0[0] * a.qscale : -INFINITY;
+      float x1 = ((mask >> (ta + 1)) & 1u) ? s0[1] * a.qscale : -INFINITY;
+      float x2 = ((mask >> (ta + 8)) & 1u) ? s1[0] * a.qscale : -INFINITY;
+      float x3 = ((mask >> (ta + 9)) & 1u) ? s1[1] * a.qscale : -INFINITY;
+      float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const float m_new = fmaxf(m_run, mx);
+      const bool any = m_new != -INFINITY;
+      const float alpha = any ? exp2f(m_run - m_new) : 1.f;
+      const float p0 = any ? exp2f(x0 - m_new) : 0.f;
+      const float p1 = any ? exp2f(x1 - m_new) : 0.f;
+      const float p2 = any ? exp2f(x2 - m_new) : 0.f;
+      const float p3 = any ? exp2f(x3 - m_new) : 0.f;
+      float ps = (p0 + p1) + (p2 + p3);
+      ps += __shfl_xor_sync(0xffffffffu, ps, 1);
+      ps += __shfl_xor_sync(0xffffffffu, ps, 2);
+      m_run = m_new;
+      l_run = l_run * alpha + ps;
+#pragma unroll
+      for (int n = 0; n < 16; ++n) {
+        o[n][0] *= alpha;
+        o[n][1] *= alpha;
+      }
+      // P as the A operand: high bf16 part and remainder; rows >= G stay zero
+      uint32_t ph0 = 0u, ph2 = 0u, pl0 = 0u, pl2 = 0u;
+      if (grow < G) {
+        ph0 = pack_bf16(p0, p1);
+        ph2 = pack_bf16(p2, p3);
+        pl0 = pack_bf16(p0 - bf16_lo_f(ph0), p1 - bf16_hi_f(ph0));
+        pl2 = pack_bf16(p2 - bf16_lo_f(ph2), p3 - bf16_hi_f(ph2));
+      }
+      // tokens this lane holds in V fragments: 2 tig, 2 tig + 1 (and +8); zero invalid ones
+      uint32_t vm_lo = 0xffffffffu, vm_hi = 0xffffffffu;
+      if (mask != 0xffffu) {
+        vm_lo = (((mask >> ta) & 1u) ? 0x0000ffffu : 0u) | (((mask >> (ta + 1)) & 1u) ? 0xffff0000u : 0u);
+        vm_hi = (((mask >> (ta + 8)) & 1u) ? 0x0000ffffu : 0u) | (((mask >> (ta + 9)) & 1u) ? 0xffff0000u : 0u);
+      }
+      const uint32_t vaddr = stage + v_tok * rs + voff + v_col;
+#pragma unroll
+      for (int pr = 0; pr < 8; ++pr) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(vaddr + pr * 32, b0, b1, b2, b3);
+        b0 &= vm_lo;
+        b1 &= vm_hi;
+        b2 &= vm_lo;
+        b3 &= vm_hi;
+        mma_bf16(o[2 * pr], ph0, 0u, ph2, 0u, b0, b1);
+        mma_bf16(o[2 * pr], pl0, 0u, pl2, 0u, b0, b1);
+        mma_bf16(o[2 * pr + 1], ph0, 0u, ph2, 0u, b2, b3);
+        mma_bf16(o[2 * pr + 1], pl0, 0u, pl2, 0u, b2, b3);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[b]);
+    }
+    if (!abort_flag && grow < G) {
+      const int64_t ph = ((int64_t)r * a.S + split) * a.Hq + (int64_t)g * G + grow;
+      float* po = a.part + ph * D;
+#pragma unroll
+      for (int n = 0; n < 16; ++n) *(float2*)(po + n * 8 + 2 * tig) = make_float2(o[n][0], o[n][1]);
+      if (tig == 0) {
+        a.ml[ph * 2 + 0] = m_run;
+        a.ml[ph * 2 + 1] = l_run;
+      }
+    }
+  }
+  __threadfence();
+  __syncthreads();
+  if (abort_flag) return;
+  if (threadIdx.x == 0) {
+    const uint32_t t = atomicAdd(&a.ticket[(int64_t)r * a.groups + grp], 1u);
+    is_last = (t == (uint32_t)(a.S - 1)) ? 1u : 0u;
+  }
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  if (warp < NW) {
+#pragma unroll 1
+    for (int x = 0; x < G; ++x) {
+      const int h = g * G + x;
+      float M = -INFINITY;
+      for (int s2 = 0; s2 < a.S; ++s2) M = fmaxf(M, __ldcg(&a.ml[(((int64_t)r * a.S + s2) * a.Hq + h) * 2]));
+      float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+      float den = 0.f;
+      if (M != -INFINITY) {
+        for (int s2 = 0; s2 < a.S; ++s2) {
+          const int64_t ph = ((int64_t)r * a.S + s2) * a.Hq + h;
+          const float ms = __ldcg(&a.ml[ph * 2]);
+          const float w = ms == -INFINITY ? 0.f : exp2f(ms - M);
+          den += w * __ldcg(&a.ml[ph * 2 + 1]);
+          const float2* po = (const float2*)(a.part + ph * D);
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const float2 v = __ldcg(&po[lane + 32 * u]);
+            acc[u][0] = fmaf(w, v.x, acc[u][0]);
+            acc[u][1] = fmaf(w, v.y, acc[u][1]);
+          }
+        }
+      }
+      const float inv = den > 0.f ? 1.f / den : 0.f;
+      float2* out = (float2*)(a.out + ((int64_t)r * a.Hq + h) * D);
+#pragma unroll
+      for (int u = 0; u < 2; ++u) out[lane + 32 * u] = make_float2(acc[u][0] * inv, acc[u][1] * inv);
+    }
+  }
+  if (threadIdx.x == 0) a.ticket[(int64_t)r * a.groups + grp] = 0u;
+}
+
 // ---- dispatch ----------------------------------------------------------------
 
 struct Plan {
+  int kind;  // 0: CUDA-core kernel (shared-latent records), 1: tensor-core GQA kernel
   int NW, G, T, groups, S, chunk;
   size_t smem;
 };
 
+constexpr int kMmaStages = 3;
+
 bool plan_for(const hs_config* c, int num_sms, Plan* pl) {
   const int64_t rec = hs_record_bytes(c);
+  int per_cta_wave;
   if (c->layout == HS_LAYOUT_GQA) {
     if (c->head_dim_qk != 128 || c->head_dim_v != 128) return false;
     const int G = c->num_q_heads / c->num_kv_heads;
@@ -370,21 +647,28 @@ bool plan_for(const hs_config* c, int num_sms, Plan* pl) {
       if (NW % 8 != 0) return false;
       NW = 8;
     }
+    if (NW != 1 && NW != 2 && NW != 4 && NW != 8) return false;
+    pl->kind = 1;
     pl->NW = NW;
     pl->G = G;
     pl->groups = c->num_kv_heads / NW;
+    pl->T = kMmaTile;
+    pl->smem = (size_t)kMmaStages * kMmaTile * (size_t)(rec + 16);
+    per_cta_wave = 1;  // one CTA per SM: the ring holds most of the shared memory
   } else {
     if (c->head_dim_qk != 576 || c->head_dim_v != 512) return false;
     if (c->num_q_heads % 8 != 0) return false;
+    pl->kind = 0;
     pl->NW = 8;
     pl->G = 1;
     pl->groups = c->num_q_heads / 8;
+    pl->T = 32 / pl->G;
+    pl->smem = (size_t)kStages * pl->T * (size_t)rec;
+    per_cta_wave = 2;
   }
-  pl->T = 32 / pl->G;
-  pl->smem = (size_t)kStages * pl->T * (size_t)rec;
   if (pl->smem > 200 * 1024) return false;
   const int per_split = c->num_requests * pl->groups;
-  int S = (2 * num_sms + per_split - 1) / per_split;
+  int S = per_cta_wave * num_sms / per_split;
   const int max_s = (c->top_k + pl->T - 1) / pl->T;
   S = S < 1 ? 1 : (S > max_s ? max_s : S);
   int chunk = (c->top_k + S - 1) / S;
@@ -394,29 +678,28 @@ bool plan_for(const hs_config* c, int num_sms, Plan* pl) {
   return true;
 }
 
-template <int DK, int DV, int G, int NW>
-cudaError_t launch_cc(const AttnArgs* a, const Plan& pl, cudaStream_t st) {
-  auto kern = k_attn_cc<DK, DV, G, NW>;
+template <typename K>
+cudaError_t launch_kernel(K kern, const AttnArgs* a, const Plan& pl, int threads, cudaStream_t st) {
   if (a == nullptr)  // preparation: raise the dynamic shared-memory limit once
     return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
   dim3 grid(pl.S, a->R, pl.groups);
-  kern<<<grid, AttnCfg<DK, DV, G, NW>::THREADS, pl.smem, st>>>(*a);
+  kern<<<grid, threads, pl.smem, st>>>(*a);
   return cudaGetLastError();
 }
 
 template <int G>
 cudaError_t launch_gqa_nw(const AttnArgs* a, const Plan& pl, cudaStream_t st) {
   switch (pl.NW) {
-    case 1: return launch_cc<128, 128, G, 1>(a, pl, st);
-    case 2: return launch_cc<128, 128, G, 2>(a, pl, st);
-    case 4: return launch_cc<128, 128, G, 4>(a, pl, st);
-    case 8: return launch_cc<128, 128, G, 8>(a, pl, st);
+    case 1: return launch_kernel(k_attn_gqa_mma<G, 1, kMmaStages>, a, pl, 2 * 32, st);
+    case 2: return launch_kernel(k_attn_gqa_mma<G, 2, kMmaStages>, a, pl, 3 * 32, st);
+    case 4: return launch_kernel(k_attn_gqa_mma<G, 4, kMmaStages>, a, pl, 5 * 32, st);
+    case 8: return launch_kernel(k_attn_gqa_mma<G, 8, kMmaStages>, a, pl, 9 * 32, st);
     default: return cudaErrorInvalidValue;
   }
 }
 
 cudaError_t dispatch(const hs_config& c, const AttnArgs* a, const Plan& pl, cudaStream_t st) {
-  if (c.layout == HS_LAYOUT_MLA) return launch_cc<576, 512, 1, 8>(a, pl, st);
+  if (pl.kind == 0) return launch_kernel(k_attn_cc<576, 512, 1, 8>, a, pl, AttnCfg<576, 512, 1, 8>::THREADS, st);
   switch (pl.G) {
     case 1: return launch_gqa_nw<1>(a, pl, st);
     case 2: return launch_gqa_nw<2>(a, pl, st);
@@ -429,9 +712,7 @@ cudaError_t dispatch(const hs_config& c, const AttnArgs* a, const Plan& pl, cuda
 
 bool hs_attn_supported(const hs_config* c) {
   Plan pl;
-  if (!plan_for(c, 152, &pl)) return false;
-  if (c->layout == HS_LAYOUT_GQA && pl.NW != 1 && pl.NW != 2 && pl.NW != 4 && pl.NW != 8) return false;
-  return true;
+  return plan_for(c, 152, &pl);
 }
 
 void hs_attn_workspace(const hs_config* c, int num_sms, size_t* floats, int* max_splits, int* max_groups) {

@@ -40,6 +40,7 @@ struct hs_pool {
   float* attn_part;      // split partials
   uint32_t* attn_ticket; // [R][attn_max_groups]
   int attn_max_splits;
+  int resolve_cs;        // CTAs per request in the resolve cluster
   int attn_max_groups;
   size_t attn_part_floats;
 };
@@ -82,5 +83,5 @@ int hs_launch_attn(hs_pool* pool, int layer, const void* d_q, const int32_t* d_l
 void hs_attn_workspace(const hs_config* cfg, int num_sms, size_t* floats, int* max_splits, int* max_groups);
 bool hs_attn_supported(const hs_config* cfg);
 int hs_attn_prepare(const hs_config* cfg, int num_sms);
-int hs_resolve_prepare(const hs_config* cfg);
+int hs_resolve_prepare(hs_pool* pool);
 size_t hs_resolve_smem_bytes(const hs_config* cfg);

@@ -178,7 +178,7 @@ extern "C" int hs_pool_create(const hs_config* cfg, int cuda_device, hs_pool** o
     rc = dev_alloc(&p->attn_part, p->attn_part_floats);
   }
   if (rc == HS_OK) rc = dev_alloc(&p->attn_ticket, R * (size_t)p->attn_max_groups);
-  if (rc == HS_OK) rc = hs_resolve_prepare(cfg);
+  if (rc == HS_OK) rc = hs_resolve_prepare(p);
   if (rc == HS_OK) rc = hs_attn_prepare(cfg, p->num_sms);
   if (rc == HS_OK) rc = do_reset(p, 0);
   if (rc == HS_OK && cudaDeviceSynchronize() != cudaSuccess) rc = HS_ERR_CUDA;

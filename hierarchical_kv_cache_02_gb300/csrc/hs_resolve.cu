@@ -34,7 +34,7 @@ struct ResolveArgs {
   uint8_t* buf;         // layer slice [R][B][rec]
   int64_t C, P0, priv_tokens, rec;
   uint64_t seed;
-  int R, L, layer, B, k, policy, log_steps, ht_bits;
+  int R, L, layer, B, k, policy, log_steps, ht_bits, cs;
 };
 
 __device__ __forceinline__ uint32_t ht_hash(int32_t p, int bits) { return ((uint32_t)p * 0x9E3779B1u) >> (32 - bits); }
@@ -74,57 +74,150 @@ __device__ __forceinline__ uint4 ld_nc_v4(const uint4* p) {
   return v;
 }
 
-// Move the m missing records host -> slots.  One work item = NV contiguous 16-byte vectors of one
-// record; ITEMS work items per thread are loaded before any of their stores.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Copy misses [q0, q1) host -> slots.  A warp moves one chunk of 32 x NV lane-contiguous 16-byte
+// vectors of one record per item (coalesced 512-byte rows); ITEMS items are loaded before any store.
 template <int NV>
-__device__ void fetch_misses(const ResolveArgs& a, int r, int m, const int32_t* miss_pos, const int32_t* victims) {
+__device__ void fetch_misses(const ResolveArgs& a, int r, int q0, int q1, const int32_t* miss_pos,
+                             const int32_t* victims) {
   constexpr int ITEMS = NV >= 8 ? 1 : 2;
-  const int64_t chunk = NV * 16;
-  const int cpr = (int)(a.rec / chunk);
-  const int total = m * cpr;
-  for (int w0 = threadIdx.x; w0 < total; w0 += ITEMS * kThreads) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int vpr = (int)(a.rec / 16);            // vectors per record
+  const int cpr = (vpr + 32 * NV - 1) / (32 * NV);
+  const int total = (q1 - q0) * cpr;
+  for (int w0 = warp; w0 < total; w0 += ITEMS * kWarps) {
     uint4 v[ITEMS][NV];
+    const uint4* src[ITEMS];
     uint4* dst[ITEMS];
+    int vbase[ITEMS];
 #pragma unroll
     for (int it = 0; it < ITEMS; ++it) {
-      const int w = w0 + it * kThreads;
+      const int w = w0 + it * kWarps;
       dst[it] = nullptr;
       if (w < total) {
-        const int q = w / cpr, c = w - q * cpr;
-        const uint4* src = (const uint4*)(hs_hist_addr(a.hist_shared, a.hist_priv, a.P0, a.priv_tokens, a.rec, a.L, r,
-                                                       a.layer, miss_pos[q]) + c * chunk);
-        dst[it] = (uint4*)(a.buf + ((int64_t)r * a.B + victims[q]) * a.rec + c * chunk);
+        const int q = q0 + w / cpr, c = w % cpr;
+        src[it] = (const uint4*)hs_hist_addr(a.hist_shared, a.hist_priv, a.P0, a.priv_tokens, a.rec, a.L, r, a.layer,
+                                             miss_pos[q]);
+        dst[it] = (uint4*)(a.buf + ((int64_t)r * a.B + victims[q]) * a.rec);
+        vbase[it] = c * 32 * NV + lane;
 #pragma unroll
-        for (int u = 0; u < NV; ++u) v[it][u] = ld_nc_v4(src + u);
+        for (int u = 0; u < NV; ++u) {
+          const int vi = vbase[it] + 32 * u;
+          if (vi < vpr) v[it][u] = ld_nc_v4(src[it] + vi);
+        }
       }
     }
 #pragma unroll
     for (int it = 0; it < ITEMS; ++it) {
       if (dst[it] != nullptr) {
 #pragma unroll
-        for (int u = 0; u < NV; ++u) dst[it][u] = v[it][u];
+        for (int u = 0; u < NV; ++u) {
+          const int vi = vbase[it] + 32 * u;
+          if (vi < vpr) dst[it][vi] = v[it][u];
+        }
       }
     }
   }
 }
 
+// The m victims are the candidates with the smallest (key, slot).  Radix select over the key range
+// of the candidates (key - min, 11-bit digits from the top) finds the threshold T and how many
+// candidates with key == T (lowest slots first) complete the set.
+__device__ void select_threshold(const uint32_t* key32, const uint8_t* flag, int B, uint32_t m, uint32_t* wbuf,
+                                 uint32_t* hist, uint32_t* sel, uint32_t* T_out, uint32_t* need_out) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  __shared__ uint32_t s_lo, s_hi;
+  uint32_t lo = 0xffffffffu, hi = 0u;
+  for (int j = tid; j < B; j += kThreads) {
+    if (flag[j] & 1u) continue;
+    lo = min(lo, key32[j]);
+    hi = max(hi, key32[j]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+    hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+  }
+  if (tid == 0) {
+    s_lo = 0xffffffffu;
+    s_hi = 0u;
+  }
+  __syncthreads();
+  if (lane == 0) {
+    atomicMin(&s_lo, lo);
+    atomicMax(&s_hi, hi);
+  }
+  __syncthreads();
+  lo = s_lo;
+  hi = s_hi;
+  const uint32_t range = hi - lo;
+  int shift = range == 0u ? 0 : 32 - __clz(range);
+  uint64_t prefix = 0;
+  uint32_t need = m;
+  while (shift > 0) {
+    const int width = shift < 11 ? shift : 11;
+    shift -= width;
+    const int nb = 1 << width;
+    for (int b = tid; b < nb; b += kThreads) hist[b] = 0u;
+    __syncthreads();
+    for (int base = tid & ~31; base < B; base += kThreads) {
+      const int j = base + lane;
+      uint32_t digit = 0xffffffffu;
+      if (j < B && !(flag[j] & 1u)) {
+        const uint64_t v = (uint64_t)(key32[j] - lo);
+        if ((v >> (shift + width)) == prefix) digit = (uint32_t)(v >> shift) & (uint32_t)(nb - 1);
+      }
+      const uint32_t peers = __match_any_sync(0xffffffffu, digit);
+      if (digit != 0xffffffffu && lane == __ffs(peers) - 1) atomicAdd(&hist[digit], (uint32_t)__popc(peers));
+    }
+    __syncthreads();
+    // bins [2 tid, 2 tid + 1]: find the bin where the running count reaches `need`
+    const int b0 = 2 * tid;
+    const uint32_t c0 = b0 < nb ? hist[b0] : 0u, c1 = b0 + 1 < nb ? hist[b0 + 1] : 0u;
+    uint32_t tot;
+    const uint32_t excl = cta_exclusive_scan(c0 + c1, wbuf, &tot);
+    if (excl < need && need <= excl + c0 + c1) {
+      if (need <= excl + c0) {
+        sel[0] = (uint32_t)b0;
+        sel[1] = need - excl;
+      } else {
+        sel[0] = (uint32_t)b0 + 1;
+        sel[1] = need - excl - c0;
+      }
+    }
+    __syncthreads();
+    prefix = (prefix << width) | sel[0];
+    need = sel[1];
+    __syncthreads();
+  }
+  *T_out = lo + (uint32_t)prefix;
+  *need_out = need;
+}
+
 template <int NV>
 __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
-  const int r = blockIdx.x;
+  const int r = blockIdx.x / a.cs;
+  const int crank = blockIdx.x % a.cs;  // rank inside the cluster of this request
   const int tid = threadIdx.x;
   const int k = a.k, B = a.B;
   const int ht_size = 1 << a.ht_bits;
   int32_t* ht_key = (int32_t*)smem;                 // [ht_size]
   int32_t* ht_val = ht_key + ht_size;               // [ht_size] smallest top-k index of the key
   int32_t* hit_slot = ht_val + ht_size;             // [k]: slot of a hit, -1 miss, -2 invalid
-  int32_t* miss_idx = hit_slot + k;                 // [k]: top-k index of the q-th miss
+  int32_t* erank = hit_slot + k;                    // [k]: rank of a hit among hits
+  int32_t* miss_idx = erank + k;                    // [k]: top-k index of the q-th miss
   int32_t* miss_pos = miss_idx + k;                 // [k]: position of the q-th miss
   int32_t* victims = miss_pos + k;                  // [k]: q-th victim slot (ascending)
-  uint8_t* slot_hit = (uint8_t*)(victims + k);      // [B]
+  uint32_t* key32 = (uint32_t*)(victims + k);       // [B]: eviction key
+  uint8_t* flag = (uint8_t*)(key32 + B);            // [B]: bit 0 hit, bit 1 victim
   __shared__ uint32_t wbuf[kWarps];
-  __shared__ uint32_t hist[256];
-  __shared__ uint32_t sel_digit, sel_need, err_bits;
+  __shared__ uint32_t hist[2048];
+  __shared__ uint32_t sel[2];
+  __shared__ uint32_t err_bits;
 
   const int32_t* topk = a.topk + (int64_t)r * k;
   int32_t* locs = a.locs + (int64_t)r * k;
@@ -133,12 +226,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
   const hs_rl_state st = a.state[r];
   const uint32_t clock = st.clock;
 
+  // ---------------- phase A: every CTA of the cluster computes the whole decision ----------------
   if (tid == 0) err_bits = ((uint64_t)clock + (uint64_t)k >= 0xFFFFFFFFull) ? (uint32_t)HS_DEVERR_CLOCK : 0u;
   for (int x = tid; x < ht_size; x += kThreads) {
     ht_key[x] = -1;
     ht_val[x] = 0x7fffffff;
   }
-  for (int j = tid; j < B; j += kThreads) slot_hit[j] = 0;
   __syncthreads();
 
   // (1) hash the selected positions; a key keeps the smallest top-k index that carries it
@@ -176,25 +269,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
   }
   __syncthreads();
 
-  // (2) probe every slot
+  // (2) probe every slot; keep its eviction key
   for (int j = tid; j < B; j += kThreads) {
     const int32_t t = tag[j];
-    if (t < 0) continue;
-    uint32_t h = ht_hash(t, a.ht_bits);
-    while (true) {
-      const int32_t key = ht_key[h];
-      if (key == t) {
-        hit_slot[ht_val[h]] = j;
-        slot_hit[j] = 1;
-        break;
+    uint8_t f = 0;
+    if (t >= 0) {
+      uint32_t h = ht_hash(t, a.ht_bits);
+      while (true) {
+        const int32_t key = ht_key[h];
+        if (key == t) {
+          hit_slot[ht_val[h]] = j;
+          f = 1;
+          break;
+        }
+        if (key == -1) break;
+        h = (h + 1) & (uint32_t)(ht_size - 1);
       }
-      if (key == -1) break;
-      h = (h + 1) & (uint32_t)(ht_size - 1);
     }
+    flag[j] = f;
+    key32[j] = hs_evict_key(a.policy, t, stamp[j], a.seed, st.nres, a.R, r, a.L, a.layer, B, j);
   }
   __syncthreads();
 
-  // (3a) rank hits and misses in top-k order; stamp hits; list misses
+  // (3a) rank hits and misses in top-k order; list the misses
   const int kpt = (k + kThreads - 1) / kThreads;
   const int i0 = min(k, tid * kpt), i1 = min(k, i0 + kpt);
   uint32_t local = 0;
@@ -203,142 +300,107 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
     local += hs >= 0 ? 1u : (hs == -1 ? 0x10000u : 0u);
   }
   uint32_t tot;
-  uint32_t pre = cta_exclusive_scan(local, wbuf, &tot);
+  const uint32_t pre = cta_exclusive_scan(local, wbuf, &tot);
   const int h = (int)(tot & 0xffffu), m = (int)(tot >> 16);
   {
     uint32_t a_rank = pre & 0xffffu, q_rank = pre >> 16;
     for (int i = i0; i < i1; ++i) {
       const int32_t hs = hit_slot[i];
       if (hs >= 0) {
-        if (a.policy != HS_POLICY_FIFO) stamp[hs] = clock + a_rank;
-        locs[i] = hs;
-        ++a_rank;
+        erank[i] = (int32_t)a_rank++;
       } else if (hs == -1) {
         miss_idx[q_rank] = i;
         miss_pos[q_rank] = topk[i];
         ++q_rank;
-      } else {
-        locs[i] = -1;
       }
     }
   }
 
-  // (3b) victims: the m candidates with the smallest (key, slot)
+  // (3b) threshold of the m smallest candidate keys
   const int ncand = B - h;
   const bool take_all = (m == ncand);
   uint32_t T = 0u, need_eq = 0u;
-  if (m > 0 && !take_all) {
-    uint32_t prefix = 0u, mask = 0u, need = (uint32_t)m;
-    for (int pass = 0; pass < 4; ++pass) {
-      const int shift = 24 - 8 * pass;
-      if (tid < 256) hist[tid] = 0u;
-      __syncthreads();
-      for (int j = tid; j < B; j += kThreads) {
-        if (slot_hit[j]) continue;
-        const uint32_t key = hs_evict_key(a.policy, tag[j], stamp[j], a.seed, st.nres, a.R, r, a.L, a.layer, B, j);
-        if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
-      }
-      __syncthreads();
-      if (tid < 32) {
-        uint32_t s = 0;
-#pragma unroll
-        for (int b = 0; b < 8; ++b) s += hist[tid * 8 + b];
-        uint32_t c = s;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          uint32_t y = __shfl_up_sync(0xffffffffu, c, o);
-          if (tid >= o) c += y;
-        }
-        const uint32_t excl = c - s;
-        if (excl < need && need <= c) {
-          uint32_t run = excl;
-          for (int b = 0; b < 8; ++b) {
-            const uint32_t hb = hist[tid * 8 + b];
-            if (run + hb >= need) {
-              sel_digit = (uint32_t)(tid * 8 + b);
-              sel_need = need - run;
-              break;
-            }
-            run += hb;
-          }
-        }
-      }
-      __syncthreads();
-      prefix |= sel_digit << shift;
-      mask |= 255u << shift;
-      need = sel_need;
-      __syncthreads();
-    }
-    T = prefix;
-    need_eq = need;
-  }
+  if (m > 0 && !take_all) select_threshold(key32, flag, B, (uint32_t)m, wbuf, hist, sel, &T, &need_eq);
 
-  // (3c) ordered compaction of the victims (ascending slot) and install the misses
+  // (3c) ordered compaction: the q-th victim in ascending slot order
   if (m > 0) {
     const int bpt = (B + kThreads - 1) / kThreads;
     const int j0 = min(B, tid * bpt), j1 = min(B, j0 + bpt);
     uint32_t cnt = 0;
     for (int j = j0; j < j1; ++j) {
-      if (slot_hit[j]) continue;
+      if (flag[j] & 1u) continue;
       if (take_all) {
         cnt += 1u;
       } else {
-        const uint32_t key = hs_evict_key(a.policy, tag[j], stamp[j], a.seed, st.nres, a.R, r, a.L, a.layer, B, j);
+        const uint32_t key = key32[j];
         cnt += key < T ? 1u : (key == T ? 0x10000u : 0u);
       }
     }
     uint32_t tot2;
     const uint32_t pre2 = cta_exclusive_scan(cnt, wbuf, &tot2);
     uint32_t less_b = pre2 & 0xffffu, eq_b = pre2 >> 16;
-    // keys are read before any write of this phase: every slot is owned by one thread
     for (int j = j0; j < j1; ++j) {
-      if (slot_hit[j]) continue;
-      bool victim;
-      uint32_t q;
+      if (flag[j] & 1u) continue;
+      int q = -1;
       if (take_all) {
-        victim = true;
-        q = less_b++;
+        q = (int)less_b++;
       } else {
-        const uint32_t key = hs_evict_key(a.policy, tag[j], stamp[j], a.seed, st.nres, a.R, r, a.L, a.layer, B, j);
+        const uint32_t key = key32[j];
         if (key < T) {
-          victim = true;
-          q = less_b + min(eq_b, need_eq);
+          q = (int)(less_b + min(eq_b, need_eq));
           ++less_b;
         } else if (key == T) {
-          victim = eq_b < need_eq;
-          q = less_b + eq_b;
+          if (eq_b < need_eq) q = (int)(less_b + eq_b);
           ++eq_b;
-        } else {
-          victim = false;
-          q = 0;
         }
       }
-      if (victim) {
-        const int i = miss_idx[q];
-        tag[j] = miss_pos[q];
-        stamp[j] = a.policy == HS_POLICY_FIFO ? clock + q : clock + (uint32_t)h + q;
-        locs[i] = j;
+      if (q >= 0) {
         victims[q] = j;
-      } else if (a.policy == HS_POLICY_SWAP_VANILLA) {
-        tag[j] = -1;
-        stamp[j] = 0u;
-      }
-    }
-  } else if (a.policy == HS_POLICY_SWAP_VANILLA) {
-    for (int j = tid; j < B; j += kThreads) {
-      if (!slot_hit[j]) {
-        tag[j] = -1;
-        stamp[j] = 0u;
+        flag[j] |= 2u;
       }
     }
   }
-  __syncthreads();
+  // every CTA of the request has read the old tags and stamps before anyone writes them
+  if (a.cs > 1) {
+    cluster_sync_all();
+  } else {
+    __syncthreads();
+  }
 
-  // (4) fetch the misses from the host history
-  if (m > 0) fetch_misses<NV>(a, r, m, miss_pos, victims);
+  // ---------------- phase B: this CTA's share of the writes and of the fetch ----------------
+  {
+    const int e0 = (int)((int64_t)k * crank / a.cs), e1 = (int)((int64_t)k * (crank + 1) / a.cs);
+    for (int i = e0 + tid; i < e1; i += kThreads) {
+      const int32_t hs = hit_slot[i];
+      if (hs >= 0) {
+        if (a.policy != HS_POLICY_FIFO) stamp[hs] = clock + (uint32_t)erank[i];
+        locs[i] = hs;
+      } else if (hs == -2) {
+        locs[i] = -1;
+      }
+    }
+    const int q0 = (int)((int64_t)m * crank / a.cs), q1 = (int)((int64_t)m * (crank + 1) / a.cs);
+    for (int q = q0 + tid; q < q1; q += kThreads) {
+      const int j = victims[q];
+      tag[j] = miss_pos[q];
+      stamp[j] = a.policy == HS_POLICY_FIFO ? clock + (uint32_t)q : clock + (uint32_t)h + (uint32_t)q;
+      locs[miss_idx[q]] = j;
+    }
+    if (a.policy == HS_POLICY_SWAP_VANILLA) {
+      const int s0 = (int)((int64_t)B * crank / a.cs), s1 = (int)((int64_t)B * (crank + 1) / a.cs);
+      for (int j = s0 + tid; j < s1; j += kThreads) {
+        if (flag[j] == 0u) {
+          tag[j] = -1;
+          stamp[j] = 0u;
+        }
+      }
+    }
+    // (4) fetch this CTA's share of the misses from the host history
+    if (q1 > q0) fetch_misses<NV>(a, r, q0, q1, miss_pos, victims);
+  }
 
   // (5) clock and counters
-  if (tid == 0) {
+  if (crank == 0 && tid == 0) {
     hs_rl_state ns = st;
     ns.clock = clock + (uint32_t)k;
     ns.nres = st.nres + 1u;
@@ -444,8 +506,62 @@ int ht_bits_for(int k) {
 
 size_t hs_resolve_smem_bytes(const hs_config* c) {
   const size_t ht = (size_t)1 << ht_bits_for(c->top_k);
-  return ht * 8 + (size_t)c->top_k * 16 + (size_t)c->buffer_slots;
+  return ht * 8 + (size_t)c->top_k * 24 + (size_t)c->buffer_slots * 5;
 }
+
+namespace {
+
+template <int NV>
+cudaError_t launch_resolve_nv(const ResolveArgs* a, int R, int cs, size_t smem, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(R * cs), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_resolve<NV>, *a);
+}
+
+template <int NV>
+int prepare_nv(const hs_config* c, int num_sms, int* cs_out) {
+  const int smem = (int)hs_resolve_smem_bytes(c);
+  if (cudaFuncSetAttribute(k_resolve<NV>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return HS_ERR_CUDA;
+  // largest cluster (<= 8 CTAs per request) that lets every request's cluster be resident at once
+  *cs_out = 1;
+  for (int cs = 8; cs >= 2; cs /= 2) {
+    if (cs * c->num_requests > num_sms) continue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(c->num_requests * cs), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, k_resolve<NV>, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      continue;
+    }
+    if (n >= c->num_requests) {
+      *cs_out = cs;
+      break;
+    }
+  }
+  return HS_OK;
+}
+
+}  // namespace
 
 int hs_launch_resolve(hs_pool* p, int layer, const int32_t* d_topk, int32_t* d_locs, cudaStream_t st) {
   const hs_config& c = p->cfg;
@@ -474,27 +590,27 @@ int hs_launch_resolve(hs_pool* p, int layer, const int32_t* d_topk, int32_t* d_l
   a.policy = c.policy;
   a.log_steps = c.log_steps;
   a.ht_bits = ht_bits_for(c.top_k);
+  a.cs = p->resolve_cs;
   const size_t smem = hs_resolve_smem_bytes(&c);
-  switch (c.io_chunk_bytes) {
-    case 16: k_resolve<1><<<c.num_requests, kThreads, smem, st>>>(a); break;
-    case 32: k_resolve<2><<<c.num_requests, kThreads, smem, st>>>(a); break;
-    case 64: k_resolve<4><<<c.num_requests, kThreads, smem, st>>>(a); break;
-    default: k_resolve<8><<<c.num_requests, kThreads, smem, st>>>(a); break;
-  }
-  return cudaGetLastError() == cudaSuccess ? HS_OK : HS_ERR_CUDA;
-}
-
-// Kernel attributes are set once at pool creation so that the launches stay capturable.
-int hs_resolve_prepare(const hs_config* c) {
-  const int smem = (int)hs_resolve_smem_bytes(c);
   cudaError_t e;
-  switch (c->io_chunk_bytes) {
-    case 16: e = cudaFuncSetAttribute(k_resolve<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem); break;
-    case 32: e = cudaFuncSetAttribute(k_resolve<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem); break;
-    case 64: e = cudaFuncSetAttribute(k_resolve<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem); break;
-    default: e = cudaFuncSetAttribute(k_resolve<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem); break;
+  switch (c.io_chunk_bytes) {
+    case 16: e = launch_resolve_nv<1>(&a, c.num_requests, a.cs, smem, st); break;
+    case 32: e = launch_resolve_nv<2>(&a, c.num_requests, a.cs, smem, st); break;
+    case 64: e = launch_resolve_nv<4>(&a, c.num_requests, a.cs, smem, st); break;
+    default: e = launch_resolve_nv<8>(&a, c.num_requests, a.cs, smem, st); break;
   }
   return e == cudaSuccess ? HS_OK : HS_ERR_CUDA;
+}
+
+// Kernel attributes and the cluster size are fixed once at pool creation; launches stay capturable.
+int hs_resolve_prepare(hs_pool* p) {
+  const hs_config* c = &p->cfg;
+  switch (c->io_chunk_bytes) {
+    case 16: return prepare_nv<1>(c, p->num_sms, &p->resolve_cs);
+    case 32: return prepare_nv<2>(c, p->num_sms, &p->resolve_cs);
+    case 64: return prepare_nv<4>(c, p->num_sms, &p->resolve_cs);
+    default: return prepare_nv<8>(c, p->num_sms, &p->resolve_cs);
+  }
 }
 
 int hs_launch_append(hs_pool* p, int layer, const int64_t* d_pos, const void* d_rec, cudaStream_t st) {
