@@ -110,6 +110,72 @@ __device__ __forceinline__ float reduce32_transposed(float (&v)[32], int lane) {
   return v[0];
 }
 
+// Combine the split partials of heads [h0, h0 + nh) of request r, in split order, one warp.
+// Split weights come from lanes over splits (parallel loads, warp reductions); the partial rows
+// are then accumulated with the loads of 4 splits issued together.
+template <int DV>
+__device__ __forceinline__ void combine_heads(const AttnArgs& a, int r, int h0, int nh, int lane) {
+  constexpr int DW = DV / 128;  // float4 per lane per row
+  for (int x = 0; x < nh; ++x) {
+    const int h = h0 + x;
+    float mloc = -INFINITY;
+    for (int s2 = lane; s2 < a.S; s2 += 32)
+      mloc = fmaxf(mloc, __ldcg(&a.ml[(((int64_t)r * a.S + s2) * a.Hq + h) * 2]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
+    const float M = mloc;
+    float acc[DW][4];
+#pragma unroll
+    for (int u = 0; u < DW; ++u) acc[u][0] = acc[u][1] = acc[u][2] = acc[u][3] = 0.f;
+    float den = 0.f;
+    if (M != -INFINITY) {
+      for (int c0 = 0; c0 < a.S; c0 += 32) {
+        float w = 0.f, lw = 0.f;
+        const int s2 = c0 + lane;
+        if (s2 < a.S) {
+          const int64_t ph = ((int64_t)r * a.S + s2) * a.Hq + h;
+          const float ms = __ldcg(&a.ml[ph * 2]);
+          w = ms == -INFINITY ? 0.f : exp2f(ms - M);
+          lw = w * __ldcg(&a.ml[ph * 2 + 1]);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o);
+        den += lw;
+        const int ns = min(32, a.S - c0);
+        for (int b0 = 0; b0 < ns; b0 += 4) {
+          float4 v[4][DW];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if (b0 + j < ns) {
+              const float4* po = (const float4*)(a.part + (((int64_t)r * a.S + c0 + b0 + j) * a.Hq + h) * DV);
+#pragma unroll
+              for (int u = 0; u < DW; ++u) v[j][u] = __ldcg(&po[lane + 32 * u]);
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float wj = __shfl_sync(0xffffffffu, w, (b0 + j) & 31);
+            if (b0 + j < ns) {
+#pragma unroll
+              for (int u = 0; u < DW; ++u) {
+                acc[u][0] = fmaf(wj, v[j][u].x, acc[u][0]);
+                acc[u][1] = fmaf(wj, v[j][u].y, acc[u][1]);
+                acc[u][2] = fmaf(wj, v[j][u].z, acc[u][2]);
+                acc[u][3] = fmaf(wj, v[j][u].w, acc[u][3]);
+              }
+            }
+          }
+        }
+      }
+    }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    float4* out = (float4*)(a.out + ((int64_t)r * a.Hq + h) * DV);
+#pragma unroll
+    for (int u = 0; u < DW; ++u)
+      out[lane + 32 * u] = make_float4(acc[u][0] * inv, acc[u][1] * inv, acc[u][2] * inv, acc[u][3] * inv);
+  }
+}
+
 template <int DK, int DV, int G, int NW>
 struct AttnCfg {
   static constexpr int T = 32 / G;      // tokens per stage
@@ -317,38 +383,7 @@ __global__ void __launch_bounds__(AttnCfg<DK, DV, G, NW>::THREADS) k_attn_cc(Att
   __syncthreads();
   if (!is_last) return;
   __threadfence();
-  if (warp < NW) {
-    const int hbase = g * G;
-#pragma unroll 1
-    for (int x = 0; x < G; ++x) {
-      const int h = hbase + x;
-      float M = -INFINITY;
-      for (int s2 = 0; s2 < a.S; ++s2) M = fmaxf(M, __ldcg(&a.ml[(((int64_t)r * a.S + s2) * a.Hq + h) * 2]));
-      float acc[DVW][2];
-#pragma unroll
-      for (int u = 0; u < DVW; ++u) acc[u][0] = acc[u][1] = 0.f;
-      float den = 0.f;
-      if (M != -INFINITY) {
-        for (int s2 = 0; s2 < a.S; ++s2) {
-          const int64_t ph = ((int64_t)r * a.S + s2) * a.Hq + h;
-          const float ms = __ldcg(&a.ml[ph * 2]);
-          const float w = ms == -INFINITY ? 0.f : exp2f(ms - M);
-          den += w * __ldcg(&a.ml[ph * 2 + 1]);
-          const float2* po = (const float2*)(a.part + ph * DV);
-#pragma unroll
-          for (int u = 0; u < DVW; ++u) {
-            const float2 v = __ldcg(&po[lane + 32 * u]);
-            acc[u][0] = fmaf(w, v.x, acc[u][0]);
-            acc[u][1] = fmaf(w, v.y, acc[u][1]);
-          }
-        }
-      }
-      const float inv = den > 0.f ? 1.f / den : 0.f;
-      float2* out = (float2*)(a.out + ((int64_t)r * a.Hq + h) * DV);
-#pragma unroll
-      for (int u = 0; u < DVW; ++u) out[lane + 32 * u] = make_float2(acc[u][0] * inv, acc[u][1] * inv);
-    }
-  }
+  if (warp < NW) combine_heads<DV>(a, r, g * G, G, lane);
   if (threadIdx.x == 0) a.ticket[(int64_t)r * a.groups + grp] = 0u;
 }
 
@@ -431,48 +466,50 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) k_attn_gqa_mma(AttnArgs a) {
   float m_run = -INFINITY, l_run = 0.f;
 
   if (warp == NW) {
-    if (lane == 0) {
-      uint32_t bad = 0u;
-      int issued = 0;
-      for (int st = 0; st < nst; ++st) {
-        const int b = st % NSTAGE;
-        if (st >= NSTAGE) {
-          if (!mbar_wait_bounded(&empty_bar[b], (uint32_t)((st / NSTAGE - 1) & 1), &abort_flag)) {
+    // producer warp: the chunk's slot list is staged in shared memory once (one coalesced read),
+    // then per stage 16 lanes validate their token and issue its bulk copy in parallel
+    int32_t* s_locs = (int32_t*)(smem + (size_t)NSTAGE * T * rs);
+    const int n = t1 - t0;
+    for (int x = lane; x < n; x += 32) s_locs[x] = locs[t0 + x];
+    __syncwarp();
+    uint32_t bad = 0u;
+    int issued = 0;
+    for (int st = 0; st < nst; ++st) {
+      const int b = st % NSTAGE;
+      if (st >= NSTAGE) {
+        bool ok = true;
+        if (lane == 0) ok = mbar_wait_bounded(&empty_bar[b], (uint32_t)((st / NSTAGE - 1) & 1), &abort_flag);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) {
+          if (lane == 0) {
             *(volatile uint32_t*)&abort_flag = 1u;
             atomicOr(a.err, (uint32_t)HS_DEVERR_TIMEOUT);
-            break;
           }
+          break;
         }
-        uint32_t mask = 0u, nvalid = 0u;
-        for (int j = 0; j < T; ++j) {
-          const int idx = t0 + st * T + j;
-          int32_t loc = idx < t1 ? locs[idx] : -1;
-          if (loc < -1 || (int64_t)loc >= a.rows) {
-            bad = 1u;
-            loc = -1;
-          }
-          if (loc >= 0) {
-            mask |= 1u << j;
-            ++nvalid;
-          }
-        }
-        tok_mask[b] = mask;
-        mbar_arrive_expect_tx(&full_bar[b], nvalid * (uint32_t)rec);
-        uint8_t* dst = smem + (size_t)b * T * rs;
-        for (int j = 0; j < T; ++j) {
-          if ((mask >> j) & 1u) {
-            const int32_t loc = locs[t0 + st * T + j];
-            bulk_g2s(dst + (size_t)j * rs, a.kv + ((int64_t)r * a.rows + loc) * rec, (uint32_t)rec, &full_bar[b]);
-          }
-        }
-        issued = st + 1;
       }
-      if (bad) atomicOr(a.err, (uint32_t)HS_DEVERR_LOC);
-      if (abort_flag) {
-        for (int st = max(0, issued - NSTAGE); st < issued; ++st) {
-          volatile uint32_t never = 0u;
-          mbar_wait_bounded(&full_bar[st % NSTAGE], (uint32_t)((st / NSTAGE) & 1), &never);
-        }
+      const int j = lane;
+      const int x = st * T + j;
+      int32_t loc = (j < T && x < n) ? s_locs[x] : -1;
+      if (loc < -1 || (int64_t)loc >= a.rows) {
+        bad = 1u;
+        loc = -1;
+      }
+      const uint32_t mask = __ballot_sync(0xffffffffu, loc >= 0);
+      if (lane == 0) {
+        tok_mask[b] = mask;
+        mbar_arrive_expect_tx(&full_bar[b], (uint32_t)__popc(mask) * (uint32_t)rec);
+      }
+      __syncwarp();
+      if (loc >= 0)
+        bulk_g2s(smem + ((size_t)b * T + j) * rs, a.kv + ((int64_t)r * a.rows + loc) * rec, (uint32_t)rec, &full_bar[b]);
+      issued = st + 1;
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(a.err, (uint32_t)HS_DEVERR_LOC);
+    if (abort_flag && lane == 0) {
+      for (int st = max(0, issued - NSTAGE); st < issued; ++st) {
+        volatile uint32_t never = 0u;
+        mbar_wait_bounded(&full_bar[st % NSTAGE], (uint32_t)((st / NSTAGE) & 1), &never);
       }
     }
   } else {
@@ -593,35 +630,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) k_attn_gqa_mma(AttnArgs a) {
   __syncthreads();
   if (!is_last) return;
   __threadfence();
-  if (warp < NW) {
-#pragma unroll 1
-    for (int x = 0; x < G; ++x) {
-      const int h = g * G + x;
-      float M = -INFINITY;
-      for (int s2 = 0; s2 < a.S; ++s2) M = fmaxf(M, __ldcg(&a.ml[(((int64_t)r * a.S + s2) * a.Hq + h) * 2]));
-      float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-      float den = 0.f;
-      if (M != -INFINITY) {
-        for (int s2 = 0; s2 < a.S; ++s2) {
-          const int64_t ph = ((int64_t)r * a.S + s2) * a.Hq + h;
-          const float ms = __ldcg(&a.ml[ph * 2]);
-          const float w = ms == -INFINITY ? 0.f : exp2f(ms - M);
-          den += w * __ldcg(&a.ml[ph * 2 + 1]);
-          const float2* po = (const float2*)(a.part + ph * D);
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const float2 v = __ldcg(&po[lane + 32 * u]);
-            acc[u][0] = fmaf(w, v.x, acc[u][0]);
-            acc[u][1] = fmaf(w, v.y, acc[u][1]);
-          }
-        }
-      }
-      const float inv = den > 0.f ? 1.f / den : 0.f;
-      float2* out = (float2*)(a.out + ((int64_t)r * a.Hq + h) * D);
-#pragma unroll
-      for (int u = 0; u < 2; ++u) out[lane + 32 * u] = make_float2(acc[u][0] * inv, acc[u][1] * inv);
-    }
-  }
+  if (warp < NW) combine_heads<D>(a, r, g * G, G, lane);
   if (threadIdx.x == 0) a.ticket[(int64_t)r * a.groups + grp] = 0u;
 }
 
@@ -653,7 +662,7 @@ bool plan_for(const hs_config* c, int num_sms, Plan* pl) {
     pl->G = G;
     pl->groups = c->num_kv_heads / NW;
     pl->T = kMmaTile;
-    pl->smem = (size_t)kMmaStages * kMmaTile * (size_t)(rec + 16);
+    pl->smem = (size_t)kMmaStages * kMmaTile * (size_t)(rec + 16);  // + the chunk's slot list, below
     per_cta_wave = 1;  // one CTA per SM: the ring holds most of the shared memory
   } else {
     if (c->head_dim_qk != 576 || c->head_dim_v != 512) return false;
@@ -666,7 +675,6 @@ bool plan_for(const hs_config* c, int num_sms, Plan* pl) {
     pl->smem = (size_t)kStages * pl->T * (size_t)rec;
     per_cta_wave = 2;
   }
-  if (pl->smem > 200 * 1024) return false;
   const int per_split = c->num_requests * pl->groups;
   int S = per_cta_wave * num_sms / per_split;
   const int max_s = (c->top_k + pl->T - 1) / pl->T;
@@ -675,7 +683,8 @@ bool plan_for(const hs_config* c, int num_sms, Plan* pl) {
   chunk = (chunk + pl->T - 1) / pl->T * pl->T;
   pl->chunk = chunk;
   pl->S = (c->top_k + chunk - 1) / chunk;
-  return true;
+  if (pl->kind == 1) pl->smem += (size_t)chunk * 4;
+  return pl->smem <= 220 * 1024;
 }
 
 template <typename K>
