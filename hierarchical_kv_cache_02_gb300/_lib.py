@@ -9,8 +9,9 @@ from . import build as _build
 
 HS_OK, HS_ERR_CONFIG, HS_ERR_ALLOC_HOST, HS_ERR_ALLOC_DEV, HS_ERR_ARG, HS_ERR_CUDA, HS_ERR_DEVICE_FLAG = (
     0, -1, -2, -3, -4, -5, -6)
+HS_ERR_SCRATCH = -7
 STATUS_NAMES = {0: "HS_OK", -1: "HS_ERR_CONFIG", -2: "HS_ERR_ALLOC_HOST", -3: "HS_ERR_ALLOC_DEV",
-                -4: "HS_ERR_ARG", -5: "HS_ERR_CUDA", -6: "HS_ERR_DEVICE_FLAG"}
+                -4: "HS_ERR_ARG", -5: "HS_ERR_CUDA", -6: "HS_ERR_DEVICE_FLAG", -7: "HS_ERR_SCRATCH"}
 POLICY_LRU, POLICY_FIFO, POLICY_RANDOM, POLICY_SWAP_VANILLA = 0, 1, 2, 3
 LAYOUT_MLA, LAYOUT_GQA = 0, 1
 DEVERR_RANGE, DEVERR_DUP, DEVERR_CLOCK, DEVERR_APPEND, DEVERR_LOC, DEVERR_TIMEOUT = 1, 2, 4, 8, 16, 32
@@ -18,7 +19,7 @@ DEVERR_RANGE, DEVERR_DUP, DEVERR_CLOCK, DEVERR_APPEND, DEVERR_LOC, DEVERR_TIMEOU
 # every entry point include/hisparse.h declares
 EXPORTS = ("hs_record_bytes", "hs_pool_create", "hs_pool_destroy", "hs_pool_reset", "hs_prefill_write",
            "hs_append_writethrough", "hs_resolve", "hs_sparse_attn", "hs_stats", "hs_read_state",
-           "hs_read_buffer", "hs_read_history")
+           "hs_read_buffer", "hs_read_history", "hs_sparse_attn_noalloc")
 
 
 class hs_config(ctypes.Structure):
@@ -87,6 +88,7 @@ def load(build_if_missing: bool = False):
             "hs_read_state": (I, [P, I, P, P, P]),
             "hs_read_buffer": (I, [P, I, I, P]),
             "hs_read_history": (I, [P, I, I, I64, I64, P]),
+            "hs_sparse_attn_noalloc": (I, [P, P, P, P, I64, F, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)

@@ -776,3 +776,112 @@ int hs_attn_prepare(const hs_config* c, int num_sms) {
   if (!plan_for(c, num_sms, &pl)) return HS_ERR_CONFIG;
   return dispatch(*c, nullptr, pl, 0) == cudaSuccess ? HS_OK : HS_ERR_CUDA;
 }
+
+// ---- attention without any allocation --------------------------------------------------
+//
+// For callers that may not allocate device memory at all: an inference engine whose own
+// allocator owns every byte of HBM, or a process that must not grow its footprint after start-up.
+// Their attention runs the same kernels as hs_sparse_attn, but the split partials, the combine
+// tickets and the error word live in this fixed file-scope array instead of a pool.  Every GPU
+// that loads the library holds it until the process exits.
+
+#include <mutex>
+
+namespace {
+
+constexpr size_t kNoAllocTicketBytes = 64 * 1024;                            // up to 16384 tickets
+constexpr size_t kNoAllocPartBytes = (size_t)HS_NOALLOC_SCRATCH_BYTES - kNoAllocTicketBytes;
+static __device__ __align__(256) unsigned char hs_noalloc_scratch[HS_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices];  // device address of hs_noalloc_scratch on each device
+int g_noalloc_sms[kMaxDevices];
+
+// Once per device, with that device current: the scratch's device address (host code only has a
+// stand-in symbol) and the kernels' shared-memory limits are fixed here.
+int noalloc_setup(int dev, const hs_config* c, void** ptr, int* sms) {
+  if (dev < 0 || dev >= kMaxDevices) return HS_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, hs_noalloc_scratch) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return HS_ERR_CUDA;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) {
+      cudaGetLastError();
+      return HS_ERR_CUDA;
+    }
+    g_noalloc_ptr[dev] = p;
+    g_noalloc_sms[dev] = n;
+  }
+  *ptr = g_noalloc_ptr[dev];
+  *sms = g_noalloc_sms[dev];
+  // the kernel for this configuration may not have had its shared-memory limit raised yet
+  return hs_attn_prepare(c, *sms);
+}
+
+}  // namespace
+
+extern "C" int hs_sparse_attn_noalloc(const hs_config* cfg, const void* d_q, const int32_t* d_locs,
+                                      const void* d_kv, int64_t kv_rows, float scale, float* d_out, void* stream) {
+  if (cfg == nullptr || d_q == nullptr || d_locs == nullptr || d_kv == nullptr || d_out == nullptr) return HS_ERR_ARG;
+  if (kv_rows < 1 || kv_rows > (int64_t)INT32_MAX || ((uintptr_t)d_kv & 15u) != 0) return HS_ERR_ARG;
+  if (cfg->num_requests < 1 || cfg->top_k < 1 || cfg->num_q_heads < 1 || cfg->num_kv_heads < 1 ||
+      cfg->num_q_heads % cfg->num_kv_heads != 0)
+    return HS_ERR_CONFIG;
+  if (cfg->layout == HS_LAYOUT_MLA && cfg->num_kv_heads != 1) return HS_ERR_CONFIG;
+  if (!hs_attn_supported(cfg)) return HS_ERR_CONFIG;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return HS_ERR_CUDA;
+  }
+  void* scratch = nullptr;
+  int sms = 0;
+  int rc = noalloc_setup(dev, cfg, &scratch, &sms);
+  if (rc != HS_OK) return rc;
+  Plan pl;
+  if (!plan_for(cfg, sms, &pl)) return HS_ERR_CONFIG;
+  const size_t part_floats = (size_t)cfg->num_requests * pl.S * cfg->num_q_heads * ((size_t)cfg->head_dim_v + 2);
+  const size_t tickets = (size_t)cfg->num_requests * pl.groups;
+  if (part_floats * sizeof(float) > kNoAllocPartBytes || (tickets + 1) * sizeof(uint32_t) > kNoAllocTicketBytes)
+    return HS_ERR_SCRATCH;
+  uint8_t* base = (uint8_t*)scratch;
+  uint32_t* ticket = (uint32_t*)base;  // [tickets] then the error word
+  float* part = (float*)(base + kNoAllocTicketBytes);
+  cudaStream_t st = (cudaStream_t)stream;
+  // tickets must start at zero; a call that timed out on the device may have left them raised
+  if (cudaMemsetAsync(ticket, 0, (tickets + 1) * sizeof(uint32_t), st) != cudaSuccess) {
+    cudaGetLastError();
+    return HS_ERR_CUDA;
+  }
+  AttnArgs a;
+  a.q = (const uint16_t*)d_q;
+  a.locs = d_locs;
+  a.kv = (const uint8_t*)d_kv;
+  a.rows = kv_rows;
+  a.out = d_out;
+  a.part = part;
+  a.ml = part + (size_t)cfg->num_requests * pl.S * cfg->num_q_heads * cfg->head_dim_v;
+  a.ticket = ticket;
+  a.err = ticket + tickets;
+  a.rec = hs_record_bytes(cfg);
+  if (cfg->layout == HS_LAYOUT_GQA) {
+    a.kstride = 2 * (int64_t)(cfg->head_dim_qk + cfg->head_dim_v);
+    a.vdelta = 2 * (int64_t)cfg->head_dim_qk;
+  } else {
+    a.kstride = 0;
+    a.vdelta = 0;
+  }
+  a.qscale = scale * kLog2e;
+  a.R = cfg->num_requests;
+  a.Hq = cfg->num_q_heads;
+  a.k = cfg->top_k;
+  a.S = pl.S;
+  a.chunk = pl.chunk;
+  a.groups = pl.groups;
+  return dispatch(*cfg, &a, pl, st) == cudaSuccess ? HS_OK : HS_ERR_CUDA;
+}

@@ -45,7 +45,8 @@ enum hs_status {
   HS_ERR_ALLOC_DEV = -3,   /* device allocation failed */
   HS_ERR_ARG = -4,         /* a call argument is out of range or NULL */
   HS_ERR_CUDA = -5,        /* a CUDA runtime call failed */
-  HS_ERR_DEVICE_FLAG = -6  /* hs_stats: a kernel recorded an error bit */
+  HS_ERR_DEVICE_FLAG = -6, /* hs_stats: a kernel recorded an error bit */
+  HS_ERR_SCRATCH = -7      /* hs_sparse_attn_noalloc: the call needs more than its fixed scratch */
 };
 
 enum hs_policy {
@@ -157,6 +158,37 @@ int hs_resolve(hs_pool* pool, int layer, const int32_t* d_topk, int32_t* d_locs,
  */
 int hs_sparse_attn(hs_pool* pool, int layer, const void* d_q, const int32_t* d_locs, const void* kv_base,
                    int64_t kv_rows, float scale, float* d_out, void* stream);
+
+/* Size of the fixed device scratch that hs_sparse_attn_noalloc uses on every GPU (8 MiB + 64 KiB). */
+#define HS_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u + 64u * 1024u)
+
+/*
+ * Sparse attention over caller-resident KV that allocates nothing.  The paper has no counterpart:
+ * this is a convenience of this library for callers that must not call cudaMalloc at all, for
+ * example code inside an inference engine whose own allocator owns all device memory, or a
+ * process that must keep its device footprint fixed after start-up.  Creating a pool would
+ * allocate the host history and the hot buffers; this call needs none of that.
+ *
+ * It computes exactly what hs_sparse_attn computes with a non-NULL kv_base, with the same
+ * kernels: for request r and query head h, softmax(scale * <q, K(row)>)-weighted V over the rows
+ * d_locs[r][i] >= 0 of d_kv, in top-k order.  Only these fields of *cfg are read: num_requests,
+ * layout, num_q_heads, num_kv_heads, head_dim_qk, head_dim_v, top_k.
+ *   d_q    : bf16 [R][Hq][head_dim_qk], device          d_locs : int32 [R][k], device
+ *   d_kv   : bf16 [R][kv_rows][record], device, 16-byte aligned
+ *   d_out  : fp32 [R][Hq][head_dim_v], device
+ * The split partials live in one file-scope device array of HS_NOALLOC_SCRATCH_BYTES per GPU,
+ * loaded with the library and held until the process exits.  A shape whose partials do not fit
+ * returns HS_ERR_SCRATCH before anything is enqueued (about R * splits * Hq * (head_dim_v + 2) * 4
+ * bytes; splits <= number of SMs / R).  Each call clears the combine tickets it uses.
+ * The first call on a device (with that device current) looks up the scratch's device address
+ * and raises the kernels' shared-memory limits; make that first call before any stream capture.
+ * Every call on a device shares the one array and finds the previous call's leftovers there:
+ * calls that may overlap on the GPU (different streams without ordering) race and corrupt each
+ * other's results.  Rows outside [0, kv_rows) are skipped; this entry point does not report them.
+ * Errors: HS_ERR_ARG, HS_ERR_CONFIG, HS_ERR_SCRATCH, HS_ERR_CUDA.
+ */
+int hs_sparse_attn_noalloc(const hs_config* cfg, const void* d_q, const int32_t* d_locs, const void* d_kv,
+                           int64_t kv_rows, float scale, float* d_out, void* stream);
 
 typedef struct {
   uint64_t hits;
