@@ -176,6 +176,75 @@ __device__ __forceinline__ void combine_heads(const AttnArgs& a, int r, int h0, 
   }
 }
 
+// Combine of NH heads at once (up to 32 splits): lane s holds split s's running max and sum for
+// every head, so the weights take one round of loads; the partial rows are then read in batches of
+// up to four splits for all NH heads together.  Larger split counts use combine_heads.
+template <int DV, int NH>
+__device__ __forceinline__ void combine_heads_wide(const AttnArgs& a, int r, int h0, int lane) {
+  constexpr int DW = DV / 128;
+  constexpr int JB = NH * DW >= 8 ? 2 : 4;  // splits per batch of loads, bounded by registers
+  float m[NH], l[NH], w[NH], den[NH], acc[NH][DW][4];
+  const bool mine = lane < a.S;
+#pragma unroll
+  for (int x = 0; x < NH; ++x) {
+    const int64_t ph = ((int64_t)r * a.S + lane) * a.Hq + h0 + x;
+    m[x] = mine ? __ldcg(&a.ml[ph * 2]) : -INFINITY;
+    l[x] = mine ? __ldcg(&a.ml[ph * 2 + 1]) : 0.f;
+  }
+#pragma unroll
+  for (int x = 0; x < NH; ++x) {
+    float M = m[x];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    w[x] = (M == -INFINITY || m[x] == -INFINITY) ? 0.f : exp2f(m[x] - M);
+    float d = w[x] * l[x];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+    den[x] = d;
+#pragma unroll
+    for (int u = 0; u < DW; ++u) acc[x][u][0] = acc[x][u][1] = acc[x][u][2] = acc[x][u][3] = 0.f;
+  }
+  for (int b0 = 0; b0 < a.S; b0 += JB) {
+    float4 v[JB][NH][DW];
+#pragma unroll
+    for (int j = 0; j < JB; ++j) {
+      if (b0 + j < a.S) {
+#pragma unroll
+        for (int x = 0; x < NH; ++x) {
+          const float4* po = (const float4*)(a.part + (((int64_t)r * a.S + b0 + j) * a.Hq + h0 + x) * DV);
+#pragma unroll
+          for (int u = 0; u < DW; ++u) v[j][x][u] = __ldcg(&po[lane + 32 * u]);
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < JB; ++j) {
+      if (b0 + j < a.S) {
+#pragma unroll
+        for (int x = 0; x < NH; ++x) {
+          const float wj = __shfl_sync(0xffffffffu, w[x], b0 + j);
+#pragma unroll
+          for (int u = 0; u < DW; ++u) {
+            acc[x][u][0] = fmaf(wj, v[j][x][u].x, acc[x][u][0]);
+            acc[x][u][1] = fmaf(wj, v[j][x][u].y, acc[x][u][1]);
+            acc[x][u][2] = fmaf(wj, v[j][x][u].z, acc[x][u][2]);
+            acc[x][u][3] = fmaf(wj, v[j][x][u].w, acc[x][u][3]);
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int x = 0; x < NH; ++x) {
+    const float inv = den[x] > 0.f ? 1.f / den[x] : 0.f;
+    float4* out = (float4*)(a.out + ((int64_t)r * a.Hq + h0 + x) * DV);
+#pragma unroll
+    for (int u = 0; u < DW; ++u)
+      out[lane + 32 * u] =
+          make_float4(acc[x][u][0] * inv, acc[x][u][1] * inv, acc[x][u][2] * inv, acc[x][u][3] * inv);
+  }
+}
+
 template <int DK, int DV, int G, int NW>
 struct AttnCfg {
   static constexpr int T = 32 / G;      // tokens per stage
@@ -383,7 +452,12 @@ __global__ void __launch_bounds__(AttnCfg<DK, DV, G, NW>::THREADS) k_attn_cc(Att
   __syncthreads();
   if (!is_last) return;
   __threadfence();
-  if (warp < NW) combine_heads<DV>(a, r, g * G, G, lane);
+  if (warp < NW) {
+    if (a.S <= 32)
+      combine_heads_wide<DV, G>(a, r, g * G, lane);
+    else
+      combine_heads<DV>(a, r, g * G, G, lane);
+  }
   if (threadIdx.x == 0) a.ticket[(int64_t)r * a.groups + grp] = 0u;
 }
 
@@ -470,7 +544,19 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) k_attn_gqa_mma(AttnArgs a) {
     // then per stage 16 lanes validate their token and issue its bulk copy in parallel
     int32_t* s_locs = (int32_t*)(smem + (size_t)NSTAGE * T * rs);
     const int n = t1 - t0;
-    for (int x = lane; x < n; x += 32) s_locs[x] = locs[t0 + x];
+    for (int x0 = 0; x0 < n; x0 += 32 * 8) {  // eight loads per lane in flight before their stores
+      int32_t v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int x = x0 + 32 * u + lane;
+        v[u] = x < n ? locs[t0 + x] : -1;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int x = x0 + 32 * u + lane;
+        if (x < n) s_locs[x] = v[u];
+      }
+    }
     __syncwarp();
     uint32_t bad = 0u;
     int issued = 0;
@@ -630,7 +716,12 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) k_attn_gqa_mma(AttnArgs a) {
   __syncthreads();
   if (!is_last) return;
   __threadfence();
-  if (warp < NW) combine_heads<D>(a, r, g * G, G, lane);
+  if (warp < NW) {
+    if (a.S <= 32)
+      combine_heads_wide<D, G>(a, r, g * G, lane);
+    else
+      combine_heads<D>(a, r, g * G, G, lane);
+  }
   if (threadIdx.x == 0) a.ticket[(int64_t)r * a.groups + grp] = 0u;
 }
 
