@@ -149,7 +149,7 @@ def barrier(world):
 class Workload:
     """Seeded synthetic inputs of one replica, resident on the GPU."""
 
-    def __init__(self, w, steps, device, seed):
+    def __init__(self, w, steps, device, seed, fetch="resolve"):
         import torch
 
         from hierarchical_kv_cache_02_gb300 import HsConfig, inputs
@@ -159,7 +159,8 @@ class Workload:
         self.cfg = HsConfig(num_requests=R, num_layers=L, capacity=w["ctx0"] + steps, layout=w["layout"],
                             num_q_heads=w["Hq"], num_kv_heads=w["Hkv"], head_dim_qk=w["Dqk"], head_dim_v=w["Dv"],
                             top_k=k, buffer_slots=w["B"], policy=0, seed=seed, io_chunk_bytes=64,
-                            shared_prefix=w["ctx0"] if w["shared"] else 0)
+                            shared_prefix=w["ctx0"] if w["shared"] else 0,
+                            fetch_in_attention=1 if fetch == "attention" else 0)
         spec = inputs.TraceSpec(ctx0=w["ctx0"], k=k, steps=steps, keep=w["keep"], recency_mean=w["mu"],
                                 appends=True, burst_every=w["burst"], far_gap=int(8 * w["mu"]))
         t0 = time.time()
@@ -199,7 +200,10 @@ def run_ours(args, w, world, rank, local):
     W, K = args.warmup, args.steps
     S = W + K
     t_setup = time.time()
-    wl = Workload(w, S, device, seed=1000 + 17 * rank)
+    fetch = args.fetch
+    if fetch == "auto":
+        fetch = "attention" if w["layout"] == 1 and w["Hkv"] <= 8 else "resolve"
+    wl = Workload(w, S, device, seed=1000 + 17 * rank, fetch=fetch)
     pool = HsPool(wl.cfg, device=local)
     wl.prefill(pool)
     torch.cuda.synchronize()
@@ -272,7 +276,7 @@ def run_ours(args, w, world, rank, local):
                    "buffer_slots": w["B"], "layout": "gqa" if w["layout"] == 1 else "mla", "q_heads": w["Hq"],
                    "kv_heads": w["Hkv"], "record_bytes": rec, "policy": "lru", "keep": w["keep"],
                    "recency_mean": w["mu"], "burst_every": w["burst"], "shared_history": w["shared"],
-                   "append": True, "parallelism": f"replicas{world}",
+                   "append": True, "miss_fetch": fetch, "parallelism": f"replicas{world}",
                    "l2": "inputs larger than L2 (each attention launch gathers "
                          f"{attn_bytes_per_launch(w) / 1e6:.0f} MB; a step touches {L} layers)"},
         "us_per_layer": {"total": max_elapsed / (K * L) * 1e6, "resolve": float(res_ms.mean() * 1e3),
@@ -435,6 +439,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="gqa_b16_l32")
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling runs)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--fetch", choices=["auto", "resolve", "attention"], default="auto",
+                    help="who copies the misses host -> HBM: the resolve kernel, or the attention while it gathers")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--traffic", type=float, default=None,

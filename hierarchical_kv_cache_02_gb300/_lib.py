@@ -39,6 +39,7 @@ class hs_config(ctypes.Structure):
         ("seed", ctypes.c_uint64),
         ("io_chunk_bytes", ctypes.c_int32),
         ("log_steps", ctypes.c_int32),
+        ("fetch_in_attention", ctypes.c_int32),
     ]
 
 

@@ -36,6 +36,14 @@ struct AttnArgs {
   int64_t kstride, vdelta;  // K of KV block g at g * kstride, V at K + vdelta (bytes)
   float qscale;             // scale * log2(e)
   int R, Hq, k, S, chunk, groups;
+  // fetch-in-attention mode (hot-buffer rows only): misses still to copy from the host history
+  const int2* pend;         // [R][k] {position, slot} or {-1, -1}; null when nothing is pending
+  uint32_t* pend_live;      // [R]
+  uint8_t* buf_w;           // writable view of the rows (the hot buffer of the layer)
+  const uint8_t* hist_shared;
+  const uint8_t* hist_priv;
+  int64_t P0, priv_tokens;
+  int L, layer;
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -503,103 +511,202 @@ __device__ __forceinline__ float bf16_hi_f(uint32_t w) { return __uint_as_float(
 
 constexpr int kMmaTile = 16;  // tokens per stage
 
-template <int G, int NW, int NSTAGE>
-__global__ void __launch_bounds__((NW + 1) * 32, 1) k_attn_gqa_mma(AttnArgs a) {
+// NP > 0 (fetch-in-attention mode): rows the resolve left in the host history are copied by
+// kFetchWarps extra warps (16-byte loads through the mapped history, round-robin over the pending
+// rows) into NP dedicated pending slots, as far ahead of their use as the slots allow (each slot
+// has its own full/empty mbarriers), while the producer keeps gathering the resident rows from HBM
+// into the stage ring; the consumers read either kind of row through per-lane ldmatrix addresses
+// and write the fetched rows back to their hot-buffer slots.
+constexpr int kFetchWarps = 2;
+
+template <int NW, int NP>
+struct MmaThreads {
+  static constexpr int value = (NW + 1 + (NP > 0 ? kFetchWarps : 0)) * 32;
+};
+
+template <int G, int NW, int NSTAGE, int NP>
+__global__ void __launch_bounds__(MmaThreads<NW, NP>::value, 1) k_attn_gqa_mma(AttnArgs a) {
   constexpr int T = kMmaTile;
   constexpr int D = 128;  // head_dim_qk == head_dim_v
+  constexpr int NPB = NP > 0 ? NP : 1;
   static_assert(G >= 1 && G <= 8, "up to 8 query heads per KV head");
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full_bar[NSTAGE];
   __shared__ __align__(8) uint64_t empty_bar[NSTAGE];
+  __shared__ __align__(8) uint64_t pfull_bar[NPB];
+  __shared__ __align__(8) uint64_t pempty_bar[NPB];
   __shared__ uint32_t tok_mask[NSTAGE];
   __shared__ uint32_t abort_flag;
+  __shared__ uint32_t use_pend;
   __shared__ uint32_t is_last;
 
   const int split = blockIdx.x, r = blockIdx.y, grp = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t0 = split * a.chunk;
   const int t1 = min(a.k, t0 + a.chunk);
-  const int nst = (t1 - t0 + T - 1) / T;
+  const int n = t1 - t0;
+  const int nst = (n + T - 1) / T;
   const int64_t rec = a.rec;
   const uint32_t rs = (uint32_t)rec + 16u;  // padded row stride in shared memory
   const int32_t* locs = a.locs + (int64_t)r * a.k;
+  // shared memory: stage ring | pending slots | slot list | pending index per token | pending list
+  uint8_t* ring = smem;
+  uint8_t* parea = smem + (size_t)NSTAGE * T * rs;
+  int32_t* s_locs = (int32_t*)(parea + (size_t)NP * rs);
+  int32_t* s_pidx = s_locs + a.chunk;  // pending index of a token (order among pending rows), or -1
+  int32_t* s_ppos = s_pidx + a.chunk;  // host position of the pi-th pending row
+  int32_t* s_ptok = s_ppos + a.chunk;  // token (chunk index) of the pi-th pending row
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NSTAGE; ++s) {
       mbar_init(&full_bar[s], 1u);
       mbar_init(&empty_bar[s], (uint32_t)NW);
     }
+    for (int s = 0; s < NPB; ++s) {
+      mbar_init(&pfull_bar[s], 1u);  // the fetch warp that filled the slot
+      mbar_init(&pempty_bar[s], (uint32_t)NW);
+    }
     abort_flag = 0u;
+    use_pend = (NP > 0 && a.pend != nullptr && a.pend_live[r] != 0u) ? 1u : 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
+  const bool pend_on = use_pend != 0u;
 
   const int g = grp * NW + warp;  // KV head of this consumer warp
   const int grow = lane >> 2, tig = lane & 3;
   float o[16][4];
   float m_run = -INFINITY, l_run = 0.f;
 
+  __shared__ int s_npend;
+  __shared__ uint32_t s_bad;
   if (warp == NW) {
-    // producer warp: the chunk's slot list is staged in shared memory once (one coalesced read),
-    // then per stage 16 lanes validate their token and issue its bulk copy in parallel
-    int32_t* s_locs = (int32_t*)(smem + (size_t)NSTAGE * T * rs);
-    const int n = t1 - t0;
-    for (int x0 = 0; x0 < n; x0 += 32 * 8) {  // eight loads per lane in flight before their stores
-      int32_t v[8];
+    // slot list (and pending list) of the chunk, read once with eight loads per lane in flight
+    const int2* pend = pend_on ? a.pend + (int64_t)r * a.k : nullptr;
+    uint32_t bad = 0u;
+    int npend = 0;
+    for (int x0 = 0; x0 < n; x0 += 32 * 8) {
+      int32_t v[8], pp[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int x = x0 + 32 * u + lane;
         v[u] = x < n ? locs[t0 + x] : -1;
+        pp[u] = (pend_on && x < n) ? pend[t0 + x].x : -1;
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int x = x0 + 32 * u + lane;
-        if (x < n) s_locs[x] = v[u];
+        int32_t loc = v[u];
+        if (loc < -1 || (int64_t)loc >= a.rows) {
+          bad = 1u;
+          loc = -1;
+        }
+        const bool isp = x < n && loc >= 0 && pp[u] >= 0;
+        const uint32_t bal = __ballot_sync(0xffffffffu, isp);
+        const int pi = npend + __popc(bal & ((1u << lane) - 1u));
+        if (x < n) {
+          s_locs[x] = loc;
+          s_pidx[x] = isp ? pi : -1;
+        }
+        if (isp) {
+          s_ppos[pi] = pp[u];
+          s_ptok[pi] = x;
+        }
+        npend += __popc(bal);
       }
     }
-    __syncwarp();
-    uint32_t bad = 0u;
+    if (lane == 0) {
+      s_npend = npend;
+      s_bad = __any_sync(0xffffffffu, bad) ? 1u : 0u;
+    } else {
+      __any_sync(0xffffffffu, bad);
+    }
+  }
+  __syncthreads();  // lists are visible to every role
+  if (warp == NW) {
+    // ---------------- producer warp: resident rows, HBM -> stage ring ----------------
+    bool ok = true;
     int issued = 0;
-    for (int st = 0; st < nst; ++st) {
+    for (int st = 0; ok && st < nst; ++st) {
       const int b = st % NSTAGE;
       if (st >= NSTAGE) {
-        bool ok = true;
-        if (lane == 0) ok = mbar_wait_bounded(&empty_bar[b], (uint32_t)((st / NSTAGE - 1) & 1), &abort_flag);
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        if (!ok) {
-          if (lane == 0) {
-            *(volatile uint32_t*)&abort_flag = 1u;
-            atomicOr(a.err, (uint32_t)HS_DEVERR_TIMEOUT);
-          }
+        bool w = true;
+        if (lane == 0) w = mbar_wait_bounded(&empty_bar[b], (uint32_t)((st / NSTAGE - 1) & 1), &abort_flag);
+        if (__shfl_sync(0xffffffffu, w ? 1 : 0, 0) == 0) {
+          ok = false;
           break;
         }
       }
       const int j = lane;
       const int x = st * T + j;
-      int32_t loc = (j < T && x < n) ? s_locs[x] : -1;
-      if (loc < -1 || (int64_t)loc >= a.rows) {
-        bad = 1u;
-        loc = -1;
-      }
+      const int32_t loc = (j < T && x < n) ? s_locs[x] : -1;
+      const bool resident = loc >= 0 && (j < T && x < n) && s_pidx[x] < 0;
       const uint32_t mask = __ballot_sync(0xffffffffu, loc >= 0);
+      const uint32_t rmask = __ballot_sync(0xffffffffu, resident);
       if (lane == 0) {
         tok_mask[b] = mask;
-        mbar_arrive_expect_tx(&full_bar[b], (uint32_t)__popc(mask) * (uint32_t)rec);
+        mbar_arrive_expect_tx(&full_bar[b], (uint32_t)__popc(rmask) * (uint32_t)rec);
       }
       __syncwarp();
-      if (loc >= 0)
-        bulk_g2s(smem + ((size_t)b * T + j) * rs, a.kv + ((int64_t)r * a.rows + loc) * rec, (uint32_t)rec, &full_bar[b]);
+      if (resident)
+        bulk_g2s(ring + ((size_t)b * T + j) * rs, a.kv + ((int64_t)r * a.rows + loc) * rec, (uint32_t)rec,
+                 &full_bar[b]);
       issued = st + 1;
     }
-    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(a.err, (uint32_t)HS_DEVERR_LOC);
+    if (!ok && lane == 0) {
+      *(volatile uint32_t*)&abort_flag = 1u;
+      atomicOr(a.err, (uint32_t)HS_DEVERR_TIMEOUT);
+    }
+    if (s_bad && lane == 0) atomicOr(a.err, (uint32_t)HS_DEVERR_LOC);
     if (abort_flag && lane == 0) {
+      // let copies already issued land before the CTA can retire
       for (int st = max(0, issued - NSTAGE); st < issued; ++st) {
         volatile uint32_t never = 0u;
         mbar_wait_bounded(&full_bar[st % NSTAGE], (uint32_t)((st / NSTAGE) & 1), &never);
       }
     }
+  } else if (warp > NW) {
+    // ---------------- fetch warps: pending rows, host history -> pending slots ----------------
+    if (NP > 0 && pend_on) {
+      const int f = warp - NW - 1;
+      const int npend = s_npend;
+      const int nv = (int)(rec / 16);
+      for (int pi = f; pi < npend; pi += kFetchWarps) {
+        const int sl = pi % NPB;
+        if (pi >= NPB) {
+          // the slot's previous row has a smaller pending index: consumers can always free it
+          bool w = true;
+          if (lane == 0) w = mbar_wait_bounded(&pempty_bar[sl], (uint32_t)((pi / NPB - 1) & 1), &abort_flag);
+          if (__shfl_sync(0xffffffffu, w ? 1 : 0, 0) == 0) {
+            if (lane == 0) {
+              *(volatile uint32_t*)&abort_flag = 1u;
+              atomicOr(a.err, (uint32_t)HS_DEVERR_TIMEOUT);
+            }
+            break;
+          }
+        }
+        const uint4* src = (const uint4*)hs_hist_addr(a.hist_shared, a.hist_priv, a.P0, a.priv_tokens, rec, a.L, r,
+                                                      a.layer, s_ppos[pi]);
+        uint4* dst = (uint4*)(parea + (size_t)sl * rs);
+        for (int v0 = 0; v0 < nv; v0 += 32 * 8) {  // eight 16-byte loads per lane in flight
+          uint4 t[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int vv = v0 + 32 * u + lane;
+            if (vv < nv) t[u] = __ldg(src + vv);
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int vv = v0 + 32 * u + lane;
+            if (vv < nv) dst[vv] = t[u];
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&pfull_bar[sl]);
+      }
+    }
   } else {
-    // query fragments (A operand, rows = heads): only rows 0..G-1 are non-zero
+    // ---------------- consumer warps: one KV head, G query heads ----------------
     uint32_t qa[8][2];
     {
       const uint32_t* qw = (const uint32_t*)(a.q + ((int64_t)r * a.Hq + (int64_t)g * G + (grow < G ? grow : 0)) * D);
@@ -610,15 +717,15 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) k_attn_gqa_mma(AttnArgs a) {
       }
     }
 #pragma unroll
-    for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    for (int n2 = 0; n2 < 16; ++n2) o[n2][0] = o[n2][1] = o[n2][2] = o[n2][3] = 0.f;
     const uint32_t koff = (uint32_t)(g * a.kstride);
     const uint32_t voff = koff + (uint32_t)a.vdelta;
-    // ldmatrix row addresses: K (non-transposed) and V (transposed) patterns
-    const uint32_t k_tok = (uint32_t)((lane & 7) + ((lane >> 4) << 3));
+    // ldmatrix rows of this lane: K (non-transposed) and V (transposed) patterns
+    const int k_tok = (lane & 7) + ((lane >> 4) << 3);
     const uint32_t k_col = (uint32_t)(((lane >> 3) & 1) * 16);
-    const uint32_t v_tok = (uint32_t)((lane & 7) + (((lane >> 3) & 1) << 3));
+    const int v_tok = (lane & 7) + (((lane >> 3) & 1) << 3);
     const uint32_t v_col = (uint32_t)((lane >> 4) * 16);
-    const uint32_t sbase = smem_u32(smem);
+    const uint32_t ring_u = smem_u32(ring), parea_u = smem_u32(parea);
     for (int st = 0; st < nst; ++st) {
       const int b = st % NSTAGE;
       if (!mbar_wait_bounded(&full_bar[b], (uint32_t)((st / NSTAGE) & 1), &abort_flag)) {
@@ -627,10 +734,43 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) k_attn_gqa_mma(AttnArgs a) {
         break;
       }
       const uint32_t mask = tok_mask[b];
-      const uint32_t stage = sbase + (uint32_t)b * T * rs;
+      uint32_t kaddr = ring_u + ((uint32_t)b * T + (uint32_t)k_tok) * rs;
+      uint32_t vaddr = ring_u + ((uint32_t)b * T + (uint32_t)v_tok) * rs;
+      uint32_t pmask = 0u;
+      if (NP > 0 && pend_on) {
+        // pending rows of this stage: wait for their slots, point this lane's rows at them
+        const int xj = st * T + (lane & 15);
+        const int pj = (xj < n) ? s_pidx[xj] : -1;
+        pmask = __ballot_sync(0xffffffffu, lane < 16 && pj >= 0);
+        bool okp = true;
+        for (uint32_t pm = pmask; pm != 0u && okp; pm &= pm - 1u) {
+          const int jj = __ffs(pm) - 1;
+          const int pi = __shfl_sync(0xffffffffu, pj, jj);
+          okp = mbar_wait_bounded(&pfull_bar[pi % NPB], (uint32_t)((pi / NPB) & 1), &abort_flag);
+        }
+        if (!okp) {
+          *(volatile uint32_t*)&abort_flag = 1u;
+          atomicOr(a.err, (uint32_t)HS_DEVERR_TIMEOUT);
+          break;
+        }
+        const int xk = st * T + k_tok, xv = st * T + v_tok;
+        const int pk = xk < n ? s_pidx[xk] : -1, pv = xv < n ? s_pidx[xv] : -1;
+        if (pk >= 0) kaddr = parea_u + (uint32_t)(pk % NPB) * rs;
+        if (pv >= 0) vaddr = parea_u + (uint32_t)(pv % NPB) * rs;
+        // fetched rows go back to their hot-buffer slots: each warp writes a 1/NW share of each
+        for (uint32_t pm = pmask; pm != 0u; pm &= pm - 1u) {
+          const int jj = __ffs(pm) - 1;
+          const int pi = __shfl_sync(0xffffffffu, pj, jj);
+          const int32_t slot = s_locs[st * T + jj];
+          const uint4* srow = (const uint4*)(parea + (size_t)(pi % NPB) * rs);
+          uint4* gdst = (uint4*)(a.buf_w + ((int64_t)r * a.rows + slot) * rec);
+          for (int vv = warp * 32 + lane; vv < (int)(rec / 16); vv += NW * 32) gdst[vv] = srow[vv];
+        }
+      }
+      kaddr += koff + k_col;
+      vaddr += voff + v_col;
       // S = Q K^T for tokens 0-7 (s0) and 8-15 (s1)
       float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
-      const uint32_t kaddr = stage + k_tok * rs + koff + k_col;
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
         uint32_t b0, b1, b2, b3;
@@ -660,9 +800,9 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) k_attn_gqa_mma(AttnArgs a) {
       m_run = m_new;
       l_run = l_run * alpha + ps;
 #pragma unroll
-      for (int n = 0; n < 16; ++n) {
-        o[n][0] *= alpha;
-        o[n][1] *= alpha;
+      for (int n2 = 0; n2 < 16; ++n2) {
+        o[n2][0] *= alpha;
+        o[n2][1] *= alpha;
       }
       // P as the A operand: high bf16 part and remainder; rows >= G stay zero
       uint32_t ph0 = 0u, ph2 = 0u, pl0 = 0u, pl2 = 0u;
@@ -678,7 +818,6 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) k_attn_gqa_mma(AttnArgs a) {
         vm_lo = (((mask >> ta) & 1u) ? 0x0000ffffu : 0u) | (((mask >> (ta + 1)) & 1u) ? 0xffff0000u : 0u);
         vm_hi = (((mask >> (ta + 8)) & 1u) ? 0x0000ffffu : 0u) | (((mask >> (ta + 9)) & 1u) ? 0xffff0000u : 0u);
       }
-      const uint32_t vaddr = stage + v_tok * rs + voff + v_col;
 #pragma unroll
       for (int pr = 0; pr < 8; ++pr) {
         uint32_t b0, b1, b2, b3;
@@ -693,13 +832,21 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) k_attn_gqa_mma(AttnArgs a) {
         mma_bf16(o[2 * pr + 1], pl0, 0u, pl2, 0u, b2, b3);
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty_bar[b]);
+      if (lane == 0) {
+        mbar_arrive(&empty_bar[b]);
+        if (NP > 0) {
+          for (uint32_t pm = pmask; pm != 0u; pm &= pm - 1u) {
+            const int pi = s_pidx[st * T + __ffs(pm) - 1];
+            mbar_arrive(&pempty_bar[pi % NPB]);
+          }
+        }
+      }
     }
     if (!abort_flag && grow < G) {
       const int64_t ph = ((int64_t)r * a.S + split) * a.Hq + (int64_t)g * G + grow;
       float* po = a.part + ph * D;
 #pragma unroll
-      for (int n = 0; n < 16; ++n) *(float2*)(po + n * 8 + 2 * tig) = make_float2(o[n][0], o[n][1]);
+      for (int n2 = 0; n2 < 16; ++n2) *(float2*)(po + n2 * 8 + 2 * tig) = make_float2(o[n2][0], o[n2][1]);
       if (tig == 0) {
         a.ml[ph * 2 + 0] = m_run;
         a.ml[ph * 2 + 1] = l_run;
@@ -722,7 +869,10 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) k_attn_gqa_mma(AttnArgs a) {
     else
       combine_heads<D>(a, r, g * G, G, lane);
   }
-  if (threadIdx.x == 0) a.ticket[(int64_t)r * a.groups + grp] = 0u;
+  if (threadIdx.x == 0) {
+    a.ticket[(int64_t)r * a.groups + grp] = 0u;
+    if (use_pend) a.pend_live[r] = 0u;  // every split has written its fetched rows back
+  }
 }
 
 // ---- dispatch ----------------------------------------------------------------
@@ -730,10 +880,13 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) k_attn_gqa_mma(AttnArgs a) {
 struct Plan {
   int kind;  // 0: CUDA-core kernel (shared-latent records), 1: tensor-core GQA kernel
   int NW, G, T, groups, S, chunk;
+  int fetch;  // 1: the GQA kernel fetches pending rows from the host (2 ring stages + kPendSlots)
   size_t smem;
 };
 
 constexpr int kMmaStages = 3;
+constexpr int kMmaStagesFetch = 2;
+constexpr int kPendSlots = 16;
 
 bool plan_for(const hs_config* c, int num_sms, Plan* pl) {
   const int64_t rec = hs_record_bytes(c);
@@ -753,12 +906,15 @@ bool plan_for(const hs_config* c, int num_sms, Plan* pl) {
     pl->G = G;
     pl->groups = c->num_kv_heads / NW;
     pl->T = kMmaTile;
-    pl->smem = (size_t)kMmaStages * kMmaTile * (size_t)(rec + 16);  // + the chunk's slot list, below
+    pl->fetch = c->fetch_in_attention != 0;
+    pl->smem = pl->fetch ? (size_t)(kMmaStagesFetch * kMmaTile + kPendSlots) * (size_t)(rec + 16)
+                         : (size_t)kMmaStages * kMmaTile * (size_t)(rec + 16);  // + the chunk lists, below
     per_cta_wave = 1;  // one CTA per SM: the ring holds most of the shared memory
   } else {
     if (c->head_dim_qk != 576 || c->head_dim_v != 512) return false;
     if (c->num_q_heads % 8 != 0) return false;
     pl->kind = 0;
+    pl->fetch = 0;
     pl->NW = 8;
     pl->G = 1;
     pl->groups = c->num_q_heads / 8;
@@ -774,7 +930,7 @@ bool plan_for(const hs_config* c, int num_sms, Plan* pl) {
   chunk = (chunk + pl->T - 1) / pl->T * pl->T;
   pl->chunk = chunk;
   pl->S = (c->top_k + chunk - 1) / chunk;
-  if (pl->kind == 1) pl->smem += (size_t)chunk * 4;
+  if (pl->kind == 1) pl->smem += (size_t)chunk * 16;  // slot list, pending index, pending list
   return pl->smem <= 220 * 1024;
 }
 
@@ -787,15 +943,21 @@ cudaError_t launch_kernel(K kern, const AttnArgs* a, const Plan& pl, int threads
   return cudaGetLastError();
 }
 
-template <int G>
-cudaError_t launch_gqa_nw(const AttnArgs* a, const Plan& pl, cudaStream_t st) {
+template <int G, int NSTAGE, int NP>
+cudaError_t launch_gqa_nw2(const AttnArgs* a, const Plan& pl, cudaStream_t st) {
   switch (pl.NW) {
-    case 1: return launch_kernel(k_attn_gqa_mma<G, 1, kMmaStages>, a, pl, 2 * 32, st);
-    case 2: return launch_kernel(k_attn_gqa_mma<G, 2, kMmaStages>, a, pl, 3 * 32, st);
-    case 4: return launch_kernel(k_attn_gqa_mma<G, 4, kMmaStages>, a, pl, 5 * 32, st);
-    case 8: return launch_kernel(k_attn_gqa_mma<G, 8, kMmaStages>, a, pl, 9 * 32, st);
+    case 1: return launch_kernel(k_attn_gqa_mma<G, 1, NSTAGE, NP>, a, pl, MmaThreads<1, NP>::value, st);
+    case 2: return launch_kernel(k_attn_gqa_mma<G, 2, NSTAGE, NP>, a, pl, MmaThreads<2, NP>::value, st);
+    case 4: return launch_kernel(k_attn_gqa_mma<G, 4, NSTAGE, NP>, a, pl, MmaThreads<4, NP>::value, st);
+    case 8: return launch_kernel(k_attn_gqa_mma<G, 8, NSTAGE, NP>, a, pl, MmaThreads<8, NP>::value, st);
     default: return cudaErrorInvalidValue;
   }
+}
+
+template <int G>
+cudaError_t launch_gqa_nw(const AttnArgs* a, const Plan& pl, cudaStream_t st) {
+  return pl.fetch ? launch_gqa_nw2<G, kMmaStagesFetch, kPendSlots>(a, pl, st)
+                  : launch_gqa_nw2<G, kMmaStages, 0>(a, pl, st);
 }
 
 cudaError_t dispatch(const hs_config& c, const AttnArgs* a, const Plan& pl, cudaStream_t st) {
@@ -809,6 +971,11 @@ cudaError_t dispatch(const hs_config& c, const AttnArgs* a, const Plan& pl, cuda
 }
 
 }  // namespace
+
+bool hs_attn_can_fetch(const hs_config* c) {
+  Plan pl;
+  return plan_for(c, 152, &pl) && pl.kind == 1 && pl.groups == 1;
+}
 
 bool hs_attn_supported(const hs_config* c) {
   Plan pl;
@@ -829,7 +996,7 @@ int hs_launch_attn(hs_pool* p, int layer, const void* d_q, const int32_t* d_locs
   Plan pl;
   if (!plan_for(&c, p->num_sms, &pl)) return HS_ERR_CONFIG;
   if (kv_base != nullptr && ((uintptr_t)kv_base & 15u) != 0) return HS_ERR_ARG;
-  AttnArgs a;
+  AttnArgs a{};
   a.q = (const uint16_t*)d_q;
   a.locs = d_locs;
   if (kv_base == nullptr) {
@@ -859,6 +1026,16 @@ int hs_launch_attn(hs_pool* p, int layer, const void* d_q, const int32_t* d_locs
   a.S = pl.S;
   a.chunk = pl.chunk;
   a.groups = pl.groups;
+  const bool hot = kv_base == nullptr;
+  a.pend = (hot && p->pend != nullptr) ? p->pend + (int64_t)layer * c.num_requests * c.top_k : nullptr;
+  a.pend_live = (hot && p->pend_live != nullptr) ? p->pend_live + (int64_t)layer * c.num_requests : nullptr;
+  a.buf_w = hot ? p->buf + (int64_t)layer * c.num_requests * c.buffer_slots * p->rec : nullptr;
+  a.hist_shared = p->dmap_shared;
+  a.hist_priv = p->dmap_priv;
+  a.P0 = c.shared_prefix;
+  a.priv_tokens = p->priv_tokens;
+  a.L = c.num_layers;
+  a.layer = layer;
   return dispatch(c, &a, pl, st) == cudaSuccess ? HS_OK : HS_ERR_CUDA;
 }
 
@@ -949,7 +1126,7 @@ extern "C" int hs_sparse_attn_noalloc(const hs_config* cfg, const void* d_q, con
     cudaGetLastError();
     return HS_ERR_CUDA;
   }
-  AttnArgs a;
+  AttnArgs a{};
   a.q = (const uint16_t*)d_q;
   a.locs = d_locs;
   a.kv = (const uint8_t*)d_kv;

@@ -37,6 +37,8 @@ struct hs_pool {
   unsigned long long* counters;
   uint32_t* step_log;
   uint32_t* err_global;  // attention-side error bits
+  int2* pend;            // [L][R][k] {position, slot} of misses the attention still has to fetch
+  uint32_t* pend_live;   // [L][R] 1 while such a list is outstanding
   float* attn_part;      // split partials
   uint32_t* attn_ticket; // [R][attn_max_groups]
   int attn_max_splits;
@@ -74,6 +76,25 @@ __device__ __forceinline__ const uint8_t* hs_hist_addr(const uint8_t* shared, co
   return priv + (((int64_t)r * L + l) * priv_tokens + (p - P0)) * rec;
 }
 
+// Finish the host -> slot copies that a resolve in fetch-in-attention mode left pending for
+// (r, l) and that no attention has completed: pend[i] = {position, slot} or {-1, -1}.  The
+// entries [k*part/nparts, k*(part+1)/nparts) are copied by this CTA, one warp per record.
+__device__ __forceinline__ void hs_copy_pending(const int2* pend, int k, const uint8_t* hist_shared,
+                                                const uint8_t* hist_priv, int64_t P0, int64_t priv_tokens,
+                                                int64_t rec, int L, int r, int l, uint8_t* buf_r, int part,
+                                                int nparts) {
+  const int e0 = (int)((int64_t)k * part / nparts), e1 = (int)((int64_t)k * (part + 1) / nparts);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  const int nv = (int)(rec / 16);
+  for (int i = e0 + warp; i < e1; i += nw) {
+    const int2 e = pend[i];
+    if (e.x < 0 || e.y < 0) continue;
+    const uint4* src = (const uint4*)hs_hist_addr(hist_shared, hist_priv, P0, priv_tokens, rec, L, r, l, e.x);
+    uint4* dst = (uint4*)(buf_r + (int64_t)e.y * rec);
+    for (int v = lane; v < nv; v += 32) dst[v] = src[v];
+  }
+}
+
 // ---- launchers (defined in the kernel translation units) -------------------
 int hs_launch_resolve(hs_pool* pool, int layer, const int32_t* d_topk, int32_t* d_locs, cudaStream_t st);
 int hs_launch_append(hs_pool* pool, int layer, const int64_t* d_pos, const void* d_rec, cudaStream_t st);
@@ -82,6 +103,7 @@ int hs_launch_attn(hs_pool* pool, int layer, const void* d_q, const int32_t* d_l
 // attention workspace requirement for a configuration (floats, splits, groups)
 void hs_attn_workspace(const hs_config* cfg, int num_sms, size_t* floats, int* max_splits, int* max_groups);
 bool hs_attn_supported(const hs_config* cfg);
+bool hs_attn_can_fetch(const hs_config* cfg);  // the attention can take over the miss fetch
 int hs_attn_prepare(const hs_config* cfg, int num_sms);
 int hs_resolve_prepare(hs_pool* pool);
 size_t hs_resolve_smem_bytes(const hs_config* cfg);

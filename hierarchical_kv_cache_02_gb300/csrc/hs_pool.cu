@@ -38,6 +38,7 @@ int check_config(const hs_config* c) {
     return HS_ERR_CONFIG;
   if (!hs_attn_supported(c)) return HS_ERR_CONFIG;
   if (hs_resolve_smem_bytes(c) > 200 * 1024) return HS_ERR_CONFIG;
+  if (c->fetch_in_attention != 0 && (c->fetch_in_attention != 1 || !hs_attn_can_fetch(c))) return HS_ERR_CONFIG;
   return HS_OK;
 }
 
@@ -84,6 +85,8 @@ void free_pool(hs_pool* p) {
   cudaFree(p->err_global);
   cudaFree(p->attn_part);
   cudaFree(p->attn_ticket);
+  cudaFree(p->pend);
+  cudaFree(p->pend_live);
   delete p;
 }
 
@@ -118,6 +121,7 @@ int do_reset(hs_pool* p, cudaStream_t st) {
   if (p->step_log && cudaMemsetAsync(p->step_log, 0, (size_t)p->cfg.log_steps * nrl * sizeof(uint32_t), st) != cudaSuccess)
     return HS_ERR_CUDA;
   if (cudaMemsetAsync(p->err_global, 0, sizeof(uint32_t), st) != cudaSuccess) return HS_ERR_CUDA;
+  if (p->pend_live && cudaMemsetAsync(p->pend_live, 0, nrl * sizeof(uint32_t), st) != cudaSuccess) return HS_ERR_CUDA;
   if (cudaMemsetAsync(p->attn_ticket, 0, (size_t)p->cfg.num_requests * p->attn_max_groups * sizeof(uint32_t), st) !=
       cudaSuccess)
     return HS_ERR_CUDA;
@@ -178,6 +182,10 @@ extern "C" int hs_pool_create(const hs_config* cfg, int cuda_device, hs_pool** o
     rc = dev_alloc(&p->attn_part, p->attn_part_floats);
   }
   if (rc == HS_OK) rc = dev_alloc(&p->attn_ticket, R * (size_t)p->attn_max_groups);
+  if (rc == HS_OK && cfg->fetch_in_attention) {
+    rc = dev_alloc(&p->pend, L * R * (size_t)cfg->top_k);
+    if (rc == HS_OK) rc = dev_alloc(&p->pend_live, L * R);
+  }
   if (rc == HS_OK) rc = hs_resolve_prepare(p);
   if (rc == HS_OK) rc = hs_attn_prepare(cfg, p->num_sms);
   if (rc == HS_OK) rc = do_reset(p, 0);

@@ -34,6 +34,8 @@ struct ResolveArgs {
   uint8_t* buf;         // layer slice [R][B][rec]
   int64_t C, P0, priv_tokens, rec;
   uint64_t seed;
+  int2* pend;            // fetch-in-attention mode: layer slice [R][k], else null
+  uint32_t* pend_live;   // layer slice [R]
   int R, L, layer, B, k, policy, log_steps, ht_bits, cs;
 };
 
@@ -226,6 +228,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
   const hs_rl_state st = a.state[r];
   const uint32_t clock = st.clock;
 
+  // fetch-in-attention mode: copies a previous resolve left to an attention that never ran are
+  // finished first (they target slots this decision may reuse); the cluster barrier below orders
+  // them before this resolve rewrites the pending list
+  if (a.pend != nullptr && a.pend_live[r] != 0u)
+    hs_copy_pending(a.pend + (int64_t)r * k, k, a.hist_shared, a.hist_priv, a.P0, a.priv_tokens, a.rec, a.L, r,
+                    a.layer, a.buf + (int64_t)r * B * a.rec, crank, a.cs);
+
   // ---------------- phase A: every CTA of the cluster computes the whole decision ----------------
   if (tid == 0) err_bits = ((uint64_t)clock + (uint64_t)k >= 0xFFFFFFFFull) ? (uint32_t)HS_DEVERR_CLOCK : 0u;
   for (int x = tid; x < ht_size; x += kThreads) {
@@ -378,6 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
       } else if (hs == -2) {
         locs[i] = -1;
       }
+      if (a.pend != nullptr && hs != -1) a.pend[(int64_t)r * k + i] = make_int2(-1, -1);
     }
     const int q0 = (int)((int64_t)m * crank / a.cs), q1 = (int)((int64_t)m * (crank + 1) / a.cs);
     for (int q = q0 + tid; q < q1; q += kThreads) {
@@ -385,6 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
       tag[j] = miss_pos[q];
       stamp[j] = a.policy == HS_POLICY_FIFO ? clock + (uint32_t)q : clock + (uint32_t)h + (uint32_t)q;
       locs[miss_idx[q]] = j;
+      if (a.pend != nullptr) a.pend[(int64_t)r * k + miss_idx[q]] = make_int2(miss_pos[q], j);
     }
     if (a.policy == HS_POLICY_SWAP_VANILLA) {
       const int s0 = (int)((int64_t)B * crank / a.cs), s1 = (int)((int64_t)B * (crank + 1) / a.cs);
@@ -395,8 +406,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
         }
       }
     }
-    // (4) fetch this CTA's share of the misses from the host history
-    if (q1 > q0) fetch_misses<NV>(a, r, q0, q1, miss_pos, victims);
+    // (4) fetch this CTA's share of the misses from the host history (or leave it to the attention)
+    if (a.pend == nullptr && q1 > q0) fetch_misses<NV>(a, r, q0, q1, miss_pos, victims);
   }
 
   // (5) clock and counters
@@ -412,6 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
     c[3] += (unsigned long long)m * (unsigned long long)a.rec;
     if (a.step_log != nullptr && st.nres < (uint32_t)a.log_steps)
       a.step_log[((int64_t)st.nres * a.L + a.layer) * a.R + r] = (uint32_t)m;
+    if (a.pend != nullptr) a.pend_live[r] = 1u;
   }
 }
 
@@ -427,13 +439,22 @@ struct AppendArgs {
   uint8_t* buf;
   int64_t C, P0, priv_tokens, rec;
   uint64_t seed;
-  int R, L, layer, B, policy;
+  const int2* pend;      // fetch-in-attention mode: layer slice [R][k], else null
+  uint32_t* pend_live;
+  int R, L, layer, B, policy, k;
 };
 
 constexpr int kAppendThreads = 256;
 
 __global__ void __launch_bounds__(kAppendThreads) k_append(AppendArgs a) {
   const int r = blockIdx.x, tid = threadIdx.x;
+  if (a.pend != nullptr && a.pend_live[r] != 0u) {
+    // finish the copies a previous resolve left pending before this append may overwrite a slot
+    hs_copy_pending(a.pend + (int64_t)r * a.k, a.k, a.hist_shared, a.hist_priv, a.P0, a.priv_tokens, a.rec, a.L, r,
+                    a.layer, a.buf + (int64_t)r * a.B * a.rec, 0, 1);
+    __syncthreads();
+    if (tid == 0) a.pend_live[r] = 0u;
+  }
   const int64_t p = a.pos[r];
   const hs_rl_state st = a.state[r];
   if (p < a.P0 || p < 0 || p >= a.C) {
@@ -591,6 +612,8 @@ int hs_launch_resolve(hs_pool* p, int layer, const int32_t* d_topk, int32_t* d_l
   a.log_steps = c.log_steps;
   a.ht_bits = ht_bits_for(c.top_k);
   a.cs = p->resolve_cs;
+  a.pend = p->pend != nullptr ? p->pend + (int64_t)layer * R * c.top_k : nullptr;
+  a.pend_live = p->pend_live != nullptr ? p->pend_live + (int64_t)layer * R : nullptr;
   const size_t smem = hs_resolve_smem_bytes(&c);
   cudaError_t e;
   switch (c.io_chunk_bytes) {
@@ -636,6 +659,9 @@ int hs_launch_append(hs_pool* p, int layer, const int64_t* d_pos, const void* d_
   a.layer = layer;
   a.B = c.buffer_slots;
   a.policy = c.policy;
+  a.k = c.top_k;
+  a.pend = p->pend != nullptr ? p->pend + (int64_t)layer * R * c.top_k : nullptr;
+  a.pend_live = p->pend_live != nullptr ? p->pend_live + (int64_t)layer * R : nullptr;
   k_append<<<c.num_requests, kAppendThreads, 0, st>>>(a);
   return cudaGetLastError() == cudaSuccess ? HS_OK : HS_ERR_CUDA;
 }

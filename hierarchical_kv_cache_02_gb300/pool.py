@@ -43,6 +43,7 @@ class HsConfig:
     io_chunk_bytes: int = 64
     log_steps: int = 0
     shared_prefix: int = 0
+    fetch_in_attention: int = 0
 
     @property
     def record_bytes(self) -> int:

@@ -90,6 +90,14 @@ typedef struct {
                              16..128, a power of two dividing the record size (summary §5: the
                              per-thread transfer size of the swap-in is a tuned knob) */
   int32_t log_steps;      /* >0: keep per-step miss counts of the first log_steps resolves */
+  int32_t fetch_in_attention; /* 0: hs_resolve copies the misses into their slots (summary §5).
+                                 1: hs_resolve only decides; the next hs_sparse_attn of the layer
+                                 reads the missing records straight from the host history while it
+                                 gathers the resident ones from HBM, and writes them to their
+                                 slots, so the host-link transfer overlaps the HBM-bound attention.
+                                 Copies left pending when no attention follows are finished by the
+                                 next hs_resolve or hs_append_writethrough of that layer.  Needs
+                                 the GQA layout with at most 8 KV heads. */
 } hs_config;
 
 /* Record size in bytes for a configuration (MLA: 2*head_dim_qk; GQA: 2*kv_heads*(qk+v)). */

@@ -16,10 +16,10 @@ from hierarchical_kv_cache_02_gb300 import (DEVERR_APPEND, DEVERR_DUP, DEVERR_LO
                                              LAYOUT_MLA, HsConfig, HsPool)
 
 
-def _gqa(R, L, C, k, B, policy=0, kvh=8, G=4, io=64, log=0, P0=0, seed=3):
+def _gqa(R, L, C, k, B, policy=0, kvh=8, G=4, io=64, log=0, P0=0, seed=3, fetch=0):
     return HsConfig(num_requests=R, num_layers=L, capacity=C, layout=LAYOUT_GQA, num_q_heads=kvh * G,
                     num_kv_heads=kvh, head_dim_qk=128, head_dim_v=128, top_k=k, buffer_slots=B, policy=policy,
-                    seed=seed, io_chunk_bytes=io, log_steps=log, shared_prefix=P0)
+                    seed=seed, io_chunk_bytes=io, log_steps=log, shared_prefix=P0, fetch_in_attention=fetch)
 
 
 def _mla(R, L, C, k, B, Hq=16, policy=0, io=64, log=0, P0=0):
@@ -82,13 +82,26 @@ def test_tiny_single_request_mla():
     run_and_compare(sc)
 
 
+@pytest.mark.parametrize("fetch", [0, 1])
 @pytest.mark.parametrize("policy", [0, 1, 2, 3])
-def test_gqa_policies_ragged(policy):
-    """3 requests x 2 layers, k=300 (not a multiple of the stage), B=640, every policy."""
+def test_gqa_policies_ragged(policy, fetch):
+    """3 requests x 2 layers, k=300 (not a multiple of the stage), B=640, every policy; misses
+    copied by the resolve (fetch=0) or by the attention while it gathers (fetch=1)."""
     B = 300 if policy == 3 else 640
-    sc = Scenario(_gqa(3, 2, 3000 + 12, 300, B, policy=policy), ctx0=3000, steps=12, appends=True, keep=0.8,
-                  recency_mean=200, seed=policy + 1)
+    sc = Scenario(_gqa(3, 2, 3000 + 12, 300, B, policy=policy, fetch=fetch), ctx0=3000, steps=12, appends=True,
+                  keep=0.8, recency_mean=200, seed=policy + 1)
     run_and_compare(sc)
+
+
+@pytest.mark.parametrize("attn_every", [2, 3])
+def test_fetch_in_attention_with_skipped_attention(attn_every):
+    """Steps without attention leave copies pending; the next append (or resolve) finishes them,
+    so state, slots, buffer contents and later attention still match the oracle."""
+    steps = 3 * attn_every + 1  # the last step runs attention, so the final buffer check sees every row
+    sc = Scenario(_gqa(2, 2, 2500 + steps, 256, 512, fetch=1), ctx0=2500, steps=steps, appends=True, seed=31)
+    run_and_compare(sc, attn_every=attn_every)
+    sc = Scenario(_gqa(2, 1, 2500, 256, 512, fetch=1), ctx0=2500, steps=steps, appends=False, seed=32)
+    run_and_compare(sc, attn_every=attn_every)
 
 
 @pytest.mark.parametrize("policy", [0, 2])
@@ -110,9 +123,10 @@ def test_gqa_group_sizes(G):
     run_and_compare(sc)
 
 
-def test_shared_prefix_history():
+@pytest.mark.parametrize("fetch", [0, 1])
+def test_shared_prefix_history(fetch):
     """Requests share one prefilled history (read-only); appended tokens are private."""
-    sc = Scenario(_gqa(3, 2, 2500 + 8, 200, 400, P0=2500), ctx0=2500, steps=8, appends=True, seed=21)
+    sc = Scenario(_gqa(3, 2, 2500 + 8, 200, 400, P0=2500, fetch=fetch), ctx0=2500, steps=8, appends=True, seed=21)
     run_and_compare(sc)
 
 
@@ -122,11 +136,14 @@ def test_buffer_as_large_as_context_no_misses_after_warmup():
     run_and_compare(sc)
 
 
-def test_small_k_and_b_equal_k():
+@pytest.mark.parametrize("fetch", [0, 1])
+def test_small_k_and_b_equal_k(fetch):
     for policy in (0, 3):
-        sc = Scenario(_gqa(2, 1, 500, 1, 1, kvh=1, G=4, policy=policy), ctx0=500, steps=10, appends=False, seed=7)
+        sc = Scenario(_gqa(2, 1, 500, 1, 1, kvh=1, G=4, policy=policy, fetch=fetch), ctx0=500, steps=10,
+                      appends=False, seed=7)
         run_and_compare(sc)
-        sc = Scenario(_gqa(2, 1, 500, 5, 5, kvh=1, G=4, policy=policy), ctx0=500, steps=10, appends=False, seed=8)
+        sc = Scenario(_gqa(2, 1, 500, 5, 5, kvh=1, G=4, policy=policy, fetch=fetch), ctx0=500, steps=10,
+                      appends=False, seed=8)
         run_and_compare(sc)
 
 
@@ -172,7 +189,7 @@ def test_append_out_of_range_flags():
 def test_exactness_cold_warm_resident_bit_identical():
     """Summary §3: the output over the hot buffer equals the output over fully resident KV,
     bit for bit, whatever the cache held before."""
-    for cfg in (_gqa(3, 1, 5000, 512, 1024), _mla(2, 1, 5000, 512, 1024, Hq=32)):
+    for cfg in (_gqa(3, 1, 5000, 512, 1024), _gqa(3, 1, 5000, 512, 1024, fetch=1), _mla(2, 1, 5000, 512, 1024, Hq=32)):
         sc = Scenario(cfg, ctx0=5000, steps=10, appends=False, keep=0.85, recency_mean=300, seed=2)
         warm = HsPool(cfg)
         prefill(warm, sc)
@@ -209,10 +226,11 @@ def test_resident_kv_bad_rows_flagged():
     pool.close()
 
 
-def test_cuda_graph_replay_matches_eager():
+@pytest.mark.parametrize("fetch", [0, 1])
+def test_cuda_graph_replay_matches_eager(fetch):
     """All calls are capturable: one decode step (append, resolve, attention for every layer)
     captured once and replayed gives the eager results bit for bit."""
-    cfg = _gqa(2, 2, 3000 + 6, 256, 512)
+    cfg = _gqa(2, 2, 3000 + 6, 256, 512, fetch=fetch)
     sc = Scenario(cfg, ctx0=3000, steps=6, appends=True, seed=14)
     eager = HsPool(cfg)
     prefill(eager, sc)
