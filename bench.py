@@ -202,7 +202,7 @@ def run_ours(args, w, world, rank, local):
     t_setup = time.time()
     fetch = args.fetch
     if fetch == "auto":
-        fetch = "attention" if w["layout"] == 1 and w["Hkv"] <= 8 else "resolve"
+        fetch = "resolve"  # each kernel against its own roofline; "attention" overlaps the link with HBM
     wl = Workload(w, S, device, seed=1000 + 17 * rank, fetch=fetch)
     pool = HsPool(wl.cfg, device=local)
     wl.prefill(pool)
