@@ -47,6 +47,12 @@ WORKLOADS = {
 }
 
 
+# dram__bytes_read.sum + dram__bytes_write.sum of one attention launch from an ncu capture of the
+# same kernel and per-launch size (profiles/k_attn_gqa_mma_gqa_b16.md); None where no capture of the
+# current kernel exists
+ATTN_TRAFFIC = {("gqa_b16_l32", "resolve"): 138.75e6}
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -218,10 +224,14 @@ def run_ours(args, w, world, rank, local):
         for l in range(L):
             if ev is not None:
                 ev[l][0].record(stream)
-            pool.append(l, wl.pos[t], wl.app[t, l])
+            if args.separate_append:
+                pool.append(l, wl.pos[t], wl.app[t, l])
             if ev is not None:
                 ev[l][1].record(stream)
-            pool.resolve(l, wl.topk[t, l], locs[l])
+            if args.separate_append:
+                pool.resolve(l, wl.topk[t, l], locs[l])
+            else:
+                pool.append_resolve(l, wl.pos[t], wl.app[t, l], wl.topk[t, l], locs[l])
             if ev is not None:
                 ev[l][2].record(stream)
             pool.sparse_attn(l, wl.q[t, l], locs[l], outs[l], scale=scale)
@@ -279,19 +289,20 @@ def run_ours(args, w, world, rank, local):
                    "append": True, "miss_fetch": fetch, "parallelism": f"replicas{world}",
                    "l2": "inputs larger than L2 (each attention launch gathers "
                          f"{attn_bytes_per_launch(w) / 1e6:.0f} MB; a step touches {L} layers)"},
-        "us_per_layer": {"total": max_elapsed / (K * L) * 1e6, "resolve": float(res_ms.mean() * 1e3),
+        "us_per_layer": {"total": max_elapsed / (K * L) * 1e6,
+                         "resolve": float(res_ms.mean() * 1e3),  # includes the append when fused
                          "sparse_attn": attn_us, "append": float(app_ms.mean() * 1e3),
                          "resolve_plus_attn": float((res_ms + att_ms).mean() * 1e3)},
         "miss_rate": float(st["misses"]) / max(1.0, float(st["hits"] + st["misses"])),
         "roofline": {"kernel": "sparse_attn", "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": args.traffic,
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": args.traffic if args.traffic is not None else ATTN_TRAFFIC.get((args.workload, fetch)),
                      "peak_source": peaks["source"],
                      "bytes_per_launch": attn_bytes_per_launch(w)},
         "host_link": {"kernel": "resolve", "miss_bytes_per_layer": miss_bytes / (K * L),
                       "achieved_gbs": miss_bytes / res_total_s / 1e9 if res_total_s > 0 else None,
                       "h2d_copy_peak_gbs": h2d,
                       "frac": (miss_bytes / res_total_s / 1e9) / h2d if res_total_s > 0 and h2d else None},
-        "gpu_launches": K * L * 3,
+        "gpu_launches": K * L * (3 if args.separate_append else 2),
         "clocks": clk,
         "setup_s": setup_secs,
         "errors": int(st["error_bits"]),
@@ -327,8 +338,7 @@ def run_e2e(pool, wl, W, K, world, locs, outs, scale):
         d_app.copy_(h_app[t], non_blocking=True)
         d_pos.copy_(h_pos[t], non_blocking=True)
         for l in range(L):
-            pool.append(l, d_pos, d_app[l])
-            pool.resolve(l, d_topk[l], locs[l])
+            pool.append_resolve(l, d_pos, d_app[l], d_topk[l], locs[l])
             pool.sparse_attn(l, d_q[l], locs[l], outs[l], scale=scale)
             h_out[t, l].copy_(outs[l], non_blocking=True)
 
@@ -439,6 +449,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="gqa_b16_l32")
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling runs)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--separate-append", action="store_true",
+                    help="append and resolve as two launches instead of the fused hs_append_resolve")
     ap.add_argument("--fetch", choices=["auto", "resolve", "attention"], default="auto",
                     help="who copies the misses host -> HBM: the resolve kernel, or the attention while it gathers")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -251,7 +251,16 @@ extern "C" int hs_resolve(hs_pool* pool, int layer, const int32_t* d_topk, int32
   if (pool == nullptr || d_topk == nullptr || d_locs == nullptr) return HS_ERR_ARG;
   if (layer < 0 || layer >= pool->cfg.num_layers) return HS_ERR_ARG;
   DeviceGuard guard(pool->device);
-  return hs_launch_resolve(pool, layer, d_topk, d_locs, (cudaStream_t)stream);
+  return hs_launch_resolve(pool, layer, nullptr, nullptr, d_topk, d_locs, (cudaStream_t)stream);
+}
+
+extern "C" int hs_append_resolve(hs_pool* pool, int layer, const int64_t* d_pos, const void* d_rec,
+                                 const int32_t* d_topk, int32_t* d_locs, void* stream) {
+  if (pool == nullptr || d_pos == nullptr || d_rec == nullptr || d_topk == nullptr || d_locs == nullptr)
+    return HS_ERR_ARG;
+  if (layer < 0 || layer >= pool->cfg.num_layers) return HS_ERR_ARG;
+  DeviceGuard guard(pool->device);
+  return hs_launch_resolve(pool, layer, d_pos, d_rec, d_topk, d_locs, (cudaStream_t)stream);
 }
 
 extern "C" int hs_sparse_attn(hs_pool* pool, int layer, const void* d_q, const int32_t* d_locs,

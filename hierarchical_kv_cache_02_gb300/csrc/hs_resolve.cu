@@ -36,6 +36,9 @@ struct ResolveArgs {
   uint64_t seed;
   int2* pend;            // fetch-in-attention mode: layer slice [R][k], else null
   uint32_t* pend_live;   // layer slice [R]
+  const int64_t* app_pos;  // fused write-through append before the resolve: [R] positions, or null
+  const uint8_t* app_rec;  // [R][rec] new records
+  uint8_t* hist_priv_w;    // writable view of the private host history
   int R, L, layer, B, k, policy, log_steps, ht_bits, cs;
 };
 
@@ -226,7 +229,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
   int32_t* tag = a.tag + (int64_t)r * B;
   uint32_t* stamp = a.stamp + (int64_t)r * B;
   const hs_rl_state st = a.state[r];
-  const uint32_t clock = st.clock;
+  __shared__ int s_app_slot;
+  __shared__ unsigned long long s_best[kWarps];
+  __shared__ int s_found[kWarps];
 
   // fetch-in-attention mode: copies a previous resolve left to an attention that never ran are
   // finished first (they target slots this decision may reuse); the cluster barrier below orders
@@ -236,7 +241,53 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
                     a.layer, a.buf + (int64_t)r * B * a.rec, crank, a.cs);
 
   // ---------------- phase A: every CTA of the cluster computes the whole decision ----------------
-  if (tid == 0) err_bits = ((uint64_t)clock + (uint64_t)k >= 0xFFFFFFFFull) ? (uint32_t)HS_DEVERR_CLOCK : 0u;
+  // fused write-through append (hs_append_resolve): the new position takes the slot that already
+  // holds it, else the slot with the smallest eviction key over all B slots; stamp = clock, clock
+  // += 1; the resolve below then sees that state
+  int app_slot = -1;
+  int64_t app_p = -1;
+  uint32_t app_err = 0u;
+  if (a.app_pos != nullptr) {
+    app_p = a.app_pos[r];
+    if (app_p < a.P0 || app_p < 0 || app_p >= a.C) {
+      app_err = (uint32_t)HS_DEVERR_APPEND;
+    } else {
+      int found = 0x7fffffff;
+      unsigned long long best = ~0ull;
+      for (int j = tid; j < B; j += kThreads) {
+        const int32_t t = tag[j];
+        if (t == (int32_t)app_p) found = min(found, j);
+        const uint32_t key = hs_evict_key(a.policy, t, stamp[j], a.seed, st.nres, a.R, r, a.L, a.layer, B, j);
+        const unsigned long long kj = ((unsigned long long)key << 32) | (unsigned)j;
+        best = kj < best ? kj : best;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        found = min(found, __shfl_xor_sync(0xffffffffu, found, o));
+        const unsigned long long y = __shfl_xor_sync(0xffffffffu, best, o);
+        best = y < best ? y : best;
+      }
+      if ((tid & 31) == 0) {
+        s_found[tid >> 5] = found;
+        s_best[tid >> 5] = best;
+      }
+      __syncthreads();
+      if (tid == 0) {
+        int f = s_found[0];
+        unsigned long long bb = s_best[0];
+        for (int w = 1; w < kWarps; ++w) {
+          f = min(f, s_found[w]);
+          bb = s_best[w] < bb ? s_best[w] : bb;
+        }
+        s_app_slot = f != 0x7fffffff ? f : (int)(bb & 0xffffffffull);
+      }
+      __syncthreads();
+      app_slot = s_app_slot;
+    }
+  }
+  const uint32_t clock = st.clock + (app_slot >= 0 ? 1u : 0u);  // the resolve's clock
+  if (tid == 0)
+    err_bits = app_err | (((uint64_t)clock + (uint64_t)k >= 0xFFFFFFFFull) ? (uint32_t)HS_DEVERR_CLOCK : 0u);
   for (int x = tid; x < ht_size; x += kThreads) {
     ht_key[x] = -1;
     ht_val[x] = 0x7fffffff;
@@ -280,7 +331,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
 
   // (2) probe every slot; keep its eviction key
   for (int j = tid; j < B; j += kThreads) {
-    const int32_t t = tag[j];
+    const bool is_app = j == app_slot;
+    const int32_t t = is_app ? (int32_t)app_p : tag[j];
+    const uint32_t stj = is_app ? st.clock : stamp[j];
     uint8_t f = 0;
     if (t >= 0) {
       uint32_t h = ht_hash(t, a.ht_bits);
@@ -296,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
       }
     }
     flag[j] = f;
-    key32[j] = hs_evict_key(a.policy, t, stamp[j], a.seed, st.nres, a.R, r, a.L, a.layer, B, j);
+    key32[j] = hs_evict_key(a.policy, t, stj, a.seed, st.nres, a.R, r, a.L, a.layer, B, j);
   }
   __syncthreads();
 
@@ -406,6 +459,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
         }
       }
     }
+    // the fused append's own writes (CTA 0): the record to the host history always; slot, tag and
+    // stamp unless the resolve reuses or empties that slot now, the stamp only where no hit restamps it
+    if (app_slot >= 0 && crank == 0) {
+      const uint4* src = (const uint4*)(a.app_rec + (int64_t)r * a.rec);
+      uint4* dh = (uint4*)(a.hist_priv_w + (((int64_t)r * a.L + a.layer) * a.priv_tokens + (app_p - a.P0)) * a.rec);
+      // the slot is rewritten by the resolve when it is a victim now, or emptied by swap-vanilla
+      // when it holds no selected position
+      const bool evicted = (flag[app_slot] & 2u) != 0u ||
+                           (a.policy == HS_POLICY_SWAP_VANILLA && (flag[app_slot] & 1u) == 0u);
+      const bool restamped = (flag[app_slot] & 1u) != 0u && a.policy != HS_POLICY_FIFO;
+      uint4* db = (uint4*)(a.buf + ((int64_t)r * B + app_slot) * a.rec);
+      const int nv = (int)(a.rec / 16);
+      for (int x = tid; x < nv; x += kThreads) {
+        const uint4 v = src[x];
+        dh[x] = v;
+        if (!evicted) db[x] = v;
+      }
+      if (tid == 0 && !evicted) {
+        tag[app_slot] = (int32_t)app_p;
+        if (!restamped) stamp[app_slot] = st.clock;
+      }
+    }
     // (4) fetch this CTA's share of the misses from the host history (or leave it to the attention)
     if (a.pend == nullptr && q1 > q0) fetch_misses<NV>(a, r, q0, q1, miss_pos, victims);
   }
@@ -420,6 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
     unsigned long long* c = a.counters + (int64_t)r * 4;
     c[0] += (unsigned long long)h;
     c[1] += (unsigned long long)m;
+    if (app_slot >= 0) c[2] += 1ull;
     c[3] += (unsigned long long)m * (unsigned long long)a.rec;
     if (a.step_log != nullptr && st.nres < (uint32_t)a.log_steps)
       a.step_log[((int64_t)st.nres * a.L + a.layer) * a.R + r] = (uint32_t)m;
@@ -584,7 +660,8 @@ int prepare_nv(const hs_config* c, int num_sms, int* cs_out) {
 
 }  // namespace
 
-int hs_launch_resolve(hs_pool* p, int layer, const int32_t* d_topk, int32_t* d_locs, cudaStream_t st) {
+int hs_launch_resolve(hs_pool* p, int layer, const int64_t* d_pos, const void* d_rec, const int32_t* d_topk,
+                      int32_t* d_locs, cudaStream_t st) {
   const hs_config& c = p->cfg;
   const int64_t R = c.num_requests, B = c.buffer_slots;
   ResolveArgs a;
@@ -614,6 +691,9 @@ int hs_launch_resolve(hs_pool* p, int layer, const int32_t* d_topk, int32_t* d_l
   a.cs = p->resolve_cs;
   a.pend = p->pend != nullptr ? p->pend + (int64_t)layer * R * c.top_k : nullptr;
   a.pend_live = p->pend_live != nullptr ? p->pend_live + (int64_t)layer * R : nullptr;
+  a.app_pos = d_pos;
+  a.app_rec = (const uint8_t*)d_rec;
+  a.hist_priv_w = p->dmap_priv;
   const size_t smem = hs_resolve_smem_bytes(&c);
   cudaError_t e;
   switch (c.io_chunk_bytes) {

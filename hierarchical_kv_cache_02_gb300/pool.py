@@ -159,6 +159,22 @@ class HsPool:
         _check("hs_resolve", self.lib.hs_resolve(self._h, int(layer), t, lo, _stream_ptr(stream, self.device)))
         return locs
 
+    def append_resolve(self, layer: int, pos, rec, topk, locs=None, stream=None):
+        """append(layer, pos, rec) then resolve(layer, topk, locs), fused into one kernel."""
+        import torch
+
+        c = self.cfg
+        R, k = c.num_requests, c.top_k
+        p = _dev_tensor(pos, torch.int64, (R,), "pos", self.device)
+        rr = _dev_tensor(rec, torch.bfloat16, (R, c.record_elems), "rec", self.device)
+        t = _dev_tensor(topk, torch.int32, (R, k), "topk", self.device)
+        if locs is None:
+            locs = torch.empty((R, k), dtype=torch.int32, device=f"cuda:{self.device}")
+        lo = _dev_tensor(locs, torch.int32, (R, k), "locs", self.device)
+        _check("hs_append_resolve", self.lib.hs_append_resolve(self._h, int(layer), p, rr, t, lo,
+                                                               _stream_ptr(stream, self.device)))
+        return locs
+
     def sparse_attn(self, layer: int, q, locs, out=None, scale=None, kv=None, stream=None):
         """q bf16 [R][Hq][Dqk]; locs int32 [R][k]; out fp32 [R][Hq][Dv].  kv: optional resident
         bf16 [R][rows][record_elems] (then locs index its rows instead of the hot buffer)."""

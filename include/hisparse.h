@@ -152,6 +152,15 @@ int hs_append_writethrough(hs_pool* pool, int layer, const int64_t* d_pos, const
 int hs_resolve(hs_pool* pool, int layer, const int32_t* d_topk, int32_t* d_locs, void* stream);
 
 /*
+ * hs_append_writethrough followed by hs_resolve for the same layer, fused into one kernel (the
+ * append's slot choice and the resolve's decision are made by the same resolve cluster): results,
+ * state and counters are identical to the two calls in sequence.  Arguments as for those calls.
+ * CAPTURABLE.
+ */
+int hs_append_resolve(hs_pool* pool, int layer, const int64_t* d_pos, const void* d_rec, const int32_t* d_topk,
+                      int32_t* d_locs, void* stream);
+
+/*
  * Sparse attention over resolved slots (summary §3 step (4)): for request r and query head h,
  *   out[r][h] = sum_i softmax_i(scale * <q[r][h], K(row_i)>) V(row_i)
  * over the entries i with d_locs[r][i] >= 0, in top-k order, with K/V taken from the record

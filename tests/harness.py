@@ -80,19 +80,25 @@ def prefill(pool, sc: Scenario):
                 pool.prefill(r, l, lo, bf16_tensor(sc.hist[(r, l)][lo:sc.ctx0]))
 
 
-def gpu_step(pool, sc: Scenario, t: int, device="cuda:0", attn=True):
-    """One decode step on the GPU; returns per-layer (locs, out) as CPU arrays."""
+def gpu_step(pool, sc: Scenario, t: int, device="cuda:0", attn=True, fused=False):
+    """One decode step on the GPU; returns per-layer (locs, out) as CPU arrays.  fused: the append
+    and the resolve of a layer go through the single fused call."""
     torch = _torch()
     c = sc.cfg
     R = c.num_requests
     res = []
     for l in range(c.num_layers):
+        topk = torch.from_numpy(sc.trace[t, l]).to(device)
         if sc.appends:
             pos = torch.full((R,), sc.ctx0 + t, dtype=torch.int64, device=device)
             rec = bf16_tensor(np.stack([sc.hist[(r, l)][sc.ctx0 + t] for r in range(R)]), device)
-            pool.append(l, pos, rec)
-        topk = torch.from_numpy(sc.trace[t, l]).to(device)
-        locs = pool.resolve(l, topk)
+            if fused:
+                locs = pool.append_resolve(l, pos, rec, topk)
+            else:
+                pool.append(l, pos, rec)
+                locs = pool.resolve(l, topk)
+        else:
+            locs = pool.resolve(l, topk)
         out = None
         if attn:
             q = bf16_tensor(sc.q[t, l], device)

@@ -28,14 +28,14 @@ def _mla(R, L, C, k, B, Hq=16, policy=0, io=64, log=0, P0=0):
                     io_chunk_bytes=io, log_steps=log, shared_prefix=P0)
 
 
-def run_and_compare(sc: Scenario, attn_every=1, check_state=True):
+def run_and_compare(sc: Scenario, attn_every=1, check_state=True, fused=False):
     cfg = sc.cfg
     pool = HsPool(cfg)
     prefill(pool, sc)
     orc = OracleRun(sc)
     worst = 0.0
     for t in range(sc.steps):
-        res = gpu_step(pool, sc, t, attn=(t % attn_every == 0))
+        res = gpu_step(pool, sc, t, attn=(t % attn_every == 0), fused=fused)
         ref = orc.step(t)
         for l in range(cfg.num_layers):
             locs, out = res[l]
@@ -91,6 +91,27 @@ def test_gqa_policies_ragged(policy, fetch):
     sc = Scenario(_gqa(3, 2, 3000 + 12, 300, B, policy=policy, fetch=fetch), ctx0=3000, steps=12, appends=True,
                   keep=0.8, recency_mean=200, seed=policy + 1)
     run_and_compare(sc)
+
+
+@pytest.mark.parametrize("fetch", [0, 1])
+@pytest.mark.parametrize("policy", [0, 1, 2, 3])
+def test_fused_append_resolve(policy, fetch):
+    """hs_append_resolve equals append then resolve: same slots, state, counters and outputs as
+    the oracle, for every policy (swap-vanilla empties the appended slot when it is unselected)."""
+    B = 300 if policy == 3 else 640
+    sc = Scenario(_gqa(3, 2, 3000 + 12, 300, B, policy=policy, fetch=fetch), ctx0=3000, steps=12, appends=True,
+                  keep=0.8, recency_mean=200, seed=policy + 41)
+    run_and_compare(sc, fused=True)
+    # the appended position is not always selected: drop it from some lists (replaced by padding)
+    sc = Scenario(_gqa(2, 1, 800 + 10, 64, 96, policy=policy, fetch=fetch), ctx0=800, steps=10, appends=True,
+                  keep=0.7, recency_mean=50, seed=policy + 51)
+    for t in range(0, 10, 2):
+        sc.trace[t, 0, 0][sc.trace[t, 0, 0] == 800 + t] = -1
+    run_and_compare(sc, fused=True)
+    if policy == 0 and fetch == 0:
+        sc = Scenario(_mla(1, 1, 4096 + 16, 256, 512), ctx0=4096, steps=16, appends=True, keep=0.9,
+                      recency_mean=512, seed=3)
+        run_and_compare(sc, fused=True)
 
 
 @pytest.mark.parametrize("attn_every", [2, 3])
