@@ -875,6 +875,240 @@ __global__ void __launch_bounds__(MmaThreads<NW, NP>::value, 1) k_attn_gqa_mma(A
   }
 }
 
+// ---- tensor-core variant for shared-latent (MLA) records ---------------------------------
+//
+// All Hq = 64 query heads read the same 576-value latent of every selected token (K = the whole
+// latent, V = its first 512 values).  Per 16-token stage, consumer warp w owns head tile
+// mt = w % 4 (16 heads) and value half dh = w / 4 (256 values):
+//   S[16 x 16] = Q[16 x 576] . K^T      (36 k-steps; the two warps of a head tile compute the
+//                                        same S, so no exchange is needed)
+//   O[16 x 256] += P[16 x 16] . V[16 x 256]
+// on mma.sync m16n8k16 (bf16 in, fp32 accumulate), P split into bf16 high part + remainder.  Q is
+// staged in shared memory once per CTA; records are staged whole (1152 B) by bulk copies into
+// rows padded to 1168 B, so every ldmatrix phase hits eight distinct bank groups.
+constexpr int kMlaStages = 4;
+constexpr int kMlaHeads = 64;
+
+template <int NSTAGE>
+__global__ void __launch_bounds__(9 * 32, 1) k_attn_mla_mma(AttnArgs a) {
+  constexpr int T = kMmaTile;
+  constexpr int NW = 8;
+  constexpr int DK = 576, DV = 512;
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t full_bar[NSTAGE];
+  __shared__ __align__(8) uint64_t empty_bar[NSTAGE];
+  __shared__ uint32_t tok_mask[NSTAGE];
+  __shared__ uint32_t abort_flag;
+
+  const int split = blockIdx.x, r = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t0 = split * a.chunk;
+  const int t1 = min(a.k, t0 + a.chunk);
+  const int n = t1 - t0;
+  const int nst = (n + T - 1) / T;
+  const int64_t rec = a.rec;                 // 1152
+  const uint32_t rs = (uint32_t)rec + 16u;   // padded row stride
+  const uint32_t qs = (uint32_t)DK * 2u + 16u;
+  const int32_t* locs = a.locs + (int64_t)r * a.k;
+  uint8_t* ring = smem;
+  uint8_t* qsm = smem + (size_t)NSTAGE * T * rs;               // [64][qs]
+  int32_t* s_locs = (int32_t*)(qsm + (size_t)kMlaHeads * qs);  // [chunk]
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NSTAGE; ++s) {
+      mbar_init(&full_bar[s], 1u);
+      mbar_init(&empty_bar[s], (uint32_t)NW);
+    }
+    abort_flag = 0u;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  // queries of this request into shared memory (all warps, 16-byte pieces)
+  {
+    const uint4* qg = (const uint4*)(a.q + (int64_t)r * kMlaHeads * DK);
+    constexpr int per_row = DK * 2 / 16;  // 72
+    for (int x = threadIdx.x; x < kMlaHeads * per_row; x += blockDim.x) {
+      const int h = x / per_row, c = x - h * per_row;
+      *(uint4*)(qsm + (size_t)h * qs + c * 16) = qg[x];
+    }
+  }
+  if (warp == NW) {
+    bool bad = false;
+    for (int x = lane; x < n; x += 32) {
+      int32_t loc = locs[t0 + x];
+      if (loc < -1 || (int64_t)loc >= a.rows) {
+        bad = true;
+        loc = -1;
+      }
+      s_locs[x] = loc;
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(a.err, (uint32_t)HS_DEVERR_LOC);
+  }
+  __syncthreads();
+
+  const int grow = lane >> 2, tig = lane & 3;
+  const int mt = warp & 3, dh = warp >> 2;
+  float o[32][4];
+  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+
+  if (warp == NW) {
+    int issued = 0;
+    bool ok = true;
+    for (int st = 0; st < nst; ++st) {
+      const int b = st % NSTAGE;
+      if (st >= NSTAGE) {
+        bool w = true;
+        if (lane == 0) w = mbar_wait_bounded(&empty_bar[b], (uint32_t)((st / NSTAGE - 1) & 1), &abort_flag);
+        if (__shfl_sync(0xffffffffu, w ? 1 : 0, 0) == 0) {
+          ok = false;
+          break;
+        }
+      }
+      const int x = st * T + lane;
+      const int32_t loc = (lane < T && x < n) ? s_locs[x] : -1;
+      const uint32_t mask = __ballot_sync(0xffffffffu, loc >= 0);
+      if (lane == 0) {
+        tok_mask[b] = mask;
+        mbar_arrive_expect_tx(&full_bar[b], (uint32_t)__popc(mask) * (uint32_t)rec);
+      }
+      __syncwarp();
+      if (loc >= 0)
+        bulk_g2s(ring + ((size_t)b * T + lane) * rs, a.kv + ((int64_t)r * a.rows + loc) * rec, (uint32_t)rec,
+                 &full_bar[b]);
+      issued = st + 1;
+    }
+    if (!ok && lane == 0) {
+      *(volatile uint32_t*)&abort_flag = 1u;
+      atomicOr(a.err, (uint32_t)HS_DEVERR_TIMEOUT);
+    }
+    if (abort_flag && lane == 0) {
+      for (int st = max(0, issued - NSTAGE); st < issued; ++st) {
+        volatile uint32_t never = 0u;
+        mbar_wait_bounded(&full_bar[st % NSTAGE], (uint32_t)((st / NSTAGE) & 1), &never);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int n2 = 0; n2 < 32; ++n2) o[n2][0] = o[n2][1] = o[n2][2] = o[n2][3] = 0.f;
+    // ldmatrix rows: Q (A operand, rows = heads), K (non-transposed), V (transposed)
+    const uint32_t qaddr = smem_u32(qsm) + (uint32_t)(mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * qs +
+                           (uint32_t)((lane >> 4) * 16);
+    const int k_tok = (lane & 7) + ((lane >> 4) << 3);
+    const uint32_t k_col = (uint32_t)(((lane >> 3) & 1) * 16);
+    const int v_tok = (lane & 7) + (((lane >> 3) & 1) << 3);
+    const uint32_t v_col = (uint32_t)((lane >> 4) * 16) + (uint32_t)dh * 256u * 2u;
+    const uint32_t ring_u = smem_u32(ring);
+    for (int st = 0; st < nst; ++st) {
+      const int b = st % NSTAGE;
+      if (!mbar_wait_bounded(&full_bar[b], (uint32_t)((st / NSTAGE) & 1), &abort_flag)) {
+        *(volatile uint32_t*)&abort_flag = 1u;
+        atomicOr(a.err, (uint32_t)HS_DEVERR_TIMEOUT);
+        break;
+      }
+      const uint32_t mask = tok_mask[b];
+      const uint32_t kaddr = ring_u + ((uint32_t)b * T + (uint32_t)k_tok) * rs + k_col;
+      const uint32_t vaddr = ring_u + ((uint32_t)b * T + (uint32_t)v_tok) * rs + v_col;
+      float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 6
+      for (int s = 0; s < DK / 16; ++s) {
+        uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+        ldsm_x4(qaddr + s * 32, a0, a1, a2, a3);
+        ldsm_x4(kaddr + s * 32, b0, b1, b2, b3);
+        mma_bf16(s0, a0, a1, a2, a3, b0, b1);
+        mma_bf16(s1, a0, a1, a2, a3, b2, b3);
+      }
+      // online softmax for rows grow (c0, c1) and grow + 8 (c2, c3)
+      const int ta = 2 * tig;
+      const bool v0 = (mask >> ta) & 1u, v1 = (mask >> (ta + 1)) & 1u, v2 = (mask >> (ta + 8)) & 1u,
+                 v3 = (mask >> (ta + 9)) & 1u;
+      float p[2][4];
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const float x0 = v0 ? s0[2 * hr] * a.qscale : -INFINITY;
+        const float x1 = v1 ? s0[2 * hr + 1] * a.qscale : -INFINITY;
+        const float x2 = v2 ? s1[2 * hr] * a.qscale : -INFINITY;
+        const float x3 = v3 ? s1[2 * hr + 1] * a.qscale : -INFINITY;
+        float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float m_new = fmaxf(m_run[hr], mx);
+        const bool any = m_new != -INFINITY;
+        const float alpha = any ? exp2f(m_run[hr] - m_new) : 1.f;
+        p[hr][0] = any ? exp2f(x0 - m_new) : 0.f;
+        p[hr][1] = any ? exp2f(x1 - m_new) : 0.f;
+        p[hr][2] = any ? exp2f(x2 - m_new) : 0.f;
+        p[hr][3] = any ? exp2f(x3 - m_new) : 0.f;
+        float ps = (p[hr][0] + p[hr][1]) + (p[hr][2] + p[hr][3]);
+        ps += __shfl_xor_sync(0xffffffffu, ps, 1);
+        ps += __shfl_xor_sync(0xffffffffu, ps, 2);
+        m_run[hr] = m_new;
+        l_run[hr] = l_run[hr] * alpha + ps;
+#pragma unroll
+        for (int n2 = 0; n2 < 32; ++n2) {
+          o[n2][2 * hr] *= alpha;
+          o[n2][2 * hr + 1] *= alpha;
+        }
+      }
+      // P (A operand): a0 rows grow / tokens 0-7, a1 rows grow+8, a2 / a3 tokens 8-15
+      const uint32_t h0 = pack_bf16(p[0][0], p[0][1]), h1 = pack_bf16(p[1][0], p[1][1]);
+      const uint32_t h2 = pack_bf16(p[0][2], p[0][3]), h3 = pack_bf16(p[1][2], p[1][3]);
+      const uint32_t l0 = pack_bf16(p[0][0] - bf16_lo_f(h0), p[0][1] - bf16_hi_f(h0));
+      const uint32_t l1 = pack_bf16(p[1][0] - bf16_lo_f(h1), p[1][1] - bf16_hi_f(h1));
+      const uint32_t l2 = pack_bf16(p[0][2] - bf16_lo_f(h2), p[0][3] - bf16_hi_f(h2));
+      const uint32_t l3 = pack_bf16(p[1][2] - bf16_lo_f(h3), p[1][3] - bf16_hi_f(h3));
+      uint32_t vm_lo = 0xffffffffu, vm_hi = 0xffffffffu;
+      if (mask != 0xffffu) {
+        vm_lo = (v0 ? 0x0000ffffu : 0u) | (v1 ? 0xffff0000u : 0u);
+        vm_hi = (v2 ? 0x0000ffffu : 0u) | (v3 ? 0xffff0000u : 0u);
+      }
+#pragma unroll
+      for (int pr = 0; pr < 16; ++pr) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(vaddr + pr * 32, b0, b1, b2, b3);
+        b0 &= vm_lo;
+        b1 &= vm_hi;
+        b2 &= vm_lo;
+        b3 &= vm_hi;
+        mma_bf16(o[2 * pr], h0, h1, h2, h3, b0, b1);
+        mma_bf16(o[2 * pr], l0, l1, l2, l3, b0, b1);
+        mma_bf16(o[2 * pr + 1], h0, h1, h2, h3, b2, b3);
+        mma_bf16(o[2 * pr + 1], l0, l1, l2, l3, b2, b3);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[b]);
+    }
+    if (!abort_flag) {
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const int h = mt * 16 + grow + 8 * hr;
+        const int64_t ph = ((int64_t)r * a.S + split) * a.Hq + h;
+        float* po = a.part + ph * DV + dh * 256;
+#pragma unroll
+        for (int n2 = 0; n2 < 32; ++n2)
+          *(float2*)(po + n2 * 8 + 2 * tig) = make_float2(o[n2][2 * hr], o[n2][2 * hr + 1]);
+        if (tig == 0 && dh == 0) {
+          a.ml[ph * 2 + 0] = m_run[hr];
+          a.ml[ph * 2 + 1] = l_run[hr];
+        }
+      }
+    }
+  }
+  // the split partials are combined by k_combine, launched right after this kernel
+}
+
+// Split combine as its own launch: one warp per (request, head), so the 64-head x 512-value partials
+// of the shared-latent layout are reduced by the whole GPU instead of one CTA per request.
+template <int DV>
+__global__ void __launch_bounds__(256) k_combine(AttnArgs a) {
+  const int r = blockIdx.x;
+  const int h = blockIdx.y * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (h >= a.Hq) return;
+  if (a.S <= 32)
+    combine_heads_wide<DV, 1>(a, r, h, lane);
+  else
+    combine_heads<DV>(a, r, h, 1, lane);
+}
+
 // ---- dispatch ----------------------------------------------------------------
 
 struct Plan {
@@ -910,6 +1144,15 @@ bool plan_for(const hs_config* c, int num_sms, Plan* pl) {
     pl->smem = pl->fetch ? (size_t)(kMmaStagesFetch * kMmaTile + kPendSlots) * (size_t)(rec + 16)
                          : (size_t)kMmaStages * kMmaTile * (size_t)(rec + 16);  // + the chunk lists, below
     per_cta_wave = 1;  // one CTA per SM: the ring holds most of the shared memory
+  } else if (c->head_dim_qk == 576 && c->head_dim_v == 512 && c->num_q_heads == kMlaHeads) {
+    pl->kind = 2;
+    pl->fetch = 0;
+    pl->NW = 8;
+    pl->G = kMlaHeads;
+    pl->groups = 1;
+    pl->T = kMmaTile;
+    pl->smem = (size_t)kMlaStages * kMmaTile * (size_t)(rec + 16) + (size_t)kMlaHeads * (576 * 2 + 16);
+    per_cta_wave = 1;
   } else {
     if (c->head_dim_qk != 576 || c->head_dim_v != 512) return false;
     if (c->num_q_heads % 8 != 0) return false;
@@ -931,6 +1174,7 @@ bool plan_for(const hs_config* c, int num_sms, Plan* pl) {
   pl->chunk = chunk;
   pl->S = (c->top_k + chunk - 1) / chunk;
   if (pl->kind == 1) pl->smem += (size_t)chunk * 16;  // slot list, pending index, pending list
+  if (pl->kind == 2) pl->smem += (size_t)chunk * 4;   // slot list
   return pl->smem <= 220 * 1024;
 }
 
@@ -961,6 +1205,12 @@ cudaError_t launch_gqa_nw(const AttnArgs* a, const Plan& pl, cudaStream_t st) {
 }
 
 cudaError_t dispatch(const hs_config& c, const AttnArgs* a, const Plan& pl, cudaStream_t st) {
+  if (pl.kind == 2) {
+    cudaError_t e = launch_kernel(k_attn_mla_mma<kMlaStages>, a, pl, 9 * 32, st);
+    if (e != cudaSuccess || a == nullptr) return e;
+    k_combine<512><<<dim3(a->R, (a->Hq + 7) / 8), 256, 0, st>>>(*a);
+    return cudaGetLastError();
+  }
   if (pl.kind == 0) return launch_kernel(k_attn_cc<576, 512, 1, 8>, a, pl, AttnCfg<576, 512, 1, 8>::THREADS, st);
   switch (pl.G) {
     case 1: return launch_gqa_nw<1>(a, pl, st);
