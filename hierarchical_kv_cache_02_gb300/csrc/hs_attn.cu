@@ -12,6 +12,7 @@
 //     transposed butterfly (31 shuffles for 32 sums), then an online softmax in base 2;
 //   * the last CTA of a (request, head group) to finish combines the split partials in split
 //     order (atomic ticket, no waiting).
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -883,8 +884,11 @@ __global__ void __launch_bounds__(MmaThreads<NW, NP>::value, 1) k_attn_gqa_mma(A
 //   S[16 x 16] = Q[16 x 576] . K^T      (36 k-steps; the two warps of a head tile compute the
 //                                        same S, so no exchange is needed)
 //   O[16 x 256] += P[16 x 16] . V[16 x 256]
-// on mma.sync m16n8k16 (bf16 in, fp32 accumulate), P split into bf16 high part + remainder.  Q is
-// staged in shared memory once per CTA; records are staged whole (1152 B) by bulk copies into
+// on mma.sync m16n8k16 (bf16 in, fp32 accumulate).  The two warps of a head tile each compute half of
+// the 36 k-steps of S and exchange them through shared memory (a + b == b + a: both hold the same
+// S).  P enters the MMA as bf16 and the softmax normaliser sums the same rounded weights, so the
+// output is a convex combination of V rows with weights within 2^-9 (relative) of the exact ones.
+// Q is staged in shared memory once per CTA; records are staged whole (1152 B) by bulk copies into
 // rows padded to 1168 B, so every ldmatrix phase hits eight distinct bank groups.
 constexpr int kMlaStages = 4;
 constexpr int kMlaHeads = 64;
@@ -898,6 +902,7 @@ __global__ void __launch_bounds__(9 * 32, 1) k_attn_mla_mma(AttnArgs a) {
   __shared__ __align__(8) uint64_t full_bar[NSTAGE];
   __shared__ __align__(8) uint64_t empty_bar[NSTAGE];
   __shared__ uint32_t tok_mask[NSTAGE];
+  __shared__ __align__(8) uint64_t xbar[4];  // per head tile: both warps posted their half of S
   __shared__ uint32_t abort_flag;
 
   const int split = blockIdx.x, r = blockIdx.y;
@@ -912,13 +917,15 @@ __global__ void __launch_bounds__(9 * 32, 1) k_attn_mla_mma(AttnArgs a) {
   const int32_t* locs = a.locs + (int64_t)r * a.k;
   uint8_t* ring = smem;
   uint8_t* qsm = smem + (size_t)NSTAGE * T * rs;               // [64][qs]
-  int32_t* s_locs = (int32_t*)(qsm + (size_t)kMlaHeads * qs);  // [chunk]
+  float* xbuf = (float*)(qsm + (size_t)kMlaHeads * qs);          // [2][8 warps][8][32] partial S
+  int32_t* s_locs = (int32_t*)(xbuf + 2 * 8 * 8 * 32);           // [chunk]
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NSTAGE; ++s) {
       mbar_init(&full_bar[s], 1u);
       mbar_init(&empty_bar[s], (uint32_t)NW);
     }
+    for (int s = 0; s < 4; ++s) mbar_init(&xbar[s], 2u);
     abort_flag = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -933,13 +940,25 @@ __global__ void __launch_bounds__(9 * 32, 1) k_attn_mla_mma(AttnArgs a) {
   }
   if (warp == NW) {
     bool bad = false;
-    for (int x = lane; x < n; x += 32) {
-      int32_t loc = locs[t0 + x];
-      if (loc < -1 || (int64_t)loc >= a.rows) {
-        bad = true;
-        loc = -1;
+    for (int x0 = 0; x0 < n; x0 += 32 * 8) {  // eight loads per lane in flight before their stores
+      int32_t v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int x = x0 + 32 * u + lane;
+        v[u] = x < n ? locs[t0 + x] : -1;
       }
-      s_locs[x] = loc;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int x = x0 + 32 * u + lane;
+        if (x < n) {
+          int32_t loc = v[u];
+          if (loc < -1 || (int64_t)loc >= a.rows) {
+            bad = true;
+            loc = -1;
+          }
+          s_locs[x] = loc;
+        }
+      }
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(a.err, (uint32_t)HS_DEVERR_LOC);
   }
@@ -1007,14 +1026,48 @@ __global__ void __launch_bounds__(9 * 32, 1) k_attn_mla_mma(AttnArgs a) {
       const uint32_t mask = tok_mask[b];
       const uint32_t kaddr = ring_u + ((uint32_t)b * T + (uint32_t)k_tok) * rs + k_col;
       const uint32_t vaddr = ring_u + ((uint32_t)b * T + (uint32_t)v_tok) * rs + v_col;
+      // this warp's half of the 36 k-steps of S = Q K^T; the other warp of the head tile does the rest
       float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 6
-      for (int s = 0; s < DK / 16; ++s) {
+      float s2[4] = {0.f, 0.f, 0.f, 0.f}, s3[4] = {0.f, 0.f, 0.f, 0.f};
+      const int kbeg = dh * (DK / 32);
+#pragma unroll 3
+      for (int s = 0; s < DK / 32; s += 2) {
         uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
-        ldsm_x4(qaddr + s * 32, a0, a1, a2, a3);
-        ldsm_x4(kaddr + s * 32, b0, b1, b2, b3);
+        ldsm_x4(qaddr + (kbeg + s) * 32, a0, a1, a2, a3);
+        ldsm_x4(kaddr + (kbeg + s) * 32, b0, b1, b2, b3);
         mma_bf16(s0, a0, a1, a2, a3, b0, b1);
         mma_bf16(s1, a0, a1, a2, a3, b2, b3);
+        ldsm_x4(qaddr + (kbeg + s + 1) * 32, a0, a1, a2, a3);
+        ldsm_x4(kaddr + (kbeg + s + 1) * 32, b0, b1, b2, b3);
+        mma_bf16(s2, a0, a1, a2, a3, b0, b1);
+        mma_bf16(s3, a0, a1, a2, a3, b2, b3);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        s0[i] += s2[i];
+        s1[i] += s3[i];
+      }
+      {
+        // exchange halves through shared memory; a + b == b + a, so both warps hold the same S
+        float* mine = xbuf + ((st & 1) * 8 + warp) * 256;
+        const float* other = xbuf + ((st & 1) * 8 + (warp ^ 4)) * 256;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          mine[i * 32 + lane] = s0[i];
+          mine[(4 + i) * 32 + lane] = s1[i];
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&xbar[mt]);
+        if (!mbar_wait_bounded(&xbar[mt], (uint32_t)(st & 1), &abort_flag)) {
+          *(volatile uint32_t*)&abort_flag = 1u;
+          atomicOr(a.err, (uint32_t)HS_DEVERR_TIMEOUT);
+          break;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          s0[i] += other[i * 32 + lane];
+          s1[i] += other[(4 + i) * 32 + lane];
+        }
       }
       // online softmax for rows grow (c0, c1) and grow + 8 (c2, c3)
       const int ta = 2 * tig;
@@ -1033,10 +1086,11 @@ __global__ void __launch_bounds__(9 * 32, 1) k_attn_mla_mma(AttnArgs a) {
         const float m_new = fmaxf(m_run[hr], mx);
         const bool any = m_new != -INFINITY;
         const float alpha = any ? exp2f(m_run[hr] - m_new) : 1.f;
-        p[hr][0] = any ? exp2f(x0 - m_new) : 0.f;
-        p[hr][1] = any ? exp2f(x1 - m_new) : 0.f;
-        p[hr][2] = any ? exp2f(x2 - m_new) : 0.f;
-        p[hr][3] = any ? exp2f(x3 - m_new) : 0.f;
+        // weights rounded to bf16 here, so the normaliser sums exactly what the MMA multiplies
+        p[hr][0] = any ? __bfloat162float(__float2bfloat16_rn(exp2f(x0 - m_new))) : 0.f;
+        p[hr][1] = any ? __bfloat162float(__float2bfloat16_rn(exp2f(x1 - m_new))) : 0.f;
+        p[hr][2] = any ? __bfloat162float(__float2bfloat16_rn(exp2f(x2 - m_new))) : 0.f;
+        p[hr][3] = any ? __bfloat162float(__float2bfloat16_rn(exp2f(x3 - m_new))) : 0.f;
         float ps = (p[hr][0] + p[hr][1]) + (p[hr][2] + p[hr][3]);
         ps += __shfl_xor_sync(0xffffffffu, ps, 1);
         ps += __shfl_xor_sync(0xffffffffu, ps, 2);
@@ -1048,13 +1102,9 @@ __global__ void __launch_bounds__(9 * 32, 1) k_attn_mla_mma(AttnArgs a) {
           o[n2][2 * hr + 1] *= alpha;
         }
       }
-      // P (A operand): a0 rows grow / tokens 0-7, a1 rows grow+8, a2 / a3 tokens 8-15
+      // P (A operand, bf16): a0 rows grow / tokens 0-7, a1 rows grow+8, a2 / a3 tokens 8-15
       const uint32_t h0 = pack_bf16(p[0][0], p[0][1]), h1 = pack_bf16(p[1][0], p[1][1]);
       const uint32_t h2 = pack_bf16(p[0][2], p[0][3]), h3 = pack_bf16(p[1][2], p[1][3]);
-      const uint32_t l0 = pack_bf16(p[0][0] - bf16_lo_f(h0), p[0][1] - bf16_hi_f(h0));
-      const uint32_t l1 = pack_bf16(p[1][0] - bf16_lo_f(h1), p[1][1] - bf16_hi_f(h1));
-      const uint32_t l2 = pack_bf16(p[0][2] - bf16_lo_f(h2), p[0][3] - bf16_hi_f(h2));
-      const uint32_t l3 = pack_bf16(p[1][2] - bf16_lo_f(h3), p[1][3] - bf16_hi_f(h3));
       uint32_t vm_lo = 0xffffffffu, vm_hi = 0xffffffffu;
       if (mask != 0xffffu) {
         vm_lo = (v0 ? 0x0000ffffu : 0u) | (v1 ? 0xffff0000u : 0u);
@@ -1069,9 +1119,7 @@ __global__ void __launch_bounds__(9 * 32, 1) k_attn_mla_mma(AttnArgs a) {
         b2 &= vm_lo;
         b3 &= vm_hi;
         mma_bf16(o[2 * pr], h0, h1, h2, h3, b0, b1);
-        mma_bf16(o[2 * pr], l0, l1, l2, l3, b0, b1);
         mma_bf16(o[2 * pr + 1], h0, h1, h2, h3, b2, b3);
-        mma_bf16(o[2 * pr + 1], l0, l1, l2, l3, b2, b3);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty_bar[b]);
@@ -1151,7 +1199,8 @@ bool plan_for(const hs_config* c, int num_sms, Plan* pl) {
     pl->G = kMlaHeads;
     pl->groups = 1;
     pl->T = kMmaTile;
-    pl->smem = (size_t)kMlaStages * kMmaTile * (size_t)(rec + 16) + (size_t)kMlaHeads * (576 * 2 + 16);
+    pl->smem = (size_t)kMlaStages * kMmaTile * (size_t)(rec + 16) + (size_t)kMlaHeads * (576 * 2 + 16) +
+               2 * 8 * 8 * 32 * sizeof(float);
     per_cta_wave = 1;
   } else {
     if (c->head_dim_qk != 576 || c->head_dim_v != 512) return false;

@@ -16,8 +16,11 @@ from hierarchical_kv_cache_02_gb300 import HsConfig, inputs
 
 POLICY_NAMES = {0: "lru", 1: "fifo", 2: "random", 3: "swap"}
 
-# attention tolerance: the stated bar (bf16 inputs, fp32 accumulation vs fp64) and a tighter
-# bound derived from fp32 rounding of <=576-term dot products and base-2 exponentials
+# attention tolerance: the stated bar (bf16 inputs, fp32 accumulation vs fp64), and for the GQA kernel,
+# whose probabilities enter the MMA as bf16 high part + remainder (~16 mantissa bits), a tighter bound
+# derived from fp32 rounding of <=576-term dot products and base-2 exponentials.  The shared-latent
+# kernel feeds bf16 probabilities (relative error <= 2^-9 per weight, normaliser summed over the same
+# rounded weights), which only the stated bar covers.
 ATOL_MAX, ATOL_MEAN = 2e-2, 2e-3
 ATOL_FP32 = 1e-4
 
@@ -134,8 +137,9 @@ class OracleRun:
                                 kvh, c.head_dim_qk, c.head_dim_v)
 
 
-def assert_attn_close(got, ref, what=""):
+def assert_attn_close(got, ref, what="", tight=True):
     err = np.abs(got.astype(np.float64) - ref)
     assert err.max() <= ATOL_MAX and err.mean() <= ATOL_MEAN, (what, float(err.max()), float(err.mean()))
-    assert err.max() <= ATOL_FP32, (what, "above the fp32 bound", float(err.max()))
+    if tight:
+        assert err.max() <= ATOL_FP32, (what, "above the fp32 bound", float(err.max()))
     return float(err.max())
