@@ -238,8 +238,48 @@ def run_ours(args, w, world, rank, local):
             if ev is not None:
                 ev[l][3].record(stream)
 
+    M = max(1, args.microbatches)
+    groups = [(R * g // M, R * (g + 1) // M - R * g // M) for g in range(M)]
+    streams = [torch.cuda.Stream() for _ in range(M)] if M > 1 else [stream]
+    gevs = [[[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(L)] for _ in range(M)]
+            for _ in range(K)] if M > 1 else None
+
+    def step_mb(t, i=None):
+        # micro-batches: each group of requests runs its layers in order on its own stream
+        for g, (r0, n) in enumerate(groups):
+            st = streams[g]
+            with torch.cuda.stream(st):
+                for l in range(L):
+                    if i is not None:
+                        gevs[i][g][l][0].record(st)
+                    pool.resolve_range(l, r0, wl.topk[t, l, r0:r0 + n], locs[l][r0:r0 + n],
+                                       pos=wl.pos[t, r0:r0 + n], rec=wl.app[t, l, r0:r0 + n], stream=st)
+                    if i is not None:
+                        gevs[i][g][l][1].record(st)
+                    pool.sparse_attn_range(l, r0, wl.q[t, l, r0:r0 + n], locs[l][r0:r0 + n],
+                                           outs[l][r0:r0 + n], scale=scale, stream=st)
+                    if i is not None:
+                        gevs[i][g][l][2].record(st)
+
+    def fork():
+        ev = torch.cuda.Event()
+        ev.record(stream)
+        for st in streams:
+            st.wait_event(ev)
+
+    def join():
+        for st in streams:
+            ev = torch.cuda.Event()
+            ev.record(st)
+            stream.wait_event(ev)
+
     for t in range(W):
-        step(t)
+        if M > 1:
+            fork()
+            step_mb(t)
+            join()
+        else:
+            step(t)
     torch.cuda.synchronize()
     pool.stats(reset=True)
     evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(L)] for _ in range(K)]
@@ -250,17 +290,28 @@ def run_ours(args, w, world, rank, local):
     barrier(world)
     torch.cuda.synchronize()
     start.record(stream)
-    for i in range(K):
-        step(W + i, evs[i])
+    if M > 1:
+        fork()
+        for i in range(K):
+            step_mb(W + i, i)
+        join()
+    else:
+        for i in range(K):
+            step(W + i, evs[i])
     stop.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop()
     elapsed = start.elapsed_time(stop) / 1e3
     st = pool.stats()
-    app_ms = np.array([[e[l][0].elapsed_time(e[l][1]) for l in range(L)] for e in evs])
-    res_ms = np.array([[e[l][1].elapsed_time(e[l][2]) for l in range(L)] for e in evs])
-    att_ms = np.array([[e[l][2].elapsed_time(e[l][3]) for l in range(L)] for e in evs])
+    if M > 1:
+        res_ms = np.array([[[e[g][l][0].elapsed_time(e[g][l][1]) for l in range(L)] for g in range(M)] for e in gevs])
+        att_ms = np.array([[[e[g][l][1].elapsed_time(e[g][l][2]) for l in range(L)] for g in range(M)] for e in gevs])
+        app_ms = np.zeros(1)
+    else:
+        app_ms = np.array([[e[l][0].elapsed_time(e[l][1]) for l in range(L)] for e in evs])
+        res_ms = np.array([[e[l][1].elapsed_time(e[l][2]) for l in range(L)] for e in evs])
+        att_ms = np.array([[e[l][2].elapsed_time(e[l][3]) for l in range(L)] for e in evs])
     max_elapsed = reduce_max(elapsed, world)
     units = world * K * L
     value = units / max_elapsed
@@ -274,10 +325,10 @@ def run_ours(args, w, world, rank, local):
     h2d = measure_h2d(device)
     peaks = load_peaks()
     attn_us = float(att_ms.mean() * 1e3)
-    achieved = attn_bytes_per_launch(w) / (attn_us * 1e-6) / 1e9
+    achieved = attn_bytes_per_launch(w) / M / (attn_us * 1e-6) / 1e9  # a launch covers R / M requests
     rec = record_bytes(w)
     miss_bytes = float(st["host_bytes"])
-    res_total_s = float(res_ms.sum() / 1e3)
+    res_total_s = float(res_ms.sum() / 1e3) / M  # M groups resolve side by side
     out = {
         "metric": METRIC, "value": value, "unit": "layer-steps/s", "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": max_elapsed / K * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -286,7 +337,7 @@ def run_ours(args, w, world, rank, local):
                    "buffer_slots": w["B"], "layout": "gqa" if w["layout"] == 1 else "mla", "q_heads": w["Hq"],
                    "kv_heads": w["Hkv"], "record_bytes": rec, "policy": "lru", "keep": w["keep"],
                    "recency_mean": w["mu"], "burst_every": w["burst"], "shared_history": w["shared"],
-                   "append": True, "miss_fetch": fetch, "parallelism": f"replicas{world}",
+                   "append": True, "miss_fetch": fetch, "microbatches": M, "parallelism": f"replicas{world}",
                    "l2": "inputs larger than L2 (each attention launch gathers "
                          f"{attn_bytes_per_launch(w) / 1e6:.0f} MB; a step touches {L} layers)"},
         "us_per_layer": {"total": max_elapsed / (K * L) * 1e6,
@@ -297,7 +348,7 @@ def run_ours(args, w, world, rank, local):
         "roofline": {"kernel": "sparse_attn", "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": args.traffic if args.traffic is not None else ATTN_TRAFFIC.get((args.workload, fetch)),
                      "peak_source": peaks["source"],
-                     "bytes_per_launch": attn_bytes_per_launch(w)},
+                     "bytes_per_launch": attn_bytes_per_launch(w) // M},
         "host_link": {"kernel": "resolve", "miss_bytes_per_layer": miss_bytes / (K * L),
                       "achieved_gbs": miss_bytes / res_total_s / 1e9 if res_total_s > 0 else None,
                       "h2d_copy_peak_gbs": h2d,
@@ -449,6 +500,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="gqa_b16_l32")
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling runs)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--microbatches", type=int, default=1,
+                    help="split the requests into this many groups, each running its layers on its own stream")
     ap.add_argument("--separate-append", action="store_true",
                     help="append and resolve as two launches instead of the fused hs_append_resolve")
     ap.add_argument("--fetch", choices=["auto", "resolve", "attention"], default="auto",

@@ -19,7 +19,8 @@ DEVERR_RANGE, DEVERR_DUP, DEVERR_CLOCK, DEVERR_APPEND, DEVERR_LOC, DEVERR_TIMEOU
 # every entry point include/hisparse.h declares
 EXPORTS = ("hs_record_bytes", "hs_pool_create", "hs_pool_destroy", "hs_pool_reset", "hs_prefill_write",
            "hs_append_writethrough", "hs_resolve", "hs_sparse_attn", "hs_stats", "hs_read_state",
-           "hs_read_buffer", "hs_read_history", "hs_sparse_attn_noalloc", "hs_append_resolve")
+           "hs_read_buffer", "hs_read_history", "hs_sparse_attn_noalloc", "hs_append_resolve",
+           "hs_resolve_range", "hs_sparse_attn_range")
 
 
 class hs_config(ctypes.Structure):
@@ -91,6 +92,8 @@ def load(build_if_missing: bool = False):
             "hs_read_history": (I, [P, I, I, I64, I64, P]),
             "hs_sparse_attn_noalloc": (I, [P, P, P, P, I64, F, P, P]),
             "hs_append_resolve": (I, [P, I, P, P, P, P, P]),
+            "hs_resolve_range": (I, [P, I, I, I, P, P, P, P, P]),
+            "hs_sparse_attn_range": (I, [P, I, I, I, P, P, F, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)

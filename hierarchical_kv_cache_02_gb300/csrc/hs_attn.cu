@@ -36,7 +36,8 @@ struct AttnArgs {
   int64_t rows, rec;
   int64_t kstride, vdelta;  // K of KV block g at g * kstride, V at K + vdelta (bytes)
   float qscale;             // scale * log2(e)
-  int R, Hq, k, S, chunk, groups;
+  int R, Hq, k, S, chunk, groups;  // R: requests in this launch (the grid), starting at r0
+  int r0;                   // first request: q, locs and out are indexed from it, pool state absolutely
   // fetch-in-attention mode (hot-buffer rows only): misses still to copy from the host history
   const int2* pend;         // [R][k] {position, slot} or {-1, -1}; null when nothing is pending
   uint32_t* pend_live;      // [R]
@@ -178,7 +179,7 @@ __device__ __forceinline__ void combine_heads(const AttnArgs& a, int r, int h0, 
       }
     }
     const float inv = den > 0.f ? 1.f / den : 0.f;
-    float4* out = (float4*)(a.out + ((int64_t)r * a.Hq + h) * DV);
+    float4* out = (float4*)(a.out + ((int64_t)(r - a.r0) * a.Hq + h) * DV);
 #pragma unroll
     for (int u = 0; u < DW; ++u)
       out[lane + 32 * u] = make_float4(acc[u][0] * inv, acc[u][1] * inv, acc[u][2] * inv, acc[u][3] * inv);
@@ -246,7 +247,7 @@ __device__ __forceinline__ void combine_heads_wide(const AttnArgs& a, int r, int
 #pragma unroll
   for (int x = 0; x < NH; ++x) {
     const float inv = den[x] > 0.f ? 1.f / den[x] : 0.f;
-    float4* out = (float4*)(a.out + ((int64_t)r * a.Hq + h0 + x) * DV);
+    float4* out = (float4*)(a.out + ((int64_t)(r - a.r0) * a.Hq + h0 + x) * DV);
 #pragma unroll
     for (int u = 0; u < DW; ++u)
       out[lane + 32 * u] =
@@ -275,13 +276,13 @@ __global__ void __launch_bounds__(AttnCfg<DK, DV, G, NW>::THREADS) k_attn_cc(Att
   __shared__ uint32_t abort_flag;
   __shared__ uint32_t is_last;
 
-  const int split = blockIdx.x, r = blockIdx.y, grp = blockIdx.z;
+  const int split = blockIdx.x, r = a.r0 + (int)blockIdx.y, grp = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t0 = split * a.chunk;
   const int t1 = min(a.k, t0 + a.chunk);
   const int nst = (t1 - t0 + T - 1) / T;
   const int64_t rec = a.rec;
-  const int32_t* locs = a.locs + (int64_t)r * a.k;
+  const int32_t* locs = a.locs + (int64_t)(r - a.r0) * a.k;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -351,7 +352,7 @@ __global__ void __launch_bounds__(AttnCfg<DK, DV, G, NW>::THREADS) k_attn_cc(Att
     const int hbase = g * G;
 #pragma unroll
     for (int x = 0; x < G; ++x) {
-      const uint32_t* qw = (const uint32_t*)(a.q + ((int64_t)r * a.Hq + hbase + x) * DK);
+      const uint32_t* qw = (const uint32_t*)(a.q + ((int64_t)(r - a.r0) * a.Hq + hbase + x) * DK);
 #pragma unroll
       for (int u = 0; u < DKW; ++u) {
         const uint32_t w = qw[lane + 32 * u];
@@ -541,7 +542,7 @@ __global__ void __launch_bounds__(MmaThreads<NW, NP>::value, 1) k_attn_gqa_mma(A
   __shared__ uint32_t use_pend;
   __shared__ uint32_t is_last;
 
-  const int split = blockIdx.x, r = blockIdx.y, grp = blockIdx.z;
+  const int split = blockIdx.x, r = a.r0 + (int)blockIdx.y, grp = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t0 = split * a.chunk;
   const int t1 = min(a.k, t0 + a.chunk);
@@ -549,7 +550,7 @@ __global__ void __launch_bounds__(MmaThreads<NW, NP>::value, 1) k_attn_gqa_mma(A
   const int nst = (n + T - 1) / T;
   const int64_t rec = a.rec;
   const uint32_t rs = (uint32_t)rec + 16u;  // padded row stride in shared memory
-  const int32_t* locs = a.locs + (int64_t)r * a.k;
+  const int32_t* locs = a.locs + (int64_t)(r - a.r0) * a.k;
   // shared memory: stage ring | pending slots | slot list | pending index per token | pending list
   uint8_t* ring = smem;
   uint8_t* parea = smem + (size_t)NSTAGE * T * rs;
@@ -710,7 +711,8 @@ __global__ void __launch_bounds__(MmaThreads<NW, NP>::value, 1) k_attn_gqa_mma(A
     // ---------------- consumer warps: one KV head, G query heads ----------------
     uint32_t qa[8][2];
     {
-      const uint32_t* qw = (const uint32_t*)(a.q + ((int64_t)r * a.Hq + (int64_t)g * G + (grow < G ? grow : 0)) * D);
+      const uint32_t* qw =
+          (const uint32_t*)(a.q + ((int64_t)(r - a.r0) * a.Hq + (int64_t)g * G + (grow < G ? grow : 0)) * D);
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
         qa[s][0] = grow < G ? qw[s * 8 + tig] : 0u;
@@ -905,7 +907,7 @@ __global__ void __launch_bounds__(9 * 32, 1) k_attn_mla_mma(AttnArgs a) {
   __shared__ __align__(8) uint64_t xbar[4];  // per head tile: both warps posted their half of S
   __shared__ uint32_t abort_flag;
 
-  const int split = blockIdx.x, r = blockIdx.y;
+  const int split = blockIdx.x, r = a.r0 + (int)blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t0 = split * a.chunk;
   const int t1 = min(a.k, t0 + a.chunk);
@@ -914,7 +916,7 @@ __global__ void __launch_bounds__(9 * 32, 1) k_attn_mla_mma(AttnArgs a) {
   const int64_t rec = a.rec;                 // 1152
   const uint32_t rs = (uint32_t)rec + 16u;   // padded row stride
   const uint32_t qs = (uint32_t)DK * 2u + 16u;
-  const int32_t* locs = a.locs + (int64_t)r * a.k;
+  const int32_t* locs = a.locs + (int64_t)(r - a.r0) * a.k;
   uint8_t* ring = smem;
   uint8_t* qsm = smem + (size_t)NSTAGE * T * rs;               // [64][qs]
   float* xbuf = (float*)(qsm + (size_t)kMlaHeads * qs);          // [2][8 warps][8][32] partial S
@@ -931,7 +933,7 @@ __global__ void __launch_bounds__(9 * 32, 1) k_attn_mla_mma(AttnArgs a) {
   }
   // queries of this request into shared memory (all warps, 16-byte pieces)
   {
-    const uint4* qg = (const uint4*)(a.q + (int64_t)r * kMlaHeads * DK);
+    const uint4* qg = (const uint4*)(a.q + (int64_t)(r - a.r0) * kMlaHeads * DK);
     constexpr int per_row = DK * 2 / 16;  // 72
     for (int x = threadIdx.x; x < kMlaHeads * per_row; x += blockDim.x) {
       const int h = x / per_row, c = x - h * per_row;
@@ -1147,7 +1149,7 @@ __global__ void __launch_bounds__(9 * 32, 1) k_attn_mla_mma(AttnArgs a) {
 // of the shared-latent layout are reduced by the whole GPU instead of one CTA per request.
 template <int DV>
 __global__ void __launch_bounds__(256) k_combine(AttnArgs a) {
-  const int r = blockIdx.x;
+  const int r = a.r0 + (int)blockIdx.x;
   const int h = blockIdx.y * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (h >= a.Hq) return;
@@ -1289,8 +1291,8 @@ void hs_attn_workspace(const hs_config* c, int num_sms, size_t* floats, int* max
   *floats = (size_t)c->num_requests * pl.S * c->num_q_heads * ((size_t)c->head_dim_v + 2);
 }
 
-int hs_launch_attn(hs_pool* p, int layer, const void* d_q, const int32_t* d_locs, const void* kv_base,
-                   int64_t kv_rows, float scale, float* d_out, cudaStream_t st) {
+int hs_launch_attn(hs_pool* p, int layer, int r0, int nreq, const void* d_q, const int32_t* d_locs,
+                   const void* kv_base, int64_t kv_rows, float scale, float* d_out, cudaStream_t st) {
   const hs_config& c = p->cfg;
   Plan pl;
   if (!plan_for(&c, p->num_sms, &pl)) return HS_ERR_CONFIG;
@@ -1319,7 +1321,8 @@ int hs_launch_attn(hs_pool* p, int layer, const void* d_q, const int32_t* d_locs
     a.vdelta = 0;
   }
   a.qscale = scale * kLog2e;
-  a.R = c.num_requests;
+  a.R = nreq;
+  a.r0 = r0;
   a.Hq = c.num_q_heads;
   a.k = c.top_k;
   a.S = pl.S;

@@ -96,11 +96,11 @@ __device__ __forceinline__ void hs_copy_pending(const int2* pend, int k, const u
 }
 
 // ---- launchers (defined in the kernel translation units) -------------------
-int hs_launch_resolve(hs_pool* pool, int layer, const int64_t* d_pos, const void* d_rec, const int32_t* d_topk,
-                      int32_t* d_locs, cudaStream_t st);
+int hs_launch_resolve(hs_pool* pool, int layer, int r0, int nreq, const int64_t* d_pos, const void* d_rec,
+                      const int32_t* d_topk, int32_t* d_locs, cudaStream_t st);
 int hs_launch_append(hs_pool* pool, int layer, const int64_t* d_pos, const void* d_rec, cudaStream_t st);
-int hs_launch_attn(hs_pool* pool, int layer, const void* d_q, const int32_t* d_locs, const void* kv_base,
-                   int64_t kv_rows, float scale, float* d_out, cudaStream_t st);
+int hs_launch_attn(hs_pool* pool, int layer, int r0, int nreq, const void* d_q, const int32_t* d_locs,
+                   const void* kv_base, int64_t kv_rows, float scale, float* d_out, cudaStream_t st);
 // attention workspace requirement for a configuration (floats, splits, groups)
 void hs_attn_workspace(const hs_config* cfg, int num_sms, size_t* floats, int* max_splits, int* max_groups);
 bool hs_attn_supported(const hs_config* cfg);

@@ -251,7 +251,8 @@ extern "C" int hs_resolve(hs_pool* pool, int layer, const int32_t* d_topk, int32
   if (pool == nullptr || d_topk == nullptr || d_locs == nullptr) return HS_ERR_ARG;
   if (layer < 0 || layer >= pool->cfg.num_layers) return HS_ERR_ARG;
   DeviceGuard guard(pool->device);
-  return hs_launch_resolve(pool, layer, nullptr, nullptr, d_topk, d_locs, (cudaStream_t)stream);
+  return hs_launch_resolve(pool, layer, 0, pool->cfg.num_requests, nullptr, nullptr, d_topk, d_locs,
+                           (cudaStream_t)stream);
 }
 
 extern "C" int hs_append_resolve(hs_pool* pool, int layer, const int64_t* d_pos, const void* d_rec,
@@ -260,7 +261,18 @@ extern "C" int hs_append_resolve(hs_pool* pool, int layer, const int64_t* d_pos,
     return HS_ERR_ARG;
   if (layer < 0 || layer >= pool->cfg.num_layers) return HS_ERR_ARG;
   DeviceGuard guard(pool->device);
-  return hs_launch_resolve(pool, layer, d_pos, d_rec, d_topk, d_locs, (cudaStream_t)stream);
+  return hs_launch_resolve(pool, layer, 0, pool->cfg.num_requests, d_pos, d_rec, d_topk, d_locs,
+                           (cudaStream_t)stream);
+}
+
+extern "C" int hs_resolve_range(hs_pool* pool, int layer, int r0, int nreq, const int64_t* d_pos, const void* d_rec,
+                                const int32_t* d_topk, int32_t* d_locs, void* stream) {
+  if (pool == nullptr || d_topk == nullptr || d_locs == nullptr) return HS_ERR_ARG;
+  if ((d_pos == nullptr) != (d_rec == nullptr)) return HS_ERR_ARG;
+  if (layer < 0 || layer >= pool->cfg.num_layers) return HS_ERR_ARG;
+  if (r0 < 0 || nreq < 1 || r0 + nreq > pool->cfg.num_requests) return HS_ERR_ARG;
+  DeviceGuard guard(pool->device);
+  return hs_launch_resolve(pool, layer, r0, nreq, d_pos, d_rec, d_topk, d_locs, (cudaStream_t)stream);
 }
 
 extern "C" int hs_sparse_attn(hs_pool* pool, int layer, const void* d_q, const int32_t* d_locs,
@@ -269,7 +281,17 @@ extern "C" int hs_sparse_attn(hs_pool* pool, int layer, const void* d_q, const i
   if (layer < 0 || layer >= pool->cfg.num_layers) return HS_ERR_ARG;
   if (kv_base != nullptr && (kv_rows < 1 || kv_rows > (int64_t)INT32_MAX)) return HS_ERR_ARG;
   DeviceGuard guard(pool->device);
-  return hs_launch_attn(pool, layer, d_q, d_locs, kv_base, kv_rows, scale, d_out, (cudaStream_t)stream);
+  return hs_launch_attn(pool, layer, 0, pool->cfg.num_requests, d_q, d_locs, kv_base, kv_rows, scale, d_out,
+                        (cudaStream_t)stream);
+}
+
+extern "C" int hs_sparse_attn_range(hs_pool* pool, int layer, int r0, int nreq, const void* d_q, const int32_t* d_locs,
+                                    float scale, float* d_out, void* stream) {
+  if (pool == nullptr || d_q == nullptr || d_locs == nullptr || d_out == nullptr) return HS_ERR_ARG;
+  if (layer < 0 || layer >= pool->cfg.num_layers) return HS_ERR_ARG;
+  if (r0 < 0 || nreq < 1 || r0 + nreq > pool->cfg.num_requests) return HS_ERR_ARG;
+  DeviceGuard guard(pool->device);
+  return hs_launch_attn(pool, layer, r0, nreq, d_q, d_locs, nullptr, 0, scale, d_out, (cudaStream_t)stream);
 }
 
 extern "C" int hs_stats(hs_pool* pool, hs_totals* totals, uint64_t* h_counters, uint32_t* h_errors,

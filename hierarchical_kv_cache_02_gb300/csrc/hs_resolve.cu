@@ -39,7 +39,8 @@ struct ResolveArgs {
   const int64_t* app_pos;  // fused write-through append before the resolve: [R] positions, or null
   const uint8_t* app_rec;  // [R][rec] new records
   uint8_t* hist_priv_w;    // writable view of the private host history
-  int R, L, layer, B, k, policy, log_steps, ht_bits, cs;
+  int R, L, layer, B, k, policy, log_steps, ht_bits, cs;  // R: all requests of the pool
+  int r0;  // first request of this launch: topk, locs and the append inputs are indexed from it
 };
 
 __device__ __forceinline__ uint32_t ht_hash(int32_t p, int bits) { return ((uint32_t)p * 0x9E3779B1u) >> (32 - bits); }
@@ -205,7 +206,7 @@ __device__ void select_threshold(const uint32_t* key32, const uint8_t* flag, int
 template <int NV>
 __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
-  const int r = blockIdx.x / a.cs;
+  const int r = a.r0 + (int)(blockIdx.x / a.cs);
   const int crank = blockIdx.x % a.cs;  // rank inside the cluster of this request
   const int tid = threadIdx.x;
   const int k = a.k, B = a.B;
@@ -224,8 +225,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
   __shared__ uint32_t sel[2];
   __shared__ uint32_t err_bits;
 
-  const int32_t* topk = a.topk + (int64_t)r * k;
-  int32_t* locs = a.locs + (int64_t)r * k;
+  const int32_t* topk = a.topk + (int64_t)(r - a.r0) * k;
+  int32_t* locs = a.locs + (int64_t)(r - a.r0) * k;
   int32_t* tag = a.tag + (int64_t)r * B;
   uint32_t* stamp = a.stamp + (int64_t)r * B;
   const hs_rl_state st = a.state[r];
@@ -248,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
   int64_t app_p = -1;
   uint32_t app_err = 0u;
   if (a.app_pos != nullptr) {
-    app_p = a.app_pos[r];
+    app_p = a.app_pos[r - a.r0];
     if (app_p < a.P0 || app_p < 0 || app_p >= a.C) {
       app_err = (uint32_t)HS_DEVERR_APPEND;
     } else {
@@ -462,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
     // the fused append's own writes (CTA 0): the record to the host history always; slot, tag and
     // stamp unless the resolve reuses or empties that slot now, the stamp only where no hit restamps it
     if (app_slot >= 0 && crank == 0) {
-      const uint4* src = (const uint4*)(a.app_rec + (int64_t)r * a.rec);
+      const uint4* src = (const uint4*)(a.app_rec + (int64_t)(r - a.r0) * a.rec);
       uint4* dh = (uint4*)(a.hist_priv_w + (((int64_t)r * a.L + a.layer) * a.priv_tokens + (app_p - a.P0)) * a.rec);
       // the slot is rewritten by the resolve when it is a victim now, or emptied by swap-vanilla
       // when it holds no selected position
@@ -609,9 +610,9 @@ size_t hs_resolve_smem_bytes(const hs_config* c) {
 namespace {
 
 template <int NV>
-cudaError_t launch_resolve_nv(const ResolveArgs* a, int R, int cs, size_t smem, cudaStream_t st) {
+cudaError_t launch_resolve_nv(const ResolveArgs* a, int nreq, int cs, size_t smem, cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(R * cs), 1, 1);
+  cfg.gridDim = dim3((unsigned)(nreq * cs), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
@@ -660,8 +661,8 @@ int prepare_nv(const hs_config* c, int num_sms, int* cs_out) {
 
 }  // namespace
 
-int hs_launch_resolve(hs_pool* p, int layer, const int64_t* d_pos, const void* d_rec, const int32_t* d_topk,
-                      int32_t* d_locs, cudaStream_t st) {
+int hs_launch_resolve(hs_pool* p, int layer, int r0, int nreq, const int64_t* d_pos, const void* d_rec,
+                      const int32_t* d_topk, int32_t* d_locs, cudaStream_t st) {
   const hs_config& c = p->cfg;
   const int64_t R = c.num_requests, B = c.buffer_slots;
   ResolveArgs a;
@@ -693,14 +694,15 @@ int hs_launch_resolve(hs_pool* p, int layer, const int64_t* d_pos, const void* d
   a.pend_live = p->pend_live != nullptr ? p->pend_live + (int64_t)layer * R : nullptr;
   a.app_pos = d_pos;
   a.app_rec = (const uint8_t*)d_rec;
+  a.r0 = r0;
   a.hist_priv_w = p->dmap_priv;
   const size_t smem = hs_resolve_smem_bytes(&c);
   cudaError_t e;
   switch (c.io_chunk_bytes) {
-    case 16: e = launch_resolve_nv<1>(&a, c.num_requests, a.cs, smem, st); break;
-    case 32: e = launch_resolve_nv<2>(&a, c.num_requests, a.cs, smem, st); break;
-    case 64: e = launch_resolve_nv<4>(&a, c.num_requests, a.cs, smem, st); break;
-    default: e = launch_resolve_nv<8>(&a, c.num_requests, a.cs, smem, st); break;
+    case 16: e = launch_resolve_nv<1>(&a, nreq, a.cs, smem, st); break;
+    case 32: e = launch_resolve_nv<2>(&a, nreq, a.cs, smem, st); break;
+    case 64: e = launch_resolve_nv<4>(&a, nreq, a.cs, smem, st); break;
+    default: e = launch_resolve_nv<8>(&a, nreq, a.cs, smem, st); break;
   }
   return e == cudaSuccess ? HS_OK : HS_ERR_CUDA;
 }

@@ -175,6 +175,43 @@ class HsPool:
                                                                _stream_ptr(stream, self.device)))
         return locs
 
+    def resolve_range(self, layer: int, r0: int, topk, locs=None, pos=None, rec=None, stream=None):
+        """Resolve (after the fused append when pos and rec are given) requests [r0, r0 + n), n =
+        topk.shape[0]; all tensors hold rows for those requests only."""
+        import torch
+
+        c = self.cfg
+        n, k = int(topk.shape[0]), c.top_k
+        t = _dev_tensor(topk, torch.int32, (n, k), "topk", self.device)
+        if locs is None:
+            locs = torch.empty((n, k), dtype=torch.int32, device=f"cuda:{self.device}")
+        lo = _dev_tensor(locs, torch.int32, (n, k), "locs", self.device)
+        p = rr = ctypes.c_void_p()
+        if (pos is None) != (rec is None):
+            raise ValueError("pos and rec go together")
+        if pos is not None:
+            p = _dev_tensor(pos, torch.int64, (n,), "pos", self.device)
+            rr = _dev_tensor(rec, torch.bfloat16, (n, c.record_elems), "rec", self.device)
+        _check("hs_resolve_range", self.lib.hs_resolve_range(self._h, int(layer), int(r0), n, p, rr, t, lo,
+                                                             _stream_ptr(stream, self.device)))
+        return locs
+
+    def sparse_attn_range(self, layer: int, r0: int, q, locs, out=None, scale=None, stream=None):
+        import torch
+
+        c = self.cfg
+        n = int(q.shape[0])
+        qp = _dev_tensor(q, torch.bfloat16, (n, c.num_q_heads, c.head_dim_qk), "q", self.device)
+        lp = _dev_tensor(locs, torch.int32, (n, c.top_k), "locs", self.device)
+        if out is None:
+            out = torch.empty((n, c.num_q_heads, c.head_dim_v), dtype=torch.float32, device=f"cuda:{self.device}")
+        op = _dev_tensor(out, torch.float32, (n, c.num_q_heads, c.head_dim_v), "out", self.device)
+        s = c.default_scale if scale is None else float(scale)
+        _check("hs_sparse_attn_range", self.lib.hs_sparse_attn_range(self._h, int(layer), int(r0), n, qp, lp,
+                                                                     ctypes.c_float(s), op,
+                                                                     _stream_ptr(stream, self.device)))
+        return out
+
     def sparse_attn(self, layer: int, q, locs, out=None, scale=None, kv=None, stream=None):
         """q bf16 [R][Hq][Dqk]; locs int32 [R][k]; out fp32 [R][Hq][Dv].  kv: optional resident
         bf16 [R][rows][record_elems] (then locs index its rows instead of the hot buffer)."""

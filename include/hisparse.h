@@ -19,8 +19,9 @@
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *   - Calls marked CAPTURABLE only enqueue kernels on `stream`: no allocation,
  *     no host synchronisation, no read of device data by the host.  They may be
- *     captured in a CUDA graph and replayed.  A pool is used from one stream at
- *     a time.
+ *     captured in a CUDA graph and replayed.  Each request of a pool is used from one
+ *     stream at a time; disjoint request ranges (the *_range calls) may run on
+ *     different streams concurrently.
  *   - Return value: HS_OK (0) or a negative hs_status.  Argument errors found on
  *     the host return at once and enqueue nothing.  Errors that only the device
  *     can see (a bad position in a top-k list, an append out of range, a timed
@@ -206,6 +207,20 @@ int hs_sparse_attn(hs_pool* pool, int layer, const void* d_q, const int32_t* d_l
  */
 int hs_sparse_attn_noalloc(const hs_config* cfg, const void* d_q, const int32_t* d_locs, const void* d_kv,
                            int64_t kv_rows, float scale, float* d_out, void* stream);
+
+/*
+ * Request-range forms (summary §3: requests are independent; each one's layers stay in order).
+ * They act on requests [r0, r0 + nreq) only; d_topk, d_locs, d_pos, d_rec, d_q and d_out hold
+ * rows for those requests, the first row being request r0.  hs_resolve_range fuses the
+ * write-through append when d_pos and d_rec are both non-NULL (both NULL: plain resolve).
+ * hs_sparse_attn_range reads the hot buffer.  Calls on disjoint ranges touch disjoint state, so
+ * two micro-batches of one pool can run on two streams and overlap one's host-link fetch with the
+ * other's HBM-bound attention.  Errors: HS_ERR_ARG for an empty or out-of-range span.  CAPTURABLE.
+ */
+int hs_resolve_range(hs_pool* pool, int layer, int r0, int nreq, const int64_t* d_pos, const void* d_rec,
+                     const int32_t* d_topk, int32_t* d_locs, void* stream);
+int hs_sparse_attn_range(hs_pool* pool, int layer, int r0, int nreq, const void* d_q, const int32_t* d_locs,
+                         float scale, float* d_out, void* stream);
 
 typedef struct {
   uint64_t hits;

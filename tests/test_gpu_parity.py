@@ -115,6 +115,61 @@ def test_fused_append_resolve(policy, fetch):
         run_and_compare(sc, fused=True)
 
 
+@pytest.mark.parametrize("layout", ["gqa", "gqa_fetch", "mla"])
+def test_request_ranges_on_two_streams(layout):
+    """Two micro-batches of one pool on two streams, each request's layers in order: slots,
+    state, counters and outputs are bit-identical to full-batch calls on a second pool."""
+    if layout == "mla":
+        cfg = _mla(4, 2, 3000 + 6, 256, 512, Hq=64)
+    else:
+        cfg = _gqa(4, 2, 3000 + 6, 256, 512, fetch=1 if layout == "gqa_fetch" else 0)
+    sc = Scenario(cfg, ctx0=3000, steps=6, appends=True, seed=61)
+    full, split = HsPool(cfg), HsPool(cfg)
+    prefill(full, sc)
+    prefill(split, sc)
+    R, L = cfg.num_requests, cfg.num_layers
+    groups = [(0, 1), (1, 3)]  # uneven on purpose
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for t in range(sc.steps):
+        ref = gpu_step(full, sc, t, fused=True)
+        outs = []
+        torch.cuda.synchronize()
+        for (r0, n), st in zip(groups, streams):
+            with torch.cuda.stream(st):
+                per_layer = []
+                for l in range(L):
+                    topk = torch.from_numpy(sc.trace[t, l, r0:r0 + n]).cuda()
+                    pos = torch.full((n,), sc.ctx0 + t, dtype=torch.int64, device="cuda")
+                    rec = bf16_tensor(np.stack([sc.hist[(r, l)][sc.ctx0 + t] for r in range(r0, r0 + n)]), "cuda")
+                    q = bf16_tensor(sc.q[t, l, r0:r0 + n], "cuda")
+                    locs = split.resolve_range(l, r0, topk, pos=pos, rec=rec, stream=st)
+                    out = split.sparse_attn_range(l, r0, q, locs, scale=sc.scale, stream=st)
+                    per_layer.append((locs, out, topk, pos, rec, q))
+                outs.append(per_layer)
+        torch.cuda.synchronize()
+        for gi, (r0, n) in enumerate(groups):
+            for l in range(L):
+                locs, out = outs[gi][l][0], outs[gi][l][1]
+                assert np.array_equal(locs.cpu().numpy(), ref[l][0][r0:r0 + n]), (t, l, gi)
+                assert np.array_equal(out.cpu().numpy(), ref[l][1][r0:r0 + n]), (t, l, gi)
+    for l in range(L):
+        a, b = full.read_state(l), split.read_state(l)
+        assert all(np.array_equal(x, y) for x, y in zip(a, b))
+    assert np.array_equal(full.stats()["per_rl"], split.stats()["per_rl"])
+    full.close()
+    split.close()
+
+
+def test_range_arguments_checked():
+    cfg = _gqa(2, 1, 100, 4, 8, kvh=1)
+    pool = HsPool(cfg)
+    from hierarchical_kv_cache_02_gb300 import HsError
+    topk = torch.zeros((2, 4), dtype=torch.int32, device="cuda")
+    with pytest.raises(HsError):
+        pool.resolve_range(0, 1, topk)  # requests 1..2 of a 2-request pool
+    pool.close()
+
+
 @pytest.mark.parametrize("attn_every", [2, 3])
 def test_fetch_in_attention_with_skipped_attention(attn_every):
     """Steps without attention leave copies pending; the next append (or resolve) finishes them,
