@@ -267,6 +267,7 @@ struct AttnCfg {
 
 template <int DK, int DV, int G, int NW>
 __global__ void __launch_bounds__(AttnCfg<DK, DV, G, NW>::THREADS) k_attn_cc(AttnArgs a) {
+  hs_pdl_enter();
   using C = AttnCfg<DK, DV, G, NW>;
   constexpr int T = C::T, DKW = C::DKW, DVW = C::DVW;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -528,6 +529,7 @@ struct MmaThreads {
 
 template <int G, int NW, int NSTAGE, int NP>
 __global__ void __launch_bounds__(MmaThreads<NW, NP>::value, 1) k_attn_gqa_mma(AttnArgs a) {
+  hs_pdl_enter();
   constexpr int T = kMmaTile;
   constexpr int D = 128;  // head_dim_qk == head_dim_v
   constexpr int NPB = NP > 0 ? NP : 1;
@@ -897,6 +899,7 @@ constexpr int kMlaHeads = 64;
 
 template <int NSTAGE>
 __global__ void __launch_bounds__(9 * 32, 1) k_attn_mla_mma(AttnArgs a) {
+  hs_pdl_enter();
   constexpr int T = kMmaTile;
   constexpr int NW = 8;
   constexpr int DK = 576, DV = 512;
@@ -1149,6 +1152,7 @@ __global__ void __launch_bounds__(9 * 32, 1) k_attn_mla_mma(AttnArgs a) {
 // of the shared-latent layout are reduced by the whole GPU instead of one CTA per request.
 template <int DV>
 __global__ void __launch_bounds__(256) k_combine(AttnArgs a) {
+  hs_pdl_enter();
   const int r = a.r0 + (int)blockIdx.x;
   const int h = blockIdx.y * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -1233,9 +1237,17 @@ template <typename K>
 cudaError_t launch_kernel(K kern, const AttnArgs* a, const Plan& pl, int threads, cudaStream_t st) {
   if (a == nullptr)  // preparation: raise the dynamic shared-memory limit once
     return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
-  dim3 grid(pl.S, a->R, pl.groups);
-  kern<<<grid, threads, pl.smem, st>>>(*a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(pl.S, a->R, pl.groups);
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.dynamicSmemBytes = pl.smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, *a);
 }
 
 template <int G, int NSTAGE, int NP>
@@ -1259,8 +1271,16 @@ cudaError_t dispatch(const hs_config& c, const AttnArgs* a, const Plan& pl, cuda
   if (pl.kind == 2) {
     cudaError_t e = launch_kernel(k_attn_mla_mma<kMlaStages>, a, pl, 9 * 32, st);
     if (e != cudaSuccess || a == nullptr) return e;
-    k_combine<512><<<dim3(a->R, (a->Hq + 7) / 8), 256, 0, st>>>(*a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a->R, (a->Hq + 7) / 8, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_combine<512>, *a);
   }
   if (pl.kind == 0) return launch_kernel(k_attn_cc<576, 512, 1, 8>, a, pl, AttnCfg<576, 512, 1, 8>::THREADS, st);
   switch (pl.G) {

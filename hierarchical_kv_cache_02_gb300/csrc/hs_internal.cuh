@@ -95,6 +95,14 @@ __device__ __forceinline__ void hs_copy_pending(const int2* pend, int k, const u
   }
 }
 
+// Programmatic dependent launch: the hot-path kernels are launched so that the next kernel of the
+// stream may start its launch while this one drains.  Every kernel waits for its predecessor's
+// completion (and memory) before touching global memory, then lets its own successor launch.
+__device__ __forceinline__ void hs_pdl_enter() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- launchers (defined in the kernel translation units) -------------------
 int hs_launch_resolve(hs_pool* pool, int layer, int r0, int nreq, const int64_t* d_pos, const void* d_rec,
                       const int32_t* d_topk, int32_t* d_locs, cudaStream_t st);

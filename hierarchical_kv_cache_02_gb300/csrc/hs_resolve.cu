@@ -205,6 +205,7 @@ __device__ void select_threshold(const uint32_t* key32, const uint8_t* flag, int
 
 template <int NV>
 __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
+  hs_pdl_enter();
   extern __shared__ __align__(16) uint8_t smem[];
   const int r = a.r0 + (int)(blockIdx.x / a.cs);
   const int crank = blockIdx.x % a.cs;  // rank inside the cluster of this request
@@ -524,6 +525,7 @@ struct AppendArgs {
 constexpr int kAppendThreads = 256;
 
 __global__ void __launch_bounds__(kAppendThreads) k_append(AppendArgs a) {
+  hs_pdl_enter();
   const int r = blockIdx.x, tid = threadIdx.x;
   if (a.pend != nullptr && a.pend_live[r] != 0u) {
     // finish the copies a previous resolve left pending before this append may overwrite a slot
@@ -616,13 +618,15 @@ cudaError_t launch_resolve_nv(const ResolveArgs* a, int nreq, int cs, size_t sme
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)cs;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, k_resolve<NV>, *a);
 }
 
