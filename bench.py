@@ -48,9 +48,8 @@ WORKLOADS = {
 
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one attention launch from an ncu capture of the
-# same kernel and per-launch size (profiles/k_attn_gqa_mma_gqa_b16.md); None where no capture of the
-# current kernel exists
-ATTN_TRAFFIC = {("gqa_b16_l32", "resolve"): 138.75e6}
+# same kernel and per-launch size (profiles/); None where no capture of the current kernel exists
+ATTN_TRAFFIC = {}
 
 
 def load_peaks():

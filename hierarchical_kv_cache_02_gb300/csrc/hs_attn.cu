@@ -474,13 +474,18 @@ __global__ void __launch_bounds__(AttnCfg<DK, DV, G, NW>::THREADS) k_attn_cc(Att
 
 // ---- tensor-core variant for GQA records ----------------------------------------
 //
-// A KV block (one KV head) serves G <= 8 query heads.  Per 16-token tile a consumer warp runs
-//   S[16 x 8] = Q[16 x 128] . K^T          (rows 0..G-1 are the heads, the rest zero padding)
-//   O[16 x 128] += P[16 x 16] . V[16 x 128]
-// on mma.sync m16n8k16 (bf16 in, fp32 accumulate).  K and V fragments come from the staged
-// records with ldmatrix (non-transposed for K, transposed for V); each staged record is padded
-// by 16 bytes so the eight rows of every 8x8 matrix fall in distinct banks.  P is split into a
-// bf16 high part and a bf16 remainder, two MMAs, so the probabilities keep ~16 mantissa bits.
+// A KV block (one KV head) serves G <= 8 query heads.  Per 16-token tile a consumer warp runs the
+// transposed products, so that tokens and value dims fill the MMA's 16-row side and the few heads
+// sit on its 8-column side:
+//   S^T[16 tokens x 8] = K[16 x 128] . Q^T[128 x 8]
+//   O^T[128 x 8]      += V^T[128 x 16] . P^T[16 x 8]
+// on mma.sync m16n8k16 (bf16 in, fp32 accumulate): 8 + 8 MMAs per tile.  K and V^T fragments come
+// from the staged records with ldmatrix (plain for K, transposed for V); each staged record is
+// padded by 16 bytes so the eight rows of every 8x8 matrix fall in distinct banks.  P is carried
+// as a bf16 high part plus a bf16 remainder (~16 mantissa bits): for G <= 4 the remainders ride in
+// columns G..2G-1 of the same MMA (Q^T repeats its heads there, so those columns see the same
+// scores), for G = 8 they take a second MMA.  P^T's fragments come from the score fragments by an
+// in-register 8x8 transpose (movmatrix).
 
 __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
@@ -503,14 +508,17 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
                : "r"(addr));
 }
 
+__device__ __forceinline__ uint32_t movm_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
-
-__device__ __forceinline__ float bf16_lo_f(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi_f(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
 constexpr int kMmaTile = 16;  // tokens per stage
 
@@ -579,8 +587,6 @@ __global__ void __launch_bounds__(MmaThreads<NW, NP>::value, 1) k_attn_gqa_mma(A
 
   const int g = grp * NW + warp;  // KV head of this consumer warp
   const int grow = lane >> 2, tig = lane & 3;
-  float o[16][4];
-  float m_run = -INFINITY, l_run = 0.f;
 
   __shared__ int s_npend;
   __shared__ uint32_t s_bad;
@@ -711,25 +717,33 @@ __global__ void __launch_bounds__(MmaThreads<NW, NP>::value, 1) k_attn_gqa_mma(A
     }
   } else {
     // ---------------- consumer warps: one KV head, G query heads ----------------
-    uint32_t qa[8][2];
+    // column c of the 8-wide MMA side: head c % G; the P high part if c < G, the remainder if
+    // G <= c < 2G (stuffed form, G <= 4), zero beyond
+    constexpr bool kStuff = G <= 4;
+    constexpr int kCols = kStuff ? 2 * G : G;
+    uint32_t qb[8][2];
     {
-      const uint32_t* qw =
-          (const uint32_t*)(a.q + ((int64_t)(r - a.r0) * a.Hq + (int64_t)g * G + (grow < G ? grow : 0)) * D);
+      const bool qon = grow < kCols;
+      const uint32_t* qw = (const uint32_t*)(a.q + ((int64_t)(r - a.r0) * a.Hq + (int64_t)g * G + (grow % G)) * D);
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
-        qa[s][0] = grow < G ? qw[s * 8 + tig] : 0u;
-        qa[s][1] = grow < G ? qw[s * 8 + 4 + tig] : 0u;
+        qb[s][0] = qon ? qw[s * 8 + tig] : 0u;
+        qb[s][1] = qon ? qw[s * 8 + 4 + tig] : 0u;
       }
     }
+    const int c0 = 2 * tig, c1 = 2 * tig + 1;  // this lane's columns
+    float ot[8][4];
 #pragma unroll
-    for (int n2 = 0; n2 < 16; ++n2) o[n2][0] = o[n2][1] = o[n2][2] = o[n2][3] = 0.f;
+    for (int m = 0; m < 8; ++m) ot[m][0] = ot[m][1] = ot[m][2] = ot[m][3] = 0.f;
+    float mr0 = -INFINITY, mr1 = -INFINITY;  // running max of columns c0, c1
+    float lp0 = 0.f, lp1 = 0.f;              // running sum of this lane's tokens (reduced at the end)
     const uint32_t koff = (uint32_t)(g * a.kstride);
     const uint32_t voff = koff + (uint32_t)a.vdelta;
-    // ldmatrix rows of this lane: K (non-transposed) and V (transposed) patterns
-    const int k_tok = (lane & 7) + ((lane >> 4) << 3);
-    const uint32_t k_col = (uint32_t)(((lane >> 3) & 1) * 16);
-    const int v_tok = (lane & 7) + (((lane >> 3) & 1) << 3);
-    const uint32_t v_col = (uint32_t)((lane >> 4) * 16);
+    // ldmatrix rows of this lane: K (plain) and V (transposed) patterns
+    const int k_tok = lane & 15;
+    const uint32_t k_col = (uint32_t)((lane >> 4) * 16);
+    const int v_tok = (lane & 7) + ((lane >> 4) << 3);
+    const uint32_t v_col = (uint32_t)(((lane >> 3) & 1) * 16);
     const uint32_t ring_u = smem_u32(ring), parea_u = smem_u32(parea);
     for (int st = 0; st < nst; ++st) {
       const int b = st % NSTAGE;
@@ -774,67 +788,81 @@ __global__ void __launch_bounds__(MmaThreads<NW, NP>::value, 1) k_attn_gqa_mma(A
       }
       kaddr += koff + k_col;
       vaddr += voff + v_col;
-      // S = Q K^T for tokens 0-7 (s0) and 8-15 (s1)
-      float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+      // S^T = K Q^T: even and odd k-steps in two accumulators (two independent MMA chains)
+      float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(kaddr + s * 32, b0, b1, b2, b3);
-        mma_bf16(s0, qa[s][0], 0u, qa[s][1], 0u, b0, b1);
-        mma_bf16(s1, qa[s][0], 0u, qa[s][1], 0u, b2, b3);
+      for (int s = 0; s < 8; s += 2) {
+        uint32_t x0, x1, x2, x3, y0, y1, y2, y3;
+        ldsm_x4(kaddr + s * 32, x0, x1, x2, x3);
+        ldsm_x4(kaddr + (s + 1) * 32, y0, y1, y2, y3);
+        mma_bf16(sa, x0, x1, x2, x3, qb[s][0], qb[s][1]);
+        mma_bf16(sb, y0, y1, y2, y3, qb[s + 1][0], qb[s + 1][1]);
       }
-      // online softmax on rows grow (< G): this lane holds tokens 2 tig, 2 tig + 1 (+8)
-      const int ta = 2 * tig;
-      float x0 = ((mask >> ta) & 1u) ? s0[0] * a.qscale : -INFINITY;
-      float x1 = ((mask >> (ta + 1)) & 1u) ? s0[1] * a.qscale : -INFINITY;
-      float x2 = ((mask >> (ta + 8)) & 1u) ? s1[0] * a.qscale : -INFINITY;
-      float x3 = ((mask >> (ta + 9)) & 1u) ? s1[1] * a.qscale : -INFINITY;
-      float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-      const float m_new = fmaxf(m_run, mx);
-      const bool any = m_new != -INFINITY;
-      const float alpha = any ? exp2f(m_run - m_new) : 1.f;
-      const float p0 = any ? exp2f(x0 - m_new) : 0.f;
-      const float p1 = any ? exp2f(x1 - m_new) : 0.f;
-      const float p2 = any ? exp2f(x2 - m_new) : 0.f;
-      const float p3 = any ? exp2f(x3 - m_new) : 0.f;
-      float ps = (p0 + p1) + (p2 + p3);
-      ps += __shfl_xor_sync(0xffffffffu, ps, 1);
-      ps += __shfl_xor_sync(0xffffffffu, ps, 2);
-      m_run = m_new;
-      l_run = l_run * alpha + ps;
+      // online softmax per column over tokens grow (elements 0, 1) and grow + 8 (elements 2, 3)
+      const bool va = ((mask >> grow) & 1u) != 0u, vb = ((mask >> (grow + 8)) & 1u) != 0u;
+      const float x00 = va ? (sa[0] + sb[0]) * a.qscale : -INFINITY;
+      const float x01 = va ? (sa[1] + sb[1]) * a.qscale : -INFINITY;
+      const float x10 = vb ? (sa[2] + sb[2]) * a.qscale : -INFINITY;
+      const float x11 = vb ? (sa[3] + sb[3]) * a.qscale : -INFINITY;
+      float mx0 = fmaxf(x00, x10), mx1 = fmaxf(x01, x11);
 #pragma unroll
-      for (int n2 = 0; n2 < 16; ++n2) {
-        o[n2][0] *= alpha;
-        o[n2][1] *= alpha;
+      for (int o = 4; o < 32; o <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
       }
-      // P as the A operand: high bf16 part and remainder; rows >= G stay zero
-      uint32_t ph0 = 0u, ph2 = 0u, pl0 = 0u, pl2 = 0u;
-      if (grow < G) {
-        ph0 = pack_bf16(p0, p1);
-        ph2 = pack_bf16(p2, p3);
-        pl0 = pack_bf16(p0 - bf16_lo_f(ph0), p1 - bf16_hi_f(ph0));
-        pl2 = pack_bf16(p2 - bf16_lo_f(ph2), p3 - bf16_hi_f(ph2));
+      const float mn0 = fmaxf(mr0, mx0), mn1 = fmaxf(mr1, mx1);
+      const bool any0 = mn0 != -INFINITY, any1 = mn1 != -INFINITY;
+      const float al0 = any0 ? exp2f(mr0 - mn0) : 1.f, al1 = any1 ? exp2f(mr1 - mn1) : 1.f;
+      const float p00 = any0 ? exp2f(x00 - mn0) : 0.f, p10 = any0 ? exp2f(x10 - mn0) : 0.f;
+      const float p01 = any1 ? exp2f(x01 - mn1) : 0.f, p11 = any1 ? exp2f(x11 - mn1) : 0.f;
+      mr0 = mn0;
+      mr1 = mn1;
+      lp0 = lp0 * al0 + (p00 + p10);
+      lp1 = lp1 * al1 + (p01 + p11);
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        ot[m][0] *= al0;
+        ot[m][1] *= al1;
+        ot[m][2] *= al0;
+        ot[m][3] *= al1;
       }
-      // tokens this lane holds in V fragments: 2 tig, 2 tig + 1 (and +8); zero invalid ones
+      // P^T fragments: this lane's column values as bf16 (high part / remainder / zero), then an
+      // 8x8 transpose per token half turns score-fragment order into B-operand order
+      uint32_t bh0, bh1, bl0 = 0u, bl1 = 0u;
+      {
+        const float h00 = __bfloat162float(__float2bfloat16_rn(p00)), h01 = __bfloat162float(__float2bfloat16_rn(p01));
+        const float h10 = __bfloat162float(__float2bfloat16_rn(p10)), h11 = __bfloat162float(__float2bfloat16_rn(p11));
+        if (kStuff) {
+          const float y00 = c0 < G ? h00 : (c0 < 2 * G ? p00 - h00 : 0.f);
+          const float y01 = c1 < G ? h01 : (c1 < 2 * G ? p01 - h01 : 0.f);
+          const float y10 = c0 < G ? h10 : (c0 < 2 * G ? p10 - h10 : 0.f);
+          const float y11 = c1 < G ? h11 : (c1 < 2 * G ? p11 - h11 : 0.f);
+          bh0 = movm_t(pack_bf16(y00, y01));
+          bh1 = movm_t(pack_bf16(y10, y11));
+        } else {
+          bh0 = movm_t(pack_bf16(h00, h01));
+          bh1 = movm_t(pack_bf16(h10, h11));
+          bl0 = movm_t(pack_bf16(p00 - h00, p01 - h01));
+          bl1 = movm_t(pack_bf16(p10 - h10, p11 - h11));
+        }
+      }
+      // V^T fragments hold tokens 2 tig, 2 tig + 1 (+ 8): zero the invalid ones
       uint32_t vm_lo = 0xffffffffu, vm_hi = 0xffffffffu;
       if (mask != 0xffffu) {
+        const int ta = 2 * tig;
         vm_lo = (((mask >> ta) & 1u) ? 0x0000ffffu : 0u) | (((mask >> (ta + 1)) & 1u) ? 0xffff0000u : 0u);
         vm_hi = (((mask >> (ta + 8)) & 1u) ? 0x0000ffffu : 0u) | (((mask >> (ta + 9)) & 1u) ? 0xffff0000u : 0u);
       }
 #pragma unroll
-      for (int pr = 0; pr < 8; ++pr) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(vaddr + pr * 32, b0, b1, b2, b3);
-        b0 &= vm_lo;
-        b1 &= vm_hi;
-        b2 &= vm_lo;
-        b3 &= vm_hi;
-        mma_bf16(o[2 * pr], ph0, 0u, ph2, 0u, b0, b1);
-        mma_bf16(o[2 * pr], pl0, 0u, pl2, 0u, b0, b1);
-        mma_bf16(o[2 * pr + 1], ph0, 0u, ph2, 0u, b2, b3);
-        mma_bf16(o[2 * pr + 1], pl0, 0u, pl2, 0u, b2, b3);
+      for (int m = 0; m < 8; ++m) {
+        uint32_t x0, x1, x2, x3;
+        ldsm_x4_t(vaddr + m * 32, x0, x1, x2, x3);
+        x0 &= vm_lo;
+        x1 &= vm_lo;
+        x2 &= vm_hi;
+        x3 &= vm_hi;
+        mma_bf16(ot[m], x0, x1, x2, x3, bh0, bh1);
+        if (!kStuff) mma_bf16(ot[m], x0, x1, x2, x3, bl0, bl1);
       }
       __syncwarp();
       if (lane == 0) {
@@ -847,14 +875,47 @@ __global__ void __launch_bounds__(MmaThreads<NW, NP>::value, 1) k_attn_gqa_mma(A
         }
       }
     }
-    if (!abort_flag && grow < G) {
-      const int64_t ph = ((int64_t)r * a.S + split) * a.Hq + (int64_t)g * G + grow;
-      float* po = a.part + ph * D;
+    // column sums over the lanes holding the other tokens
 #pragma unroll
-      for (int n2 = 0; n2 < 16; ++n2) *(float2*)(po + n2 * 8 + 2 * tig) = make_float2(o[n2][0], o[n2][1]);
-      if (tig == 0) {
-        a.ml[ph * 2 + 0] = m_run;
-        a.ml[ph * 2 + 1] = l_run;
+    for (int o = 4; o < 32; o <<= 1) {
+      lp0 += __shfl_xor_sync(0xffffffffu, lp0, o);
+      lp1 += __shfl_xor_sync(0xffffffffu, lp1, o);
+    }
+    // stuffed form: add each head's remainder column (G..2G-1) to its high column
+    if (kStuff) {
+      constexpr int xo = G == 4 ? 2 : 1;  // lane distance between columns c and c + G
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        if (G == 1) {
+          ot[m][0] += ot[m][1];
+          ot[m][2] += ot[m][3];
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) ot[m][e] += __shfl_xor_sync(0xffffffffu, ot[m][e], xo);
+        }
+      }
+    }
+    if (!abort_flag) {
+      // heads of this lane's columns (both columns are real heads unless G == 1)
+      const bool own0 = c0 < G, own1 = c1 < G;
+      const int64_t ph0 = ((int64_t)r * a.S + split) * a.Hq + (int64_t)g * G + c0;
+      if (own0) {
+        float* po = a.part + ph0 * D;
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+          po[16 * m + grow] = ot[m][0];
+          po[16 * m + grow + 8] = ot[m][2];
+        }
+        if (grow == 0) *(float2*)(a.ml + ph0 * 2) = make_float2(mr0, lp0);
+      }
+      if (own1) {
+        float* po = a.part + (ph0 + 1) * D;
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+          po[16 * m + grow] = ot[m][1];
+          po[16 * m + grow + 8] = ot[m][3];
+        }
+        if (grow == 0) *(float2*)(a.ml + (ph0 + 1) * 2) = make_float2(mr1, lp1);
       }
     }
   }
@@ -878,6 +939,332 @@ __global__ void __launch_bounds__(MmaThreads<NW, NP>::value, 1) k_attn_gqa_mma(A
     a.ticket[(int64_t)r * a.groups + grp] = 0u;
     if (use_pend) a.pend_live[r] = 0u;  // every split has written its fetched rows back
   }
+}
+
+// ---- GQA, one CTA per (request, KV head, split) ------------------------------------------
+//
+// Each CTA gathers one KV head's 512-byte K|V slice of every selected record (128 CTAs for 16
+// requests x 8 KV heads; a split of the top-k list only when requests x KV heads leave SMs idle).
+// Its eight consumer warps take the 16-token stages round robin (warp w: stages w, w + 8, ...),
+// each through its own kGqaStages buffers, and only compute.  Each consumer has a producer warp
+// that requests its stages in order, one 512-byte bulk copy per token (lanes 0-15), on the
+// buffer's full mbarrier, and waits for the consumer to hand the buffer back through its empty
+// mbarrier (all waits bounded).  Issuing a bulk copy costs the issuing warp tens of nanoseconds, so
+// the copies are spread over eight warps and kept out of the consumers' instruction streams.  Rows
+// of padding entries are zero-filled instead, so the math needs no masking of V.  The per-tile
+// math is the transposed MMA form described above.  At the end the consumers' (max, sum, O) are
+// merged through shared memory in warp order, so the reduction order is fixed by the top-k order
+// alone; with one split the CTA writes the final output, otherwise a partial that the last split of
+// the (request, KV head) combines.
+constexpr int kGqaWarps = 8;           // consumer warps
+constexpr int kGqaProducers = 8;       // producer warps, one per consumer
+constexpr int kGqaStages = 3;          // buffers per consumer warp
+constexpr int kGqaRow = 512 + 16;      // staged slice (K 256 B | V 256 B) + 16 B pad for ldmatrix
+
+__device__ __forceinline__ float fast_exp2(float x) {  // 2^x; -inf gives +0
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <int G>
+__global__ void __launch_bounds__((kGqaWarps + kGqaProducers) * 32, 1) k_attn_gqa(AttnArgs a) {
+  hs_pdl_enter();
+  constexpr int T = kMmaTile, D = 128, NW = kGqaWarps, NS = kGqaStages, RW = kGqaRow;
+  constexpr bool kStuff = G <= 4;        // P remainders ride in columns G..2G-1 of the same MMA
+  constexpr int kCols = kStuff ? 2 * G : G;
+  constexpr int DP = D + 4;              // row stride of the merge area (conflict-free stores)
+  static_assert(G == 1 || G == 2 || G == 4 || G == 8, "1, 2, 4 or 8 query heads per KV head");
+  static_assert(NW * kCols * DP * 4 <= NW * NS * T * RW, "merge area fits in the buffers");
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t full[NW][NS];
+  __shared__ __align__(8) uint64_t empty[NW][NS];
+  __shared__ float s_m[NW][8], s_l[NW][8], s_fin[8][2];
+  __shared__ uint32_t is_last, abort_flag;
+
+  const int split = blockIdx.x, r = a.r0 + (int)blockIdx.y, g = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int grow = lane >> 2, tig = lane & 3;
+  const int t0 = split * a.chunk;
+  const int n = min(a.k, t0 + a.chunk) - t0;
+  const int nst = (n + T - 1) / T;
+  const int64_t rec = a.rec;
+  int32_t* s_locs = (int32_t*)(smem + (size_t)NW * NS * T * RW);
+  if (threadIdx.x == 0) {
+    for (int w = 0; w < NW; ++w)
+      for (int b = 0; b < NS; ++b) {
+        mbar_init(&full[w][b], 1u);
+        mbar_init(&empty[w][b], 1u);
+      }
+    abort_flag = 0u;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  {
+    // the chunk's slot list, eight loads per thread in flight; invalid entries become padding
+    const int32_t* locs = a.locs + (int64_t)(r - a.r0) * a.k + t0;
+    constexpr int NT = (NW + kGqaProducers) * 32;
+    bool bad = false;
+    for (int x0 = 0; x0 < n; x0 += NT * 8) {
+      int32_t v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int x = x0 + u * NT + (int)threadIdx.x;
+        v[u] = x < n ? locs[x] : -1;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int x = x0 + u * NT + (int)threadIdx.x;
+        if (x < n) {
+          int32_t loc = v[u];
+          if (loc < -1 || (int64_t)loc >= a.rows) {
+            bad = true;
+            loc = -1;
+          }
+          s_locs[x] = loc;
+        }
+      }
+    }
+    if (bad) atomicOr(a.err, (uint32_t)HS_DEVERR_LOC);
+  }
+  __syncthreads();
+
+  // consumer state: columns c0, c1 of the 8-wide MMA side (head c % G; high part, remainder or
+  // zero padding, see above), running max / sum per column, O^T accumulators
+  const int c0 = 2 * tig, c1 = 2 * tig + 1;
+  float ot[8][4];
+#pragma unroll
+  for (int m = 0; m < 8; ++m) ot[m][0] = ot[m][1] = ot[m][2] = ot[m][3] = 0.f;
+  float mr0 = -INFINITY, mr1 = -INFINITY, lp0 = 0.f, lp1 = 0.f;
+
+  if (warp >= NW) {
+    // ---------------- producers: producer pw fills consumer pw's buffers, stage by stage ----------------
+    const int w = warp - NW;
+    const int ni = w < nst ? (nst - w + NW - 1) / NW : 0;
+    const uint8_t* kvg = a.kv + (int64_t)r * a.rows * rec + (int64_t)g * a.kstride;
+    bool ok = true;
+    int issued = 0;
+    for (int i = 0; i < ni; ++i) {
+      const int b = i % NS;
+      if (i >= NS) {
+        bool okw = true;
+        if (lane == 0) okw = mbar_wait_bounded(&empty[w][b], (uint32_t)((i / NS - 1) & 1), &abort_flag);
+        if (__shfl_sync(0xffffffffu, okw ? 1 : 0, 0) == 0) {
+          ok = false;
+          break;
+        }
+      }
+      const int x = (w + NW * i) * T + (lane & 15);
+      const int32_t loc = (lane < T && x < n) ? s_locs[x] : -1;
+      const uint32_t vmask = __ballot_sync(0xffffffffu, lane < T && loc >= 0);
+      uint8_t* dst = smem + ((size_t)(w * NS + b) * T) * RW;
+      if (vmask != 0xffffu) {
+        // padding rows (and the tail past the chunk) read as zeros
+        for (uint32_t zm = ~vmask & 0xffffu; zm != 0u; zm &= zm - 1u)
+          *(uint4*)(dst + (__ffs(zm) - 1) * RW + lane * 16) = make_uint4(0u, 0u, 0u, 0u);
+        __syncwarp();
+      }
+      if (lane == 0) mbar_arrive_expect_tx(&full[w][b], (uint32_t)__popc(vmask) * 512u);
+      __syncwarp();
+      if (loc >= 0) bulk_g2s(dst + lane * RW, kvg + (int64_t)loc * rec, 512u, &full[w][b]);
+      issued = i + 1;
+    }
+    if (!ok && lane == 0) {
+      *(volatile uint32_t*)&abort_flag = 1u;
+      atomicOr(a.err, (uint32_t)HS_DEVERR_TIMEOUT);
+      // let this warp's copies already requested (the last use of each buffer) land before retiring
+      volatile uint32_t never = 0u;
+      for (int i = max(0, issued - NS); i < issued; ++i)
+        mbar_wait_bounded(&full[w][i % NS], (uint32_t)((i / NS) & 1), &never);
+    }
+  } else {
+    // ---------------- consumers: warp w takes stages w, w + NW, ... ----------------
+    const int ni = warp < nst ? (nst - warp + NW - 1) / NW : 0;
+    const uint32_t ring_u = smem_u32(smem) + (uint32_t)(warp * NS * T * RW);
+    uint32_t qb[8][2];
+    {
+      const bool qon = grow < kCols;
+      const uint32_t* qw =
+          (const uint32_t*)(a.q + ((int64_t)(r - a.r0) * a.Hq + (int64_t)g * G + (grow % G)) * D);
+#pragma unroll
+      for (int s2 = 0; s2 < 8; ++s2) {
+        qb[s2][0] = qon ? qw[s2 * 8 + tig] : 0u;
+        qb[s2][1] = qon ? qw[s2 * 8 + 4 + tig] : 0u;
+      }
+    }
+    const uint32_t k_lane = (uint32_t)((lane & 15) * RW + (lane >> 4) * 16);
+    const uint32_t v_lane = (uint32_t)(((lane & 7) + ((lane >> 4) << 3)) * RW + 256 + ((lane >> 3) & 1) * 16);
+    for (int i = 0; i < ni; ++i) {
+      const int b = i % NS;
+      if (!mbar_wait_bounded(&full[warp][b], (uint32_t)((i / NS) & 1), &abort_flag)) {
+        *(volatile uint32_t*)&abort_flag = 1u;
+        atomicOr(a.err, (uint32_t)HS_DEVERR_TIMEOUT);
+        break;
+      }
+      const int xj = (warp + NW * i) * T + (lane & 15);
+      const uint32_t mask = __ballot_sync(0xffffffffu, lane < 16 && xj < n && s_locs[xj] >= 0) & 0xffffu;
+      const uint32_t base = ring_u + (uint32_t)(b * T * RW);
+      // S^T = K Q^T in two MMA chains
+      float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int s2 = 0; s2 < 8; s2 += 2) {
+        uint32_t x0, x1, x2, x3, y0, y1, y2, y3;
+        ldsm_x4(base + k_lane + s2 * 32, x0, x1, x2, x3);
+        ldsm_x4(base + k_lane + (s2 + 1) * 32, y0, y1, y2, y3);
+        mma_bf16(sa, x0, x1, x2, x3, qb[s2][0], qb[s2][1]);
+        mma_bf16(sb, y0, y1, y2, y3, qb[s2 + 1][0], qb[s2 + 1][1]);
+      }
+      const bool va = ((mask >> grow) & 1u) != 0u, vb = ((mask >> (grow + 8)) & 1u) != 0u;
+      const float x00 = va ? (sa[0] + sb[0]) * a.qscale : -INFINITY;
+      const float x01 = va ? (sa[1] + sb[1]) * a.qscale : -INFINITY;
+      const float x10 = vb ? (sa[2] + sb[2]) * a.qscale : -INFINITY;
+      const float x11 = vb ? (sa[3] + sb[3]) * a.qscale : -INFINITY;
+      float mx0 = fmaxf(x00, x10), mx1 = fmaxf(x01, x11);
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+      }
+      const float mn0 = fmaxf(mr0, mx0), mn1 = fmaxf(mr1, mx1);
+      // a column with no valid token yet keeps max -inf: its weights are zero, its scale one
+      const float ms0 = mn0 == -INFINITY ? 0.f : mn0, ms1 = mn1 == -INFINITY ? 0.f : mn1;
+      const float p00 = fast_exp2(x00 - ms0), p10 = fast_exp2(x10 - ms0);
+      const float p01 = fast_exp2(x01 - ms1), p11 = fast_exp2(x11 - ms1);
+      if (__any_sync(0xffffffffu, mn0 != mr0 || mn1 != mr1)) {
+        const float al0 = fast_exp2(mr0 - ms0), al1 = fast_exp2(mr1 - ms1);
+        lp0 *= al0;
+        lp1 *= al1;
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+          ot[m][0] *= al0;
+          ot[m][1] *= al1;
+          ot[m][2] *= al0;
+          ot[m][3] *= al1;
+        }
+      }
+      mr0 = mn0;
+      mr1 = mn1;
+      lp0 += p00 + p10;
+      lp1 += p01 + p11;
+      uint32_t bh0, bh1, bl0 = 0u, bl1 = 0u;
+      {
+        const float h00 = __bfloat162float(__float2bfloat16_rn(p00)), h01 = __bfloat162float(__float2bfloat16_rn(p01));
+        const float h10 = __bfloat162float(__float2bfloat16_rn(p10)), h11 = __bfloat162float(__float2bfloat16_rn(p11));
+        if (kStuff) {
+          const float y00 = c0 < G ? h00 : (c0 < 2 * G ? p00 - h00 : 0.f);
+          const float y01 = c1 < G ? h01 : (c1 < 2 * G ? p01 - h01 : 0.f);
+          const float y10 = c0 < G ? h10 : (c0 < 2 * G ? p10 - h10 : 0.f);
+          const float y11 = c1 < G ? h11 : (c1 < 2 * G ? p11 - h11 : 0.f);
+          bh0 = movm_t(pack_bf16(y00, y01));
+          bh1 = movm_t(pack_bf16(y10, y11));
+        } else {
+          bh0 = movm_t(pack_bf16(h00, h01));
+          bh1 = movm_t(pack_bf16(h10, h11));
+          bl0 = movm_t(pack_bf16(p00 - h00, p01 - h01));
+          bl1 = movm_t(pack_bf16(p10 - h10, p11 - h11));
+        }
+      }
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        uint32_t x0, x1, x2, x3;
+        ldsm_x4_t(base + v_lane + m * 32, x0, x1, x2, x3);
+        mma_bf16(ot[m], x0, x1, x2, x3, bh0, bh1);
+        if (!kStuff) mma_bf16(ot[m], x0, x1, x2, x3, bl0, bl1);
+      }
+      __syncwarp();  // every lane is done with buffer b before it is handed back
+      if (lane == 0) mbar_arrive(&empty[warp][b]);
+    }
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      lp0 += __shfl_xor_sync(0xffffffffu, lp0, o);
+      lp1 += __shfl_xor_sync(0xffffffffu, lp1, o);
+    }
+    if (grow == 0) {
+      if (c0 < G) {
+        s_m[warp][c0] = mr0;
+        s_l[warp][c0] = lp0;
+      }
+      if (c1 < G) {
+        s_m[warp][c1] = mr1;
+        s_l[warp][c1] = lp1;
+      }
+    }
+  }
+  __syncthreads();  // (A) stats in place, no buffer read any more
+  if (abort_flag) return;
+  // merge: each consumer column scaled by exp2(m_w - M) into red[w][c][.]; the producer warp's
+  // lanes h < G compute the per-head max M and normaliser
+  float* red = (float*)smem;
+  if (warp < NW) {
+    float M0 = -INFINITY, M1 = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      M0 = fmaxf(M0, s_m[w][c0 % G]);
+      M1 = fmaxf(M1, s_m[w][c1 % G]);
+    }
+    const float w0 = mr0 == -INFINITY ? 0.f : exp2f(mr0 - M0);
+    const float w1 = mr1 == -INFINITY ? 0.f : exp2f(mr1 - M1);
+    if (c0 < kCols) {
+      float* rw = red + ((size_t)warp * kCols + c0) * DP;
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        rw[16 * m + grow] = ot[m][0] * w0;
+        rw[16 * m + grow + 8] = ot[m][2] * w0;
+      }
+    }
+    if (c1 < kCols) {
+      float* rw = red + ((size_t)warp * kCols + c1) * DP;
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        rw[16 * m + grow] = ot[m][1] * w1;
+        rw[16 * m + grow + 8] = ot[m][3] * w1;
+      }
+    }
+  } else if (warp == NW && lane < G) {
+    float M = -INFINITY, den = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, s_m[w][lane]);
+#pragma unroll
+    for (int w = 0; w < NW; ++w) den += s_m[w][lane] == -INFINITY ? 0.f : s_l[w][lane] * exp2f(s_m[w][lane] - M);
+    s_fin[lane][0] = M;
+    s_fin[lane][1] = den;
+  }
+  __syncthreads();  // (B)
+  // sum over warps in warp order (high part, then remainder); one thread per (head, value)
+  for (int e = (int)threadIdx.x; e < G * D; e += (NW + kGqaProducers) * 32) {
+    const int h = e / D, d = e % D;
+    float acc = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      acc += red[((size_t)w * kCols + h) * DP + d];
+      if (kStuff) acc += red[((size_t)w * kCols + h + G) * DP + d];
+    }
+    const float den = s_fin[h][1];
+    const int hq = g * G + h;
+    if (a.S == 1) {
+      a.out[((int64_t)(r - a.r0) * a.Hq + hq) * D + d] = den > 0.f ? acc / den : 0.f;
+    } else {
+      const int64_t ph = ((int64_t)r * a.S + split) * a.Hq + hq;
+      a.part[ph * D + d] = acc;
+      if (d == 0) *(float2*)(a.ml + ph * 2) = make_float2(s_fin[h][0], den);
+    }
+  }
+  if (a.S == 1) return;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const uint32_t t = atomicAdd(&a.ticket[(int64_t)r * a.groups + g], 1u);
+    is_last = (t == (uint32_t)(a.S - 1)) ? 1u : 0u;
+  }
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  if (warp == 0) {
+    if (a.S <= 32)
+      combine_heads_wide<D, G>(a, r, g * G, lane);
+    else
+      combine_heads<D>(a, r, g * G, G, lane);
+  }
+  if (threadIdx.x == 0) a.ticket[(int64_t)r * a.groups + g] = 0u;
 }
 
 // ---- tensor-core variant for shared-latent (MLA) records ---------------------------------
@@ -1166,13 +1553,12 @@ __global__ void __launch_bounds__(256) k_combine(AttnArgs a) {
 // ---- dispatch ----------------------------------------------------------------
 
 struct Plan {
-  int kind;  // 0: CUDA-core kernel (shared-latent records), 1: tensor-core GQA kernel
+  int kind;  // 0: CUDA-core shared-latent, 1: GQA per KV head, 2: shared-latent mma, 3: GQA with the miss fetch
   int NW, G, T, groups, S, chunk;
   int fetch;  // 1: the GQA kernel fetches pending rows from the host (2 ring stages + kPendSlots)
   size_t smem;
 };
 
-constexpr int kMmaStages = 3;
 constexpr int kMmaStagesFetch = 2;
 constexpr int kPendSlots = 16;
 
@@ -1183,21 +1569,29 @@ bool plan_for(const hs_config* c, int num_sms, Plan* pl) {
     if (c->head_dim_qk != 128 || c->head_dim_v != 128) return false;
     const int G = c->num_q_heads / c->num_kv_heads;
     if (G != 1 && G != 2 && G != 4 && G != 8) return false;
-    int NW = c->num_kv_heads;
-    if (NW > 8) {
-      if (NW % 8 != 0) return false;
-      NW = 8;
-    }
-    if (NW != 1 && NW != 2 && NW != 4 && NW != 8) return false;
-    pl->kind = 1;
-    pl->NW = NW;
     pl->G = G;
-    pl->groups = c->num_kv_heads / NW;
     pl->T = kMmaTile;
-    pl->fetch = c->fetch_in_attention != 0;
-    pl->smem = pl->fetch ? (size_t)(kMmaStagesFetch * kMmaTile + kPendSlots) * (size_t)(rec + 16)
-                         : (size_t)kMmaStages * kMmaTile * (size_t)(rec + 16);  // + the chunk lists, below
-    per_cta_wave = 1;  // one CTA per SM: the ring holds most of the shared memory
+    if (c->fetch_in_attention != 0) {
+      // misses copied inside the attention: all KV heads of a request in one CTA
+      int NW = c->num_kv_heads;
+      if (NW > 8) {
+        if (NW % 8 != 0) return false;
+        NW = 8;
+      }
+      if (NW != 1 && NW != 2 && NW != 4 && NW != 8) return false;
+      pl->kind = 3;
+      pl->NW = NW;
+      pl->groups = c->num_kv_heads / NW;
+      pl->fetch = 1;
+      pl->smem = (size_t)(kMmaStagesFetch * kMmaTile + kPendSlots) * (size_t)(rec + 16);
+    } else {
+      pl->kind = 1;
+      pl->NW = kGqaWarps;
+      pl->groups = c->num_kv_heads;  // one KV head per CTA
+      pl->fetch = 0;
+      pl->smem = (size_t)kGqaWarps * kGqaStages * kMmaTile * kGqaRow;
+    }
+    per_cta_wave = 1;  // one CTA per SM: the staging buffers hold most of the shared memory
   } else if (c->head_dim_qk == 576 && c->head_dim_v == 512 && c->num_q_heads == kMlaHeads) {
     pl->kind = 2;
     pl->fetch = 0;
@@ -1228,7 +1622,8 @@ bool plan_for(const hs_config* c, int num_sms, Plan* pl) {
   chunk = (chunk + pl->T - 1) / pl->T * pl->T;
   pl->chunk = chunk;
   pl->S = (c->top_k + chunk - 1) / chunk;
-  if (pl->kind == 1) pl->smem += (size_t)chunk * 16;  // slot list, pending index, pending list
+  if (pl->kind == 1) pl->smem += (size_t)chunk * 4;   // slot list
+  if (pl->kind == 3) pl->smem += (size_t)chunk * 16;  // slot list, pending index, pending list
   if (pl->kind == 2) pl->smem += (size_t)chunk * 4;   // slot list
   return pl->smem <= 220 * 1024;
 }
@@ -1261,11 +1656,6 @@ cudaError_t launch_gqa_nw2(const AttnArgs* a, const Plan& pl, cudaStream_t st) {
   }
 }
 
-template <int G>
-cudaError_t launch_gqa_nw(const AttnArgs* a, const Plan& pl, cudaStream_t st) {
-  return pl.fetch ? launch_gqa_nw2<G, kMmaStagesFetch, kPendSlots>(a, pl, st)
-                  : launch_gqa_nw2<G, kMmaStages, 0>(a, pl, st);
-}
 
 cudaError_t dispatch(const hs_config& c, const AttnArgs* a, const Plan& pl, cudaStream_t st) {
   if (pl.kind == 2) {
@@ -1283,19 +1673,29 @@ cudaError_t dispatch(const hs_config& c, const AttnArgs* a, const Plan& pl, cuda
     return cudaLaunchKernelEx(&cfg, k_combine<512>, *a);
   }
   if (pl.kind == 0) return launch_kernel(k_attn_cc<576, 512, 1, 8>, a, pl, AttnCfg<576, 512, 1, 8>::THREADS, st);
+  if (pl.kind == 1) {
+    switch (pl.G) {
+      case 1: return launch_kernel(k_attn_gqa<1>, a, pl, (kGqaWarps + kGqaProducers) * 32, st);
+      case 2: return launch_kernel(k_attn_gqa<2>, a, pl, (kGqaWarps + kGqaProducers) * 32, st);
+      case 4: return launch_kernel(k_attn_gqa<4>, a, pl, (kGqaWarps + kGqaProducers) * 32, st);
+      default: return launch_kernel(k_attn_gqa<8>, a, pl, (kGqaWarps + kGqaProducers) * 32, st);
+    }
+  }
   switch (pl.G) {
-    case 1: return launch_gqa_nw<1>(a, pl, st);
-    case 2: return launch_gqa_nw<2>(a, pl, st);
-    case 4: return launch_gqa_nw<4>(a, pl, st);
-    default: return launch_gqa_nw<8>(a, pl, st);
+    case 1: return launch_gqa_nw2<1, kMmaStagesFetch, kPendSlots>(a, pl, st);
+    case 2: return launch_gqa_nw2<2, kMmaStagesFetch, kPendSlots>(a, pl, st);
+    case 4: return launch_gqa_nw2<4, kMmaStagesFetch, kPendSlots>(a, pl, st);
+    default: return launch_gqa_nw2<8, kMmaStagesFetch, kPendSlots>(a, pl, st);
   }
 }
 
 }  // namespace
 
 bool hs_attn_can_fetch(const hs_config* c) {
+  hs_config f = *c;
+  f.fetch_in_attention = 1;
   Plan pl;
-  return plan_for(c, 152, &pl) && pl.kind == 1 && pl.groups == 1;
+  return plan_for(&f, 152, &pl) && pl.kind == 3 && pl.groups == 1;
 }
 
 bool hs_attn_supported(const hs_config* c) {
