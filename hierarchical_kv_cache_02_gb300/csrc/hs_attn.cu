@@ -31,7 +31,7 @@ struct AttnArgs {
   float* out;            // [R][Hq][DV]
   float* part;           // [R][S][Hq][DV]
   float* ml;             // [R][S][Hq][2]
-  uint32_t* ticket;      // [R][groups]
+  uint32_t* ticket;      // [R][groups + 1]: split tickets per group, then the pending-list count
   uint32_t* err;
   int64_t rows, rec;
   int64_t kstride, vdelta;  // K of KV block g at g * kstride, V at K + vdelta (bytes)
@@ -457,7 +457,7 @@ __global__ void __launch_bounds__(AttnCfg<DK, DV, G, NW>::THREADS) k_attn_cc(Att
   __syncthreads();
   if (abort_flag) return;
   if (threadIdx.x == 0) {
-    const uint32_t t = atomicAdd(&a.ticket[(int64_t)r * a.groups + grp], 1u);
+    const uint32_t t = atomicAdd(&a.ticket[(int64_t)r * (a.groups + 1) + grp], 1u);
     is_last = (t == (uint32_t)(a.S - 1)) ? 1u : 0u;
   }
   __syncthreads();
@@ -469,7 +469,7 @@ __global__ void __launch_bounds__(AttnCfg<DK, DV, G, NW>::THREADS) k_attn_cc(Att
     else
       combine_heads<DV>(a, r, g * G, G, lane);
   }
-  if (threadIdx.x == 0) a.ticket[(int64_t)r * a.groups + grp] = 0u;
+  if (threadIdx.x == 0) a.ticket[(int64_t)r * (a.groups + 1) + grp] = 0u;
 }
 
 // ---- tensor-core variant for GQA records ----------------------------------------
@@ -522,425 +522,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 constexpr int kMmaTile = 16;  // tokens per stage
 
-// NP > 0 (fetch-in-attention mode): rows the resolve left in the host history are copied by
-// kFetchWarps extra warps (16-byte loads through the mapped history, round-robin over the pending
-// rows) into NP dedicated pending slots, as far ahead of their use as the slots allow (each slot
-// has its own full/empty mbarriers), while the producer keeps gathering the resident rows from HBM
-// into the stage ring; the consumers read either kind of row through per-lane ldmatrix addresses
-// and write the fetched rows back to their hot-buffer slots.
-constexpr int kFetchWarps = 2;
-
-template <int NW, int NP>
-struct MmaThreads {
-  static constexpr int value = (NW + 1 + (NP > 0 ? kFetchWarps : 0)) * 32;
-};
-
-template <int G, int NW, int NSTAGE, int NP>
-__global__ void __launch_bounds__(MmaThreads<NW, NP>::value, 1) k_attn_gqa_mma(AttnArgs a) {
-  hs_pdl_enter();
-  constexpr int T = kMmaTile;
-  constexpr int D = 128;  // head_dim_qk == head_dim_v
-  constexpr int NPB = NP > 0 ? NP : 1;
-  static_assert(G >= 1 && G <= 8, "up to 8 query heads per KV head");
-  extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ __align__(8) uint64_t full_bar[NSTAGE];
-  __shared__ __align__(8) uint64_t empty_bar[NSTAGE];
-  __shared__ __align__(8) uint64_t pfull_bar[NPB];
-  __shared__ __align__(8) uint64_t pempty_bar[NPB];
-  __shared__ uint32_t tok_mask[NSTAGE];
-  __shared__ uint32_t abort_flag;
-  __shared__ uint32_t use_pend;
-  __shared__ uint32_t is_last;
-
-  const int split = blockIdx.x, r = a.r0 + (int)blockIdx.y, grp = blockIdx.z;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t0 = split * a.chunk;
-  const int t1 = min(a.k, t0 + a.chunk);
-  const int n = t1 - t0;
-  const int nst = (n + T - 1) / T;
-  const int64_t rec = a.rec;
-  const uint32_t rs = (uint32_t)rec + 16u;  // padded row stride in shared memory
-  const int32_t* locs = a.locs + (int64_t)(r - a.r0) * a.k;
-  // shared memory: stage ring | pending slots | slot list | pending index per token | pending list
-  uint8_t* ring = smem;
-  uint8_t* parea = smem + (size_t)NSTAGE * T * rs;
-  int32_t* s_locs = (int32_t*)(parea + (size_t)NP * rs);
-  int32_t* s_pidx = s_locs + a.chunk;  // pending index of a token (order among pending rows), or -1
-  int32_t* s_ppos = s_pidx + a.chunk;  // host position of the pi-th pending row
-  int32_t* s_ptok = s_ppos + a.chunk;  // token (chunk index) of the pi-th pending row
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < NSTAGE; ++s) {
-      mbar_init(&full_bar[s], 1u);
-      mbar_init(&empty_bar[s], (uint32_t)NW);
-    }
-    for (int s = 0; s < NPB; ++s) {
-      mbar_init(&pfull_bar[s], 1u);  // the fetch warp that filled the slot
-      mbar_init(&pempty_bar[s], (uint32_t)NW);
-    }
-    abort_flag = 0u;
-    use_pend = (NP > 0 && a.pend != nullptr && a.pend_live[r] != 0u) ? 1u : 0u;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  __syncthreads();
-  const bool pend_on = use_pend != 0u;
-
-  const int g = grp * NW + warp;  // KV head of this consumer warp
-  const int grow = lane >> 2, tig = lane & 3;
-
-  __shared__ int s_npend;
-  __shared__ uint32_t s_bad;
-  if (warp == NW) {
-    // slot list (and pending list) of the chunk, read once with eight loads per lane in flight
-    const int2* pend = pend_on ? a.pend + (int64_t)r * a.k : nullptr;
-    uint32_t bad = 0u;
-    int npend = 0;
-    for (int x0 = 0; x0 < n; x0 += 32 * 8) {
-      int32_t v[8], pp[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int x = x0 + 32 * u + lane;
-        v[u] = x < n ? locs[t0 + x] : -1;
-        pp[u] = (pend_on && x < n) ? pend[t0 + x].x : -1;
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int x = x0 + 32 * u + lane;
-        int32_t loc = v[u];
-        if (loc < -1 || (int64_t)loc >= a.rows) {
-          bad = 1u;
-          loc = -1;
-        }
-        const bool isp = x < n && loc >= 0 && pp[u] >= 0;
-        const uint32_t bal = __ballot_sync(0xffffffffu, isp);
-        const int pi = npend + __popc(bal & ((1u << lane) - 1u));
-        if (x < n) {
-          s_locs[x] = loc;
-          s_pidx[x] = isp ? pi : -1;
-        }
-        if (isp) {
-          s_ppos[pi] = pp[u];
-          s_ptok[pi] = x;
-        }
-        npend += __popc(bal);
-      }
-    }
-    if (lane == 0) {
-      s_npend = npend;
-      s_bad = __any_sync(0xffffffffu, bad) ? 1u : 0u;
-    } else {
-      __any_sync(0xffffffffu, bad);
-    }
-  }
-  __syncthreads();  // lists are visible to every role
-  if (warp == NW) {
-    // ---------------- producer warp: resident rows, HBM -> stage ring ----------------
-    bool ok = true;
-    int issued = 0;
-    for (int st = 0; ok && st < nst; ++st) {
-      const int b = st % NSTAGE;
-      if (st >= NSTAGE) {
-        bool w = true;
-        if (lane == 0) w = mbar_wait_bounded(&empty_bar[b], (uint32_t)((st / NSTAGE - 1) & 1), &abort_flag);
-        if (__shfl_sync(0xffffffffu, w ? 1 : 0, 0) == 0) {
-          ok = false;
-          break;
-        }
-      }
-      const int j = lane;
-      const int x = st * T + j;
-      const int32_t loc = (j < T && x < n) ? s_locs[x] : -1;
-      const bool resident = loc >= 0 && (j < T && x < n) && s_pidx[x] < 0;
-      const uint32_t mask = __ballot_sync(0xffffffffu, loc >= 0);
-      const uint32_t rmask = __ballot_sync(0xffffffffu, resident);
-      if (lane == 0) {
-        tok_mask[b] = mask;
-        mbar_arrive_expect_tx(&full_bar[b], (uint32_t)__popc(rmask) * (uint32_t)rec);
-      }
-      __syncwarp();
-      if (resident)
-        bulk_g2s(ring + ((size_t)b * T + j) * rs, a.kv + ((int64_t)r * a.rows + loc) * rec, (uint32_t)rec,
-                 &full_bar[b]);
-      issued = st + 1;
-    }
-    if (!ok && lane == 0) {
-      *(volatile uint32_t*)&abort_flag = 1u;
-      atomicOr(a.err, (uint32_t)HS_DEVERR_TIMEOUT);
-    }
-    if (s_bad && lane == 0) atomicOr(a.err, (uint32_t)HS_DEVERR_LOC);
-    if (abort_flag && lane == 0) {
-      // let copies already issued land before the CTA can retire
-      for (int st = max(0, issued - NSTAGE); st < issued; ++st) {
-        volatile uint32_t never = 0u;
-        mbar_wait_bounded(&full_bar[st % NSTAGE], (uint32_t)((st / NSTAGE) & 1), &never);
-      }
-    }
-  } else if (warp > NW) {
-    // ---------------- fetch warps: pending rows, host history -> pending slots ----------------
-    if (NP > 0 && pend_on) {
-      const int f = warp - NW - 1;
-      const int npend = s_npend;
-      const int nv = (int)(rec / 16);
-      for (int pi = f; pi < npend; pi += kFetchWarps) {
-        const int sl = pi % NPB;
-        if (pi >= NPB) {
-          // the slot's previous row has a smaller pending index: consumers can always free it
-          bool w = true;
-          if (lane == 0) w = mbar_wait_bounded(&pempty_bar[sl], (uint32_t)((pi / NPB - 1) & 1), &abort_flag);
-          if (__shfl_sync(0xffffffffu, w ? 1 : 0, 0) == 0) {
-            if (lane == 0) {
-              *(volatile uint32_t*)&abort_flag = 1u;
-              atomicOr(a.err, (uint32_t)HS_DEVERR_TIMEOUT);
-            }
-            break;
-          }
-        }
-        const uint4* src = (const uint4*)hs_hist_addr(a.hist_shared, a.hist_priv, a.P0, a.priv_tokens, rec, a.L, r,
-                                                      a.layer, s_ppos[pi]);
-        uint4* dst = (uint4*)(parea + (size_t)sl * rs);
-        for (int v0 = 0; v0 < nv; v0 += 32 * 8) {  // eight 16-byte loads per lane in flight
-          uint4 t[8];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int vv = v0 + 32 * u + lane;
-            if (vv < nv) t[u] = __ldg(src + vv);
-          }
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int vv = v0 + 32 * u + lane;
-            if (vv < nv) dst[vv] = t[u];
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&pfull_bar[sl]);
-      }
-    }
-  } else {
-    // ---------------- consumer warps: one KV head, G query heads ----------------
-    // column c of the 8-wide MMA side: head c % G; the P high part if c < G, the remainder if
-    // G <= c < 2G (stuffed form, G <= 4), zero beyond
-    constexpr bool kStuff = G <= 4;
-    constexpr int kCols = kStuff ? 2 * G : G;
-    uint32_t qb[8][2];
-    {
-      const bool qon = grow < kCols;
-      const uint32_t* qw = (const uint32_t*)(a.q + ((int64_t)(r - a.r0) * a.Hq + (int64_t)g * G + (grow % G)) * D);
-#pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        qb[s][0] = qon ? qw[s * 8 + tig] : 0u;
-        qb[s][1] = qon ? qw[s * 8 + 4 + tig] : 0u;
-      }
-    }
-    const int c0 = 2 * tig, c1 = 2 * tig + 1;  // this lane's columns
-    float ot[8][4];
-#pragma unroll
-    for (int m = 0; m < 8; ++m) ot[m][0] = ot[m][1] = ot[m][2] = ot[m][3] = 0.f;
-    float mr0 = -INFINITY, mr1 = -INFINITY;  // running max of columns c0, c1
-    float lp0 = 0.f, lp1 = 0.f;              // running sum of this lane's tokens (reduced at the end)
-    const uint32_t koff = (uint32_t)(g * a.kstride);
-    const uint32_t voff = koff + (uint32_t)a.vdelta;
-    // ldmatrix rows of this lane: K (plain) and V (transposed) patterns
-    const int k_tok = lane & 15;
-    const uint32_t k_col = (uint32_t)((lane >> 4) * 16);
-    const int v_tok = (lane & 7) + ((lane >> 4) << 3);
-    const uint32_t v_col = (uint32_t)(((lane >> 3) & 1) * 16);
-    const uint32_t ring_u = smem_u32(ring), parea_u = smem_u32(parea);
-    for (int st = 0; st < nst; ++st) {
-      const int b = st % NSTAGE;
-      if (!mbar_wait_bounded(&full_bar[b], (uint32_t)((st / NSTAGE) & 1), &abort_flag)) {
-        *(volatile uint32_t*)&abort_flag = 1u;
-        atomicOr(a.err, (uint32_t)HS_DEVERR_TIMEOUT);
-        break;
-      }
-      const uint32_t mask = tok_mask[b];
-      uint32_t kaddr = ring_u + ((uint32_t)b * T + (uint32_t)k_tok) * rs;
-      uint32_t vaddr = ring_u + ((uint32_t)b * T + (uint32_t)v_tok) * rs;
-      uint32_t pmask = 0u;
-      if (NP > 0 && pend_on) {
-        // pending rows of this stage: wait for their slots, point this lane's rows at them
-        const int xj = st * T + (lane & 15);
-        const int pj = (xj < n) ? s_pidx[xj] : -1;
-        pmask = __ballot_sync(0xffffffffu, lane < 16 && pj >= 0);
-        bool okp = true;
-        for (uint32_t pm = pmask; pm != 0u && okp; pm &= pm - 1u) {
-          const int jj = __ffs(pm) - 1;
-          const int pi = __shfl_sync(0xffffffffu, pj, jj);
-          okp = mbar_wait_bounded(&pfull_bar[pi % NPB], (uint32_t)((pi / NPB) & 1), &abort_flag);
-        }
-        if (!okp) {
-          *(volatile uint32_t*)&abort_flag = 1u;
-          atomicOr(a.err, (uint32_t)HS_DEVERR_TIMEOUT);
-          break;
-        }
-        const int xk = st * T + k_tok, xv = st * T + v_tok;
-        const int pk = xk < n ? s_pidx[xk] : -1, pv = xv < n ? s_pidx[xv] : -1;
-        if (pk >= 0) kaddr = parea_u + (uint32_t)(pk % NPB) * rs;
-        if (pv >= 0) vaddr = parea_u + (uint32_t)(pv % NPB) * rs;
-        // fetched rows go back to their hot-buffer slots: each warp writes a 1/NW share of each
-        for (uint32_t pm = pmask; pm != 0u; pm &= pm - 1u) {
-          const int jj = __ffs(pm) - 1;
-          const int pi = __shfl_sync(0xffffffffu, pj, jj);
-          const int32_t slot = s_locs[st * T + jj];
-          const uint4* srow = (const uint4*)(parea + (size_t)(pi % NPB) * rs);
-          uint4* gdst = (uint4*)(a.buf_w + ((int64_t)r * a.rows + slot) * rec);
-          for (int vv = warp * 32 + lane; vv < (int)(rec / 16); vv += NW * 32) gdst[vv] = srow[vv];
-        }
-      }
-      kaddr += koff + k_col;
-      vaddr += voff + v_col;
-      // S^T = K Q^T: even and odd k-steps in two accumulators (two independent MMA chains)
-      float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int s = 0; s < 8; s += 2) {
-        uint32_t x0, x1, x2, x3, y0, y1, y2, y3;
-        ldsm_x4(kaddr + s * 32, x0, x1, x2, x3);
-        ldsm_x4(kaddr + (s + 1) * 32, y0, y1, y2, y3);
-        mma_bf16(sa, x0, x1, x2, x3, qb[s][0], qb[s][1]);
-        mma_bf16(sb, y0, y1, y2, y3, qb[s + 1][0], qb[s + 1][1]);
-      }
-      // online softmax per column over tokens grow (elements 0, 1) and grow + 8 (elements 2, 3)
-      const bool va = ((mask >> grow) & 1u) != 0u, vb = ((mask >> (grow + 8)) & 1u) != 0u;
-      const float x00 = va ? (sa[0] + sb[0]) * a.qscale : -INFINITY;
-      const float x01 = va ? (sa[1] + sb[1]) * a.qscale : -INFINITY;
-      const float x10 = vb ? (sa[2] + sb[2]) * a.qscale : -INFINITY;
-      const float x11 = vb ? (sa[3] + sb[3]) * a.qscale : -INFINITY;
-      float mx0 = fmaxf(x00, x10), mx1 = fmaxf(x01, x11);
-#pragma unroll
-      for (int o = 4; o < 32; o <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-      }
-      const float mn0 = fmaxf(mr0, mx0), mn1 = fmaxf(mr1, mx1);
-      const bool any0 = mn0 != -INFINITY, any1 = mn1 != -INFINITY;
-      const float al0 = any0 ? exp2f(mr0 - mn0) : 1.f, al1 = any1 ? exp2f(mr1 - mn1) : 1.f;
-      const float p00 = any0 ? exp2f(x00 - mn0) : 0.f, p10 = any0 ? exp2f(x10 - mn0) : 0.f;
-      const float p01 = any1 ? exp2f(x01 - mn1) : 0.f, p11 = any1 ? exp2f(x11 - mn1) : 0.f;
-      mr0 = mn0;
-      mr1 = mn1;
-      lp0 = lp0 * al0 + (p00 + p10);
-      lp1 = lp1 * al1 + (p01 + p11);
-#pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        ot[m][0] *= al0;
-        ot[m][1] *= al1;
-        ot[m][2] *= al0;
-        ot[m][3] *= al1;
-      }
-      // P^T fragments: this lane's column values as bf16 (high part / remainder / zero), then an
-      // 8x8 transpose per token half turns score-fragment order into B-operand order
-      uint32_t bh0, bh1, bl0 = 0u, bl1 = 0u;
-      {
-        const float h00 = __bfloat162float(__float2bfloat16_rn(p00)), h01 = __bfloat162float(__float2bfloat16_rn(p01));
-        const float h10 = __bfloat162float(__float2bfloat16_rn(p10)), h11 = __bfloat162float(__float2bfloat16_rn(p11));
-        if (kStuff) {
-          const float y00 = c0 < G ? h00 : (c0 < 2 * G ? p00 - h00 : 0.f);
-          const float y01 = c1 < G ? h01 : (c1 < 2 * G ? p01 - h01 : 0.f);
-          const float y10 = c0 < G ? h10 : (c0 < 2 * G ? p10 - h10 : 0.f);
-          const float y11 = c1 < G ? h11 : (c1 < 2 * G ? p11 - h11 : 0.f);
-          bh0 = movm_t(pack_bf16(y00, y01));
-          bh1 = movm_t(pack_bf16(y10, y11));
-        } else {
-          bh0 = movm_t(pack_bf16(h00, h01));
-          bh1 = movm_t(pack_bf16(h10, h11));
-          bl0 = movm_t(pack_bf16(p00 - h00, p01 - h01));
-          bl1 = movm_t(pack_bf16(p10 - h10, p11 - h11));
-        }
-      }
-      // V^T fragments hold tokens 2 tig, 2 tig + 1 (+ 8): zero the invalid ones
-      uint32_t vm_lo = 0xffffffffu, vm_hi = 0xffffffffu;
-      if (mask != 0xffffu) {
-        const int ta = 2 * tig;
-        vm_lo = (((mask >> ta) & 1u) ? 0x0000ffffu : 0u) | (((mask >> (ta + 1)) & 1u) ? 0xffff0000u : 0u);
-        vm_hi = (((mask >> (ta + 8)) & 1u) ? 0x0000ffffu : 0u) | (((mask >> (ta + 9)) & 1u) ? 0xffff0000u : 0u);
-      }
-#pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        uint32_t x0, x1, x2, x3;
-        ldsm_x4_t(vaddr + m * 32, x0, x1, x2, x3);
-        x0 &= vm_lo;
-        x1 &= vm_lo;
-        x2 &= vm_hi;
-        x3 &= vm_hi;
-        mma_bf16(ot[m], x0, x1, x2, x3, bh0, bh1);
-        if (!kStuff) mma_bf16(ot[m], x0, x1, x2, x3, bl0, bl1);
-      }
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&empty_bar[b]);
-        if (NP > 0) {
-          for (uint32_t pm = pmask; pm != 0u; pm &= pm - 1u) {
-            const int pi = s_pidx[st * T + __ffs(pm) - 1];
-            mbar_arrive(&pempty_bar[pi % NPB]);
-          }
-        }
-      }
-    }
-    // column sums over the lanes holding the other tokens
-#pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-      lp0 += __shfl_xor_sync(0xffffffffu, lp0, o);
-      lp1 += __shfl_xor_sync(0xffffffffu, lp1, o);
-    }
-    // stuffed form: add each head's remainder column (G..2G-1) to its high column
-    if (kStuff) {
-      constexpr int xo = G == 4 ? 2 : 1;  // lane distance between columns c and c + G
-#pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        if (G == 1) {
-          ot[m][0] += ot[m][1];
-          ot[m][2] += ot[m][3];
-        } else {
-#pragma unroll
-          for (int e = 0; e < 4; ++e) ot[m][e] += __shfl_xor_sync(0xffffffffu, ot[m][e], xo);
-        }
-      }
-    }
-    if (!abort_flag) {
-      // heads of this lane's columns (both columns are real heads unless G == 1)
-      const bool own0 = c0 < G, own1 = c1 < G;
-      const int64_t ph0 = ((int64_t)r * a.S + split) * a.Hq + (int64_t)g * G + c0;
-      if (own0) {
-        float* po = a.part + ph0 * D;
-#pragma unroll
-        for (int m = 0; m < 8; ++m) {
-          po[16 * m + grow] = ot[m][0];
-          po[16 * m + grow + 8] = ot[m][2];
-        }
-        if (grow == 0) *(float2*)(a.ml + ph0 * 2) = make_float2(mr0, lp0);
-      }
-      if (own1) {
-        float* po = a.part + (ph0 + 1) * D;
-#pragma unroll
-        for (int m = 0; m < 8; ++m) {
-          po[16 * m + grow] = ot[m][1];
-          po[16 * m + grow + 8] = ot[m][3];
-        }
-        if (grow == 0) *(float2*)(a.ml + (ph0 + 1) * 2) = make_float2(mr1, lp1);
-      }
-    }
-  }
-  __threadfence();
-  __syncthreads();
-  if (abort_flag) return;
-  if (threadIdx.x == 0) {
-    const uint32_t t = atomicAdd(&a.ticket[(int64_t)r * a.groups + grp], 1u);
-    is_last = (t == (uint32_t)(a.S - 1)) ? 1u : 0u;
-  }
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-  if (warp < NW) {
-    if (a.S <= 32)
-      combine_heads_wide<D, G>(a, r, g * G, lane);
-    else
-      combine_heads<D>(a, r, g * G, G, lane);
-  }
-  if (threadIdx.x == 0) {
-    a.ticket[(int64_t)r * a.groups + grp] = 0u;
-    if (use_pend) a.pend_live[r] = 0u;  // every split has written its fetched rows back
-  }
-}
-
 // ---- GQA, one CTA per (request, KV head, split) ------------------------------------------
 //
 // Each CTA gathers one KV head's 512-byte K|V slice of every selected record (128 CTAs for 16
@@ -956,10 +537,22 @@ __global__ void __launch_bounds__(MmaThreads<NW, NP>::value, 1) k_attn_gqa_mma(A
 // merged through shared memory in warp order, so the reduction order is fixed by the top-k order
 // alone; with one split the CTA writes the final output, otherwise a partial that the last split of
 // the (request, KV head) combines.
+//
+// FETCH (misses copied inside the attention): the resolve only decided, and left {position, slot}
+// for every miss.  A producer loads the pending rows of its stage from the mapped host history with
+// 16-byte loads while the stage's resident rows arrive by bulk copy, stores them into the stage
+// buffer and writes them back to their hot-buffer slots (each CTA its own KV head's slice), so the
+// host-link transfer overlaps the HBM gather and the math.  The buffer's full mbarrier then takes
+// the producer's arrival only after those stores.  The last CTA of a request to finish clears the
+// request's pending flag.
 constexpr int kGqaWarps = 8;           // consumer warps
 constexpr int kGqaProducers = 8;       // producer warps, one per consumer
 constexpr int kGqaStages = 3;          // buffers per consumer warp
 constexpr int kGqaRow = 512 + 16;      // staged slice (K 256 B | V 256 B) + 16 B pad for ldmatrix
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
 
 __device__ __forceinline__ float fast_exp2(float x) {  // 2^x; -inf gives +0
   float y;
@@ -967,7 +560,7 @@ __device__ __forceinline__ float fast_exp2(float x) {  // 2^x; -inf gives +0
   return y;
 }
 
-template <int G>
+template <int G, bool FETCH>
 __global__ void __launch_bounds__((kGqaWarps + kGqaProducers) * 32, 1) k_attn_gqa(AttnArgs a) {
   hs_pdl_enter();
   constexpr int T = kMmaTile, D = 128, NW = kGqaWarps, NS = kGqaStages, RW = kGqaRow;
@@ -980,7 +573,7 @@ __global__ void __launch_bounds__((kGqaWarps + kGqaProducers) * 32, 1) k_attn_gq
   __shared__ __align__(8) uint64_t full[NW][NS];
   __shared__ __align__(8) uint64_t empty[NW][NS];
   __shared__ float s_m[NW][8], s_l[NW][8], s_fin[8][2];
-  __shared__ uint32_t is_last, abort_flag;
+  __shared__ uint32_t is_last, abort_flag, use_pend;
 
   const int split = blockIdx.x, r = a.r0 + (int)blockIdx.y, g = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -990,7 +583,9 @@ __global__ void __launch_bounds__((kGqaWarps + kGqaProducers) * 32, 1) k_attn_gq
   const int nst = (n + T - 1) / T;
   const int64_t rec = a.rec;
   int32_t* s_locs = (int32_t*)(smem + (size_t)NW * NS * T * RW);
+  int32_t* s_ppos = s_locs + a.chunk;  // FETCH: host position of a pending token, else -1
   if (threadIdx.x == 0) {
+    use_pend = (FETCH && a.pend != nullptr && a.pend_live[r] != 0u) ? 1u : 0u;
     for (int w = 0; w < NW; ++w)
       for (int b = 0; b < NS; ++b) {
         mbar_init(&full[w][b], 1u);
@@ -1026,7 +621,14 @@ __global__ void __launch_bounds__((kGqaWarps + kGqaProducers) * 32, 1) k_attn_gq
     }
     if (bad) atomicOr(a.err, (uint32_t)HS_DEVERR_LOC);
   }
+  if (FETCH && a.pend != nullptr) {
+    // pending positions of the chunk (the list is current only while the request's flag is up)
+    const bool on = a.pend_live[r] != 0u;
+    const int2* pend = a.pend + (int64_t)r * a.k + t0;
+    for (int x = (int)threadIdx.x; x < n; x += (NW + kGqaProducers) * 32) s_ppos[x] = on ? pend[x].x : -1;
+  }
   __syncthreads();
+  const bool pend_on = FETCH && use_pend != 0u;
 
   // consumer state: columns c0, c1 of the 8-wide MMA side (head c % G; high part, remainder or
   // zero padding, see above), running max / sum per column, O^T accumulators
@@ -1043,6 +645,36 @@ __global__ void __launch_bounds__((kGqaWarps + kGqaProducers) * 32, 1) k_attn_gq
     const uint8_t* kvg = a.kv + (int64_t)r * a.rows * rec + (int64_t)g * a.kstride;
     bool ok = true;
     int issued = 0;
+    // stage i of this producer: its tokens' slots (lanes 0-15), host positions of pending ones, masks
+    auto stage_info = [&](int i, int32_t& loc, int32_t& pp, uint32_t& vmask, uint32_t& pmask) {
+      const int x = (w + NW * i) * T + (lane & 15);
+      loc = (i < ni && lane < T && x < n) ? s_locs[x] : -1;
+      pp = (FETCH && pend_on && loc >= 0) ? s_ppos[x] : -1;
+      vmask = __ballot_sync(0xffffffffu, lane < T && loc >= 0);
+      pmask = FETCH ? __ballot_sync(0xffffffffu, lane < T && pp >= 0) : 0u;
+    };
+    // FETCH: up to kPre pending rows of a stage are requested from the host one stage ahead of use
+    // (deeper request windows measured slower: the link is the bound, more requests only queue)
+    constexpr int kPre = FETCH ? 8 : 1;
+    uint4 vc[kPre], vn[kPre];
+    auto host_row = [&](int32_t pos) -> const uint4* {
+      const uint8_t* h = hs_hist_addr(a.hist_shared, a.hist_priv, a.P0, a.priv_tokens, rec, a.L, r, a.layer, pos);
+      return (const uint4*)(h + (int64_t)g * a.kstride) + lane;
+    };
+    auto request = [&](uint32_t pmask_, int32_t pp_, uint4 (&v)[kPre]) {
+      uint32_t pm = pmask_;
+#pragma unroll
+      for (int u = 0; u < kPre; ++u) {
+        if (pm != 0u) {
+          v[u] = __ldg(host_row(__shfl_sync(0xffffffffu, pp_, __ffs(pm) - 1)));
+          pm &= pm - 1u;
+        }
+      }
+    };
+    int32_t loc, pp;
+    uint32_t vmask, pmask;
+    stage_info(0, loc, pp, vmask, pmask);
+    if (FETCH) request(pmask, pp, vc);
     for (int i = 0; i < ni; ++i) {
       const int b = i % NS;
       if (i >= NS) {
@@ -1053,9 +685,6 @@ __global__ void __launch_bounds__((kGqaWarps + kGqaProducers) * 32, 1) k_attn_gq
           break;
         }
       }
-      const int x = (w + NW * i) * T + (lane & 15);
-      const int32_t loc = (lane < T && x < n) ? s_locs[x] : -1;
-      const uint32_t vmask = __ballot_sync(0xffffffffu, lane < T && loc >= 0);
       uint8_t* dst = smem + ((size_t)(w * NS + b) * T) * RW;
       if (vmask != 0xffffu) {
         // padding rows (and the tail past the chunk) read as zeros
@@ -1063,9 +692,45 @@ __global__ void __launch_bounds__((kGqaWarps + kGqaProducers) * 32, 1) k_attn_gq
           *(uint4*)(dst + (__ffs(zm) - 1) * RW + lane * 16) = make_uint4(0u, 0u, 0u, 0u);
         __syncwarp();
       }
-      if (lane == 0) mbar_arrive_expect_tx(&full[w][b], (uint32_t)__popc(vmask) * 512u);
-      __syncwarp();
-      if (loc >= 0) bulk_g2s(dst + lane * RW, kvg + (int64_t)loc * rec, 512u, &full[w][b]);
+      if (!FETCH || pmask == 0u) {
+        if (lane == 0) mbar_arrive_expect_tx(&full[w][b], (uint32_t)__popc(vmask) * 512u);
+        __syncwarp();
+        if (loc >= 0) bulk_g2s(dst + lane * RW, kvg + (int64_t)loc * rec, 512u, &full[w][b]);
+      } else {
+        // resident rows by bulk copy; the arrival comes after the pending rows are stored, below
+        if (lane == 0) mbar_expect_tx(&full[w][b], (uint32_t)__popc(vmask & ~pmask) * 512u);
+        __syncwarp();
+        if (loc >= 0 && pp < 0) bulk_g2s(dst + lane * RW, kvg + (int64_t)loc * rec, 512u, &full[w][b]);
+      }
+      int32_t loc2, pp2;
+      uint32_t vmask2, pmask2;
+      stage_info(i + 1, loc2, pp2, vmask2, pmask2);
+      if (FETCH) {
+        request(pmask2, pp2, vn);  // the next stage's pending rows, before this stage's are stored
+        if (pmask != 0u) {
+          // pending rows into the stage and back to their hot-buffer slots (each CTA its KV head's slice)
+          uint32_t pm = pmask;
+#pragma unroll
+          for (int u = 0; u < kPre + 16; ++u) {  // the first kPre were requested a stage ago
+            if (pm != 0u) {
+              const int j = __ffs(pm) - 1;
+              pm &= pm - 1u;
+              const uint4 v = u < kPre ? vc[u < kPre ? u : 0] : __ldg(host_row(__shfl_sync(0xffffffffu, pp, j)));
+              *(uint4*)(dst + j * RW + lane * 16) = v;
+              const int32_t slot = __shfl_sync(0xffffffffu, loc, j);
+              *((uint4*)(a.buf_w + ((int64_t)r * a.rows + slot) * rec + (int64_t)g * a.kstride) + lane) = v;
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&full[w][b]);
+        }
+#pragma unroll
+        for (int u = 0; u < kPre; ++u) vc[u] = vn[u];
+      }
+      loc = loc2;
+      pp = pp2;
+      vmask = vmask2;
+      pmask = pmask2;
       issued = i + 1;
     }
     if (!ok && lane == 0) {
@@ -1191,6 +856,15 @@ __global__ void __launch_bounds__((kGqaWarps + kGqaProducers) * 32, 1) k_attn_gq
   }
   __syncthreads();  // (A) stats in place, no buffer read any more
   if (abort_flag) return;
+  if (pend_on && threadIdx.x == 0) {
+    // every CTA of the request has written its slices of the fetched rows back: the list is done
+    uint32_t* cnt = &a.ticket[(int64_t)r * (a.groups + 1) + a.groups];
+    const uint32_t t = atomicAdd(cnt, 1u);
+    if (t == (uint32_t)(a.S * a.groups - 1)) {
+      *cnt = 0u;
+      a.pend_live[r] = 0u;
+    }
+  }
   // merge: each consumer column scaled by exp2(m_w - M) into red[w][c][.]; the producer warp's
   // lanes h < G compute the per-head max M and normaliser
   float* red = (float*)smem;
@@ -1252,7 +926,7 @@ __global__ void __launch_bounds__((kGqaWarps + kGqaProducers) * 32, 1) k_attn_gq
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
-    const uint32_t t = atomicAdd(&a.ticket[(int64_t)r * a.groups + g], 1u);
+    const uint32_t t = atomicAdd(&a.ticket[(int64_t)r * (a.groups + 1) + g], 1u);
     is_last = (t == (uint32_t)(a.S - 1)) ? 1u : 0u;
   }
   __syncthreads();
@@ -1264,7 +938,7 @@ __global__ void __launch_bounds__((kGqaWarps + kGqaProducers) * 32, 1) k_attn_gq
     else
       combine_heads<D>(a, r, g * G, G, lane);
   }
-  if (threadIdx.x == 0) a.ticket[(int64_t)r * a.groups + g] = 0u;
+  if (threadIdx.x == 0) a.ticket[(int64_t)r * (a.groups + 1) + g] = 0u;
 }
 
 // ---- tensor-core variant for shared-latent (MLA) records ---------------------------------
@@ -1555,12 +1229,10 @@ __global__ void __launch_bounds__(256) k_combine(AttnArgs a) {
 struct Plan {
   int kind;  // 0: CUDA-core shared-latent, 1: GQA per KV head, 2: shared-latent mma, 3: GQA with the miss fetch
   int NW, G, T, groups, S, chunk;
-  int fetch;  // 1: the GQA kernel fetches pending rows from the host (2 ring stages + kPendSlots)
+  int fetch;  // 1: the GQA kernel also copies the misses the resolve left pending
   size_t smem;
 };
 
-constexpr int kMmaStagesFetch = 2;
-constexpr int kPendSlots = 16;
 
 bool plan_for(const hs_config* c, int num_sms, Plan* pl) {
   const int64_t rec = hs_record_bytes(c);
@@ -1571,26 +1243,11 @@ bool plan_for(const hs_config* c, int num_sms, Plan* pl) {
     if (G != 1 && G != 2 && G != 4 && G != 8) return false;
     pl->G = G;
     pl->T = kMmaTile;
-    if (c->fetch_in_attention != 0) {
-      // misses copied inside the attention: all KV heads of a request in one CTA
-      int NW = c->num_kv_heads;
-      if (NW > 8) {
-        if (NW % 8 != 0) return false;
-        NW = 8;
-      }
-      if (NW != 1 && NW != 2 && NW != 4 && NW != 8) return false;
-      pl->kind = 3;
-      pl->NW = NW;
-      pl->groups = c->num_kv_heads / NW;
-      pl->fetch = 1;
-      pl->smem = (size_t)(kMmaStagesFetch * kMmaTile + kPendSlots) * (size_t)(rec + 16);
-    } else {
-      pl->kind = 1;
-      pl->NW = kGqaWarps;
-      pl->groups = c->num_kv_heads;  // one KV head per CTA
-      pl->fetch = 0;
-      pl->smem = (size_t)kGqaWarps * kGqaStages * kMmaTile * kGqaRow;
-    }
+    pl->kind = 1;
+    pl->NW = kGqaWarps;
+    pl->groups = c->num_kv_heads;  // one KV head per CTA
+    pl->fetch = c->fetch_in_attention != 0;
+    pl->smem = (size_t)kGqaWarps * kGqaStages * kMmaTile * kGqaRow;
     per_cta_wave = 1;  // one CTA per SM: the staging buffers hold most of the shared memory
   } else if (c->head_dim_qk == 576 && c->head_dim_v == 512 && c->num_q_heads == kMlaHeads) {
     pl->kind = 2;
@@ -1622,8 +1279,7 @@ bool plan_for(const hs_config* c, int num_sms, Plan* pl) {
   chunk = (chunk + pl->T - 1) / pl->T * pl->T;
   pl->chunk = chunk;
   pl->S = (c->top_k + chunk - 1) / chunk;
-  if (pl->kind == 1) pl->smem += (size_t)chunk * 4;   // slot list
-  if (pl->kind == 3) pl->smem += (size_t)chunk * 16;  // slot list, pending index, pending list
+  if (pl->kind == 1) pl->smem += (size_t)chunk * (pl->fetch ? 8 : 4);  // slot list (+ pending positions)
   if (pl->kind == 2) pl->smem += (size_t)chunk * 4;   // slot list
   return pl->smem <= 220 * 1024;
 }
@@ -1645,16 +1301,6 @@ cudaError_t launch_kernel(K kern, const AttnArgs* a, const Plan& pl, int threads
   return cudaLaunchKernelEx(&cfg, kern, *a);
 }
 
-template <int G, int NSTAGE, int NP>
-cudaError_t launch_gqa_nw2(const AttnArgs* a, const Plan& pl, cudaStream_t st) {
-  switch (pl.NW) {
-    case 1: return launch_kernel(k_attn_gqa_mma<G, 1, NSTAGE, NP>, a, pl, MmaThreads<1, NP>::value, st);
-    case 2: return launch_kernel(k_attn_gqa_mma<G, 2, NSTAGE, NP>, a, pl, MmaThreads<2, NP>::value, st);
-    case 4: return launch_kernel(k_attn_gqa_mma<G, 4, NSTAGE, NP>, a, pl, MmaThreads<4, NP>::value, st);
-    case 8: return launch_kernel(k_attn_gqa_mma<G, 8, NSTAGE, NP>, a, pl, MmaThreads<8, NP>::value, st);
-    default: return cudaErrorInvalidValue;
-  }
-}
 
 
 cudaError_t dispatch(const hs_config& c, const AttnArgs* a, const Plan& pl, cudaStream_t st) {
@@ -1673,19 +1319,19 @@ cudaError_t dispatch(const hs_config& c, const AttnArgs* a, const Plan& pl, cuda
     return cudaLaunchKernelEx(&cfg, k_combine<512>, *a);
   }
   if (pl.kind == 0) return launch_kernel(k_attn_cc<576, 512, 1, 8>, a, pl, AttnCfg<576, 512, 1, 8>::THREADS, st);
-  if (pl.kind == 1) {
+  if (pl.fetch) {
     switch (pl.G) {
-      case 1: return launch_kernel(k_attn_gqa<1>, a, pl, (kGqaWarps + kGqaProducers) * 32, st);
-      case 2: return launch_kernel(k_attn_gqa<2>, a, pl, (kGqaWarps + kGqaProducers) * 32, st);
-      case 4: return launch_kernel(k_attn_gqa<4>, a, pl, (kGqaWarps + kGqaProducers) * 32, st);
-      default: return launch_kernel(k_attn_gqa<8>, a, pl, (kGqaWarps + kGqaProducers) * 32, st);
+      case 1: return launch_kernel(k_attn_gqa<1, true>, a, pl, (kGqaWarps + kGqaProducers) * 32, st);
+      case 2: return launch_kernel(k_attn_gqa<2, true>, a, pl, (kGqaWarps + kGqaProducers) * 32, st);
+      case 4: return launch_kernel(k_attn_gqa<4, true>, a, pl, (kGqaWarps + kGqaProducers) * 32, st);
+      default: return launch_kernel(k_attn_gqa<8, true>, a, pl, (kGqaWarps + kGqaProducers) * 32, st);
     }
   }
   switch (pl.G) {
-    case 1: return launch_gqa_nw2<1, kMmaStagesFetch, kPendSlots>(a, pl, st);
-    case 2: return launch_gqa_nw2<2, kMmaStagesFetch, kPendSlots>(a, pl, st);
-    case 4: return launch_gqa_nw2<4, kMmaStagesFetch, kPendSlots>(a, pl, st);
-    default: return launch_gqa_nw2<8, kMmaStagesFetch, kPendSlots>(a, pl, st);
+    case 1: return launch_kernel(k_attn_gqa<1, false>, a, pl, (kGqaWarps + kGqaProducers) * 32, st);
+    case 2: return launch_kernel(k_attn_gqa<2, false>, a, pl, (kGqaWarps + kGqaProducers) * 32, st);
+    case 4: return launch_kernel(k_attn_gqa<4, false>, a, pl, (kGqaWarps + kGqaProducers) * 32, st);
+    default: return launch_kernel(k_attn_gqa<8, false>, a, pl, (kGqaWarps + kGqaProducers) * 32, st);
   }
 }
 
@@ -1695,7 +1341,7 @@ bool hs_attn_can_fetch(const hs_config* c) {
   hs_config f = *c;
   f.fetch_in_attention = 1;
   Plan pl;
-  return plan_for(&f, 152, &pl) && pl.kind == 3 && pl.groups == 1;
+  return plan_for(&f, 152, &pl) && pl.kind == 1;
 }
 
 bool hs_attn_supported(const hs_config* c) {
@@ -1703,11 +1349,11 @@ bool hs_attn_supported(const hs_config* c) {
   return plan_for(c, 152, &pl);
 }
 
-void hs_attn_workspace(const hs_config* c, int num_sms, size_t* floats, int* max_splits, int* max_groups) {
+void hs_attn_workspace(const hs_config* c, int num_sms, size_t* floats, int* max_splits, int* tickets_per_req) {
   Plan pl;
   plan_for(c, num_sms, &pl);
   *max_splits = pl.S;
-  *max_groups = pl.groups;
+  *tickets_per_req = pl.groups + 1;  // one per group, then the pending-list count
   *floats = (size_t)c->num_requests * pl.S * c->num_q_heads * ((size_t)c->head_dim_v + 2);
 }
 
@@ -1836,7 +1482,7 @@ extern "C" int hs_sparse_attn_noalloc(const hs_config* cfg, const void* d_q, con
   Plan pl;
   if (!plan_for(cfg, sms, &pl)) return HS_ERR_CONFIG;
   const size_t part_floats = (size_t)cfg->num_requests * pl.S * cfg->num_q_heads * ((size_t)cfg->head_dim_v + 2);
-  const size_t tickets = (size_t)cfg->num_requests * pl.groups;
+  const size_t tickets = (size_t)cfg->num_requests * (pl.groups + 1);
   if (part_floats * sizeof(float) > kNoAllocPartBytes || (tickets + 1) * sizeof(uint32_t) > kNoAllocTicketBytes)
     return HS_ERR_SCRATCH;
   uint8_t* base = (uint8_t*)scratch;

@@ -40,10 +40,10 @@ struct hs_pool {
   int2* pend;            // [L][R][k] {position, slot} of misses the attention still has to fetch
   uint32_t* pend_live;   // [L][R] 1 while such a list is outstanding
   float* attn_part;      // split partials
-  uint32_t* attn_ticket; // [R][attn_max_groups]
+  uint32_t* attn_ticket; // [R][attn_tickets_per_req]: per-group split tickets, then the pending-list count
   int attn_max_splits;
   int resolve_cs;        // CTAs per request in the resolve cluster
-  int attn_max_groups;
+  int attn_tickets_per_req;
   size_t attn_part_floats;
 };
 
@@ -110,7 +110,7 @@ int hs_launch_append(hs_pool* pool, int layer, const int64_t* d_pos, const void*
 int hs_launch_attn(hs_pool* pool, int layer, int r0, int nreq, const void* d_q, const int32_t* d_locs,
                    const void* kv_base, int64_t kv_rows, float scale, float* d_out, cudaStream_t st);
 // attention workspace requirement for a configuration (floats, splits, groups)
-void hs_attn_workspace(const hs_config* cfg, int num_sms, size_t* floats, int* max_splits, int* max_groups);
+void hs_attn_workspace(const hs_config* cfg, int num_sms, size_t* floats, int* max_splits, int* tickets_per_req);
 bool hs_attn_supported(const hs_config* cfg);
 bool hs_attn_can_fetch(const hs_config* cfg);  // the attention can take over the miss fetch
 int hs_attn_prepare(const hs_config* cfg, int num_sms);

@@ -122,7 +122,7 @@ int do_reset(hs_pool* p, cudaStream_t st) {
     return HS_ERR_CUDA;
   if (cudaMemsetAsync(p->err_global, 0, sizeof(uint32_t), st) != cudaSuccess) return HS_ERR_CUDA;
   if (p->pend_live && cudaMemsetAsync(p->pend_live, 0, nrl * sizeof(uint32_t), st) != cudaSuccess) return HS_ERR_CUDA;
-  if (cudaMemsetAsync(p->attn_ticket, 0, (size_t)p->cfg.num_requests * p->attn_max_groups * sizeof(uint32_t), st) !=
+  if (cudaMemsetAsync(p->attn_ticket, 0, (size_t)p->cfg.num_requests * p->attn_tickets_per_req * sizeof(uint32_t), st) !=
       cudaSuccess)
     return HS_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? HS_OK : HS_ERR_CUDA;
@@ -178,10 +178,10 @@ extern "C" int hs_pool_create(const hs_config* cfg, int cuda_device, hs_pool** o
   if (rc == HS_OK) rc = dev_alloc(&p->step_log, (size_t)cfg->log_steps * L * R);
   if (rc == HS_OK) rc = dev_alloc(&p->err_global, 1);
   if (rc == HS_OK) {
-    hs_attn_workspace(cfg, p->num_sms, &p->attn_part_floats, &p->attn_max_splits, &p->attn_max_groups);
+    hs_attn_workspace(cfg, p->num_sms, &p->attn_part_floats, &p->attn_max_splits, &p->attn_tickets_per_req);
     rc = dev_alloc(&p->attn_part, p->attn_part_floats);
   }
-  if (rc == HS_OK) rc = dev_alloc(&p->attn_ticket, R * (size_t)p->attn_max_groups);
+  if (rc == HS_OK) rc = dev_alloc(&p->attn_ticket, R * (size_t)p->attn_tickets_per_req);
   if (rc == HS_OK && cfg->fetch_in_attention) {
     rc = dev_alloc(&p->pend, L * R * (size_t)cfg->top_k);
     if (rc == HS_OK) rc = dev_alloc(&p->pend_live, L * R);
