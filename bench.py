@@ -49,7 +49,7 @@ WORKLOADS = {
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one attention launch from an ncu capture of the
 # same kernel and per-launch size (profiles/); None where no capture of the current kernel exists
-ATTN_TRAFFIC = {("gqa_b16_l32", "resolve"): 138.07e6}  # profiles/k_attn_gqa_gqa_b16.md
+ATTN_TRAFFIC = {("gqa_b16_l32", "resolve"): 138.07e6}
 
 
 def load_peaks():
@@ -330,6 +330,7 @@ def run_ours(args, w, world, rank, local):
 
     # ---- host-link peak on this machine: pinned H2D copy, best of 5 ----
     h2d = measure_h2d(device)
+    floor_us = measure_launch_floor()
     peaks = load_peaks()
     attn_us = float(att_ms.mean() * 1e3)
     achieved = attn_bytes_per_launch(w) / M / (attn_us * 1e-6) / 1e9  # a launch covers R / M requests
@@ -359,7 +360,11 @@ def run_ours(args, w, world, rank, local):
         "roofline": {"kernel": "sparse_attn", "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": args.traffic if args.traffic is not None else ATTN_TRAFFIC.get((args.workload, fetch)),
                      "peak_source": peaks["source"],
-                     "bytes_per_launch": attn_bytes_per_launch(w) // M},
+                     "bytes_per_launch": attn_bytes_per_launch(w) // M,
+                     # the same with the event floor of an empty kernel taken out of the launch time
+                     "launch_floor_us": floor_us,
+                     "frac_excl_launch_floor": (attn_bytes_per_launch(w) / M / ((attn_us - floor_us) * 1e-6) / 1e9)
+                     / peaks["hbm_gbs"] if attn_us > floor_us else None},
         # the kernel that moves the misses over the host link: the resolve, or the attention when the
         # copies were left to it
         "host_link": {"kernel": link_kernel, "miss_bytes_per_layer": miss_bytes / (K * L),
@@ -442,6 +447,24 @@ def measure_h2d(device):
         best = min(best, s.elapsed_time(e) / 1e3)
     del h, d
     return n / best / 1e9
+
+
+def measure_launch_floor():
+    """CUDA-event time of a kernel that does nothing (median of 30 enqueued back to back, so the device
+    never waits for the host): the per-launch floor that the event pairs around every kernel of the
+    breakdown pass include."""
+    import torch
+
+    torch.cuda._sleep(1000000)  # keep the device busy while the pairs are enqueued
+    pairs = []
+    for _ in range(30):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        torch.cuda._sleep(1)
+        e.record()
+        pairs.append((s, e))
+    torch.cuda.synchronize()
+    return float(np.median([s.elapsed_time(e) * 1e3 for s, e in pairs]))
 
 
 # --------------------------------------------------------------------------------------------

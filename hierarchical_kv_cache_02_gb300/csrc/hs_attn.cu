@@ -573,6 +573,7 @@ __global__ void __launch_bounds__((kGqaWarps + kGqaProducers) * 32, 1) k_attn_gq
   __shared__ __align__(8) uint64_t full[NW][NS];
   __shared__ __align__(8) uint64_t empty[NW][NS];
   __shared__ float s_m[NW][8], s_l[NW][8], s_fin[8][2];
+  __shared__ uint32_t s_mask[NW][NS];  // valid tokens of the stage in each buffer (bit j: token j)
   __shared__ uint32_t is_last, abort_flag, use_pend;
 
   const int split = blockIdx.x, r = a.r0 + (int)blockIdx.y, g = blockIdx.z;
@@ -582,8 +583,6 @@ __global__ void __launch_bounds__((kGqaWarps + kGqaProducers) * 32, 1) k_attn_gq
   const int n = min(a.k, t0 + a.chunk) - t0;
   const int nst = (n + T - 1) / T;
   const int64_t rec = a.rec;
-  int32_t* s_locs = (int32_t*)(smem + (size_t)NW * NS * T * RW);
-  int32_t* s_ppos = s_locs + a.chunk;  // FETCH: host position of a pending token, else -1
   if (threadIdx.x == 0) {
     use_pend = (FETCH && a.pend != nullptr && a.pend_live[r] != 0u) ? 1u : 0u;
     for (int w = 0; w < NW; ++w)
@@ -593,39 +592,6 @@ __global__ void __launch_bounds__((kGqaWarps + kGqaProducers) * 32, 1) k_attn_gq
       }
     abort_flag = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  {
-    // the chunk's slot list, eight loads per thread in flight; invalid entries become padding
-    const int32_t* locs = a.locs + (int64_t)(r - a.r0) * a.k + t0;
-    constexpr int NT = (NW + kGqaProducers) * 32;
-    bool bad = false;
-    for (int x0 = 0; x0 < n; x0 += NT * 8) {
-      int32_t v[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int x = x0 + u * NT + (int)threadIdx.x;
-        v[u] = x < n ? locs[x] : -1;
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int x = x0 + u * NT + (int)threadIdx.x;
-        if (x < n) {
-          int32_t loc = v[u];
-          if (loc < -1 || (int64_t)loc >= a.rows) {
-            bad = true;
-            loc = -1;
-          }
-          s_locs[x] = loc;
-        }
-      }
-    }
-    if (bad) atomicOr(a.err, (uint32_t)HS_DEVERR_LOC);
-  }
-  if (FETCH && a.pend != nullptr) {
-    // pending positions of the chunk (the list is current only while the request's flag is up)
-    const bool on = a.pend_live[r] != 0u;
-    const int2* pend = a.pend + (int64_t)r * a.k + t0;
-    for (int x = (int)threadIdx.x; x < n; x += (NW + kGqaProducers) * 32) s_ppos[x] = on ? pend[x].x : -1;
   }
   __syncthreads();
   const bool pend_on = FETCH && use_pend != 0u;
@@ -645,11 +611,23 @@ __global__ void __launch_bounds__((kGqaWarps + kGqaProducers) * 32, 1) k_attn_gq
     const uint8_t* kvg = a.kv + (int64_t)r * a.rows * rec + (int64_t)g * a.kstride;
     bool ok = true;
     int issued = 0;
-    // stage i of this producer: its tokens' slots (lanes 0-15), host positions of pending ones, masks
-    auto stage_info = [&](int i, int32_t& loc, int32_t& pp, uint32_t& vmask, uint32_t& pmask) {
-      const int x = (w + NW * i) * T + (lane & 15);
-      loc = (i < ni && lane < T && x < n) ? s_locs[x] : -1;
-      pp = (FETCH && pend_on && loc >= 0) ? s_ppos[x] : -1;
+    // the slot (and, FETCH, the pending host position) of token `lane` of stage i, read from global
+    // memory two stages before use; invalid slots become padding
+    const int32_t* locs_r = a.locs + (int64_t)(r - a.r0) * a.k + t0;
+    const int2* pend_r = pend_on ? a.pend + (int64_t)r * a.k + t0 : nullptr;
+    auto load_raw = [&](int i, int32_t& l, int32_t& q) {
+      const int x = (w + NW * i) * T + lane;
+      const bool in = i < ni && lane < T && x < n;
+      l = in ? locs_r[x] : -1;
+      q = (FETCH && in && pend_on) ? pend_r[x].x : -1;
+    };
+    auto stage_info = [&](int32_t l, int32_t q, int32_t& loc, int32_t& pp, uint32_t& vmask, uint32_t& pmask) {
+      if (l < -1 || (int64_t)l >= a.rows) {
+        atomicOr(a.err, (uint32_t)HS_DEVERR_LOC);
+        l = -1;
+      }
+      loc = l;
+      pp = (FETCH && l >= 0) ? q : -1;
       vmask = __ballot_sync(0xffffffffu, lane < T && loc >= 0);
       pmask = FETCH ? __ballot_sync(0xffffffffu, lane < T && pp >= 0) : 0u;
     };
@@ -671,9 +649,13 @@ __global__ void __launch_bounds__((kGqaWarps + kGqaProducers) * 32, 1) k_attn_gq
         }
       }
     };
+    int32_t raw_l0, raw_q0, raw_l1, raw_q1;
+    load_raw(0, raw_l0, raw_q0);
+    load_raw(1, raw_l1, raw_q1);
     int32_t loc, pp;
     uint32_t vmask, pmask;
-    stage_info(0, loc, pp, vmask, pmask);
+    stage_info(raw_l0, raw_q0, loc, pp, vmask, pmask);
+    load_raw(2, raw_l0, raw_q0);
     if (FETCH) request(pmask, pp, vc);
     for (int i = 0; i < ni; ++i) {
       const int b = i % NS;
@@ -686,6 +668,7 @@ __global__ void __launch_bounds__((kGqaWarps + kGqaProducers) * 32, 1) k_attn_gq
         }
       }
       uint8_t* dst = smem + ((size_t)(w * NS + b) * T) * RW;
+      if (lane == 0) s_mask[w][b] = vmask;
       if (vmask != 0xffffu) {
         // padding rows (and the tail past the chunk) read as zeros
         for (uint32_t zm = ~vmask & 0xffffu; zm != 0u; zm &= zm - 1u)
@@ -704,7 +687,10 @@ __global__ void __launch_bounds__((kGqaWarps + kGqaProducers) * 32, 1) k_attn_gq
       }
       int32_t loc2, pp2;
       uint32_t vmask2, pmask2;
-      stage_info(i + 1, loc2, pp2, vmask2, pmask2);
+      stage_info(raw_l1, raw_q1, loc2, pp2, vmask2, pmask2);
+      raw_l1 = raw_l0;
+      raw_q1 = raw_q0;
+      load_raw(i + 3, raw_l0, raw_q0);
       if (FETCH) {
         request(pmask2, pp2, vn);  // the next stage's pending rows, before this stage's are stored
         if (pmask != 0u) {
@@ -765,8 +751,7 @@ __global__ void __launch_bounds__((kGqaWarps + kGqaProducers) * 32, 1) k_attn_gq
         atomicOr(a.err, (uint32_t)HS_DEVERR_TIMEOUT);
         break;
       }
-      const int xj = (warp + NW * i) * T + (lane & 15);
-      const uint32_t mask = __ballot_sync(0xffffffffu, lane < 16 && xj < n && s_locs[xj] >= 0) & 0xffffu;
+      const uint32_t mask = s_mask[warp][b];
       const uint32_t base = ring_u + (uint32_t)(b * T * RW);
       // S^T = K Q^T in two MMA chains
       float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
@@ -1279,15 +1264,19 @@ bool plan_for(const hs_config* c, int num_sms, Plan* pl) {
   chunk = (chunk + pl->T - 1) / pl->T * pl->T;
   pl->chunk = chunk;
   pl->S = (c->top_k + chunk - 1) / chunk;
-  if (pl->kind == 1) pl->smem += (size_t)chunk * (pl->fetch ? 8 : 4);  // slot list (+ pending positions)
+
   if (pl->kind == 2) pl->smem += (size_t)chunk * 4;   // slot list
   return pl->smem <= 220 * 1024;
 }
 
 template <typename K>
 cudaError_t launch_kernel(K kern, const AttnArgs* a, const Plan& pl, int threads, cudaStream_t st) {
-  if (a == nullptr)  // preparation: raise the dynamic shared-memory limit once
-    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+  if (a == nullptr) {  // preparation, once: the dynamic shared-memory limit and the largest carveout
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
+    return e;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(pl.S, a->R, pl.groups);
   cfg.blockDim = dim3(threads, 1, 1);
@@ -1306,6 +1295,9 @@ cudaError_t launch_kernel(K kern, const AttnArgs* a, const Plan& pl, int threads
 cudaError_t dispatch(const hs_config& c, const AttnArgs* a, const Plan& pl, cudaStream_t st) {
   if (pl.kind == 2) {
     cudaError_t e = launch_kernel(k_attn_mla_mma<kMlaStages>, a, pl, 9 * 32, st);
+    if (e == cudaSuccess && a == nullptr)
+      e = cudaFuncSetAttribute(k_combine<512>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess || a == nullptr) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a->R, (a->Hq + 7) / 8, 1);

@@ -635,6 +635,11 @@ int prepare_nv(const hs_config* c, int num_sms, int* cs_out) {
   const int smem = (int)hs_resolve_smem_bytes(c);
   if (cudaFuncSetAttribute(k_resolve<NV>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return HS_ERR_CUDA;
+  // the same (largest) shared-memory carveout as the attention kernels, so the SMs keep their
+  // L1/shared split from one kernel of a decode step to the next
+  if (cudaFuncSetAttribute(k_resolve<NV>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+    return HS_ERR_CUDA;
   // largest cluster (<= 8 CTAs per request) that lets every request's cluster be resident at once
   *cs_out = 1;
   for (int cs = 8; cs >= 2; cs /= 2) {
