@@ -154,7 +154,7 @@ def barrier(world):
 class Workload:
     """Seeded synthetic inputs of one replica, resident on the GPU."""
 
-    def __init__(self, w, steps, device, seed, fetch="resolve"):
+    def __init__(self, w, steps, device, seed, fetch="resolve", index_share=1):
         import torch
 
         from hierarchical_kv_cache_02_gb300 import HsConfig, inputs
@@ -170,6 +170,10 @@ class Workload:
                                 appends=True, burst_every=w["burst"], far_gap=int(8 * w["mu"]))
         t0 = time.time()
         self.trace_host = inputs.drift_traces(spec, R, L, seed=seed)            # [S][L][R][k]
+        if index_share > 1:
+            # layer groups share one selection (the group's first layer's), as with a shared indexer
+            for l in range(L):
+                self.trace_host[:, l] = self.trace_host[:, index_share * (l // index_share)]
         self.trace_secs = time.time() - t0
         self.topk = torch.from_numpy(self.trace_host).to(device)
         E = self.cfg.record_elems
@@ -208,7 +212,8 @@ def run_ours(args, w, world, rank, local):
     fetch = args.fetch
     if fetch == "auto":
         fetch = "resolve"  # each kernel against its own roofline; "attention" overlaps the link with HBM
-    wl = Workload(w, S, device, seed=1000 + 17 * rank, fetch=fetch)
+    G = max(1, args.index_share)
+    wl = Workload(w, S, device, seed=1000 + 17 * rank, fetch=fetch, index_share=G)
     pool = HsPool(wl.cfg, device=local)
     wl.prefill(pool)
     torch.cuda.synchronize()
@@ -236,6 +241,40 @@ def run_ours(args, w, world, rank, local):
             pool.sparse_attn(l, wl.q[t, l], locs[l], outs[l], scale=scale)
             if ev is not None:
                 ev[l][3].record(stream)
+
+    # group mode: attentions on their own stream, resolves of the group each on a side stream (equal
+    # priorities: giving the attentions priority measured slower, the resolves' fetches then lack SMs)
+    astream = torch.cuda.Stream() if G > 1 else stream
+    side = [torch.cuda.Stream() for _ in range(G)] if G > 1 else []
+
+    def step_group(t, ev=None):
+        # layer-group prefetch: a group's selection is known once the layer before the group has
+        # finished its attention, so all resolves of the group (with their host fetches) start then,
+        # each on its own stream; the attentions follow in layer order as their resolves complete
+        for l0 in range(0, L, G):
+            known = torch.cuda.Event()
+            known.record(astream)
+            done = []
+            for j, l in enumerate(range(l0, min(L, l0 + G))):
+                st = side[j]
+                st.wait_event(known)
+                with torch.cuda.stream(st):
+                    if ev is not None:
+                        ev[l][1].record(st)
+                    pool.append_resolve(l, wl.pos[t], wl.app[t, l], wl.topk[t, l], locs[l], stream=st)
+                    if ev is not None:
+                        ev[l][2].record(st)
+                e = torch.cuda.Event()
+                e.record(st)
+                done.append(e)
+            for j, l in enumerate(range(l0, min(L, l0 + G))):
+                astream.wait_event(done[j])
+                with torch.cuda.stream(astream):
+                    if ev is not None:
+                        ev[l][0].record(astream)
+                    pool.sparse_attn(l, wl.q[t, l], locs[l], outs[l], scale=scale, stream=astream)
+                    if ev is not None:
+                        ev[l][3].record(astream)
 
     M = max(1, args.microbatches)
     groups = [(R * g // M, R * (g + 1) // M - R * g // M) for g in range(M)]
@@ -280,6 +319,10 @@ def run_ours(args, w, world, rank, local):
                 fork()
                 step_mb(t)
                 join()
+            elif G > 1:
+                astream.wait_stream(stream)
+                step_group(t)
+                stream.wait_stream(astream)
             else:
                 step(t)
         torch.cuda.synchronize()
@@ -293,6 +336,11 @@ def run_ours(args, w, world, rank, local):
             for i in range(K):
                 step_mb(W + i, i if timed_events else None)
             join()
+        elif G > 1:
+            astream.wait_stream(stream)
+            for i in range(K):
+                step_group(W + i, evs[i] if timed_events else None)
+            stream.wait_stream(astream)
         else:
             for i in range(K):
                 step(W + i, evs[i] if timed_events else None)
@@ -315,6 +363,11 @@ def run_ours(args, w, world, rank, local):
         res_ms = np.array([[[e[g][l][0].elapsed_time(e[g][l][1]) for l in range(L)] for g in range(M)] for e in gevs])
         att_ms = np.array([[[e[g][l][1].elapsed_time(e[g][l][2]) for l in range(L)] for g in range(M)] for e in gevs])
         app_ms = np.zeros(1)
+    elif G > 1:
+        # resolves on their own streams, attentions on the main stream after their resolve
+        app_ms = np.zeros(1)
+        res_ms = np.array([[e[l][1].elapsed_time(e[l][2]) for l in range(L)] for e in evs])
+        att_ms = np.array([[e[l][0].elapsed_time(e[l][3]) for l in range(L)] for e in evs])
     else:
         app_ms = np.array([[e[l][0].elapsed_time(e[l][1]) for l in range(L)] for e in evs])
         res_ms = np.array([[e[l][1].elapsed_time(e[l][2]) for l in range(L)] for e in evs])
@@ -325,7 +378,7 @@ def run_ours(args, w, world, rank, local):
 
     # ---- end to end through the public API: inputs from pinned host memory, outputs back -----
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and G == 1:
         e2e = run_e2e(pool, wl, W, K, world, locs, outs, scale)
 
     # ---- host-link peak on this machine: pinned H2D copy, best of 5 ----
@@ -339,6 +392,9 @@ def run_ours(args, w, world, rank, local):
     res_total_s = float(res_ms.sum() / 1e3) / M  # M groups resolve side by side
     link_kernel = "sparse_attn" if fetch == "attention" else "resolve"
     link_s = float(att_ms.sum() / 1e3) / M if fetch == "attention" else res_total_s
+    if G > 1:
+        # the group's resolves overlap one another and the attentions: link rate over the wall time
+        link_kernel, link_s = "resolve (overlapped; whole-step wall time)", max_elapsed
     out = {
         "metric": METRIC, "value": value, "unit": "layer-steps/s", "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": max_elapsed / K * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -347,7 +403,8 @@ def run_ours(args, w, world, rank, local):
                    "buffer_slots": w["B"], "layout": "gqa" if w["layout"] == 1 else "mla", "q_heads": w["Hq"],
                    "kv_heads": w["Hkv"], "record_bytes": rec, "policy": "lru", "keep": w["keep"],
                    "recency_mean": w["mu"], "burst_every": w["burst"], "shared_history": w["shared"],
-                   "append": True, "miss_fetch": fetch, "microbatches": M, "parallelism": f"replicas{world}",
+                   "append": True, "miss_fetch": fetch, "microbatches": M,
+                   "index_share": G, "parallelism": f"replicas{world}",
                    "l2": "inputs larger than L2 (each attention launch gathers "
                          f"{attn_bytes_per_launch(w) / 1e6:.0f} MB; a step touches {L} layers)"},
         "kernel_timing": "second timed pass over the same steps from the same cold start, CUDA events "
@@ -543,6 +600,9 @@ def main():
     ap.add_argument("--fetch", choices=["auto", "resolve", "attention"], default="auto",
                     help="who copies the misses host -> HBM: the resolve kernel, or the attention while it gathers")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--index-share", type=int, default=1,
+                    help="layer groups of this size share one selection; their resolves (and host fetches) "
+                         "run together on side streams, overlapping the attentions (exact layer-group prefetch)")
     ap.add_argument("--no-alt", action="store_true",
                     help="skip the second pass with the miss copies inside the attention (GQA)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -570,6 +630,17 @@ def main():
         out["fetch_in_attention"] = {k: alt[k] for k in ("value", "unit", "ms_per_step", "us_per_layer", "miss_rate",
                                                          "host_link", "clocks", "errors")}
         out["fetch_in_attention"]["hbm_gbs_attention"] = alt["roofline"]["achieved"]
+    if args.fetch == "auto" and w["layout"] == 1 and not args.no_alt and args.index_share == 1 and w["L"] >= 4:
+        # a different workload: layer groups of 4 share one selection (as with a shared indexer), so a
+        # group's resolves and host fetches start together and overlap the attentions (exact
+        # layer-group prefetch); misses copied inside the attention
+        grp_args = argparse.Namespace(**vars(args))
+        grp_args.fetch, grp_args.no_e2e, grp_args.index_share = "attention", True, 4
+        grp = run_ours(grp_args, w, world, rank, local)
+        out["layer_group_prefetch"] = {k: grp[k] for k in ("value", "unit", "ms_per_step", "miss_rate", "host_link",
+                                                           "clocks", "errors")}
+        out["layer_group_prefetch"]["us_per_layer"] = grp["us_per_layer"]["total"]
+        out["layer_group_prefetch"]["workload"] = "same sizes; layer groups of 4 share one top-k selection"
     if rank == 0 and not args.no_cpu_baseline:
         per, desc, n = oracle_sample(w, steps=min(16, args.warmup + args.steps), seed=99, budget_s=args.cpu_seconds)
         out["cpu_baseline"] = {"value": 1.0 / (w["R"] * per), "unit": "layer-steps/s", "cores": 1, "kind": "oracle",

@@ -160,6 +160,62 @@ def test_request_ranges_on_two_streams(layout):
     split.close()
 
 
+@pytest.mark.parametrize("fetch", [0, 1])
+def test_layer_group_schedule_on_side_streams(fetch):
+    """Layer groups sharing one selection (exact layer-group prefetch): the group's resolves run at
+    once, each layer on its own stream, and the attentions follow on another stream as their
+    resolve completes.  Slots, outputs, state and counters are bit-identical to the plain
+    layer-by-layer schedule on a second pool."""
+    cfg = _gqa(4, 4, 3000 + 6, 256, 512, fetch=fetch)
+    sc = Scenario(cfg, ctx0=3000, steps=6, appends=True, seed=67)
+    G = 2
+    for l in range(cfg.num_layers):
+        sc.trace[:, l] = sc.trace[:, G * (l // G)]
+    seq, grp = HsPool(cfg), HsPool(cfg)
+    prefill(seq, sc)
+    prefill(grp, sc)
+    R, L = cfg.num_requests, cfg.num_layers
+    side = [torch.cuda.Stream() for _ in range(G)]
+    astream = torch.cuda.Stream()
+    for t in range(sc.steps):
+        ref = gpu_step(seq, sc, t, fused=True)
+        torch.cuda.synchronize()
+        ins = []
+        for l in range(L):
+            ins.append((torch.from_numpy(sc.trace[t, l]).cuda(),
+                        torch.full((R,), sc.ctx0 + t, dtype=torch.int64, device="cuda"),
+                        bf16_tensor(np.stack([sc.hist[(r, l)][sc.ctx0 + t] for r in range(R)]), "cuda"),
+                        bf16_tensor(sc.q[t, l], "cuda")))
+        torch.cuda.synchronize()
+        locs = [torch.empty((R, cfg.top_k), dtype=torch.int32, device="cuda") for _ in range(L)]
+        outs = [None] * L
+        for l0 in range(0, L, G):
+            known = torch.cuda.Event()
+            known.record(astream)
+            done = []
+            for j, l in enumerate(range(l0, l0 + G)):
+                side[j].wait_event(known)
+                topk, pos, rec, _ = ins[l]
+                grp.append_resolve(l, pos, rec, topk, locs[l], stream=side[j])
+                e = torch.cuda.Event()
+                e.record(side[j])
+                done.append(e)
+            for j, l in enumerate(range(l0, l0 + G)):
+                astream.wait_event(done[j])
+                with torch.cuda.stream(astream):
+                    outs[l] = grp.sparse_attn(l, ins[l][3], locs[l], scale=sc.scale, stream=astream)
+        torch.cuda.synchronize()
+        for l in range(L):
+            assert np.array_equal(locs[l].cpu().numpy(), ref[l][0]), (t, l)
+            assert np.array_equal(outs[l].cpu().numpy(), ref[l][1]), (t, l)
+    for l in range(L):
+        a, b = seq.read_state(l), grp.read_state(l)
+        assert all(np.array_equal(x, y) for x, y in zip(a, b))
+    assert np.array_equal(seq.stats()["per_rl"], grp.stats()["per_rl"])
+    seq.close()
+    grp.close()
+
+
 def test_range_arguments_checked():
     cfg = _gqa(2, 1, 100, 4, 8, kvh=1)
     pool = HsPool(cfg)
