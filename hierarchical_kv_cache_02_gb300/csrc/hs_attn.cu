@@ -1,17 +1,18 @@
 // Sparse attention over resolved slots (HiSparse summary §3 step (4): the physical slots
 // published by RESOLVE go to the sparse-attention backend, which gathers exactly those records).
 //
-// CUDA-core variant, used when few query heads share a KV block (GQA, 4 heads per KV head) and
-// as the MLA fallback.  Design:
-//   * grid (split, request, head group); a split is a fixed range of top-k entries, so the
-//     reduction order depends only on the top-k order and never on which slot holds a record
-//     (cold, warm and fully-resident runs are bit-identical);
-//   * one producer warp gathers whole records HBM -> shared memory with cp.async.bulk into a
-//     3-stage ring guarded by mbarriers (bounded waits); consumer warps own one KV block each;
-//   * per stage, a warp holds G heads x T tokens = 32 logits per lane and reduces them with a
-//     transposed butterfly (31 shuffles for 32 sums), then an online softmax in base 2;
-//   * the last CTA of a (request, head group) to finish combines the split partials in split
-//     order (atomic ticket, no waiting).
+// Kernels in this file:
+//   * k_attn_gqa: GQA records, one CTA per (request, KV head); bulk-copy producers and consumers
+//     on mma.sync in a transposed form (tokens on the MMA's row side);
+//   * k_attn_mla_umma: shared-latent records with 64 query heads on tcgen05 tensor cores, the
+//     accumulators in tensor memory; split partials merged by k_combine;
+//   * k_attn_cc: CUDA-core fallback for other shared-latent head counts (a producer warp gathers
+//     whole records with cp.async.bulk into a 3-stage ring; consumers reduce 32 logits per lane
+//     with a transposed butterfly and keep an online softmax in base 2).
+// In every kernel a split is a fixed range of top-k entries and all reductions run in a fixed
+// order, so the result depends only on the top-k order, never on which slot holds a record:
+// cold, warm and fully-resident runs are bit-identical.  Partials are combined in split order
+// by the last CTA to finish (atomic ticket, no waiting) or by k_combine.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -926,276 +927,8 @@ __global__ void __launch_bounds__((kGqaWarps + kGqaProducers) * 32, 1) k_attn_gq
   if (threadIdx.x == 0) a.ticket[(int64_t)r * (a.groups + 1) + g] = 0u;
 }
 
-// ---- tensor-core variant for shared-latent (MLA) records ---------------------------------
-//
-// All Hq = 64 query heads read the same 576-value latent of every selected token (K = the whole
-// latent, V = its first 512 values).  Per 16-token stage, consumer warp w owns head tile
-// mt = w % 4 (16 heads) and value half dh = w / 4 (256 values):
-//   S[16 x 16] = Q[16 x 576] . K^T      (36 k-steps; the two warps of a head tile compute the
-//                                        same S, so no exchange is needed)
-//   O[16 x 256] += P[16 x 16] . V[16 x 256]
-// on mma.sync m16n8k16 (bf16 in, fp32 accumulate).  The two warps of a head tile each compute half of
-// the 36 k-steps of S and exchange them through shared memory (a + b == b + a: both hold the same
-// S).  P enters the MMA as bf16 and the softmax normaliser sums the same rounded weights, so the
-// output is a convex combination of V rows with weights within 2^-9 (relative) of the exact ones.
-// Q is staged in shared memory once per CTA; records are staged whole (1152 B) by bulk copies into
-// rows padded to 1168 B, so every ldmatrix phase hits eight distinct bank groups.
-constexpr int kMlaStages = 4;
-constexpr int kMlaHeads = 64;
+constexpr int kMlaHeads = 64;  // query heads of the shared-latent tensor-core kernel
 
-template <int NSTAGE>
-__global__ void __launch_bounds__(9 * 32, 1) k_attn_mla_mma(AttnArgs a) {
-  hs_pdl_enter();
-  constexpr int T = kMmaTile;
-  constexpr int NW = 8;
-  constexpr int DK = 576, DV = 512;
-  extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ __align__(8) uint64_t full_bar[NSTAGE];
-  __shared__ __align__(8) uint64_t empty_bar[NSTAGE];
-  __shared__ uint32_t tok_mask[NSTAGE];
-  __shared__ __align__(8) uint64_t xbar[4];  // per head tile: both warps posted their half of S
-  __shared__ uint32_t abort_flag;
-
-  const int split = blockIdx.x, r = a.r0 + (int)blockIdx.y;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t0 = split * a.chunk;
-  const int t1 = min(a.k, t0 + a.chunk);
-  const int n = t1 - t0;
-  const int nst = (n + T - 1) / T;
-  const int64_t rec = a.rec;                 // 1152
-  const uint32_t rs = (uint32_t)rec + 16u;   // padded row stride
-  const uint32_t qs = (uint32_t)DK * 2u + 16u;
-  const int32_t* locs = a.locs + (int64_t)(r - a.r0) * a.k;
-  uint8_t* ring = smem;
-  uint8_t* qsm = smem + (size_t)NSTAGE * T * rs;               // [64][qs]
-  float* xbuf = (float*)(qsm + (size_t)kMlaHeads * qs);          // [2][8 warps][8][32] partial S
-  int32_t* s_locs = (int32_t*)(xbuf + 2 * 8 * 8 * 32);           // [chunk]
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < NSTAGE; ++s) {
-      mbar_init(&full_bar[s], 1u);
-      mbar_init(&empty_bar[s], (uint32_t)NW);
-    }
-    for (int s = 0; s < 4; ++s) mbar_init(&xbar[s], 2u);
-    abort_flag = 0u;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  // queries of this request into shared memory (all warps, 16-byte pieces)
-  {
-    const uint4* qg = (const uint4*)(a.q + (int64_t)(r - a.r0) * kMlaHeads * DK);
-    constexpr int per_row = DK * 2 / 16;  // 72
-    for (int x = threadIdx.x; x < kMlaHeads * per_row; x += blockDim.x) {
-      const int h = x / per_row, c = x - h * per_row;
-      *(uint4*)(qsm + (size_t)h * qs + c * 16) = qg[x];
-    }
-  }
-  if (warp == NW) {
-    bool bad = false;
-    for (int x0 = 0; x0 < n; x0 += 32 * 8) {  // eight loads per lane in flight before their stores
-      int32_t v[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int x = x0 + 32 * u + lane;
-        v[u] = x < n ? locs[t0 + x] : -1;
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int x = x0 + 32 * u + lane;
-        if (x < n) {
-          int32_t loc = v[u];
-          if (loc < -1 || (int64_t)loc >= a.rows) {
-            bad = true;
-            loc = -1;
-          }
-          s_locs[x] = loc;
-        }
-      }
-    }
-    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(a.err, (uint32_t)HS_DEVERR_LOC);
-  }
-  __syncthreads();
-
-  const int grow = lane >> 2, tig = lane & 3;
-  const int mt = warp & 3, dh = warp >> 2;
-  float o[32][4];
-  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-
-  if (warp == NW) {
-    int issued = 0;
-    bool ok = true;
-    for (int st = 0; st < nst; ++st) {
-      const int b = st % NSTAGE;
-      if (st >= NSTAGE) {
-        bool w = true;
-        if (lane == 0) w = mbar_wait_bounded(&empty_bar[b], (uint32_t)((st / NSTAGE - 1) & 1), &abort_flag);
-        if (__shfl_sync(0xffffffffu, w ? 1 : 0, 0) == 0) {
-          ok = false;
-          break;
-        }
-      }
-      const int x = st * T + lane;
-      const int32_t loc = (lane < T && x < n) ? s_locs[x] : -1;
-      const uint32_t mask = __ballot_sync(0xffffffffu, loc >= 0);
-      if (lane == 0) {
-        tok_mask[b] = mask;
-        mbar_arrive_expect_tx(&full_bar[b], (uint32_t)__popc(mask) * (uint32_t)rec);
-      }
-      __syncwarp();
-      if (loc >= 0)
-        bulk_g2s(ring + ((size_t)b * T + lane) * rs, a.kv + ((int64_t)r * a.rows + loc) * rec, (uint32_t)rec,
-                 &full_bar[b]);
-      issued = st + 1;
-    }
-    if (!ok && lane == 0) {
-      *(volatile uint32_t*)&abort_flag = 1u;
-      atomicOr(a.err, (uint32_t)HS_DEVERR_TIMEOUT);
-    }
-    if (abort_flag && lane == 0) {
-      for (int st = max(0, issued - NSTAGE); st < issued; ++st) {
-        volatile uint32_t never = 0u;
-        mbar_wait_bounded(&full_bar[st % NSTAGE], (uint32_t)((st / NSTAGE) & 1), &never);
-      }
-    }
-  } else {
-#pragma unroll
-    for (int n2 = 0; n2 < 32; ++n2) o[n2][0] = o[n2][1] = o[n2][2] = o[n2][3] = 0.f;
-    // ldmatrix rows: Q (A operand, rows = heads), K (non-transposed), V (transposed)
-    const uint32_t qaddr = smem_u32(qsm) + (uint32_t)(mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * qs +
-                           (uint32_t)((lane >> 4) * 16);
-    const int k_tok = (lane & 7) + ((lane >> 4) << 3);
-    const uint32_t k_col = (uint32_t)(((lane >> 3) & 1) * 16);
-    const int v_tok = (lane & 7) + (((lane >> 3) & 1) << 3);
-    const uint32_t v_col = (uint32_t)((lane >> 4) * 16) + (uint32_t)dh * 256u * 2u;
-    const uint32_t ring_u = smem_u32(ring);
-    for (int st = 0; st < nst; ++st) {
-      const int b = st % NSTAGE;
-      if (!mbar_wait_bounded(&full_bar[b], (uint32_t)((st / NSTAGE) & 1), &abort_flag)) {
-        *(volatile uint32_t*)&abort_flag = 1u;
-        atomicOr(a.err, (uint32_t)HS_DEVERR_TIMEOUT);
-        break;
-      }
-      const uint32_t mask = tok_mask[b];
-      const uint32_t kaddr = ring_u + ((uint32_t)b * T + (uint32_t)k_tok) * rs + k_col;
-      const uint32_t vaddr = ring_u + ((uint32_t)b * T + (uint32_t)v_tok) * rs + v_col;
-      // this warp's half of the 36 k-steps of S = Q K^T; the other warp of the head tile does the rest
-      float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
-      float s2[4] = {0.f, 0.f, 0.f, 0.f}, s3[4] = {0.f, 0.f, 0.f, 0.f};
-      const int kbeg = dh * (DK / 32);
-#pragma unroll 3
-      for (int s = 0; s < DK / 32; s += 2) {
-        uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
-        ldsm_x4(qaddr + (kbeg + s) * 32, a0, a1, a2, a3);
-        ldsm_x4(kaddr + (kbeg + s) * 32, b0, b1, b2, b3);
-        mma_bf16(s0, a0, a1, a2, a3, b0, b1);
-        mma_bf16(s1, a0, a1, a2, a3, b2, b3);
-        ldsm_x4(qaddr + (kbeg + s + 1) * 32, a0, a1, a2, a3);
-        ldsm_x4(kaddr + (kbeg + s + 1) * 32, b0, b1, b2, b3);
-        mma_bf16(s2, a0, a1, a2, a3, b0, b1);
-        mma_bf16(s3, a0, a1, a2, a3, b2, b3);
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        s0[i] += s2[i];
-        s1[i] += s3[i];
-      }
-      {
-        // exchange halves through shared memory; a + b == b + a, so both warps hold the same S
-        float* mine = xbuf + ((st & 1) * 8 + warp) * 256;
-        const float* other = xbuf + ((st & 1) * 8 + (warp ^ 4)) * 256;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          mine[i * 32 + lane] = s0[i];
-          mine[(4 + i) * 32 + lane] = s1[i];
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&xbar[mt]);
-        if (!mbar_wait_bounded(&xbar[mt], (uint32_t)(st & 1), &abort_flag)) {
-          *(volatile uint32_t*)&abort_flag = 1u;
-          atomicOr(a.err, (uint32_t)HS_DEVERR_TIMEOUT);
-          break;
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          s0[i] += other[i * 32 + lane];
-          s1[i] += other[(4 + i) * 32 + lane];
-        }
-      }
-      // online softmax for rows grow (c0, c1) and grow + 8 (c2, c3)
-      const int ta = 2 * tig;
-      const bool v0 = (mask >> ta) & 1u, v1 = (mask >> (ta + 1)) & 1u, v2 = (mask >> (ta + 8)) & 1u,
-                 v3 = (mask >> (ta + 9)) & 1u;
-      float p[2][4];
-#pragma unroll
-      for (int hr = 0; hr < 2; ++hr) {
-        const float x0 = v0 ? s0[2 * hr] * a.qscale : -INFINITY;
-        const float x1 = v1 ? s0[2 * hr + 1] * a.qscale : -INFINITY;
-        const float x2 = v2 ? s1[2 * hr] * a.qscale : -INFINITY;
-        const float x3 = v3 ? s1[2 * hr + 1] * a.qscale : -INFINITY;
-        float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float m_new = fmaxf(m_run[hr], mx);
-        const bool any = m_new != -INFINITY;
-        const float alpha = any ? exp2f(m_run[hr] - m_new) : 1.f;
-        // weights rounded to bf16 here, so the normaliser sums exactly what the MMA multiplies
-        p[hr][0] = any ? __bfloat162float(__float2bfloat16_rn(exp2f(x0 - m_new))) : 0.f;
-        p[hr][1] = any ? __bfloat162float(__float2bfloat16_rn(exp2f(x1 - m_new))) : 0.f;
-        p[hr][2] = any ? __bfloat162float(__float2bfloat16_rn(exp2f(x2 - m_new))) : 0.f;
-        p[hr][3] = any ? __bfloat162float(__float2bfloat16_rn(exp2f(x3 - m_new))) : 0.f;
-        float ps = (p[hr][0] + p[hr][1]) + (p[hr][2] + p[hr][3]);
-        ps += __shfl_xor_sync(0xffffffffu, ps, 1);
-        ps += __shfl_xor_sync(0xffffffffu, ps, 2);
-        m_run[hr] = m_new;
-        l_run[hr] = l_run[hr] * alpha + ps;
-#pragma unroll
-        for (int n2 = 0; n2 < 32; ++n2) {
-          o[n2][2 * hr] *= alpha;
-          o[n2][2 * hr + 1] *= alpha;
-        }
-      }
-      // P (A operand, bf16): a0 rows grow / tokens 0-7, a1 rows grow+8, a2 / a3 tokens 8-15
-      const uint32_t h0 = pack_bf16(p[0][0], p[0][1]), h1 = pack_bf16(p[1][0], p[1][1]);
-      const uint32_t h2 = pack_bf16(p[0][2], p[0][3]), h3 = pack_bf16(p[1][2], p[1][3]);
-      uint32_t vm_lo = 0xffffffffu, vm_hi = 0xffffffffu;
-      if (mask != 0xffffu) {
-        vm_lo = (v0 ? 0x0000ffffu : 0u) | (v1 ? 0xffff0000u : 0u);
-        vm_hi = (v2 ? 0x0000ffffu : 0u) | (v3 ? 0xffff0000u : 0u);
-      }
-#pragma unroll
-      for (int pr = 0; pr < 16; ++pr) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(vaddr + pr * 32, b0, b1, b2, b3);
-        b0 &= vm_lo;
-        b1 &= vm_hi;
-        b2 &= vm_lo;
-        b3 &= vm_hi;
-        mma_bf16(o[2 * pr], h0, h1, h2, h3, b0, b1);
-        mma_bf16(o[2 * pr + 1], h0, h1, h2, h3, b2, b3);
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty_bar[b]);
-    }
-    if (!abort_flag) {
-#pragma unroll
-      for (int hr = 0; hr < 2; ++hr) {
-        const int h = mt * 16 + grow + 8 * hr;
-        const int64_t ph = ((int64_t)r * a.S + split) * a.Hq + h;
-        float* po = a.part + ph * DV + dh * 256;
-#pragma unroll
-        for (int n2 = 0; n2 < 32; ++n2)
-          *(float2*)(po + n2 * 8 + 2 * tig) = make_float2(o[n2][2 * hr], o[n2][2 * hr + 1]);
-        if (tig == 0 && dh == 0) {
-          a.ml[ph * 2 + 0] = m_run[hr];
-          a.ml[ph * 2 + 1] = l_run[hr];
-        }
-      }
-    }
-  }
-  // the split partials are combined by k_combine, launched right after this kernel
-}
-
-// Split combine as its own launch: one warp per (request, head), so the 64-head x 512-value partials
-// of the shared-latent layout are reduced by the whole GPU instead of one CTA per request.
 template <int DV>
 __global__ void __launch_bounds__(256) k_combine(AttnArgs a) {
   hs_pdl_enter();
@@ -1209,10 +942,398 @@ __global__ void __launch_bounds__(256) k_combine(AttnArgs a) {
     combine_heads<DV>(a, r, h, 1, lane);
 }
 
+// ---- shared-latent records on tcgen05 tensor cores (64 heads) -----------------------------
+//
+// One CTA per (request, split of the top-k list); a split is walked in 128-token tiles.  Per tile,
+// with tokens on the MMA's 128-row side and the 64 heads on its N side:
+//   S^T[128 x 64] = K[128 x 576] . Q^T       36 tcgen05.mma (K = 16 each) into TMEM columns 0-63
+//   O^T[512 x 64] += V^T[512 x 128] . P^T    4 row tiles x 8 k-steps into TMEM columns 64-319
+// Operands sit in shared memory in the canonical no-swizzle layout (8 x 16-byte core matrices).
+// The gathered tile is one buffer of 128 rows: as K it is read K-major (core matrices 128 B apart
+// along the dims, 9216 B apart along the tokens), as V^T MN-major from the same bytes.  Q is streamed
+// per tile in two halves of 288 dims; P^T is written MN-major (heads contiguous).
+// Roles: eight producer warps gather rows with cp.async straight into that layout (padding rows
+// zero-filled) and arrive on mbarriers when their copies land; one thread issues the MMAs and
+// commits them to mbarriers; a 128-thread warpgroup (one token, i.e. one TMEM lane, per thread)
+// runs the softmax.  The running max per head is raised only when a score exceeds it by more than
+// 2^8 (softmax is shift-invariant; weights stay <= 256 in bf16 and fp32), and only then is the O^T
+// accumulator rescaled in TMEM.  The normaliser sums the same bf16-rounded weights the MMA uses.
+// The split partials (O, max, sum) are combined by k_combine in split order.
+constexpr int kUTok = 128, kUHeads = 64, kUDim = 576;
+constexpr int kUKv = kUTok * kUDim * 2;              // 147456 B: gathered tile
+constexpr int kUQh = kUHeads * (kUDim / 2) * 2;      // 36864 B: half of Q
+constexpr int kUP = kUTok * kUHeads * 2;             // 16384 B: P^T
+constexpr int kUSboKv = (kUDim / 8) * 128;           // 9216 B between 8-token groups of the tile
+constexpr int kUSboQ = (kUDim / 2 / 8) * 128;        // 4608 B between 8-head groups of a Q half
+constexpr int kUProd = 8;                            // producer warps
+constexpr int kUWarpMma = 4;                         // warp of the MMA issuer
+constexpr int kUThreads = (4 + 1 + kUProd) * 32;
+constexpr float kULazy = 8.f;                        // log2 headroom before the max is raised
+
+// 16-byte cp.async; src_bytes = 0 writes zeros (nothing is read)
+__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+// one arrival on *bar once every cp.async this thread issued before has landed
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ uint64_t umma_sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  // start address, leading / stride byte offsets (16-byte units), descriptor version 1, no swizzle
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46);
+}
+__device__ __forceinline__ uint32_t umma_idesc_bf16(int M, int N, int a_mn, int b_mn) {
+  // fp32 accumulator, bf16 A and B, operand majors, N / 8, M / 16
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ void umma_bf16(uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+               "l"(a), "l"(b), "r"(id), "r"(acc)
+               : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t x[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3]), "=r"(x[4]), "=r"(x[5]), "=r"(x[6]), "=r"(x[7]),
+        "=r"(x[8]), "=r"(x[9]), "=r"(x[10]), "=r"(x[11]), "=r"(x[12]), "=r"(x[13]), "=r"(x[14]), "=r"(x[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(x[i]);
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+      "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+      "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])),
+      "r"(__float_as_uint(v[11])), "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])),
+      "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15]))
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void named_sync_128() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// 32 partial maxima per lane -> lane l holds the warp-wide max of value l (transposed butterfly)
+__device__ __forceinline__ float reduce32_max_transposed(float (&v)[32], int lane) {
+#pragma unroll
+  for (int step = 0; step < 5; ++step) {
+    const int off = 16 >> step;
+    const int n = 32 >> step;
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      const float send = upper ? v[i] : v[i + n / 2];
+      const float keep = upper ? v[i + n / 2] : v[i];
+      v[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, off));
+    }
+  }
+  return v[0];
+}
+
+__global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_umma(AttnArgs a) {
+  hs_pdl_enter();
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* sKV = smem;
+  uint8_t* sQ = smem + kUKv;
+  uint8_t* sP = sQ + kUQh;
+  int32_t* s_locs = (int32_t*)(sP + kUP);  // [chunk]
+  __shared__ __align__(8) uint64_t bar_kv, bar_q, bar_qfree, bar_s, bar_p, bar_pv, bar_fin;
+  __shared__ uint32_t s_tmem, abort_flag;
+  __shared__ float s_m[kUHeads], s_l[kUHeads], s_alpha[kUHeads], s_red[4][kUHeads];
+  __shared__ uint32_t s_need[2][4];
+
+  const int split = blockIdx.x, r = a.r0 + (int)blockIdx.y;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int t0 = split * a.chunk;
+  const int n = min(a.k, t0 + a.chunk) - t0;
+  const int ntile = (n + kUTok - 1) / kUTok;
+  if (tid == 0) {
+    mbar_init(&bar_kv, kUProd * 32);  // one arrival per producer lane once its copies landed
+    mbar_init(&bar_q, kUProd * 32);
+    mbar_init(&bar_qfree, 1u);        // MMA commits
+    mbar_init(&bar_s, 1u);
+    mbar_init(&bar_pv, 1u);
+    mbar_init(&bar_fin, 1u);
+    mbar_init(&bar_p, 128u);          // softmax threads
+    abort_flag = 0u;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  for (int h = tid; h < kUHeads; h += kUThreads) {
+    s_m[h] = -INFINITY;
+    s_l[h] = 0.f;
+  }
+  {
+    const int32_t* locs = a.locs + (int64_t)(r - a.r0) * a.k + t0;
+    bool bad = false;
+    for (int x = tid; x < n; x += kUThreads) {
+      int32_t loc = locs[x];
+      if (loc < -1 || (int64_t)loc >= a.rows) {
+        bad = true;
+        loc = -1;
+      }
+      s_locs[x] = loc;
+    }
+    if (bad) atomicOr(a.err, (uint32_t)HS_DEVERR_LOC);
+  }
+  if (warp == kUWarpMma) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(&s_tmem))
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = s_tmem;
+
+  if (warp > kUWarpMma) {
+    // ---------------- producers: Q halves and gathered tiles, cp.async into the MMA layout ----------------
+    const int pw = warp - kUWarpMma - 1, pl = pw * 32 + lane;
+    const uint16_t* qr = a.q + (int64_t)(r - a.r0) * a.Hq * kUDim;
+    const uint32_t sq_u = smem_u32(sQ), skv_u = smem_u32(sKV);
+    const uint8_t* kvr = a.kv + (int64_t)r * a.rows * a.rec;
+    bool ok = true;
+    auto load_q = [&](int g) {  // global half index g = 2 tile + half
+      if (g >= 1) {
+        bool w = true;
+        if (lane == 0) w = mbar_wait_bounded(&bar_qfree, (uint32_t)((g - 1) & 1), &abort_flag);
+        if (__shfl_sync(0xffffffffu, w ? 1 : 0, 0) == 0) return false;
+      }
+      const int half = g & 1;
+      for (int e = pl; e < kUHeads * 36; e += kUProd * 32) {
+        const int ng = e / 288, rem = e % 288, c = rem / 8, hn = ng * 8 + rem % 8;
+        cp_async16_zfill(sq_u + (uint32_t)(ng * kUSboQ + c * 128 + (rem % 8) * 16),
+                         qr + (int64_t)hn * kUDim + half * 288 + c * 8, 16u);
+      }
+      cp_async_arrive_noinc(&bar_q);
+      return true;
+    };
+    for (int i = 0; ok && i < ntile; ++i) {
+      ok = load_q(2 * i);
+      if (!ok) break;
+      if (i >= 1) {
+        bool w = true;
+        if (lane == 0) w = mbar_wait_bounded(&bar_pv, (uint32_t)((i - 1) & 1), &abort_flag);
+        if (__shfl_sync(0xffffffffu, w ? 1 : 0, 0) == 0) {
+          ok = false;
+          break;
+        }
+      }
+      // this warp's two 8-token groups: lane -> row (lane & 7), 16-byte column 4 j + (lane >> 3)
+#pragma unroll
+      for (int g2 = 0; g2 < 2; ++g2) {
+        const int rg = 2 * pw + g2;
+        const int row = rg * 8 + (lane & 7);
+        const int x = i * kUTok + row;
+        const int32_t loc = x < n ? s_locs[x] : -1;
+        const uint8_t* src = kvr + (loc >= 0 ? (int64_t)loc * a.rec : 0);
+        const uint32_t dst = skv_u + (uint32_t)(rg * kUSboKv + (lane & 7) * 16);
+        const uint32_t nb = loc >= 0 ? 16u : 0u;
+#pragma unroll 6
+        for (int j = 0; j < 18; ++j) {
+          const int c = 4 * j + (lane >> 3);
+          cp_async16_zfill(dst + (uint32_t)(c * 128), src + c * 16, nb);
+        }
+      }
+      cp_async_arrive_noinc(&bar_kv);
+      ok = load_q(2 * i + 1);
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    if (!ok && lane == 0) {
+      *(volatile uint32_t*)&abort_flag = 1u;
+      atomicOr(a.err, (uint32_t)HS_DEVERR_TIMEOUT);
+    }
+  } else if (warp == kUWarpMma) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      const uint32_t id_s = umma_idesc_bf16(128, 64, 0, 0), id_o = umma_idesc_bf16(128, 64, 1, 1);
+      const uint32_t skv_u = smem_u32(sKV), sq_u = smem_u32(sQ), sp_u = smem_u32(sP);
+      bool ok = true;
+      for (int i = 0; ok && i < ntile; ++i) {
+        for (int half = 0; half < 2 && ok; ++half) {
+          ok = mbar_wait_bounded(&bar_q, (uint32_t)((2 * i + half) & 1), &abort_flag);
+          if (ok && half == 0) ok = mbar_wait_bounded(&bar_kv, (uint32_t)(i & 1), &abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll 6
+          for (int s2 = 0; s2 < 18; ++s2) {
+            const uint64_t da = umma_sdesc(skv_u + (uint32_t)((36 * half + 2 * s2) * 128), 128, kUSboKv);
+            const uint64_t db = umma_sdesc(sq_u + (uint32_t)(2 * s2 * 128), 128, kUSboQ);
+            umma_bf16(tb, da, db, id_s, (half | s2) != 0 ? 1u : 0u);
+          }
+          umma_commit(&bar_qfree);
+        }
+        if (!ok) break;
+        umma_commit(&bar_s);
+        ok = mbar_wait_bounded(&bar_p, (uint32_t)(i & 1), &abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint64_t da = umma_sdesc(skv_u + (uint32_t)(mt * 16 * 128 + ks * 2 * kUSboKv), kUSboKv, 128);
+            const uint64_t db = umma_sdesc(sp_u + (uint32_t)(ks * 2 * 1024), 1024, 128);
+            umma_bf16(tb + 64u + 64u * (uint32_t)mt, da, db, id_o, (i | ks) != 0 ? 1u : 0u);
+          }
+        }
+        umma_commit(&bar_pv);
+      }
+      if (!ok) {
+        *(volatile uint32_t*)&abort_flag = 1u;
+        atomicOr(a.err, (uint32_t)HS_DEVERR_TIMEOUT);
+      }
+      // every MMA issued has completed before the accumulator can be released
+      umma_commit(&bar_fin);
+      volatile uint32_t never = 0u;
+      mbar_wait_bounded(&bar_fin, 0u, &never);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- softmax warpgroup: thread = token of the tile = TMEM lane ----------------
+    // Every thread of the warpgroup passes the same sequence of named barriers on every tile: a
+    // wait that gives up only marks the thread (ok = false, no TMEM access, zero weights), so a
+    // barrier can never miss a thread.
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    bool ok = true;
+    for (int i = 0; i < ntile; ++i) {
+      if (ok) ok = mbar_wait_bounded(&bar_s, (uint32_t)(i & 1), &abort_flag);
+      // the previous tile's O^T update has read P^T (and is complete before any rescale)
+      if (ok && i >= 1) ok = mbar_wait_bounded(&bar_pv, (uint32_t)((i - 1) & 1), &abort_flag);
+      tc_fence_after();
+      const int x = i * kUTok + tid;
+      const bool valid = ok && x < n && s_locs[x] >= 0;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {  // heads [32 hh, 32 hh + 32)
+        float v[32];
+        auto load_scores = [&]() {
+          float t16[16];
+          if (!ok) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = -INFINITY;
+            return;
+          }
+          tmem_ld16(tb + lane_base + (uint32_t)(32 * hh), t16);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = valid ? t16[j] * a.qscale : -INFINITY;
+          tmem_ld16(tb + lane_base + (uint32_t)(32 * hh + 16), t16);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[16 + j] = valid ? t16[j] * a.qscale : -INFINITY;
+        };
+        load_scores();
+        bool need = false;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) need |= v[j] > s_m[32 * hh + j] + kULazy;
+        const int par = (2 * i + hh) & 1;
+        const bool need_w = __any_sync(0xffffffffu, need);
+        if (lane == 0) s_need[par][warp] = need_w ? 1u : 0u;
+        named_sync_128();
+        const bool any = (s_need[par][0] | s_need[par][1] | s_need[par][2] | s_need[par][3]) != 0u;
+        if (any) {
+          // exact tile max per head, then raise the running max where needed and rescale
+          const float wm = reduce32_max_transposed(v, lane);  // head 32 hh + lane over this warp's tokens
+          s_red[warp][32 * hh + lane] = wm;
+          named_sync_128();
+          if (tid < 32) {
+            const int h = 32 * hh + tid;
+            const float tmax = fmaxf(fmaxf(s_red[0][h], s_red[1][h]), fmaxf(s_red[2][h], s_red[3][h]));
+            const float mo = s_m[h];
+            const float mn = tmax > mo + kULazy ? tmax : mo;
+            // a head with nothing accumulated yet has zero sums and accumulators: nothing to scale
+            s_alpha[h] = (mn == mo || mo == -INFINITY) ? 1.f : fast_exp2(mo - mn);
+            s_m[h] = mn;
+            s_l[h] *= s_alpha[h];
+          }
+          named_sync_128();
+          bool resc = false;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) resc |= s_alpha[32 * hh + j] != 1.f;
+          if (resc && ok) {
+            if (i >= 1) {
+              // O^T columns of these heads, all four 128-dim row tiles, scaled in TMEM
+#pragma unroll 1
+              for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll
+                for (int c0 = 0; c0 < 32; c0 += 16) {
+                  float o[16];
+                  const uint32_t ta = tb + lane_base + 64u + 64u * (uint32_t)mt + (uint32_t)(32 * hh + c0);
+                  tmem_ld16(ta, o);
+#pragma unroll
+                  for (int j = 0; j < 16; ++j) o[j] *= s_alpha[32 * hh + c0 + j];
+                  tmem_st16(ta, o);
+                }
+              }
+            }
+          }
+          load_scores();
+        }
+        // weights (bf16) and P^T: heads contiguous, 8-token groups 1024 B apart
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float m0 = s_m[32 * hh + 2 * j], m1 = s_m[32 * hh + 2 * j + 1];
+          pk[j] = pack_bf16(valid ? fast_exp2(v[2 * j] - m0) : 0.f, valid ? fast_exp2(v[2 * j + 1] - m1) : 0.f);
+          v[2 * j] = __uint_as_float(pk[j] << 16);  // the rounded weights, as the MMA sees them
+          v[2 * j + 1] = __uint_as_float(pk[j] & 0xffff0000u);
+        }
+        uint8_t* prow = sP + (tid >> 3) * 1024 + (tid & 7) * 16;
+#pragma unroll
+        for (int hg = 0; hg < 4; ++hg)
+          *(uint4*)(prow + (4 * hh + hg) * 128) = make_uint4(pk[4 * hg], pk[4 * hg + 1], pk[4 * hg + 2], pk[4 * hg + 3]);
+        // this tile's weight sums per head: this warp's tokens, then the four warps in order
+        s_red[warp][32 * hh + lane] = reduce32_transposed(v, lane);
+      }
+      named_sync_128();
+      if (tid < kUHeads) s_l[tid] += (s_red[0][tid] + s_red[1][tid]) + (s_red[2][tid] + s_red[3][tid]);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // P^T is read by the tensor cores
+      tc_fence_before();
+      mbar_arrive(&bar_p);
+    }
+    if (ok) ok = mbar_wait_bounded(&bar_pv, (uint32_t)((ntile - 1) & 1), &abort_flag);
+    if (!ok) {
+      *(volatile uint32_t*)&abort_flag = 1u;
+      atomicOr(a.err, (uint32_t)HS_DEVERR_TIMEOUT);
+    }
+    tc_fence_after();
+    named_sync_128();
+    if (ok && abort_flag == 0u) {
+      const int64_t ph0 = ((int64_t)r * a.S + split) * a.Hq;
+      if (tid < kUHeads) *(float2*)(a.ml + (ph0 + tid) * 2) = make_float2(s_m[tid], s_l[tid]);
+      // O^T rows (value dims) of this thread, every head
+#pragma unroll 1
+      for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll
+        for (int c0 = 0; c0 < kUHeads; c0 += 16) {
+          float o[16];
+          tmem_ld16(tb + lane_base + 64u + 64u * (uint32_t)mt + (uint32_t)c0, o);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) a.part[(ph0 + c0 + j) * 512 + mt * 128 + tid] = o[j];
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kUWarpMma) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tb) : "memory");
+}
+
 // ---- dispatch ----------------------------------------------------------------
 
 struct Plan {
-  int kind;  // 0: CUDA-core shared-latent, 1: GQA per KV head, 2: shared-latent mma, 3: GQA with the miss fetch
+  int kind;  // 0: CUDA-core shared-latent, 1: GQA per KV head, 4: shared-latent on tcgen05
   int NW, G, T, groups, S, chunk;
   int fetch;  // 1: the GQA kernel also copies the misses the resolve left pending
   size_t smem;
@@ -1235,14 +1356,14 @@ bool plan_for(const hs_config* c, int num_sms, Plan* pl) {
     pl->smem = (size_t)kGqaWarps * kGqaStages * kMmaTile * kGqaRow;
     per_cta_wave = 1;  // one CTA per SM: the staging buffers hold most of the shared memory
   } else if (c->head_dim_qk == 576 && c->head_dim_v == 512 && c->num_q_heads == kMlaHeads) {
-    pl->kind = 2;
+    // tcgen05 kernel: 128-token tiles; the tile, a Q half and P^T take the shared memory
+    pl->kind = 4;
     pl->fetch = 0;
-    pl->NW = 8;
+    pl->NW = 4;
     pl->G = kMlaHeads;
     pl->groups = 1;
-    pl->T = kMmaTile;
-    pl->smem = (size_t)kMlaStages * kMmaTile * (size_t)(rec + 16) + (size_t)kMlaHeads * (576 * 2 + 16) +
-               2 * 8 * 8 * 32 * sizeof(float);
+    pl->T = kUTok;
+    pl->smem = (size_t)kUKv + kUQh + kUP;
     per_cta_wave = 1;
   } else {
     if (c->head_dim_qk != 576 || c->head_dim_v != 512) return false;
@@ -1265,7 +1386,7 @@ bool plan_for(const hs_config* c, int num_sms, Plan* pl) {
   pl->chunk = chunk;
   pl->S = (c->top_k + chunk - 1) / chunk;
 
-  if (pl->kind == 2) pl->smem += (size_t)chunk * 4;   // slot list
+  if (pl->kind == 4) pl->smem += (size_t)chunk * 4;   // slot list
   return pl->smem <= 220 * 1024;
 }
 
@@ -1293,8 +1414,8 @@ cudaError_t launch_kernel(K kern, const AttnArgs* a, const Plan& pl, int threads
 
 
 cudaError_t dispatch(const hs_config& c, const AttnArgs* a, const Plan& pl, cudaStream_t st) {
-  if (pl.kind == 2) {
-    cudaError_t e = launch_kernel(k_attn_mla_mma<kMlaStages>, a, pl, 9 * 32, st);
+  if (pl.kind == 4) {
+    cudaError_t e = launch_kernel(k_attn_mla_umma, a, pl, kUThreads, st);
     if (e == cudaSuccess && a == nullptr)
       e = cudaFuncSetAttribute(k_combine<512>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                (int)cudaSharedmemCarveoutMaxShared);
