@@ -41,6 +41,11 @@ WORKLOADS = {
     # stress: batch 16, 4 layers, MLA, ctx 262144, k 2048, B 8192, bursts every 32 steps
     "stress_b16_l4": dict(R=16, L=4, ctx0=262144, layout=0, Hq=64, Hkv=1, Dqk=576, Dv=512, k=2048, B=8192,
                           keep=0.88, mu=2048.0, burst=32, shared=False, steps=128),
+    # compressed entries (one record per 4 tokens): batch 8, 1 layer, 32768-token context = 8192
+    # entries, top-512 entries (2048 tokens), B 1024, MLA latent, 64 heads; an entry is complete only
+    # after 4 tokens, so the decode steps append nothing
+    "csa_b8": dict(R=8, L=1, ctx0=8192, layout=0, Hq=64, Hkv=1, Dqk=576, Dv=512, k=512, B=1024,
+                   keep=0.88, mu=512.0, burst=0, shared=False, steps=128, appends=False),
     # tiny: 1 request, 1 layer, MLA 16 heads, ctx 4096, k 256, B 512, keep 90%, recency 512
     "tiny": dict(R=1, L=1, ctx0=4096, layout=0, Hq=16, Hkv=1, Dqk=576, Dv=512, k=256, B=512,
                  keep=0.9, mu=512.0, burst=0, shared=False, steps=64),
@@ -166,8 +171,9 @@ class Workload:
                             top_k=k, buffer_slots=w["B"], policy=0, seed=seed, io_chunk_bytes=64,
                             shared_prefix=w["ctx0"] if w["shared"] else 0,
                             fetch_in_attention=1 if fetch == "attention" else 0)
+        self.appends = w.get("appends", True)
         spec = inputs.TraceSpec(ctx0=w["ctx0"], k=k, steps=steps, keep=w["keep"], recency_mean=w["mu"],
-                                appends=True, burst_every=w["burst"], far_gap=int(8 * w["mu"]))
+                                appends=self.appends, burst_every=w["burst"], far_gap=int(8 * w["mu"]))
         t0 = time.time()
         self.trace_host = inputs.drift_traces(spec, R, L, seed=seed)            # [S][L][R][k]
         if index_share > 1:
@@ -228,11 +234,11 @@ def run_ours(args, w, world, rank, local):
         for l in range(L):
             if ev is not None:
                 ev[l][0].record(stream)
-            if args.separate_append:
+            if args.separate_append and wl.appends:
                 pool.append(l, wl.pos[t], wl.app[t, l])
             if ev is not None:
                 ev[l][1].record(stream)
-            if args.separate_append:
+            if args.separate_append or not wl.appends:
                 pool.resolve(l, wl.topk[t, l], locs[l])
             else:
                 pool.append_resolve(l, wl.pos[t], wl.app[t, l], wl.topk[t, l], locs[l])
@@ -261,7 +267,10 @@ def run_ours(args, w, world, rank, local):
                 with torch.cuda.stream(st):
                     if ev is not None:
                         ev[l][1].record(st)
-                    pool.append_resolve(l, wl.pos[t], wl.app[t, l], wl.topk[t, l], locs[l], stream=st)
+                    if wl.appends:
+                        pool.append_resolve(l, wl.pos[t], wl.app[t, l], wl.topk[t, l], locs[l], stream=st)
+                    else:
+                        pool.resolve(l, wl.topk[t, l], locs[l], stream=st)
                     if ev is not None:
                         ev[l][2].record(st)
                 e = torch.cuda.Event()
@@ -464,7 +473,10 @@ def run_e2e(pool, wl, W, K, world, locs, outs, scale):
         d_app.copy_(h_app[t], non_blocking=True)
         d_pos.copy_(h_pos[t], non_blocking=True)
         for l in range(L):
-            pool.append_resolve(l, d_pos, d_app[l], d_topk[l], locs[l])
+            if wl.appends:
+                pool.append_resolve(l, d_pos, d_app[l], d_topk[l], locs[l])
+            else:
+                pool.resolve(l, d_topk[l], locs[l])
             pool.sparse_attn(l, d_q[l], locs[l], outs[l], scale=scale)
             h_out[t, l].copy_(outs[l], non_blocking=True)
 
@@ -535,7 +547,8 @@ def oracle_sample(w, steps, seed, budget_s, pairs_max=64):
     from hierarchical_kv_cache_02_gb300 import inputs
 
     R, L, k = w["R"], w["L"], w["k"]
-    spec = inputs.TraceSpec(ctx0=w["ctx0"], k=k, steps=steps, keep=w["keep"], recency_mean=w["mu"], appends=True,
+    appends = w.get("appends", True)
+    spec = inputs.TraceSpec(ctx0=w["ctx0"], k=k, steps=steps, keep=w["keep"], recency_mean=w["mu"], appends=appends,
                             burst_every=w["burst"], far_gap=int(8 * w["mu"]))
     E = record_bytes(w) // 2
     kvh = 0 if w["layout"] == 0 else w["Hkv"]
@@ -551,7 +564,8 @@ def oracle_sample(w, steps, seed, budget_s, pairs_max=64):
         cache = oracle.Cache(w["B"], k, "lru", R=R, L=L, r=r, l=l, C=w["ctx0"] + steps)
         t0 = time.perf_counter()
         for t in range(steps):
-            cache.append(w["ctx0"] + t)
+            if appends:
+                cache.append(w["ctx0"] + t)
             cache.resolve(tr[t])
             oracle.attention(q[t], hist, tr[t], scale, kvh, w["Dqk"], w["Dv"])
             n_rl_steps += 1

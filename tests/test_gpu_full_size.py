@@ -135,6 +135,19 @@ def test_full_stress_bursts():
     run_full(cfg, ctx0, steps, spec, pairs, samples, seed=17, state_every=16)
 
 
+def test_full_csa_batch8():
+    """Compressed entries (one record per 4 tokens): batch 8, 1 layer, 8192 entries (a 32768-token
+    context), 576-dim latent, 64 heads, top-512 entries, B=1024, LRU, 96 steps, no appends (an entry
+    is complete only after 4 tokens)."""
+    ctx0, steps = 8192, 96
+    cfg = HsConfig(num_requests=8, num_layers=1, capacity=ctx0, layout=LAYOUT_MLA, num_q_heads=64,
+                   num_kv_heads=1, head_dim_qk=576, head_dim_v=512, top_k=512, buffer_slots=1024, seed=19)
+    spec = inputs.TraceSpec(ctx0=ctx0, k=512, steps=steps, keep=0.88, recency_mean=512, appends=False)
+    pairs = [(1, 0), (6, 0)]
+    samples = {(0, 1, 0), (95, 6, 0), (48, 1, 0)}
+    run_full(cfg, ctx0, steps, spec, pairs, samples, seed=23, appends=False)
+
+
 def test_policy_sweep_miss_curves():
     """One request, context 131072, k=2048, 256 steps, keep 85%: swap-vanilla B=2048, LRU / FIFO /
     random B=4096, LRU B=8192.  Per-step miss curves of the GPU equal the oracle's bit for bit, and
