@@ -15,12 +15,13 @@ STATUS_NAMES = {0: "HS_OK", -1: "HS_ERR_CONFIG", -2: "HS_ERR_ALLOC_HOST", -3: "H
 POLICY_LRU, POLICY_FIFO, POLICY_RANDOM, POLICY_SWAP_VANILLA = 0, 1, 2, 3
 LAYOUT_MLA, LAYOUT_GQA = 0, 1
 DEVERR_RANGE, DEVERR_DUP, DEVERR_CLOCK, DEVERR_APPEND, DEVERR_LOC, DEVERR_TIMEOUT = 1, 2, 4, 8, 16, 32
+DEVERR_PAGE = 64
 
 # every entry point include/hisparse.h declares
 EXPORTS = ("hs_record_bytes", "hs_pool_create", "hs_pool_destroy", "hs_pool_reset", "hs_prefill_write",
            "hs_append_writethrough", "hs_resolve", "hs_sparse_attn", "hs_stats", "hs_read_state",
            "hs_read_buffer", "hs_read_history", "hs_sparse_attn_noalloc", "hs_append_resolve",
-           "hs_resolve_range", "hs_sparse_attn_range")
+           "hs_resolve_range", "hs_sparse_attn_range", "hs_reserve", "hs_release", "hs_host_usage")
 
 
 class hs_config(ctypes.Structure):
@@ -41,6 +42,8 @@ class hs_config(ctypes.Structure):
         ("io_chunk_bytes", ctypes.c_int32),
         ("log_steps", ctypes.c_int32),
         ("fetch_in_attention", ctypes.c_int32),
+        ("host_page_tokens", ctypes.c_int32),
+        ("host_on_demand", ctypes.c_int32),
     ]
 
 
@@ -94,6 +97,9 @@ def load(build_if_missing: bool = False):
             "hs_append_resolve": (I, [P, I, P, P, P, P, P]),
             "hs_resolve_range": (I, [P, I, I, I, P, P, P, P, P]),
             "hs_sparse_attn_range": (I, [P, I, I, I, P, P, F, P, P]),
+            "hs_reserve": (I, [P, I, I, I64]),
+            "hs_release": (I, [P, I]),
+            "hs_host_usage": (I, [P, P, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)

@@ -40,12 +40,9 @@ struct AttnArgs {
   int R, Hq, k, S, chunk, groups;  // R: requests in this launch (the grid), starting at r0
   int r0;                   // first request: q, locs and out are indexed from it, pool state absolutely
   // fetch-in-attention mode (hot-buffer rows only): misses still to copy from the host history
-  const int2* pend;         // [R][k] {position, slot} or {-1, -1}; null when nothing is pending
+  const hs_pending* pend;   // [R][k] host address and slot of a miss still to copy (src 0: none); null: none
   uint32_t* pend_live;      // [R]
   uint8_t* buf_w;           // writable view of the rows (the hot buffer of the layer)
-  const uint8_t* hist_shared;
-  const uint8_t* hist_priv;
-  int64_t P0, priv_tokens;
   int L, layer;
 };
 
@@ -612,48 +609,50 @@ __global__ void __launch_bounds__((kGqaWarps + kGqaProducers) * 32, 1) k_attn_gq
     const uint8_t* kvg = a.kv + (int64_t)r * a.rows * rec + (int64_t)g * a.kstride;
     bool ok = true;
     int issued = 0;
-    // the slot (and, FETCH, the pending host position) of token `lane` of stage i, read from global
-    // memory two stages before use; invalid slots become padding
+    // the slot (and, FETCH, the host address of a pending record, 0 if none) of token `lane` of
+    // stage i, read from global memory two stages before use; invalid slots become padding
     const int32_t* locs_r = a.locs + (int64_t)(r - a.r0) * a.k + t0;
-    const int2* pend_r = pend_on ? a.pend + (int64_t)r * a.k + t0 : nullptr;
-    auto load_raw = [&](int i, int32_t& l, int32_t& q) {
+    const hs_pending* pend_r = pend_on ? a.pend + (int64_t)r * a.k + t0 : nullptr;
+    auto load_raw = [&](int i, int32_t& l, uint64_t& q) {
       const int x = (w + NW * i) * T + lane;
       const bool in = i < ni && lane < T && x < n;
       l = in ? locs_r[x] : -1;
-      q = (FETCH && in && pend_on) ? pend_r[x].x : -1;
+      q = (FETCH && in && pend_on) ? pend_r[x].src : 0ull;
     };
-    auto stage_info = [&](int32_t l, int32_t q, int32_t& loc, int32_t& pp, uint32_t& vmask, uint32_t& pmask) {
+    auto stage_info = [&](int32_t l, uint64_t q, int32_t& loc, uint64_t& pp, uint32_t& vmask, uint32_t& pmask) {
       if (l < -1 || (int64_t)l >= a.rows) {
         atomicOr(a.err, (uint32_t)HS_DEVERR_LOC);
         l = -1;
       }
       loc = l;
-      pp = (FETCH && l >= 0) ? q : -1;
+      pp = (FETCH && l >= 0) ? q : 0ull;
       vmask = __ballot_sync(0xffffffffu, lane < T && loc >= 0);
-      pmask = FETCH ? __ballot_sync(0xffffffffu, lane < T && pp >= 0) : 0u;
+      pmask = FETCH ? __ballot_sync(0xffffffffu, lane < T && pp != 0ull) : 0u;
     };
     // FETCH: up to kPre pending rows of a stage are requested from the host one stage ahead of use
     // (deeper request windows measured slower: the link is the bound, more requests only queue)
     constexpr int kPre = FETCH ? 8 : 1;
     uint4 vc[kPre], vn[kPre];
-    auto host_row = [&](int32_t pos) -> const uint4* {
-      const uint8_t* h = hs_hist_addr(a.hist_shared, a.hist_priv, a.P0, a.priv_tokens, rec, a.L, r, a.layer, pos);
-      return (const uint4*)(h + (int64_t)g * a.kstride) + lane;
+    // this lane's 16 bytes of KV head g's slice of the host record at `src`
+    auto load_row = [&](uint64_t src) -> uint4 {
+      return __ldg((const uint4*)((const uint8_t*)(uintptr_t)src + (int64_t)g * a.kstride) + lane);
     };
-    auto request = [&](uint32_t pmask_, int32_t pp_, uint4 (&v)[kPre]) {
+    auto request = [&](uint32_t pmask_, uint64_t pp_, uint4 (&v)[kPre]) {
       uint32_t pm = pmask_;
 #pragma unroll
       for (int u = 0; u < kPre; ++u) {
         if (pm != 0u) {
-          v[u] = __ldg(host_row(__shfl_sync(0xffffffffu, pp_, __ffs(pm) - 1)));
+          v[u] = load_row(__shfl_sync(0xffffffffu, pp_, __ffs(pm) - 1));
           pm &= pm - 1u;
         }
       }
     };
-    int32_t raw_l0, raw_q0, raw_l1, raw_q1;
+    int32_t raw_l0, raw_l1;
+    uint64_t raw_q0, raw_q1;
     load_raw(0, raw_l0, raw_q0);
     load_raw(1, raw_l1, raw_q1);
-    int32_t loc, pp;
+    int32_t loc;
+    uint64_t pp;
     uint32_t vmask, pmask;
     stage_info(raw_l0, raw_q0, loc, pp, vmask, pmask);
     load_raw(2, raw_l0, raw_q0);
@@ -684,9 +683,10 @@ __global__ void __launch_bounds__((kGqaWarps + kGqaProducers) * 32, 1) k_attn_gq
         // resident rows by bulk copy; the arrival comes after the pending rows are stored, below
         if (lane == 0) mbar_expect_tx(&full[w][b], (uint32_t)__popc(vmask & ~pmask) * 512u);
         __syncwarp();
-        if (loc >= 0 && pp < 0) bulk_g2s(dst + lane * RW, kvg + (int64_t)loc * rec, 512u, &full[w][b]);
+        if (loc >= 0 && pp == 0ull) bulk_g2s(dst + lane * RW, kvg + (int64_t)loc * rec, 512u, &full[w][b]);
       }
-      int32_t loc2, pp2;
+      int32_t loc2;
+      uint64_t pp2;
       uint32_t vmask2, pmask2;
       stage_info(raw_l1, raw_q1, loc2, pp2, vmask2, pmask2);
       raw_l1 = raw_l0;
@@ -702,7 +702,7 @@ __global__ void __launch_bounds__((kGqaWarps + kGqaProducers) * 32, 1) k_attn_gq
             if (pm != 0u) {
               const int j = __ffs(pm) - 1;
               pm &= pm - 1u;
-              const uint4 v = u < kPre ? vc[u < kPre ? u : 0] : __ldg(host_row(__shfl_sync(0xffffffffu, pp, j)));
+              const uint4 v = u < kPre ? vc[u < kPre ? u : 0] : load_row(__shfl_sync(0xffffffffu, pp, j));
               *(uint4*)(dst + j * RW + lane * 16) = v;
               const int32_t slot = __shfl_sync(0xffffffffu, loc, j);
               *((uint4*)(a.buf_w + ((int64_t)r * a.rows + slot) * rec + (int64_t)g * a.kstride) + lane) = v;
@@ -754,21 +754,24 @@ __global__ void __launch_bounds__((kGqaWarps + kGqaProducers) * 32, 1) k_attn_gq
       }
       const uint32_t mask = s_mask[warp][b];
       const uint32_t base = ring_u + (uint32_t)(b * T * RW);
-      // S^T = K Q^T in two MMA chains
-      float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+      // S^T = K Q^T in four independent MMA chains (k-steps s, s + 4)
+      float sacc[4][4];
 #pragma unroll
-      for (int s2 = 0; s2 < 8; s2 += 2) {
-        uint32_t x0, x1, x2, x3, y0, y1, y2, y3;
+      for (int c = 0; c < 4; ++c) sacc[c][0] = sacc[c][1] = sacc[c][2] = sacc[c][3] = 0.f;
+#pragma unroll
+      for (int s2 = 0; s2 < 8; ++s2) {
+        uint32_t x0, x1, x2, x3;
         ldsm_x4(base + k_lane + s2 * 32, x0, x1, x2, x3);
-        ldsm_x4(base + k_lane + (s2 + 1) * 32, y0, y1, y2, y3);
-        mma_bf16(sa, x0, x1, x2, x3, qb[s2][0], qb[s2][1]);
-        mma_bf16(sb, y0, y1, y2, y3, qb[s2 + 1][0], qb[s2 + 1][1]);
+        mma_bf16(sacc[s2 & 3], x0, x1, x2, x3, qb[s2][0], qb[s2][1]);
       }
+      float sv[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sv[e] = (sacc[0][e] + sacc[1][e]) + (sacc[2][e] + sacc[3][e]);
       const bool va = ((mask >> grow) & 1u) != 0u, vb = ((mask >> (grow + 8)) & 1u) != 0u;
-      const float x00 = va ? (sa[0] + sb[0]) * a.qscale : -INFINITY;
-      const float x01 = va ? (sa[1] + sb[1]) * a.qscale : -INFINITY;
-      const float x10 = vb ? (sa[2] + sb[2]) * a.qscale : -INFINITY;
-      const float x11 = vb ? (sa[3] + sb[3]) * a.qscale : -INFINITY;
+      const float x00 = va ? sv[0] * a.qscale : -INFINITY;
+      const float x01 = va ? sv[1] * a.qscale : -INFINITY;
+      const float x10 = vb ? sv[2] * a.qscale : -INFINITY;
+      const float x11 = vb ? sv[3] * a.qscale : -INFINITY;
       float mx0 = fmaxf(x00, x10), mx1 = fmaxf(x01, x11);
 #pragma unroll
       for (int o = 4; o < 32; o <<= 1) {
@@ -1511,10 +1514,6 @@ int hs_launch_attn(hs_pool* p, int layer, int r0, int nreq, const void* d_q, con
   a.pend = (hot && p->pend != nullptr) ? p->pend + (int64_t)layer * c.num_requests * c.top_k : nullptr;
   a.pend_live = (hot && p->pend_live != nullptr) ? p->pend_live + (int64_t)layer * c.num_requests : nullptr;
   a.buf_w = hot ? p->buf + (int64_t)layer * c.num_requests * c.buffer_slots * p->rec : nullptr;
-  a.hist_shared = p->dmap_shared;
-  a.hist_priv = p->dmap_priv;
-  a.P0 = c.shared_prefix;
-  a.priv_tokens = p->priv_tokens;
   a.L = c.num_layers;
   a.layer = layer;
   return dispatch(c, &a, pl, st) == cudaSuccess ? HS_OK : HS_ERR_CUDA;

@@ -1,6 +1,8 @@
 // Internal declarations shared by the translation units of libhisparse.
 // Layouts (all row-major):
-//   host history   shared [L][P0][rec] and private [R][L][C - P0][rec]   (pinned, device-mapped)
+//   host history   pages of 2^page_shift records (pinned, device-mapped), found through the page
+//                  table [R][L][max_pages] of device addresses (0 = not reserved); the pages of
+//                  the shared prefix appear in every request's table
 //   hot buffer     [L][R][B][rec]                                        (HBM)
 //   tag / stamp    [L][R][B]  int32 (-1 empty) / uint32 (0 empty)
 //   state          [L][R]     {clock, nres, err, pad}
@@ -20,16 +22,25 @@ struct hs_rl_state {
   uint32_t pad;
 };
 
+struct hs_host_pages;  // host-side page allocator and the host mirror of the page table
+
+// A miss the resolve left to the attention (fetch-in-attention mode): the device address of its
+// record in the mapped host history (0: nothing pending for this top-k entry) and its slot.
+struct hs_pending {
+  uint64_t src;
+  int32_t slot;
+  int32_t pos;
+};
+
 struct hs_pool {
   hs_config cfg;
   int device;
   int num_sms;
-  int64_t rec;          // record bytes
-  int64_t priv_tokens;  // capacity - shared_prefix
-  uint8_t* host_shared;  // host pointers (cudaHostAlloc, mapped)
-  uint8_t* host_priv;
-  uint8_t* dmap_shared;  // device aliases of the same memory
-  uint8_t* dmap_priv;
+  int64_t rec;           // record bytes
+  uint64_t* page_table;  // device [R][L][max_pages]: device address of each host page, 0 = none
+  int64_t max_pages;     // pages per (request, layer): ceil(capacity / page size)
+  int page_shift;        // log2 of the records per page
+  hs_host_pages* host;
   uint8_t* buf;
   int32_t* tag;
   uint32_t* stamp;
@@ -37,7 +48,7 @@ struct hs_pool {
   unsigned long long* counters;
   uint32_t* step_log;
   uint32_t* err_global;  // attention-side error bits
-  int2* pend;            // [L][R][k] {position, slot} of misses the attention still has to fetch
+  hs_pending* pend;      // [L][R][k] misses the attention still has to fetch
   uint32_t* pend_live;   // [L][R] 1 while such a list is outstanding
   float* attn_part;      // split partials
   uint32_t* attn_ticket; // [R][attn_tickets_per_req]: per-group split tickets, then the pending-list count
@@ -68,29 +79,46 @@ __device__ __forceinline__ uint32_t hs_evict_key(int policy, int32_t tag, uint32
   return stamp;
 }
 
-// device address of position p of (r, l) in the mapped host history
-__device__ __forceinline__ const uint8_t* hs_hist_addr(const uint8_t* shared, const uint8_t* priv, int64_t P0,
-                                                       int64_t priv_tokens, int64_t rec, int L, int r, int l,
-                                                       int64_t p) {
-  if (p < P0) return shared + ((int64_t)l * P0 + p) * rec;
-  return priv + (((int64_t)r * L + l) * priv_tokens + (p - P0)) * rec;
+// device address of position p of (r, l) in the mapped host history, or null when its page is not
+// reserved
+__device__ __forceinline__ uint8_t* hs_page_addr(const uint64_t* pt, int64_t max_pages, int shift, int64_t rec,
+                                                 int L, int r, int l, int64_t p) {
+  const uint64_t page = pt[((int64_t)r * L + l) * max_pages + (p >> shift)];
+  if (page == 0ull) return nullptr;
+  return (uint8_t*)page + (p & ((1ll << shift) - 1)) * rec;
+}
+
+// The same through one (request, layer) row of the table: a copy in shared memory, or the row in
+// global memory when it is longer than a kernel caches.
+constexpr int kPageRowCache = 1024;  // entries a kernel keeps in shared memory (8 KB)
+__device__ __forceinline__ uint8_t* hs_page_row_addr(const uint64_t* row, int shift, int64_t rec, int64_t p) {
+  const uint64_t page = row[p >> shift];
+  if (page == 0ull) return nullptr;
+  return (uint8_t*)page + (p & ((1ll << shift) - 1)) * rec;
+}
+// Copy the row of (r, l) into `cache` when it fits; returns the row to use.  Needs a barrier
+// between this and the first use.
+__device__ __forceinline__ const uint64_t* hs_page_row(const uint64_t* pt, int64_t max_pages, int L, int r, int l,
+                                                       uint64_t* cache) {
+  const uint64_t* row = pt + ((int64_t)r * L + l) * max_pages;
+  if (max_pages > kPageRowCache) return row;
+  for (int64_t i = threadIdx.x; i < max_pages; i += blockDim.x) cache[i] = row[i];
+  return cache;
 }
 
 // Finish the host -> slot copies that a resolve in fetch-in-attention mode left pending for
-// (r, l) and that no attention has completed: pend[i] = {position, slot} or {-1, -1}.  The
-// entries [k*part/nparts, k*(part+1)/nparts) are copied by this CTA, one warp per record.
-__device__ __forceinline__ void hs_copy_pending(const int2* pend, int k, const uint8_t* hist_shared,
-                                                const uint8_t* hist_priv, int64_t P0, int64_t priv_tokens,
-                                                int64_t rec, int L, int r, int l, uint8_t* buf_r, int part,
+// (r, l) and that no attention has completed.  The entries [k*part/nparts, k*(part+1)/nparts) are
+// copied by this CTA, one warp per record.
+__device__ __forceinline__ void hs_copy_pending(const hs_pending* pend, int k, int64_t rec, uint8_t* buf_r, int part,
                                                 int nparts) {
   const int e0 = (int)((int64_t)k * part / nparts), e1 = (int)((int64_t)k * (part + 1) / nparts);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
   const int nv = (int)(rec / 16);
   for (int i = e0 + warp; i < e1; i += nw) {
-    const int2 e = pend[i];
-    if (e.x < 0 || e.y < 0) continue;
-    const uint4* src = (const uint4*)hs_hist_addr(hist_shared, hist_priv, P0, priv_tokens, rec, L, r, l, e.x);
-    uint4* dst = (uint4*)(buf_r + (int64_t)e.y * rec);
+    const hs_pending e = pend[i];
+    if (e.src == 0ull) continue;
+    const uint4* src = (const uint4*)e.src;
+    uint4* dst = (uint4*)(buf_r + (int64_t)e.slot * rec);
     for (int v = lane; v < nv; v += 32) dst[v] = src[v];
   }
 }

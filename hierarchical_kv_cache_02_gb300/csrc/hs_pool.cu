@@ -1,6 +1,8 @@
 // Host side of the C ABI: configuration checks, pool memory, prefill, stats and inspection.
 // The memory layer follows the HiSparse summary §3 and §8: a pinned host pool holds the
-// authoritative KV history; HBM holds only B slots per (request, layer) plus metadata.
+// authoritative KV history; HBM holds only B slots per (request, layer) plus metadata.  The host
+// pool is paged: fixed-size pages carved from large pinned, device-mapped slabs, found by the
+// kernels through a device page table, reserved up front or on demand and returned to a free list.
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -19,6 +21,15 @@ bool fault_requested(const char* what) {
 }
 
 bool is_pow2(int64_t v) { return v > 0 && (v & (v - 1)) == 0; }
+
+// records per host page: the configured power of two, or 1024, or the largest power of two <= 1024
+// that divides the shared prefix (a page never mixes shared and private positions)
+int64_t page_tokens_for(const hs_config* c) {
+  if (c->host_page_tokens > 0) return c->host_page_tokens;
+  int64_t pt = 1024;
+  while (c->shared_prefix > 0 && c->shared_prefix % pt != 0) pt >>= 1;
+  return pt;
+}
 
 int check_config(const hs_config* c) {
   if (c == nullptr) return HS_ERR_ARG;
@@ -39,6 +50,11 @@ int check_config(const hs_config* c) {
   if (!hs_attn_supported(c)) return HS_ERR_CONFIG;
   if (hs_resolve_smem_bytes(c) > 200 * 1024) return HS_ERR_CONFIG;
   if (c->fetch_in_attention != 0 && (c->fetch_in_attention != 1 || !hs_attn_can_fetch(c))) return HS_ERR_CONFIG;
+  if (c->host_page_tokens < 0 || c->host_page_tokens > (1 << 20) ||
+      (c->host_page_tokens > 0 && !is_pow2(c->host_page_tokens)))
+    return HS_ERR_CONFIG;
+  if (c->shared_prefix > 0 && c->shared_prefix % page_tokens_for(c) != 0) return HS_ERR_CONFIG;
+  if (c->host_on_demand != 0 && c->host_on_demand != 1) return HS_ERR_CONFIG;
   return HS_OK;
 }
 
@@ -54,6 +70,21 @@ int dev_alloc(T** p, size_t count) {
   }
   return HS_OK;
 }
+
+}  // namespace
+
+// Pinned host pages and the host mirror of the page table.
+struct hs_host_pages {
+  int64_t page_tokens = 0, page_bytes = 0, shared_pages = 0;
+  std::vector<std::pair<uint8_t*, uint8_t*>> slabs;       // (host, device) of each pinned slab
+  std::vector<size_t> slab_bytes;
+  std::vector<std::pair<uint8_t*, uint8_t*>> free_pages;  // (host, device)
+  std::vector<uint8_t*> host_pt;                          // [R][L][max_pages] host address, null = none
+  std::vector<uint64_t> dev_pt;                           // the same pages' device addresses
+  int64_t pages_in_use = 0;
+};
+
+namespace {
 
 int host_alloc(uint8_t** h, uint8_t** d, size_t bytes) {
   *h = nullptr;
@@ -74,8 +105,11 @@ int host_alloc(uint8_t** h, uint8_t** d, size_t bytes) {
 
 void free_pool(hs_pool* p) {
   if (p == nullptr) return;
-  if (p->host_shared) cudaFreeHost(p->host_shared);
-  if (p->host_priv) cudaFreeHost(p->host_priv);
+  if (p->host != nullptr) {
+    for (auto& sl : p->host->slabs) cudaFreeHost(sl.first);
+    delete p->host;
+  }
+  cudaFree(p->page_table);
   cudaFree(p->buf);
   cudaFree(p->tag);
   cudaFree(p->stamp);
@@ -128,6 +162,79 @@ int do_reset(hs_pool* p, cudaStream_t st) {
   return cudaGetLastError() == cudaSuccess ? HS_OK : HS_ERR_CUDA;
 }
 
+// Pinned slabs.  The GPU reads scattered host rows faster from few large mappings than from many
+// small ones: on the 16-request, 32-layer GQA decode workload (17 GB of history) one slab for the
+// whole reservation decodes as fast as flat arrays, while one 516 MB slab per (request, layer) cost
+// 4-15% (slower miss copies).  So a reservation made at creation takes a single slab; a slab made
+// on demand is at least kSlabMin and at least a quarter of what is already pinned (few slabs as the
+// pool grows, at most a quarter over-reserved), never more pages than the page table could still take.
+constexpr size_t kSlabMin = (size_t)256 << 20;
+
+// n more pages on the free list
+int grow_free_pages(hs_pool* p, int64_t n) {
+  hs_host_pages& h = *p->host;
+  while ((int64_t)h.free_pages.size() < n) {
+    const int64_t want = n - (int64_t)h.free_pages.size();
+    const int64_t R = p->cfg.num_requests, L = p->cfg.num_layers;  // distinct pages: shared ones once per layer
+    const int64_t room = L * h.shared_pages + R * L * (p->max_pages - h.shared_pages) - h.pages_in_use -
+                         (int64_t)h.free_pages.size();
+    size_t pinned = 0;
+    for (size_t b : h.slab_bytes) pinned += b;
+    const int64_t min_pages = std::max<int64_t>(1, (int64_t)(std::max(kSlabMin, pinned / 4) / (size_t)h.page_bytes));
+    const int64_t np = std::max(want, std::min(min_pages, room));
+    uint8_t *hp = nullptr, *dp = nullptr;
+    int rc = host_alloc(&hp, &dp, (size_t)(np * h.page_bytes));
+    if (rc != HS_OK) {
+      if (hp) cudaFreeHost(hp);
+      return rc;
+    }
+    h.slabs.push_back({hp, dp});
+    h.slab_bytes.push_back((size_t)(np * h.page_bytes));
+    for (int64_t i = np - 1; i >= 0; --i) h.free_pages.push_back({hp + i * h.page_bytes, dp + i * h.page_bytes});
+  }
+  return HS_OK;
+}
+
+// Give every missing page of pages [pg0, pg1) of (req, layer) a page; the shared prefix's pages are
+// one per layer, mapped into every request's table.  Updates the host mirror only; *changed is set
+// when an entry changed.
+int reserve_pages(hs_pool* p, int req, int layer, int64_t pg0, int64_t pg1, bool* changed) {
+  hs_host_pages& h = *p->host;
+  const int R = p->cfg.num_requests, L = p->cfg.num_layers;
+  pg1 = std::min(pg1, p->max_pages);
+  int64_t need = 0;
+  for (int64_t g = pg0; g < pg1; ++g)
+    if (h.host_pt[((int64_t)req * L + layer) * p->max_pages + g] == nullptr) ++need;
+  if (need == 0) return HS_OK;
+  int rc = grow_free_pages(p, need);
+  if (rc != HS_OK) return rc;
+  for (int64_t g = pg0; g < pg1; ++g) {
+    const int64_t e = ((int64_t)req * L + layer) * p->max_pages + g;
+    if (h.host_pt[e] != nullptr) continue;
+    const auto pg = h.free_pages.back();
+    h.free_pages.pop_back();
+    ++h.pages_in_use;
+    const int r0 = g < h.shared_pages ? 0 : req, r1 = g < h.shared_pages ? R : req + 1;
+    for (int r = r0; r < r1; ++r) {  // a shared page appears in every request's table
+      const int64_t er = ((int64_t)r * L + layer) * p->max_pages + g;
+      h.host_pt[er] = pg.first;
+      h.dev_pt[er] = (uint64_t)(uintptr_t)pg.second;
+    }
+    *changed = true;
+  }
+  return HS_OK;
+}
+
+int upload_page_table(hs_pool* p) {
+  const size_t n = p->host->dev_pt.size();
+  if (cudaDeviceSynchronize() != cudaSuccess ||
+      cudaMemcpy(p->page_table, p->host->dev_pt.data(), n * sizeof(uint64_t), cudaMemcpyHostToDevice) != cudaSuccess) {
+    cudaGetLastError();
+    return HS_ERR_CUDA;
+  }
+  return HS_OK;
+}
+
 struct DeviceGuard {
   int prev = -1;
   explicit DeviceGuard(int dev) {
@@ -164,12 +271,29 @@ extern "C" int hs_pool_create(const hs_config* cfg, int cuda_device, hs_pool** o
   p->device = cuda_device;
   cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, cuda_device);
   p->rec = hs_record_bytes(cfg);
-  p->priv_tokens = cfg->capacity - cfg->shared_prefix;
   const size_t R = cfg->num_requests, L = cfg->num_layers, B = cfg->buffer_slots;
   const size_t rec = (size_t)p->rec;
-
-  rc = host_alloc(&p->host_shared, &p->dmap_shared, L * (size_t)cfg->shared_prefix * rec);
-  if (rc == HS_OK) rc = host_alloc(&p->host_priv, &p->dmap_priv, R * L * (size_t)p->priv_tokens * rec);
+  // host pages and their table
+  p->host = new hs_host_pages();
+  p->host->page_tokens = page_tokens_for(cfg);
+  p->host->page_bytes = p->host->page_tokens * p->rec;
+  p->host->shared_pages = cfg->shared_prefix / p->host->page_tokens;
+  p->page_shift = 0;
+  while ((1ll << p->page_shift) < p->host->page_tokens) ++p->page_shift;
+  p->max_pages = (cfg->capacity + p->host->page_tokens - 1) / p->host->page_tokens;
+  p->host->host_pt.assign(R * L * (size_t)p->max_pages, nullptr);
+  p->host->dev_pt.assign(R * L * (size_t)p->max_pages, 0ull);
+  rc = dev_alloc(&p->page_table, R * L * (size_t)p->max_pages);
+  if (rc == HS_OK && cfg->host_on_demand == 0) {  // every page of [0, capacity) now, from one slab
+    const int64_t sp = p->host->shared_pages;
+    rc = grow_free_pages(p, (int64_t)L * sp + (int64_t)(R * L) * (p->max_pages - sp));  // all of them
+    bool changed = false;
+    for (int r = 0; rc == HS_OK && r < (int)R; ++r)
+      for (int l = 0; rc == HS_OK && l < (int)L; ++l) rc = reserve_pages(p, r, l, 0, p->max_pages, &changed);
+  }
+  if (rc == HS_OK && cudaMemcpy(p->page_table, p->host->dev_pt.data(), p->host->dev_pt.size() * sizeof(uint64_t),
+                                cudaMemcpyHostToDevice) != cudaSuccess)
+    rc = HS_ERR_CUDA;
   if (rc == HS_OK) rc = dev_alloc(&p->buf, L * R * B * rec);
   if (rc == HS_OK) rc = dev_alloc(&p->tag, L * R * B);
   if (rc == HS_OK) rc = dev_alloc(&p->stamp, L * R * B);
@@ -221,21 +345,68 @@ extern "C" int hs_prefill_write(hs_pool* pool, int req, int layer, int64_t pos0,
   if (pos0 < 0 || n < 0 || pos0 + n > c.capacity) return HS_ERR_ARG;
   if (n == 0) return HS_OK;
   DeviceGuard guard(pool->device);
-  const int64_t P0 = c.shared_prefix, rec = pool->rec;
+  hs_host_pages& h = *pool->host;
+  const int64_t pt = h.page_tokens, rec = pool->rec;
+  bool changed = false;
+  int rc = reserve_pages(pool, req, layer, pos0 / pt, (pos0 + n + pt - 1) / pt, &changed);
+  if (rc != HS_OK) return rc;
+  if (changed && (rc = upload_page_table(pool)) != HS_OK) return rc;
   const uint8_t* s = (const uint8_t*)src;
   cudaStream_t st = (cudaStream_t)stream;
-  int64_t a = pos0, end = pos0 + n;
-  if (a < P0) {  // shared part
-    int64_t b = std::min(end, P0);
-    uint8_t* dst = pool->host_shared + ((int64_t)layer * P0 + a) * rec;
+  for (int64_t a = pos0; a < pos0 + n;) {  // one copy per page
+    const int64_t b = std::min(pos0 + n, (a / pt + 1) * pt);
+    uint8_t* dst = h.host_pt[((int64_t)req * c.num_layers + layer) * pool->max_pages + a / pt] + (a % pt) * rec;
     if (cudaMemcpyAsync(dst, s, (size_t)((b - a) * rec), cudaMemcpyDefault, st) != cudaSuccess) return HS_ERR_CUDA;
     s += (b - a) * rec;
     a = b;
   }
-  if (a < end) {
-    uint8_t* dst = pool->host_priv + (((int64_t)req * c.num_layers + layer) * pool->priv_tokens + (a - P0)) * rec;
-    if (cudaMemcpyAsync(dst, s, (size_t)((end - a) * rec), cudaMemcpyDefault, st) != cudaSuccess) return HS_ERR_CUDA;
+  return HS_OK;
+}
+
+extern "C" int hs_reserve(hs_pool* pool, int req, int layer, int64_t end) {
+  if (pool == nullptr) return HS_ERR_ARG;
+  const hs_config& c = pool->cfg;
+  if (req < 0 || req >= c.num_requests || layer < -1 || layer >= c.num_layers) return HS_ERR_ARG;
+  if (end < 0 || end > c.capacity) return HS_ERR_ARG;
+  DeviceGuard guard(pool->device);
+  const int64_t pg1 = (end + pool->host->page_tokens - 1) / pool->host->page_tokens;
+  bool changed = false;
+  int rc = HS_OK;
+  for (int l = layer < 0 ? 0 : layer; rc == HS_OK && l < (layer < 0 ? c.num_layers : layer + 1); ++l)
+    rc = reserve_pages(pool, req, l, 0, pg1, &changed);
+  if (rc == HS_OK && changed) rc = upload_page_table(pool);
+  return rc;
+}
+
+extern "C" int hs_release(hs_pool* pool, int req) {
+  if (pool == nullptr || req < 0 || req >= pool->cfg.num_requests) return HS_ERR_ARG;
+  DeviceGuard guard(pool->device);
+  if (cudaDeviceSynchronize() != cudaSuccess) return HS_ERR_CUDA;  // no kernel reads them any more
+  hs_host_pages& h = *pool->host;
+  const int L = pool->cfg.num_layers;
+  bool changed = false;
+  for (int l = 0; l < L; ++l) {
+    for (int64_t g = h.shared_pages; g < pool->max_pages; ++g) {
+      const int64_t e = ((int64_t)req * L + l) * pool->max_pages + g;
+      if (h.host_pt[e] == nullptr) continue;
+      h.free_pages.push_back({h.host_pt[e], (uint8_t*)(uintptr_t)h.dev_pt[e]});
+      h.host_pt[e] = nullptr;
+      h.dev_pt[e] = 0ull;
+      --h.pages_in_use;
+      changed = true;
+    }
   }
+  return changed ? upload_page_table(pool) : HS_OK;
+}
+
+extern "C" int hs_host_usage(hs_pool* pool, int64_t* pages_in_use, int64_t* pages_free, int64_t* bytes_pinned) {
+  if (pool == nullptr) return HS_ERR_ARG;
+  const hs_host_pages& h = *pool->host;
+  size_t b = 0;
+  for (size_t x : h.slab_bytes) b += x;
+  if (pages_in_use) *pages_in_use = h.pages_in_use;
+  if (pages_free) *pages_free = (int64_t)h.free_pages.size();
+  if (bytes_pinned) *bytes_pinned = (int64_t)b;
   return HS_OK;
 }
 
@@ -382,21 +553,18 @@ extern "C" int hs_read_history(hs_pool* pool, int req, int layer, int64_t pos0, 
   if (pos0 < 0 || n < 0 || pos0 + n > c.capacity) return HS_ERR_ARG;
   DeviceGuard guard(pool->device);
   if (cudaDeviceSynchronize() != cudaSuccess) return HS_ERR_CUDA;
-  const int64_t P0 = c.shared_prefix, rec = pool->rec;
+  const hs_host_pages& h = *pool->host;
+  const int64_t pt = h.page_tokens, rec = pool->rec;
   uint8_t* d = (uint8_t*)dst;
-  for (int64_t p = pos0; p < pos0 + n;) {
-    if (p < P0) {
-      int64_t b = std::min(pos0 + n, P0);
-      memcpy(d, pool->host_shared + ((int64_t)layer * P0 + p) * rec, (size_t)((b - p) * rec));
-      d += (b - p) * rec;
-      p = b;
-    } else {
-      int64_t b = pos0 + n;
-      memcpy(d, pool->host_priv + (((int64_t)req * c.num_layers + layer) * pool->priv_tokens + (p - P0)) * rec,
-             (size_t)((b - p) * rec));
-      d += (b - p) * rec;
-      p = b;
-    }
+  for (int64_t p = pos0; p < pos0 + n;) {  // page by page; pages not reserved read as zeros
+    const int64_t b = std::min(pos0 + n, (p / pt + 1) * pt);
+    const uint8_t* page = h.host_pt[((int64_t)req * c.num_layers + layer) * pool->max_pages + p / pt];
+    if (page != nullptr)
+      memcpy(d, page + (p % pt) * rec, (size_t)((b - p) * rec));
+    else
+      memset(d, 0, (size_t)((b - p) * rec));
+    d += (b - p) * rec;
+    p = b;
   }
   return HS_OK;
 }

@@ -29,16 +29,16 @@ struct ResolveArgs {
   hs_rl_state* state;   // layer slice [R]
   unsigned long long* counters;  // layer slice [R][4]
   uint32_t* step_log;   // [log_steps][L][R] or null
-  const uint8_t* hist_shared;
-  const uint8_t* hist_priv;
+  const uint64_t* pt;   // host page table [R][L][max_pages]
+  uint32_t* err_global; // pool-wide error word (errors found outside the deciding CTA)
   uint8_t* buf;         // layer slice [R][B][rec]
-  int64_t C, P0, priv_tokens, rec;
+  int64_t C, P0, max_pages, rec;
+  int page_shift;
   uint64_t seed;
-  int2* pend;            // fetch-in-attention mode: layer slice [R][k], else null
+  hs_pending* pend;      // fetch-in-attention mode: layer slice [R][k], else null
   uint32_t* pend_live;   // layer slice [R]
   const int64_t* app_pos;  // fused write-through append before the resolve: [R] positions, or null
   const uint8_t* app_rec;  // [R][rec] new records
-  uint8_t* hist_priv_w;    // writable view of the private host history
   int R, L, layer, B, k, policy, log_steps, ht_bits, cs;  // R: all requests of the pool
   int r0;  // first request of this launch: topk, locs and the append inputs are indexed from it
 };
@@ -87,7 +87,7 @@ __device__ __forceinline__ void cluster_sync_all() {
 // Copy misses [q0, q1) host -> slots.  A warp moves one chunk of 32 x NV lane-contiguous 16-byte
 // vectors of one record per item (coalesced 512-byte rows); ITEMS items are loaded before any store.
 template <int NV>
-__device__ void fetch_misses(const ResolveArgs& a, int r, int q0, int q1, const int32_t* miss_pos,
+__device__ void fetch_misses(const ResolveArgs& a, int r, int q0, int q1, const uint64_t* s_src,
                              const int32_t* victims) {
   constexpr int ITEMS = NV >= 8 ? 1 : 2;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -105,8 +105,8 @@ __device__ void fetch_misses(const ResolveArgs& a, int r, int q0, int q1, const 
       dst[it] = nullptr;
       if (w < total) {
         const int q = q0 + w / cpr, c = w % cpr;
-        src[it] = (const uint4*)hs_hist_addr(a.hist_shared, a.hist_priv, a.P0, a.priv_tokens, a.rec, a.L, r, a.layer,
-                                             miss_pos[q]);
+        src[it] = (const uint4*)s_src[q - q0];
+        if (src[it] == nullptr) continue;  // page not reserved (flagged): the slot keeps its contents
         dst[it] = (uint4*)(a.buf + ((int64_t)r * a.B + victims[q]) * a.rec);
         vbase[it] = c * 32 * NV + lane;
 #pragma unroll
@@ -234,13 +234,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
   __shared__ int s_app_slot;
   __shared__ unsigned long long s_best[kWarps];
   __shared__ int s_found[kWarps];
+  __shared__ uint64_t s_pt[kPageRowCache];
+  // this (request, layer)'s row of the host page table, cached for phase B (the decision's barriers
+  // order it before the first use; the pointer is recomputed where it is used rather than kept live)
+  hs_page_row(a.pt, a.max_pages, a.L, r, a.layer, s_pt);
+  auto pt_row = [&]() -> const uint64_t* {
+    return a.max_pages <= kPageRowCache ? s_pt : a.pt + ((int64_t)r * a.L + a.layer) * a.max_pages;
+  };
 
   // fetch-in-attention mode: copies a previous resolve left to an attention that never ran are
   // finished first (they target slots this decision may reuse); the cluster barrier below orders
   // them before this resolve rewrites the pending list
   if (a.pend != nullptr && a.pend_live[r] != 0u)
-    hs_copy_pending(a.pend + (int64_t)r * k, k, a.hist_shared, a.hist_priv, a.P0, a.priv_tokens, a.rec, a.L, r,
-                    a.layer, a.buf + (int64_t)r * B * a.rec, crank, a.cs);
+    hs_copy_pending(a.pend + (int64_t)r * k, k, a.rec, a.buf + (int64_t)r * B * a.rec, crank, a.cs);
 
   // ---------------- phase A: every CTA of the cluster computes the whole decision ----------------
   // fused write-through append (hs_append_resolve): the new position takes the slot that already
@@ -249,9 +255,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
   int app_slot = -1;
   int64_t app_p = -1;
   uint32_t app_err = 0u;
+  uint4* app_dh = nullptr;  // the append's place in the host history
   if (a.app_pos != nullptr) {
     app_p = a.app_pos[r - a.r0];
-    if (app_p < a.P0 || app_p < 0 || app_p >= a.C) {
+    if (app_p >= a.P0 && app_p >= 0 && app_p < a.C)
+      app_dh = (uint4*)hs_page_addr(a.pt, a.max_pages, a.page_shift, a.rec, a.L, r, a.layer, app_p);
+    if (app_dh == nullptr) {  // outside [shared_prefix, capacity), or its host page is not reserved
       app_err = (uint32_t)HS_DEVERR_APPEND;
     } else {
       int found = 0x7fffffff;
@@ -442,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
       } else if (hs == -2) {
         locs[i] = -1;
       }
-      if (a.pend != nullptr && hs != -1) a.pend[(int64_t)r * k + i] = make_int2(-1, -1);
+      if (a.pend != nullptr && hs != -1) a.pend[(int64_t)r * k + i] = hs_pending{0ull, -1, -1};
     }
     const int q0 = (int)((int64_t)m * crank / a.cs), q1 = (int)((int64_t)m * (crank + 1) / a.cs);
     for (int q = q0 + tid; q < q1; q += kThreads) {
@@ -450,7 +459,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
       tag[j] = miss_pos[q];
       stamp[j] = a.policy == HS_POLICY_FIFO ? clock + (uint32_t)q : clock + (uint32_t)h + (uint32_t)q;
       locs[miss_idx[q]] = j;
-      if (a.pend != nullptr) a.pend[(int64_t)r * k + miss_idx[q]] = make_int2(miss_pos[q], j);
+      if (a.pend != nullptr) {
+        // the record's host address, resolved once here; a page not reserved leaves nothing pending
+        const uint8_t* src = hs_page_row_addr(pt_row(), a.page_shift, a.rec, miss_pos[q]);
+        if (src == nullptr) atomicOr(a.err_global, (uint32_t)HS_DEVERR_PAGE);
+        a.pend[(int64_t)r * k + miss_idx[q]] = hs_pending{(uint64_t)(uintptr_t)src, src ? j : -1, miss_pos[q]};
+      }
     }
     if (a.policy == HS_POLICY_SWAP_VANILLA) {
       const int s0 = (int)((int64_t)B * crank / a.cs), s1 = (int)((int64_t)B * (crank + 1) / a.cs);
@@ -465,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
     // stamp unless the resolve reuses or empties that slot now, the stamp only where no hit restamps it
     if (app_slot >= 0 && crank == 0) {
       const uint4* src = (const uint4*)(a.app_rec + (int64_t)(r - a.r0) * a.rec);
-      uint4* dh = (uint4*)(a.hist_priv_w + (((int64_t)r * a.L + a.layer) * a.priv_tokens + (app_p - a.P0)) * a.rec);
+      uint4* dh = app_dh;
       // the slot is rewritten by the resolve when it is a victim now, or emptied by swap-vanilla
       // when it holds no selected position
       const bool evicted = (flag[app_slot] & 2u) != 0u ||
@@ -484,7 +498,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
       }
     }
     // (4) fetch this CTA's share of the misses from the host history (or leave it to the attention)
-    if (a.pend == nullptr && q1 > q0) fetch_misses<NV>(a, r, q0, q1, miss_pos, victims);
+    if (a.pend == nullptr && q1 > q0) {
+      // host addresses of this CTA's misses, resolved once (in the hash table's space: dead by now)
+      uint64_t* s_src = (uint64_t*)ht_key;
+      const uint64_t* row = pt_row();
+      for (int q = q0 + tid; q < q1; q += kThreads) {
+        const uint8_t* src = hs_page_row_addr(row, a.page_shift, a.rec, miss_pos[q]);
+        if (src == nullptr) atomicOr(a.err_global, (uint32_t)HS_DEVERR_PAGE);
+        s_src[q - q0] = (uint64_t)(uintptr_t)src;
+      }
+      __syncthreads();
+      fetch_misses<NV>(a, r, q0, q1, s_src, victims);
+    }
   }
 
   // (5) clock and counters
@@ -512,12 +537,13 @@ struct AppendArgs {
   uint32_t* stamp;
   hs_rl_state* state;
   unsigned long long* counters;
-  uint8_t* hist_shared;
-  uint8_t* hist_priv;
+  const uint64_t* pt;    // host page table [R][L][max_pages]
+  uint32_t* err_global;
   uint8_t* buf;
-  int64_t C, P0, priv_tokens, rec;
+  int64_t C, P0, max_pages, rec;
+  int page_shift;
   uint64_t seed;
-  const int2* pend;      // fetch-in-attention mode: layer slice [R][k], else null
+  const hs_pending* pend;  // fetch-in-attention mode: layer slice [R][k], else null
   uint32_t* pend_live;
   int R, L, layer, B, policy, k;
 };
@@ -529,14 +555,16 @@ __global__ void __launch_bounds__(kAppendThreads) k_append(AppendArgs a) {
   const int r = blockIdx.x, tid = threadIdx.x;
   if (a.pend != nullptr && a.pend_live[r] != 0u) {
     // finish the copies a previous resolve left pending before this append may overwrite a slot
-    hs_copy_pending(a.pend + (int64_t)r * a.k, a.k, a.hist_shared, a.hist_priv, a.P0, a.priv_tokens, a.rec, a.L, r,
-                    a.layer, a.buf + (int64_t)r * a.B * a.rec, 0, 1);
+    hs_copy_pending(a.pend + (int64_t)r * a.k, a.k, a.rec, a.buf + (int64_t)r * a.B * a.rec, 0, 1);
     __syncthreads();
     if (tid == 0) a.pend_live[r] = 0u;
   }
   const int64_t p = a.pos[r];
   const hs_rl_state st = a.state[r];
-  if (p < a.P0 || p < 0 || p >= a.C) {
+  uint4* dh = (p >= a.P0 && p >= 0 && p < a.C)
+                  ? (uint4*)hs_page_addr(a.pt, a.max_pages, a.page_shift, a.rec, a.L, r, a.layer, p)
+                  : nullptr;
+  if (dh == nullptr) {  // outside [shared_prefix, capacity), or its host page is not reserved
     if (tid == 0) a.state[r].err = st.err | (uint32_t)HS_DEVERR_APPEND;
     return;
   }
@@ -577,7 +605,6 @@ __global__ void __launch_bounds__(kAppendThreads) k_append(AppendArgs a) {
   __syncthreads();
   const int slot = s_slot;
   const uint4* src = (const uint4*)(a.rec_in + (int64_t)r * a.rec);
-  uint4* dh = (uint4*)(a.hist_priv + (((int64_t)r * a.L + a.layer) * a.priv_tokens + (p - a.P0)) * a.rec);
   uint4* db = (uint4*)(a.buf + ((int64_t)r * a.B + slot) * a.rec);
   const int nv = (int)(a.rec / 16);
   for (int x = tid; x < nv; x += kAppendThreads) {
@@ -682,12 +709,13 @@ int hs_launch_resolve(hs_pool* p, int layer, int r0, int nreq, const int64_t* d_
   a.state = p->state + (int64_t)layer * R;
   a.counters = p->counters + (int64_t)layer * R * 4;
   a.step_log = c.log_steps > 0 ? p->step_log : nullptr;
-  a.hist_shared = p->dmap_shared;
-  a.hist_priv = p->dmap_priv;
+  a.pt = p->page_table;
+  a.err_global = p->err_global;
   a.buf = p->buf + (int64_t)layer * R * B * p->rec;
   a.C = c.capacity;
   a.P0 = c.shared_prefix;
-  a.priv_tokens = p->priv_tokens;
+  a.max_pages = p->max_pages;
+  a.page_shift = p->page_shift;
   a.rec = p->rec;
   a.seed = c.seed;
   a.R = c.num_requests;
@@ -704,7 +732,6 @@ int hs_launch_resolve(hs_pool* p, int layer, int r0, int nreq, const int64_t* d_
   a.app_pos = d_pos;
   a.app_rec = (const uint8_t*)d_rec;
   a.r0 = r0;
-  a.hist_priv_w = p->dmap_priv;
   const size_t smem = hs_resolve_smem_bytes(&c);
   cudaError_t e;
   switch (c.io_chunk_bytes) {
@@ -737,12 +764,13 @@ int hs_launch_append(hs_pool* p, int layer, const int64_t* d_pos, const void* d_
   a.stamp = p->stamp + (int64_t)layer * R * B;
   a.state = p->state + (int64_t)layer * R;
   a.counters = p->counters + (int64_t)layer * R * 4;
-  a.hist_shared = p->dmap_shared;
-  a.hist_priv = p->dmap_priv;
+  a.pt = p->page_table;
+  a.err_global = p->err_global;
   a.buf = p->buf + (int64_t)layer * R * B * p->rec;
   a.C = c.capacity;
   a.P0 = c.shared_prefix;
-  a.priv_tokens = p->priv_tokens;
+  a.max_pages = p->max_pages;
+  a.page_shift = p->page_shift;
   a.rec = p->rec;
   a.seed = c.seed;
   a.R = c.num_requests;

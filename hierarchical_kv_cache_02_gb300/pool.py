@@ -44,6 +44,8 @@ class HsConfig:
     log_steps: int = 0
     shared_prefix: int = 0
     fetch_in_attention: int = 0
+    host_page_tokens: int = 0
+    host_on_demand: int = 0
 
     @property
     def record_bytes(self) -> int:
@@ -265,6 +267,21 @@ class HsPool:
         out = np.empty((c.buffer_slots, c.record_elems), dtype=np.uint16)
         _check("hs_read_buffer", self.lib.hs_read_buffer(self._h, int(req), int(layer), out.ctypes.data))
         return out
+
+    # -- memory layer: paged host pool ------------------------------------------------
+    def reserve(self, req: int, end: int, layer: int = -1):
+        """Reserve the host pages of (req, layer) covering positions [0, end); layer -1: all layers."""
+        _check("hs_reserve", self.lib.hs_reserve(self._h, int(req), int(layer), int(end)))
+
+    def release(self, req: int):
+        """Return the private host pages of request `req` (all layers) to the pool's free list."""
+        _check("hs_release", self.lib.hs_release(self._h, int(req)))
+
+    def host_usage(self) -> dict:
+        used, free, pinned = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+        _check("hs_host_usage", self.lib.hs_host_usage(self._h, ctypes.byref(used), ctypes.byref(free),
+                                                       ctypes.byref(pinned)))
+        return {"pages_in_use": used.value, "pages_free": free.value, "bytes_pinned": pinned.value}
 
     def read_history(self, req: int, layer: int, pos0: int, n: int):
         out = np.empty((n, self.cfg.record_elems), dtype=np.uint16)

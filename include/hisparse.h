@@ -67,9 +67,12 @@ enum hs_device_error {
   HS_DEVERR_RANGE = 1,    /* a top-k entry outside [0, capacity) other than -1 */
   HS_DEVERR_DUP = 2,      /* a top-k entry repeating an earlier one in the same list */
   HS_DEVERR_CLOCK = 4,    /* the 32-bit recency clock of a (request, layer) would wrap */
-  HS_DEVERR_APPEND = 8,   /* an append position outside [shared_prefix, capacity) */
+  HS_DEVERR_APPEND = 8,   /* an append position outside [shared_prefix, capacity), or on a host
+                             page not reserved (hs_reserve) */
   HS_DEVERR_LOC = 16,     /* an attention slot index outside [0, rows) */
-  HS_DEVERR_TIMEOUT = 32  /* a bounded wait inside a kernel gave up */
+  HS_DEVERR_TIMEOUT = 32, /* a bounded wait inside a kernel gave up */
+  HS_DEVERR_PAGE = 64     /* a miss fetch read a position whose host page is not reserved (the
+                             slot keeps its old contents) */
 };
 
 typedef struct {
@@ -98,18 +101,30 @@ typedef struct {
                                  slots, so the host-link transfer overlaps the HBM-bound attention.
                                  Copies left pending when no attention follows are finished by the
                                  next hs_resolve or hs_append_writethrough of that layer.  Needs
-                                 the GQA layout with at most 8 KV heads. */
+                                 the GQA layout. */
+  int32_t host_page_tokens;   /* positions per host page (summary §8, the memory layer allocates
+                                 the host pool in pages): 0 = automatic (1024, or the largest power
+                                 of two <= 1024 dividing shared_prefix); else a power of two that
+                                 divides shared_prefix */
+  int32_t host_on_demand;     /* 0: every page of [0, capacity) is reserved at pool creation.
+                                 1: pages are reserved on demand: by hs_prefill_write for the
+                                 positions it writes and by hs_reserve ahead of appends; a
+                                 request's private pages return to the pool with hs_release. */
 } hs_config;
 
 /* Record size in bytes for a configuration (MLA: 2*head_dim_qk; GQA: 2*kv_heads*(qk+v)). */
 int64_t hs_record_bytes(const hs_config* cfg);
 
 /*
- * Create a pool on `cuda_device` (summary §3, §8 "memory layer"): pinned, device-mapped host
- * history [L][shared_prefix][rec] + [R][L][capacity - shared_prefix][rec], hot buffer
- * [L][R][B][rec] in HBM, tags (-1 = empty), stamps (0 = empty), per-(request, layer) clock
- * (starts at 1), counters and attention workspace.  All slots start empty.  Synchronous,
- * not capturable.  Errors: HS_ERR_CONFIG, HS_ERR_ALLOC_HOST, HS_ERR_ALLOC_DEV, HS_ERR_CUDA.
+ * Create a pool on `cuda_device` (summary §3, §8 "memory layer").
+ *   - Host history: pinned, device-mapped pages of host_page_tokens records, carved from large
+ *     pinned slabs.  A device page table [R][L][ceil(capacity / page)] maps every (request, layer,
+ *     position) to its page.  The pages of [0, shared_prefix) are one copy per layer, mapped into
+ *     every request's table.
+ *   - Hot buffer [L][R][B][rec] in HBM, tags (-1 = empty), stamps (0 = empty), per-(request,
+ *     layer) clock (starts at 1), counters and attention workspace.  All slots start empty.
+ * With host_on_demand = 0 every page is reserved here; else none is.  Synchronous, not
+ * capturable.  Errors: HS_ERR_CONFIG, HS_ERR_ALLOC_HOST, HS_ERR_ALLOC_DEV, HS_ERR_CUDA.
  * Environment HS_FAULT=alloc_host|alloc_dev makes the named allocation fail (for tests).
  */
 int hs_pool_create(const hs_config* cfg, int cuda_device, hs_pool** out);
@@ -123,9 +138,10 @@ int hs_pool_reset(hs_pool* pool, void* stream);
 /*
  * Prefill write (summary §3 step (1)): copy n records from `src` (host or device memory,
  * [n][rec] bytes) into the host history of (req, layer) at positions [pos0, pos0 + n).
- * Positions below shared_prefix go to the shared history whatever `req` is.  Writes only the
- * host pool; the hot buffer is filled on demand by hs_resolve.  Enqueued on `stream`; the
- * caller keeps `src` alive until the stream reaches this point.  Errors: HS_ERR_ARG.
+ * Positions below shared_prefix go to the shared history whatever `req` is.  Reserves the pages
+ * it writes (synchronously), then enqueues the copy on `stream`; the caller keeps `src` alive
+ * until the stream reaches this point.  Writes only the host pool; the hot buffer is filled on
+ * demand by hs_resolve.  Errors: HS_ERR_ARG, HS_ERR_ALLOC_HOST, HS_ERR_CUDA.
  */
 int hs_prefill_write(hs_pool* pool, int req, int layer, int64_t pos0, int64_t n, const void* src,
                      void* stream);
@@ -251,8 +267,28 @@ int hs_read_state(hs_pool* pool, int layer, int32_t* h_tag, uint32_t* h_stamp, u
 /* Inspection: copy the hot buffer of (req, layer), [B][rec] bytes, to host memory `dst`. */
 int hs_read_buffer(hs_pool* pool, int req, int layer, void* dst);
 
-/* Inspection: copy n records of the host history of (req, layer) from position pos0 to `dst`. */
+/* Inspection: copy n records of the host history of (req, layer) from position pos0 to `dst`;
+ * positions on pages not reserved read as zeros. */
 int hs_read_history(hs_pool* pool, int req, int layer, int64_t pos0, int64_t n, void* dst);
+
+/*
+ * Memory layer (summary §8: paged host pool, grown on demand): reserve the host pages of
+ * (req, layer) that cover positions [0, end) -- layer = -1: every layer -- so that appends up to
+ * `end` have somewhere to go.  Pages of the shared prefix are reserved once per layer.
+ * Synchronous (it updates the device page table); call it outside captured graphs, before the
+ * decode steps that append there.  Errors: HS_ERR_ARG, HS_ERR_ALLOC_HOST, HS_ERR_CUDA.
+ */
+int hs_reserve(hs_pool* pool, int req, int layer, int64_t end);
+
+/*
+ * Return the private host pages of request `req` (every layer) to the pool's free list, for
+ * reuse by later reservations; the shared prefix stays.  The request's history reads as zeros
+ * afterwards.  Synchronises the device first.  Errors: HS_ERR_ARG, HS_ERR_CUDA.
+ */
+int hs_release(hs_pool* pool, int req);
+
+/* Host memory of the pool: pages mapped in some table, pages on the free list, pinned bytes held. */
+int hs_host_usage(hs_pool* pool, int64_t* pages_in_use, int64_t* pages_free, int64_t* bytes_pinned);
 
 #ifdef __cplusplus
 }
