@@ -35,7 +35,7 @@ _lib = None
 
 LRU, FIFO, RANDOM, SWAP = 0, 1, 2, 3
 POLICY = {"lru": LRU, "fifo": FIFO, "random": RANDOM, "swap": SWAP}
-ERR_RANGE, ERR_DUP, ERR_CLOCK, ERR_APPEND = 1, 2, 4, 8
+ERR_RANGE, ERR_DUP, ERR_CLOCK, ERR_APPEND, ERR_SLOTS = 1, 2, 4, 8, 128
 
 
 def build() -> str:
@@ -55,6 +55,8 @@ def _load():
             P, I, I64, U64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint64
             lib.orc_cache_new.restype = P
             lib.orc_cache_new.argtypes = [I, I, I, U64, I, I, I, I, I64]
+            lib.orc_set_cap.restype = I
+            lib.orc_set_cap.argtypes = [P, I]
             lib.orc_cache_free.restype = None
             lib.orc_cache_free.argtypes = [P]
             lib.orc_resolve.restype = I
@@ -102,6 +104,11 @@ class Cache:
 
     def append(self, p):
         return self.lib.orc_append(self._h, int(p))
+
+    def set_cap(self, cap):
+        """The buffer now holds slots [0, cap) only (a buffer grown on demand)."""
+        if self.lib.orc_set_cap(self._h, int(cap)) != 0:
+            raise ValueError("cap outside [0, B]")
 
     def slots(self):
         tag = np.empty(self.B, dtype=np.int32)

@@ -33,7 +33,13 @@
  *     history and into the slot that already holds its position, else the slot
  *     with the smallest key over all slots; stamp = clock, clock += 1;
  *   - invalid top-k entries (out of [0, C), or a repeat of an earlier entry) set
- *     an error bit and are treated as padding (-1).
+ *     an error bit and are treated as padding (-1);
+ *   - a buffer grown on demand (§8: the coordinator allocates and grows the
+ *     per-request, per-layer device cache as it is needed) holds only its first
+ *     `cap` slots: resolve and append probe, evict and install among slots
+ *     [0, cap) alone, the random key keeps its counter over all B slots; a
+ *     buffer of fewer than k slots cannot take a step: resolve and append then
+ *     set an error bit, change nothing and return -1 locations.
  */
 #include <math.h>
 #include <stdint.h>
@@ -41,10 +47,11 @@
 #include <string.h>
 
 enum { ORC_LRU = 0, ORC_FIFO = 1, ORC_RANDOM = 2, ORC_SWAP = 3 };
-enum { ORC_ERR_RANGE = 1, ORC_ERR_DUP = 2, ORC_ERR_CLOCK = 4, ORC_ERR_APPEND = 8 };
+enum { ORC_ERR_RANGE = 1, ORC_ERR_DUP = 2, ORC_ERR_CLOCK = 4, ORC_ERR_APPEND = 8, ORC_ERR_SLOTS = 128 };
 
 typedef struct {
     int B, k, policy;
+    int cap;                /* slots [0, cap) exist; B unless the buffer was grown on demand */
     uint64_t seed;
     int R, L, r, l;
     int64_t C;
@@ -61,7 +68,7 @@ orc_cache *orc_cache_new(int B, int k, int policy, uint64_t seed, int R, int L, 
     if (B < 1 || k < 1 || k > B || C < 1 || policy < 0 || policy > 3) return NULL;
     orc_cache *c = (orc_cache *)calloc(1, sizeof(orc_cache));
     if (!c) return NULL;
-    c->B = B; c->k = k; c->policy = policy; c->seed = seed;
+    c->B = B; c->k = k; c->policy = policy; c->seed = seed; c->cap = B;
     c->R = R; c->L = L; c->r = r; c->l = l; c->C = C;
     c->tag = (int32_t *)malloc(sizeof(int32_t) * (size_t)B);
     c->stamp = (uint32_t *)calloc((size_t)B, sizeof(uint32_t));
@@ -71,6 +78,13 @@ orc_cache *orc_cache_new(int B, int k, int policy, uint64_t seed, int R, int L, 
     for (int64_t p = 0; p < C; ++p) c->where[p] = -1;
     c->clock = 1;
     return c;
+}
+
+/* the buffer now holds slots [0, cap), 0 <= cap <= B */
+int orc_set_cap(orc_cache *c, int cap) {
+    if (cap < 0 || cap > c->B) return -1;
+    c->cap = cap;
+    return 0;
 }
 
 void orc_cache_free(orc_cache *c) {
@@ -132,10 +146,16 @@ uint32_t orc_validate(const int32_t *S, int k, int64_t C, uint8_t *valid) {
  * RESOLVE one step (§3 and §5 of the HiSparse summary): look the selected
  * positions up in the hot buffer, keep the hits, evict victims for the misses,
  * install the misses, update the stamps.  locs[i] = slot of S[i] after the step,
- * or -1 for padding / invalid entries.  Returns the number of misses.
+ * or -1 for padding / invalid entries.  Returns the number of misses, or -1 when
+ * the buffer holds fewer than k slots.
  */
 int orc_resolve(orc_cache *c, const int32_t *S, int32_t *locs) {
-    const int B = c->B, k = c->k;
+    const int B = c->cap, k = c->k;
+    if (B < k) {  /* too few slots for a step */
+        c->err |= ORC_ERR_SLOTS;
+        for (int i = 0; i < k; ++i) locs[i] = -1;
+        return -1;
+    }
     uint8_t *valid = (uint8_t *)malloc((size_t)k);
     int32_t *hit_slot = (int32_t *)malloc(sizeof(int32_t) * (size_t)k);
     uint8_t *slot_hit = (uint8_t *)calloc((size_t)B, 1);
@@ -199,17 +219,19 @@ int orc_resolve(orc_cache *c, const int32_t *S, int32_t *locs) {
 
 /*
  * Write-through append of position p (§3 step (5)): returns the slot that now
- * holds p, or -1 (and an error bit) when p is outside [0, C).
+ * holds p, or -1 (and an error bit) when p is outside [0, C) or the buffer holds
+ * fewer than k slots.
  */
 int orc_append(orc_cache *c, int64_t p) {
     if (p < 0 || p >= c->C) { c->err |= ORC_ERR_APPEND; return -1; }
     if ((uint64_t)c->clock + 1u >= 0xFFFFFFFFull) c->err |= ORC_ERR_CLOCK;
+    if (c->cap < c->k) { c->err |= ORC_ERR_SLOTS; return -1; }
     int slot = -1;
-    for (int j = 0; j < c->B; ++j) if (c->tag[j] == (int32_t)p) slot = j;
+    for (int j = 0; j < c->cap; ++j) if (c->tag[j] == (int32_t)p) slot = j;
     if (slot < 0) {
         slot = 0;
         uint32_t best = orc_key(c, 0);
-        for (int j = 1; j < c->B; ++j) {
+        for (int j = 1; j < c->cap; ++j) {
             uint32_t kj = orc_key(c, j);
             if (kj < best) { best = kj; slot = j; }
         }

@@ -10,7 +10,10 @@ off-by-one in the stamps) fails at least one of them:
   * B = k: swap-vanilla and LRU misses = |S_t minus S_{t-1}|;
   * Belady equals the exhaustive minimum on tiny traces, and lower-bounds LRU,
     FIFO, random and swap-vanilla;
-  * the random policy's key is splitmix64 at the stated counter.
+  * the random policy's key is splitmix64 at the stated counter;
+  * a buffer grown on demand (slots [0, cap) only) is the recency list / queue of
+    cap entries, equals the full buffer while its growth stays ahead of the
+    context, and refuses a step with fewer than k slots.
 """
 import itertools
 import json
@@ -290,3 +293,75 @@ def test_policy_order_on_drift_traces():
     assert swap > fifo >= lru > bel
     assert rnd >= lru
     assert lru2 < lru
+
+
+# ---- buffers grown on demand: only slots [0, cap) exist ----------------------------------
+
+@pytest.mark.parametrize("seed", range(4))
+@pytest.mark.parametrize("B,cap,k,npos", [(32, 8, 3, 20), (64, 16, 5, 40), (20, 6, 6, 12)])
+def test_capped_lru_is_the_recency_list_of_cap_entries(seed, B, cap, k, npos):
+    rng = np.random.default_rng(300 + seed)
+    trace = _random_trace(rng, 30, k, npos)
+    c = oracle.Cache(B, k, "lru", C=npos)
+    c.set_cap(cap)
+    for S, (m_ref, order) in zip(trace, _lru_list_model(cap, trace)):
+        m, locs = c.resolve(S)
+        assert m == m_ref
+        assert (locs < cap).all()
+        tag, stamp = c.slots()
+        assert (tag[cap:] == -1).all() and (stamp[cap:] == 0).all()
+        occ = tag >= 0
+        assert [int(t) for _, t in sorted(zip(stamp[occ].tolist(), tag[occ].tolist()))] == order
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_capped_fifo_is_the_insertion_queue_of_cap_entries(seed):
+    rng = np.random.default_rng(400 + seed)
+    B, cap, k, npos = 40, 10, 4, 30
+    trace = _random_trace(rng, 30, k, npos)
+    c = oracle.Cache(B, k, "fifo", C=npos)
+    c.set_cap(cap)
+    for S, (m_ref, queue) in zip(trace, _fifo_queue_model(cap, trace)):
+        m, _ = c.resolve(S)
+        assert m == m_ref
+        tag, stamp = c.slots()
+        occ = tag >= 0
+        assert [int(t) for _, t in sorted(zip(stamp[occ].tolist(), tag[occ].tolist()))] == queue
+
+
+@pytest.mark.parametrize("policy", ["lru", "fifo", "random", "swap"])
+def test_growth_ahead_of_the_context_equals_the_full_buffer(policy):
+    """Empty slots go first, lowest slot first: a buffer whose cap stays >= min(B, context) never
+    evicts where the full buffer would not, so every step matches the full buffer exactly."""
+    ctx0, k, B, T, page = 40, 8, 128, 60, 16
+    spec = inputs.TraceSpec(ctx0=ctx0, k=k, steps=T, keep=0.7, recency_mean=12, appends=True)
+    tr = inputs.drift_traces(spec, 1, 1, seed=17)[:, 0, 0]
+    full = oracle.Cache(B, k, policy, seed=3, C=ctx0 + T)
+    grown = oracle.Cache(B, k, policy, seed=3, C=ctx0 + T)
+    for t, S in enumerate(tr):
+        ctx = ctx0 + t + 1  # the append makes position ctx0 + t
+        grown.set_cap(min(B, -(-max(ctx, k) // page) * page))
+        assert full.append(ctx0 + t) == grown.append(ctx0 + t)
+        a, b = full.resolve(S), grown.resolve(S)
+        assert a[0] == b[0] and np.array_equal(a[1], b[1]), t
+        assert all(np.array_equal(x, y) for x, y in zip(full.slots(), grown.slots())), t
+    assert full.counters() == grown.counters()
+
+
+@pytest.mark.parametrize("policy", ["lru", "random"])
+def test_fewer_than_k_slots_refuse_the_step(policy):
+    c = oracle.Cache(16, 6, policy, C=100)
+    c.set_cap(16)
+    c.resolve(np.arange(6, dtype=np.int32))
+    before = (c.slots(), c.counters())
+    c.set_cap(5)
+    m, locs = c.resolve(np.arange(10, 16, dtype=np.int32))
+    assert m == -1 and (locs == -1).all()
+    assert c.append(50) == -1
+    tag, stamp = c.slots()
+    cnt = c.counters()
+    assert np.array_equal(tag, before[0][0]) and np.array_equal(stamp, before[0][1])
+    assert cnt["err"] == oracle.ERR_SLOTS
+    assert {k_: v for k_, v in cnt.items() if k_ != "err"} == {k_: v for k_, v in before[1].items() if k_ != "err"}
+    with pytest.raises(ValueError):
+        c.set_cap(17)
