@@ -15,13 +15,14 @@ STATUS_NAMES = {0: "HS_OK", -1: "HS_ERR_CONFIG", -2: "HS_ERR_ALLOC_HOST", -3: "H
 POLICY_LRU, POLICY_FIFO, POLICY_RANDOM, POLICY_SWAP_VANILLA = 0, 1, 2, 3
 LAYOUT_MLA, LAYOUT_GQA = 0, 1
 DEVERR_RANGE, DEVERR_DUP, DEVERR_CLOCK, DEVERR_APPEND, DEVERR_LOC, DEVERR_TIMEOUT = 1, 2, 4, 8, 16, 32
-DEVERR_PAGE = 64
+DEVERR_PAGE, DEVERR_SLOTS = 64, 128
 
 # every entry point include/hisparse.h declares
 EXPORTS = ("hs_record_bytes", "hs_pool_create", "hs_pool_destroy", "hs_pool_reset", "hs_prefill_write",
            "hs_append_writethrough", "hs_resolve", "hs_sparse_attn", "hs_stats", "hs_read_state",
            "hs_read_buffer", "hs_read_history", "hs_sparse_attn_noalloc", "hs_append_resolve",
-           "hs_resolve_range", "hs_sparse_attn_range", "hs_reserve", "hs_release", "hs_host_usage")
+           "hs_resolve_range", "hs_sparse_attn_range", "hs_reserve", "hs_release", "hs_host_usage",
+           "hs_device_usage")
 
 
 class hs_config(ctypes.Structure):
@@ -44,6 +45,9 @@ class hs_config(ctypes.Structure):
         ("fetch_in_attention", ctypes.c_int32),
         ("host_page_tokens", ctypes.c_int32),
         ("host_on_demand", ctypes.c_int32),
+        ("buffer_page_slots", ctypes.c_int32),
+        ("device_pool_slots", ctypes.c_int64),
+        ("host_to_device_ratio", ctypes.c_double),
     ]
 
 
@@ -100,6 +104,7 @@ def load(build_if_missing: bool = False):
             "hs_reserve": (I, [P, I, I, I64]),
             "hs_release": (I, [P, I]),
             "hs_host_usage": (I, [P, P, P, P]),
+            "hs_device_usage": (I, [P, P, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)

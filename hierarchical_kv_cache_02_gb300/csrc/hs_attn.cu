@@ -28,13 +28,16 @@ constexpr float kLog2e = 1.4426950408889634f;
 struct AttnArgs {
   const uint16_t* q;     // [R][Hq][DK] bf16
   const int32_t* locs;   // [R][k]
-  const uint8_t* kv;     // row base: row (r, loc) at kv + (r * rows + loc) * rec
+  const uint8_t* kv;     // caller rows (kv_pt null): row (r, loc) at kv + (r * rows + loc) * rec
+  const uint64_t* kv_pt; // hot-buffer rows: [R][kv_pages] device address of each buffer page
+  const int32_t* kv_cap; // hot-buffer rows: [R] rows each buffer holds (<= rows)
+  int kv_pages, kv_shift;
   float* out;            // [R][Hq][DV]
   float* part;           // [R][S][Hq][DV]
   float* ml;             // [R][S][Hq][2]
   uint32_t* ticket;      // [R][groups + 1]: split tickets per group, then the pending-list count
   uint32_t* err;
-  int64_t rows, rec;
+  int64_t rows, rec;     // rows: per request (the configured B for the hot buffer)
   int64_t kstride, vdelta;  // K of KV block g at g * kstride, V at K + vdelta (bytes)
   float qscale;             // scale * log2(e)
   int R, Hq, k, S, chunk, groups;  // R: requests in this launch (the grid), starting at r0
@@ -42,11 +45,27 @@ struct AttnArgs {
   // fetch-in-attention mode (hot-buffer rows only): misses still to copy from the host history
   const hs_pending* pend;   // [R][k] host address and slot of a miss still to copy (src 0: none); null: none
   uint32_t* pend_live;      // [R]
-  uint8_t* buf_w;           // writable view of the rows (the hot buffer of the layer)
   int L, layer;
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+// Rows of request r.  A hot buffer is paged (a row of page addresses); caller rows are contiguous
+// and take the form of one page of 2^31 rows, so every kernel addresses both the same way:
+// row `loc` lives at pg[loc >> shift] + (loc mod 2^shift) * rec.
+__device__ __forceinline__ void rows_setup(const AttnArgs& a, int r, uint64_t* s_pg) {
+  if (a.kv_pt != nullptr) {
+    for (int i = threadIdx.x; i < a.kv_pages; i += blockDim.x) s_pg[i] = a.kv_pt[(int64_t)r * a.kv_pages + i];
+  } else if (threadIdx.x == 0) {
+    s_pg[0] = (uint64_t)(uintptr_t)(a.kv + (int64_t)r * a.rows * a.rec);
+  }
+}
+__device__ __forceinline__ int64_t rows_of(const AttnArgs& a, int r) {
+  return a.kv_cap != nullptr ? min(a.rows, (int64_t)a.kv_cap[r]) : a.rows;
+}
+__device__ __forceinline__ uint8_t* row_addr(const uint64_t* s_pg, int shift, int64_t rec, int32_t loc) {
+  return (uint8_t*)(uintptr_t)s_pg[loc >> shift] + (int64_t)(loc & (int32_t)((1u << shift) - 1u)) * rec;
+}
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
@@ -274,6 +293,7 @@ __global__ void __launch_bounds__(AttnCfg<DK, DV, G, NW>::THREADS) k_attn_cc(Att
   __shared__ uint32_t tok_mask[kStages];
   __shared__ uint32_t abort_flag;
   __shared__ uint32_t is_last;
+  __shared__ uint64_t s_pg[kMaxSlotPages];
 
   const int split = blockIdx.x, r = a.r0 + (int)blockIdx.y, grp = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -282,7 +302,9 @@ __global__ void __launch_bounds__(AttnCfg<DK, DV, G, NW>::THREADS) k_attn_cc(Att
   const int nst = (t1 - t0 + T - 1) / T;
   const int64_t rec = a.rec;
   const int32_t* locs = a.locs + (int64_t)(r - a.r0) * a.k;
+  const int64_t rows_r = rows_of(a, r);
 
+  rows_setup(a, r, s_pg);
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full_bar[s], 1u);
@@ -316,7 +338,7 @@ __global__ void __launch_bounds__(AttnCfg<DK, DV, G, NW>::THREADS) k_attn_cc(Att
         for (int j = 0; j < T; ++j) {
           const int idx = t0 + st * T + j;
           int32_t loc = idx < t1 ? locs[idx] : -1;
-          if (loc < -1 || (int64_t)loc >= a.rows) {
+          if (loc < -1 || (int64_t)loc >= rows_r) {
             bad = 1u;
             loc = -1;
           }
@@ -332,7 +354,7 @@ __global__ void __launch_bounds__(AttnCfg<DK, DV, G, NW>::THREADS) k_attn_cc(Att
 #pragma unroll
         for (int j = 0; j < T; ++j) {
           if (lc[j] >= 0)
-            bulk_g2s(dst + (size_t)j * rec, a.kv + ((int64_t)r * a.rows + lc[j]) * rec, (uint32_t)rec, &full_bar[b]);
+            bulk_g2s(dst + (size_t)j * rec, row_addr(s_pg, a.kv_shift, rec, lc[j]), (uint32_t)rec, &full_bar[b]);
         }
         issued = st + 1;
       }
@@ -573,6 +595,7 @@ __global__ void __launch_bounds__((kGqaWarps + kGqaProducers) * 32, 1) k_attn_gq
   __shared__ float s_m[NW][8], s_l[NW][8], s_fin[8][2];
   __shared__ uint32_t s_mask[NW][NS];  // valid tokens of the stage in each buffer (bit j: token j)
   __shared__ uint32_t is_last, abort_flag, use_pend;
+  __shared__ uint64_t s_pg[kMaxSlotPages];
 
   const int split = blockIdx.x, r = a.r0 + (int)blockIdx.y, g = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -606,7 +629,17 @@ __global__ void __launch_bounds__((kGqaWarps + kGqaProducers) * 32, 1) k_attn_gq
     // ---------------- producers: producer pw fills consumer pw's buffers, stage by stage ----------------
     const int w = warp - NW;
     const int ni = w < nst ? (nst - w + NW - 1) / NW : 0;
-    const uint8_t* kvg = a.kv + (int64_t)r * a.rows * rec + (int64_t)g * a.kstride;
+    const int64_t goff = (int64_t)g * a.kstride;  // KV head g's slice of a row
+    const int rows_r = (int)rows_of(a, r);
+    {  // the page row, filled by the producers for the producers
+      const int pt = (int)threadIdx.x - NW * 32;
+      if (a.kv_pt != nullptr) {
+        if (pt < a.kv_pages) s_pg[pt] = a.kv_pt[(int64_t)r * a.kv_pages + pt];
+      } else if (pt == 0) {
+        s_pg[0] = (uint64_t)(uintptr_t)(a.kv + (int64_t)r * a.rows * rec);
+      }
+      asm volatile("bar.sync 2, %0;" ::"n"(kGqaProducers * 32) : "memory");
+    }
     bool ok = true;
     int issued = 0;
     // the slot (and, FETCH, the host address of a pending record, 0 if none) of token `lane` of
@@ -620,7 +653,7 @@ __global__ void __launch_bounds__((kGqaWarps + kGqaProducers) * 32, 1) k_attn_gq
       q = (FETCH && in && pend_on) ? pend_r[x].src : 0ull;
     };
     auto stage_info = [&](int32_t l, uint64_t q, int32_t& loc, uint64_t& pp, uint32_t& vmask, uint32_t& pmask) {
-      if (l < -1 || (int64_t)l >= a.rows) {
+      if (l < -1 || l >= rows_r) {
         atomicOr(a.err, (uint32_t)HS_DEVERR_LOC);
         l = -1;
       }
@@ -678,12 +711,13 @@ __global__ void __launch_bounds__((kGqaWarps + kGqaProducers) * 32, 1) k_attn_gq
       if (!FETCH || pmask == 0u) {
         if (lane == 0) mbar_arrive_expect_tx(&full[w][b], (uint32_t)__popc(vmask) * 512u);
         __syncwarp();
-        if (loc >= 0) bulk_g2s(dst + lane * RW, kvg + (int64_t)loc * rec, 512u, &full[w][b]);
+        if (loc >= 0) bulk_g2s(dst + lane * RW, row_addr(s_pg, a.kv_shift, rec, loc) + goff, 512u, &full[w][b]);
       } else {
         // resident rows by bulk copy; the arrival comes after the pending rows are stored, below
         if (lane == 0) mbar_expect_tx(&full[w][b], (uint32_t)__popc(vmask & ~pmask) * 512u);
         __syncwarp();
-        if (loc >= 0 && pp == 0ull) bulk_g2s(dst + lane * RW, kvg + (int64_t)loc * rec, 512u, &full[w][b]);
+        if (loc >= 0 && pp == 0ull)
+          bulk_g2s(dst + lane * RW, row_addr(s_pg, a.kv_shift, rec, loc) + goff, 512u, &full[w][b]);
       }
       int32_t loc2;
       uint64_t pp2;
@@ -705,7 +739,7 @@ __global__ void __launch_bounds__((kGqaWarps + kGqaProducers) * 32, 1) k_attn_gq
               const uint4 v = u < kPre ? vc[u < kPre ? u : 0] : load_row(__shfl_sync(0xffffffffu, pp, j));
               *(uint4*)(dst + j * RW + lane * 16) = v;
               const int32_t slot = __shfl_sync(0xffffffffu, loc, j);
-              *((uint4*)(a.buf_w + ((int64_t)r * a.rows + slot) * rec + (int64_t)g * a.kstride) + lane) = v;
+              *((uint4*)(row_addr(s_pg, a.kv_shift, rec, slot) + goff) + lane) = v;
             }
           }
           __syncwarp();
@@ -1057,6 +1091,7 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_umma(AttnArgs a) {
   __shared__ uint32_t s_tmem, abort_flag;
   __shared__ float s_m[kUHeads], s_l[kUHeads], s_alpha[kUHeads], s_red[4][kUHeads];
   __shared__ uint32_t s_need[2][4];
+  __shared__ uint64_t s_pg[kMaxSlotPages];
 
   const int split = blockIdx.x, r = a.r0 + (int)blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1078,12 +1113,14 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_umma(AttnArgs a) {
     s_m[h] = -INFINITY;
     s_l[h] = 0.f;
   }
+  rows_setup(a, r, s_pg);
   {
     const int32_t* locs = a.locs + (int64_t)(r - a.r0) * a.k + t0;
+    const int64_t rows_r = rows_of(a, r);
     bool bad = false;
     for (int x = tid; x < n; x += kUThreads) {
       int32_t loc = locs[x];
-      if (loc < -1 || (int64_t)loc >= a.rows) {
+      if (loc < -1 || (int64_t)loc >= rows_r) {
         bad = true;
         loc = -1;
       }
@@ -1106,7 +1143,6 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_umma(AttnArgs a) {
     const int pw = warp - kUWarpMma - 1, pl = pw * 32 + lane;
     const uint16_t* qr = a.q + (int64_t)(r - a.r0) * a.Hq * kUDim;
     const uint32_t sq_u = smem_u32(sQ), skv_u = smem_u32(sKV);
-    const uint8_t* kvr = a.kv + (int64_t)r * a.rows * a.rec;
     bool ok = true;
     auto load_q = [&](int g) {  // global half index g = 2 tile + half
       if (g >= 1) {
@@ -1141,7 +1177,8 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_umma(AttnArgs a) {
         const int row = rg * 8 + (lane & 7);
         const int x = i * kUTok + row;
         const int32_t loc = x < n ? s_locs[x] : -1;
-        const uint8_t* src = kvr + (loc >= 0 ? (int64_t)loc * a.rec : 0);
+        // padding reads nothing (zero fill); its source is any mapped address
+        const uint8_t* src = loc >= 0 ? row_addr(s_pg, a.kv_shift, a.rec, loc) : (const uint8_t*)a.q;
         const uint32_t dst = skv_u + (uint32_t)(rg * kUSboKv + (lane & 7) * 16);
         const uint32_t nb = loc >= 0 ? 16u : 0u;
 #pragma unroll 6
@@ -1482,11 +1519,16 @@ int hs_launch_attn(hs_pool* p, int layer, int r0, int nreq, const void* d_q, con
   AttnArgs a{};
   a.q = (const uint16_t*)d_q;
   a.locs = d_locs;
-  if (kv_base == nullptr) {
-    a.kv = p->buf + (int64_t)layer * c.num_requests * c.buffer_slots * p->rec;
+  if (kv_base == nullptr) {  // the layer's hot buffers, through the slot table
+    a.kv_pt = p->slot_table + (int64_t)layer * c.num_requests * p->slot_pages;
+    a.kv_cap = p->slot_cap + (int64_t)layer * c.num_requests;
+    a.kv_pages = p->slot_pages;
+    a.kv_shift = p->slot_shift;
     a.rows = c.buffer_slots;
   } else {
     a.kv = (const uint8_t*)kv_base;
+    a.kv_pages = 1;
+    a.kv_shift = 31;
     a.rows = kv_rows;
   }
   a.out = d_out;
@@ -1513,7 +1555,6 @@ int hs_launch_attn(hs_pool* p, int layer, int r0, int nreq, const void* d_q, con
   const bool hot = kv_base == nullptr;
   a.pend = (hot && p->pend != nullptr) ? p->pend + (int64_t)layer * c.num_requests * c.top_k : nullptr;
   a.pend_live = (hot && p->pend_live != nullptr) ? p->pend_live + (int64_t)layer * c.num_requests : nullptr;
-  a.buf_w = hot ? p->buf + (int64_t)layer * c.num_requests * c.buffer_slots * p->rec : nullptr;
   a.L = c.num_layers;
   a.layer = layer;
   return dispatch(c, &a, pl, st) == cudaSuccess ? HS_OK : HS_ERR_CUDA;
@@ -1610,6 +1651,8 @@ extern "C" int hs_sparse_attn_noalloc(const hs_config* cfg, const void* d_q, con
   a.q = (const uint16_t*)d_q;
   a.locs = d_locs;
   a.kv = (const uint8_t*)d_kv;
+  a.kv_pages = 1;
+  a.kv_shift = 31;
   a.rows = kv_rows;
   a.out = d_out;
   a.part = part;

@@ -23,6 +23,8 @@ struct hs_rl_state {
 };
 
 struct hs_host_pages;  // host-side page allocator and the host mirror of the page table
+struct hs_dev_pages;   // device cache pool allocator and the host mirror of the slot table
+constexpr int kMaxSlotPages = 64;  // device buffer pages per (request, layer)
 
 // A miss the resolve left to the attention (fetch-in-attention mode): the device address of its
 // record in the mapped host history (0: nothing pending for this top-k entry) and its slot.
@@ -41,7 +43,12 @@ struct hs_pool {
   int64_t max_pages;     // pages per (request, layer): ceil(capacity / page size)
   int page_shift;        // log2 of the records per page
   hs_host_pages* host;
-  uint8_t* buf;
+  uint8_t* buf;          // the device cache pool: pages of slot_page slots x rec bytes
+  uint64_t* slot_table;  // device [L][R][slot_pages]: device address of each buffer page, 0 = none
+  int32_t* slot_cap;     // device [L][R]: slots the buffer holds, min(B, pages x slot_page)
+  int slot_pages;        // pages per buffer: ceil(B / slot_page), <= kMaxSlotPages
+  int slot_shift;        // log2 of the slots per page
+  hs_dev_pages* dev;
   int32_t* tag;
   uint32_t* stamp;
   hs_rl_state* state;
@@ -106,11 +113,16 @@ __device__ __forceinline__ const uint64_t* hs_page_row(const uint64_t* pt, int64
   return cache;
 }
 
+// Slot j of a buffer whose page row (device addresses of its pages) is `row`.
+__device__ __forceinline__ uint8_t* hs_slot_addr(const uint64_t* row, int shift, int64_t rec, int j) {
+  return (uint8_t*)(uintptr_t)row[j >> shift] + (int64_t)(j & ((1 << shift) - 1)) * rec;
+}
+
 // Finish the host -> slot copies that a resolve in fetch-in-attention mode left pending for
 // (r, l) and that no attention has completed.  The entries [k*part/nparts, k*(part+1)/nparts) are
-// copied by this CTA, one warp per record.
-__device__ __forceinline__ void hs_copy_pending(const hs_pending* pend, int k, int64_t rec, uint8_t* buf_r, int part,
-                                                int nparts) {
+// copied by this CTA, one warp per record; `slots` is the buffer's page row.
+__device__ __forceinline__ void hs_copy_pending(const hs_pending* pend, int k, int64_t rec, const uint64_t* slots,
+                                                int slot_shift, int part, int nparts) {
   const int e0 = (int)((int64_t)k * part / nparts), e1 = (int)((int64_t)k * (part + 1) / nparts);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
   const int nv = (int)(rec / 16);
@@ -118,7 +130,7 @@ __device__ __forceinline__ void hs_copy_pending(const hs_pending* pend, int k, i
     const hs_pending e = pend[i];
     if (e.src == 0ull) continue;
     const uint4* src = (const uint4*)e.src;
-    uint4* dst = (uint4*)(buf_r + (int64_t)e.slot * rec);
+    uint4* dst = (uint4*)hs_slot_addr(slots, slot_shift, rec, e.slot);
     for (int v = lane; v < nv; v += 32) dst[v] = src[v];
   }
 }

@@ -3,6 +3,9 @@
 // authoritative KV history; HBM holds only B slots per (request, layer) plus metadata.  The host
 // pool is paged: fixed-size pages carved from large pinned, device-mapped slabs, found by the
 // kernels through a device page table, reserved up front or on demand and returned to a free list.
+// The hot buffers are paged the same way in one device cache pool: a (request, layer) buffer holds
+// all its pages from creation, or grows page by page as its context grows (§8: the coordinator
+// allocates and grows the per-request, per-layer device cache on demand).
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -55,7 +58,22 @@ int check_config(const hs_config* c) {
     return HS_ERR_CONFIG;
   if (c->shared_prefix > 0 && c->shared_prefix % page_tokens_for(c) != 0) return HS_ERR_CONFIG;
   if (c->host_on_demand != 0 && c->host_on_demand != 1) return HS_ERR_CONFIG;
+  if (c->buffer_page_slots < 0 || c->buffer_page_slots > (1 << 20) ||
+      (c->buffer_page_slots > 0 && (!is_pow2(c->buffer_page_slots) ||
+                                    (c->buffer_slots + c->buffer_page_slots - 1) / c->buffer_page_slots > kMaxSlotPages)))
+    return HS_ERR_CONFIG;
+  if (c->device_pool_slots < 0) return HS_ERR_CONFIG;
+  if (!(c->host_to_device_ratio >= 0.0) || c->host_to_device_ratio > 1e12) return HS_ERR_CONFIG;  // rejects NaN
   return HS_OK;
+}
+
+// slots per device buffer page: the configured power of two, or the smallest power of two >= 16
+// that cuts B into at most kMaxSlotPages pages
+int64_t slot_page_for(const hs_config* c) {
+  if (c->buffer_page_slots > 0) return c->buffer_page_slots;
+  int64_t ps = 16;
+  while ((c->buffer_slots + ps - 1) / ps > kMaxSlotPages) ps <<= 1;
+  return ps;
 }
 
 template <typename T>
@@ -84,6 +102,16 @@ struct hs_host_pages {
   int64_t pages_in_use = 0;
 };
 
+// The device cache pool: pages of page_slots slots, and the host mirror of the slot table.
+struct hs_dev_pages {
+  int64_t page_slots = 0, page_bytes = 0, total_pages = 0;
+  bool on_demand = false;               // device_pool_slots > 0: buffers grow page by page
+  std::vector<int64_t> free_pages;      // page indices; the next one handed out is at the back
+  std::vector<uint64_t> table;          // [L][R][slot_pages] device address of each page, 0 = none
+  std::vector<int32_t> npages;          // [L][R] pages each buffer holds (its first ones, in order)
+  int64_t pages_in_use = 0;
+};
+
 namespace {
 
 int host_alloc(uint8_t** h, uint8_t** d, size_t bytes) {
@@ -109,7 +137,10 @@ void free_pool(hs_pool* p) {
     for (auto& sl : p->host->slabs) cudaFreeHost(sl.first);
     delete p->host;
   }
+  delete p->dev;
   cudaFree(p->page_table);
+  cudaFree(p->slot_table);
+  cudaFree(p->slot_cap);
   cudaFree(p->buf);
   cudaFree(p->tag);
   cudaFree(p->stamp);
@@ -170,6 +201,9 @@ int do_reset(hs_pool* p, cudaStream_t st) {
 // pool grows, at most a quarter over-reserved), never more pages than the page table could still take.
 constexpr size_t kSlabMin = (size_t)256 << 20;
 
+// bytes of the device cache pool (the base of host_to_device_ratio)
+int64_t dev_pool_bytes(const hs_pool* p) { return p->dev->total_pages * p->dev->page_bytes; }
+
 // n more pages on the free list
 int grow_free_pages(hs_pool* p, int64_t n) {
   hs_host_pages& h = *p->host;
@@ -181,7 +215,13 @@ int grow_free_pages(hs_pool* p, int64_t n) {
     size_t pinned = 0;
     for (size_t b : h.slab_bytes) pinned += b;
     const int64_t min_pages = std::max<int64_t>(1, (int64_t)(std::max(kSlabMin, pinned / 4) / (size_t)h.page_bytes));
-    const int64_t np = std::max(want, std::min(min_pages, room));
+    int64_t np = std::max(want, std::min(min_pages, room));
+    if (p->cfg.host_to_device_ratio > 0.0) {  // the host pool's bound relative to the device cache pool
+      const double limit = p->cfg.host_to_device_ratio * (double)dev_pool_bytes(p);
+      const int64_t allow = (int64_t)((limit - (double)pinned) / (double)h.page_bytes);
+      if (allow < want) return HS_ERR_ALLOC_HOST;
+      np = std::min(np, allow);
+    }
     uint8_t *hp = nullptr, *dp = nullptr;
     int rc = host_alloc(&hp, &dp, (size_t)(np * h.page_bytes));
     if (rc != HS_OK) {
@@ -195,6 +235,15 @@ int grow_free_pages(hs_pool* p, int64_t n) {
   return HS_OK;
 }
 
+// host pages of (req, layer) among [pg0, pg1) that have none yet
+int64_t host_pages_missing(const hs_pool* p, int req, int layer, int64_t pg0, int64_t pg1) {
+  const hs_host_pages& h = *p->host;
+  int64_t need = 0;
+  for (int64_t g = pg0; g < std::min(pg1, p->max_pages); ++g)
+    if (h.host_pt[((int64_t)req * p->cfg.num_layers + layer) * p->max_pages + g] == nullptr) ++need;
+  return need;
+}
+
 // Give every missing page of pages [pg0, pg1) of (req, layer) a page; the shared prefix's pages are
 // one per layer, mapped into every request's table.  Updates the host mirror only; *changed is set
 // when an entry changed.
@@ -202,9 +251,7 @@ int reserve_pages(hs_pool* p, int req, int layer, int64_t pg0, int64_t pg1, bool
   hs_host_pages& h = *p->host;
   const int R = p->cfg.num_requests, L = p->cfg.num_layers;
   pg1 = std::min(pg1, p->max_pages);
-  int64_t need = 0;
-  for (int64_t g = pg0; g < pg1; ++g)
-    if (h.host_pt[((int64_t)req * L + layer) * p->max_pages + g] == nullptr) ++need;
+  const int64_t need = host_pages_missing(p, req, layer, pg0, pg1);
   if (need == 0) return HS_OK;
   int rc = grow_free_pages(p, need);
   if (rc != HS_OK) return rc;
@@ -225,14 +272,84 @@ int reserve_pages(hs_pool* p, int req, int layer, int64_t pg0, int64_t pg1, bool
   return HS_OK;
 }
 
-int upload_page_table(hs_pool* p) {
-  const size_t n = p->host->dev_pt.size();
+// device buffer pages (req, layer) needs to cover positions [0, end): min(B, max(end, k)) slots
+int64_t dev_pages_missing(const hs_pool* p, int req, int layer, int64_t end) {
+  const hs_dev_pages& d = *p->dev;
+  if (!d.on_demand) return 0;
+  const int64_t want = std::min<int64_t>(p->cfg.buffer_slots, std::max<int64_t>(end, p->cfg.top_k));
+  const int64_t np = (want + d.page_slots - 1) / d.page_slots;
+  return std::max<int64_t>(0, np - d.npages[(int64_t)layer * p->cfg.num_requests + req]);
+}
+
+// Grow the buffer of (req, layer) by `n` pages from the free list (the caller checked they exist).
+void grow_buffer(hs_pool* p, int req, int layer, int64_t n, bool* changed) {
+  hs_dev_pages& d = *p->dev;
+  const int64_t rl = (int64_t)layer * p->cfg.num_requests + req;
+  for (int64_t i = 0; i < n; ++i) {
+    const int64_t pg = d.free_pages.back();
+    d.free_pages.pop_back();
+    d.table[rl * p->slot_pages + d.npages[rl]] = (uint64_t)(uintptr_t)(p->buf + pg * d.page_bytes);
+    ++d.npages[rl];
+    ++d.pages_in_use;
+    *changed = true;
+  }
+}
+
+// Reserve, for request `req` and layers [l0, l1), host pages [pg0, pg1) and (dev_end >= 0) device
+// slots covering positions [0, dev_end); all or nothing.
+int reserve_range(hs_pool* p, int req, int l0, int l1, int64_t pg0, int64_t pg1, int64_t dev_end, bool* changed) {
+  int64_t host_need = 0, dev_need = 0;
+  for (int l = l0; l < l1; ++l) {
+    host_need += host_pages_missing(p, req, l, pg0, pg1);
+    if (dev_end >= 0) dev_need += dev_pages_missing(p, req, l, dev_end);
+  }
+  if (dev_need > (int64_t)p->dev->free_pages.size()) return HS_ERR_ALLOC_DEV;
+  int rc = grow_free_pages(p, host_need);
+  if (rc != HS_OK) return rc;
+  for (int l = l0; l < l1; ++l) {
+    rc = reserve_pages(p, req, l, pg0, pg1, changed);  // cannot fail: the free list holds enough
+    if (rc != HS_OK) return rc;
+    if (dev_end >= 0) grow_buffer(p, req, l, dev_pages_missing(p, req, l, dev_end), changed);
+  }
+  return HS_OK;
+}
+
+// Both tables to the device, after every kernel that may read them has finished.
+int upload_tables(hs_pool* p) {
+  const hs_dev_pages& d = *p->dev;
+  std::vector<int32_t> cap(d.npages.size());
+  for (size_t i = 0; i < cap.size(); ++i)
+    cap[i] = (int32_t)std::min<int64_t>(p->cfg.buffer_slots, d.npages[i] * d.page_slots);
   if (cudaDeviceSynchronize() != cudaSuccess ||
-      cudaMemcpy(p->page_table, p->host->dev_pt.data(), n * sizeof(uint64_t), cudaMemcpyHostToDevice) != cudaSuccess) {
+      cudaMemcpy(p->page_table, p->host->dev_pt.data(), p->host->dev_pt.size() * sizeof(uint64_t),
+                 cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaMemcpy(p->slot_table, d.table.data(), d.table.size() * sizeof(uint64_t), cudaMemcpyHostToDevice) !=
+          cudaSuccess ||
+      cudaMemcpy(p->slot_cap, cap.data(), cap.size() * sizeof(int32_t), cudaMemcpyHostToDevice) != cudaSuccess) {
     cudaGetLastError();
     return HS_ERR_CUDA;
   }
   return HS_OK;
+}
+
+// A released request starts cold: empty slots, clock 1, no resolves, no errors, nothing pending.
+__global__ void k_release(int32_t* tag, uint32_t* stamp, hs_rl_state* state, uint32_t* pend_live, int R, int L, int B,
+                          int req) {
+  const size_t i0 = (size_t)blockIdx.x * blockDim.x + threadIdx.x, stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t i = i0; i < (size_t)L * B; i += stride) {
+    const size_t e = ((i / B) * R + req) * B + i % B;
+    tag[e] = -1;
+    stamp[e] = 0u;
+  }
+  for (size_t l = i0; l < (size_t)L; l += stride) {
+    hs_rl_state s;
+    s.clock = 1u;
+    s.nres = 0u;
+    s.err = 0u;
+    s.pad = 0u;
+    state[l * R + req] = s;
+    if (pend_live != nullptr) pend_live[l * R + req] = 0u;
+  }
 }
 
 struct DeviceGuard {
@@ -272,7 +389,34 @@ extern "C" int hs_pool_create(const hs_config* cfg, int cuda_device, hs_pool** o
   cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, cuda_device);
   p->rec = hs_record_bytes(cfg);
   const size_t R = cfg->num_requests, L = cfg->num_layers, B = cfg->buffer_slots;
-  const size_t rec = (size_t)p->rec;
+  // the device cache pool and its slot table (first: the host pool's bound refers to its size)
+  p->dev = new hs_dev_pages();
+  hs_dev_pages& d = *p->dev;
+  d.page_slots = slot_page_for(cfg);
+  d.page_bytes = d.page_slots * p->rec;
+  d.on_demand = cfg->device_pool_slots > 0;
+  p->slot_pages = (int)((B + d.page_slots - 1) / d.page_slots);
+  p->slot_shift = 0;
+  while ((1ll << p->slot_shift) < d.page_slots) ++p->slot_shift;
+  d.total_pages = d.on_demand ? (cfg->device_pool_slots + d.page_slots - 1) / d.page_slots
+                              : (int64_t)(L * R) * p->slot_pages;
+  d.table.assign(L * R * (size_t)p->slot_pages, 0ull);
+  d.npages.assign(L * R, 0);
+  rc = dev_alloc(&p->buf, (size_t)(d.total_pages * d.page_bytes));
+  if (rc == HS_OK) rc = dev_alloc(&p->slot_table, d.table.size());
+  if (rc == HS_OK) rc = dev_alloc(&p->slot_cap, L * R);
+  if (rc == HS_OK) {
+    if (d.on_demand) {  // every page free, page 0 handed out first
+      for (int64_t i = d.total_pages - 1; i >= 0; --i) d.free_pages.push_back(i);
+    } else {  // buffer (l, r) holds pages [(l R + r) P, (l R + r + 1) P): the flat [L][R][B] layout
+      for (size_t rl = 0; rl < L * R; ++rl) {
+        for (int i = 0; i < p->slot_pages; ++i)
+          d.table[rl * p->slot_pages + i] = (uint64_t)(uintptr_t)(p->buf + ((int64_t)rl * p->slot_pages + i) * d.page_bytes);
+        d.npages[rl] = p->slot_pages;
+      }
+      d.pages_in_use = d.total_pages;
+    }
+  }
   // host pages and their table
   p->host = new hs_host_pages();
   p->host->page_tokens = page_tokens_for(cfg);
@@ -283,7 +427,7 @@ extern "C" int hs_pool_create(const hs_config* cfg, int cuda_device, hs_pool** o
   p->max_pages = (cfg->capacity + p->host->page_tokens - 1) / p->host->page_tokens;
   p->host->host_pt.assign(R * L * (size_t)p->max_pages, nullptr);
   p->host->dev_pt.assign(R * L * (size_t)p->max_pages, 0ull);
-  rc = dev_alloc(&p->page_table, R * L * (size_t)p->max_pages);
+  if (rc == HS_OK) rc = dev_alloc(&p->page_table, R * L * (size_t)p->max_pages);
   if (rc == HS_OK && cfg->host_on_demand == 0) {  // every page of [0, capacity) now, from one slab
     const int64_t sp = p->host->shared_pages;
     rc = grow_free_pages(p, (int64_t)L * sp + (int64_t)(R * L) * (p->max_pages - sp));  // all of them
@@ -291,10 +435,7 @@ extern "C" int hs_pool_create(const hs_config* cfg, int cuda_device, hs_pool** o
     for (int r = 0; rc == HS_OK && r < (int)R; ++r)
       for (int l = 0; rc == HS_OK && l < (int)L; ++l) rc = reserve_pages(p, r, l, 0, p->max_pages, &changed);
   }
-  if (rc == HS_OK && cudaMemcpy(p->page_table, p->host->dev_pt.data(), p->host->dev_pt.size() * sizeof(uint64_t),
-                                cudaMemcpyHostToDevice) != cudaSuccess)
-    rc = HS_ERR_CUDA;
-  if (rc == HS_OK) rc = dev_alloc(&p->buf, L * R * B * rec);
+  if (rc == HS_OK) rc = upload_tables(p);
   if (rc == HS_OK) rc = dev_alloc(&p->tag, L * R * B);
   if (rc == HS_OK) rc = dev_alloc(&p->stamp, L * R * B);
   if (rc == HS_OK) rc = dev_alloc(&p->state, L * R);
@@ -348,9 +489,9 @@ extern "C" int hs_prefill_write(hs_pool* pool, int req, int layer, int64_t pos0,
   hs_host_pages& h = *pool->host;
   const int64_t pt = h.page_tokens, rec = pool->rec;
   bool changed = false;
-  int rc = reserve_pages(pool, req, layer, pos0 / pt, (pos0 + n + pt - 1) / pt, &changed);
+  int rc = reserve_range(pool, req, layer, layer + 1, pos0 / pt, (pos0 + n + pt - 1) / pt, -1, &changed);
   if (rc != HS_OK) return rc;
-  if (changed && (rc = upload_page_table(pool)) != HS_OK) return rc;
+  if (changed && (rc = upload_tables(pool)) != HS_OK) return rc;
   const uint8_t* s = (const uint8_t*)src;
   cudaStream_t st = (cudaStream_t)stream;
   for (int64_t a = pos0; a < pos0 + n;) {  // one copy per page
@@ -371,10 +512,8 @@ extern "C" int hs_reserve(hs_pool* pool, int req, int layer, int64_t end) {
   DeviceGuard guard(pool->device);
   const int64_t pg1 = (end + pool->host->page_tokens - 1) / pool->host->page_tokens;
   bool changed = false;
-  int rc = HS_OK;
-  for (int l = layer < 0 ? 0 : layer; rc == HS_OK && l < (layer < 0 ? c.num_layers : layer + 1); ++l)
-    rc = reserve_pages(pool, req, l, 0, pg1, &changed);
-  if (rc == HS_OK && changed) rc = upload_page_table(pool);
+  int rc = reserve_range(pool, req, layer < 0 ? 0 : layer, layer < 0 ? c.num_layers : layer + 1, 0, pg1, end, &changed);
+  if (rc == HS_OK && changed) rc = upload_tables(pool);
   return rc;
 }
 
@@ -396,7 +535,36 @@ extern "C" int hs_release(hs_pool* pool, int req) {
       changed = true;
     }
   }
-  return changed ? upload_page_table(pool) : HS_OK;
+  hs_dev_pages& d = *pool->dev;
+  const int R = pool->cfg.num_requests;
+  if (d.on_demand) {
+    for (int l = 0; l < L; ++l) {
+      const int64_t rl = (int64_t)l * R + req;
+      for (int i = d.npages[rl] - 1; i >= 0; --i) {
+        uint64_t& e = d.table[rl * pool->slot_pages + i];
+        d.free_pages.push_back((int64_t)(((uint8_t*)(uintptr_t)e - pool->buf) / d.page_bytes));
+        e = 0ull;
+        --d.pages_in_use;
+        changed = true;
+      }
+      d.npages[rl] = 0;
+    }
+  }
+  const int B = pool->cfg.buffer_slots;
+  k_release<<<std::min(pool->num_sms * 4, (L * B + 255) / 256), 256>>>(pool->tag, pool->stamp, pool->state,
+                                                                       pool->pend_live, R, L, B, req);
+  if (cudaGetLastError() != cudaSuccess) return HS_ERR_CUDA;
+  if (changed) return upload_tables(pool);  // synchronises after the reset
+  return cudaDeviceSynchronize() == cudaSuccess ? HS_OK : HS_ERR_CUDA;
+}
+
+extern "C" int hs_device_usage(hs_pool* pool, int64_t* pages_in_use, int64_t* pages_free, int64_t* page_slots) {
+  if (pool == nullptr) return HS_ERR_ARG;
+  const hs_dev_pages& d = *pool->dev;
+  if (pages_in_use) *pages_in_use = d.pages_in_use;
+  if (pages_free) *pages_free = d.on_demand ? (int64_t)d.free_pages.size() : 0;
+  if (page_slots) *page_slots = d.page_slots;
+  return HS_OK;
 }
 
 extern "C" int hs_host_usage(hs_pool* pool, int64_t* pages_in_use, int64_t* pages_free, int64_t* bytes_pinned) {
@@ -540,10 +708,21 @@ extern "C" int hs_read_buffer(hs_pool* pool, int req, int layer, void* dst) {
   if (pool == nullptr || dst == nullptr) return HS_ERR_ARG;
   if (req < 0 || req >= pool->cfg.num_requests || layer < 0 || layer >= pool->cfg.num_layers) return HS_ERR_ARG;
   DeviceGuard guard(pool->device);
-  const size_t R = pool->cfg.num_requests, B = pool->cfg.buffer_slots, rec = pool->rec;
+  const int64_t R = pool->cfg.num_requests, B = pool->cfg.buffer_slots, rec = pool->rec;
   if (cudaDeviceSynchronize() != cudaSuccess) return HS_ERR_CUDA;
-  const uint8_t* src = pool->buf + ((size_t)layer * R + req) * B * rec;
-  return cudaMemcpy(dst, src, B * rec, cudaMemcpyDeviceToHost) == cudaSuccess ? HS_OK : HS_ERR_CUDA;
+  const hs_dev_pages& d = *pool->dev;
+  const int64_t rl = (int64_t)layer * R + req;
+  for (int i = 0; i < pool->slot_pages; ++i) {  // page by page; pages the buffer lacks read as zeros
+    const int64_t j0 = i * d.page_slots, n = std::min<int64_t>(d.page_slots, B - j0);
+    uint8_t* out = (uint8_t*)dst + j0 * rec;
+    if (i < d.npages[rl]) {
+      const void* src = (const void*)(uintptr_t)d.table[rl * pool->slot_pages + i];
+      if (cudaMemcpy(out, src, (size_t)(n * rec), cudaMemcpyDeviceToHost) != cudaSuccess) return HS_ERR_CUDA;
+    } else {
+      memset(out, 0, (size_t)(n * rec));
+    }
+  }
+  return HS_OK;
 }
 
 extern "C" int hs_read_history(hs_pool* pool, int req, int layer, int64_t pos0, int64_t n, void* dst) {

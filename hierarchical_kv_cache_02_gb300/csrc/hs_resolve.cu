@@ -11,6 +11,8 @@
 //   (5) publish the page-table update and the dense vector of physical slots (locs).
 // APPEND is step (5) of the decode flow in §3: the new token's record is written through to
 // the host history and installed in the hot buffer.
+// A buffer grown on demand (§8) holds slots [0, cap) only: both kernels probe, evict and install
+// there alone, and refuse a (request, layer) with fewer than k slots (HS_DEVERR_SLOTS).
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -31,9 +33,10 @@ struct ResolveArgs {
   uint32_t* step_log;   // [log_steps][L][R] or null
   const uint64_t* pt;   // host page table [R][L][max_pages]
   uint32_t* err_global; // pool-wide error word (errors found outside the deciding CTA)
-  uint8_t* buf;         // layer slice [R][B][rec]
+  const uint64_t* spt;  // layer slice [R][spp] of the slot table: device address of each buffer page
+  const int32_t* scap;  // layer slice [R]: slots each buffer holds
   int64_t C, P0, max_pages, rec;
-  int page_shift;
+  int page_shift, sshift, spp;
   uint64_t seed;
   hs_pending* pend;      // fetch-in-attention mode: layer slice [R][k], else null
   uint32_t* pend_live;   // layer slice [R]
@@ -87,8 +90,8 @@ __device__ __forceinline__ void cluster_sync_all() {
 // Copy misses [q0, q1) host -> slots.  A warp moves one chunk of 32 x NV lane-contiguous 16-byte
 // vectors of one record per item (coalesced 512-byte rows); ITEMS items are loaded before any store.
 template <int NV>
-__device__ void fetch_misses(const ResolveArgs& a, int r, int q0, int q1, const uint64_t* s_src,
-                             const int32_t* victims) {
+__device__ void fetch_misses(const ResolveArgs& a, int q0, int q1, const uint64_t* s_src, const int32_t* victims,
+                             const uint64_t* slots) {
   constexpr int ITEMS = NV >= 8 ? 1 : 2;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int vpr = (int)(a.rec / 16);            // vectors per record
@@ -107,7 +110,7 @@ __device__ void fetch_misses(const ResolveArgs& a, int r, int q0, int q1, const 
         const int q = q0 + w / cpr, c = w % cpr;
         src[it] = (const uint4*)s_src[q - q0];
         if (src[it] == nullptr) continue;  // page not reserved (flagged): the slot keeps its contents
-        dst[it] = (uint4*)(a.buf + ((int64_t)r * a.B + victims[q]) * a.rec);
+        dst[it] = (uint4*)hs_slot_addr(slots, a.sshift, a.rec, victims[q]);
         vbase[it] = c * 32 * NV + lane;
 #pragma unroll
         for (int u = 0; u < NV; ++u) {
@@ -210,7 +213,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
   const int r = a.r0 + (int)(blockIdx.x / a.cs);
   const int crank = blockIdx.x % a.cs;  // rank inside the cluster of this request
   const int tid = threadIdx.x;
-  const int k = a.k, B = a.B;
+  const int k = a.k, BK = a.B;              // BK: the configured B (the random key's counter)
+  const int B = min(BK, a.scap[r]);         // slots this buffer holds: all work is over [0, B)
   const int ht_size = 1 << a.ht_bits;
   int32_t* ht_key = (int32_t*)smem;                 // [ht_size]
   int32_t* ht_val = ht_key + ht_size;               // [ht_size] smallest top-k index of the key
@@ -228,9 +232,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
 
   const int32_t* topk = a.topk + (int64_t)(r - a.r0) * k;
   int32_t* locs = a.locs + (int64_t)(r - a.r0) * k;
-  int32_t* tag = a.tag + (int64_t)r * B;
-  uint32_t* stamp = a.stamp + (int64_t)r * B;
+  int32_t* tag = a.tag + (int64_t)r * BK;
+  uint32_t* stamp = a.stamp + (int64_t)r * BK;
   const hs_rl_state st = a.state[r];
+  const uint64_t* slots_g = a.spt + (int64_t)r * a.spp;
+  if (B < k) {
+    // too few slots for a step (a buffer not grown): nothing changes; the locations are -1 and the
+    // fused append is skipped too (same decision in every CTA of the cluster: no barrier is reached)
+    for (int i = crank * kThreads + tid; i < k; i += a.cs * kThreads) locs[i] = -1;
+    if (crank == 0 && tid == 0) {
+      uint32_t e = (uint32_t)HS_DEVERR_SLOTS;
+      if (a.app_pos != nullptr) {
+        const int64_t p = a.app_pos[r - a.r0];
+        if (p < a.P0 || p < 0 || p >= a.C ||
+            hs_page_addr(a.pt, a.max_pages, a.page_shift, a.rec, a.L, r, a.layer, p) == nullptr)
+          e |= (uint32_t)HS_DEVERR_APPEND;
+      }
+      a.state[r].err = st.err | e;
+    }
+    return;
+  }
+  __shared__ uint64_t s_slots[kMaxSlotPages];  // this buffer's page row (first used after the decision)
+  for (int i = tid; i < a.spp; i += kThreads) s_slots[i] = slots_g[i];
   __shared__ int s_app_slot;
   __shared__ unsigned long long s_best[kWarps];
   __shared__ int s_found[kWarps];
@@ -246,11 +269,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
   // finished first (they target slots this decision may reuse); the cluster barrier below orders
   // them before this resolve rewrites the pending list
   if (a.pend != nullptr && a.pend_live[r] != 0u)
-    hs_copy_pending(a.pend + (int64_t)r * k, k, a.rec, a.buf + (int64_t)r * B * a.rec, crank, a.cs);
+    hs_copy_pending(a.pend + (int64_t)r * k, k, a.rec, slots_g, a.sshift, crank, a.cs);
 
   // ---------------- phase A: every CTA of the cluster computes the whole decision ----------------
   // fused write-through append (hs_append_resolve): the new position takes the slot that already
-  // holds it, else the slot with the smallest eviction key over all B slots; stamp = clock, clock
+  // holds it, else the slot with the smallest eviction key over the buffer's slots; stamp = clock, clock
   // += 1; the resolve below then sees that state
   int app_slot = -1;
   int64_t app_p = -1;
@@ -268,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
       for (int j = tid; j < B; j += kThreads) {
         const int32_t t = tag[j];
         if (t == (int32_t)app_p) found = min(found, j);
-        const uint32_t key = hs_evict_key(a.policy, t, stamp[j], a.seed, st.nres, a.R, r, a.L, a.layer, B, j);
+        const uint32_t key = hs_evict_key(a.policy, t, stamp[j], a.seed, st.nres, a.R, r, a.L, a.layer, BK, j);
         const unsigned long long kj = ((unsigned long long)key << 32) | (unsigned)j;
         best = kj < best ? kj : best;
       }
@@ -360,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
       }
     }
     flag[j] = f;
-    key32[j] = hs_evict_key(a.policy, t, stj, a.seed, st.nres, a.R, r, a.L, a.layer, B, j);
+    key32[j] = hs_evict_key(a.policy, t, stj, a.seed, st.nres, a.R, r, a.L, a.layer, BK, j);
   }
   __syncthreads();
 
@@ -485,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
       const bool evicted = (flag[app_slot] & 2u) != 0u ||
                            (a.policy == HS_POLICY_SWAP_VANILLA && (flag[app_slot] & 1u) == 0u);
       const bool restamped = (flag[app_slot] & 1u) != 0u && a.policy != HS_POLICY_FIFO;
-      uint4* db = (uint4*)(a.buf + ((int64_t)r * B + app_slot) * a.rec);
+      uint4* db = (uint4*)hs_slot_addr(s_slots, a.sshift, a.rec, app_slot);
       const int nv = (int)(a.rec / 16);
       for (int x = tid; x < nv; x += kThreads) {
         const uint4 v = src[x];
@@ -508,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
         s_src[q - q0] = (uint64_t)(uintptr_t)src;
       }
       __syncthreads();
-      fetch_misses<NV>(a, r, q0, q1, s_src, victims);
+      fetch_misses<NV>(a, q0, q1, s_src, victims, s_slots);
     }
   }
 
@@ -539,9 +562,10 @@ struct AppendArgs {
   unsigned long long* counters;
   const uint64_t* pt;    // host page table [R][L][max_pages]
   uint32_t* err_global;
-  uint8_t* buf;
+  const uint64_t* spt;   // layer slice [R][spp] of the slot table
+  const int32_t* scap;   // layer slice [R]: slots each buffer holds
   int64_t C, P0, max_pages, rec;
-  int page_shift;
+  int page_shift, sshift, spp;
   uint64_t seed;
   const hs_pending* pend;  // fetch-in-attention mode: layer slice [R][k], else null
   uint32_t* pend_live;
@@ -555,7 +579,7 @@ __global__ void __launch_bounds__(kAppendThreads) k_append(AppendArgs a) {
   const int r = blockIdx.x, tid = threadIdx.x;
   if (a.pend != nullptr && a.pend_live[r] != 0u) {
     // finish the copies a previous resolve left pending before this append may overwrite a slot
-    hs_copy_pending(a.pend + (int64_t)r * a.k, a.k, a.rec, a.buf + (int64_t)r * a.B * a.rec, 0, 1);
+    hs_copy_pending(a.pend + (int64_t)r * a.k, a.k, a.rec, a.spt + (int64_t)r * a.spp, a.sshift, 0, 1);
     __syncthreads();
     if (tid == 0) a.pend_live[r] = 0u;
   }
@@ -568,11 +592,16 @@ __global__ void __launch_bounds__(kAppendThreads) k_append(AppendArgs a) {
     if (tid == 0) a.state[r].err = st.err | (uint32_t)HS_DEVERR_APPEND;
     return;
   }
+  const int B = min(a.B, a.scap[r]);  // slots this buffer holds
+  if (B < a.k) {                      // too few for a step: nothing changes
+    if (tid == 0) a.state[r].err = st.err | (uint32_t)HS_DEVERR_SLOTS;
+    return;
+  }
   int32_t* tag = a.tag + (int64_t)r * a.B;
   uint32_t* stamp = a.stamp + (int64_t)r * a.B;
   int found = 0x7fffffff;
   unsigned long long best = ~0ull;
-  for (int j = tid; j < a.B; j += kAppendThreads) {
+  for (int j = tid; j < B; j += kAppendThreads) {
     const int32_t t = tag[j];
     if (t == (int32_t)p) found = min(found, j);
     const uint32_t key = hs_evict_key(a.policy, t, stamp[j], a.seed, st.nres, a.R, r, a.L, a.layer, a.B, j);
@@ -605,7 +634,7 @@ __global__ void __launch_bounds__(kAppendThreads) k_append(AppendArgs a) {
   __syncthreads();
   const int slot = s_slot;
   const uint4* src = (const uint4*)(a.rec_in + (int64_t)r * a.rec);
-  uint4* db = (uint4*)(a.buf + ((int64_t)r * a.B + slot) * a.rec);
+  uint4* db = (uint4*)hs_slot_addr(a.spt + (int64_t)r * a.spp, a.sshift, a.rec, slot);
   const int nv = (int)(a.rec / 16);
   for (int x = tid; x < nv; x += kAppendThreads) {
     const uint4 v = src[x];
@@ -711,7 +740,10 @@ int hs_launch_resolve(hs_pool* p, int layer, int r0, int nreq, const int64_t* d_
   a.step_log = c.log_steps > 0 ? p->step_log : nullptr;
   a.pt = p->page_table;
   a.err_global = p->err_global;
-  a.buf = p->buf + (int64_t)layer * R * B * p->rec;
+  a.spt = p->slot_table + (int64_t)layer * R * p->slot_pages;
+  a.scap = p->slot_cap + (int64_t)layer * R;
+  a.sshift = p->slot_shift;
+  a.spp = p->slot_pages;
   a.C = c.capacity;
   a.P0 = c.shared_prefix;
   a.max_pages = p->max_pages;
@@ -766,7 +798,10 @@ int hs_launch_append(hs_pool* p, int layer, const int64_t* d_pos, const void* d_
   a.counters = p->counters + (int64_t)layer * R * 4;
   a.pt = p->page_table;
   a.err_global = p->err_global;
-  a.buf = p->buf + (int64_t)layer * R * B * p->rec;
+  a.spt = p->slot_table + (int64_t)layer * R * p->slot_pages;
+  a.scap = p->slot_cap + (int64_t)layer * R;
+  a.sshift = p->slot_shift;
+  a.spp = p->slot_pages;
   a.C = c.capacity;
   a.P0 = c.shared_prefix;
   a.max_pages = p->max_pages;

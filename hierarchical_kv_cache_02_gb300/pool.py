@@ -46,6 +46,9 @@ class HsConfig:
     fetch_in_attention: int = 0
     host_page_tokens: int = 0
     host_on_demand: int = 0
+    buffer_page_slots: int = 0
+    device_pool_slots: int = 0
+    host_to_device_ratio: float = 0.0
 
     @property
     def record_bytes(self) -> int:
@@ -64,7 +67,8 @@ class HsConfig:
     def to_c(self) -> _lib.hs_config:
         c = _lib.hs_config()
         for f in fields(self):
-            setattr(c, f.name, int(getattr(self, f.name)))
+            v = getattr(self, f.name)
+            setattr(c, f.name, float(v) if f.name == "host_to_device_ratio" else int(v))
         return c
 
 
@@ -270,12 +274,20 @@ class HsPool:
 
     # -- memory layer: paged host pool ------------------------------------------------
     def reserve(self, req: int, end: int, layer: int = -1):
-        """Reserve the host pages of (req, layer) covering positions [0, end); layer -1: all layers."""
+        """Reserve the host pages of (req, layer) covering positions [0, end) and, with a device cache
+        pool, grow its buffer to min(B, max(end, k)) slots; layer -1: all layers.  All or nothing."""
         _check("hs_reserve", self.lib.hs_reserve(self._h, int(req), int(layer), int(end)))
 
     def release(self, req: int):
-        """Return the private host pages of request `req` (all layers) to the pool's free list."""
+        """End request `req`: its private host pages (and device buffer pages, with a device cache
+        pool) return to the free lists and its buffers are emptied; its counters stay."""
         _check("hs_release", self.lib.hs_release(self._h, int(req)))
+
+    def device_usage(self) -> dict:
+        used, free, page = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+        _check("hs_device_usage", self.lib.hs_device_usage(self._h, ctypes.byref(used), ctypes.byref(free),
+                                                           ctypes.byref(page)))
+        return {"pages_in_use": used.value, "pages_free": free.value, "page_slots": page.value}
 
     def host_usage(self) -> dict:
         used, free, pinned = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()

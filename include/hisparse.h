@@ -71,8 +71,11 @@ enum hs_device_error {
                              page not reserved (hs_reserve) */
   HS_DEVERR_LOC = 16,     /* an attention slot index outside [0, rows) */
   HS_DEVERR_TIMEOUT = 32, /* a bounded wait inside a kernel gave up */
-  HS_DEVERR_PAGE = 64     /* a miss fetch read a position whose host page is not reserved (the
+  HS_DEVERR_PAGE = 64,    /* a miss fetch read a position whose host page is not reserved (the
                              slot keeps its old contents) */
+  HS_DEVERR_SLOTS = 128   /* a resolve or append on a (request, layer) whose device buffer holds
+                             fewer than top_k slots (device_pool_slots > 0 and not reserved):
+                             the call changed nothing for it and its locations are -1 */
 };
 
 typedef struct {
@@ -110,6 +113,21 @@ typedef struct {
                                  1: pages are reserved on demand: by hs_prefill_write for the
                                  positions it writes and by hs_reserve ahead of appends; a
                                  request's private pages return to the pool with hs_release. */
+  int32_t buffer_page_slots;  /* slots per device buffer page: 0 = automatic (the smallest power of
+                                 two >= 16 that cuts B into at most 64 pages); else a power of two
+                                 with ceil(B / buffer_page_slots) <= 64 */
+  int64_t device_pool_slots;  /* summary §8, the coordinator allocates and grows the per-request,
+                                 per-layer device cache on demand.  0: every (request, layer) buffer
+                                 holds all B slots from creation.  > 0: the device cache pool holds
+                                 this many slots (rounded up to whole pages); a buffer holds only
+                                 the pages hs_reserve gave it -- min(B, max(end, top_k)) slots
+                                 rounded up to a page -- and
+                                 resolve and append use its slots [0, that count) alone.  With the
+                                 growth kept ahead of the positions a request uses, every result is
+                                 identical to the full buffer's. */
+  double host_to_device_ratio; /* > 0: the pinned host history may hold at most this many times the
+                                  device cache pool's bytes; reservations beyond fail with
+                                  HS_ERR_ALLOC_HOST.  0: no bound. */
 } hs_config;
 
 /* Record size in bytes for a configuration (MLA: 2*head_dim_qk; GQA: 2*kv_heads*(qk+v)). */
@@ -121,9 +139,12 @@ int64_t hs_record_bytes(const hs_config* cfg);
  *     pinned slabs.  A device page table [R][L][ceil(capacity / page)] maps every (request, layer,
  *     position) to its page.  The pages of [0, shared_prefix) are one copy per layer, mapped into
  *     every request's table.
- *   - Hot buffer [L][R][B][rec] in HBM, tags (-1 = empty), stamps (0 = empty), per-(request,
- *     layer) clock (starts at 1), counters and attention workspace.  All slots start empty.
- * With host_on_demand = 0 every page is reserved here; else none is.  Synchronous, not
+ *   - Hot buffers in HBM: one device cache pool of pages of buffer_page_slots slots x rec bytes; a
+ *     device slot table [L][R][ceil(B / page)] maps each (layer, request, slot) to its page.  Tags
+ *     [L][R][B] (-1 = empty), stamps (0 = empty), per-(request, layer) clock (starts at 1),
+ *     counters and attention workspace.  All slots start empty.
+ * With host_on_demand = 0 every host page is reserved here; else none is.  With
+ * device_pool_slots = 0 every buffer gets all its pages here; else none does.  Synchronous, not
  * capturable.  Errors: HS_ERR_CONFIG, HS_ERR_ALLOC_HOST, HS_ERR_ALLOC_DEV, HS_ERR_CUDA.
  * Environment HS_FAULT=alloc_host|alloc_dev makes the named allocation fail (for tests).
  */
@@ -141,7 +162,8 @@ int hs_pool_reset(hs_pool* pool, void* stream);
  * Positions below shared_prefix go to the shared history whatever `req` is.  Reserves the pages
  * it writes (synchronously), then enqueues the copy on `stream`; the caller keeps `src` alive
  * until the stream reaches this point.  Writes only the host pool; the hot buffer is filled on
- * demand by hs_resolve.  Errors: HS_ERR_ARG, HS_ERR_ALLOC_HOST, HS_ERR_CUDA.
+ * demand by hs_resolve (a device buffer grown on demand grows only by hs_reserve).
+ * Errors: HS_ERR_ARG, HS_ERR_ALLOC_HOST, HS_ERR_CUDA.
  */
 int hs_prefill_write(hs_pool* pool, int req, int layer, int64_t pos0, int64_t n, const void* src,
                      void* stream);
@@ -264,7 +286,8 @@ int hs_stats(hs_pool* pool, hs_totals* totals, uint64_t* h_counters, uint32_t* h
  */
 int hs_read_state(hs_pool* pool, int layer, int32_t* h_tag, uint32_t* h_stamp, uint32_t* h_clock);
 
-/* Inspection: copy the hot buffer of (req, layer), [B][rec] bytes, to host memory `dst`. */
+/* Inspection: copy the hot buffer of (req, layer), [B][rec] bytes, to host memory `dst`; slots
+ * the buffer does not hold read as zeros. */
 int hs_read_buffer(hs_pool* pool, int req, int layer, void* dst);
 
 /* Inspection: copy n records of the host history of (req, layer) from position pos0 to `dst`;
@@ -272,23 +295,31 @@ int hs_read_buffer(hs_pool* pool, int req, int layer, void* dst);
 int hs_read_history(hs_pool* pool, int req, int layer, int64_t pos0, int64_t n, void* dst);
 
 /*
- * Memory layer (summary §8: paged host pool, grown on demand): reserve the host pages of
- * (req, layer) that cover positions [0, end) -- layer = -1: every layer -- so that appends up to
- * `end` have somewhere to go.  Pages of the shared prefix are reserved once per layer.
- * Synchronous (it updates the device page table); call it outside captured graphs, before the
- * decode steps that append there.  Errors: HS_ERR_ARG, HS_ERR_ALLOC_HOST, HS_ERR_CUDA.
+ * Memory layer (summary §8: paged host pool and device cache pool, grown on demand): reserve the
+ * host pages of (req, layer) that cover positions [0, end) -- layer = -1: every layer -- so that
+ * appends up to `end` have somewhere to go, and (device_pool_slots > 0) grow its device buffer to
+ * min(B, max(end, top_k)) slots rounded up to a page.  Pages of the shared prefix are reserved
+ * once per layer.  Nothing is reserved when the call fails.  Synchronous (it updates the device
+ * tables); call it outside captured graphs, before the decode steps that use those positions.
+ * Errors: HS_ERR_ARG, HS_ERR_ALLOC_HOST, HS_ERR_ALLOC_DEV (device cache pool exhausted), HS_ERR_CUDA.
  */
 int hs_reserve(hs_pool* pool, int req, int layer, int64_t end);
 
 /*
- * Return the private host pages of request `req` (every layer) to the pool's free list, for
- * reuse by later reservations; the shared prefix stays.  The request's history reads as zeros
- * afterwards.  Synchronises the device first.  Errors: HS_ERR_ARG, HS_ERR_CUDA.
+ * End request `req` (every layer): its private host pages, and with device_pool_slots > 0 its
+ * device buffer pages, return to the free lists for reuse by later reservations; the shared prefix
+ * stays.  Its buffers are emptied (tags -1, stamps 0, clock 1, resolve count 0, error bits 0, no
+ * copies pending), so a new request in this index starts cold; its counters are kept.  The
+ * request's history reads as zeros afterwards.  Synchronises the device first.
+ * Errors: HS_ERR_ARG, HS_ERR_CUDA.
  */
 int hs_release(hs_pool* pool, int req);
 
 /* Host memory of the pool: pages mapped in some table, pages on the free list, pinned bytes held. */
 int hs_host_usage(hs_pool* pool, int64_t* pages_in_use, int64_t* pages_free, int64_t* bytes_pinned);
+
+/* Device cache pool: pages held by some buffer, pages free, slots per page. */
+int hs_device_usage(hs_pool* pool, int64_t* pages_in_use, int64_t* pages_free, int64_t* page_slots);
 
 #ifdef __cplusplus
 }
