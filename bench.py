@@ -323,8 +323,8 @@ def run_ours(args, w, world, rank, local):
     # the headline pass replays the K timed steps as one captured CUDA graph (single stream)
     use_graph = not args.no_graph and G == 1 and M == 1
 
-    def run_steps(timed_events):
-        """Cold start, W untimed warm-up steps, then K timed steps; returns seconds and pool stats."""
+    def warm_up():
+        """Cold start, then the W untimed warm-up steps."""
         pool.reset()
         for t in range(W):
             if M > 1:
@@ -339,13 +339,21 @@ def run_ours(args, w, world, rank, local):
                 step(t)
         torch.cuda.synchronize()
         pool.stats(reset=True)
+
+    def run_steps(timed_events):
+        """Cold start, W untimed warm-up steps, then K timed steps; returns seconds and pool stats."""
         graph = None
         if use_graph and not timed_events:
-            graph = torch.cuda.CUDAGraph()  # capture only: nothing runs until the replay
+            # capture the timed steps after the warm-up and replay them once untimed (a graph's first
+            # launch also uploads it); the timed replay then starts over from the same state
+            warm_up()
+            graph = torch.cuda.CUDAGraph()
             with torch.cuda.graph(graph):
                 for i in range(K):
                     step(W + i)
+            graph.replay()
             torch.cuda.synchronize()
+        warm_up()
         start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier(world)
         torch.cuda.synchronize()
