@@ -470,8 +470,10 @@ def run_ours(args, w, world, rank, local):
 
 
 def run_e2e(pool, wl, W, K, world, locs, outs, scale):
-    """Same steps after a cold reset, with this step's top-k, queries and new records copied
-    from pinned host memory and the attention outputs copied back inside the timed region."""
+    """Same steps after a cold reset, with every step's top-k, queries and new records copied from
+    pinned host memory and all its attention outputs copied back, inside the timed region.  As a
+    serving loop would, a copy stream moves step t+1's inputs in and step t's outputs out while
+    step t computes (inputs and outputs double-buffered)."""
     import torch
 
     w = wl.w
@@ -482,35 +484,63 @@ def run_e2e(pool, wl, W, K, world, locs, outs, scale):
     h_app = wl.app.cpu().pin_memory()
     h_pos = wl.pos.cpu().pin_memory()
     h_out = torch.empty((S, L, R, w["Hq"], w["Dv"]), dtype=torch.float32).pin_memory()
-    d_topk = torch.empty((L, R, k), dtype=torch.int32, device=wl.device)
-    d_q = torch.empty((L, R, w["Hq"], w["Dqk"]), dtype=torch.bfloat16, device=wl.device)
-    d_app = torch.empty((L, R, wl.cfg.record_elems), dtype=torch.bfloat16, device=wl.device)
-    d_pos = torch.empty((R,), dtype=torch.int64, device=wl.device)
+    dev = wl.device
+    d_topk = [torch.empty((L, R, k), dtype=torch.int32, device=dev) for _ in range(2)]
+    d_q = [torch.empty((L, R, w["Hq"], w["Dqk"]), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    d_app = [torch.empty((L, R, wl.cfg.record_elems), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    d_pos = [torch.empty((R,), dtype=torch.int64, device=dev) for _ in range(2)]
+    d_out = [torch.empty((L, R, w["Hq"], w["Dv"]), dtype=torch.float32, device=dev) for _ in range(2)]
     stream = torch.cuda.current_stream()
+    copy = torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]    # inputs of the buffer's step have landed
+    ev_done = [torch.cuda.Event() for _ in range(2)]  # the buffer's step has computed
+    ev_out = [torch.cuda.Event() for _ in range(2)]   # its outputs are back on the host
+    for e in ev_done + ev_out:
+        e.record(stream)
 
-    def step(t):
-        d_topk.copy_(h_topk[t], non_blocking=True)
-        d_q.copy_(h_q[t], non_blocking=True)
-        d_app.copy_(h_app[t], non_blocking=True)
-        d_pos.copy_(h_pos[t], non_blocking=True)
+    def copy_in(t):
+        b = t % 2
+        copy.wait_event(ev_done[b])  # the step that used these buffers two steps ago is done
+        with torch.cuda.stream(copy):
+            d_topk[b].copy_(h_topk[t], non_blocking=True)
+            d_q[b].copy_(h_q[t], non_blocking=True)
+            d_app[b].copy_(h_app[t], non_blocking=True)
+            d_pos[b].copy_(h_pos[t], non_blocking=True)
+            ev_in[b].record(copy)
+
+    def compute_and_copy_out(t):
+        b = t % 2
+        stream.wait_event(ev_in[b])
+        stream.wait_event(ev_out[b])  # outputs of two steps ago have left these buffers
         for l in range(L):
             if wl.appends:
-                pool.append_resolve(l, d_pos, d_app[l], d_topk[l], locs[l])
+                pool.append_resolve(l, d_pos[b], d_app[b][l], d_topk[b][l], locs[l])
             else:
-                pool.resolve(l, d_topk[l], locs[l])
-            pool.sparse_attn(l, d_q[l], locs[l], outs[l], scale=scale)
-            h_out[t, l].copy_(outs[l], non_blocking=True)
+                pool.resolve(l, d_topk[b][l], locs[l])
+            pool.sparse_attn(l, d_q[b][l], locs[l], d_out[b][l], scale=scale)
+        ev_done[b].record(stream)
+        copy.wait_event(ev_done[b])
+        with torch.cuda.stream(copy):
+            h_out[t].copy_(d_out[b], non_blocking=True)
+            ev_out[b].record(copy)
+
+    def run(t0, t1):
+        copy_in(t0)
+        for t in range(t0, t1):
+            if t + 1 < t1:
+                copy_in(t + 1)
+            compute_and_copy_out(t)
+        stream.wait_stream(copy)
 
     pool.reset()
-    for t in range(W):
-        step(t)
+    run(0, W)
     torch.cuda.synchronize()
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
     start.record(stream)
-    for i in range(K):
-        step(W + i)
+    copy.wait_stream(stream)
+    run(W, S)
     stop.record(stream)
     torch.cuda.synchronize()
     barrier(world)

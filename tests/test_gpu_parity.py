@@ -280,6 +280,44 @@ def test_small_k_and_b_equal_k(fetch):
         run_and_compare(sc)
 
 
+@pytest.mark.parametrize("policy", [0, 3])
+def test_repeats_of_resident_missing_and_appended_positions(policy):
+    """A repeated position counts at its first occurrence only, whether the position is resident (a
+    hit), missing, or the token the fused append has just written."""
+    cfg = _gqa(2, 1, 600 + 8, 64, 128, policy=policy, kvh=2)
+    sc = Scenario(cfg, ctx0=600, steps=5, appends=True, seed=21)
+    tr = sc.trace.copy()
+    prev = set(tr[1, 0, 0].tolist())                   # resident after step 1 (B = 128 >= 2 k)
+    e = next(i for i in range(7) if int(tr[2, 0, 0, i]) in prev)
+    tr[2, 0, 0, 7] = tr[2, 0, 0, e]                    # a resident position, repeated
+    seen = set(tr[:3, 0, 1].ravel().tolist())
+    fresh = next(p for p in range(600) if p not in seen)
+    tr[2, 0, 1, 10] = fresh                            # missing, and repeated
+    tr[2, 0, 1, 11] = fresh
+    tr[3, 0, 0, 1] = 600 + 3                           # the token appended this step, twice
+    tr[3, 0, 0, 2] = 600 + 3
+    sc.trace = tr
+    pool = HsPool(cfg)
+    prefill(pool, sc)
+    orc = OracleRun(sc)
+    for t in range(sc.steps):
+        res = gpu_step(pool, sc, t, fused=True)
+        ref = orc.step(t)
+        for r in range(2):
+            assert np.array_equal(res[0][0][r], ref[(r, 0)][1]), (t, r)
+            assert_attn_close(res[0][1][r], orc.attention(t, r, 0), (t, r))
+    tag, stamp, clock = pool.read_state(0)
+    for r in range(2):
+        otag, ostamp = orc.caches[(r, 0)].slots()
+        assert np.array_equal(tag[r], otag) and np.array_equal(stamp[r], ostamp)
+    st = pool.stats()
+    assert (st["errors"][:, 0] == DEVERR_DUP).all()
+    assert [orc.caches[(r, 0)].counters()["err"] for r in range(2)] == [DEVERR_DUP, DEVERR_DUP]
+    assert np.array_equal(st["per_rl"][:, 0, :3], np.array([[orc.caches[(r, 0)].counters()[x] for x in
+                                                             ("hits", "misses", "appends")] for r in range(2)]))
+    pool.close()
+
+
 def test_padding_duplicates_and_out_of_range():
     """Invalid entries are skipped like padding, flagged, and attention ignores them."""
     cfg = _gqa(2, 1, 400, 16, 32, kvh=2)
