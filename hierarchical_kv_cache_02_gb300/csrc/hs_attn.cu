@@ -5,14 +5,14 @@
 //   * k_attn_gqa: GQA records, one CTA per (request, KV head); bulk-copy producers and consumers
 //     on mma.sync in a transposed form (tokens on the MMA's row side);
 //   * k_attn_mla_umma: shared-latent records with 64 query heads on tcgen05 tensor cores, the
-//     accumulators in tensor memory; split partials merged by k_combine;
+//     accumulators in tensor memory; split partials merged by k_combine_wide;
 //   * k_attn_cc: CUDA-core fallback for other shared-latent head counts (a producer warp gathers
 //     whole records with cp.async.bulk into a 3-stage ring; consumers reduce 32 logits per lane
 //     with a transposed butterfly and keep an online softmax in base 2).
 // In every kernel a split is a fixed range of top-k entries and all reductions run in a fixed
 // order, so the result depends only on the top-k order, never on which slot holds a record:
 // cold, warm and fully-resident runs are bit-identical.  Partials are combined in split order
-// by the last CTA to finish (atomic ticket, no waiting) or by k_combine.
+// by the last CTA to finish (atomic ticket, no waiting) or by k_combine_wide.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -966,17 +966,51 @@ __global__ void __launch_bounds__((kGqaWarps + kGqaProducers) * 32, 1) k_attn_gq
 
 constexpr int kMlaHeads = 64;  // query heads of the shared-latent tensor-core kernel
 
-template <int DV>
-__global__ void __launch_bounds__(256) k_combine(AttnArgs a) {
+
+// Split partials of the tensor-core shared-latent kernel, merged in split order: one warp per
+// (request, head, 128-dim quarter of the value), lane = 4 consecutive dims, every split's partial
+// loaded before any is used (one round trip to L2 rather than one per pair of splits).  The same
+// arithmetic as combine_heads_wide, so the result is identical.
+__global__ void __launch_bounds__(256, 2) k_combine_wide(AttnArgs a) {
   hs_pdl_enter();
+  constexpr int DV = 512, JB = 16;
   const int r = a.r0 + (int)blockIdx.x;
-  const int h = blockIdx.y * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = (int)blockIdx.y * 2 + (w >> 2), c = w & 3;
   if (h >= a.Hq) return;
-  if (a.S <= 32)
-    combine_heads_wide<DV, 1>(a, r, h, lane);
-  else
-    combine_heads<DV>(a, r, h, 1, lane);
+  const bool mine = lane < a.S;  // lane j holds split j's max and sum (S <= 32)
+  const int64_t phl = ((int64_t)r * a.S + lane) * a.Hq + h;
+  const float m = mine ? __ldcg(&a.ml[phl * 2]) : -INFINITY;
+  const float l = mine ? __ldcg(&a.ml[phl * 2 + 1]) : 0.f;
+  float M = m;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  const float wt = (M == -INFINITY || m == -INFINITY) ? 0.f : exp2f(m - M);
+  float den = wt * l;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  const float4* p = (const float4*)(a.part + ((int64_t)r * a.S * a.Hq + h) * DV) + 32 * c + lane;
+  const int64_t step = (int64_t)a.Hq * (DV / 4);  // float4s from one split's partial to the next
+  for (int b0 = 0; b0 < a.S; b0 += JB) {
+    float4 v[JB];
+#pragma unroll
+    for (int j = 0; j < JB; ++j)
+      if (b0 + j < a.S) v[j] = __ldcg(p + (b0 + j) * step);
+#pragma unroll
+    for (int j = 0; j < JB; ++j) {
+      if (b0 + j < a.S) {
+        const float wj = __shfl_sync(0xffffffffu, wt, b0 + j);
+        acc.x = fmaf(wj, v[j].x, acc.x);
+        acc.y = fmaf(wj, v[j].y, acc.y);
+        acc.z = fmaf(wj, v[j].z, acc.z);
+        acc.w = fmaf(wj, v[j].w, acc.w);
+      }
+    }
+  }
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  ((float4*)(a.out + ((int64_t)(r - a.r0) * a.Hq + h) * DV))[32 * c + lane] =
+      make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
 }
 
 // ---- shared-latent records on tcgen05 tensor cores (64 heads) -----------------------------
@@ -995,7 +1029,7 @@ __global__ void __launch_bounds__(256) k_combine(AttnArgs a) {
 // runs the softmax.  The running max per head is raised only when a score exceeds it by more than
 // 2^8 (softmax is shift-invariant; weights stay <= 256 in bf16 and fp32), and only then is the O^T
 // accumulator rescaled in TMEM.  The normaliser sums the same bf16-rounded weights the MMA uses.
-// The split partials (O, max, sum) are combined by k_combine in split order.
+// The split partials (O, max, sum) are combined by k_combine_wide in split order.
 constexpr int kUTok = 128, kUHeads = 64, kUDim = 576;
 constexpr int kUKv = kUTok * kUDim * 2;              // 147456 B: gathered tile
 constexpr int kUQh = kUHeads * (kUDim / 2) * 2;      // 36864 B: half of Q
@@ -1457,11 +1491,11 @@ cudaError_t dispatch(const hs_config& c, const AttnArgs* a, const Plan& pl, cuda
   if (pl.kind == 4) {
     cudaError_t e = launch_kernel(k_attn_mla_umma, a, pl, kUThreads, st);
     if (e == cudaSuccess && a == nullptr)
-      e = cudaFuncSetAttribute(k_combine<512>, cudaFuncAttributePreferredSharedMemoryCarveout,
+      e = cudaFuncSetAttribute(k_combine_wide, cudaFuncAttributePreferredSharedMemoryCarveout,
                                (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess || a == nullptr) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(a->R, (a->Hq + 7) / 8, 1);
+    cfg.gridDim = dim3(a->R, (a->Hq + 1) / 2, 1);
     cfg.blockDim = dim3(256, 1, 1);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -1469,7 +1503,7 @@ cudaError_t dispatch(const hs_config& c, const AttnArgs* a, const Plan& pl, cuda
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_combine<512>, *a);
+    return cudaLaunchKernelEx(&cfg, k_combine_wide, *a);
   }
   if (pl.kind == 0) return launch_kernel(k_attn_cc<576, 512, 1, 8>, a, pl, AttnCfg<576, 512, 1, 8>::THREADS, st);
   if (pl.fetch) {
