@@ -1021,8 +1021,9 @@ __global__ void __launch_bounds__(256, 2) k_combine_wide(AttnArgs a) {
 //   O^T[512 x 64] += V^T[512 x 128] . P^T    4 row tiles x 8 k-steps into TMEM columns 64-319
 // Operands sit in shared memory in the canonical no-swizzle layout (8 x 16-byte core matrices).
 // The gathered tile is one buffer of 128 rows: as K it is read K-major (core matrices 128 B apart
-// along the dims, 9216 B apart along the tokens), as V^T MN-major from the same bytes.  Q is streamed
-// per tile in two halves of 288 dims; P^T is written MN-major (heads contiguous).
+// along the dims, 9216 B apart along the tokens), as V^T MN-major from the same bytes.  Q (all 576
+// dims, the same layout with 64 rows) is loaded per tile beside the gather; once S is complete Q is
+// dead and P^T is written MN-major (heads contiguous) over it.
 // Roles: eight producer warps gather rows with cp.async straight into that layout (padding rows
 // zero-filled) and arrive on mbarriers when their copies land; one thread issues the MMAs and
 // commits them to mbarriers; a 128-thread warpgroup (one token, i.e. one TMEM lane, per thread)
@@ -1032,10 +1033,8 @@ __global__ void __launch_bounds__(256, 2) k_combine_wide(AttnArgs a) {
 // The split partials (O, max, sum) are combined by k_combine_wide in split order.
 constexpr int kUTok = 128, kUHeads = 64, kUDim = 576;
 constexpr int kUKv = kUTok * kUDim * 2;              // 147456 B: gathered tile
-constexpr int kUQh = kUHeads * (kUDim / 2) * 2;      // 36864 B: half of Q
-constexpr int kUP = kUTok * kUHeads * 2;             // 16384 B: P^T
-constexpr int kUSboKv = (kUDim / 8) * 128;           // 9216 B between 8-token groups of the tile
-constexpr int kUSboQ = (kUDim / 2 / 8) * 128;        // 4608 B between 8-head groups of a Q half
+constexpr int kUQ = kUHeads * kUDim * 2;             // 73728 B: Q; P^T (16384 B) later reuses it
+constexpr int kUSboKv = (kUDim / 8) * 128;           // 9216 B between 8-row groups (tile and Q)
 constexpr int kUProd = 8;                            // producer warps
 constexpr int kUWarpMma = 4;                         // warp of the MMA issuer
 constexpr int kUThreads = (4 + 1 + kUProd) * 32;
@@ -1119,9 +1118,8 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_umma(AttnArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* sKV = smem;
   uint8_t* sQ = smem + kUKv;
-  uint8_t* sP = sQ + kUQh;
-  int32_t* s_locs = (int32_t*)(sP + kUP);  // [chunk]
-  __shared__ __align__(8) uint64_t bar_kv, bar_q, bar_qfree, bar_s, bar_p, bar_pv, bar_fin;
+  uint8_t* sP = sQ;  // P^T is written once S (the last reader of Q) is complete
+  __shared__ __align__(8) uint64_t bar_kv, bar_q, bar_s, bar_p, bar_pv, bar_fin;
   __shared__ uint32_t s_tmem, abort_flag;
   __shared__ float s_m[kUHeads], s_l[kUHeads], s_alpha[kUHeads], s_red[4][kUHeads];
   __shared__ uint32_t s_need[2][4];
@@ -1135,8 +1133,7 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_umma(AttnArgs a) {
   if (tid == 0) {
     mbar_init(&bar_kv, kUProd * 32);  // one arrival per producer lane once its copies landed
     mbar_init(&bar_q, kUProd * 32);
-    mbar_init(&bar_qfree, 1u);        // MMA commits
-    mbar_init(&bar_s, 1u);
+    mbar_init(&bar_s, 1u);            // MMA commits
     mbar_init(&bar_pv, 1u);
     mbar_init(&bar_fin, 1u);
     mbar_init(&bar_p, 128u);          // softmax threads
@@ -1148,20 +1145,10 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_umma(AttnArgs a) {
     s_l[h] = 0.f;
   }
   rows_setup(a, r, s_pg);
-  {
-    const int32_t* locs = a.locs + (int64_t)(r - a.r0) * a.k + t0;
-    const int64_t rows_r = rows_of(a, r);
-    bool bad = false;
-    for (int x = tid; x < n; x += kUThreads) {
-      int32_t loc = locs[x];
-      if (loc < -1 || (int64_t)loc >= rows_r) {
-        bad = true;
-        loc = -1;
-      }
-      s_locs[x] = loc;
-    }
-    if (bad) atomicOr(a.err, (uint32_t)HS_DEVERR_LOC);
-  }
+  // the split's slots; producers and softmax apply the same validity test (outside [0, rows) or
+  // padding: a zero row and a zero weight)
+  const int32_t* locs = a.locs + (int64_t)(r - a.r0) * a.k + t0;
+  const int64_t rows_r = rows_of(a, r);
   if (warp == kUWarpMma) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(&s_tmem))
                  : "memory");
@@ -1173,30 +1160,13 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_umma(AttnArgs a) {
   const uint32_t tb = s_tmem;
 
   if (warp > kUWarpMma) {
-    // ---------------- producers: Q halves and gathered tiles, cp.async into the MMA layout ----------------
+    // ---------------- producers: gathered tile, then Q, cp.async into the MMA layout ----------------
     const int pw = warp - kUWarpMma - 1, pl = pw * 32 + lane;
     const uint16_t* qr = a.q + (int64_t)(r - a.r0) * a.Hq * kUDim;
     const uint32_t sq_u = smem_u32(sQ), skv_u = smem_u32(sKV);
-    bool ok = true;
-    auto load_q = [&](int g) {  // global half index g = 2 tile + half
-      if (g >= 1) {
-        bool w = true;
-        if (lane == 0) w = mbar_wait_bounded(&bar_qfree, (uint32_t)((g - 1) & 1), &abort_flag);
-        if (__shfl_sync(0xffffffffu, w ? 1 : 0, 0) == 0) return false;
-      }
-      const int half = g & 1;
-      for (int e = pl; e < kUHeads * 36; e += kUProd * 32) {
-        const int ng = e / 288, rem = e % 288, c = rem / 8, hn = ng * 8 + rem % 8;
-        cp_async16_zfill(sq_u + (uint32_t)(ng * kUSboQ + c * 128 + (rem % 8) * 16),
-                         qr + (int64_t)hn * kUDim + half * 288 + c * 8, 16u);
-      }
-      cp_async_arrive_noinc(&bar_q);
-      return true;
-    };
+    bool ok = true, bad = false;
     for (int i = 0; ok && i < ntile; ++i) {
-      ok = load_q(2 * i);
-      if (!ok) break;
-      if (i >= 1) {
+      if (i >= 1) {  // the previous tile's value product has read the tile and P^T (over Q)
         bool w = true;
         if (lane == 0) w = mbar_wait_bounded(&bar_pv, (uint32_t)((i - 1) & 1), &abort_flag);
         if (__shfl_sync(0xffffffffu, w ? 1 : 0, 0) == 0) {
@@ -1210,7 +1180,11 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_umma(AttnArgs a) {
         const int rg = 2 * pw + g2;
         const int row = rg * 8 + (lane & 7);
         const int x = i * kUTok + row;
-        const int32_t loc = x < n ? s_locs[x] : -1;
+        int32_t loc = x < n ? locs[x] : -1;
+        if (loc < -1 || (int64_t)loc >= rows_r) {
+          bad = true;
+          loc = -1;
+        }
         // padding reads nothing (zero fill); its source is any mapped address
         const uint8_t* src = loc >= 0 ? row_addr(s_pg, a.kv_shift, a.rec, loc) : (const uint8_t*)a.q;
         const uint32_t dst = skv_u + (uint32_t)(rg * kUSboKv + (lane & 7) * 16);
@@ -1222,8 +1196,15 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_umma(AttnArgs a) {
         }
       }
       cp_async_arrive_noinc(&bar_kv);
-      ok = load_q(2 * i + 1);
+      // Q: 64 heads x 72 chunks of 16 bytes, 8-head groups 9216 B apart
+      for (int e = pl; e < kUHeads * 72; e += kUProd * 32) {
+        const int ng = e / 576, rem = e % 576, c = rem / 8, hn = ng * 8 + rem % 8;
+        cp_async16_zfill(sq_u + (uint32_t)(ng * kUSboKv + c * 128 + (rem % 8) * 16), qr + (int64_t)hn * kUDim + c * 8,
+                         16u);
+      }
+      cp_async_arrive_noinc(&bar_q);
     }
+    if (bad) atomicOr(a.err, (uint32_t)HS_DEVERR_LOC);
     asm volatile("cp.async.wait_all;" ::: "memory");
     if (!ok && lane == 0) {
       *(volatile uint32_t*)&abort_flag = 1u;
@@ -1233,23 +1214,19 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_umma(AttnArgs a) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       const uint32_t id_s = umma_idesc_bf16(128, 64, 0, 0), id_o = umma_idesc_bf16(128, 64, 1, 1);
-      const uint32_t skv_u = smem_u32(sKV), sq_u = smem_u32(sQ), sp_u = smem_u32(sP);
+      const uint32_t skv_u = smem_u32(sKV), sq_u = smem_u32(sQ), sp_u = smem_u32(sP);  // sP == sQ
       bool ok = true;
       for (int i = 0; ok && i < ntile; ++i) {
-        for (int half = 0; half < 2 && ok; ++half) {
-          ok = mbar_wait_bounded(&bar_q, (uint32_t)((2 * i + half) & 1), &abort_flag);
-          if (ok && half == 0) ok = mbar_wait_bounded(&bar_kv, (uint32_t)(i & 1), &abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-#pragma unroll 6
-          for (int s2 = 0; s2 < 18; ++s2) {
-            const uint64_t da = umma_sdesc(skv_u + (uint32_t)((36 * half + 2 * s2) * 128), 128, kUSboKv);
-            const uint64_t db = umma_sdesc(sq_u + (uint32_t)(2 * s2 * 128), 128, kUSboQ);
-            umma_bf16(tb, da, db, id_s, (half | s2) != 0 ? 1u : 0u);
-          }
-          umma_commit(&bar_qfree);
-        }
+        ok = mbar_wait_bounded(&bar_kv, (uint32_t)(i & 1), &abort_flag);
+        if (ok) ok = mbar_wait_bounded(&bar_q, (uint32_t)(i & 1), &abort_flag);
         if (!ok) break;
+        tc_fence_after();
+#pragma unroll 6
+        for (int s2 = 0; s2 < 36; ++s2) {  // K = 576 in steps of 16: two core matrices of each operand
+          const uint64_t da = umma_sdesc(skv_u + (uint32_t)(2 * s2 * 128), 128, kUSboKv);
+          const uint64_t db = umma_sdesc(sq_u + (uint32_t)(2 * s2 * 128), 128, kUSboKv);
+          umma_bf16(tb, da, db, id_s, s2 != 0 ? 1u : 0u);
+        }
         umma_commit(&bar_s);
         ok = mbar_wait_bounded(&bar_p, (uint32_t)(i & 1), &abort_flag);
         if (!ok) break;
@@ -1288,7 +1265,8 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_umma(AttnArgs a) {
       if (ok && i >= 1) ok = mbar_wait_bounded(&bar_pv, (uint32_t)((i - 1) & 1), &abort_flag);
       tc_fence_after();
       const int x = i * kUTok + tid;
-      const bool valid = ok && x < n && s_locs[x] >= 0;
+      const int32_t lx = x < n ? locs[x] : -1;
+      const bool valid = ok && lx >= 0 && (int64_t)lx < rows_r;
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {  // heads [32 hh, 32 hh + 32)
         float v[32];
@@ -1437,7 +1415,7 @@ bool plan_for(const hs_config* c, int num_sms, Plan* pl) {
     pl->G = kMlaHeads;
     pl->groups = 1;
     pl->T = kUTok;
-    pl->smem = (size_t)kUKv + kUQh + kUP;
+    pl->smem = (size_t)kUKv + kUQ;
     per_cta_wave = 1;
   } else {
     if (c->head_dim_qk != 576 || c->head_dim_v != 512) return false;
@@ -1460,7 +1438,6 @@ bool plan_for(const hs_config* c, int num_sms, Plan* pl) {
   pl->chunk = chunk;
   pl->S = (c->top_k + chunk - 1) / chunk;
 
-  if (pl->kind == 4) pl->smem += (size_t)chunk * 4;   // slot list
   return pl->smem <= 220 * 1024;
 }
 
