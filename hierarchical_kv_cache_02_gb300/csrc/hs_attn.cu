@@ -13,10 +13,14 @@
 // order, so the result depends only on the top-k order, never on which slot holds a record:
 // cold, warm and fully-resident runs are bit-identical.  Partials are combined in split order
 // by the last CTA to finish (atomic ticket, no waiting) or by k_combine_wide.
+#include <cuda.h>  // CUtensorMap (the encoder is reached through the runtime's driver entry point)
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
+#include <string.h>
+
+#include <new>
 
 #include "hs_internal.cuh"
 
@@ -30,6 +34,8 @@ struct AttnArgs {
   const int32_t* locs;   // [R][k]
   const uint8_t* kv;     // caller rows (kv_pt null): row (r, loc) at kv + (r * rows + loc) * rec
   const uint64_t* kv_pt; // hot-buffer rows: [R][kv_pages] device address of each buffer page
+  const uint8_t* kv_pool;   // hot-buffer rows: base of the device cache pool (row = byte offset / rec)
+  const CUtensorMap* kv_tmap;  // host copy of the pool's tensor map (tensor-core shared-latent kernel), or null
   const int32_t* kv_cap; // hot-buffer rows: [R] rows each buffer holds (<= rows)
   int kv_pages, kv_shift;
   float* out;            // [R][Hq][DV]
@@ -1049,10 +1055,21 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-__device__ __forceinline__ uint64_t umma_sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
-  // start address, leading / stride byte offsets (16-byte units), descriptor version 1, no swizzle
+__device__ __forceinline__ uint64_t umma_sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t layout = 0) {
+  // start address, leading / stride byte offsets (16-byte units), descriptor version 1, layout type
+  // (0: no swizzle; 2: 128-byte swizzle, atoms 1024-byte aligned so the base offset is 0)
   return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46);
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) | ((uint64_t)layout << 61);
+}
+// TMA gather of four rows (row coordinates y0..y3, -1 reads zeros) x one 64-element column block
+// (x, a multiple of 64) of a 2-D tensor map, 128-byte swizzled into shared memory at dst
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int x, int y0, int y1, int y2, int y3,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"((uint64_t)map), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(smem_u32(bar))
+      : "memory");
 }
 __device__ __forceinline__ uint32_t umma_idesc_bf16(int M, int N, int a_mn, int b_mn) {
   // fp32 accumulator, bf16 A and B, operand majors, N / 8, M / 16
@@ -1113,9 +1130,12 @@ __device__ __forceinline__ float reduce32_max_transposed(float (&v)[32], int lan
   return v[0];
 }
 
-__global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_umma(AttnArgs a) {
+template <bool TMA>
+__global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_umma(AttnArgs a, const __grid_constant__ CUtensorMap tmap) {
   hs_pdl_enter();
-  extern __shared__ __align__(128) uint8_t smem[];
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  // the tile starts 1024-byte aligned (the period of the 128-byte swizzle); the launch adds 1 KB
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sKV = smem;
   uint8_t* sQ = smem + kUKv;
   uint8_t* sP = sQ;  // P^T is written once S (the last reader of Q) is complete
@@ -1124,6 +1144,7 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_umma(AttnArgs a) {
   __shared__ float s_m[kUHeads], s_l[kUHeads], s_alpha[kUHeads], s_red[4][kUHeads];
   __shared__ uint32_t s_need[2][4];
   __shared__ uint64_t s_pg[kMaxSlotPages];
+  __shared__ int32_t s_pgrow[kMaxSlotPages];  // TMA: pool row of each page's first slot
 
   const int split = blockIdx.x, r = a.r0 + (int)blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1131,7 +1152,7 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_umma(AttnArgs a) {
   const int n = min(a.k, t0 + a.chunk) - t0;
   const int ntile = (n + kUTok - 1) / kUTok;
   if (tid == 0) {
-    mbar_init(&bar_kv, kUProd * 32);  // one arrival per producer lane once its copies landed
+    mbar_init(&bar_kv, TMA ? 1u : kUProd * 32);  // TMA: one expect-tx arrival; else one per producer lane
     mbar_init(&bar_q, kUProd * 32);
     mbar_init(&bar_s, 1u);            // MMA commits
     mbar_init(&bar_pv, 1u);
@@ -1145,6 +1166,10 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_umma(AttnArgs a) {
     s_l[h] = 0.f;
   }
   rows_setup(a, r, s_pg);
+  if (TMA && tid < a.kv_pages) {
+    const uint64_t pg = a.kv_pt[(int64_t)r * a.kv_pages + tid];
+    s_pgrow[tid] = pg != 0ull ? (int32_t)((pg - (uint64_t)(uintptr_t)a.kv_pool) / (uint64_t)a.rec) : -1;
+  }
   // the split's slots; producers and softmax apply the same validity test (outside [0, rows) or
   // padding: a zero row and a zero weight)
   const int32_t* locs = a.locs + (int64_t)(r - a.r0) * a.k + t0;
@@ -1165,6 +1190,7 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_umma(AttnArgs a) {
     const uint16_t* qr = a.q + (int64_t)(r - a.r0) * a.Hq * kUDim;
     const uint32_t sq_u = smem_u32(sQ), skv_u = smem_u32(sKV);
     bool ok = true, bad = false;
+    int gathered = 0;  // TMA: tiles whose gather was issued
     for (int i = 0; ok && i < ntile; ++i) {
       if (i >= 1) {  // the previous tile's value product has read the tile and P^T (over Q)
         bool w = true;
@@ -1174,28 +1200,51 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_umma(AttnArgs a) {
           break;
         }
       }
-      // this warp's two 8-token groups: lane -> row (lane & 7), 16-byte column 4 j + (lane >> 3)
+      if (TMA) {
+        // 9 column blocks of 64 dims x 32 groups of 4 rows, gathered by the tensor memory accelerator
+        // into the 128-byte swizzled tile (blocks 16 KB apart, rows 128 B apart); padding reads zeros
+        if (pl == 0) mbar_arrive_expect_tx(&bar_kv, (uint32_t)kUKv);
+        const int msk = (int)((1u << a.kv_shift) - 1u);
+        for (int o = pl; o < 9 * 32; o += kUProd * 32) {
+          const int kb = o >> 5, g4 = o & 31;
+          int rr[4];
 #pragma unroll
-      for (int g2 = 0; g2 < 2; ++g2) {
-        const int rg = 2 * pw + g2;
-        const int row = rg * 8 + (lane & 7);
-        const int x = i * kUTok + row;
-        int32_t loc = x < n ? locs[x] : -1;
-        if (loc < -1 || (int64_t)loc >= rows_r) {
-          bad = true;
-          loc = -1;
+          for (int u = 0; u < 4; ++u) {
+            const int x = i * kUTok + 4 * g4 + u;
+            int32_t loc = x < n ? locs[x] : -1;
+            if (loc < -1 || (int64_t)loc >= rows_r) {
+              bad = true;
+              loc = -1;
+            }
+            rr[u] = loc >= 0 ? s_pgrow[loc >> a.kv_shift] + (loc & msk) : -1;
+          }
+          tma_gather4(skv_u + (uint32_t)(kb * 16384 + g4 * 512), &tmap, kb * 64, rr[0], rr[1], rr[2], rr[3], &bar_kv);
         }
-        // padding reads nothing (zero fill); its source is any mapped address
-        const uint8_t* src = loc >= 0 ? row_addr(s_pg, a.kv_shift, a.rec, loc) : (const uint8_t*)a.q;
-        const uint32_t dst = skv_u + (uint32_t)(rg * kUSboKv + (lane & 7) * 16);
-        const uint32_t nb = loc >= 0 ? 16u : 0u;
+        gathered = i + 1;
+      } else {
+        // this warp's two 8-token groups: lane -> row (lane & 7), 16-byte column 4 j + (lane >> 3)
+#pragma unroll
+        for (int g2 = 0; g2 < 2; ++g2) {
+          const int rg = 2 * pw + g2;
+          const int row = rg * 8 + (lane & 7);
+          const int x = i * kUTok + row;
+          int32_t loc = x < n ? locs[x] : -1;
+          if (loc < -1 || (int64_t)loc >= rows_r) {
+            bad = true;
+            loc = -1;
+          }
+          // padding reads nothing (zero fill); its source is any mapped address
+          const uint8_t* src = loc >= 0 ? row_addr(s_pg, a.kv_shift, a.rec, loc) : (const uint8_t*)a.q;
+          const uint32_t dst = skv_u + (uint32_t)(rg * kUSboKv + (lane & 7) * 16);
+          const uint32_t nb = loc >= 0 ? 16u : 0u;
 #pragma unroll 6
-        for (int j = 0; j < 18; ++j) {
-          const int c = 4 * j + (lane >> 3);
-          cp_async16_zfill(dst + (uint32_t)(c * 128), src + c * 16, nb);
+          for (int j = 0; j < 18; ++j) {
+            const int c = 4 * j + (lane >> 3);
+            cp_async16_zfill(dst + (uint32_t)(c * 128), src + c * 16, nb);
+          }
         }
+        cp_async_arrive_noinc(&bar_kv);
       }
-      cp_async_arrive_noinc(&bar_kv);
       // Q: 64 heads x 72 chunks of 16 bytes, 8-head groups 9216 B apart
       for (int e = pl; e < kUHeads * 72; e += kUProd * 32) {
         const int ng = e / 576, rem = e % 576, c = rem / 8, hn = ng * 8 + rem % 8;
@@ -1205,6 +1254,11 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_umma(AttnArgs a) {
       cp_async_arrive_noinc(&bar_q);
     }
     if (bad) atomicOr(a.err, (uint32_t)HS_DEVERR_LOC);
+    if (TMA && !ok && gathered > 0 && pl == 0) {
+      // a wait gave up: the last gather still lands in this CTA's shared memory before it may exit
+      volatile uint32_t never = 0u;
+      mbar_wait_bounded(&bar_kv, (uint32_t)((gathered - 1) & 1), &never);
+    }
     asm volatile("cp.async.wait_all;" ::: "memory");
     if (!ok && lane == 0) {
       *(volatile uint32_t*)&abort_flag = 1u;
@@ -1223,7 +1277,9 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_umma(AttnArgs a) {
         tc_fence_after();
 #pragma unroll 6
         for (int s2 = 0; s2 < 36; ++s2) {  // K = 576 in steps of 16: two core matrices of each operand
-          const uint64_t da = umma_sdesc(skv_u + (uint32_t)(2 * s2 * 128), 128, kUSboKv);
+          // tile K-major: swizzled, a k-step is 32 B inside a 128-byte row of a 64-dim block; else core matrices
+          const uint64_t da = TMA ? umma_sdesc(skv_u + (uint32_t)((s2 >> 2) * 16384 + (s2 & 3) * 32), 16, 1024, 2)
+                                  : umma_sdesc(skv_u + (uint32_t)(2 * s2 * 128), 128, kUSboKv);
           const uint64_t db = umma_sdesc(sq_u + (uint32_t)(2 * s2 * 128), 128, kUSboKv);
           umma_bf16(tb, da, db, id_s, s2 != 0 ? 1u : 0u);
         }
@@ -1235,7 +1291,11 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_umma(AttnArgs a) {
         for (int mt = 0; mt < 4; ++mt) {
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
-            const uint64_t da = umma_sdesc(skv_u + (uint32_t)(mt * 16 * 128 + ks * 2 * kUSboKv), kUSboKv, 128);
+            // V^T MN-major from the same bytes: swizzled, LBO = 16 KB between 64-dim blocks, SBO = 1 KB
+            // between 8-token groups; else LBO along the tokens, SBO along the dims
+            const uint64_t da =
+                TMA ? umma_sdesc(skv_u + (uint32_t)(mt * 32768 + ks * 2048), 16384, 1024, 2)
+                    : umma_sdesc(skv_u + (uint32_t)(mt * 16 * 128 + ks * 2 * kUSboKv), kUSboKv, 128);
             const uint64_t db = umma_sdesc(sp_u + (uint32_t)(ks * 2 * 1024), 1024, 128);
             umma_bf16(tb + 64u + 64u * (uint32_t)mt, da, db, id_o, (i | ks) != 0 ? 1u : 0u);
           }
@@ -1415,7 +1475,7 @@ bool plan_for(const hs_config* c, int num_sms, Plan* pl) {
     pl->G = kMlaHeads;
     pl->groups = 1;
     pl->T = kUTok;
-    pl->smem = (size_t)kUKv + kUQ;
+    pl->smem = (size_t)kUKv + kUQ + 1024;  // + the alignment of the swizzled tile
     per_cta_wave = 1;
   } else {
     if (c->head_dim_qk != 576 || c->head_dim_v != 512) return false;
@@ -1466,7 +1526,32 @@ cudaError_t launch_kernel(K kern, const AttnArgs* a, const Plan& pl, int threads
 
 cudaError_t dispatch(const hs_config& c, const AttnArgs* a, const Plan& pl, cudaStream_t st) {
   if (pl.kind == 4) {
-    cudaError_t e = launch_kernel(k_attn_mla_umma, a, pl, kUThreads, st);
+    cudaError_t e = cudaSuccess;
+    if (a == nullptr) {  // preparation: shared-memory limit and carveout of both variants
+      for (auto kern : {k_attn_mla_umma<true>, k_attn_mla_umma<false>}) {
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+        if (e == cudaSuccess)
+          e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                   (int)cudaSharedmemCarveoutMaxShared);
+      }
+    } else {
+      // hot-buffer rows through the pool's tensor map (TMA gather); caller rows by cp.async
+      CUtensorMap tm;
+      memset(&tm, 0, sizeof(tm));
+      if (a->kv_tmap != nullptr) tm = *a->kv_tmap;
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(pl.S, a->R, pl.groups);
+      cfg.blockDim = dim3(kUThreads, 1, 1);
+      cfg.dynamicSmemBytes = pl.smem;
+      cfg.stream = st;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      e = a->kv_tmap != nullptr ? cudaLaunchKernelEx(&cfg, k_attn_mla_umma<true>, *a, tm)
+                                : cudaLaunchKernelEx(&cfg, k_attn_mla_umma<false>, *a, tm);
+    }
     if (e == cudaSuccess && a == nullptr)
       e = cudaFuncSetAttribute(k_combine_wide, cudaFuncAttributePreferredSharedMemoryCarveout,
                                (int)cudaSharedmemCarveoutMaxShared);
@@ -1532,6 +1617,8 @@ int hs_launch_attn(hs_pool* p, int layer, int r0, int nreq, const void* d_q, con
   a.locs = d_locs;
   if (kv_base == nullptr) {  // the layer's hot buffers, through the slot table
     a.kv_pt = p->slot_table + (int64_t)layer * c.num_requests * p->slot_pages;
+    a.kv_pool = p->buf;
+    a.kv_tmap = (const CUtensorMap*)p->attn_tmap;
     a.kv_cap = p->slot_cap + (int64_t)layer * c.num_requests;
     a.kv_pages = p->slot_pages;
     a.kv_shift = p->slot_shift;
@@ -1569,6 +1656,39 @@ int hs_launch_attn(hs_pool* p, int layer, int r0, int nreq, const void* d_q, con
   a.L = c.num_layers;
   a.layer = layer;
   return dispatch(c, &a, pl, st) == cudaSuccess ? HS_OK : HS_ERR_CUDA;
+}
+
+// The device cache pool as a 2-D tensor (rows = slots of every page, 576 bf16 each) for the TMA
+// gather of the tensor-core shared-latent kernel; null (and the cp.async gather) when that kernel is
+// not used or the encoder is unavailable.
+void* hs_attn_make_pool_map(const hs_config* c, int num_sms, void* pool_base, int64_t pool_rows) {
+  Plan pl;
+  if (!plan_for(c, num_sms, &pl) || pl.kind != 4 || pool_base == nullptr || pool_rows < 1) return nullptr;
+  typedef CUresult (*EncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                               const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                               CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      fn == nullptr || q != cudaDriverEntryPointSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  CUtensorMap* tm = new (std::align_val_t(64)) CUtensorMap;
+  const cuuint64_t gdim[2] = {(cuuint64_t)kUDim, (cuuint64_t)pool_rows};
+  const cuuint64_t gstride[1] = {(cuuint64_t)kUDim * 2};
+  const cuuint32_t box[2] = {64, 1}, estr[2] = {1, 1};
+  if (((EncodeFn)fn)(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pool_base, gdim, gstride, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+    ::operator delete(tm, std::align_val_t(64));
+    return nullptr;
+  }
+  return tm;
+}
+
+void hs_attn_free_pool_map(void* m) {
+  if (m != nullptr) ::operator delete(m, std::align_val_t(64));
 }
 
 int hs_attn_prepare(const hs_config* c, int num_sms) {
