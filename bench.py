@@ -408,7 +408,7 @@ def run_ours(args, w, world, rank, local):
     # ---- end to end through the public API: inputs from pinned host memory, outputs back -----
     e2e = None
     if not args.no_e2e and G == 1:
-        e2e = run_e2e(pool, wl, W, K, world, locs, outs, scale)
+        e2e = run_e2e(pool, wl, W, K, world, locs, outs, scale, use_graph)
 
     # ---- host-link peak on this machine: pinned H2D copy, best of 5 ----
     h2d = measure_h2d(device)
@@ -469,7 +469,7 @@ def run_ours(args, w, world, rank, local):
     return out
 
 
-def run_e2e(pool, wl, W, K, world, locs, outs, scale):
+def run_e2e(pool, wl, W, K, world, locs, outs, scale, use_graph=False):
     """Same steps after a cold reset, with every step's top-k, queries and new records copied from
     pinned host memory and all its attention outputs copied back, inside the timed region.  As a
     serving loop would, a copy stream moves step t+1's inputs in and step t's outputs out while
@@ -495,8 +495,6 @@ def run_e2e(pool, wl, W, K, world, locs, outs, scale):
     ev_in = [torch.cuda.Event() for _ in range(2)]    # inputs of the buffer's step have landed
     ev_done = [torch.cuda.Event() for _ in range(2)]  # the buffer's step has computed
     ev_out = [torch.cuda.Event() for _ in range(2)]   # its outputs are back on the host
-    for e in ev_done + ev_out:
-        e.record(stream)
 
     def copy_in(t):
         b = t % 2
@@ -510,28 +508,44 @@ def run_e2e(pool, wl, W, K, world, locs, outs, scale):
 
     def compute_and_copy_out(t):
         b = t % 2
-        stream.wait_event(ev_in[b])
-        stream.wait_event(ev_out[b])  # outputs of two steps ago have left these buffers
+        cur = torch.cuda.current_stream()
+        cur.wait_event(ev_in[b])
+        cur.wait_event(ev_out[b])  # outputs of two steps ago have left these buffers
         for l in range(L):
             if wl.appends:
                 pool.append_resolve(l, d_pos[b], d_app[b][l], d_topk[b][l], locs[l])
             else:
                 pool.resolve(l, d_topk[b][l], locs[l])
             pool.sparse_attn(l, d_q[b][l], locs[l], d_out[b][l], scale=scale)
-        ev_done[b].record(stream)
+        ev_done[b].record(cur)
         copy.wait_event(ev_done[b])
         with torch.cuda.stream(copy):
             h_out[t].copy_(d_out[b], non_blocking=True)
             ev_out[b].record(copy)
 
     def run(t0, t1):
+        cur = torch.cuda.current_stream()
+        for e in ev_done + ev_out:  # no step is using either buffer yet
+            e.record(cur)
+        copy.wait_stream(cur)
         copy_in(t0)
         for t in range(t0, t1):
             if t + 1 < t1:
                 copy_in(t + 1)
             compute_and_copy_out(t)
-        stream.wait_stream(copy)
+        cur.wait_stream(copy)
 
+    graph = None
+    if use_graph:
+        # the timed steps, copies included, as one captured graph, replayed once untimed first
+        pool.reset()
+        run(0, W)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            run(W, S)
+        graph.replay()
+        torch.cuda.synchronize()
     pool.reset()
     run(0, W)
     torch.cuda.synchronize()
@@ -539,8 +553,10 @@ def run_e2e(pool, wl, W, K, world, locs, outs, scale):
     barrier(world)
     torch.cuda.synchronize()
     start.record(stream)
-    copy.wait_stream(stream)
-    run(W, S)
+    if graph is not None:
+        graph.replay()
+    else:
+        run(W, S)
     stop.record(stream)
     torch.cuda.synchronize()
     barrier(world)
