@@ -1130,29 +1130,7 @@ __device__ __forceinline__ float reduce32_max_transposed(float (&v)[32], int lan
   return v[0];
 }
 
-// DSMEM helpers for the cluster reduction of the split partials
-__device__ __forceinline__ uint32_t dsmem_map(uint32_t local_addr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_addr), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ float dsmem_ld(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-  return v;
-}
-__device__ __forceinline__ void dsmem_st4(uint32_t addr, float x, float y, float z, float w) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(x), "f"(y), "f"(z), "f"(w)
-               : "memory");
-}
-__device__ __forceinline__ void cluster_barrier() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// TMA: gather the tile from the pool's tensor map; CL: the splits of a request form one thread-block
-// cluster and merge their partials in distributed shared memory (no partials in global memory, no
-// combine kernel)
-template <bool TMA, bool CL>
+template <bool TMA>
 __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_umma(AttnArgs a, const __grid_constant__ CUtensorMap tmap) {
   hs_pdl_enter();
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -1442,7 +1420,7 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_umma(AttnArgs a, cons
     }
     tc_fence_after();
     named_sync_128();
-    if (!CL && ok && abort_flag == 0u) {
+    if (ok && abort_flag == 0u) {
       const int64_t ph0 = ((int64_t)r * a.S + split) * a.Hq;
       if (tid < kUHeads) *(float2*)(a.ml + (ph0 + tid) * 2) = make_float2(s_m[tid], s_l[tid]);
       // O^T rows (value dims) of this thread, every head
@@ -1461,60 +1439,6 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_umma(AttnArgs a, cons
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (CL) {
-    // Every split's running max and sum are final and its tile buffer is free: the buffer now
-    // receives, from each split, the slice of value dims this CTA owns, [S][512 / S][64] fp32.
-    cluster_barrier();
-    const int S = (int)gridDim.x, dpc = 512 / S;
-    const bool good = abort_flag == 0u;
-    float* recv = (float*)sKV;
-    float* mlc = (float*)sQ;  // [S][2][64]: every split's running max and sum (Q / P^T are dead)
-    for (int t = tid; t < S * 2 * kUHeads; t += kUThreads) {
-      const int c = t / (2 * kUHeads), w = (t / kUHeads) & 1, h = t % kUHeads;
-      mlc[t] = dsmem_ld(dsmem_map(smem_u32(w ? &s_l[h] : &s_m[h]), (uint32_t)c));
-    }
-    __syncthreads();
-    if (tid < kUHeads) {  // per head: the global max, this split's scale, 1 / the global sum
-      float M = -INFINITY;
-      for (int c = 0; c < S; ++c) M = fmaxf(M, mlc[c * 2 * kUHeads + tid]);
-      float L = 0.f;
-      for (int c = 0; c < S; ++c) {
-        const float mc = mlc[c * 2 * kUHeads + tid], lc = mlc[c * 2 * kUHeads + kUHeads + tid];
-        L += (M == -INFINITY || mc == -INFINITY) ? 0.f : lc * exp2f(mc - M);
-      }
-      s_alpha[tid] = (M == -INFINITY || s_m[tid] == -INFINITY) ? 0.f : exp2f(s_m[tid] - M);
-      s_red[0][tid] = L > 0.f ? 1.f / L : 0.f;
-    }
-    __syncthreads();
-    if (warp < 4) {  // softmax warpgroup: thread = value dim of each 128-dim row tile of O^T
-#pragma unroll 1
-      for (int mt = 0; mt < 4; ++mt) {
-        const int d = mt * 128 + tid;
-        const uint32_t dst = dsmem_map(smem_u32(recv + ((int64_t)split * dpc + d % dpc) * kUHeads), (uint32_t)(d / dpc));
-#pragma unroll
-        for (int c0 = 0; c0 < kUHeads; c0 += 16) {
-          float o[16];
-          tmem_ld16(tb + ((uint32_t)(warp * 32) << 16) + 64u + 64u * (uint32_t)mt + (uint32_t)c0, o);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) o[j] = good ? o[j] * s_alpha[c0 + j] : 0.f;
-#pragma unroll
-          for (int j = 0; j < 16; j += 4) dsmem_st4(dst + (uint32_t)(c0 + j) * 4u, o[j], o[j + 1], o[j + 2], o[j + 3]);
-        }
-      }
-    }
-    cluster_barrier();
-    // this CTA's value dims, every head: sum over the splits in split order
-    float* outr = a.out + (int64_t)(r - a.r0) * a.Hq * 512;
-    for (int idx = tid; idx < dpc * kUHeads; idx += kUThreads) {  // heads fastest: conflict-free reads
-      const int ld = idx / kUHeads, h = idx - ld * kUHeads;
-      float acc = 0.f;
-      for (int c = 0; c < S; ++c) acc += recv[((int64_t)c * dpc + ld) * kUHeads + h];
-      outr[(int64_t)h * 512 + split * dpc + ld] = acc * s_red[0][h];
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-  }
   if (warp == kUWarpMma) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tb) : "memory");
 }
 
@@ -1600,101 +1524,38 @@ cudaError_t launch_kernel(K kern, const AttnArgs* a, const Plan& pl, int threads
 
 
 
-// Co-resident clusters of 1, 2, 4, 8 and 16 CTAs of the tensor-core shared-latent kernel, per device
-// (measured once when the kernel is prepared; 0 = not measured).  A launch merges its split partials
-// in a cluster only when the pool's every request fits at once, so the choice depends on the
-// configuration and the device, never on the launch: results do not depend on how calls are split.
-constexpr int kMaxMlaDevices = 64;
-int g_mla_clusters[kMaxMlaDevices][5];
-
-int log2_pow2(int v) {
-  for (int x = 0; x < 5; ++x)
-    if ((1 << x) == v) return x;
-  return -1;
-}
-
-bool mla_cluster_merge(const hs_config& c, const Plan& pl) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) {
-    cudaGetLastError();
-    return false;
-  }
-  const int lg = log2_pow2(pl.S);
-  return dev >= 0 && dev < kMaxMlaDevices && lg >= 0 && g_mla_clusters[dev][lg] >= c.num_requests;
-}
-
-template <bool TMA, bool CL>
-cudaError_t launch_mla(const AttnArgs* a, const Plan& pl, const CUtensorMap& tm, cudaStream_t st) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(pl.S, a->R, pl.groups);
-  cfg.blockDim = dim3(kUThreads, 1, 1);
-  cfg.dynamicSmemBytes = pl.smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeClusterDimension;  // the splits of a request form one cluster
-  attr[1].val.clusterDim.x = (unsigned)pl.S;
-  attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = CL ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, k_attn_mla_umma<TMA, CL>, *a, tm);
-}
-
-cudaError_t prepare_mla(const Plan& pl) {
-  cudaError_t e = cudaSuccess;
-  for (auto kern : {k_attn_mla_umma<true, false>, k_attn_mla_umma<false, false>, k_attn_mla_umma<true, true>,
-                    k_attn_mla_umma<false, true>}) {
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
-  }
-  for (auto kern : {k_attn_mla_umma<true, true>, k_attn_mla_umma<false, true>})
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(k_combine_wide, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             (int)cudaSharedmemCarveoutMaxShared);
-  if (e != cudaSuccess) return e;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxMlaDevices) {
-    cudaGetLastError();
-    return cudaSuccess;
-  }
-  for (int lg = 0; lg < 5; ++lg) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(1u << lg, 1, 1);
-    cfg.blockDim = dim3(kUThreads, 1, 1);
-    cfg.dynamicSmemBytes = pl.smem;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 1u << lg;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, k_attn_mla_umma<true, true>, &cfg) != cudaSuccess) {
-      cudaGetLastError();
-      n = 0;
-    }
-    g_mla_clusters[dev][lg] = n;
-  }
-  return cudaSuccess;
-}
-
 cudaError_t dispatch(const hs_config& c, const AttnArgs* a, const Plan& pl, cudaStream_t st) {
   if (pl.kind == 4) {
-    if (a == nullptr) return prepare_mla(pl);
-    // hot-buffer rows through the pool's tensor map (TMA gather); caller rows by cp.async
-    CUtensorMap tm;
-    memset(&tm, 0, sizeof(tm));
-    const bool tma = a->kv_tmap != nullptr;
-    if (tma) tm = *a->kv_tmap;
-    if (mla_cluster_merge(c, pl))
-      return tma ? launch_mla<true, true>(a, pl, tm, st) : launch_mla<false, true>(a, pl, tm, st);
-    cudaError_t e = tma ? launch_mla<true, false>(a, pl, tm, st) : launch_mla<false, false>(a, pl, tm, st);
-    if (e != cudaSuccess) return e;
+    cudaError_t e = cudaSuccess;
+    if (a == nullptr) {  // preparation: shared-memory limit and carveout of both variants
+      for (auto kern : {k_attn_mla_umma<true>, k_attn_mla_umma<false>}) {
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+        if (e == cudaSuccess)
+          e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                   (int)cudaSharedmemCarveoutMaxShared);
+      }
+    } else {
+      // hot-buffer rows through the pool's tensor map (TMA gather); caller rows by cp.async
+      CUtensorMap tm;
+      memset(&tm, 0, sizeof(tm));
+      if (a->kv_tmap != nullptr) tm = *a->kv_tmap;
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(pl.S, a->R, pl.groups);
+      cfg.blockDim = dim3(kUThreads, 1, 1);
+      cfg.dynamicSmemBytes = pl.smem;
+      cfg.stream = st;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      e = a->kv_tmap != nullptr ? cudaLaunchKernelEx(&cfg, k_attn_mla_umma<true>, *a, tm)
+                                : cudaLaunchKernelEx(&cfg, k_attn_mla_umma<false>, *a, tm);
+    }
+    if (e == cudaSuccess && a == nullptr)
+      e = cudaFuncSetAttribute(k_combine_wide, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess || a == nullptr) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a->R, (a->Hq + 1) / 2, 1);
     cfg.blockDim = dim3(256, 1, 1);

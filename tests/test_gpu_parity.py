@@ -244,6 +244,15 @@ def test_mla_64_heads_no_append(policy):
     run_and_compare(sc)
 
 
+@pytest.mark.parametrize("R,k", [(2, 2048), (3, 1024)])
+def test_mla_64_heads_long_selections(R, k):
+    """Few requests with long selections: 16 (R = 2) or 8 (R = 3) splits per request, whose partials
+    a GPU that fits every request's cluster at once merges in distributed shared memory."""
+    sc = Scenario(_mla(R, 1, 6000 + 6, k, 2 * k, Hq=64), ctx0=6000, steps=6, appends=True, keep=0.85,
+                  recency_mean=800, seed=17)
+    run_and_compare(sc, fused=True)
+
+
 @pytest.mark.parametrize("io", [16, 32, 128])
 def test_io_chunk_sizes(io):
     sc = Scenario(_gqa(2, 1, 2000 + 6, 128, 256, kvh=2, G=4, io=io), ctx0=2000, steps=6, appends=True, seed=9)
