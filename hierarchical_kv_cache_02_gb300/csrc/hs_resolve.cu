@@ -64,13 +64,13 @@ __device__ __forceinline__ uint32_t cta_exclusive_scan(uint32_t v, uint32_t* wbu
   if (lane == 31) wbuf[w] = x;
   __syncthreads();
   if (w == 0) {
-    uint32_t s = wbuf[lane];
+    uint32_t s = lane < kWarps ? wbuf[lane] : 0u;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       uint32_t y = __shfl_up_sync(0xffffffffu, s, o);
       if (lane >= o) s += y;
     }
-    wbuf[lane] = s;  // inclusive prefix over warps
+    if (lane < kWarps) wbuf[lane] = s;  // inclusive prefix over warps
   }
   __syncthreads();
   const uint32_t base = w > 0 ? wbuf[w - 1] : 0u;
@@ -193,18 +193,26 @@ __device__ void select_threshold(const uint32_t* key32, const uint8_t* flag, int
       if (digit != 0xffffffffu && lane == __ffs(peers) - 1) atomicAdd(&hist[digit], (uint32_t)__popc(peers));
     }
     __syncthreads();
-    // bins [2 tid, 2 tid + 1]: find the bin where the running count reaches `need`
-    const int b0 = 2 * tid;
-    const uint32_t c0 = b0 < nb ? hist[b0] : 0u, c1 = b0 + 1 < nb ? hist[b0 + 1] : 0u;
+    // bins [BPT tid, BPT tid + BPT): find the bin where the running count reaches `need`
+    constexpr int BPT = 2048 / kThreads;
+    const int b0 = BPT * tid;
+    uint32_t c[BPT], csum = 0u;
+#pragma unroll
+    for (int u = 0; u < BPT; ++u) {
+      c[u] = b0 + u < nb ? hist[b0 + u] : 0u;
+      csum += c[u];
+    }
     uint32_t tot;
-    const uint32_t excl = cta_exclusive_scan(c0 + c1, wbuf, &tot);
-    if (excl < need && need <= excl + c0 + c1) {
-      if (need <= excl + c0) {
-        sel[0] = (uint32_t)b0;
-        sel[1] = need - excl;
-      } else {
-        sel[0] = (uint32_t)b0 + 1;
-        sel[1] = need - excl - c0;
+    const uint32_t excl = cta_exclusive_scan(csum, wbuf, &tot);
+    if (excl < need && need <= excl + csum) {
+      uint32_t run = excl;
+#pragma unroll
+      for (int u = 0; u < BPT; ++u) {
+        if (run < need && need <= run + c[u]) {
+          sel[0] = (uint32_t)(b0 + u);
+          sel[1] = need - run;
+        }
+        run += c[u];
       }
     }
     __syncthreads();
