@@ -369,7 +369,8 @@ def test_append_out_of_range_flags():
 def test_exactness_cold_warm_resident_bit_identical():
     """Summary §3: the output over the hot buffer equals the output over fully resident KV,
     bit for bit, whatever the cache held before."""
-    for cfg in (_gqa(3, 1, 5000, 512, 1024), _gqa(3, 1, 5000, 512, 1024, fetch=1), _mla(2, 1, 5000, 512, 1024, Hq=32)):
+    for cfg in (_gqa(3, 1, 5000, 512, 1024), _gqa(3, 1, 5000, 512, 1024, fetch=1), _mla(2, 1, 5000, 512, 1024, Hq=32),
+                _mla(2, 1, 5000, 512, 1024, Hq=64)):  # 64 heads: hot rows by TMA gather, resident rows by cp.async
         sc = Scenario(cfg, ctx0=5000, steps=10, appends=False, keep=0.85, recency_mean=300, seed=2)
         warm = HsPool(cfg)
         prefill(warm, sc)
