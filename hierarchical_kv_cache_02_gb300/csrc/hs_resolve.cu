@@ -93,9 +93,10 @@ __device__ __forceinline__ void cp_async16(void* smem_dst, const void* src) {
                : "memory");
 }
 
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 
 // Copy misses [q0, q1) host -> slots.  A warp moves one chunk of 32 x NV lane-contiguous 16-byte
 // vectors of one record per item (coalesced 512-byte rows); ITEMS items are loaded before any store.
@@ -145,33 +146,11 @@ __device__ void fetch_misses(const ResolveArgs& a, int q0, int q1, const uint64_
 // The m victims are the candidates with the smallest (key, slot).  Radix select over the key range
 // of the candidates (key - min, 11-bit digits from the top) finds the threshold T and how many
 // candidates with key == T (lowest slots first) complete the set.
-__device__ void select_threshold(const uint32_t* key32, const uint8_t* flag, int B, uint32_t m, uint32_t* wbuf,
-                                 uint32_t* hist, uint32_t* sel, uint32_t* T_out, uint32_t* need_out) {
+__device__ void select_threshold(const uint32_t* key32, const uint8_t* flag, int B, uint32_t m, uint32_t lo,
+                                 uint32_t hi, uint32_t* wbuf, uint32_t* hist, uint32_t* sel, uint32_t* T_out,
+                                 uint32_t* need_out) {
+  // lo, hi: the smallest and largest candidate key (found by the probe)
   const int tid = threadIdx.x, lane = tid & 31;
-  __shared__ uint32_t s_lo, s_hi;
-  uint32_t lo = 0xffffffffu, hi = 0u;
-  for (int j = tid; j < B; j += kThreads) {
-    if (flag[j] & 1u) continue;
-    lo = min(lo, key32[j]);
-    hi = max(hi, key32[j]);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
-    hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
-  }
-  if (tid == 0) {
-    s_lo = 0xffffffffu;
-    s_hi = 0u;
-  }
-  __syncthreads();
-  if (lane == 0) {
-    atomicMin(&s_lo, lo);
-    atomicMax(&s_hi, hi);
-  }
-  __syncthreads();
-  lo = s_lo;
-  hi = s_hi;
   const uint32_t range = hi - lo;
   int shift = range == 0u ? 0 : 32 - __clz(range);
   uint64_t prefix = 0;
@@ -324,64 +303,74 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
         s_best[tid >> 5] = best;
       }
       __syncthreads();
-      if (tid == 0) {
-        int f = s_found[0];
-        unsigned long long bb = s_best[0];
-        for (int w = 1; w < kWarps; ++w) {
-          f = min(f, s_found[w]);
-          bb = s_best[w] < bb ? s_best[w] : bb;
+      if (tid < 32) {  // one warp combines the warps' results
+        int f = tid < kWarps ? s_found[tid] : 0x7fffffff;
+        unsigned long long bb = tid < kWarps ? s_best[tid] : ~0ull;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          f = min(f, __shfl_xor_sync(0xffffffffu, f, o));
+          const unsigned long long y = __shfl_xor_sync(0xffffffffu, bb, o);
+          bb = y < bb ? y : bb;
         }
-        s_app_slot = f != 0x7fffffff ? f : (int)(bb & 0xffffffffull);
+        if (tid == 0) s_app_slot = f != 0x7fffffff ? f : (int)(bb & 0xffffffffull);
       }
       __syncthreads();
       app_slot = s_app_slot;
     }
   }
   const uint32_t clock = st.clock + (app_slot >= 0 ? 1u : 0u);  // the resolve's clock
-  if (tid == 0)
+  __shared__ uint32_t s_dups, s_klo, s_khi;
+  if (tid == 0) {
     err_bits = app_err | (((uint64_t)clock + (uint64_t)k >= 0xFFFFFFFFull) ? (uint32_t)HS_DEVERR_CLOCK : 0u);
+    s_dups = 0u;
+    s_klo = 0xffffffffu;
+    s_khi = 0u;
+  }
   for (int x = tid; x < ht_size; x += kThreads) {
     ht_key[x] = -1;
     ht_val[x] = 0x7fffffff;
   }
   __syncthreads();
 
-  // (1) hash the selected positions; a key keeps the smallest top-k index that carries it
-  for (int i = tid; i < k; i += kThreads) {
-    const int32_t s = topk[i];
-    if (s == -1) continue;
-    if (s < 0 || (int64_t)s >= a.C) {
-      atomicOr(&err_bits, (uint32_t)HS_DEVERR_RANGE);
-      continue;
-    }
-    uint32_t h = ht_hash(s, a.ht_bits);
-    while (true) {
-      const int32_t prev = atomicCAS(&ht_key[h], -1, s);
-      if (prev == -1 || prev == s) {
-        atomicMin(&ht_val[h], i);
-        break;
-      }
-      h = (h + 1) & (uint32_t)(ht_size - 1);
-    }
-  }
-  __syncthreads();
+  // (1) hash the selected positions; a key keeps the smallest top-k index that carries it.  Entries
+  // start as misses (-1) or invalid (-2); repeats are sorted out below only when an insert met its key.
   for (int i = tid; i < k; i += kThreads) {
     const int32_t s = topk[i];
     int32_t state = -2;
     if (s >= 0 && (int64_t)s < a.C) {
       uint32_t h = ht_hash(s, a.ht_bits);
-      while (ht_key[h] != s) h = (h + 1) & (uint32_t)(ht_size - 1);
-      if (ht_val[h] == i) {
-        state = -1;
-      } else {
-        atomicOr(&err_bits, (uint32_t)HS_DEVERR_DUP);
+      while (true) {
+        const int32_t prev = atomicCAS(&ht_key[h], -1, s);
+        if (prev == -1 || prev == s) {
+          atomicMin(&ht_val[h], i);
+          if (prev == s) s_dups = 1u;
+          break;
+        }
+        h = (h + 1) & (uint32_t)(ht_size - 1);
       }
+      state = -1;
+    } else if (s != -1) {
+      atomicOr(&err_bits, (uint32_t)HS_DEVERR_RANGE);
     }
     hit_slot[i] = state;
   }
   __syncthreads();
+  if (s_dups != 0u) {  // a repeated position: only its first occurrence (smallest index) is valid
+    for (int i = tid; i < k; i += kThreads) {
+      if (hit_slot[i] != -1) continue;
+      const int32_t s = topk[i];
+      uint32_t h = ht_hash(s, a.ht_bits);
+      while (ht_key[h] != s) h = (h + 1) & (uint32_t)(ht_size - 1);
+      if (ht_val[h] != i) {
+        hit_slot[i] = -2;
+        atomicOr(&err_bits, (uint32_t)HS_DEVERR_DUP);
+      }
+    }
+    __syncthreads();
+  }
 
-  // (2) probe every slot; keep its eviction key
+  // (2) probe every slot; keep its eviction key and the candidates' key range
+  uint32_t klo = 0xffffffffu, khi = 0u;
   for (int j = tid; j < B; j += kThreads) {
     const bool is_app = j == app_slot;
     const int32_t t = is_app ? (int32_t)app_p : tag[j];
@@ -401,9 +390,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
       }
     }
     flag[j] = f;
-    key32[j] = hs_evict_key(a.policy, t, stj, a.seed, st.nres, a.R, r, a.L, a.layer, BK, j);
+    const uint32_t key = hs_evict_key(a.policy, t, stj, a.seed, st.nres, a.R, r, a.L, a.layer, BK, j);
+    key32[j] = key;
+    if (f == 0) {
+      klo = min(klo, key);
+      khi = max(khi, key);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    klo = min(klo, __shfl_xor_sync(0xffffffffu, klo, o));
+    khi = max(khi, __shfl_xor_sync(0xffffffffu, khi, o));
+  }
+  if ((tid & 31) == 0) {
+    atomicMin(&s_klo, klo);
+    atomicMax(&s_khi, khi);
   }
   __syncthreads();
+  // every old tag and stamp this CTA needs has been read and used: the cluster's writes may follow
+  if (a.cs > 1) cluster_arrive_relaxed();
 
   // (3a) rank hits and misses in top-k order; list the misses
   const int kpt = (k + kThreads - 1) / kThreads;
@@ -433,7 +438,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
   // (4, early) this CTA's first misses start crossing the host link now; the victims are chosen
   // meanwhile and the staged records reach their slots in phase B
   const int q0 = (int)((int64_t)m * crank / a.cs), q1 = (int)((int64_t)m * (crank + 1) / a.cs);
-  uint8_t* stage = smem + a.stage_off;
+  // 128-byte aligned (the launch adds the slack): a 16-byte copy from host memory keeps its offset
+  // within the 32-byte sector on both sides, else the copy engine splits every sector in two and
+  // the host link carries twice the bytes (measured: 32 instead of 16 sectors per 512-byte request)
+  uint8_t* stage = (uint8_t*)(((uintptr_t)(smem + a.stage_off) + 127u) & ~(uintptr_t)127u);
   const int nstage = a.pend == nullptr ? min(q1 - q0, a.stage_recs) : 0;
   if (nstage > 0) {
     __syncthreads();  // the miss list is complete
@@ -451,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
   const int ncand = B - h;
   const bool take_all = (m == ncand);
   uint32_t T = 0u, need_eq = 0u;
-  if (m > 0 && !take_all) select_threshold(key32, flag, B, (uint32_t)m, wbuf, hist, sel, &T, &need_eq);
+  if (m > 0 && !take_all) select_threshold(key32, flag, B, (uint32_t)m, s_klo, s_khi, wbuf, hist, sel, &T, &need_eq);
 
   // (3c) ordered compaction: the q-th victim in ascending slot order
   if (m > 0) {
@@ -492,11 +500,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
     }
   }
   // every CTA of the request has read the old tags and stamps before anyone writes them
-  if (a.cs > 1) {
-    cluster_sync_all();
-  } else {
-    __syncthreads();
-  }
+  __syncthreads();
+  if (a.cs > 1) cluster_wait();
 
   // ---------------- phase B: this CTA's share of the writes and of the fetch ----------------
   {
@@ -719,13 +724,13 @@ namespace {
 // back (measured on the GQA decode workload: 16 KB +4%, 32 KB +6%, 96 KB -1% per layer-step).
 constexpr size_t kStageBytes = 32 * 1024;
 size_t resolve_launch_smem(const hs_config* c, int* stage_off, int* stage_recs) {
-  const size_t base = (hs_resolve_smem_bytes(c) + 15) & ~(size_t)15;
+  const size_t base = (hs_resolve_smem_bytes(c) + 127) & ~(size_t)127;
   const size_t rec = (size_t)hs_record_bytes(c);
   size_t room = base < 200 * 1024 ? 200 * 1024 - base : 0;
   room = room < kStageBytes ? room : kStageBytes;
   *stage_off = (int)base;
   *stage_recs = c->fetch_in_attention ? 0 : (int)(room / rec);
-  return base + (size_t)*stage_recs * rec;
+  return base + (size_t)*stage_recs * rec + (*stage_recs > 0 ? 128 : 0);  // + alignment slack
 }
 
 template <int NV>
