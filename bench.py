@@ -288,40 +288,57 @@ def run_ours(args, w, world, rank, local):
     M = max(1, args.microbatches)
     groups = [(R * g // M, R * (g + 1) // M - R * g // M) for g in range(M)]
     streams = [torch.cuda.Stream() for _ in range(M)] if M > 1 else [stream]
-    gevs = [[[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(L)] for _ in range(M)]
+    gevs = [[[[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(L)] for _ in range(M)]
             for _ in range(K)] if M > 1 else None
 
     def step_mb(t, i=None):
-        # micro-batches: each group of requests runs its layers in order on its own stream
-        for g, (r0, n) in enumerate(groups):
-            st = streams[g]
-            with torch.cuda.stream(st):
-                for l in range(L):
+        # micro-batches: each group of requests runs its layers in order on its own stream.  The
+        # groups' resolves form one chain (group g's resolve of layer l after group g-1's), and so do
+        # their attentions, so one group's resolve runs while the group before it is in its attention
+        # and the attentions (which copy the misses when fetch_in_attention is set) follow one another
+        # on the host link instead of sharing it
+        last_res, last_att = None, None
+        for l in range(L):
+            for g, (r0, n) in enumerate(groups):
+                st = streams[g]
+                with torch.cuda.stream(st):
+                    if last_res is not None:
+                        st.wait_event(last_res)
                     if i is not None:
                         gevs[i][g][l][0].record(st)
                     pool.resolve_range(l, r0, wl.topk[t, l, r0:r0 + n], locs[l][r0:r0 + n],
                                        pos=wl.pos[t, r0:r0 + n], rec=wl.app[t, l, r0:r0 + n], stream=st)
+                    last_res = torch.cuda.Event()
+                    last_res.record(st)
                     if i is not None:
                         gevs[i][g][l][1].record(st)
-                    pool.sparse_attn_range(l, r0, wl.q[t, l, r0:r0 + n], locs[l][r0:r0 + n],
-                                           outs[l][r0:r0 + n], scale=scale, stream=st)
+                    if last_att is not None:
+                        st.wait_event(last_att)
                     if i is not None:
                         gevs[i][g][l][2].record(st)
+                    pool.sparse_attn_range(l, r0, wl.q[t, l, r0:r0 + n], locs[l][r0:r0 + n],
+                                           outs[l][r0:r0 + n], scale=scale, stream=st)
+                    last_att = torch.cuda.Event()
+                    last_att.record(st)
+                    if i is not None:
+                        gevs[i][g][l][3].record(st)
 
     def fork():
+        cur = torch.cuda.current_stream()
         ev = torch.cuda.Event()
-        ev.record(stream)
+        ev.record(cur)
         for st in streams:
             st.wait_event(ev)
 
     def join():
+        cur = torch.cuda.current_stream()
         for st in streams:
             ev = torch.cuda.Event()
             ev.record(st)
-            stream.wait_event(ev)
+            cur.wait_event(ev)
 
-    # the headline pass replays the K timed steps as one captured CUDA graph (single stream)
-    use_graph = not args.no_graph and G == 1 and M == 1
+    # the headline pass replays the K timed steps as one captured CUDA graph
+    use_graph = not args.no_graph and G == 1
 
     def warm_up():
         """Cold start, then the W untimed warm-up steps."""
@@ -349,8 +366,14 @@ def run_ours(args, w, world, rank, local):
             warm_up()
             graph = torch.cuda.CUDAGraph()
             with torch.cuda.graph(graph):
-                for i in range(K):
-                    step(W + i)
+                if M > 1:
+                    fork()
+                    for i in range(K):
+                        step_mb(W + i)
+                    join()
+                else:
+                    for i in range(K):
+                        step(W + i)
             graph.replay()
             torch.cuda.synchronize()
         warm_up()
@@ -390,7 +413,7 @@ def run_ours(args, w, world, rank, local):
     elapsed_ev, st_ev = run_steps(True)
     if M > 1:
         res_ms = np.array([[[e[g][l][0].elapsed_time(e[g][l][1]) for l in range(L)] for g in range(M)] for e in gevs])
-        att_ms = np.array([[[e[g][l][1].elapsed_time(e[g][l][2]) for l in range(L)] for g in range(M)] for e in gevs])
+        att_ms = np.array([[[e[g][l][2].elapsed_time(e[g][l][3]) for l in range(L)] for g in range(M)] for e in gevs])
         app_ms = np.zeros(1)
     elif G > 1:
         # resolves on their own streams, attentions on the main stream after their resolve
@@ -401,6 +424,8 @@ def run_ours(args, w, world, rank, local):
         app_ms = np.array([[e[l][0].elapsed_time(e[l][1]) for l in range(L)] for e in evs])
         res_ms = np.array([[e[l][1].elapsed_time(e[l][2]) for l in range(L)] for e in evs])
         att_ms = np.array([[e[l][2].elapsed_time(e[l][3]) for l in range(L)] for e in evs])
+    # pass 3: the attention alone, its L launches of the last step back to back
+    attn_b2b_us = time_attention_back_to_back(pool, wl, locs, outs, scale, W + K - 1) if M == 1 and G == 1 else None
     max_elapsed = reduce_max(elapsed, world)
     units = world * K * L
     value = units / max_elapsed
@@ -415,12 +440,16 @@ def run_ours(args, w, world, rank, local):
     floor_us = measure_launch_floor()
     peaks = load_peaks()
     attn_us = float(att_ms.mean() * 1e3)
-    achieved = attn_bytes_per_launch(w) / M / (attn_us * 1e-6) / 1e9  # a launch covers R / M requests
+    # the roofline takes the back-to-back launch time where there is one (the event pair around a
+    # single launch also holds the launch latency that the event between two kernels exposes)
+    roof_us = attn_b2b_us if attn_b2b_us is not None else attn_us
+    achieved = attn_bytes_per_launch(w) / M / (roof_us * 1e-6) / 1e9  # a launch covers R / M requests
+    achieved_ev = attn_bytes_per_launch(w) / M / (attn_us * 1e-6) / 1e9
     rec = record_bytes(w)
     miss_bytes = float(st["host_bytes"])
-    res_total_s = float(res_ms.sum() / 1e3) / M  # M groups resolve side by side
+    res_total_s = float(res_ms.sum() / 1e3)  # micro-batches' resolves (and attentions) run one after another
     link_kernel = "sparse_attn" if fetch == "attention" else "resolve"
-    link_s = float(att_ms.sum() / 1e3) / M if fetch == "attention" else res_total_s
+    link_s = float(att_ms.sum() / 1e3) if fetch == "attention" else res_total_s
     if G > 1:
         # the group's resolves overlap one another and the attentions: link rate over the wall time
         link_kernel, link_s = "resolve (overlapped; whole-step wall time)", max_elapsed
@@ -448,10 +477,14 @@ def run_ours(args, w, world, rank, local):
                      "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": args.traffic if args.traffic is not None else ATTN_TRAFFIC.get((args.workload, fetch)),
                      "peak_source": peaks["source"],
                      "bytes_per_launch": attn_bytes_per_launch(w) // M,
-                     # the same with the event floor of an empty kernel taken out of the launch time
-                     "launch_floor_us": floor_us,
-                     "frac_excl_launch_floor": (attn_bytes_per_launch(w) / M / ((attn_us - floor_us) * 1e-6) / 1e9)
-                     / peaks["hbm_gbs"] if attn_us > floor_us else None},
+                     "launch_us": roof_us,
+                     "timing": ("CUDA events around 3 replays of a captured graph of the last timed step's "
+                                f"{L} attention launches back to back (inputs of each launch larger than L2)")
+                     if attn_b2b_us is not None else "CUDA events around each launch",
+                     # the same from the event pairs around each launch of the breakdown pass
+                     "per_launch_events_us": attn_us,
+                     "frac_per_launch_events": achieved_ev / peaks["hbm_gbs"],
+                     "launch_floor_us": floor_us},
         # the kernel that moves the misses over the host link: the resolve, or the attention when the
         # copies were left to it
         "host_link": {"kernel": link_kernel, "miss_bytes_per_layer": miss_bytes / (K * L),
@@ -565,6 +598,35 @@ def run_e2e(pool, wl, W, K, world, locs, outs, scale, use_graph=False):
     d2h_bytes = L * R * w["Hq"] * w["Dv"] * 4
     return {"value": world * K * L / el, "unit": "layer-steps/s", "h2d_bytes_per_step": int(h2d_bytes),
             "d2h_bytes_per_step": int(d2h_bytes), "ms_per_step": el / K * 1e3}
+
+
+def time_attention_back_to_back(pool, wl, locs, outs, scale, t, reps=3):
+    """Mean device time of one attention launch: the L layers' launches of step t, captured as one
+    graph (programmatic dependent launch between them, no events in between), replayed once untimed,
+    then `reps` times between two CUDA events.  Every launch gathers its own layer's hot buffers, more
+    than L2 holds, so no launch finds its rows cached by the one before."""
+    import torch
+
+    L = wl.w["L"]
+
+    def launches():
+        for l in range(L):
+            pool.sparse_attn(l, wl.q[t, l], locs[l], outs[l], scale=scale)
+
+    launches()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        launches()
+    graph.replay()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(reps):
+        graph.replay()
+    e.record()
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) * 1e3 / (reps * L)
 
 
 def measure_h2d(device):
@@ -707,12 +769,13 @@ def main():
     if args.fetch == "auto" and w["layout"] == 1 and not args.no_alt:
         # the same steps with the miss copies moved into the attention kernel (overlapping the host
         # link with the HBM gather): reported beside the headline, which keeps the copies in the resolve
+        # in two micro-batches, so one half's resolve runs while the other half's attention copies
         alt_args = argparse.Namespace(**vars(args))
-        alt_args.fetch, alt_args.no_e2e = "attention", True
+        alt_args.fetch, alt_args.no_e2e, alt_args.microbatches = "attention", True, 2
         alt = run_ours(alt_args, w, world, rank, local)
         out["fetch_in_attention"] = {k: alt[k] for k in ("value", "unit", "ms_per_step", "us_per_layer", "miss_rate",
                                                          "host_link", "clocks", "errors")}
-        out["fetch_in_attention"]["hbm_gbs_attention"] = alt["roofline"]["achieved"]
+        out["fetch_in_attention"]["microbatches"] = 2
     if args.fetch == "auto" and w["layout"] == 1 and not args.no_alt and args.index_share == 1 and w["L"] >= 4:
         # a different workload: layer groups of 4 share one selection (as with a shared indexer), so a
         # group's resolves and host fetches start together and overlap the attentions (exact

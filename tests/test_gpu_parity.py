@@ -216,6 +216,73 @@ def test_layer_group_schedule_on_side_streams(fetch):
     grp.close()
 
 
+@pytest.mark.parametrize("fetch", [0, 1])
+def test_chained_microbatches_in_one_graph(fetch):
+    """The bench's two-micro-batch schedule: each half on its own stream, the halves' resolves in one
+    chain and their attentions in another, every step captured in one CUDA graph.  Slots, outputs,
+    state and counters are bit-identical to full-batch calls on a second pool."""
+    R, L, steps = 4, 3, 6
+    cfg = _gqa(R, L, 3000 + steps, 256, 512, fetch=fetch)
+    sc = Scenario(cfg, ctx0=3000, steps=steps, appends=True, seed=67)
+    full, split = HsPool(cfg), HsPool(cfg)
+    prefill(full, sc)
+    prefill(split, sc)
+    refs = [gpu_step(full, sc, t, fused=True) for t in range(steps)]
+    dev = "cuda"
+    topk = torch.from_numpy(sc.trace).to(dev)                                     # [S][L][R][k]
+    q = bf16_tensor(sc.q, dev)                                                     # [S][L][R][Hq][D]
+    rec = bf16_tensor(np.stack([np.stack([np.stack([sc.hist[(r, l)][sc.ctx0 + t] for r in range(R)])
+                                          for l in range(L)]) for t in range(steps)]), dev)
+    pos = (torch.arange(steps, dtype=torch.int64, device=dev) + sc.ctx0).view(steps, 1).expand(steps, R).contiguous()
+    locs = torch.empty((steps, L, R, cfg.top_k), dtype=torch.int32, device=dev)
+    outs = torch.empty((steps, L, R, cfg.num_q_heads, cfg.head_dim_v), dtype=torch.float32, device=dev)
+    groups = [(0, 2), (2, 2)]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        cur = torch.cuda.current_stream()
+        ev = torch.cuda.Event()
+        ev.record(cur)
+        for st in streams:
+            st.wait_event(ev)
+        last_res = last_att = None
+        for t in range(steps):
+            for l in range(L):
+                for (r0, n), st in zip(groups, streams):
+                    with torch.cuda.stream(st):
+                        if last_res is not None:
+                            st.wait_event(last_res)
+                        split.resolve_range(l, r0, topk[t, l, r0:r0 + n], locs[t, l, r0:r0 + n],
+                                            pos=pos[t, r0:r0 + n], rec=rec[t, l, r0:r0 + n], stream=st)
+                        last_res = torch.cuda.Event()
+                        last_res.record(st)
+                        if last_att is not None:
+                            st.wait_event(last_att)
+                        split.sparse_attn_range(l, r0, q[t, l, r0:r0 + n], locs[t, l, r0:r0 + n],
+                                                outs[t, l, r0:r0 + n], scale=sc.scale, stream=st)
+                        last_att = torch.cuda.Event()
+                        last_att.record(st)
+        for st in streams:
+            ev = torch.cuda.Event()
+            ev.record(st)
+            cur.wait_event(ev)
+    graph.replay()
+    torch.cuda.synchronize()
+    for t in range(steps):
+        for l in range(L):
+            assert np.array_equal(locs[t, l].cpu().numpy(), refs[t][l][0]), (t, l)
+            assert np.array_equal(outs[t, l].cpu().numpy(), refs[t][l][1]), (t, l)
+    for l in range(L):
+        a, b = full.read_state(l), split.read_state(l)
+        assert all(np.array_equal(x, y) for x, y in zip(a, b))
+    sf, ss = full.stats(), split.stats()
+    assert np.array_equal(sf["per_rl"], ss["per_rl"])
+    assert ss["error_bits"] == 0
+    full.close()
+    split.close()
+
+
 def test_range_arguments_checked():
     cfg = _gqa(2, 1, 100, 4, 8, kvh=1)
     pool = HsPool(cfg)
