@@ -637,15 +637,6 @@ __global__ void __launch_bounds__((kGqaWarps + kGqaProducers) * 32, 1) k_attn_gq
     const int ni = w < nst ? (nst - w + NW - 1) / NW : 0;
     const int64_t goff = (int64_t)g * a.kstride;  // KV head g's slice of a row
     const int rows_r = (int)rows_of(a, r);
-    {  // the page row, filled by the producers for the producers
-      const int pt = (int)threadIdx.x - NW * 32;
-      if (a.kv_pt != nullptr) {
-        if (pt < a.kv_pages) s_pg[pt] = a.kv_pt[(int64_t)r * a.kv_pages + pt];
-      } else if (pt == 0) {
-        s_pg[0] = (uint64_t)(uintptr_t)(a.kv + (int64_t)r * a.rows * rec);
-      }
-      asm volatile("bar.sync 2, %0;" ::"n"(kGqaProducers * 32) : "memory");
-    }
     bool ok = true;
     int issued = 0;
     // the slot (and, FETCH, the host address of a pending record, 0 if none) of token `lane` of
@@ -686,15 +677,27 @@ __global__ void __launch_bounds__((kGqaWarps + kGqaProducers) * 32, 1) k_attn_gq
         }
       }
     };
-    int32_t raw_l0, raw_l1;
-    uint64_t raw_q0, raw_q1;
+    // the first three stages' slots are requested before the page row, so the loads overlap
+    int32_t raw_l0, raw_l1, raw_l2;
+    uint64_t raw_q0, raw_q1, raw_q2;
     load_raw(0, raw_l0, raw_q0);
     load_raw(1, raw_l1, raw_q1);
+    load_raw(2, raw_l2, raw_q2);
+    {  // the page row, filled by the producers for the producers
+      const int pt = (int)threadIdx.x - NW * 32;
+      if (a.kv_pt != nullptr) {
+        if (pt < a.kv_pages) s_pg[pt] = a.kv_pt[(int64_t)r * a.kv_pages + pt];
+      } else if (pt == 0) {
+        s_pg[0] = (uint64_t)(uintptr_t)(a.kv + (int64_t)r * a.rows * rec);
+      }
+      asm volatile("bar.sync 2, %0;" ::"n"(kGqaProducers * 32) : "memory");
+    }
     int32_t loc;
     uint64_t pp;
     uint32_t vmask, pmask;
     stage_info(raw_l0, raw_q0, loc, pp, vmask, pmask);
-    load_raw(2, raw_l0, raw_q0);
+    raw_l0 = raw_l2;
+    raw_q0 = raw_q2;
     if (FETCH) request(pmask, pp, vc);
     for (int i = 0; i < ni; ++i) {
       const int b = i % NS;
