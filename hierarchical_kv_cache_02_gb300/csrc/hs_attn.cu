@@ -1074,6 +1074,14 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map
       "l"((uint64_t)map), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(smem_u32(bar))
       : "memory");
 }
+// TMA load of one box of a 2-D tensor map at element coordinates (x, y) into shared memory at dst
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"((uint64_t)map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
 __device__ __forceinline__ uint32_t umma_idesc_bf16(int M, int N, int a_mn, int b_mn) {
   // fp32 accumulator, bf16 A and B, operand majors, N / 8, M / 16
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
@@ -1134,7 +1142,8 @@ __device__ __forceinline__ float reduce32_max_transposed(float (&v)[32], int lan
 }
 
 template <bool TMA>
-__global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_umma(AttnArgs a, const __grid_constant__ CUtensorMap tmap) {
+__global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_umma(AttnArgs a, const __grid_constant__ CUtensorMap tmap,
+                                                                  const __grid_constant__ CUtensorMap qmap) {
   hs_pdl_enter();
   extern __shared__ __align__(128) uint8_t smem_raw[];
   // the tile starts 1024-byte aligned (the period of the 128-byte swizzle); the launch adds 1 KB
@@ -1156,7 +1165,7 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_umma(AttnArgs a, cons
   const int ntile = (n + kUTok - 1) / kUTok;
   if (tid == 0) {
     mbar_init(&bar_kv, TMA ? 1u : kUProd * 32);  // TMA: one expect-tx arrival; else one per producer lane
-    mbar_init(&bar_q, kUProd * 32);
+    mbar_init(&bar_q, TMA ? 1u : kUProd * 32);
     mbar_init(&bar_s, 1u);            // MMA commits
     mbar_init(&bar_pv, 1u);
     mbar_init(&bar_fin, 1u);
@@ -1248,19 +1257,30 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_umma(AttnArgs a, cons
         }
         cp_async_arrive_noinc(&bar_kv);
       }
-      // Q: 64 heads x 72 chunks of 16 bytes, 8-head groups 9216 B apart
-      for (int e = pl; e < kUHeads * 72; e += kUProd * 32) {
-        const int ng = e / 576, rem = e % 576, c = rem / 8, hn = ng * 8 + rem % 8;
-        cp_async16_zfill(sq_u + (uint32_t)(ng * kUSboKv + c * 128 + (rem % 8) * 16), qr + (int64_t)hn * kUDim + c * 8,
-                         16u);
+      if (TMA) {
+        // Q: 9 boxes of 64 dims x 64 heads from the launch's Q tensor map, 128-byte swizzled like the
+        // tile (blocks 8 KB apart, heads 128 B apart)
+        if (pl == 0) {
+          mbar_arrive_expect_tx(&bar_q, (uint32_t)kUQ);
+          for (int kb = 0; kb < 9; ++kb)
+            tma_load_2d(sq_u + (uint32_t)(kb * 8192), &qmap, kb * 64, (r - a.r0) * kUHeads, &bar_q);
+        }
+      } else {
+        // Q: 64 heads x 72 chunks of 16 bytes, 8-head groups 9216 B apart
+        for (int e = pl; e < kUHeads * 72; e += kUProd * 32) {
+          const int ng = e / 576, rem = e % 576, c = rem / 8, hn = ng * 8 + rem % 8;
+          cp_async16_zfill(sq_u + (uint32_t)(ng * kUSboKv + c * 128 + (rem % 8) * 16),
+                           qr + (int64_t)hn * kUDim + c * 8, 16u);
+        }
+        cp_async_arrive_noinc(&bar_q);
       }
-      cp_async_arrive_noinc(&bar_q);
     }
     if (bad) atomicOr(a.err, (uint32_t)HS_DEVERR_LOC);
     if (TMA && !ok && gathered > 0 && pl == 0) {
-      // a wait gave up: the last gather still lands in this CTA's shared memory before it may exit
+      // a wait gave up: the last gather and Q still land in this CTA's shared memory before it may exit
       volatile uint32_t never = 0u;
       mbar_wait_bounded(&bar_kv, (uint32_t)((gathered - 1) & 1), &never);
+      mbar_wait_bounded(&bar_q, (uint32_t)((gathered - 1) & 1), &never);
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
     if (!ok && lane == 0) {
@@ -1283,7 +1303,8 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_umma(AttnArgs a, cons
           // tile K-major: swizzled, a k-step is 32 B inside a 128-byte row of a 64-dim block; else core matrices
           const uint64_t da = TMA ? umma_sdesc(skv_u + (uint32_t)((s2 >> 2) * 16384 + (s2 & 3) * 32), 16, 1024, 2)
                                   : umma_sdesc(skv_u + (uint32_t)(2 * s2 * 128), 128, kUSboKv);
-          const uint64_t db = umma_sdesc(sq_u + (uint32_t)(2 * s2 * 128), 128, kUSboKv);
+          const uint64_t db = TMA ? umma_sdesc(sq_u + (uint32_t)((s2 >> 2) * 8192 + (s2 & 3) * 32), 16, 1024, 2)
+                                  : umma_sdesc(sq_u + (uint32_t)(2 * s2 * 128), 128, kUSboKv);
           umma_bf16(tb, da, db, id_s, s2 != 0 ? 1u : 0u);
         }
         umma_commit(&bar_s);
@@ -1527,6 +1548,39 @@ cudaError_t launch_kernel(K kern, const AttnArgs* a, const Plan& pl, int threads
 
 
 
+typedef CUresult (*EncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                             const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                             CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The driver's tensor-map encoder, looked up once through the runtime; null if unavailable.
+EncodeFn tensor_map_encoder() {
+  static const EncodeFn fn = []() -> EncodeFn {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        f == nullptr || q != cudaDriverEntryPointSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    return (EncodeFn)f;
+  }();
+  return fn;
+}
+
+// Q of the launch's requests as a 2-D tensor (rows = request x head, 576 bf16 each) in boxes of 64
+// dims x 64 heads, 128-byte swizzled: the tensor-core kernel's Q operand layout.  False (and Q by
+// cp.async) when the encoder is missing or refuses the address.
+bool encode_q_map(CUtensorMap* m, const void* q, int nreq) {
+  const EncodeFn fn = tensor_map_encoder();
+  if (fn == nullptr || q == nullptr || ((uintptr_t)q & 15u) != 0) return false;
+  const cuuint64_t gdim[2] = {(cuuint64_t)kUDim, (cuuint64_t)nreq * kUHeads};
+  const cuuint64_t gstride[1] = {(cuuint64_t)kUDim * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)kUHeads}, estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q), gdim, gstride, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t dispatch(const hs_config& c, const AttnArgs* a, const Plan& pl, cudaStream_t st) {
   if (pl.kind == 4) {
     cudaError_t e = cudaSuccess;
@@ -1538,10 +1592,13 @@ cudaError_t dispatch(const hs_config& c, const AttnArgs* a, const Plan& pl, cuda
                                    (int)cudaSharedmemCarveoutMaxShared);
       }
     } else {
-      // hot-buffer rows through the pool's tensor map (TMA gather); caller rows by cp.async
-      CUtensorMap tm;
+      // hot-buffer rows through the pool's tensor map (TMA gather) and Q through its own map; caller
+      // rows (or a Q the encoder refuses) by cp.async
+      CUtensorMap tm, qm;
       memset(&tm, 0, sizeof(tm));
-      if (a->kv_tmap != nullptr) tm = *a->kv_tmap;
+      memset(&qm, 0, sizeof(qm));
+      const bool tma = a->kv_tmap != nullptr && encode_q_map(&qm, a->q, a->R);
+      if (tma) tm = *a->kv_tmap;
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(pl.S, a->R, pl.groups);
       cfg.blockDim = dim3(kUThreads, 1, 1);
@@ -1552,8 +1609,8 @@ cudaError_t dispatch(const hs_config& c, const AttnArgs* a, const Plan& pl, cuda
       attr[0].val.programmaticStreamSerializationAllowed = 1;
       cfg.attrs = attr;
       cfg.numAttrs = 1;
-      e = a->kv_tmap != nullptr ? cudaLaunchKernelEx(&cfg, k_attn_mla_umma<true>, *a, tm)
-                                : cudaLaunchKernelEx(&cfg, k_attn_mla_umma<false>, *a, tm);
+      e = tma ? cudaLaunchKernelEx(&cfg, k_attn_mla_umma<true>, *a, tm, qm)
+              : cudaLaunchKernelEx(&cfg, k_attn_mla_umma<false>, *a, tm, qm);
     }
     if (e == cudaSuccess && a == nullptr)
       e = cudaFuncSetAttribute(k_combine_wide, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -1667,21 +1724,13 @@ int hs_launch_attn(hs_pool* p, int layer, int r0, int nreq, const void* d_q, con
 void* hs_attn_make_pool_map(const hs_config* c, int num_sms, void* pool_base, int64_t pool_rows) {
   Plan pl;
   if (!plan_for(c, num_sms, &pl) || pl.kind != 4 || pool_base == nullptr || pool_rows < 1) return nullptr;
-  typedef CUresult (*EncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                               const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                               CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-  void* fn = nullptr;
-  cudaDriverEntryPointQueryResult q;
-  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
-      fn == nullptr || q != cudaDriverEntryPointSuccess) {
-    cudaGetLastError();
-    return nullptr;
-  }
+  const EncodeFn fn = tensor_map_encoder();
+  if (fn == nullptr) return nullptr;
   CUtensorMap* tm = new (std::align_val_t(64)) CUtensorMap;
   const cuuint64_t gdim[2] = {(cuuint64_t)kUDim, (cuuint64_t)pool_rows};
   const cuuint64_t gstride[1] = {(cuuint64_t)kUDim * 2};
   const cuuint32_t box[2] = {64, 1}, estr[2] = {1, 1};
-  if (((EncodeFn)fn)(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pool_base, gdim, gstride, box, estr,
+  if (fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pool_base, gdim, gstride, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
     ::operator delete(tm, std::align_val_t(64));
