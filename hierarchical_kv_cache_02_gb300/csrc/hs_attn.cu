@@ -1801,6 +1801,7 @@ extern "C" int hs_sparse_attn_noalloc(const hs_config* cfg, const void* d_q, con
                                       const void* d_kv, int64_t kv_rows, float scale, float* d_out, void* stream) {
   if (cfg == nullptr || d_q == nullptr || d_locs == nullptr || d_kv == nullptr || d_out == nullptr) return HS_ERR_ARG;
   if (kv_rows < 1 || kv_rows > (int64_t)INT32_MAX || ((uintptr_t)d_kv & 15u) != 0) return HS_ERR_ARG;
+  if (!hs_aligned(d_q, 16) || !hs_aligned(d_out, 16) || !hs_aligned(d_locs, 4)) return HS_ERR_ARG;
   if (cfg->num_requests < 1 || cfg->top_k < 1 || cfg->num_q_heads < 1 || cfg->num_kv_heads < 1 ||
       cfg->num_q_heads % cfg->num_kv_heads != 0)
     return HS_ERR_CONFIG;

@@ -136,6 +136,10 @@ __device__ __forceinline__ void hs_copy_pending(const hs_pending* pend, int k, i
   }
 }
 
+// Alignment the kernels' vector accesses need: 16 bytes for queries, outputs and appended records
+// (16-byte loads and stores), 8 for positions, 4 for top-k lists and slot lists.
+inline bool hs_aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1u)) == 0; }
+
 // Programmatic dependent launch: the hot-path kernels are launched so that the next kernel of the
 // stream may start its launch while this one drains.  Every kernel waits for its predecessor's
 // completion (and memory) before touching global memory, then lets its own successor launch.

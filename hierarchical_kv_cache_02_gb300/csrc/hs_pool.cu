@@ -583,6 +583,7 @@ extern "C" int hs_host_usage(hs_pool* pool, int64_t* pages_in_use, int64_t* page
 extern "C" int hs_append_writethrough(hs_pool* pool, int layer, const int64_t* d_pos, const void* d_rec,
                                       void* stream) {
   if (pool == nullptr || d_pos == nullptr || d_rec == nullptr) return HS_ERR_ARG;
+  if (!hs_aligned(d_pos, 8) || !hs_aligned(d_rec, 16)) return HS_ERR_ARG;
   if (layer < 0 || layer >= pool->cfg.num_layers) return HS_ERR_ARG;
   DeviceGuard guard(pool->device);
   return hs_launch_append(pool, layer, d_pos, d_rec, (cudaStream_t)stream);
@@ -590,6 +591,7 @@ extern "C" int hs_append_writethrough(hs_pool* pool, int layer, const int64_t* d
 
 extern "C" int hs_resolve(hs_pool* pool, int layer, const int32_t* d_topk, int32_t* d_locs, void* stream) {
   if (pool == nullptr || d_topk == nullptr || d_locs == nullptr) return HS_ERR_ARG;
+  if (!hs_aligned(d_topk, 4) || !hs_aligned(d_locs, 4)) return HS_ERR_ARG;
   if (layer < 0 || layer >= pool->cfg.num_layers) return HS_ERR_ARG;
   DeviceGuard guard(pool->device);
   return hs_launch_resolve(pool, layer, 0, pool->cfg.num_requests, nullptr, nullptr, d_topk, d_locs,
@@ -599,6 +601,8 @@ extern "C" int hs_resolve(hs_pool* pool, int layer, const int32_t* d_topk, int32
 extern "C" int hs_append_resolve(hs_pool* pool, int layer, const int64_t* d_pos, const void* d_rec,
                                  const int32_t* d_topk, int32_t* d_locs, void* stream) {
   if (pool == nullptr || d_pos == nullptr || d_rec == nullptr || d_topk == nullptr || d_locs == nullptr)
+    return HS_ERR_ARG;
+  if (!hs_aligned(d_pos, 8) || !hs_aligned(d_rec, 16) || !hs_aligned(d_topk, 4) || !hs_aligned(d_locs, 4))
     return HS_ERR_ARG;
   if (layer < 0 || layer >= pool->cfg.num_layers) return HS_ERR_ARG;
   DeviceGuard guard(pool->device);
@@ -610,6 +614,8 @@ extern "C" int hs_resolve_range(hs_pool* pool, int layer, int r0, int nreq, cons
                                 const int32_t* d_topk, int32_t* d_locs, void* stream) {
   if (pool == nullptr || d_topk == nullptr || d_locs == nullptr) return HS_ERR_ARG;
   if ((d_pos == nullptr) != (d_rec == nullptr)) return HS_ERR_ARG;
+  if (!hs_aligned(d_pos, 8) || !hs_aligned(d_rec, 16) || !hs_aligned(d_topk, 4) || !hs_aligned(d_locs, 4))
+    return HS_ERR_ARG;
   if (layer < 0 || layer >= pool->cfg.num_layers) return HS_ERR_ARG;
   if (r0 < 0 || nreq < 1 || r0 + nreq > pool->cfg.num_requests) return HS_ERR_ARG;
   DeviceGuard guard(pool->device);
@@ -619,6 +625,7 @@ extern "C" int hs_resolve_range(hs_pool* pool, int layer, int r0, int nreq, cons
 extern "C" int hs_sparse_attn(hs_pool* pool, int layer, const void* d_q, const int32_t* d_locs,
                               const void* kv_base, int64_t kv_rows, float scale, float* d_out, void* stream) {
   if (pool == nullptr || d_q == nullptr || d_locs == nullptr || d_out == nullptr) return HS_ERR_ARG;
+  if (!hs_aligned(d_q, 16) || !hs_aligned(d_out, 16) || !hs_aligned(d_locs, 4)) return HS_ERR_ARG;
   if (layer < 0 || layer >= pool->cfg.num_layers) return HS_ERR_ARG;
   if (kv_base != nullptr && (kv_rows < 1 || kv_rows > (int64_t)INT32_MAX)) return HS_ERR_ARG;
   DeviceGuard guard(pool->device);
@@ -629,6 +636,7 @@ extern "C" int hs_sparse_attn(hs_pool* pool, int layer, const void* d_q, const i
 extern "C" int hs_sparse_attn_range(hs_pool* pool, int layer, int r0, int nreq, const void* d_q, const int32_t* d_locs,
                                     float scale, float* d_out, void* stream) {
   if (pool == nullptr || d_q == nullptr || d_locs == nullptr || d_out == nullptr) return HS_ERR_ARG;
+  if (!hs_aligned(d_q, 16) || !hs_aligned(d_out, 16) || !hs_aligned(d_locs, 4)) return HS_ERR_ARG;
   if (layer < 0 || layer >= pool->cfg.num_layers) return HS_ERR_ARG;
   if (r0 < 0 || nreq < 1 || r0 + nreq > pool->cfg.num_requests) return HS_ERR_ARG;
   DeviceGuard guard(pool->device);

@@ -16,6 +16,9 @@
  *   - Pointers named d_* are device pointers (or device-visible managed memory)
  *     owned by the caller; the library never frees them.  Host pointers are
  *     named h_* or src/dst with the rule stated at the call.
+ *   - Alignment of device arguments (the kernels move them with vector loads and
+ *     stores): d_q, d_out, d_rec and d_kv 16 bytes, d_pos 8 bytes, d_topk and
+ *     d_locs 4 bytes.  A misaligned pointer returns HS_ERR_ARG.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *   - Calls marked CAPTURABLE only enqueue kernels on `stream`: no allocation,
  *     no host synchronisation, no read of device data by the host.  They may be

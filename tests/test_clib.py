@@ -69,3 +69,17 @@ def test_null_arguments(lib):
     assert lib.hs_resolve(None, 0, None, None, None) == _lib.HS_ERR_ARG
     assert lib.hs_sparse_attn(None, 0, None, None, None, 0, ctypes.c_float(1.0), None, None) == _lib.HS_ERR_ARG
     assert lib.hs_pool_destroy(None) == _lib.HS_OK
+
+
+@pytest.mark.parametrize("which", ["q", "out", "locs"])
+def test_misaligned_attention_arguments_rejected_on_host(lib, which):
+    """The attention kernels move queries and outputs in 16-byte vectors and slot lists in 4-byte
+    words: a misaligned pointer is refused before anything touches the device (the addresses here
+    are never dereferenced)."""
+    cfg = HsConfig(num_requests=1, num_layers=1, capacity=64, top_k=8, buffer_slots=16).to_c()
+    ptrs = {"q": 0x10000, "locs": 0x20000, "kv": 0x30000, "out": 0x40000}
+    ptrs[which] += 8 if which != "locs" else 2
+    rc = lib.hs_sparse_attn_noalloc(ctypes.byref(cfg), ctypes.c_void_p(ptrs["q"]), ctypes.c_void_p(ptrs["locs"]),
+                                    ctypes.c_void_p(ptrs["kv"]), ctypes.c_int64(16), ctypes.c_float(1.0),
+                                    ctypes.c_void_p(ptrs["out"]), None)
+    assert rc == _lib.HS_ERR_ARG
