@@ -277,6 +277,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
   uint32_t app_err = 0u;
   uint4* app_dh = nullptr;  // the append's place in the host history
   if (a.app_pos != nullptr) {
+    // the tags and stamps of this thread's first slots are requested before the append position and
+    // its host page, so those dependent loads overlap them
+    constexpr int kAppBatch = 4;
+    int32_t tb[kAppBatch];
+    uint32_t sb[kAppBatch];
+#pragma unroll
+    for (int u = 0; u < kAppBatch; ++u) {
+      const int j = tid + u * kThreads;
+      tb[u] = j < B ? tag[j] : -1;
+      sb[u] = j < B ? stamp[j] : 0u;
+    }
     app_p = a.app_pos[r - a.r0];
     if (app_p >= a.P0 && app_p >= 0 && app_p < a.C)
       app_dh = (uint4*)hs_page_addr(a.pt, a.max_pages, a.page_shift, a.rec, a.L, r, a.layer, app_p);
@@ -285,13 +296,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
     } else {
       int found = 0x7fffffff;
       unsigned long long best = ~0ull;
-      for (int j = tid; j < B; j += kThreads) {
-        const int32_t t = tag[j];
+      auto visit = [&](int j, int32_t t, uint32_t sj) {
         if (t == (int32_t)app_p) found = min(found, j);
-        const uint32_t key = hs_evict_key(a.policy, t, stamp[j], a.seed, st.nres, a.R, r, a.L, a.layer, BK, j);
+        const uint32_t key = hs_evict_key(a.policy, t, sj, a.seed, st.nres, a.R, r, a.L, a.layer, BK, j);
         const unsigned long long kj = ((unsigned long long)key << 32) | (unsigned)j;
         best = kj < best ? kj : best;
+      };
+#pragma unroll
+      for (int u = 0; u < kAppBatch; ++u) {
+        const int j = tid + u * kThreads;
+        if (j < B) visit(j, tb[u], sb[u]);
       }
+      for (int j = tid + kAppBatch * kThreads; j < B; j += kThreads) visit(j, tag[j], stamp[j]);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         found = min(found, __shfl_xor_sync(0xffffffffu, found, o));
@@ -369,12 +385,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
     __syncthreads();
   }
 
-  // (2) probe every slot; keep its eviction key and the candidates' key range
+  // (2) probe every slot; keep its eviction key and the candidates' key range.  The tags and stamps
+  // of a thread's first kProbeBatch slots are loaded together before any is probed, so their load
+  // latencies overlap instead of following one another through the probe loop.
   uint32_t klo = 0xffffffffu, khi = 0u;
-  for (int j = tid; j < B; j += kThreads) {
+  auto probe_slot = [&](int j, int32_t tj, uint32_t sj) {
     const bool is_app = j == app_slot;
-    const int32_t t = is_app ? (int32_t)app_p : tag[j];
-    const uint32_t stj = is_app ? st.clock : stamp[j];
+    const int32_t t = is_app ? (int32_t)app_p : tj;
+    const uint32_t stj = is_app ? st.clock : sj;
     uint8_t f = 0;
     if (t >= 0) {
       uint32_t h = ht_hash(t, a.ht_bits);
@@ -396,6 +414,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
       klo = min(klo, key);
       khi = max(khi, key);
     }
+  };
+  {
+    constexpr int kProbeBatch = 4;
+    int32_t tb[kProbeBatch];
+    uint32_t sb[kProbeBatch];
+#pragma unroll
+    for (int u = 0; u < kProbeBatch; ++u) {
+      const int j = tid + u * kThreads;
+      tb[u] = j < B ? tag[j] : -1;
+      sb[u] = j < B ? stamp[j] : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < kProbeBatch; ++u) {
+      const int j = tid + u * kThreads;
+      if (j < B) probe_slot(j, tb[u], sb[u]);
+    }
+    for (int j = tid + kProbeBatch * kThreads; j < B; j += kThreads) probe_slot(j, tag[j], stamp[j]);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
