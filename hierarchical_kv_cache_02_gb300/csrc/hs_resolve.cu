@@ -737,27 +737,34 @@ __global__ void __launch_bounds__(kAppendThreads) k_append(AppendArgs a) {
   }
 }
 
-int ht_bits_for(int k) {
+// Early miss copies: 32 KB per CTA is what the host link moves in the ~10 us the victims take to
+// choose, with 64 CTAs fetching; a larger area issues more copies than the link drains and holds the
+// decision back (measured on the GQA decode workload: 16 KB +4%, 32 KB +6%, 96 KB -1% per layer-step).
+constexpr size_t kStageBytes = 32 * 1024;
+
+// Shared memory of the decision's arrays with a hash table of 2^bits entries.
+size_t decision_smem(const hs_config* c, int bits) {
+  return ((size_t)1 << bits) * 8 + (size_t)c->top_k * 24 + (size_t)c->buffer_slots * 5;
+}
+
+// Hash table of the selected positions: at most a quarter full where that leaves room for the early
+// miss copies, else at most half full.  Every probe of a slot whose tag is not selected runs to an
+// empty entry, and a warp waits for its longest chain: on the batch-8 shared-latent workload a half
+// full table made the probe pass 2.6 us of a ~21 us decision.
+int ht_bits_for(const hs_config* c) {
   int bits = 1;
-  while ((1 << bits) < 2 * k) ++bits;
-  return bits;
+  while ((1 << bits) < 2 * c->top_k) ++bits;
+  return decision_smem(c, bits + 1) + kStageBytes <= 200 * 1024 ? bits + 1 : bits;
 }
 
 }  // namespace
 
-size_t hs_resolve_smem_bytes(const hs_config* c) {
-  const size_t ht = (size_t)1 << ht_bits_for(c->top_k);
-  return ht * 8 + (size_t)c->top_k * 24 + (size_t)c->buffer_slots * 5;
-}
+size_t hs_resolve_smem_bytes(const hs_config* c) { return decision_smem(c, ht_bits_for(c)); }
 
 namespace {
 
 // Dynamic shared memory of a resolve launch: the decision's arrays, then (misses copied by the
 // resolve) a staging area for the early miss copies, up to kStageBytes within 200 KB in all.
-// 32 KB per CTA is what the host link moves in the ~10 us the victims take to choose, with 64
-// CTAs fetching; a larger area issues more copies than the link drains and holds the decision
-// back (measured on the GQA decode workload: 16 KB +4%, 32 KB +6%, 96 KB -1% per layer-step).
-constexpr size_t kStageBytes = 32 * 1024;
 size_t resolve_launch_smem(const hs_config* c, int* stage_off, int* stage_recs) {
   const size_t base = (hs_resolve_smem_bytes(c) + 127) & ~(size_t)127;
   const size_t rec = (size_t)hs_record_bytes(c);
@@ -859,7 +866,7 @@ int hs_launch_resolve(hs_pool* p, int layer, int r0, int nreq, const int64_t* d_
   a.k = c.top_k;
   a.policy = c.policy;
   a.log_steps = c.log_steps;
-  a.ht_bits = ht_bits_for(c.top_k);
+  a.ht_bits = ht_bits_for(&c);
   a.cs = p->resolve_cs;
   a.pend = p->pend != nullptr ? p->pend + (int64_t)layer * R * c.top_k : nullptr;
   a.pend_live = p->pend_live != nullptr ? p->pend_live + (int64_t)layer * R : nullptr;
