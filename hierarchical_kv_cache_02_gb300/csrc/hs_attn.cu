@@ -1492,7 +1492,7 @@ bool plan_for(const hs_config* c, int num_sms, Plan* pl) {
     pl->smem = (size_t)kGqaWarps * kGqaStages * kMmaTile * kGqaRow;
     per_cta_wave = 1;  // one CTA per SM: the staging buffers hold most of the shared memory
   } else if (c->head_dim_qk == 576 && c->head_dim_v == 512 && c->num_q_heads == kMlaHeads) {
-    // tcgen05 kernel: 128-token tiles; the tile, a Q half and P^T take the shared memory
+    // tcgen05 kernel: 128-token tiles; the tile and Q (P^T later written over Q) take the shared memory
     pl->kind = 4;
     pl->fetch = 0;
     pl->NW = 4;
