@@ -53,6 +53,9 @@ struct ResolveArgs {
 __device__ __forceinline__ uint32_t ht_hash(int32_t p, int bits) { return ((uint32_t)p * 0x9E3779B1u) >> (32 - bits); }
 
 // Exclusive scan of one uint32 per thread over the CTA; *total receives the sum.
+// kTrailing = false leaves out the last barrier, which only keeps wbuf from being rewritten while
+// it is read: for a caller that passes another barrier before its next scan.
+template <bool kTrailing = true>
 __device__ __forceinline__ uint32_t cta_exclusive_scan(uint32_t v, uint32_t* wbuf, uint32_t* total) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   uint32_t x = v;
@@ -75,7 +78,7 @@ __device__ __forceinline__ uint32_t cta_exclusive_scan(uint32_t v, uint32_t* wbu
   __syncthreads();
   const uint32_t base = w > 0 ? wbuf[w - 1] : 0u;
   *total = wbuf[kWarps - 1];
-  __syncthreads();
+  if (kTrailing) __syncthreads();
   return base + x - v;
 }
 
@@ -145,22 +148,24 @@ __device__ void fetch_misses(const ResolveArgs& a, int q0, int q1, const uint64_
 
 // The m victims are the candidates with the smallest (key, slot).  Radix select over the key range
 // of the candidates (key - min, 11-bit digits from the top) finds the threshold T and how many
-// candidates with key == T (lowest slots first) complete the set.
+// candidates with key == T (lowest slots first) complete the set.  Passes alternate between two
+// histograms and two selection words, both zero on entry: each thread clears the bins it has read,
+// so a histogram is zero again two passes later and a pass needs no barrier to clear one.
 __device__ void select_threshold(const uint32_t* key32, const uint8_t* flag, int B, uint32_t m, uint32_t lo,
-                                 uint32_t hi, uint32_t* wbuf, uint32_t* hist, uint32_t* sel, uint32_t* T_out,
-                                 uint32_t* need_out) {
+                                 uint32_t hi, uint32_t* wbuf, uint32_t (*hist)[2048], uint32_t (*sel)[2],
+                                 uint32_t* T_out, uint32_t* need_out) {
   // lo, hi: the smallest and largest candidate key (found by the probe)
   const int tid = threadIdx.x, lane = tid & 31;
   const uint32_t range = hi - lo;
   int shift = range == 0u ? 0 : 32 - __clz(range);
   uint64_t prefix = 0;
   uint32_t need = m;
-  while (shift > 0) {
+  for (int pass = 0; shift > 0; ++pass) {
     const int width = shift < 11 ? shift : 11;
     shift -= width;
     const int nb = 1 << width;
-    for (int b = tid; b < nb; b += kThreads) hist[b] = 0u;
-    __syncthreads();
+    uint32_t* h = hist[pass & 1];
+    uint32_t* sl = sel[pass & 1];
     for (int base = tid & ~31; base < B; base += kThreads) {
       const int j = base + lane;
       uint32_t digit = 0xffffffffu;
@@ -169,7 +174,7 @@ __device__ void select_threshold(const uint32_t* key32, const uint8_t* flag, int
         if ((v >> (shift + width)) == prefix) digit = (uint32_t)(v >> shift) & (uint32_t)(nb - 1);
       }
       const uint32_t peers = __match_any_sync(0xffffffffu, digit);
-      if (digit != 0xffffffffu && lane == __ffs(peers) - 1) atomicAdd(&hist[digit], (uint32_t)__popc(peers));
+      if (digit != 0xffffffffu && lane == __ffs(peers) - 1) atomicAdd(&h[digit], (uint32_t)__popc(peers));
     }
     __syncthreads();
     // bins [BPT tid, BPT tid + BPT): find the bin where the running count reaches `need`
@@ -178,26 +183,30 @@ __device__ void select_threshold(const uint32_t* key32, const uint8_t* flag, int
     uint32_t c[BPT], csum = 0u;
 #pragma unroll
     for (int u = 0; u < BPT; ++u) {
-      c[u] = b0 + u < nb ? hist[b0 + u] : 0u;
+      c[u] = 0u;
+      if (b0 + u < nb) {
+        c[u] = h[b0 + u];
+        h[b0 + u] = 0u;  // only this thread reads this bin
+      }
       csum += c[u];
     }
     uint32_t tot;
-    const uint32_t excl = cta_exclusive_scan(csum, wbuf, &tot);
+    // no trailing barrier: the one below comes before the next pass's scan rewrites wbuf
+    const uint32_t excl = cta_exclusive_scan<false>(csum, wbuf, &tot);
     if (excl < need && need <= excl + csum) {
       uint32_t run = excl;
 #pragma unroll
       for (int u = 0; u < BPT; ++u) {
         if (run < need && need <= run + c[u]) {
-          sel[0] = (uint32_t)(b0 + u);
-          sel[1] = need - run;
+          sl[0] = (uint32_t)(b0 + u);
+          sl[1] = need - run;
         }
         run += c[u];
       }
     }
     __syncthreads();
-    prefix = (prefix << width) | sel[0];
-    need = sel[1];
-    __syncthreads();
+    prefix = (prefix << width) | sl[0];
+    need = sl[1];
   }
   *T_out = lo + (uint32_t)prefix;
   *need_out = need;
@@ -223,8 +232,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
   uint32_t* key32 = (uint32_t*)(victims + k);       // [B]: eviction key
   uint8_t* flag = (uint8_t*)(key32 + B);            // [B]: bit 0 hit, bit 1 victim
   __shared__ uint32_t wbuf[kWarps];
-  __shared__ uint32_t hist[2048];
-  __shared__ uint32_t sel[2];
+  __shared__ uint32_t hist[2][2048];  // the victim select's histograms, zero outside the select
+  __shared__ uint32_t sel[2][2];
   __shared__ uint32_t err_bits;
 
   const int32_t* topk = a.topk + (int64_t)(r - a.r0) * k;
@@ -346,6 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
     ht_key[x] = -1;
     ht_val[x] = 0x7fffffff;
   }
+  for (int x = tid; x < 2 * 2048; x += kThreads) hist[x >> 11][x & 2047] = 0u;
   __syncthreads();
 
   // (1) hash the selected positions; a key keeps the smallest top-k index that carries it.  Entries
