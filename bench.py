@@ -9,7 +9,11 @@ traces keeping 88% per step (recency mean 2048).  The 16 requests share one pref
 
 Printed: one JSON line (rank 0).  `value` = decode layer-steps/s (one layer for the whole
 batch) with every input resident in HBM; `e2e` = the same with per-step inputs copied from
-pinned host memory and outputs copied back inside the timed region.
+pinned host memory and outputs copied back inside the timed region.  `roofline` rates the
+attention against HBM from its launches timed back to back; `host_link` rates the resolve's miss
+copies against a pinned copy measured in the same run.  The GQA workload also reports two other
+schedules of the same steps: two micro-batches with the misses copied inside the attention, and
+(a different selection pattern) layer groups sharing one top-k.
 `--impl reference` times the CPU oracle (test infrastructure, single-threaded) on a bounded
 sample of the same workload instead.
 """
@@ -744,7 +748,8 @@ def main():
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling runs)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--microbatches", type=int, default=1,
-                    help="split the requests into this many groups, each running its layers on its own stream")
+                    help="split the requests into this many groups, each running its layers on its own stream; "
+                         "the groups' resolves form one chain and their attentions another")
     ap.add_argument("--separate-append", action="store_true",
                     help="append and resolve as two launches instead of the fused hs_append_resolve")
     ap.add_argument("--fetch", choices=["auto", "resolve", "attention"], default="auto",
@@ -756,7 +761,8 @@ def main():
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the headline pass's kernels one by one instead of replaying a captured graph")
     ap.add_argument("--no-alt", action="store_true",
-                    help="skip the second pass with the miss copies inside the attention (GQA)")
+                    help="skip the extra GQA passes: two micro-batches with the miss copies inside the "
+                         "attention, and layer groups sharing one selection")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per attention launch from an ncu capture of the same kernel")
