@@ -1,6 +1,9 @@
 // Fused RESOLVE and write-through APPEND kernels.
 //
-// RESOLVE follows the fused kernel of the HiSparse summary (§5), one CTA per (request, layer):
+// RESOLVE follows the fused kernel of the HiSparse summary (§5), which runs one CTA per (request,
+// layer).  Here a thread-block cluster serves each request of a launch: every CTA of the cluster
+// computes the whole decision from the same inputs, then takes its share of the writes and of the
+// host copies, so the copies of one request are spread over several SMs.  The steps:
 //   (1) build a shared-memory hash table of the k selected positions;
 //   (2) probe every hot-buffer slot in parallel: hit, or a candidate for eviction;
 //   (3) parallel scans: rank hits and misses in top-k order, select the m victims (radix select
