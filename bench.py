@@ -75,6 +75,12 @@ def record_bytes(w):
     return 2 * w["Dqk"] if w["layout"] == 0 else 2 * w["Hkv"] * (w["Dqk"] + w["Dv"])
 
 
+def steps_exceed_l2(w):
+    """True when one step's attention launches together gather well over L2's size, so that timing
+    them back to back (and step after step) never finds a launch's rows left in L2 by the last."""
+    return w["L"] * attn_bytes_per_launch(w) >= 2 * L2_BYTES
+
+
 def attn_bytes_per_launch(w):
     """Algorithmic bytes of one attention launch (one layer, all requests): the k gathered
     records, q, the fp32 output and the slot list."""
@@ -431,7 +437,7 @@ def run_ours(args, w, world, rank, local):
         att_ms = np.array([[e[l][2].elapsed_time(e[l][3]) for l in range(L)] for e in evs])
     # pass 3: the attention alone, its L launches of the last step back to back; only where the L
     # launches together gather well over L2's size, so that no replay finds the last one's rows cached
-    big = L * attn_bytes_per_launch(w) >= 2 * L2_BYTES
+    big = steps_exceed_l2(w)
     attn_b2b_us = (time_attention_back_to_back(pool, wl, locs, outs, scale, W + K - 1)
                    if M == 1 and G == 1 and big else None)
     max_elapsed = reduce_max(elapsed, world)
