@@ -26,3 +26,26 @@ def test_latent_attention_bytes_per_launch():
 def test_back_to_back_timing_only_above_l2(name, exceeds):
     # 32 GQA launches gather 4.3 GB per step; the single-layer latent workloads stay inside L2
     assert bench.steps_exceed_l2(bench.WORKLOADS[name]) is exceeds
+
+
+def test_reference_arm_prints_its_line():
+    """`bench.py --impl reference` times the CPU oracle and prints one JSON line with the keys the
+    reference arm carries: impl, the same metric and unit, a cpu_baseline and a zero-copy e2e."""
+    import json
+    import os
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, HS_REF_STEP_SECONDS="0.05")
+    out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "tiny", "--steps", "1",
+                          "--warmup", "3"], cwd=root, env=env, capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "layer-steps/s"
+    assert d["higher_is_better"] is True and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
