@@ -75,6 +75,13 @@ def record_bytes(w):
     return 2 * w["Dqk"] if w["layout"] == 0 else 2 * w["Hkv"] * (w["Dqk"] + w["Dv"])
 
 
+def launches_per_layer(w, separate_append=False):
+    """This library's kernels launched per layer of a step: the resolve (the append fused in, or its
+    own launch), then the attention; the 64-head shared-latent attention adds its split combine."""
+    attn = 2 if w["layout"] == 0 and w["Hq"] == 64 else 1
+    return 1 + (1 if separate_append else 0) + attn
+
+
 def steps_exceed_l2(w):
     """True when one step's attention launches together gather well over L2's size, so that timing
     them back to back (and step after step) never finds a launch's rows left in L2 by the last."""
@@ -508,7 +515,7 @@ def run_ours(args, w, world, rank, local):
                       "achieved_gbs": miss_bytes / link_s / 1e9 if link_s > 0 else None,
                       "h2d_copy_peak_gbs": h2d,
                       "frac": (miss_bytes / link_s / 1e9) / h2d if link_s > 0 and h2d else None},
-        "gpu_launches": K * L * (3 if args.separate_append else 2),
+        "gpu_launches": K * L * launches_per_layer(w, args.separate_append),
         "clocks": clk,
         "setup_s": setup_secs,
         "errors": int(st["error_bits"]),

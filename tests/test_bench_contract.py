@@ -49,3 +49,11 @@ def test_reference_arm_prints_its_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+@pytest.mark.parametrize("name, per_layer", [("gqa_b16_l32", 2), ("mla_b8", 3), ("csa_b8", 3), ("stress_b16_l4", 3),
+                                             ("tiny", 2)])
+def test_launches_per_layer(name, per_layer):
+    # resolve (append fused) + attention; the 64-head shared-latent attention also launches its combine
+    assert bench.launches_per_layer(bench.WORKLOADS[name]) == per_layer
+    assert bench.launches_per_layer(bench.WORKLOADS[name], separate_append=True) == per_layer + 1
