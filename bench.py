@@ -508,13 +508,18 @@ def run_ours(args, w, world, rank, local):
                      # the same from the event pairs around each launch of the breakdown pass
                      "per_launch_events_us": attn_us,
                      "frac_per_launch_events": achieved_ev / peaks["hbm_gbs"],
-                     "launch_floor_us": floor_us},
+                     "launch_floor_us": floor_us,
+                     "share_of_layer": float(att_ms.mean() / (res_ms.mean() + att_ms.mean()))},
         # the kernel that moves the misses over the host link: the resolve, or the attention when the
         # copies were left to it
-        "host_link": {"kernel": link_kernel, "miss_bytes_per_layer": miss_bytes / (K * L),
+        # the resolve takes most of a layer's time and is bound by the host link, a resource with no
+        # measured peak: its roofline is this object, against a pinned copy timed in this run
+        "host_link": {"kernel": link_kernel, "bound": "host link (NVLink-C2C)",
+                      "miss_bytes_per_layer": miss_bytes / (K * L),
                       "achieved_gbs": miss_bytes / link_s / 1e9 if link_s > 0 else None,
                       "h2d_copy_peak_gbs": h2d,
-                      "frac": (miss_bytes / link_s / 1e9) / h2d if link_s > 0 and h2d else None},
+                      "frac": (miss_bytes / link_s / 1e9) / h2d if link_s > 0 and h2d else None,
+                      "share_of_layer": float(res_ms.mean() / (res_ms.mean() + att_ms.mean()))},
         "gpu_launches": K * L * launches_per_layer(w, args.separate_append),
         "clocks": clk,
         "setup_s": setup_secs,
