@@ -222,6 +222,12 @@ class Workload:
                 pool.prefill(r, l, 0, self.history_layer(l, r))
 
 
+def replica_seed(rank):
+    """Seed of the synthetic inputs of replica `rank`: every rank serves its own batch of requests
+    (its own traces, queries and histories), as independent replicas sharded by request would."""
+    return 1000 + 17 * rank
+
+
 def run_ours(args, w, world, rank, local):
     import torch
 
@@ -237,7 +243,7 @@ def run_ours(args, w, world, rank, local):
     if fetch == "auto":
         fetch = "resolve"  # each kernel against its own roofline; "attention" overlaps the link with HBM
     G = max(1, args.index_share)
-    wl = Workload(w, S, device, seed=1000 + 17 * rank, fetch=fetch, index_share=G)
+    wl = Workload(w, S, device, seed=replica_seed(rank), fetch=fetch, index_share=G)
     pool = HsPool(wl.cfg, device=local)
     wl.prefill(pool)
     torch.cuda.synchronize()
@@ -739,20 +745,100 @@ def oracle_sample(w, steps, seed, budget_s, pairs_max=64):
     return per, desc, n_rl_steps
 
 
+def cpu_info():
+    """CPU model and the number of online cores of this host (for the CPU baselines)."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if model is None:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for line in f:
+                    if line.lower().startswith(("model name", "cpu model")):
+                        model = line.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    return {"cpu_model": model or "unknown", "nproc": os.cpu_count()}
+
+
 def run_reference(args, w, world, rank):
-    """CPU oracle on the host cores, bounded sample per step (rank 0 only)."""
+    """The CPU oracle on the host cores (rank 0 only).  Each of the W + K steps advances the same
+    sample of (request, layer) pairs by one decode step -- append, resolve, fp64 attention -- which
+    is a bounded part of the workload's R x L pairs; the K timed steps give the rate per (request,
+    layer)-step, and `value` extrapolates it to whole layers (R pairs each) of the workload."""
     if rank != 0:
         return None
+    import torch
+
+    import oracle
+    from hierarchical_kv_cache_02_gb300 import inputs
+
     K, W = args.steps, args.warmup
-    budget_per_step = float(os.environ.get("HS_REF_STEP_SECONDS", "1.0"))
-    per, desc, n = oracle_sample(w, steps=min(W + K, w["steps"]), seed=99, budget_s=budget_per_step * (K + W))
-    value = 1.0 / (w["R"] * per)
+    budget = float(os.environ.get("HS_REF_STEP_SECONDS", "1.0"))  # seconds of oracle work per step
+    R, L, k = w["R"], w["L"], w["k"]
+    steps = W + K
+    appends = w.get("appends", True)
+    spec = inputs.TraceSpec(ctx0=w["ctx0"], k=k, steps=steps, keep=w["keep"], recency_mean=w["mu"], appends=appends,
+                            burst_every=w["burst"], far_gap=int(8 * w["mu"]))
+    E = record_bytes(w) // 2
+    kvh = 0 if w["layout"] == 0 else w["Hkv"]
+    scale = float(np.float32(1.0 / math.sqrt(w["Dqk"])))
+    # one history stands in for every sampled pair: the oracle's cost does not depend on the values
+    hist = inputs.normal_bf16((w["ctx0"] + steps, E), seed=99).view(torch.int16).numpy().view(np.uint16)
+    pairs = []
+
+    def add_pair(p):
+        r, l = p % R, (p * 7) % L
+        tr = inputs.drift_traces(spec, 1, 1, seed=99 + r * 65536 + l)[:, 0, 0]  # the trace of (r, l)
+        q = inputs.normal_bf16((steps, w["Hq"], w["Dqk"]), seed=100 + p).view(torch.int16).numpy().view(np.uint16)
+        pairs.append((oracle.Cache(w["B"], k, "lru", R=R, L=L, r=r, l=l, C=w["ctx0"] + steps), tr, q))
+
+    def advance(i, t):
+        cache, tr, q = pairs[i]
+        if appends:
+            cache.append(w["ctx0"] + t)
+        cache.resolve(tr[t])
+        oracle.attention(q[t], hist, tr[t], scale, kvh, w["Dqk"], w["Dv"])
+
+    # size the sample on the first warm-up step: pairs are added until the step has used its budget
+    t0 = time.perf_counter()
+    while len(pairs) < R * L and (not pairs or time.perf_counter() - t0 < budget):
+        add_pair(len(pairs))
+        advance(len(pairs) - 1, 0)
+    P = len(pairs)
+    for t in range(1, W):
+        for i in range(P):
+            advance(i, t)
+    t_start = time.perf_counter()
+    for t in range(W, steps):
+        for i in range(P):
+            advance(i, t)
+    elapsed = time.perf_counter() - t_start
+    per = elapsed / (P * K)  # seconds per (request, layer)-step
+    value = 1.0 / (R * per)
+    desc = (f"each of the {K} timed steps (after {W} warm-up steps) advanced the same {P} of the workload's "
+            f"{R * L} (request, layer) pairs by one decode step (append, resolve, fp64 attention): {P * K} "
+            f"(request, layer)-steps in {elapsed:.1f} s on 1 core; value = 1 / ({R} x s per (request, layer)-step), "
+            f"extrapolated from the sample to whole layers")
+    info = cpu_info()
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": "layer-steps/s", "n_gpus": world,
-            "steps": K, "warmup": W, "ms_per_step": w["L"] / value * 1e3, "higher_is_better": True,
+            "steps": K, "warmup": W, "ms_per_step": elapsed / K * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload, "requests": w["R"], "layers": w["L"], "context": w["ctx0"],
-                       "top_k": w["k"], "buffer_slots": w["B"]},
-            "cpu_baseline": {"value": value, "unit": "layer-steps/s", "cores": 1, "kind": "oracle", "sample": desc},
+            "extrapolated": True,
+            "timed_work": {"pairs_per_step": P, "pairs_per_layer": R, "layers": L,
+                           "ms_per_step": "wall time of one sampled step as run (P pairs), not of a whole step",
+                           "seconds_timed": elapsed},
+            "config": {"workload": args.workload, "requests": R, "layers": L, "context": w["ctx0"],
+                       "top_k": k, "buffer_slots": w["B"]},
+            "cpu_baseline": {"value": value, "unit": "layer-steps/s", "cores": 1, "kind": "oracle", "sample": desc,
+                             **info},
             "e2e": {"value": value, "unit": "layer-steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -821,7 +907,7 @@ def main():
     if rank == 0 and not args.no_cpu_baseline:
         per, desc, n = oracle_sample(w, steps=min(16, args.warmup + args.steps), seed=99, budget_s=args.cpu_seconds)
         out["cpu_baseline"] = {"value": 1.0 / (w["R"] * per), "unit": "layer-steps/s", "cores": 1, "kind": "oracle",
-                               "sample": desc}
+                               "sample": desc, **cpu_info()}
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:

@@ -1761,7 +1761,8 @@ int hs_attn_prepare(const hs_config* c, int num_sms) {
 
 namespace {
 
-constexpr size_t kNoAllocTicketBytes = 64 * 1024;                            // up to 16384 tickets
+constexpr size_t kNoAllocTicketBytes = 64 * 1024;  // the error word, then up to 16380 tickets
+constexpr size_t kNoAllocTicketOff = 16;            // tickets start here (the error word is at 0)
 constexpr size_t kNoAllocPartBytes = (size_t)HS_NOALLOC_SCRATCH_BYTES - kNoAllocTicketBytes;
 static __device__ __align__(256) unsigned char hs_noalloc_scratch[HS_NOALLOC_SCRATCH_BYTES];
 
@@ -1802,11 +1803,23 @@ extern "C" int hs_sparse_attn_noalloc(const hs_config* cfg, const void* d_q, con
   if (cfg == nullptr || d_q == nullptr || d_locs == nullptr || d_kv == nullptr || d_out == nullptr) return HS_ERR_ARG;
   if (kv_rows < 1 || kv_rows > (int64_t)INT32_MAX || ((uintptr_t)d_kv & 15u) != 0) return HS_ERR_ARG;
   if (!hs_aligned(d_q, 16) || !hs_aligned(d_out, 16) || !hs_aligned(d_locs, 4)) return HS_ERR_ARG;
-  if (cfg->num_requests < 1 || cfg->top_k < 1 || cfg->num_q_heads < 1 || cfg->num_kv_heads < 1 ||
-      cfg->num_q_heads % cfg->num_kv_heads != 0)
+  // only the documented fields decide the kernel and its split plan: the rest of *cfg (pool
+  // settings such as fetch_in_attention) is ignored
+  hs_config c;
+  memset(&c, 0, sizeof(c));
+  c.num_requests = cfg->num_requests;
+  c.num_layers = 1;
+  c.layout = cfg->layout;
+  c.num_q_heads = cfg->num_q_heads;
+  c.num_kv_heads = cfg->num_kv_heads;
+  c.head_dim_qk = cfg->head_dim_qk;
+  c.head_dim_v = cfg->head_dim_v;
+  c.top_k = cfg->top_k;
+  if (c.num_requests < 1 || c.top_k < 1 || c.num_q_heads < 1 || c.num_kv_heads < 1 ||
+      c.num_q_heads % c.num_kv_heads != 0)
     return HS_ERR_CONFIG;
-  if (cfg->layout == HS_LAYOUT_MLA && cfg->num_kv_heads != 1) return HS_ERR_CONFIG;
-  if (!hs_attn_supported(cfg)) return HS_ERR_CONFIG;
+  if (c.layout == HS_LAYOUT_MLA && c.num_kv_heads != 1) return HS_ERR_CONFIG;
+  if (!hs_attn_supported(&c)) return HS_ERR_CONFIG;
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) {
     cudaGetLastError();
@@ -1814,20 +1827,30 @@ extern "C" int hs_sparse_attn_noalloc(const hs_config* cfg, const void* d_q, con
   }
   void* scratch = nullptr;
   int sms = 0;
-  int rc = noalloc_setup(dev, cfg, &scratch, &sms);
+  int rc = noalloc_setup(dev, &c, &scratch, &sms);
   if (rc != HS_OK) return rc;
   Plan pl;
-  if (!plan_for(cfg, sms, &pl)) return HS_ERR_CONFIG;
-  const size_t part_floats = (size_t)cfg->num_requests * pl.S * cfg->num_q_heads * ((size_t)cfg->head_dim_v + 2);
-  const size_t tickets = (size_t)cfg->num_requests * (pl.groups + 1);
-  if (part_floats * sizeof(float) > kNoAllocPartBytes || (tickets + 1) * sizeof(uint32_t) > kNoAllocTicketBytes)
+  if (!plan_for(&c, sms, &pl)) return HS_ERR_CONFIG;
+  const size_t o_floats = (size_t)c.num_requests * pl.S * c.num_q_heads * c.head_dim_v;
+  const size_t ml_floats = (size_t)c.num_requests * pl.S * c.num_q_heads * 2;
+  const size_t tickets = (size_t)c.num_requests * (pl.groups + 1);
+  if ((o_floats + ml_floats) * sizeof(float) > kNoAllocPartBytes ||
+      kNoAllocTicketOff + tickets * sizeof(uint32_t) > kNoAllocTicketBytes)
     return HS_ERR_SCRATCH;
   uint8_t* base = (uint8_t*)scratch;
-  uint32_t* ticket = (uint32_t*)base;  // [tickets] then the error word
+  uint32_t* err = (uint32_t*)base;  // fixed offset: the error word comes first
+  uint32_t* ticket = (uint32_t*)(base + kNoAllocTicketOff);
   float* part = (float*)(base + kNoAllocTicketBytes);
+  float* ml = part + o_floats;
   cudaStream_t st = (cudaStream_t)stream;
-  // tickets must start at zero; a call that timed out on the device may have left them raised
-  if (cudaMemsetAsync(ticket, 0, (tickets + 1) * sizeof(uint32_t), st) != cudaSuccess) {
+  // The error word and the tickets start at zero (a call whose wait gave up may have left tickets
+  // raised).  The split statistics and the output start as NaN (all bits set): a CTA whose bounded
+  // wait gave up writes neither, so its request's output stays NaN (the combine of a NaN statistic
+  // gives NaN) instead of an earlier call's values.
+  if (cudaMemsetAsync(base, 0, kNoAllocTicketOff + tickets * sizeof(uint32_t), st) != cudaSuccess ||
+      cudaMemsetAsync(ml, 0xff, ml_floats * sizeof(float), st) != cudaSuccess ||
+      cudaMemsetAsync(d_out, 0xff, (size_t)c.num_requests * c.num_q_heads * c.head_dim_v * sizeof(float), st) !=
+          cudaSuccess) {
     cudaGetLastError();
     return HS_ERR_CUDA;
   }
@@ -1840,23 +1863,23 @@ extern "C" int hs_sparse_attn_noalloc(const hs_config* cfg, const void* d_q, con
   a.rows = kv_rows;
   a.out = d_out;
   a.part = part;
-  a.ml = part + (size_t)cfg->num_requests * pl.S * cfg->num_q_heads * cfg->head_dim_v;
+  a.ml = ml;
   a.ticket = ticket;
-  a.err = ticket + tickets;
-  a.rec = hs_record_bytes(cfg);
-  if (cfg->layout == HS_LAYOUT_GQA) {
-    a.kstride = 2 * (int64_t)(cfg->head_dim_qk + cfg->head_dim_v);
-    a.vdelta = 2 * (int64_t)cfg->head_dim_qk;
+  a.err = err;
+  a.rec = hs_record_bytes(&c);
+  if (c.layout == HS_LAYOUT_GQA) {
+    a.kstride = 2 * (int64_t)(c.head_dim_qk + c.head_dim_v);
+    a.vdelta = 2 * (int64_t)c.head_dim_qk;
   } else {
     a.kstride = 0;
     a.vdelta = 0;
   }
   a.qscale = scale * kLog2e;
-  a.R = cfg->num_requests;
-  a.Hq = cfg->num_q_heads;
-  a.k = cfg->top_k;
+  a.R = c.num_requests;
+  a.Hq = c.num_q_heads;
+  a.k = c.top_k;
   a.S = pl.S;
   a.chunk = pl.chunk;
   a.groups = pl.groups;
-  return dispatch(*cfg, &a, pl, st) == cudaSuccess ? HS_OK : HS_ERR_CUDA;
+  return dispatch(c, &a, pl, st) == cudaSuccess ? HS_OK : HS_ERR_CUDA;
 }

@@ -182,7 +182,12 @@ int hs_prefill_write(hs_pool* pool, int req, int layer, int64_t pos0, int64_t n,
 int hs_append_writethrough(hs_pool* pool, int layer, const int64_t* d_pos, const void* d_rec, void* stream);
 
 /*
- * Fused RESOLVE (summary §5), one CTA per request: hash the k positions of d_topk[r]
+ * Fused RESOLVE (summary §5).  The summary runs one CTA per request; here a thread-block cluster
+ * serves each request: every CTA of the cluster computes the whole decision below from the same
+ * inputs, then writes its share of the slots and fetches its share of the misses, so one request's
+ * host copies are spread over several SMs.  The cluster holds the largest of 8, 4 or 2 CTAs for
+ * which every request's cluster fits on the GPU at once (fixed at hs_pool_create), else 1.
+ * The decision: hash the k positions of d_topk[r]
  * (int32 [R][k], device; -1 = padding) in shared memory, probe all B slots for hits, choose
  * the m victims among the slots holding no selected position (smallest eviction key, then
  * lowest slot; victims in ascending slot order take the misses in top-k order), update the
@@ -229,21 +234,26 @@ int hs_sparse_attn(hs_pool* pool, int layer, const void* d_q, const int32_t* d_l
  * allocate the host history and the hot buffers; this call needs none of that.
  *
  * It computes exactly what hs_sparse_attn computes with a non-NULL kv_base, with the same
- * kernels: for request r and query head h, softmax(scale * <q, K(row)>)-weighted V over the rows
- * d_locs[r][i] >= 0 of d_kv, in top-k order.  Only these fields of *cfg are read: num_requests,
- * layout, num_q_heads, num_kv_heads, head_dim_qk, head_dim_v, top_k.
+ * kernels and the same split plan, so the two give bit-identical outputs: for request r and query
+ * head h, softmax(scale * <q, K(row)>)-weighted V over the rows d_locs[r][i] >= 0 of d_kv, in
+ * top-k order.  Only these fields of *cfg are read: num_requests, layout, num_q_heads,
+ * num_kv_heads, head_dim_qk, head_dim_v, top_k (pool settings such as fetch_in_attention are
+ * ignored).
  *   d_q    : bf16 [R][Hq][head_dim_qk], device          d_locs : int32 [R][k], device
  *   d_kv   : bf16 [R][kv_rows][record], device, 16-byte aligned
  *   d_out  : fp32 [R][Hq][head_dim_v], device
  * The split partials live in one file-scope device array of HS_NOALLOC_SCRATCH_BYTES per GPU,
  * loaded with the library and held until the process exits.  A shape whose partials do not fit
  * returns HS_ERR_SCRATCH before anything is enqueued (about R * splits * Hq * (head_dim_v + 2) * 4
- * bytes; splits <= number of SMs / R).  Each call clears the combine tickets it uses.
+ * bytes; splits <= number of SMs / R).  Each call first clears the combine tickets and the error
+ * word it uses and fills d_out with NaN.
  * The first call on a device (with that device current) looks up the scratch's device address
  * and raises the kernels' shared-memory limits; make that first call before any stream capture.
  * Every call on a device shares the one array and finds the previous call's leftovers there:
  * calls that may overlap on the GPU (different streams without ordering) race and corrupt each
- * other's results.  Rows outside [0, kv_rows) are skipped; this entry point does not report them.
+ * other's results.  Rows outside [0, kv_rows) are skipped and not reported.  A bounded wait inside
+ * a kernel that gives up (about a second without progress, a stalled GPU) leaves the affected
+ * requests' outputs NaN; there is no pool whose error word could report it.
  * Errors: HS_ERR_ARG, HS_ERR_CONFIG, HS_ERR_SCRATCH, HS_ERR_CUDA.
  */
 int hs_sparse_attn_noalloc(const hs_config* cfg, const void* d_q, const int32_t* d_locs, const void* d_kv,

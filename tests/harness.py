@@ -143,3 +143,31 @@ def assert_attn_close(got, ref, what="", tight=True):
     if tight:
         assert err.max() <= ATOL_FP32, (what, "above the fp32 bound", float(err.max()))
     return float(err.max())
+
+
+def assert_layer_matches_oracle(sc: Scenario, orc: OracleRun, ref_step, t, l, locs, out=None, what=""):
+    """Slots of every request of layer l at step t equal the oracle's (ref_step = orc.step(t)), and
+    the attention output (if given) is within the tolerance of fp64 over the selected positions."""
+    c = sc.cfg
+    for r in range(c.num_requests):
+        assert np.array_equal(locs[r], ref_step[(r, l)][1]), (what, t, r, l)
+        if out is not None:
+            assert_attn_close(out[r], orc.attention(t, r, l), (what, t, r, l), tight=c.layout == 1)
+
+
+def assert_pool_matches_oracle(pool, orc: OracleRun, what=""):
+    """Tags, stamps and clocks of every layer, and the per-(request, layer) counters, equal the
+    oracle's; no error bit is set."""
+    c = orc.sc.cfg
+    for l in range(c.num_layers):
+        tag, stamp, clock = pool.read_state(l)
+        for r in range(c.num_requests):
+            otag, ostamp = orc.caches[(r, l)].slots()
+            assert np.array_equal(tag[r], otag) and np.array_equal(stamp[r], ostamp), (what, r, l)
+            assert clock[r] == orc.caches[(r, l)].counters()["clock"], (what, r, l)
+    st = pool.stats()
+    for (r, l), cache in orc.caches.items():
+        cnt = cache.counters()
+        assert list(st["per_rl"][r, l, :3]) == [cnt["hits"], cnt["misses"], cnt["appends"]], (what, r, l)
+        assert st["per_rl"][r, l, 3] == cnt["misses"] * c.record_bytes, (what, r, l)
+    assert st["error_bits"] == 0, what

@@ -37,9 +37,13 @@ def test_reference_arm_prints_its_line():
     import sys
 
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    import time
+
     env = dict(os.environ, HS_REF_STEP_SECONDS="0.05")
-    out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "tiny", "--steps", "1",
+    t0 = time.time()
+    out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "tiny", "--steps", "2",
                           "--warmup", "3"], cwd=root, env=env, capture_output=True, text=True, timeout=600)
+    wall = time.time() - t0
     assert out.returncode == 0, out.stderr[-2000:]
     lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
     assert len(lines) == 1
@@ -49,6 +53,11 @@ def test_reference_arm_prints_its_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    # the line claims only what ran: its steps took steps x ms_per_step inside the run's wall time, and
+    # the rate extrapolated from the sampled pairs says so
+    assert d["steps"] == 2 and d["steps"] * d["ms_per_step"] / 1e3 <= wall
+    assert d["extrapolated"] is True and d["timed_work"]["pairs_per_step"] >= 1
+    assert d["cpu_baseline"]["nproc"] >= 1 and d["cpu_baseline"]["cpu_model"]
 
 
 @pytest.mark.parametrize("name, per_layer", [("gqa_b16_l32", 2), ("mla_b8", 3), ("csa_b8", 3), ("stress_b16_l4", 3),

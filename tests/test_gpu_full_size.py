@@ -26,7 +26,10 @@ def _bits(t):
     return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-def run_full(cfg, ctx0, steps, spec, pairs, attn_samples, seed, state_every=8, shared=False, appends=True):
+def run_full(cfg, ctx0, steps, spec, pairs, attn_samples, seed, state_every=8, shared=False, appends=True,
+             fused=False):
+    """fused: each layer's append and resolve go through the single fused call (hs_append_resolve),
+    the form bench.py times; else through the two separate calls."""
     R, L, k, E = cfg.num_requests, cfg.num_layers, cfg.top_k, cfg.record_elems
     trace = inputs.drift_traces(spec, R, L, seed=seed)                          # [S][L][R][k]
     pool = HsPool(cfg)
@@ -55,8 +58,13 @@ def run_full(cfg, ctx0, steps, spec, pairs, attn_samples, seed, state_every=8, s
         for l in range(L):
             if appends:
                 pos = torch.full((R,), ctx0 + t, dtype=torch.int64, device="cuda")
-                pool.append(l, pos, app[t, l])
-            pool.resolve(l, topk[t, l], locs[l])
+                if fused:
+                    pool.append_resolve(l, pos, app[t, l], topk[t, l], locs[l])
+                else:
+                    pool.append(l, pos, app[t, l])
+                    pool.resolve(l, topk[t, l], locs[l])
+            else:
+                pool.resolve(l, topk[t, l], locs[l])
             pool.sparse_attn(l, q[t, l], locs[l], out, scale=scale)
             if l in sampled_layers:
                 got_locs = locs[l].cpu().numpy()
@@ -94,23 +102,27 @@ def run_full(cfg, ctx0, steps, spec, pairs, attn_samples, seed, state_every=8, s
     return worst
 
 
-def test_full_mla_batch8():
+@pytest.mark.parametrize("fused", [False, True])
+def test_full_mla_batch8(fused):
     """Batch 8, 1 layer, context 32768, 576-dim latent, 64 heads, k=2048, B=4096, LRU, 128 steps,
-    drift keep 88% / recency mean 2048, write-through append every step."""
+    drift keep 88% / recency mean 2048, write-through append every step (fused = True: fused into
+    the resolve, the call bench.py times)."""
     ctx0, steps = 32768, 128
     cfg = HsConfig(num_requests=8, num_layers=1, capacity=ctx0 + steps, layout=LAYOUT_MLA, num_q_heads=64,
                    num_kv_heads=1, head_dim_qk=576, head_dim_v=512, top_k=2048, buffer_slots=4096, seed=3)
     spec = inputs.TraceSpec(ctx0=ctx0, k=2048, steps=steps, keep=0.88, recency_mean=2048, appends=True)
     pairs = [(0, 0), (5, 0)]
     samples = {(0, 0, 0), (127, 0, 0), (64, 5, 0)}
-    run_full(cfg, ctx0, steps, spec, pairs, samples, seed=11)
+    run_full(cfg, ctx0, steps, spec, pairs, samples, seed=11, fused=fused)
 
 
-@pytest.mark.parametrize("fetch", [0, 1])
-def test_full_gqa_batch16_32_layers(fetch):
+@pytest.mark.parametrize("fetch,fused", [(0, False), (0, True), (1, False), (1, True)])
+def test_full_gqa_batch16_32_layers(fetch, fused):
     """Batch 16, 32 layers, 8 KV heads x (128 K + 128 V), 32 q heads, context 131072 shared by the
     requests (17 GB pinned), k=2048, B=4096, drift keep 88%, write-through append, 64 steps
-    (16 with the misses fetched inside the attention)."""
+    (16 with the misses fetched inside the attention).  fused = True runs hs_append_resolve (16
+    resolve clusters with the early miss copies staged in shared memory), the call the headline
+    bench times; fetch = 1 with fused = True is the bench's two-micro-batch pass at full batch."""
     ctx0 = 131072
     steps = 64 if fetch == 0 else 16
     cfg = HsConfig(num_requests=16, num_layers=32, capacity=ctx0 + steps, layout=LAYOUT_GQA, num_q_heads=32,
@@ -119,12 +131,13 @@ def test_full_gqa_batch16_32_layers(fetch):
     spec = inputs.TraceSpec(ctx0=ctx0, k=2048, steps=steps, keep=0.88, recency_mean=2048, appends=True)
     pairs = [(3, 7), (15, 31)]
     samples = {(steps - 1, 3, 7), (steps // 2, 15, 31), (0, 15, 31)}
-    run_full(cfg, ctx0, steps, spec, pairs, samples, seed=13, shared=True)
+    run_full(cfg, ctx0, steps, spec, pairs, samples, seed=13, shared=True, fused=fused)
 
 
 def test_full_stress_bursts():
     """Batch 16, 4 layers, context 262144, 576-dim latent, 64 heads, k=2048, B=8192, LRU, bursts
-    (every 32 steps 40% of the top-k jumps to a far region), 128 steps with write-through append."""
+    (every 32 steps 40% of the top-k jumps to a far region), 128 steps with write-through append
+    fused into the resolve (the call bench.py times)."""
     ctx0, steps = 262144, 128
     cfg = HsConfig(num_requests=16, num_layers=4, capacity=ctx0 + steps, layout=LAYOUT_MLA, num_q_heads=64,
                    num_kv_heads=1, head_dim_qk=576, head_dim_v=512, top_k=2048, buffer_slots=8192, seed=7)
@@ -132,7 +145,7 @@ def test_full_stress_bursts():
                             burst_every=32, burst_frac=0.4, far_gap=8 * 2048)
     pairs = [(2, 1), (11, 3)]
     samples = {(32, 2, 1), (96, 11, 3)}
-    run_full(cfg, ctx0, steps, spec, pairs, samples, seed=17, state_every=16)
+    run_full(cfg, ctx0, steps, spec, pairs, samples, seed=17, state_every=16, fused=True)
 
 
 def test_full_csa_batch8():

@@ -7,7 +7,8 @@ Attention: max-abs <= 2e-2 and mean-abs <= 2e-3 against fp64 (and within the fp3
 import numpy as np
 import pytest
 
-from harness import OracleRun, Scenario, assert_attn_close, bf16_tensor, gpu_step, prefill
+from harness import (OracleRun, Scenario, assert_attn_close, assert_layer_matches_oracle, assert_pool_matches_oracle,
+                     bf16_tensor, gpu_step, prefill)
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -117,8 +118,9 @@ def test_fused_append_resolve(policy, fetch):
 
 @pytest.mark.parametrize("layout", ["gqa", "gqa_fetch", "mla"])
 def test_request_ranges_on_two_streams(layout):
-    """Two micro-batches of one pool on two streams, each request's layers in order: slots,
-    state, counters and outputs are bit-identical to full-batch calls on a second pool."""
+    """Two micro-batches of one pool on two streams, each request's layers in order: slots, state
+    and counters equal the oracle's, outputs are within the attention tolerance of its fp64
+    attention, and everything is bit-identical to full-batch calls on a second pool."""
     if layout == "mla":
         cfg = _mla(4, 2, 3000 + 6, 256, 512, Hq=64)
     else:
@@ -127,11 +129,13 @@ def test_request_ranges_on_two_streams(layout):
     full, split = HsPool(cfg), HsPool(cfg)
     prefill(full, sc)
     prefill(split, sc)
+    orc = OracleRun(sc)
     R, L = cfg.num_requests, cfg.num_layers
     groups = [(0, 1), (1, 3)]  # uneven on purpose
     streams = [torch.cuda.Stream(), torch.cuda.Stream()]
     for t in range(sc.steps):
         ref = gpu_step(full, sc, t, fused=True)
+        oref = orc.step(t)
         outs = []
         torch.cuda.synchronize()
         for (r0, n), st in zip(groups, streams):
@@ -147,11 +151,13 @@ def test_request_ranges_on_two_streams(layout):
                     per_layer.append((locs, out, topk, pos, rec, q))
                 outs.append(per_layer)
         torch.cuda.synchronize()
-        for gi, (r0, n) in enumerate(groups):
-            for l in range(L):
-                locs, out = outs[gi][l][0], outs[gi][l][1]
-                assert np.array_equal(locs.cpu().numpy(), ref[l][0][r0:r0 + n]), (t, l, gi)
-                assert np.array_equal(out.cpu().numpy(), ref[l][1][r0:r0 + n]), (t, l, gi)
+        for l in range(L):
+            got_locs = np.concatenate([outs[gi][l][0].cpu().numpy() for gi in range(len(groups))])
+            got_out = np.concatenate([outs[gi][l][1].cpu().numpy() for gi in range(len(groups))])
+            assert_layer_matches_oracle(sc, orc, oref, t, l, got_locs, got_out, "request ranges")
+            assert np.array_equal(got_locs, ref[l][0]), (t, l)
+            assert np.array_equal(got_out, ref[l][1]), (t, l)
+    assert_pool_matches_oracle(split, orc, "request ranges")
     for l in range(L):
         a, b = full.read_state(l), split.read_state(l)
         assert all(np.array_equal(x, y) for x, y in zip(a, b))
@@ -164,8 +170,9 @@ def test_request_ranges_on_two_streams(layout):
 def test_layer_group_schedule_on_side_streams(fetch):
     """Layer groups sharing one selection (exact layer-group prefetch): the group's resolves run at
     once, each layer on its own stream, and the attentions follow on another stream as their
-    resolve completes.  Slots, outputs, state and counters are bit-identical to the plain
-    layer-by-layer schedule on a second pool."""
+    resolve completes.  Slots, state and counters equal the oracle's stepped beside it, outputs are
+    within the attention tolerance of its fp64 attention, and everything is bit-identical to the
+    plain layer-by-layer schedule on a second pool."""
     cfg = _gqa(4, 4, 3000 + 6, 256, 512, fetch=fetch)
     sc = Scenario(cfg, ctx0=3000, steps=6, appends=True, seed=67)
     G = 2
@@ -174,6 +181,7 @@ def test_layer_group_schedule_on_side_streams(fetch):
     seq, grp = HsPool(cfg), HsPool(cfg)
     prefill(seq, sc)
     prefill(grp, sc)
+    orc = OracleRun(sc)
     R, L = cfg.num_requests, cfg.num_layers
     side = [torch.cuda.Stream() for _ in range(G)]
     astream = torch.cuda.Stream()
@@ -205,9 +213,13 @@ def test_layer_group_schedule_on_side_streams(fetch):
                 with torch.cuda.stream(astream):
                     outs[l] = grp.sparse_attn(l, ins[l][3], locs[l], scale=sc.scale, stream=astream)
         torch.cuda.synchronize()
+        oref = orc.step(t)
         for l in range(L):
-            assert np.array_equal(locs[l].cpu().numpy(), ref[l][0]), (t, l)
-            assert np.array_equal(outs[l].cpu().numpy(), ref[l][1]), (t, l)
+            got_locs, got_out = locs[l].cpu().numpy(), outs[l].cpu().numpy()
+            assert_layer_matches_oracle(sc, orc, oref, t, l, got_locs, got_out, "layer groups")
+            assert np.array_equal(got_locs, ref[l][0]), (t, l)
+            assert np.array_equal(got_out, ref[l][1]), (t, l)
+    assert_pool_matches_oracle(grp, orc, "layer groups")
     for l in range(L):
         a, b = seq.read_state(l), grp.read_state(l)
         assert all(np.array_equal(x, y) for x, y in zip(a, b))
@@ -219,8 +231,9 @@ def test_layer_group_schedule_on_side_streams(fetch):
 @pytest.mark.parametrize("fetch", [0, 1])
 def test_chained_microbatches_in_one_graph(fetch):
     """The bench's two-micro-batch schedule: each half on its own stream, the halves' resolves in one
-    chain and their attentions in another, every step captured in one CUDA graph.  Slots, outputs,
-    state and counters are bit-identical to full-batch calls on a second pool."""
+    chain and their attentions in another, every step captured in one CUDA graph.  Slots, state and
+    counters equal the oracle's, outputs are within the attention tolerance of its fp64 attention,
+    and everything is bit-identical to full-batch calls on a second pool."""
     R, L, steps = 4, 3, 6
     cfg = _gqa(R, L, 3000 + steps, 256, 512, fetch=fetch)
     sc = Scenario(cfg, ctx0=3000, steps=steps, appends=True, seed=67)
@@ -269,10 +282,15 @@ def test_chained_microbatches_in_one_graph(fetch):
             cur.wait_event(ev)
     graph.replay()
     torch.cuda.synchronize()
+    orc = OracleRun(sc)
     for t in range(steps):
+        oref = orc.step(t)
         for l in range(L):
-            assert np.array_equal(locs[t, l].cpu().numpy(), refs[t][l][0]), (t, l)
-            assert np.array_equal(outs[t, l].cpu().numpy(), refs[t][l][1]), (t, l)
+            got_locs, got_out = locs[t, l].cpu().numpy(), outs[t, l].cpu().numpy()
+            assert_layer_matches_oracle(sc, orc, oref, t, l, got_locs, got_out, "micro-batches")
+            assert np.array_equal(got_locs, refs[t][l][0]), (t, l)
+            assert np.array_equal(got_out, refs[t][l][1]), (t, l)
+    assert_pool_matches_oracle(split, orc, "micro-batches")
     for l in range(L):
         a, b = full.read_state(l), split.read_state(l)
         assert all(np.array_equal(x, y) for x, y in zip(a, b))
