@@ -4,8 +4,9 @@
 // Kernels in this file:
 //   * k_attn_gqa: GQA records, one CTA per (request, KV head); bulk-copy producers and consumers
 //     on mma.sync in a transposed form (tokens on the MMA's row side);
-//   * k_attn_mla_umma: shared-latent records with 64 query heads on tcgen05 tensor cores, the
-//     accumulators in tensor memory; split partials merged by k_combine_wide;
+//   * k_attn_mla_pipe: shared-latent records with 64 query heads on tcgen05 tensor cores, the
+//     accumulators in tensor memory, the tiles streamed by TMA through a ring; split partials merged
+//     by k_combine_wide;
 //   * k_attn_cc: CUDA-core fallback for other shared-latent head counts (a producer warp gathers
 //     whole records with cp.async.bulk into a 3-stage ring; consumers reduce 32 logits per lane
 //     with a transposed butterfly and keep an online softmax in base 2).
@@ -34,8 +35,6 @@ struct AttnArgs {
   const int32_t* locs;   // [R][k]
   const uint8_t* kv;     // caller rows (kv_pt null): row (r, loc) at kv + (r * rows + loc) * rec
   const uint64_t* kv_pt; // hot-buffer rows: [R][kv_pages] device address of each buffer page
-  const uint8_t* kv_pool;   // hot-buffer rows: base of the device cache pool (row = byte offset / rec)
-  const CUtensorMap* kv_tmap;  // host copy of the pool's tensor map (tensor-core shared-latent kernel), or null
   const int32_t* kv_cap; // hot-buffer rows: [R] rows each buffer holds (<= rows)
   int kv_pages, kv_shift;
   float* out;            // [R][Hq][DV]
@@ -1022,32 +1021,66 @@ __global__ void __launch_bounds__(256, 2) k_combine_wide(AttnArgs a) {
       make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
 }
 
-// ---- shared-latent records on tcgen05 tensor cores (64 heads) -----------------------------
+// ---- shared-latent records on tcgen05 tensor cores (64 heads), pipelined over tiles --------
 //
-// One CTA per (request, split of the top-k list); a split is walked in 128-token tiles.  Per tile,
-// with tokens on the MMA's 128-row side and the 64 heads on its N side:
-//   S^T[128 x 64] = K[128 x 576] . Q^T       36 tcgen05.mma (K = 16 each) into TMEM columns 0-63
-//   O^T[512 x 64] += V^T[512 x 128] . P^T    4 row tiles x 8 k-steps into TMEM columns 64-319
-// Operands sit in shared memory in the canonical no-swizzle layout (8 x 16-byte core matrices).
-// The gathered tile is one buffer of 128 rows: as K it is read K-major (core matrices 128 B apart
-// along the dims, 9216 B apart along the tokens), as V^T MN-major from the same bytes.  Q (all 576
-// dims, the same layout with 64 rows) is loaded per tile beside the gather; once S is complete Q is
-// dead and P^T is written MN-major (heads contiguous) over it.
-// Roles: eight producer warps gather rows with cp.async straight into that layout (padding rows
-// zero-filled) and arrive on mbarriers when their copies land; one thread issues the MMAs and
-// commits them to mbarriers; a 128-thread warpgroup (one token, i.e. one TMEM lane, per thread)
-// runs the softmax.  The running max per head is raised only when a score exceeds it by more than
-// 2^8 (softmax is shift-invariant; weights stay <= 256 in bf16 and fp32), and only then is the O^T
-// accumulator rescaled in TMEM.  The normaliser sums the same bf16-rounded weights the MMA uses.
-// The split partials (O, max, sum) are combined by k_combine_wide in split order.
+// One CTA per (request, split of the top-k list); a split is walked in tiles of up to 128 tokens
+// (the last one ragged: its missing rows are zero-filled and get zero weight).  Per tile, with the
+// tokens on the MMA's 128-row side and the 64 heads on its N side:
+//   S^T[128 x 64]  = K[128 x 576] . Q^T      36 tcgen05.mma (K = 16 each) into a TMEM S buffer
+//   O^T[512 x 64] += V^T[512 x 128] . P^T    4 row tiles x 8 k-steps into TMEM columns 128-383
+// Q (all 576 dims of the 64 heads, 72 KB, loaded once by TMA) stays in shared memory for the whole
+// split.  The records stream through a ring of four 32 KB slots, each holding two 64-dim blocks of a
+// tile (128 rows x 128 B per block) in the 128-byte swizzled layout the MMA reads.  Six producer
+// warps fill a slot with 16-byte cp.async copies straight into that layout: one warp instruction
+// moves four whole 128-byte lines (rows 4q..4q+3, lane -> row 4q + lane / 8, chunk lane % 8, stored at
+// chunk (lane % 8) XOR (row % 8)), so the loads are fully coalesced.  Every tile is gathered twice: its
+// nine blocks for the scores (five slot loads: dims 0-127, ..., 384-511, then 512-575 alone), then its
+// eight value blocks for the value product (four slot loads), which the first pass has just brought
+// into L2.  The load order is
+//   K(0), K(1), V(0), K(2), V(1), ..., K(n-1), V(n-2), V(n-1),
+// and one thread of warp 8 consumes the loads in that order, issuing S(0), S(1), PV(0), S(2), PV(1),
+// ..., so the scores of tile i+1 are computed while the softmax of tile i runs.
+// Why this shape (measured on this GPU, per SM): a tcgen05.mma costs its issuing thread 51-75 cycles
+// whatever its size up to N = 128, so 128-token tiles (68 products per 128 tokens) beat 64-token tiles
+// with M = 64 products (104); holding a 128-token tile's value blocks from the score pass to the value
+// pass would need 128 KB beside Q and stall the next tile's loads; TMA tile::gather4 builds the same
+// layout but completes only about 60 of its 512-byte gathers per microsecond (32 GB/s), while 16-byte
+// cp.async reaches about 42 GB/s from HBM and 50 GB/s from L2; a ring with one in-order consumer
+// never waits on a slot two loads ahead (two consumers of one ring can, and an mbarrier parity test
+// then passes a phase early).
+// Roles: warps 9-14 produce (each lane keeps the record addresses of its rows of a tile in registers;
+// the first tile's slot indices are requested before the setup barrier); warp 8 allocates TMEM and one
+// of its threads issues the MMAs, releasing each ring slot by a commit once its products are done;
+// warps 0-7 run the softmax as two warpgroups, warpgroup g on heads 32g..32g+31, each thread on one
+// token (= TMEM lane).  S alternates between two TMEM buffers (columns 0-63, 64-127).  The running
+// max of a head is raised only when a score exceeds it by more than 2^8 (softmax is shift-invariant;
+// weights stay <= 256, exact in bf16's range), and only then is its O^T column rescaled in TMEM.
+// Weights are rounded to bf16 for the MMA and the normaliser sums the same rounded weights.  Partials
+// (O, max, sum) per split are combined by k_combine_wide in split order.  Every wait is bounded; a
+// CTA that gives up writes no partial.
 constexpr int kUTok = 128, kUHeads = 64, kUDim = 576;
-constexpr int kUKv = kUTok * kUDim * 2;              // 147456 B: gathered tile
-constexpr int kUQ = kUHeads * kUDim * 2;             // 73728 B: Q; P^T (16384 B) later reuses it
-constexpr int kUSboKv = (kUDim / 8) * 128;           // 9216 B between 8-row groups (tile and Q)
-constexpr int kUProd = 8;                            // producer warps
-constexpr int kUWarpMma = 4;                         // warp of the MMA issuer
-constexpr int kUThreads = (4 + 1 + kUProd) * 32;
-constexpr float kULazy = 8.f;                        // log2 headroom before the max is raised
+constexpr int kUQ = kUHeads * kUDim * 2;   // 73728 B: Q, nine 64-dim blocks of 64 heads x 128 B
+constexpr int kUP = kUTok * kUHeads * 2;   // 16384 B: P^T of one tile
+constexpr int kUBlk = kUTok * 128;         // 16384 B: one 64-dim block of a tile
+constexpr int kUSlot = 2 * kUBlk;          // a ring slot holds two blocks
+constexpr int kURing = 4;                  // ring slots
+constexpr int kUWarpMma = 8, kUWarpProd = 9, kUProd = 6;  // MMA warp, first producer warp, producers
+constexpr int kURowsPerLane = (32 + kUProd - 1) / kUProd;  // rows of a tile per producer lane
+constexpr int kUThreads = (kUWarpProd + kUProd) * 32;
+constexpr int kUTmemO = 128;               // first TMEM column of O^T (after the two S buffers)
+constexpr float kULazy = 8.f;              // log2 headroom before the max is raised
+constexpr size_t kUSmem = (size_t)kUQ + kUP + (size_t)kURing * kUSlot + 1024;  // + 1 KB alignment
+
+// one lane of the (fully active) warp
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
 
 // 16-byte cp.async; src_bytes = 0 writes zeros (nothing is read)
 __device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void* src, uint32_t src_bytes) {
@@ -1063,16 +1096,6 @@ __device__ __forceinline__ uint64_t umma_sdesc(uint32_t addr, uint32_t lbo, uint
   // (0: no swizzle; 2: 128-byte swizzle, atoms 1024-byte aligned so the base offset is 0)
   return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) | ((uint64_t)layout << 61);
-}
-// TMA gather of four rows (row coordinates y0..y3, -1 reads zeros) x one 64-element column block
-// (x, a multiple of 64) of a 2-D tensor map, 128-byte swizzled into shared memory at dst
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int x, int y0, int y1, int y2, int y3,
-                                            uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-      "l"((uint64_t)map), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(smem_u32(bar))
-      : "memory");
 }
 // TMA load of one box of a 2-D tensor map at element coordinates (x, y) into shared memory at dst
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
@@ -1099,30 +1122,40 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t x[16];
+// 32 consecutive TMEM columns of this thread's lane
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t x[32];
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
       : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3]), "=r"(x[4]), "=r"(x[5]), "=r"(x[6]), "=r"(x[7]),
-        "=r"(x[8]), "=r"(x[9]), "=r"(x[10]), "=r"(x[11]), "=r"(x[12]), "=r"(x[13]), "=r"(x[14]), "=r"(x[15])
+        "=r"(x[8]), "=r"(x[9]), "=r"(x[10]), "=r"(x[11]), "=r"(x[12]), "=r"(x[13]), "=r"(x[14]), "=r"(x[15]),
+        "=r"(x[16]), "=r"(x[17]), "=r"(x[18]), "=r"(x[19]), "=r"(x[20]), "=r"(x[21]), "=r"(x[22]), "=r"(x[23]),
+        "=r"(x[24]), "=r"(x[25]), "=r"(x[26]), "=r"(x[27]), "=r"(x[28]), "=r"(x[29]), "=r"(x[30]), "=r"(x[31])
       : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(x[i]);
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(x[i]);
 }
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
   asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
-          taddr),
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
       "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
       "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
       "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])),
       "r"(__float_as_uint(v[11])), "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])),
-      "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15]))
+      "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])),
+      "r"(__float_as_uint(v[17])), "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])),
+      "r"(__float_as_uint(v[20])), "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])),
+      "r"(__float_as_uint(v[23])), "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])),
+      "r"(__float_as_uint(v[26])), "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])),
+      "r"(__float_as_uint(v[29])), "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
       : "memory");
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
-__device__ __forceinline__ void named_sync_128() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// barrier of one softmax warpgroup (ids 1 and 2; 0 is __syncthreads)
+__device__ __forceinline__ void wg_sync(int g) { asm volatile("bar.sync %0, 128;" ::"r"(1 + g) : "memory"); }
 
 // 32 partial maxima per lane -> lane l holds the warp-wide max of value l (transposed butterfly)
 __device__ __forceinline__ float reduce32_max_transposed(float (&v)[32], int lane) {
@@ -1141,51 +1174,66 @@ __device__ __forceinline__ float reduce32_max_transposed(float (&v)[32], int lan
   return v[0];
 }
 
-template <bool TMA>
-__global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_umma(AttnArgs a, const __grid_constant__ CUtensorMap tmap,
-                                                                  const __grid_constant__ CUtensorMap qmap) {
+// bounded wait of a whole warp: lane 0 waits, the result is the warp's
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile uint32_t* abort) {
+  bool w = true;
+  if ((threadIdx.x & 31) == 0) w = mbar_wait_bounded(bar, parity, abort);
+  return __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+}
+
+__global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_pipe(AttnArgs a, const __grid_constant__ CUtensorMap qmap) {
   hs_pdl_enter();
   extern __shared__ __align__(128) uint8_t smem_raw[];
-  // the tile starts 1024-byte aligned (the period of the 128-byte swizzle); the launch adds 1 KB
+  // Q and the ring start 1024-byte aligned (the period of the 128-byte swizzle); the launch adds 1 KB
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint8_t* sKV = smem;
-  uint8_t* sQ = smem + kUKv;
-  uint8_t* sP = sQ;  // P^T is written once S (the last reader of Q) is complete
-  __shared__ __align__(8) uint64_t bar_kv, bar_q, bar_s, bar_p, bar_pv, bar_fin;
+  uint8_t* sQ = smem;
+  uint8_t* sRing = smem + kUQ;
+  uint8_t* sP = sRing + kURing * kUSlot;
+  __shared__ __align__(8) uint64_t bar_full[kURing], bar_empty[kURing];
+  __shared__ __align__(8) uint64_t bar_q, bar_s[2], bar_p, bar_pv, bar_fin;
   __shared__ uint32_t s_tmem, abort_flag;
-  __shared__ float s_m[kUHeads], s_l[kUHeads], s_alpha[kUHeads], s_red[4][kUHeads];
-  __shared__ uint32_t s_need[2][4];
+  __shared__ uint32_t s_need[2][2][4];            // [parity][warpgroup][warp]
+  __shared__ uint32_t s_resc[2];                  // [warpgroup]: some head's max was raised this tile
+  __shared__ __align__(16) float s_m[2][32];      // [warpgroup][head]: running max (base 2)
+  __shared__ __align__(16) float s_alpha[2][32];  // [warpgroup][head]: rescale of this tile
+  __shared__ __align__(16) float s_max[2][4][32]; // [warpgroup][warp][head]: per-warp tile max
+  __shared__ __align__(16) float s_sum[2][4][32]; // [warpgroup][warp][head]: per-warp tile weight sum
   __shared__ uint64_t s_pg[kMaxSlotPages];
-  __shared__ int32_t s_pgrow[kMaxSlotPages];  // TMA: pool row of each page's first slot
 
   const int split = blockIdx.x, r = a.r0 + (int)blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int t0 = split * a.chunk;
   const int n = min(a.k, t0 + a.chunk) - t0;
-  const int ntile = (n + kUTok - 1) / kUTok;
+  const int nt = (n + kUTok - 1) / kUTok;
   if (tid == 0) {
-    mbar_init(&bar_kv, TMA ? 1u : kUProd * 32);  // TMA: one expect-tx arrival; else one per producer lane
-    mbar_init(&bar_q, TMA ? 1u : kUProd * 32);
-    mbar_init(&bar_s, 1u);            // MMA commits
+    for (int s = 0; s < kURing; ++s) {
+      mbar_init(&bar_full[s], (uint32_t)(kUProd * 32));  // every producer thread, once its copies land
+      mbar_init(&bar_empty[s], 1u);                      // one MMA commit
+    }
+    mbar_init(&bar_q, 1u);
+    mbar_init(&bar_s[0], 1u);
+    mbar_init(&bar_s[1], 1u);
+    mbar_init(&bar_p, 256u);  // every softmax thread, once its weights are in place
     mbar_init(&bar_pv, 1u);
     mbar_init(&bar_fin, 1u);
-    mbar_init(&bar_p, 128u);          // softmax threads
     abort_flag = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  for (int h = tid; h < kUHeads; h += kUThreads) {
-    s_m[h] = -INFINITY;
-    s_l[h] = 0.f;
-  }
+  if (tid < 64) s_m[tid >> 5][tid & 31] = -INFINITY;
   rows_setup(a, r, s_pg);
-  if (TMA && tid < a.kv_pages) {
-    const uint64_t pg = a.kv_pt[(int64_t)r * a.kv_pages + tid];
-    s_pgrow[tid] = pg != 0ull ? (int32_t)((pg - (uint64_t)(uintptr_t)a.kv_pool) / (uint64_t)a.rec) : -1;
-  }
-  // the split's slots; producers and softmax apply the same validity test (outside [0, rows) or
-  // padding: a zero row and a zero weight)
   const int32_t* locs = a.locs + (int64_t)(r - a.r0) * a.k + t0;
   const int64_t rows_r = rows_of(a, r);
+  // producers: this lane's rows of a tile are 4 (pw + kUProd e) + lane / 8; the first tile's slot
+  // indices are requested before the setup barrier
+  const int pw = warp - kUWarpProd, crow = lane >> 3, cch = lane & 7;
+  int32_t lfirst[kURowsPerLane];
+  if (warp >= kUWarpProd) {
+#pragma unroll
+    for (int e = 0; e < kURowsPerLane; ++e) {
+      const int q = pw + kUProd * e, x = 4 * q + crow;
+      lfirst[e] = (q < 32 && x < n) ? locs[x] : -1;
+    }
+  }
   if (warp == kUWarpMma) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(&s_tmem))
                  : "memory");
@@ -1195,268 +1243,269 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_umma(AttnArgs a, cons
   __syncthreads();
   tc_fence_after();
   const uint32_t tb = s_tmem;
+  const uint32_t sq_u = smem_u32(sQ), ring_u = smem_u32(sRing), sp_u = smem_u32(sP);
 
-  if (warp > kUWarpMma) {
-    // ---------------- producers: gathered tile, then Q, cp.async into the MMA layout ----------------
-    const int pw = warp - kUWarpMma - 1, pl = pw * 32 + lane;
-    const uint16_t* qr = a.q + (int64_t)(r - a.r0) * a.Hq * kUDim;
-    const uint32_t sq_u = smem_u32(sQ), skv_u = smem_u32(sKV);
+  if (warp >= kUWarpProd) {
+    // ---------------- producers: Q once by TMA, then the tiles' blocks through the ring ----------------
+    if (pw == 0 && lane == 0) {
+      mbar_arrive_expect_tx(&bar_q, (uint32_t)kUQ);
+      for (int kb = 0; kb < 9; ++kb)
+        tma_load_2d(sq_u + (uint32_t)(kb * 8192), &qmap, kb * 64, (r - a.r0) * kUHeads, &bar_q);
+    }
     bool ok = true, bad = false;
-    int gathered = 0;  // TMA: tiles whose gather was issued
-    for (int i = 0; ok && i < ntile; ++i) {
-      if (i >= 1) {  // the previous tile's value product has read the tile and P^T (over Q)
-        bool w = true;
-        if (lane == 0) w = mbar_wait_bounded(&bar_pv, (uint32_t)((i - 1) & 1), &abort_flag);
-        if (__shfl_sync(0xffffffffu, w ? 1 : 0, 0) == 0) {
-          ok = false;
-          break;
+    // record addresses (0: padding, invalid, or past the split) of this lane's rows, for the tile
+    // whose scores are being gathered and for the one whose values are
+    uint64_t rows_k[kURowsPerLane], rows_v[kURowsPerLane];
+    int u = 0;  // loads issued
+    // one slot load: blocks kb0 (and kb0 + 1 when two) of a tile whose rows are `rows`
+    auto load = [&](const uint64_t (&rows)[kURowsPerLane], int kb0, int nblk) -> bool {
+      const int slot = u % kURing;
+      if (u >= kURing && !warp_wait(&bar_empty[slot], (uint32_t)((u / kURing - 1) & 1), &abort_flag)) return false;
+      const uint32_t sbase = ring_u + (uint32_t)(slot * kUSlot);
+      for (int b = 0; b < nblk; ++b) {
+        const int coff = (kb0 + b) * 128 + cch * 16;
+#pragma unroll
+        for (int e = 0; e < kURowsPerLane; ++e) {
+          const int q = pw + kUProd * e;
+          if (q < 32) {
+            const int row = 4 * q + crow;
+            const uint64_t src = rows[e];
+            cp_async16_zfill(sbase + (uint32_t)(b * kUBlk + row * 128 + ((cch ^ (row & 7)) << 4)),
+                             src != 0ull ? (const void*)(uintptr_t)(src + coff) : (const void*)a.q,
+                             src != 0ull ? 16u : 0u);
+          }
         }
       }
-      if (TMA) {
-        // 9 column blocks of 64 dims x 32 groups of 4 rows, gathered by the tensor memory accelerator
-        // into the 128-byte swizzled tile (blocks 16 KB apart, rows 128 B apart); padding reads zeros
-        if (pl == 0) mbar_arrive_expect_tx(&bar_kv, (uint32_t)kUKv);
-        const int msk = (int)((1u << a.kv_shift) - 1u);
-        for (int o = pl; o < 9 * 32; o += kUProd * 32) {
-          const int kb = o >> 5, g4 = o & 31;
-          int rr[4];
+      cp_async_arrive_noinc(&bar_full[slot]);
+      ++u;
+      return true;
+    };
+    for (int i = 0; ok && i <= nt; ++i) {
+      if (i < nt) {
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int x = i * kUTok + 4 * g4 + u;
-            int32_t loc = x < n ? locs[x] : -1;
-            if (loc < -1 || (int64_t)loc >= rows_r) {
-              bad = true;
-              loc = -1;
-            }
-            rr[u] = loc >= 0 ? s_pgrow[loc >> a.kv_shift] + (loc & msk) : -1;
-          }
-          tma_gather4(skv_u + (uint32_t)(kb * 16384 + g4 * 512), &tmap, kb * 64, rr[0], rr[1], rr[2], rr[3], &bar_kv);
-        }
-        gathered = i + 1;
-      } else {
-        // this warp's two 8-token groups: lane -> row (lane & 7), 16-byte column 4 j + (lane >> 3)
-#pragma unroll
-        for (int g2 = 0; g2 < 2; ++g2) {
-          const int rg = 2 * pw + g2;
-          const int row = rg * 8 + (lane & 7);
-          const int x = i * kUTok + row;
-          int32_t loc = x < n ? locs[x] : -1;
+        for (int e = 0; e < kURowsPerLane; ++e) {
+          const int q = pw + kUProd * e, x = i * kUTok + 4 * q + crow;
+          int32_t loc = i == 0 ? lfirst[e] : ((q < 32 && x < n) ? locs[x] : -1);
           if (loc < -1 || (int64_t)loc >= rows_r) {
             bad = true;
             loc = -1;
           }
-          // padding reads nothing (zero fill); its source is any mapped address
-          const uint8_t* src = loc >= 0 ? row_addr(s_pg, a.kv_shift, a.rec, loc) : (const uint8_t*)a.q;
-          const uint32_t dst = skv_u + (uint32_t)(rg * kUSboKv + (lane & 7) * 16);
-          const uint32_t nb = loc >= 0 ? 16u : 0u;
-#pragma unroll 6
-          for (int j = 0; j < 18; ++j) {
-            const int c = 4 * j + (lane >> 3);
-            cp_async16_zfill(dst + (uint32_t)(c * 128), src + c * 16, nb);
-          }
+          rows_k[e] = loc >= 0 ? (uint64_t)(uintptr_t)row_addr(s_pg, a.kv_shift, a.rec, loc) : 0ull;
         }
-        cp_async_arrive_noinc(&bar_kv);
+        for (int p = 0; ok && p < 5; ++p) ok = load(rows_k, 2 * p, p < 4 ? 2 : 1);  // scores: all 9 blocks
       }
-      if (TMA) {
-        // Q: 9 boxes of 64 dims x 64 heads from the launch's Q tensor map, 128-byte swizzled like the
-        // tile (blocks 8 KB apart, heads 128 B apart)
-        if (pl == 0) {
-          mbar_arrive_expect_tx(&bar_q, (uint32_t)kUQ);
-          for (int kb = 0; kb < 9; ++kb)
-            tma_load_2d(sq_u + (uint32_t)(kb * 8192), &qmap, kb * 64, (r - a.r0) * kUHeads, &bar_q);
-        }
-      } else {
-        // Q: 64 heads x 72 chunks of 16 bytes, 8-head groups 9216 B apart
-        for (int e = pl; e < kUHeads * 72; e += kUProd * 32) {
-          const int ng = e / 576, rem = e % 576, c = rem / 8, hn = ng * 8 + rem % 8;
-          cp_async16_zfill(sq_u + (uint32_t)(ng * kUSboKv + c * 128 + (rem % 8) * 16),
-                           qr + (int64_t)hn * kUDim + c * 8, 16u);
-        }
-        cp_async_arrive_noinc(&bar_q);
-      }
+      if (i >= 1)
+        for (int p = 0; ok && p < 4; ++p) ok = load(rows_v, 2 * p, 2);  // values of the tile before
+#pragma unroll
+      for (int e = 0; e < kURowsPerLane; ++e) rows_v[e] = rows_k[e];
     }
     if (bad) atomicOr(a.err, (uint32_t)HS_DEVERR_LOC);
-    if (TMA && !ok && gathered > 0 && pl == 0) {
-      // a wait gave up: the last gather and Q still land in this CTA's shared memory before it may exit
-      volatile uint32_t never = 0u;
-      mbar_wait_bounded(&bar_kv, (uint32_t)((gathered - 1) & 1), &never);
-      mbar_wait_bounded(&bar_q, (uint32_t)((gathered - 1) & 1), &never);
-    }
-    asm volatile("cp.async.wait_all;" ::: "memory");
     if (!ok && lane == 0) {
       *(volatile uint32_t*)&abort_flag = 1u;
       atomicOr(a.err, (uint32_t)HS_DEVERR_TIMEOUT);
     }
-  } else if (warp == kUWarpMma) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0) {
-      const uint32_t id_s = umma_idesc_bf16(128, 64, 0, 0), id_o = umma_idesc_bf16(128, 64, 1, 1);
-      const uint32_t skv_u = smem_u32(sKV), sq_u = smem_u32(sQ), sp_u = smem_u32(sP);  // sP == sQ
-      bool ok = true;
-      for (int i = 0; ok && i < ntile; ++i) {
-        ok = mbar_wait_bounded(&bar_kv, (uint32_t)(i & 1), &abort_flag);
-        if (ok) ok = mbar_wait_bounded(&bar_q, (uint32_t)(i & 1), &abort_flag);
-        if (!ok) break;
-        tc_fence_after();
-#pragma unroll 6
-        for (int s2 = 0; s2 < 36; ++s2) {  // K = 576 in steps of 16: two core matrices of each operand
-          // tile K-major: swizzled, a k-step is 32 B inside a 128-byte row of a 64-dim block; else core matrices
-          const uint64_t da = TMA ? umma_sdesc(skv_u + (uint32_t)((s2 >> 2) * 16384 + (s2 & 3) * 32), 16, 1024, 2)
-                                  : umma_sdesc(skv_u + (uint32_t)(2 * s2 * 128), 128, kUSboKv);
-          const uint64_t db = TMA ? umma_sdesc(sq_u + (uint32_t)((s2 >> 2) * 8192 + (s2 & 3) * 32), 16, 1024, 2)
-                                  : umma_sdesc(sq_u + (uint32_t)(2 * s2 * 128), 128, kUSboKv);
-          umma_bf16(tb, da, db, id_s, s2 != 0 ? 1u : 0u);
-        }
-        umma_commit(&bar_s);
-        ok = mbar_wait_bounded(&bar_p, (uint32_t)(i & 1), &abort_flag);
-        if (!ok) break;
-        tc_fence_after();
-#pragma unroll 1
-        for (int mt = 0; mt < 4; ++mt) {
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            // V^T MN-major from the same bytes: swizzled, LBO = 16 KB between 64-dim blocks, SBO = 1 KB
-            // between 8-token groups; else LBO along the tokens, SBO along the dims
-            const uint64_t da =
-                TMA ? umma_sdesc(skv_u + (uint32_t)(mt * 32768 + ks * 2048), 16384, 1024, 2)
-                    : umma_sdesc(skv_u + (uint32_t)(mt * 16 * 128 + ks * 2 * kUSboKv), kUSboKv, 128);
-            const uint64_t db = umma_sdesc(sp_u + (uint32_t)(ks * 2 * 1024), 1024, 128);
-            umma_bf16(tb + 64u + 64u * (uint32_t)mt, da, db, id_o, (i | ks) != 0 ? 1u : 0u);
-          }
-        }
-        umma_commit(&bar_pv);
-      }
-      if (!ok) {
-        *(volatile uint32_t*)&abort_flag = 1u;
-        atomicOr(a.err, (uint32_t)HS_DEVERR_TIMEOUT);
-      }
-      // every MMA issued has completed before the accumulator can be released
-      umma_commit(&bar_fin);
+    // every copy this thread issued lands in shared memory before the CTA may exit (the MMA issuer
+    // may have given up before consuming the last loads); Q likewise
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    if (pw == 0 && lane == 0) {
       volatile uint32_t never = 0u;
-      mbar_wait_bounded(&bar_fin, 0u, &never);
+      mbar_wait_bounded(&bar_q, 0u, &never);
     }
-    __syncwarp();
-  } else {
-    // ---------------- softmax warpgroup: thread = token of the tile = TMEM lane ----------------
-    // Every thread of the warpgroup passes the same sequence of named barriers on every tile: a
-    // wait that gives up only marks the thread (ok = false, no TMEM access, zero weights), so a
-    // barrier can never miss a thread.
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    bool ok = true;
-    for (int i = 0; i < ntile; ++i) {
-      if (ok) ok = mbar_wait_bounded(&bar_s, (uint32_t)(i & 1), &abort_flag);
-      // the previous tile's O^T update has read P^T (and is complete before any rescale)
-      if (ok && i >= 1) ok = mbar_wait_bounded(&bar_pv, (uint32_t)((i - 1) & 1), &abort_flag);
+  } else if (warp == kUWarpMma) {
+    // ---------------- MMA issuer: S(0), S(1), PV(0), S(2), PV(1), ... ----------------
+    const uint32_t id_s = umma_idesc_bf16(128, 64, 0, 0), id_o = umma_idesc_bf16(128, 64, 1, 1);
+    // operand descriptors, built once: a score k-step moves 32 B inside an operand (2 in the
+    // descriptor's address field, 16-byte units), a value k-step of 16 tokens 2 KB (128); no carry:
+    // shared addresses stay below 256 KB
+    const uint64_t dq0 = umma_sdesc(sq_u, 16, 1024, 2);         // Q block 0, K-major swizzled
+    const uint64_t dk0 = umma_sdesc(ring_u, 16, 1024, 2);       // ring slot 0 as a K operand
+    // V^T MN-major from the same bytes: LBO = 16 KB between a slot's two 64-dim blocks, SBO = 1 KB
+    // between 8-token groups; P^T MN-major, no swizzle (heads contiguous)
+    const uint64_t dv0 = umma_sdesc(ring_u, kUBlk, 1024, 2);
+    const uint64_t dp = umma_sdesc(sp_u, 1024, 128);
+    constexpr uint64_t kSlotStep = kUSlot >> 4, kBlkStep = kUBlk >> 4, kQStep = 8192 >> 4;
+    bool ok = warp_wait(&bar_q, 0u, &abort_flag);
+    int u = 0;  // loads consumed
+    auto take = [&]() -> int {  // wait for the next load; returns its slot, or -1
+      const int slot = u % kURing;
+      if (!warp_wait(&bar_full[slot], (uint32_t)((u / kURing) & 1), &abort_flag)) return -1;
+      // the producers' copies are generic-proxy writes; the tensor cores read through the async proxy
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       tc_fence_after();
-      const int x = i * kUTok + tid;
+      return slot;
+    };
+    for (int i = 0; ok && i <= nt; ++i) {
+      if (i < nt) {
+        const uint32_t dS = tb + (uint32_t)((i & 1) * 64);
+        for (int p = 0; ok && p < 5; ++p) {
+          const int slot = take();
+          if (slot < 0) {
+            ok = false;
+            break;
+          }
+          if (elect_one()) {
+            for (int b = 0; b < (p < 4 ? 2 : 1); ++b) {
+              const int kb = 2 * p + b;
+              const uint64_t dk = dk0 + (uint64_t)slot * kSlotStep + (uint64_t)b * kBlkStep;
+              const uint64_t dq = dq0 + (uint64_t)kb * kQStep;
+#pragma unroll
+              for (int ks = 0; ks < 4; ++ks)
+                umma_bf16(dS, dk + (uint64_t)(2 * ks), dq + (uint64_t)(2 * ks), id_s, (kb | ks) != 0 ? 1u : 0u);
+            }
+            umma_commit(&bar_empty[slot]);
+            if (p == 4) umma_commit(&bar_s[i & 1]);
+          }
+          __syncwarp();
+          ++u;
+        }
+      }
+      if (ok && i >= 1) {
+        const int j = i - 1;
+        ok = warp_wait(&bar_p, (uint32_t)(j & 1), &abort_flag);
+        if (ok) tc_fence_after();
+        for (int mt = 0; ok && mt < 4; ++mt) {
+          const int slot = take();
+          if (slot < 0) {
+            ok = false;
+            break;
+          }
+          if (elect_one()) {
+            const uint64_t dv = dv0 + (uint64_t)slot * kSlotStep;
+            const uint32_t dO = tb + (uint32_t)(kUTmemO + 64 * mt);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+              umma_bf16(dO, dv + (uint64_t)(128 * ks), dp + (uint64_t)(128 * ks), id_o, (j | ks) != 0 ? 1u : 0u);
+            umma_commit(&bar_empty[slot]);
+            if (mt == 3) umma_commit(&bar_pv);
+          }
+          __syncwarp();
+          ++u;
+        }
+      }
+    }
+    if (!ok && lane == 0) {
+      *(volatile uint32_t*)&abort_flag = 1u;
+      atomicOr(a.err, (uint32_t)HS_DEVERR_TIMEOUT);
+    }
+    // every product issued has completed before the accumulator can be released
+    if (elect_one()) umma_commit(&bar_fin);
+    __syncwarp();
+    {
+      volatile uint32_t never = 0u;
+      warp_wait(&bar_fin, 0u, &never);
+    }
+  } else {
+    // ---------------- softmax: warpgroup g = heads 32g..32g+31, thread = token = TMEM lane ----------------
+    // Every thread of a warpgroup passes the same sequence of its barrier: a wait that gives up only
+    // marks the thread (ok = false: no TMEM access, zero weights), so a barrier never misses a thread.
+    const int g = warp >> 2, wq = warp & 3, tok = wq * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    float lsum = 0.f;  // warp 0 of the warpgroup: running weight sum of head 32g + lane
+    bool ok = true;
+    for (int i = 0; i < nt; ++i) {
+      if (ok) ok = mbar_wait_bounded(&bar_s[i & 1], (uint32_t)((i >> 1) & 1), &abort_flag);
+      tc_fence_after();
+      const int x = i * kUTok + tok;
       const int32_t lx = x < n ? locs[x] : -1;
       const bool valid = ok && lx >= 0 && (int64_t)lx < rows_r;
+      float v[32];
+      if (ok) tmem_ld32(tb + lane_base + (uint32_t)((i & 1) * 64 + 32 * g), v);
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {  // heads [32 hh, 32 hh + 32)
-        float v[32];
-        auto load_scores = [&]() {
-          float t16[16];
-          if (!ok) {
+      for (int jj = 0; jj < 32; ++jj) v[jj] = valid ? v[jj] * a.qscale : -INFINITY;
+      bool need = false;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = -INFINITY;
-            return;
-          }
-          tmem_ld16(tb + lane_base + (uint32_t)(32 * hh), t16);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = valid ? t16[j] * a.qscale : -INFINITY;
-          tmem_ld16(tb + lane_base + (uint32_t)(32 * hh + 16), t16);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) v[16 + j] = valid ? t16[j] * a.qscale : -INFINITY;
-        };
-        load_scores();
-        bool need = false;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) need |= v[j] > s_m[32 * hh + j] + kULazy;
-        const int par = (2 * i + hh) & 1;
-        const bool need_w = __any_sync(0xffffffffu, need);
-        if (lane == 0) s_need[par][warp] = need_w ? 1u : 0u;
-        named_sync_128();
-        const bool any = (s_need[par][0] | s_need[par][1] | s_need[par][2] | s_need[par][3]) != 0u;
-        if (any) {
-          // exact tile max per head, then raise the running max where needed and rescale
-          const float wm = reduce32_max_transposed(v, lane);  // head 32 hh + lane over this warp's tokens
-          s_red[warp][32 * hh + lane] = wm;
-          named_sync_128();
-          if (tid < 32) {
-            const int h = 32 * hh + tid;
-            const float tmax = fmaxf(fmaxf(s_red[0][h], s_red[1][h]), fmaxf(s_red[2][h], s_red[3][h]));
-            const float mo = s_m[h];
-            const float mn = tmax > mo + kULazy ? tmax : mo;
-            // a head with nothing accumulated yet has zero sums and accumulators: nothing to scale
-            s_alpha[h] = (mn == mo || mo == -INFINITY) ? 1.f : fast_exp2(mo - mn);
-            s_m[h] = mn;
-            s_l[h] *= s_alpha[h];
-          }
-          named_sync_128();
-          bool resc = false;
-#pragma unroll
-          for (int j = 0; j < 32; ++j) resc |= s_alpha[32 * hh + j] != 1.f;
-          if (resc && ok) {
-            if (i >= 1) {
-              // O^T columns of these heads, all four 128-dim row tiles, scaled in TMEM
-#pragma unroll 1
-              for (int mt = 0; mt < 4; ++mt) {
-#pragma unroll
-                for (int c0 = 0; c0 < 32; c0 += 16) {
-                  float o[16];
-                  const uint32_t ta = tb + lane_base + 64u + 64u * (uint32_t)mt + (uint32_t)(32 * hh + c0);
-                  tmem_ld16(ta, o);
-#pragma unroll
-                  for (int j = 0; j < 16; ++j) o[j] *= s_alpha[32 * hh + c0 + j];
-                  tmem_st16(ta, o);
-                }
-              }
-            }
-          }
-          load_scores();
-        }
-        // weights (bf16) and P^T: heads contiguous, 8-token groups 1024 B apart
-        uint32_t pk[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float m0 = s_m[32 * hh + 2 * j], m1 = s_m[32 * hh + 2 * j + 1];
-          pk[j] = pack_bf16(valid ? fast_exp2(v[2 * j] - m0) : 0.f, valid ? fast_exp2(v[2 * j + 1] - m1) : 0.f);
-          v[2 * j] = __uint_as_float(pk[j] << 16);  // the rounded weights, as the MMA sees them
-          v[2 * j + 1] = __uint_as_float(pk[j] & 0xffff0000u);
-        }
-        uint8_t* prow = sP + (tid >> 3) * 1024 + (tid & 7) * 16;
-#pragma unroll
-        for (int hg = 0; hg < 4; ++hg)
-          *(uint4*)(prow + (4 * hh + hg) * 128) = make_uint4(pk[4 * hg], pk[4 * hg + 1], pk[4 * hg + 2], pk[4 * hg + 3]);
-        // this tile's weight sums per head: this warp's tokens, then the four warps in order
-        s_red[warp][32 * hh + lane] = reduce32_transposed(v, lane);
+      for (int j4 = 0; j4 < 8; ++j4) {
+        const float4 m4 = *(const float4*)&s_m[g][4 * j4];
+        need |= v[4 * j4] > m4.x + kULazy;
+        need |= v[4 * j4 + 1] > m4.y + kULazy;
+        need |= v[4 * j4 + 2] > m4.z + kULazy;
+        need |= v[4 * j4 + 3] > m4.w + kULazy;
       }
-      named_sync_128();
-      if (tid < kUHeads) s_l[tid] += (s_red[0][tid] + s_red[1][tid]) + (s_red[2][tid] + s_red[3][tid]);
+      const int par = i & 1;
+      const bool need_w = __any_sync(0xffffffffu, need);
+      if (lane == 0) s_need[par][g][wq] = need_w ? 1u : 0u;
+      wg_sync(g);
+      const bool any = (s_need[par][g][0] | s_need[par][g][1] | s_need[par][g][2] | s_need[par][g][3]) != 0u;
+      bool resc = false;
+      if (any) {
+        // exact tile max per head; warp 0 of the warpgroup raises the running max where needed
+        float t[32];
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) t[jj] = v[jj];
+        s_max[g][wq][lane] = reduce32_max_transposed(t, lane);  // head 32g + lane over this warp's tokens
+        wg_sync(g);
+        if (wq == 0) {
+          const float tm = fmaxf(fmaxf(s_max[g][0][lane], s_max[g][1][lane]), fmaxf(s_max[g][2][lane], s_max[g][3][lane]));
+          const float mo = s_m[g][lane];
+          const float mn = tm > mo + kULazy ? tm : mo;
+          // a head with nothing accumulated yet has zero sums and accumulators: nothing to scale
+          const float al = (mn == mo || mo == -INFINITY) ? 1.f : fast_exp2(mo - mn);
+          s_alpha[g][lane] = al;
+          s_m[g][lane] = mn;
+          lsum *= al;
+          const bool rw = __any_sync(0xffffffffu, al != 1.f);
+          if (lane == 0) s_resc[g] = rw ? 1u : 0u;
+        }
+        wg_sync(g);
+        resc = s_resc[g] != 0u;
+      }
+      // the previous tile's value product is complete: P^T may be rewritten and O^T rescaled
+      if (ok && i >= 1) ok = mbar_wait_bounded(&bar_pv, (uint32_t)((i - 1) & 1), &abort_flag);
+      tc_fence_after();
+      if (resc && ok && i >= 1) {
+#pragma unroll 1
+        for (int mt = 0; mt < 4; ++mt) {
+          float o[32];
+          const uint32_t ta = tb + lane_base + (uint32_t)(kUTmemO + 64 * mt + 32 * g);
+          tmem_ld32(ta, o);
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) o[jj] *= s_alpha[g][jj];
+          tmem_st32(ta, o);
+        }
+      }
+      // weights (bf16) and P^T: heads contiguous, 8-token groups 1024 B apart
+      uint32_t pk[16];
+#pragma unroll
+      for (int j4 = 0; j4 < 8; ++j4) {
+        const float4 m4 = *(const float4*)&s_m[g][4 * j4];
+        pk[2 * j4] = pack_bf16(valid ? fast_exp2(v[4 * j4] - m4.x) : 0.f, valid ? fast_exp2(v[4 * j4 + 1] - m4.y) : 0.f);
+        pk[2 * j4 + 1] =
+            pack_bf16(valid ? fast_exp2(v[4 * j4 + 2] - m4.z) : 0.f, valid ? fast_exp2(v[4 * j4 + 3] - m4.w) : 0.f);
+      }
+#pragma unroll
+      for (int jj = 0; jj < 16; ++jj) {
+        v[2 * jj] = __uint_as_float(pk[jj] << 16);  // the rounded weights, as the MMA sees them
+        v[2 * jj + 1] = __uint_as_float(pk[jj] & 0xffff0000u);
+      }
+      uint8_t* prow = sP + (tok >> 3) * 1024 + (tok & 7) * 16;
+#pragma unroll
+      for (int hg = 0; hg < 4; ++hg)
+        *(uint4*)(prow + (4 * g + hg) * 128) = make_uint4(pk[4 * hg], pk[4 * hg + 1], pk[4 * hg + 2], pk[4 * hg + 3]);
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // P^T is read by the tensor cores
       tc_fence_before();
       mbar_arrive(&bar_p);
+      // this tile's weight sums per head: this warp's tokens, then the four warps in order
+      s_sum[g][wq][lane] = reduce32_transposed(v, lane);
+      wg_sync(g);
+      if (wq == 0) lsum += (s_sum[g][0][lane] + s_sum[g][1][lane]) + (s_sum[g][2][lane] + s_sum[g][3][lane]);
     }
-    if (ok) ok = mbar_wait_bounded(&bar_pv, (uint32_t)((ntile - 1) & 1), &abort_flag);
+    if (ok) ok = mbar_wait_bounded(&bar_pv, (uint32_t)((nt - 1) & 1), &abort_flag);
     if (!ok) {
       *(volatile uint32_t*)&abort_flag = 1u;
       atomicOr(a.err, (uint32_t)HS_DEVERR_TIMEOUT);
     }
     tc_fence_after();
-    named_sync_128();
+    wg_sync(g);
     if (ok && abort_flag == 0u) {
-      const int64_t ph0 = ((int64_t)r * a.S + split) * a.Hq;
-      if (tid < kUHeads) *(float2*)(a.ml + (ph0 + tid) * 2) = make_float2(s_m[tid], s_l[tid]);
-      // O^T rows (value dims) of this thread, every head
+      const int64_t ph0 = ((int64_t)r * a.S + split) * a.Hq + 32 * g;
+      if (wq == 0) *(float2*)(a.ml + (ph0 + lane) * 2) = make_float2(s_m[g][lane], lsum);
+      // O^T rows (value dims) of this thread, the warpgroup's heads; a warp stores 32 consecutive dims
 #pragma unroll 1
       for (int mt = 0; mt < 4; ++mt) {
+        float o[32];
+        tmem_ld32(tb + lane_base + (uint32_t)(kUTmemO + 64 * mt + 32 * g), o);
 #pragma unroll
-        for (int c0 = 0; c0 < kUHeads; c0 += 16) {
-          float o[16];
-          tmem_ld16(tb + lane_base + 64u + 64u * (uint32_t)mt + (uint32_t)c0, o);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) a.part[(ph0 + c0 + j) * 512 + mt * 128 + tid] = o[j];
-        }
+        for (int jj = 0; jj < 32; ++jj) a.part[(ph0 + jj) * 512 + mt * 128 + tok] = o[jj];
       }
     }
   }
@@ -1492,15 +1541,25 @@ bool plan_for(const hs_config* c, int num_sms, Plan* pl) {
     pl->smem = (size_t)kGqaWarps * kGqaStages * kMmaTile * kGqaRow;
     per_cta_wave = 1;  // one CTA per SM: the staging buffers hold most of the shared memory
   } else if (c->head_dim_qk == 576 && c->head_dim_v == 512 && c->num_q_heads == kMlaHeads) {
-    // tcgen05 kernel: 128-token tiles; the tile and Q (P^T later written over Q) take the shared memory
+    // tcgen05 kernel: Q resident, the tiles streamed through the ring.  One CTA per SM; splits of any
+    // multiple of 16 tokens (a ragged last tile reads zero rows), at least 64 tokens each so that a
+    // CTA's Q load (72 KB) does not outweigh its records, at most 32 per request (the wide combine)
     pl->kind = 4;
     pl->fetch = 0;
-    pl->NW = 4;
+    pl->NW = 8;
     pl->G = kMlaHeads;
     pl->groups = 1;
-    pl->T = kUTok;
-    pl->smem = (size_t)kUKv + kUQ + 1024;  // + the alignment of the swizzled tile
-    per_cta_wave = 1;
+    pl->T = 16;
+    pl->smem = kUSmem;
+    int S = num_sms / c->num_requests;
+    const int max_s = (c->top_k + 63) / 64;
+    S = S < 1 ? 1 : (S > max_s ? max_s : S);
+    S = S > 32 ? 32 : S;
+    int chunk = (c->top_k + S - 1) / S;
+    chunk = (chunk + 15) / 16 * 16;
+    pl->chunk = chunk;
+    pl->S = (c->top_k + chunk - 1) / chunk;
+    return pl->smem <= 227 * 1024;
   } else {
     if (c->head_dim_qk != 576 || c->head_dim_v != 512) return false;
     if (c->num_q_heads % 8 != 0) return false;
@@ -1584,21 +1643,16 @@ bool encode_q_map(CUtensorMap* m, const void* q, int nreq) {
 cudaError_t dispatch(const hs_config& c, const AttnArgs* a, const Plan& pl, cudaStream_t st) {
   if (pl.kind == 4) {
     cudaError_t e = cudaSuccess;
-    if (a == nullptr) {  // preparation: shared-memory limit and carveout of both variants
-      for (auto kern : {k_attn_mla_umma<true>, k_attn_mla_umma<false>}) {
-        if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
-        if (e == cudaSuccess)
-          e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                   (int)cudaSharedmemCarveoutMaxShared);
-      }
+    if (a == nullptr) {  // preparation: shared-memory limit and carveout
+      e = cudaFuncSetAttribute(k_attn_mla_pipe, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_attn_mla_pipe, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
     } else {
-      // hot-buffer rows through the pool's tensor map (TMA gather) and Q through its own map; caller
-      // rows (or a Q the encoder refuses) by cp.async
-      CUtensorMap tm, qm;
-      memset(&tm, 0, sizeof(tm));
+      // Q through a tensor map of the launch's queries, encoded for this launch
+      CUtensorMap qm;
       memset(&qm, 0, sizeof(qm));
-      const bool tma = a->kv_tmap != nullptr && encode_q_map(&qm, a->q, a->R);
-      if (tma) tm = *a->kv_tmap;
+      if (!encode_q_map(&qm, a->q, a->R)) return cudaErrorNotSupported;
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(pl.S, a->R, pl.groups);
       cfg.blockDim = dim3(kUThreads, 1, 1);
@@ -1609,8 +1663,7 @@ cudaError_t dispatch(const hs_config& c, const AttnArgs* a, const Plan& pl, cuda
       attr[0].val.programmaticStreamSerializationAllowed = 1;
       cfg.attrs = attr;
       cfg.numAttrs = 1;
-      e = tma ? cudaLaunchKernelEx(&cfg, k_attn_mla_umma<true>, *a, tm, qm)
-              : cudaLaunchKernelEx(&cfg, k_attn_mla_umma<false>, *a, tm, qm);
+      e = cudaLaunchKernelEx(&cfg, k_attn_mla_pipe, *a, qm);
     }
     if (e == cudaSuccess && a == nullptr)
       e = cudaFuncSetAttribute(k_combine_wide, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -1677,8 +1730,6 @@ int hs_launch_attn(hs_pool* p, int layer, int r0, int nreq, const void* d_q, con
   a.locs = d_locs;
   if (kv_base == nullptr) {  // the layer's hot buffers, through the slot table
     a.kv_pt = p->slot_table + (int64_t)layer * c.num_requests * p->slot_pages;
-    a.kv_pool = p->buf;
-    a.kv_tmap = (const CUtensorMap*)p->attn_tmap;
     a.kv_cap = p->slot_cap + (int64_t)layer * c.num_requests;
     a.kv_pages = p->slot_pages;
     a.kv_shift = p->slot_shift;
@@ -1716,31 +1767,6 @@ int hs_launch_attn(hs_pool* p, int layer, int r0, int nreq, const void* d_q, con
   a.L = c.num_layers;
   a.layer = layer;
   return dispatch(c, &a, pl, st) == cudaSuccess ? HS_OK : HS_ERR_CUDA;
-}
-
-// The device cache pool as a 2-D tensor (rows = slots of every page, 576 bf16 each) for the TMA
-// gather of the tensor-core shared-latent kernel; null (and the cp.async gather) when that kernel is
-// not used or the encoder is unavailable.
-void* hs_attn_make_pool_map(const hs_config* c, int num_sms, void* pool_base, int64_t pool_rows) {
-  Plan pl;
-  if (!plan_for(c, num_sms, &pl) || pl.kind != 4 || pool_base == nullptr || pool_rows < 1) return nullptr;
-  const EncodeFn fn = tensor_map_encoder();
-  if (fn == nullptr) return nullptr;
-  CUtensorMap* tm = new (std::align_val_t(64)) CUtensorMap;
-  const cuuint64_t gdim[2] = {(cuuint64_t)kUDim, (cuuint64_t)pool_rows};
-  const cuuint64_t gstride[1] = {(cuuint64_t)kUDim * 2};
-  const cuuint32_t box[2] = {64, 1}, estr[2] = {1, 1};
-  if (fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pool_base, gdim, gstride, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
-    ::operator delete(tm, std::align_val_t(64));
-    return nullptr;
-  }
-  return tm;
-}
-
-void hs_attn_free_pool_map(void* m) {
-  if (m != nullptr) ::operator delete(m, std::align_val_t(64));
 }
 
 int hs_attn_prepare(const hs_config* c, int num_sms) {

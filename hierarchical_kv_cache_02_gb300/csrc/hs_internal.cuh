@@ -49,7 +49,6 @@ struct hs_pool {
   int slot_pages;        // pages per buffer: ceil(B / slot_page), <= kMaxSlotPages
   int slot_shift;        // log2 of the slots per page
   hs_dev_pages* dev;
-  void* attn_tmap;       // tensor map of the pool for the TMA gather of shared-latent records, or null
   int32_t* tag;
   uint32_t* stamp;
   hs_rl_state* state;
@@ -159,8 +158,5 @@ void hs_attn_workspace(const hs_config* cfg, int num_sms, size_t* floats, int* m
 bool hs_attn_supported(const hs_config* cfg);
 bool hs_attn_can_fetch(const hs_config* cfg);  // the attention can take over the miss fetch
 int hs_attn_prepare(const hs_config* cfg, int num_sms);
-// tensor map of the device cache pool for the TMA gather (host memory, opaque), or null
-void* hs_attn_make_pool_map(const hs_config* cfg, int num_sms, void* pool_base, int64_t pool_rows);
-void hs_attn_free_pool_map(void* map);
 int hs_resolve_prepare(hs_pool* pool);
 size_t hs_resolve_smem_bytes(const hs_config* cfg);

@@ -138,7 +138,6 @@ void free_pool(hs_pool* p) {
     delete p->host;
   }
   delete p->dev;
-  hs_attn_free_pool_map(p->attn_tmap);
   cudaFree(p->page_table);
   cudaFree(p->slot_table);
   cudaFree(p->slot_cap);
@@ -454,7 +453,6 @@ extern "C" int hs_pool_create(const hs_config* cfg, int cuda_device, hs_pool** o
   }
   if (rc == HS_OK) rc = hs_resolve_prepare(p);
   if (rc == HS_OK) rc = hs_attn_prepare(cfg, p->num_sms);
-  if (rc == HS_OK) p->attn_tmap = hs_attn_make_pool_map(cfg, p->num_sms, p->buf, d.total_pages * d.page_slots);
   if (rc == HS_OK) rc = do_reset(p, 0);
   if (rc == HS_OK && cudaDeviceSynchronize() != cudaSuccess) rc = HS_ERR_CUDA;
   if (rc != HS_OK) {
