@@ -56,6 +56,8 @@ WORKLOADS = {
 }
 
 
+DEFAULT_WORKLOAD = "gqa_b16_l32"
+
 # dram__bytes_read.sum + dram__bytes_write.sum of one attention launch from an ncu capture of the
 # same kernel and per-launch size (profiles/); None where no capture of the current kernel exists
 ATTN_TRAFFIC = {("gqa_b16_l32", "resolve"): 138.44e6}
@@ -451,8 +453,14 @@ def run_ours(args, w, world, rank, local):
     # pass 3: the attention alone, its L launches of the last step back to back; only where the L
     # launches together gather well over L2's size, so that no replay finds the last one's rows cached
     big = steps_exceed_l2(w)
-    attn_b2b_us = (time_attention_back_to_back(pool, wl, locs, outs, scale, W + K - 1)
-                   if M == 1 and G == 1 and big else None)
+    # a step that gathers at least half of L2 is timed as replays with L2 flushed in between; a smaller
+    # one stays in L2 from one decode step to the next, as the hot buffers of such a workload would
+    flushed = not big and w["L"] * attn_bytes_per_launch(w) * 2 >= L2_BYTES
+    attn_b2b_us = None
+    if M == 1 and G == 1 and big:
+        attn_b2b_us = time_attention_back_to_back(pool, wl, locs, outs, scale, W + K - 1)
+    elif M == 1 and G == 1 and flushed:
+        attn_b2b_us = time_attention_flushed(pool, wl, locs, outs, scale, W + K - 1)
     max_elapsed = reduce_max(elapsed, world)
     units = world * K * L
     value = units / max_elapsed
@@ -493,6 +501,9 @@ def run_ours(args, w, world, rank, local):
                    "launch": "one captured CUDA graph of the timed steps" if use_graph else "stream launches",
                    "l2": (f"inputs larger than L2 (each attention launch gathers "
                           f"{attn_bytes_per_launch(w) / 1e6:.0f} MB; a step touches {L} layers)") if big else
+                         (f"a step's {L} attention launches gather {L * attn_bytes_per_launch(w) / 1e6:.0f} MB, "
+                          "more than L2, and the steps run without a flush; the attention roofline is timed "
+                          "with L2 flushed before each replay") if flushed else
                          (f"inputs smaller than L2, no flush: a step's {L} attention launch(es) gather "
                           f"{L * attn_bytes_per_launch(w) / 1e6:.0f} MB, so the hot buffers stay in L2 "
                           "from one decode step to the next, as they would in this workload's steady state")},
@@ -510,6 +521,9 @@ def run_ours(args, w, world, rank, local):
                      "launch_us": roof_us,
                      "timing": ("CUDA events around 3 replays of a captured graph of the last timed step's "
                                 f"{L} attention launches back to back (inputs of each launch larger than L2)")
+                     if attn_b2b_us is not None and big else
+                     (f"CUDA events around each of 5 replays of a captured graph of the last timed step's {L} "
+                      "attention launches, L2 flushed before each replay (median)")
                      if attn_b2b_us is not None else "CUDA events around each launch",
                      # the same from the event pairs around each launch of the breakdown pass
                      "per_launch_events_us": attn_us,
@@ -662,6 +676,40 @@ def time_attention_back_to_back(pool, wl, locs, outs, scale, t, reps=3):
     e.record()
     torch.cuda.synchronize()
     return s.elapsed_time(e) * 1e3 / (reps * L)
+
+
+def time_attention_flushed(pool, wl, locs, outs, scale, t, reps=5):
+    """Mean device time of one attention launch for workloads whose step gathers less than twice L2:
+    the L layers' launches of step t, captured as one graph, replayed `reps` times; before each
+    replay a write of twice L2's size evicts what the last replay left there, and CUDA events on the
+    launching stream bracket the replay alone (the event pair's own latency is spread over L launches)."""
+    import torch
+
+    L = wl.w["L"]
+
+    def launches():
+        for l in range(L):
+            pool.sparse_attn(l, wl.q[t, l], locs[l], outs[l], scale=scale)
+
+    launches()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        launches()
+    graph.replay()
+    flush = torch.empty(int(2 * L2_BYTES) // 4, dtype=torch.float32, device=wl.device)
+    torch.cuda.synchronize()
+    times = []
+    for i in range(reps):
+        flush.fill_(float(i))
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        graph.replay()
+        e.record()
+        torch.cuda.synchronize()
+        times.append(s.elapsed_time(e) * 1e3 / L)
+    del flush
+    return float(np.median(times))
 
 
 def measure_h2d(device):
@@ -848,7 +896,7 @@ def main():
     ap.add_argument("--steps", type=int, default=56)
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="gqa_b16_l32")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling runs)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--microbatches", type=int, default=1,
@@ -867,6 +915,9 @@ def main():
     ap.add_argument("--no-alt", action="store_true",
                     help="skip the extra GQA passes: two micro-batches with the miss copies inside the "
                          "attention, and layer groups sharing one selection")
+    ap.add_argument("--no-latent", action="store_true",
+                    help="skip the shared-latent workloads (stress batch, MLA batch of 8) reported beside the "
+                         "default GQA line")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per attention launch from an ncu capture of the same kernel")
@@ -904,6 +955,18 @@ def main():
                                                            "clocks", "errors")}
         out["layer_group_prefetch"]["us_per_layer"] = grp["us_per_layer"]["total"]
         out["layer_group_prefetch"]["workload"] = "same sizes; layer groups of 4 share one top-k selection"
+    if (args.workload == DEFAULT_WORKLOAD and args.fetch == "auto" and not args.no_alt and not args.no_latent
+            and args.microbatches == 1 and args.index_share == 1 and not args.layers):
+        # the shared-latent workloads of the same metric, each with its own attention and resolve
+        # rooflines (the 64-head tcgen05 attention and its split combine; the resolve's host link)
+        latent = {}
+        for name in ("stress_b16_l4", "mla_b8"):
+            la = argparse.Namespace(**vars(args))
+            la.workload, la.no_e2e = name, True
+            res = run_ours(la, dict(WORKLOADS[name]), world, rank, local)
+            latent[name] = {k: res[k] for k in ("value", "unit", "ms_per_step", "us_per_layer", "miss_rate", "roofline",
+                                                "host_link", "gpu_launches", "clocks", "errors", "config")}
+        out["shared_latent"] = latent
     if rank == 0 and not args.no_cpu_baseline:
         per, desc, n = oracle_sample(w, steps=min(16, args.warmup + args.steps), seed=99, budget_s=args.cpu_seconds)
         out["cpu_baseline"] = {"value": 1.0 / (w["R"] * per), "unit": "layer-steps/s", "cores": 1, "kind": "oracle",
