@@ -976,9 +976,10 @@ constexpr int kMlaHeads = 64;  // query heads of the shared-latent tensor-core k
 
 
 // Split partials of the tensor-core shared-latent kernel, merged in split order: one warp per
-// (request, head, 128-dim quarter of the value), lane = 4 consecutive dims, every split's partial
-// loaded before any is used (one round trip to L2 rather than one per pair of splits).  The same
-// arithmetic as combine_heads_wide, so the result is identical.
+// (request, head, 128-dim quarter of the value), lane = 4 consecutive dims.  Every split's partial row
+// is requested first, then the splits' maxima and sums, so the two round trips to memory overlap
+// rather than follow one another.  The same arithmetic as combine_heads_wide, so the result is
+// identical.
 __global__ void __launch_bounds__(256, 2) k_combine_wide(AttnArgs a) {
   hs_pdl_enter();
   constexpr int DV = 512, JB = 16;
@@ -986,6 +987,12 @@ __global__ void __launch_bounds__(256, 2) k_combine_wide(AttnArgs a) {
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = (int)blockIdx.y * 2 + (w >> 2), c = w & 3;
   if (h >= a.Hq) return;
+  const float4* p = (const float4*)(a.part + ((int64_t)r * a.S * a.Hq + h) * DV) + 32 * c + lane;
+  const int64_t step = (int64_t)a.Hq * (DV / 4);  // float4s from one split's partial to the next
+  float4 v[JB];
+#pragma unroll
+  for (int j = 0; j < JB; ++j)
+    if (j < a.S) v[j] = __ldcg(p + j * step);
   const bool mine = lane < a.S;  // lane j holds split j's max and sum (S <= 32)
   const int64_t phl = ((int64_t)r * a.S + lane) * a.Hq + h;
   const float m = mine ? __ldcg(&a.ml[phl * 2]) : -INFINITY;
@@ -998,13 +1005,12 @@ __global__ void __launch_bounds__(256, 2) k_combine_wide(AttnArgs a) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  const float4* p = (const float4*)(a.part + ((int64_t)r * a.S * a.Hq + h) * DV) + 32 * c + lane;
-  const int64_t step = (int64_t)a.Hq * (DV / 4);  // float4s from one split's partial to the next
   for (int b0 = 0; b0 < a.S; b0 += JB) {
-    float4 v[JB];
+    if (b0 > 0) {
 #pragma unroll
-    for (int j = 0; j < JB; ++j)
-      if (b0 + j < a.S) v[j] = __ldcg(p + (b0 + j) * step);
+      for (int j = 0; j < JB; ++j)
+        if (b0 + j < a.S) v[j] = __ldcg(p + (b0 + j) * step);
+    }
 #pragma unroll
     for (int j = 0; j < JB; ++j) {
       if (b0 + j < a.S) {
