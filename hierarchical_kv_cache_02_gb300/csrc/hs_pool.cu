@@ -44,6 +44,7 @@ int check_config(const hs_config* c) {
   if (c->layout == HS_LAYOUT_MLA && (c->num_kv_heads != 1 || c->head_dim_v > c->head_dim_qk)) return HS_ERR_CONFIG;
   if (c->num_q_heads % c->num_kv_heads != 0) return HS_ERR_CONFIG;
   if (c->top_k < 1 || c->top_k > c->buffer_slots || c->buffer_slots > 16384) return HS_ERR_CONFIG;
+  if (c->top_k > 4096) return HS_ERR_CONFIG;  // the resolve holds a thread's four top-k entries in registers
   if (c->policy < HS_POLICY_LRU || c->policy > HS_POLICY_SWAP_VANILLA) return HS_ERR_CONFIG;
   if (c->log_steps < 0) return HS_ERR_CONFIG;
   int64_t rec = hs_record_bytes(c);

@@ -281,6 +281,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
     hs_copy_pending(a.pend + (int64_t)r * k, k, a.rec, slots_g, a.sshift, crank, a.cs);
 
   // ---------------- phase A: every CTA of the cluster computes the whole decision ----------------
+  // The loads that start it go out together: the tags and stamps of this thread's first slots, its
+  // top-k entries and, for the fused append, the new position and its host page; the hash table and
+  // the select's histograms are cleared meanwhile.  The hash is then built while the append's slot
+  // search reduces, so the two share their barriers, and the probe reuses the tags and stamps.
+  constexpr int kBatch = 4;  // slots and top-k entries a thread loads up front (k <= 4 x kThreads)
+  int32_t tb[kBatch], tk[kBatch];
+  uint32_t sb[kBatch];
+#pragma unroll
+  for (int u = 0; u < kBatch; ++u) {
+    const int j = tid + u * kThreads;
+    tb[u] = j < B ? tag[j] : -1;
+    sb[u] = j < B ? stamp[j] : 0u;
+    tk[u] = j < k ? topk[j] : -1;
+  }
   // fused write-through append (hs_append_resolve): the new position takes the slot that already
   // holds it, else the slot with the smallest eviction key over the buffer's slots; stamp = clock, clock
   // += 1; the resolve below then sees that state
@@ -289,67 +303,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
   uint32_t app_err = 0u;
   uint4* app_dh = nullptr;  // the append's place in the host history
   if (a.app_pos != nullptr) {
-    // the tags and stamps of this thread's first slots are requested before the append position and
-    // its host page, so those dependent loads overlap them
-    constexpr int kAppBatch = 4;
-    int32_t tb[kAppBatch];
-    uint32_t sb[kAppBatch];
-#pragma unroll
-    for (int u = 0; u < kAppBatch; ++u) {
-      const int j = tid + u * kThreads;
-      tb[u] = j < B ? tag[j] : -1;
-      sb[u] = j < B ? stamp[j] : 0u;
-    }
     app_p = a.app_pos[r - a.r0];
     if (app_p >= a.P0 && app_p >= 0 && app_p < a.C)
       app_dh = (uint4*)hs_page_addr(a.pt, a.max_pages, a.page_shift, a.rec, a.L, r, a.layer, app_p);
-    if (app_dh == nullptr) {  // outside [shared_prefix, capacity), or its host page is not reserved
-      app_err = (uint32_t)HS_DEVERR_APPEND;
-    } else {
-      int found = 0x7fffffff;
-      unsigned long long best = ~0ull;
-      auto visit = [&](int j, int32_t t, uint32_t sj) {
-        if (t == (int32_t)app_p) found = min(found, j);
-        const uint32_t key = hs_evict_key(a.policy, t, sj, a.seed, st.nres, a.R, r, a.L, a.layer, BK, j);
-        const unsigned long long kj = ((unsigned long long)key << 32) | (unsigned)j;
-        best = kj < best ? kj : best;
-      };
-#pragma unroll
-      for (int u = 0; u < kAppBatch; ++u) {
-        const int j = tid + u * kThreads;
-        if (j < B) visit(j, tb[u], sb[u]);
-      }
-      for (int j = tid + kAppBatch * kThreads; j < B; j += kThreads) visit(j, tag[j], stamp[j]);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        found = min(found, __shfl_xor_sync(0xffffffffu, found, o));
-        const unsigned long long y = __shfl_xor_sync(0xffffffffu, best, o);
-        best = y < best ? y : best;
-      }
-      if ((tid & 31) == 0) {
-        s_found[tid >> 5] = found;
-        s_best[tid >> 5] = best;
-      }
-      __syncthreads();
-      if (tid < 32) {  // one warp combines the warps' results
-        int f = tid < kWarps ? s_found[tid] : 0x7fffffff;
-        unsigned long long bb = tid < kWarps ? s_best[tid] : ~0ull;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          f = min(f, __shfl_xor_sync(0xffffffffu, f, o));
-          const unsigned long long y = __shfl_xor_sync(0xffffffffu, bb, o);
-          bb = y < bb ? y : bb;
-        }
-        if (tid == 0) s_app_slot = f != 0x7fffffff ? f : (int)(bb & 0xffffffffull);
-      }
-      __syncthreads();
-      app_slot = s_app_slot;
-    }
+    if (app_dh == nullptr) app_err = (uint32_t)HS_DEVERR_APPEND;  // outside [shared_prefix, capacity), or no page
   }
-  const uint32_t clock = st.clock + (app_slot >= 0 ? 1u : 0u);  // the resolve's clock
   __shared__ uint32_t s_dups, s_klo, s_khi;
   if (tid == 0) {
-    err_bits = app_err | (((uint64_t)clock + (uint64_t)k >= 0xFFFFFFFFull) ? (uint32_t)HS_DEVERR_CLOCK : 0u);
+    err_bits = app_err;
     s_dups = 0u;
     s_klo = 0xffffffffu;
     s_khi = 0u;
@@ -363,44 +324,88 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
 
   // (1) hash the selected positions; a key keeps the smallest top-k index that carries it.  Entries
   // start as misses (-1) or invalid (-2); repeats are sorted out below only when an insert met its key.
-  for (int i = tid; i < k; i += kThreads) {
-    const int32_t s = topk[i];
+#pragma unroll
+  for (int u = 0; u < kBatch; ++u) {
+    const int i = tid + u * kThreads;
+    if (i >= k) break;
+    const int32_t sv = tk[u];
     int32_t state = -2;
-    if (s >= 0 && (int64_t)s < a.C) {
-      uint32_t h = ht_hash(s, a.ht_bits);
+    if (sv >= 0 && (int64_t)sv < a.C) {
+      uint32_t hh = ht_hash(sv, a.ht_bits);
       while (true) {
-        const int32_t prev = atomicCAS(&ht_key[h], -1, s);
-        if (prev == -1 || prev == s) {
-          atomicMin(&ht_val[h], i);
-          if (prev == s) s_dups = 1u;
+        const int32_t prev = atomicCAS(&ht_key[hh], -1, sv);
+        if (prev == -1 || prev == sv) {
+          atomicMin(&ht_val[hh], i);
+          if (prev == sv) s_dups = 1u;
           break;
         }
-        h = (h + 1) & (uint32_t)(ht_size - 1);
+        hh = (hh + 1) & (uint32_t)(ht_size - 1);
       }
       state = -1;
-    } else if (s != -1) {
+    } else if (sv != -1) {
       atomicOr(&err_bits, (uint32_t)HS_DEVERR_RANGE);
     }
     hit_slot[i] = state;
   }
-  __syncthreads();
+  // the append's slot search over the tags and stamps already loaded (and the rest of the slots)
+  const bool app_on = a.app_pos != nullptr && app_dh != nullptr;
+  if (app_on) {
+    int found = 0x7fffffff;
+    unsigned long long best = ~0ull;
+    auto visit = [&](int j, int32_t t, uint32_t sj) {
+      if (t == (int32_t)app_p) found = min(found, j);
+      const uint32_t key = hs_evict_key(a.policy, t, sj, a.seed, st.nres, a.R, r, a.L, a.layer, BK, j);
+      const unsigned long long kj = ((unsigned long long)key << 32) | (unsigned)j;
+      best = kj < best ? kj : best;
+    };
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int j = tid + u * kThreads;
+      if (j < B) visit(j, tb[u], sb[u]);
+    }
+    for (int j = tid + kBatch * kThreads; j < B; j += kThreads) visit(j, tag[j], stamp[j]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      found = min(found, __shfl_xor_sync(0xffffffffu, found, o));
+      const unsigned long long y = __shfl_xor_sync(0xffffffffu, best, o);
+      best = y < best ? y : best;
+    }
+    if ((tid & 31) == 0) {
+      s_found[tid >> 5] = found;
+      s_best[tid >> 5] = best;
+    }
+  }
+  __syncthreads();  // the hash table and the append's per-warp results are complete
+  if (app_on && tid < 32) {  // one warp combines the warps' results
+    int f = tid < kWarps ? s_found[tid] : 0x7fffffff;
+    unsigned long long bb = tid < kWarps ? s_best[tid] : ~0ull;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      f = min(f, __shfl_xor_sync(0xffffffffu, f, o));
+      const unsigned long long y = __shfl_xor_sync(0xffffffffu, bb, o);
+      bb = y < bb ? y : bb;
+    }
+    if (tid == 0) s_app_slot = f != 0x7fffffff ? f : (int)(bb & 0xffffffffull);
+  }
   if (s_dups != 0u) {  // a repeated position: only its first occurrence (smallest index) is valid
     for (int i = tid; i < k; i += kThreads) {
       if (hit_slot[i] != -1) continue;
-      const int32_t s = topk[i];
-      uint32_t h = ht_hash(s, a.ht_bits);
-      while (ht_key[h] != s) h = (h + 1) & (uint32_t)(ht_size - 1);
-      if (ht_val[h] != i) {
+      const int32_t sv = topk[i];
+      uint32_t hh = ht_hash(sv, a.ht_bits);
+      while (ht_key[hh] != sv) hh = (hh + 1) & (uint32_t)(ht_size - 1);
+      if (ht_val[hh] != i) {
         hit_slot[i] = -2;
         atomicOr(&err_bits, (uint32_t)HS_DEVERR_DUP);
       }
     }
-    __syncthreads();
   }
+  __syncthreads();  // the append's slot and the sorted-out repeats are known
+  if (app_on) app_slot = s_app_slot;
+  const uint32_t clock = st.clock + (app_slot >= 0 ? 1u : 0u);  // the resolve's clock
+  if (tid == 0 && (uint64_t)clock + (uint64_t)k >= 0xFFFFFFFFull) atomicOr(&err_bits, (uint32_t)HS_DEVERR_CLOCK);
 
-  // (2) probe every slot; keep its eviction key and the candidates' key range.  The tags and stamps
-  // of a thread's first kProbeBatch slots are loaded together before any is probed, so their load
-  // latencies overlap instead of following one another through the probe loop.
+  // (2) probe every slot; keep its eviction key and the candidates' key range (the tags and stamps of
+  // a thread's first kBatch slots are the ones loaded at the start).
   uint32_t klo = 0xffffffffu, khi = 0u;
   auto probe_slot = [&](int j, int32_t tj, uint32_t sj) {
     const bool is_app = j == app_slot;
@@ -429,21 +434,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
     }
   };
   {
-    constexpr int kProbeBatch = 4;
-    int32_t tb[kProbeBatch];
-    uint32_t sb[kProbeBatch];
 #pragma unroll
-    for (int u = 0; u < kProbeBatch; ++u) {
-      const int j = tid + u * kThreads;
-      tb[u] = j < B ? tag[j] : -1;
-      sb[u] = j < B ? stamp[j] : 0u;
-    }
-#pragma unroll
-    for (int u = 0; u < kProbeBatch; ++u) {
+    for (int u = 0; u < kBatch; ++u) {
       const int j = tid + u * kThreads;
       if (j < B) probe_slot(j, tb[u], sb[u]);
     }
-    for (int j = tid + kProbeBatch * kThreads; j < B; j += kThreads) probe_slot(j, tag[j], stamp[j]);
+    for (int j = tid + kBatch * kThreads; j < B; j += kThreads) probe_slot(j, tag[j], stamp[j]);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {

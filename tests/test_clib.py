@@ -46,6 +46,7 @@ def test_record_bytes(lib):
 
 @pytest.mark.parametrize("change", [
     dict(top_k=5000, buffer_slots=4096),          # k > B
+    dict(top_k=4097, buffer_slots=8192),          # k above the resolve's limit of 4096
     dict(buffer_slots=20000, top_k=10),           # B too large
     dict(io_chunk_bytes=48),                      # not a power of two
     dict(io_chunk_bytes=256),                     # above the limit
