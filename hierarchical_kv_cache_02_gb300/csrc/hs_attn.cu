@@ -25,6 +25,18 @@
 
 #include "hs_internal.cuh"
 
+#ifdef HS_PHASE_TRACE
+// phase stamps of k_attn_mla_pipe (see HS_PHASE); read and cleared by the two calls below
+__device__ unsigned long long hs_phase_attn[256][64];
+extern "C" int hs_phase_attn_read(void* host) {
+  return (int)cudaMemcpyFromSymbol(host, hs_phase_attn, sizeof(hs_phase_attn));
+}
+extern "C" int hs_phase_attn_clear() {
+  static unsigned long long zero[256][64];
+  return (int)cudaMemcpyToSymbol(hs_phase_attn, zero, sizeof(zero));
+}
+#endif
+
 namespace {
 
 constexpr int kStages = 3;
@@ -1189,6 +1201,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 
 __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_pipe(AttnArgs a, const __grid_constant__ CUtensorMap qmap) {
   hs_pdl_enter();
+  HS_PHASE(hs_phase_attn, 0, threadIdx.x == 0);
   extern __shared__ __align__(128) uint8_t smem_raw[];
   // Q and the ring start 1024-byte aligned (the period of the 128-byte swizzle); the launch adds 1 KB
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -1250,6 +1263,7 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_pipe(AttnArgs a, cons
   tc_fence_after();
   const uint32_t tb = s_tmem;
   const uint32_t sq_u = smem_u32(sQ), ring_u = smem_u32(sRing), sp_u = smem_u32(sP);
+  HS_PHASE(hs_phase_attn, 1, tid == 0);
 
   if (warp >= kUWarpProd) {
     // ---------------- producers: Q once by TMA, then the tiles' blocks through the ring ----------------
@@ -1282,6 +1296,7 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_pipe(AttnArgs a, cons
           }
         }
       }
+      HS_PHASE(hs_phase_attn, 2 + u, lane == 0 && pw == 0 && u < 18);  // load u issued
       cp_async_arrive_noinc(&bar_full[slot]);
       ++u;
       return true;
@@ -1349,6 +1364,7 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_pipe(AttnArgs a, cons
             ok = false;
             break;
           }
+          HS_PHASE(hs_phase_attn, 20 + u, lane == 0 && u < 18);  // load u landed, its score products issued
           if (elect_one()) {
             for (int b = 0; b < (p < 4 ? 2 : 1); ++b) {
               const int kb = 2 * p + b;
@@ -1359,6 +1375,7 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_pipe(AttnArgs a, cons
                 umma_bf16(dS, dk + (uint64_t)(2 * ks), dq + (uint64_t)(2 * ks), id_s, (kb | ks) != 0 ? 1u : 0u);
             }
             umma_commit(&bar_empty[slot]);
+            HS_PHASE(hs_phase_attn, 38 + i, p == 4 && i < 2);  // scores of tile i complete (issued)
             if (p == 4) umma_commit(&bar_s[i & 1]);
           }
           __syncwarp();
@@ -1383,6 +1400,7 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_pipe(AttnArgs a, cons
               umma_bf16(dO, dv + (uint64_t)(128 * ks), dp + (uint64_t)(128 * ks), id_o, (j | ks) != 0 ? 1u : 0u);
             umma_commit(&bar_empty[slot]);
             if (mt == 3) umma_commit(&bar_pv);
+            HS_PHASE(hs_phase_attn, 40 + j, mt == 3 && j < 3);  // value product of tile j issued
           }
           __syncwarp();
           ++u;
@@ -1411,6 +1429,7 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_pipe(AttnArgs a, cons
     for (int i = 0; i < nt; ++i) {
       if (ok) ok = mbar_wait_bounded(&bar_s[i & 1], (uint32_t)((i >> 1) & 1), &abort_flag);
       tc_fence_after();
+      HS_PHASE(hs_phase_attn, 43 + i, tid == 0 && i < 3);  // softmax saw the scores of tile i
       const int x = i * kUTok + tok;
       const int32_t lx = x < n ? locs[x] : -1;
       const bool valid = ok && lx >= 0 && (int64_t)lx < rows_r;
@@ -1490,11 +1509,13 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_pipe(AttnArgs a, cons
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // P^T is read by the tensor cores
       tc_fence_before();
       mbar_arrive(&bar_p);
+      HS_PHASE(hs_phase_attn, 46 + i, tid == 0 && i < 3);  // weights of tile i written
       // this tile's weight sums per head: this warp's tokens, then the four warps in order
       s_sum[g][wq][lane] = reduce32_transposed(v, lane);
       wg_sync(g);
       if (wq == 0) lsum += (s_sum[g][0][lane] + s_sum[g][1][lane]) + (s_sum[g][2][lane] + s_sum[g][3][lane]);
     }
+    HS_PHASE(hs_phase_attn, 49, tid == 0);
     if (ok) ok = mbar_wait_bounded(&bar_pv, (uint32_t)((nt - 1) & 1), &abort_flag);
     if (!ok) {
       *(volatile uint32_t*)&abort_flag = 1u;
@@ -1513,6 +1534,7 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_pipe(AttnArgs a, cons
 #pragma unroll
         for (int jj = 0; jj < 32; ++jj) a.part[(ph0 + jj) * 512 + mt * 128 + tok] = o[jj];
       }
+      HS_PHASE(hs_phase_attn, 50, tid == 0);  // partial written
     }
   }
   tc_fence_before();

@@ -147,6 +147,26 @@ __device__ __forceinline__ void hs_pdl_enter() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// ---- phase stamps (built only with -DHS_PHASE_TRACE, for the phase tables of the profiles) ----
+// Thread 0 of each of the first 256 CTAs of a launch records %globaltimer at numbered points of a
+// kernel into `table` ([256][64], a device array of the kernel's translation unit, read out by its
+// hs_phase_*_read function).  The normal build compiles the stamps away.
+#ifdef HS_PHASE_TRACE
+#define HS_PHASE(table, ev, cond)                                                                \
+  do {                                                                                          \
+    const unsigned _c = blockIdx.x + gridDim.x * blockIdx.y;                                    \
+    if ((cond) && _c < 256u) {                                                                  \
+      unsigned long long _t;                                                                    \
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(_t));                                    \
+      table[_c][ev] = _t;                                                                       \
+    }                                                                                           \
+  } while (0)
+#else
+#define HS_PHASE(table, ev, cond) \
+  do {                            \
+  } while (0)
+#endif
+
 // ---- launchers (defined in the kernel translation units) -------------------
 int hs_launch_resolve(hs_pool* pool, int layer, int r0, int nreq, const int64_t* d_pos, const void* d_rec,
                       const int32_t* d_topk, int32_t* d_locs, cudaStream_t st);

@@ -24,6 +24,18 @@
 
 #include "hs_internal.cuh"
 
+#ifdef HS_PHASE_TRACE
+// phase stamps of k_resolve (see HS_PHASE); read and cleared by the two calls below
+__device__ unsigned long long hs_phase_res[256][64];
+extern "C" int hs_phase_resolve_read(void* host) {
+  return (int)cudaMemcpyFromSymbol(host, hs_phase_res, sizeof(hs_phase_res));
+}
+extern "C" int hs_phase_resolve_clear() {
+  static unsigned long long zero[256][64];
+  return (int)cudaMemcpyToSymbol(hs_phase_res, zero, sizeof(zero));
+}
+#endif
+
 namespace {
 
 constexpr int kThreads = 1024;
@@ -218,6 +230,7 @@ __device__ void select_threshold(const uint32_t* key32, const uint8_t* flag, int
 template <int NV>
 __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
   hs_pdl_enter();
+  HS_PHASE(hs_phase_res, 0, threadIdx.x == 0);
   extern __shared__ __align__(16) uint8_t smem[];
   const int r = a.r0 + (int)(blockIdx.x / a.cs);
   const int crank = blockIdx.x % a.cs;  // rank inside the cluster of this request
@@ -322,6 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
   for (int x = tid; x < 2 * 2048; x += kThreads) hist[x >> 11][x & 2047] = 0u;
   __syncthreads();
 
+  HS_PHASE(hs_phase_res, 1, tid == 0);
   // (1) hash the selected positions; a key keeps the smallest top-k index that carries it.  Entries
   // start as misses (-1) or invalid (-2); repeats are sorted out below only when an insert met its key.
 #pragma unroll
@@ -404,6 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
   const uint32_t clock = st.clock + (app_slot >= 0 ? 1u : 0u);  // the resolve's clock
   if (tid == 0 && (uint64_t)clock + (uint64_t)k >= 0xFFFFFFFFull) atomicOr(&err_bits, (uint32_t)HS_DEVERR_CLOCK);
 
+  HS_PHASE(hs_phase_res, 2, tid == 0);
   // (2) probe every slot; keep its eviction key and the candidates' key range (the tags and stamps of
   // a thread's first kBatch slots are the ones loaded at the start).
   uint32_t klo = 0xffffffffu, khi = 0u;
@@ -454,6 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
   // every old tag and stamp this CTA needs has been read and used: the cluster's writes may follow
   if (a.cs > 1) cluster_arrive_relaxed();
 
+  HS_PHASE(hs_phase_res, 3, tid == 0);
   // (3a) rank hits and misses in top-k order; list the misses
   const int kpt = (k + kThreads - 1) / kThreads;
   const int i0 = min(k, tid * kpt), i1 = min(k, i0 + kpt);
@@ -479,6 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
     }
   }
 
+  HS_PHASE(hs_phase_res, 4, tid == 0);
   // (4, early) this CTA's first misses start crossing the host link now; the victims are chosen
   // meanwhile and the staged records reach their slots in phase B
   const int q0 = (int)((int64_t)m * crank / a.cs), q1 = (int)((int64_t)m * (crank + 1) / a.cs);
@@ -499,12 +516,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
     asm volatile("cp.async.commit_group;" ::: "memory");
   }
 
+  HS_PHASE(hs_phase_res, 5, tid == 0);
   // (3b) threshold of the m smallest candidate keys
   const int ncand = B - h;
   const bool take_all = (m == ncand);
   uint32_t T = 0u, need_eq = 0u;
   if (m > 0 && !take_all) select_threshold(key32, flag, B, (uint32_t)m, s_klo, s_khi, wbuf, hist, sel, &T, &need_eq);
 
+  HS_PHASE(hs_phase_res, 6, tid == 0);
   // (3c) ordered compaction: the q-th victim in ascending slot order
   if (m > 0) {
     const int bpt = (B + kThreads - 1) / kThreads;
@@ -546,6 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
   // every CTA of the request has read the old tags and stamps before anyone writes them
   __syncthreads();
   if (a.cs > 1) cluster_wait();
+  HS_PHASE(hs_phase_res, 7, tid == 0);
 
   // ---------------- phase B: this CTA's share of the writes and of the fetch ----------------
   {
@@ -603,6 +623,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
         if (!restamped) stamp[app_slot] = st.clock;
       }
     }
+    HS_PHASE(hs_phase_res, 8, tid == 0);
     // (4) fetch this CTA's share of the misses from the host history (or leave it to the attention)
     if (a.pend == nullptr && q1 > q0) {
       // host addresses of this CTA's misses, resolved once (in the hash table's space: dead by now)
@@ -629,6 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
     }
   }
 
+  HS_PHASE(hs_phase_res, 9, tid == 0);
   // (5) clock and counters
   if (crank == 0 && tid == 0) {
     hs_rl_state ns = st;

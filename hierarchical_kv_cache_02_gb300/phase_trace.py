@@ -1,0 +1,120 @@
+"""Phase tables of the fused resolve and the shared-latent tensor-core attention.
+
+Builds a variant of the library with -DHS_PHASE_TRACE (in _build/phase/, leaving the normal build
+alone), in which thread 0 of each CTA records %globaltimer at the boundaries of the kernels' phases.
+For each named workload of bench.py it runs the decode steps to a steady state, records one launch
+of the resolve (layer 0) and, for the shared-latent workloads, one launch of the attention, and
+prints the median over the CTAs of each stamp, in microseconds from the first CTA's start.
+
+    python -m hierarchical_kv_cache_02_gb300.phase_trace gqa_b16_l32 mla_b8 stress_b16_l4
+
+Needs a GPU.  The workloads are those of bench.py (GQA with 4 of its 32 layers: one layer's steady
+state is the same).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import sys
+
+import numpy as np
+
+from . import build as _build
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+TRACE_LIB = os.path.join(_build.BUILD, "phase", "libhisparse_phase.so")
+
+RESOLVE = ["start", "append slot", "hash", "probe", "rank", "early copies issued", "select",
+           "compaction + cluster sync", "writes", "host fetch"]
+ATTN = {0: "start", 1: "setup", 38: "scores of tile 0 issued", 39: "scores of tile 1 issued",
+        40: "value product of tile 0 issued", 41: "value product of tile 1 issued",
+        43: "softmax: scores of tile 0 seen", 44: "softmax: scores of tile 1 seen",
+        46: "softmax: weights of tile 0 written", 47: "softmax: weights of tile 1 written",
+        49: "softmax: waiting for the last value product", 50: "partial written"}
+for _u in range(18):
+    ATTN[2 + _u] = f"load {_u} issued"
+    ATTN[20 + _u] = f"load {_u} landed (score products issued)"
+
+
+def _table(tr, names):
+    used = tr[:, 0] > 0
+    if not used.any():
+        return []
+    t0 = int(tr[used, 0].min())
+    rows = []
+    for ev in sorted(names):
+        col = tr[used, ev].astype(np.int64)
+        col = col[col > 0]
+        if len(col):
+            rel = (col - t0) / 1e3
+            rows.append((names[ev], len(col), float(np.median(rel)), float(rel.min()), float(rel.max())))
+    return rows, int(used.sum())
+
+
+def main(argv):
+    root = os.path.dirname(_HERE)
+    if root not in sys.path:
+        sys.path.insert(0, root)
+    _build.build_library(force=True, extra_flags=("-DHS_PHASE_TRACE",), lib=TRACE_LIB,
+                         build_dir=os.path.join(_build.BUILD, "phase"))
+    _build.LIB = TRACE_LIB  # this process loads the traced variant
+    import torch
+
+    import bench
+    from . import HsPool, _lib
+
+    lib = _lib.load()
+    for fn in ("hs_phase_resolve_read", "hs_phase_attn_read"):
+        getattr(lib, fn).argtypes = [ctypes.c_void_p]
+    for fn in ("hs_phase_resolve_clear", "hs_phase_attn_clear"):
+        getattr(lib, fn).argtypes = []
+    for name in argv or ["gqa_b16_l32", "mla_b8", "stress_b16_l4"]:
+        w = dict(bench.WORKLOADS[name])
+        if name == "gqa_b16_l32":
+            w["L"] = 4
+        W = 24
+        wl = bench.Workload(w, W + 1, "cuda", seed=bench.replica_seed(0))
+        pool = HsPool(wl.cfg)
+        wl.prefill(pool)
+        R, L, k = w["R"], w["L"], w["k"]
+        locs = [torch.empty((R, k), dtype=torch.int32, device="cuda") for _ in range(L)]
+        outs = [torch.empty((R, w["Hq"], w["Dv"]), dtype=torch.float32, device="cuda") for _ in range(L)]
+        appends = w.get("appends", True)
+        res_tr = np.zeros((256, 64), dtype=np.uint64)
+        att_tr = np.zeros((256, 64), dtype=np.uint64)
+        for t in range(W + 1):
+            for l in range(L):
+                traced = t == W and l == 0
+                if traced:
+                    torch.cuda.synchronize()
+                    lib.hs_phase_resolve_clear()
+                    lib.hs_phase_attn_clear()
+                    torch.cuda.synchronize()
+                if appends:
+                    pool.append_resolve(l, wl.pos[t], wl.app[t, l], wl.topk[t, l], locs[l])
+                else:
+                    pool.resolve(l, wl.topk[t, l], locs[l])
+                if traced:
+                    torch.cuda.synchronize()
+                    lib.hs_phase_resolve_read(res_tr.ctypes.data)
+                pool.sparse_attn(l, wl.q[t, l], locs[l], outs[l], scale=wl.cfg.default_scale)
+                if traced:
+                    torch.cuda.synchronize()
+                    lib.hs_phase_attn_read(att_tr.ctypes.data)
+        st = pool.stats()
+        pool.close()
+        print(f"{name}: misses per (request, layer, step) {st['misses'] / (R * L * (W + 1)):.0f} of k = {k}")
+        rows, n = _table(res_tr, dict(enumerate(RESOLVE)))
+        print(f"  k_resolve, {n} CTAs (median / min / max over the CTAs, us from the first CTA's start)")
+        for nm, cnt, med, lo, hi in rows:
+            print(f"    {nm:44s} {med:7.2f} {lo:7.2f} {hi:7.2f}")
+        tab = _table(att_tr, ATTN)
+        if tab:
+            rows, n = tab
+            print(f"  k_attn_mla_pipe, {n} CTAs")
+            for nm, cnt, med, lo, hi in rows:
+                print(f"    {nm:44s} {med:7.2f} {lo:7.2f} {hi:7.2f}   ({cnt} CTAs)")
+
+
+if __name__ == "__main__":
+    main(sys.argv[1:])
