@@ -5,8 +5,8 @@
 //   * k_attn_gqa: GQA records, one CTA per (request, KV head); bulk-copy producers and consumers
 //     on mma.sync in a transposed form (tokens on the MMA's row side);
 //   * k_attn_mla_pipe: shared-latent records with 64 query heads on tcgen05 tensor cores, the
-//     accumulators in tensor memory, the tiles streamed by TMA through a ring; split partials merged
-//     by k_combine_wide;
+//     accumulators in tensor memory, Q loaded once by TMA and the tiles streamed through a ring by
+//     16-byte cp.async; split partials merged by k_combine_wide;
 //   * k_attn_cc: CUDA-core fallback for other shared-latent head counts (a producer warp gathers
 //     whole records with cp.async.bulk into a 3-stage ring; consumers reduce 32 logits per lane
 //     with a transposed butterfly and keep an online softmax in base 2).
