@@ -1051,13 +1051,15 @@ __global__ void __launch_bounds__(256, 2) k_combine_wide(AttnArgs a) {
 // tile (128 rows x 128 B per block) in the 128-byte swizzled layout the MMA reads.  Six producer
 // warps fill a slot with 16-byte cp.async copies straight into that layout: one warp instruction
 // moves four whole 128-byte lines (rows 4q..4q+3, lane -> row 4q + lane / 8, chunk lane % 8, stored at
-// chunk (lane % 8) XOR (row % 8)), so the loads are fully coalesced.  Every tile is gathered twice: its
-// nine blocks for the scores (five slot loads: dims 0-127, ..., 384-511, then 512-575 alone), then its
-// eight value blocks for the value product (four slot loads), which the first pass has just brought
-// into L2.  The load order is
+// chunk (lane % 8) XOR (row % 8)), so the loads are fully coalesced.  In a split of several tiles every
+// tile is gathered twice: its nine blocks for the scores (five slot loads: dims 512-575 alone, then
+// 0-127, ..., 384-511), then its eight value blocks for the value product (four slot loads), which the
+// first pass has just brought into L2.  The load order is
 //   K(0), K(1), V(0), K(2), V(1), ..., K(n-1), V(n-2), V(n-1),
 // and one thread of warp 8 consumes the loads in that order, issuing S(0), S(1), PV(0), S(2), PV(1),
-// ..., so the scores of tile i+1 are computed while the softmax of tile i runs.
+// ..., so the scores of tile i+1 are computed while the softmax of tile i runs.  A split of one tile
+// loads only K(0): the slot of dims 512-575 is released after the scores, the four slots of dims 0-511
+// stay in place for the value product.
 // Why this shape (measured on this GPU, per SM): a tcgen05.mma costs its issuing thread 51-75 cycles
 // whatever its size up to N = 128, so 128-token tiles (68 products per 128 tokens) beat 64-token tiles
 // with M = 64 products (104); holding a 128-token tile's value blocks from the score pass to the value
@@ -1209,7 +1211,7 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_pipe(AttnArgs a, cons
   uint8_t* sRing = smem + kUQ;
   uint8_t* sP = sRing + kURing * kUSlot;
   __shared__ __align__(8) uint64_t bar_full[kURing], bar_empty[kURing];
-  __shared__ __align__(8) uint64_t bar_q, bar_s[2], bar_p, bar_pv, bar_fin;
+  __shared__ __align__(8) uint64_t bar_q, bar_s[2], bar_p, bar_pv, bar_fin, bar_o[4];
   __shared__ uint32_t s_tmem, abort_flag;
   __shared__ uint32_t s_need[2][2][4];            // [parity][warpgroup][warp]
   __shared__ uint32_t s_resc[2];                  // [warpgroup]: some head's max was raised this tile
@@ -1224,6 +1226,9 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_pipe(AttnArgs a, cons
   const int t0 = split * a.chunk;
   const int n = min(a.k, t0 + a.chunk) - t0;
   const int nt = (n + kUTok - 1) / kUTok;
+  // a split of one tile keeps the four slots of its value blocks from the score pass to the value
+  // product (nothing else is loaded after them); longer splits re-read the values from L2
+  const bool hold = nt == 1;
   if (tid == 0) {
     for (int s = 0; s < kURing; ++s) {
       mbar_init(&bar_full[s], (uint32_t)(kUProd * 32));  // every producer thread, once its copies land
@@ -1235,6 +1240,7 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_pipe(AttnArgs a, cons
     mbar_init(&bar_p, 256u);  // every softmax thread, once its weights are in place
     mbar_init(&bar_pv, 1u);
     mbar_init(&bar_fin, 1u);
+    for (int mt = 0; mt < 4; ++mt) mbar_init(&bar_o[mt], 1u);  // value rows 128 mt.. of the last tile done
     abort_flag = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -1313,10 +1319,13 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_pipe(AttnArgs a, cons
           }
           rows_k[e] = loc >= 0 ? (uint64_t)(uintptr_t)row_addr(s_pg, a.kv_shift, a.rec, loc) : 0ull;
         }
-        for (int p = 0; ok && p < 5; ++p) ok = load(rows_k, 2 * p, p < 4 ? 2 : 1);  // scores: all 9 blocks
+        // scores: all 9 blocks, the last one first, so that blocks 0-7 (the values) fill whole slots
+        ok = load(rows_k, 8, 1);
+        for (int p = 0; ok && p < 4; ++p) ok = load(rows_k, 2 * p, 2);
       }
-      if (i >= 1)
-        for (int p = 0; ok && p < 4; ++p) ok = load(rows_v, 2 * p, 2);  // values of the tile before
+      // values of the tile before; a split of one tile keeps its value blocks from the score pass
+      if (i >= 1 && !hold)
+        for (int p = 0; ok && p < 4; ++p) ok = load(rows_v, 2 * p, 2);
 #pragma unroll
       for (int e = 0; e < kURowsPerLane; ++e) rows_v[e] = rows_k[e];
     }
@@ -1341,9 +1350,10 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_pipe(AttnArgs a, cons
     const uint64_t dq0 = umma_sdesc(sq_u, 16, 1024, 2);         // Q block 0, K-major swizzled
     const uint64_t dk0 = umma_sdesc(ring_u, 16, 1024, 2);       // ring slot 0 as a K operand
     // V^T MN-major from the same bytes: LBO = 16 KB between a slot's two 64-dim blocks, SBO = 1 KB
-    // between 8-token groups; P^T MN-major, no swizzle (heads contiguous)
+    // between 8-token groups; P^T MN-major, 128-byte swizzled (a token's 64 heads fill one 128-byte
+    // row, so N holds a single atom), SBO = 1 KB between 8-token groups
     const uint64_t dv0 = umma_sdesc(ring_u, kUBlk, 1024, 2);
-    const uint64_t dp = umma_sdesc(sp_u, 1024, 128);
+    const uint64_t dp = umma_sdesc(sp_u, kUP, 1024, 2);
     constexpr uint64_t kSlotStep = kUSlot >> 4, kBlkStep = kUBlk >> 4, kQStep = 8192 >> 4;
     bool ok = warp_wait(&bar_q, 0u, &abort_flag);
     int u = 0;  // loads consumed
@@ -1366,15 +1376,16 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_pipe(AttnArgs a, cons
           }
           HS_PHASE(hs_phase_attn, 20 + u, lane == 0 && u < 18);  // load u landed, its score products issued
           if (elect_one()) {
-            for (int b = 0; b < (p < 4 ? 2 : 1); ++b) {
-              const int kb = 2 * p + b;
+            // load 0 of a tile is block 8, load p >= 1 blocks 2(p-1) and 2(p-1)+1
+            for (int b = 0; b < (p == 0 ? 1 : 2); ++b) {
+              const int kb = p == 0 ? 8 : 2 * (p - 1) + b;
               const uint64_t dk = dk0 + (uint64_t)slot * kSlotStep + (uint64_t)b * kBlkStep;
               const uint64_t dq = dq0 + (uint64_t)kb * kQStep;
 #pragma unroll
               for (int ks = 0; ks < 4; ++ks)
-                umma_bf16(dS, dk + (uint64_t)(2 * ks), dq + (uint64_t)(2 * ks), id_s, (kb | ks) != 0 ? 1u : 0u);
+                umma_bf16(dS, dk + (uint64_t)(2 * ks), dq + (uint64_t)(2 * ks), id_s, (p | ks) != 0 ? 1u : 0u);
             }
-            umma_commit(&bar_empty[slot]);
+            if (p == 0 || !hold) umma_commit(&bar_empty[slot]);
             HS_PHASE(hs_phase_attn, 38 + i, p == 4 && i < 2);  // scores of tile i complete (issued)
             if (p == 4) umma_commit(&bar_s[i & 1]);
           }
@@ -1386,8 +1397,10 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_pipe(AttnArgs a, cons
         const int j = i - 1;
         ok = warp_wait(&bar_p, (uint32_t)(j & 1), &abort_flag);
         if (ok) tc_fence_after();
+        HS_PHASE(hs_phase_attn, 51, lane == 0 && j == 0);  // the MMA thread saw the weights of tile 0
         for (int mt = 0; ok && mt < 4; ++mt) {
-          const int slot = take();
+          // held: value blocks 2mt, 2mt+1 are score load 1 + mt of the split's only tile, still in place
+          const int slot = hold ? (1 + mt) % kURing : take();
           if (slot < 0) {
             ok = false;
             break;
@@ -1398,12 +1411,14 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_pipe(AttnArgs a, cons
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)
               umma_bf16(dO, dv + (uint64_t)(128 * ks), dp + (uint64_t)(128 * ks), id_o, (j | ks) != 0 ? 1u : 0u);
-            umma_commit(&bar_empty[slot]);
+            if (!hold) umma_commit(&bar_empty[slot]);
             if (mt == 3) umma_commit(&bar_pv);
+            if (j == nt - 1) umma_commit(&bar_o[mt]);  // the epilogue reads these rows meanwhile
             HS_PHASE(hs_phase_attn, 40 + j, mt == 3 && j < 3);  // value product of tile j issued
+            HS_PHASE(hs_phase_attn, 52 + mt, j == 0);           // its value rows 128 mt.. issued (tile 0)
           }
           __syncwarp();
-          ++u;
+          if (!hold) ++u;
         }
       }
     }
@@ -1502,10 +1517,13 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_pipe(AttnArgs a, cons
         v[2 * jj] = __uint_as_float(pk[jj] << 16);  // the rounded weights, as the MMA sees them
         v[2 * jj + 1] = __uint_as_float(pk[jj] & 0xffff0000u);
       }
-      uint8_t* prow = sP + (tok >> 3) * 1024 + (tok & 7) * 16;
+      // P^T row tok: the 64 heads' weights (128 B), 128-byte swizzled like the tiles (the 16-byte
+      // chunk of heads 8c..8c+7 at chunk c XOR (tok mod 8))
+      uint8_t* prow = sP + tok * 128;
 #pragma unroll
       for (int hg = 0; hg < 4; ++hg)
-        *(uint4*)(prow + (4 * g + hg) * 128) = make_uint4(pk[4 * hg], pk[4 * hg + 1], pk[4 * hg + 2], pk[4 * hg + 3]);
+        *(uint4*)(prow + (((4 * g + hg) ^ (tok & 7)) << 4)) =
+            make_uint4(pk[4 * hg], pk[4 * hg + 1], pk[4 * hg + 2], pk[4 * hg + 3]);
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // P^T is read by the tensor cores
       tc_fence_before();
       mbar_arrive(&bar_p);
@@ -1516,26 +1534,28 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_pipe(AttnArgs a, cons
       if (wq == 0) lsum += (s_sum[g][0][lane] + s_sum[g][1][lane]) + (s_sum[g][2][lane] + s_sum[g][3][lane]);
     }
     HS_PHASE(hs_phase_attn, 49, tid == 0);
-    if (ok) ok = mbar_wait_bounded(&bar_pv, (uint32_t)((nt - 1) & 1), &abort_flag);
-    if (!ok) {
-      *(volatile uint32_t*)&abort_flag = 1u;
-      atomicOr(a.err, (uint32_t)HS_DEVERR_TIMEOUT);
-    }
-    tc_fence_after();
-    wg_sync(g);
-    if (ok && abort_flag == 0u) {
-      const int64_t ph0 = ((int64_t)r * a.S + split) * a.Hq + 32 * g;
-      if (wq == 0) *(float2*)(a.ml + (ph0 + lane) * 2) = make_float2(s_m[g][lane], lsum);
-      // O^T rows (value dims) of this thread, the warpgroup's heads; a warp stores 32 consecutive dims
+    // the partial, 128 value rows at a time as the last tile's value product completes them: O^T
+    // rows (value dims) of this thread, the warpgroup's heads; a warp stores 32 consecutive dims
+    const int64_t ph0 = ((int64_t)r * a.S + split) * a.Hq + 32 * g;
 #pragma unroll 1
-      for (int mt = 0; mt < 4; ++mt) {
+    for (int mt = 0; mt < 4; ++mt) {
+      if (ok) ok = mbar_wait_bounded(&bar_o[mt], 0u, &abort_flag);
+      tc_fence_after();
+      HS_PHASE(hs_phase_attn, 56, tid == 0 && mt == 0);  // value rows 0-127 of the last tile complete
+      if (ok && abort_flag == 0u) {
         float o[32];
         tmem_ld32(tb + lane_base + (uint32_t)(kUTmemO + 64 * mt + 32 * g), o);
 #pragma unroll
         for (int jj = 0; jj < 32; ++jj) a.part[(ph0 + jj) * 512 + mt * 128 + tok] = o[jj];
       }
-      HS_PHASE(hs_phase_attn, 50, tid == 0);  // partial written
     }
+    if (!ok) {
+      *(volatile uint32_t*)&abort_flag = 1u;
+      atomicOr(a.err, (uint32_t)HS_DEVERR_TIMEOUT);
+    }
+    // max and sum last: a split that gave up leaves them unwritten
+    if (ok && abort_flag == 0u && wq == 0) *(float2*)(a.ml + (ph0 + lane) * 2) = make_float2(s_m[g][lane], lsum);
+    HS_PHASE(hs_phase_attn, 50, tid == 0);  // partial written
   }
   tc_fence_before();
   __syncthreads();

@@ -188,8 +188,18 @@ __device__ void select_threshold(const uint32_t* key32, const uint8_t* flag, int
         const uint64_t v = (uint64_t)(key32[j] - lo);
         if ((v >> (shift + width)) == prefix) digit = (uint32_t)(v >> shift) & (uint32_t)(nb - 1);
       }
-      const uint32_t peers = __match_any_sync(0xffffffffu, digit);
-      if (digit != 0xffffffffu && lane == __ffs(peers) - 1) atomicAdd(&h[digit], (uint32_t)__popc(peers));
+      // the lanes sharing the first counted lane's digit add once (empty slots and old stamps crowd
+      // into a few bins); the others add one each
+      const uint32_t part = __ballot_sync(0xffffffffu, digit != 0xffffffffu);
+      if (part != 0u) {
+        const uint32_t d0 = __shfl_sync(0xffffffffu, digit, __ffs(part) - 1);
+        const uint32_t same = __ballot_sync(0xffffffffu, digit == d0);
+        if (digit == d0) {
+          if (lane == __ffs(same) - 1) atomicAdd(&h[digit], (uint32_t)__popc(same));
+        } else if (digit != 0xffffffffu) {
+          atomicAdd(&h[digit], 1u);
+        }
+      }
     }
     __syncthreads();
     // bins [BPT tid, BPT tid + BPT): find the bin where the running count reaches `need`
@@ -470,28 +480,37 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
   if (a.cs > 1) cluster_arrive_relaxed();
 
   HS_PHASE(hs_phase_res, 3, tid == 0);
-  // (3a) rank hits and misses in top-k order; list the misses
-  const int kpt = (k + kThreads - 1) / kThreads;
-  const int i0 = min(k, tid * kpt), i1 = min(k, i0 + kpt);
+  // (3a) rank hits and misses in top-k order; list the misses.  Each warp takes a run of consecutive
+  // entries, 32 at a time, and ranks its lanes by ballot.
+  const int lane = tid & 31;
+  const uint32_t below = (1u << lane) - 1u;  // the lanes before this one
+  const int kchunk = (((k + kWarps - 1) / kWarps) + 31) & ~31;
+  const int i0 = min(k, (tid >> 5) * kchunk), i1 = min(k, i0 + kchunk);
   uint32_t local = 0;
-  for (int i = i0; i < i1; ++i) {
-    const int32_t hs = hit_slot[i];
-    local += hs >= 0 ? 1u : (hs == -1 ? 0x10000u : 0u);
+  for (int ib = i0; ib < i1; ib += 32) {
+    const int i = ib + lane;
+    const int32_t hs = i < i1 ? hit_slot[i] : -2;
+    local += (uint32_t)__popc(__ballot_sync(0xffffffffu, hs >= 0)) +
+             ((uint32_t)__popc(__ballot_sync(0xffffffffu, hs == -1)) << 16);
   }
   uint32_t tot;
-  const uint32_t pre = cta_exclusive_scan(local, wbuf, &tot);
+  const uint32_t pre = __shfl_sync(0xffffffffu, cta_exclusive_scan(lane == 0 ? local : 0u, wbuf, &tot), 0);
   const int h = (int)(tot & 0xffffu), m = (int)(tot >> 16);
   {
     uint32_t a_rank = pre & 0xffffu, q_rank = pre >> 16;
-    for (int i = i0; i < i1; ++i) {
-      const int32_t hs = hit_slot[i];
+    for (int ib = i0; ib < i1; ib += 32) {
+      const int i = ib + lane;
+      const int32_t hs = i < i1 ? hit_slot[i] : -2;
+      const uint32_t bh = __ballot_sync(0xffffffffu, hs >= 0), bm = __ballot_sync(0xffffffffu, hs == -1);
       if (hs >= 0) {
-        erank[i] = (int32_t)a_rank++;
+        erank[i] = (int32_t)(a_rank + (uint32_t)__popc(bh & below));
       } else if (hs == -1) {
-        miss_idx[q_rank] = i;
-        miss_pos[q_rank] = topk[i];
-        ++q_rank;
+        const uint32_t q = q_rank + (uint32_t)__popc(bm & below);
+        miss_idx[q] = i;
+        miss_pos[q] = topk[i];
       }
+      a_rank += (uint32_t)__popc(bh);
+      q_rank += (uint32_t)__popc(bm);
     }
   }
 
@@ -524,42 +543,52 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
   if (m > 0 && !take_all) select_threshold(key32, flag, B, (uint32_t)m, s_klo, s_khi, wbuf, hist, sel, &T, &need_eq);
 
   HS_PHASE(hs_phase_res, 6, tid == 0);
-  // (3c) ordered compaction: the q-th victim in ascending slot order
+  // (3c) ordered compaction: the q-th victim in ascending slot order.  A slot is a victim when its
+  // key is below T, or equals T and fewer than need_eq slots below it do; each warp takes a run of
+  // consecutive slots, 32 at a time, and ranks its lanes by ballot.
   if (m > 0) {
-    const int bpt = (B + kThreads - 1) / kThreads;
-    const int j0 = min(B, tid * bpt), j1 = min(B, j0 + bpt);
-    uint32_t cnt = 0;
-    for (int j = j0; j < j1; ++j) {
-      if (flag[j] & 1u) continue;
-      if (take_all) {
-        cnt += 1u;
-      } else {
-        const uint32_t key = key32[j];
-        cnt += key < T ? 1u : (key == T ? 0x10000u : 0u);
+    const int chunk = (((B + kWarps - 1) / kWarps) + 31) & ~31;
+    const int j0 = min(B, (tid >> 5) * chunk), j1 = min(B, j0 + chunk);
+    auto classify = [&](int j, bool& lt, bool& eq) {
+      lt = false;
+      eq = false;
+      if (j < j1 && !(flag[j] & 1u)) {
+        if (take_all) {
+          lt = true;
+        } else {
+          const uint32_t key = key32[j];
+          lt = key < T;
+          eq = key == T;
+        }
       }
+    };
+    uint32_t cnt = 0;
+    for (int jb = j0; jb < j1; jb += 32) {
+      bool lt, eq;
+      classify(jb + lane, lt, eq);
+      cnt += (uint32_t)__popc(__ballot_sync(0xffffffffu, lt)) + ((uint32_t)__popc(__ballot_sync(0xffffffffu, eq)) << 16);
     }
     uint32_t tot2;
-    const uint32_t pre2 = cta_exclusive_scan(cnt, wbuf, &tot2);
+    const uint32_t pre2 = __shfl_sync(0xffffffffu, cta_exclusive_scan(lane == 0 ? cnt : 0u, wbuf, &tot2), 0);
     uint32_t less_b = pre2 & 0xffffu, eq_b = pre2 >> 16;
-    for (int j = j0; j < j1; ++j) {
-      if (flag[j] & 1u) continue;
+    for (int jb = j0; jb < j1; jb += 32) {
+      const int j = jb + lane;
+      bool lt, eq;
+      classify(j, lt, eq);
+      const uint32_t bl = __ballot_sync(0xffffffffu, lt), be = __ballot_sync(0xffffffffu, eq);
+      const uint32_t lb = less_b + (uint32_t)__popc(bl & below), eb = eq_b + (uint32_t)__popc(be & below);
       int q = -1;
-      if (take_all) {
-        q = (int)less_b++;
-      } else {
-        const uint32_t key = key32[j];
-        if (key < T) {
-          q = (int)(less_b + min(eq_b, need_eq));
-          ++less_b;
-        } else if (key == T) {
-          if (eq_b < need_eq) q = (int)(less_b + eq_b);
-          ++eq_b;
-        }
+      if (lt) {
+        q = (int)(lb + min(eb, need_eq));
+      } else if (eq && eb < need_eq) {
+        q = (int)(lb + eb);
       }
       if (q >= 0) {
         victims[q] = j;
         flag[j] |= 2u;
       }
+      less_b += (uint32_t)__popc(bl);
+      eq_b += (uint32_t)__popc(be);
     }
   }
   // every CTA of the request has read the old tags and stamps before anyone writes them
