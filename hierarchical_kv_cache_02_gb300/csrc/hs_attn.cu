@@ -993,8 +993,10 @@ constexpr int kMlaHeads = 64;  // query heads of the shared-latent tensor-core k
 // rather than follow one another.  The same arithmetic as combine_heads_wide, so the result is
 // identical.
 __global__ void __launch_bounds__(256, 2) k_combine_wide(AttnArgs a) {
+  HS_PHASE(hs_phase_attn, 57, threadIdx.x == 0);  // combine CTA resident
   hs_pdl_enter();
-  constexpr int DV = 512, JB = 16;
+  HS_PHASE(hs_phase_attn, 58, threadIdx.x == 0);  // the attention grid is complete
+  constexpr int DV = 512, JB = 24;  // splits requested at once (one round trip up to 24 splits)
   const int r = a.r0 + (int)blockIdx.x;
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = (int)blockIdx.y * 2 + (w >> 2), c = w & 3;
@@ -1037,6 +1039,7 @@ __global__ void __launch_bounds__(256, 2) k_combine_wide(AttnArgs a) {
   const float inv = den > 0.f ? 1.f / den : 0.f;
   ((float4*)(a.out + ((int64_t)(r - a.r0) * a.Hq + h) * DV))[32 * c + lane] =
       make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+  HS_PHASE(hs_phase_attn, 59, threadIdx.x == 0);  // this CTA's rows written
 }
 
 // ---- shared-latent records on tcgen05 tensor cores (64 heads), pipelined over tiles --------
@@ -1057,9 +1060,13 @@ __global__ void __launch_bounds__(256, 2) k_combine_wide(AttnArgs a) {
 // first pass has just brought into L2.  The load order is
 //   K(0), K(1), V(0), K(2), V(1), ..., K(n-1), V(n-2), V(n-1),
 // and one thread of warp 8 consumes the loads in that order, issuing S(0), S(1), PV(0), S(2), PV(1),
-// ..., so the scores of tile i+1 are computed while the softmax of tile i runs.  A split of one tile
-// loads only K(0): the slot of dims 512-575 is released after the scores, the four slots of dims 0-511
-// stay in place for the value product.
+// ..., so the scores of tile i+1 are computed while the softmax of tile i runs.  (Alternating the
+// slot loads of K(i+1) and V(i) measured slower: the value product of tile i then waits for its
+// softmax while holding slots, and its products arrive one 128-row tile at a time.)  A value
+// product takes two 128-row tiles of O^T at a time and interleaves their k-steps, so consecutive
+// products accumulate into different TMEM columns (measured: 90 instead of 125 cycles a product).
+// A split of one tile loads only K(0): the slot of dims 512-575 is released after the scores, the
+// four slots of dims 0-511 stay in place for the value product.
 // Why this shape (measured on this GPU, per SM): a tcgen05.mma costs its issuing thread 51-75 cycles
 // whatever its size up to N = 128, so 128-token tiles (68 products per 128 tokens) beat 64-token tiles
 // with M = 64 products (104); holding a 128-token tile's value blocks from the score pass to the value
@@ -1080,7 +1087,7 @@ __global__ void __launch_bounds__(256, 2) k_combine_wide(AttnArgs a) {
 // CTA that gives up writes no partial.
 constexpr int kUTok = 128, kUHeads = 64, kUDim = 576;
 constexpr int kUQ = kUHeads * kUDim * 2;   // 73728 B: Q, nine 64-dim blocks of 64 heads x 128 B
-constexpr int kUP = kUTok * kUHeads * 2;   // 16384 B: P^T of one tile
+constexpr int kUP = kUTok * kUHeads * 2;   // 16384 B: the weights P of one tile
 constexpr int kUBlk = kUTok * 128;         // 16384 B: one 64-dim block of a tile
 constexpr int kUSlot = 2 * kUBlk;          // a ring slot holds two blocks
 constexpr int kURing = 4;                  // ring slots
@@ -1307,19 +1314,29 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_pipe(AttnArgs a, cons
       ++u;
       return true;
     };
+    int32_t lcur[kURowsPerLane];  // slot indices of this lane's rows of the tile about to be loaded
+#pragma unroll
+    for (int e = 0; e < kURowsPerLane; ++e) lcur[e] = lfirst[e];
     for (int i = 0; ok && i <= nt; ++i) {
       if (i < nt) {
 #pragma unroll
         for (int e = 0; e < kURowsPerLane; ++e) {
-          const int q = pw + kUProd * e, x = i * kUTok + 4 * q + crow;
-          int32_t loc = i == 0 ? lfirst[e] : ((q < 32 && x < n) ? locs[x] : -1);
+          int32_t loc = lcur[e];
           if (loc < -1 || (int64_t)loc >= rows_r) {
             bad = true;
             loc = -1;
           }
           rows_k[e] = loc >= 0 ? (uint64_t)(uintptr_t)row_addr(s_pg, a.kv_shift, a.rec, loc) : 0ull;
         }
-        // scores: all 9 blocks, the last one first, so that blocks 0-7 (the values) fill whole slots
+        // the next tile's slot indices are requested now, a tile ahead of their use
+#pragma unroll
+        for (int e = 0; e < kURowsPerLane; ++e) {
+          const int q = pw + kUProd * e, x = (i + 1) * kUTok + 4 * q + crow;
+          lcur[e] = (i + 1 < nt && q < 32 && x < n) ? locs[x] : -1;
+        }
+      }
+      // scores: all 9 blocks, the last one first, so that blocks 0-7 (the values) fill whole slots
+      if (i < nt) {
         ok = load(rows_k, 8, 1);
         for (int p = 0; ok && p < 4; ++p) ok = load(rows_k, 2 * p, 2);
       }
@@ -1343,17 +1360,17 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_pipe(AttnArgs a, cons
     }
   } else if (warp == kUWarpMma) {
     // ---------------- MMA issuer: S(0), S(1), PV(0), S(2), PV(1), ... ----------------
-    const uint32_t id_s = umma_idesc_bf16(128, 64, 0, 0), id_o = umma_idesc_bf16(128, 64, 1, 1);
+    const uint32_t id_s = umma_idesc_bf16(128, 64, 0, 0), id_o = umma_idesc_bf16(128, 64, 1, 0);
     // operand descriptors, built once: a score k-step moves 32 B inside an operand (2 in the
     // descriptor's address field, 16-byte units), a value k-step of 16 tokens 2 KB (128); no carry:
     // shared addresses stay below 256 KB
     const uint64_t dq0 = umma_sdesc(sq_u, 16, 1024, 2);         // Q block 0, K-major swizzled
     const uint64_t dk0 = umma_sdesc(ring_u, 16, 1024, 2);       // ring slot 0 as a K operand
     // V^T MN-major from the same bytes: LBO = 16 KB between a slot's two 64-dim blocks, SBO = 1 KB
-    // between 8-token groups; P^T MN-major, 128-byte swizzled (a token's 64 heads fill one 128-byte
-    // row, so N holds a single atom), SBO = 1 KB between 8-token groups
+    // between 8-token groups; P K-major swizzled like Q (two 8 KB blocks of 64 tokens; a k-step of
+    // 16 tokens moves 32 B inside a block)
     const uint64_t dv0 = umma_sdesc(ring_u, kUBlk, 1024, 2);
-    const uint64_t dp = umma_sdesc(sp_u, kUP, 1024, 2);
+    const uint64_t dp = umma_sdesc(sp_u, 16, 1024, 2);
     constexpr uint64_t kSlotStep = kUSlot >> 4, kBlkStep = kUBlk >> 4, kQStep = 8192 >> 4;
     bool ok = warp_wait(&bar_q, 0u, &abort_flag);
     int u = 0;  // loads consumed
@@ -1366,6 +1383,7 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_pipe(AttnArgs a, cons
       return slot;
     };
     for (int i = 0; ok && i <= nt; ++i) {
+      const int j = i - 1;  // the tile whose value product is issued in this round
       if (i < nt) {
         const uint32_t dS = tb + (uint32_t)((i & 1) * 64);
         for (int p = 0; ok && p < 5; ++p) {
@@ -1393,32 +1411,44 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_pipe(AttnArgs a, cons
           ++u;
         }
       }
-      if (ok && i >= 1) {
-        const int j = i - 1;
+      if (ok && j >= 0) {
+        // the values of tile j (a split of one tile: still in place from its score pass)
         ok = warp_wait(&bar_p, (uint32_t)(j & 1), &abort_flag);
         if (ok) tc_fence_after();
         HS_PHASE(hs_phase_attn, 51, lane == 0 && j == 0);  // the MMA thread saw the weights of tile 0
-        for (int mt = 0; ok && mt < 4; ++mt) {
-          // held: value blocks 2mt, 2mt+1 are score load 1 + mt of the split's only tile, still in place
-          const int slot = hold ? (1 + mt) % kURing : take();
-          if (slot < 0) {
-            ok = false;
-            break;
+        // two 128-row tiles of O^T at a time, their k-steps interleaved so that consecutive products
+        // accumulate into different TMEM columns
+        for (int pr = 0; ok && pr < 2; ++pr) {
+          int sl[2];
+          for (int x = 0; ok && x < 2; ++x) {
+            // held: value blocks 2mt, 2mt+1 are score load 1 + mt of the split's only tile, still in place
+            sl[x] = hold ? (1 + 2 * pr + x) % kURing : take();
+            if (sl[x] < 0) ok = false;
+            if (!hold) ++u;
           }
+          if (!ok) break;
           if (elect_one()) {
-            const uint64_t dv = dv0 + (uint64_t)slot * kSlotStep;
-            const uint32_t dO = tb + (uint32_t)(kUTmemO + 64 * mt);
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks)
-              umma_bf16(dO, dv + (uint64_t)(128 * ks), dp + (uint64_t)(128 * ks), id_o, (j | ks) != 0 ? 1u : 0u);
-            if (!hold) umma_commit(&bar_empty[slot]);
-            if (mt == 3) umma_commit(&bar_pv);
-            if (j == nt - 1) umma_commit(&bar_o[mt]);  // the epilogue reads these rows meanwhile
-            HS_PHASE(hs_phase_attn, 40 + j, mt == 3 && j < 3);  // value product of tile j issued
-            HS_PHASE(hs_phase_attn, 52 + mt, j == 0);           // its value rows 128 mt.. issued (tile 0)
+            for (int ks = 0; ks < 8; ++ks) {
+              const uint64_t dpk = dp + (uint64_t)((ks >> 2) * kQStep + 2 * (ks & 3));
+#pragma unroll
+              for (int x = 0; x < 2; ++x)
+                umma_bf16(tb + (uint32_t)(kUTmemO + 64 * (2 * pr + x)), dv0 + (uint64_t)sl[x] * kSlotStep + (uint64_t)(128 * ks),
+                          dpk, id_o, (j | ks) != 0 ? 1u : 0u);
+            }
+            if (!hold) {
+              umma_commit(&bar_empty[sl[0]]);
+              umma_commit(&bar_empty[sl[1]]);
+            }
+            if (pr == 1) umma_commit(&bar_pv);
+            if (j == nt - 1) {  // the epilogue reads these rows meanwhile
+              umma_commit(&bar_o[2 * pr]);
+              umma_commit(&bar_o[2 * pr + 1]);
+            }
+            HS_PHASE(hs_phase_attn, 40 + j, pr == 1 && j < 3);  // value product of tile j issued
+            HS_PHASE(hs_phase_attn, 53 + 2 * pr, j == 0);        // its value rows 256 pr.. issued (tile 0)
           }
           __syncwarp();
-          if (!hold) ++u;
         }
       }
     }
@@ -1489,7 +1519,7 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_pipe(AttnArgs a, cons
         wg_sync(g);
         resc = s_resc[g] != 0u;
       }
-      // the previous tile's value product is complete: P^T may be rewritten and O^T rescaled
+      // the previous tile's value product is complete: P may be rewritten and O^T rescaled
       if (ok && i >= 1) ok = mbar_wait_bounded(&bar_pv, (uint32_t)((i - 1) & 1), &abort_flag);
       tc_fence_after();
       if (resc && ok && i >= 1) {
@@ -1503,7 +1533,7 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_pipe(AttnArgs a, cons
           tmem_st32(ta, o);
         }
       }
-      // weights (bf16) and P^T: heads contiguous, 8-token groups 1024 B apart
+      // weights (bf16)
       uint32_t pk[16];
 #pragma unroll
       for (int j4 = 0; j4 < 8; ++j4) {
@@ -1517,14 +1547,20 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_pipe(AttnArgs a, cons
         v[2 * jj] = __uint_as_float(pk[jj] << 16);  // the rounded weights, as the MMA sees them
         v[2 * jj + 1] = __uint_as_float(pk[jj] & 0xffff0000u);
       }
-      // P^T row tok: the 64 heads' weights (128 B), 128-byte swizzled like the tiles (the 16-byte
-      // chunk of heads 8c..8c+7 at chunk c XOR (tok mod 8))
-      uint8_t* prow = sP + tok * 128;
+      // P (the value product's B operand, K-major): two blocks of 64 tokens, each 64 head rows of
+      // 128 B, 128-byte swizzled like Q (tokens 8c..8c+7 of head h in the 16-byte chunk c XOR (h mod 8)).
+      // A warp's store of one head writes 64 contiguous bytes of its row: no bank conflict.
+      {
+        uint8_t* pblk = sP + (tok >> 6) * 8192 + (tok & 7) * 2;
+        const int c = (tok & 63) >> 3;
 #pragma unroll
-      for (int hg = 0; hg < 4; ++hg)
-        *(uint4*)(prow + (((4 * g + hg) ^ (tok & 7)) << 4)) =
-            make_uint4(pk[4 * hg], pk[4 * hg + 1], pk[4 * hg + 2], pk[4 * hg + 3]);
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // P^T is read by the tensor cores
+        for (int jj = 0; jj < 16; ++jj) {
+          const int h0 = 32 * g + 2 * jj;
+          *(uint16_t*)(pblk + h0 * 128 + ((c ^ (h0 & 7)) << 4)) = (uint16_t)(pk[jj] & 0xffffu);
+          *(uint16_t*)(pblk + (h0 + 1) * 128 + ((c ^ ((h0 + 1) & 7)) << 4)) = (uint16_t)(pk[jj] >> 16);
+        }
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // P is read by the tensor cores
       tc_fence_before();
       mbar_arrive(&bar_p);
       HS_PHASE(hs_phase_attn, 46 + i, tid == 0 && i < 3);  // weights of tile i written

@@ -31,9 +31,9 @@ ATTN = {0: "start", 1: "setup", 38: "scores of tile 0 issued", 39: "scores of ti
         43: "softmax: scores of tile 0 seen", 44: "softmax: scores of tile 1 seen",
         46: "softmax: weights of tile 0 written", 47: "softmax: weights of tile 1 written",
         49: "softmax: waiting for the last value product", 50: "partial written",
-        51: "value product of tile 0: weights seen", 52: "value rows 0-127 of tile 0 issued",
-        53: "value rows 128-255 of tile 0 issued", 54: "value rows 256-383 of tile 0 issued",
-        55: "value rows 384-511 of tile 0 issued", 56: "softmax: value rows 0-127 of the last tile complete"}
+        51: "value product of tile 0: weights seen", 53: "value rows 0-255 of tile 0 issued",
+        55: "value rows 256-511 of tile 0 issued", 56: "softmax: value rows 0-127 of the last tile complete",
+        57: "combine: CTA resident", 58: "combine: attention grid complete", 59: "combine: rows written"}
 for _u in range(18):
     ATTN[2 + _u] = f"load {_u} issued"
     ATTN[20 + _u] = f"load {_u} landed (score products issued)"
@@ -46,7 +46,7 @@ def _table(tr, names):
     t0 = int(tr[used, 0].min())
     rows = []
     for ev in sorted(names):
-        col = tr[used, ev].astype(np.int64)
+        col = tr[:, ev].astype(np.int64)  # every CTA that stamped it (a later kernel may have more)
         col = col[col > 0]
         if len(col):
             rel = (col - t0) / 1e3
