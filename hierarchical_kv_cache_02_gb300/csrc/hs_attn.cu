@@ -1069,16 +1069,17 @@ __global__ void __launch_bounds__(256, 2) k_combine_wide(AttnArgs a) {
 // four slots of dims 0-511 stay in place for the value product.
 // Why this shape (measured on this GPU, per SM): a tcgen05.mma costs its issuing thread 51-75 cycles
 // whatever its size up to N = 128, so 128-token tiles (68 products per 128 tokens) beat 64-token tiles
-// with M = 64 products (104); holding a 128-token tile's value blocks from the score pass to the value
-// pass would need 128 KB beside Q and stall the next tile's loads; TMA tile::gather4 builds the same
+// with M = 64 products (104); in a split of several tiles, holding a tile's value blocks (128 KB beside
+// Q) from its score pass to its value pass would stall the next tile's loads; TMA tile::gather4 builds the same
 // layout but completes only about 60 of its 512-byte gathers per microsecond (32 GB/s), while 16-byte
 // cp.async reaches about 42 GB/s from HBM and 50 GB/s from L2; a ring with one in-order consumer
 // never waits on a slot two loads ahead (two consumers of one ring can, and an mbarrier parity test
 // then passes a phase early).
 // Roles: warps 9-14 produce (each lane keeps the record addresses of its rows of a tile in registers;
-// the first tile's slot indices are requested before the setup barrier); warp 8 allocates TMEM and one
-// of its threads issues the MMAs, releasing each ring slot by a commit once its products are done;
-// warps 0-7 run the softmax as two warpgroups, warpgroup g on heads 32g..32g+31, each thread on one
+// the first tile's slot indices are requested before the setup barrier, each later tile's a tile
+// ahead); warp 8 allocates TMEM and one of its threads issues the MMAs, releasing each ring slot by
+// a commit once its products are done; the partial is stored as the last tile's value product
+// completes each 128 rows of it; warps 0-7 run the softmax as two warpgroups, warpgroup g on heads 32g..32g+31, each thread on one
 // token (= TMEM lane).  S alternates between two TMEM buffers (columns 0-63, 64-127).  The running
 // max of a head is raised only when a score exceeds it by more than 2^8 (softmax is shift-invariant;
 // weights stay <= 256, exact in bf16's range), and only then is its O^T column rescaled in TMEM.

@@ -93,16 +93,23 @@ def main(argv):
                     lib.hs_phase_resolve_clear()
                     lib.hs_phase_attn_clear()
                     torch.cuda.synchronize()
-                if appends:
-                    pool.append_resolve(l, wl.pos[t], wl.app[t, l], wl.topk[t, l], locs[l])
-                else:
-                    pool.resolve(l, wl.topk[t, l], locs[l])
+
+                def layer():
+                    if appends:
+                        pool.append_resolve(l, wl.pos[t], wl.app[t, l], wl.topk[t, l], locs[l])
+                    else:
+                        pool.resolve(l, wl.topk[t, l], locs[l])
+                    pool.sparse_attn(l, wl.q[t, l], locs[l], outs[l], scale=wl.cfg.default_scale)
+
+                # every layer runs as a captured graph replayed once, as in the bench, so the traced
+                # layer's timeline shows the kernels' launch overlap without host launch costs
+                graph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(graph):
+                    layer()
+                graph.replay()
                 if traced:
                     torch.cuda.synchronize()
                     lib.hs_phase_resolve_read(res_tr.ctypes.data)
-                pool.sparse_attn(l, wl.q[t, l], locs[l], outs[l], scale=wl.cfg.default_scale)
-                if traced:
-                    torch.cuda.synchronize()
                     lib.hs_phase_attn_read(att_tr.ctypes.data)
         st = pool.stats()
         pool.close()
@@ -112,6 +119,21 @@ def main(argv):
         for nm, cnt, med, lo, hi in rows:
             print(f"    {nm:44s} {med:7.2f} {lo:7.2f} {hi:7.2f}")
         tab = _table(att_tr, ATTN)
+        # one timeline over both tables (the same %globaltimer), from the resolve's first CTA start
+        r0 = int(res_tr[res_tr[:, 0] > 0, 0].min())
+
+        def _span(tr, ev, fn):
+            col = tr[:, ev].astype(np.int64)
+            col = col[col > 0]
+            return (fn(col) - r0) / 1e3 if len(col) else float("nan")
+
+        line = (f"  timeline (us from the resolve's first CTA start): resolve done {_span(res_tr, 9, np.max):.2f}")
+        if tab:
+            line += (f", attention first CTA {_span(att_tr, 0, np.min):.2f}, last partial "
+                     f"{_span(att_tr, 50, np.max):.2f}")
+            if (att_tr[:, 59] > 0).any():
+                line += f", combine done {_span(att_tr, 59, np.max):.2f}"
+        print(line)
         if tab:
             rows, n = tab
             print(f"  k_attn_mla_pipe, {n} CTAs")

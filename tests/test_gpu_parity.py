@@ -331,10 +331,20 @@ def test_mla_64_heads_no_append(policy):
 
 @pytest.mark.parametrize("R,k", [(2, 2048), (3, 1024)])
 def test_mla_64_heads_long_selections(R, k):
-    """Few requests with long selections: 16 (R = 2) or 8 (R = 3) splits per request, whose partials
-    a GPU that fits every request's cluster at once merges in distributed shared memory."""
+    """Few requests with long selections: 32 (R = 2) or 16 (R = 3) splits of 64 tokens per request
+    (one-tile splits: the value blocks stay in place from the score pass), merged by the split
+    combine."""
     sc = Scenario(_mla(R, 1, 6000 + 6, k, 2 * k, Hq=64), ctx0=6000, steps=6, appends=True, keep=0.85,
                   recency_mean=800, seed=17)
+    run_and_compare(sc, fused=True)
+
+
+def test_mla_64_heads_multi_tile_splits():
+    """Many requests: on 152 SMs, 3 splits per request of 352, 352 and 320 tokens, i.e. three 128-token tiles
+    each (the last one ragged), so the score pass of a tile runs while the previous tile's value
+    blocks are re-read, and the running max and sums carry across tiles."""
+    sc = Scenario(_mla(40, 1, 3000 + 4, 1024, 2048, Hq=64), ctx0=3000, steps=4, appends=True, keep=0.85,
+                  recency_mean=400, seed=23)
     run_and_compare(sc, fused=True)
 
 
@@ -455,7 +465,7 @@ def test_exactness_cold_warm_resident_bit_identical():
     """Summary §3: the output over the hot buffer equals the output over fully resident KV,
     bit for bit, whatever the cache held before."""
     for cfg in (_gqa(3, 1, 5000, 512, 1024), _gqa(3, 1, 5000, 512, 1024, fetch=1), _mla(2, 1, 5000, 512, 1024, Hq=32),
-                _mla(2, 1, 5000, 512, 1024, Hq=64)):  # 64 heads: hot rows by TMA gather, resident rows by cp.async
+                _mla(2, 1, 5000, 512, 1024, Hq=64)):  # 64 heads: the tcgen05 kernel, hot slots vs resident rows
         sc = Scenario(cfg, ctx0=5000, steps=10, appends=False, keep=0.85, recency_mean=300, seed=2)
         warm = HsPool(cfg)
         prefill(warm, sc)
