@@ -105,9 +105,42 @@ __device__ __forceinline__ uint4 ld_nc_v4(const uint4* p) {
   return v;
 }
 
-__device__ __forceinline__ void cp_async16(void* smem_dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(smem_dst)),
-               "l"(src)
+// mbarrier and bulk-copy helpers for the early miss copies
+__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ void mbar_init1(uint64_t* bar) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_expect(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive1(uint64_t* bar) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_addr(bar)) : "memory");
+}
+// wait for phase `parity` of `bar`, at most about one second (%globaltimer); false when it gave up
+__device__ __forceinline__ bool mbar_wait_1s(uint64_t* bar, uint32_t parity) {
+  uint64_t t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if ((it & 63u) == 0u) {
+      uint64_t t;
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+      if (it == 0u) t0 = t;
+      else if (t - t0 > 1000000000ull) return false;
+    }
+  }
+}
+// one bulk copy global -> this CTA's shared memory, completing on `bar` (16-byte aligned, size a
+// multiple of 16)
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_addr(dst)),
+               "l"(src), "r"(bytes), "r"(smem_addr(bar))
                : "memory");
 }
 
@@ -261,6 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
   __shared__ uint32_t hist[2][2048];  // the victim select's histograms, zero outside the select
   __shared__ uint32_t sel[2][2];
   __shared__ uint32_t err_bits;
+  __shared__ __align__(8) uint64_t bar_stage;  // the early miss copies (one phase per launch)
 
   const int32_t* topk = a.topk + (int64_t)(r - a.r0) * k;
   int32_t* locs = a.locs + (int64_t)(r - a.r0) * k;
@@ -334,6 +368,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
   __shared__ uint32_t s_dups, s_klo, s_khi;
   if (tid == 0) {
     err_bits = app_err;
+    mbar_init1(&bar_stage);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     s_dups = 0u;
     s_klo = 0xffffffffu;
     s_khi = 0u;
@@ -516,23 +552,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
 
   HS_PHASE(hs_phase_res, 4, tid == 0);
   // (4, early) this CTA's first misses start crossing the host link now; the victims are chosen
-  // meanwhile and the staged records reach their slots in phase B
+  // meanwhile and the staged records reach their slots in phase B.  One bulk copy per record (lane 0
+  // of warp e mod 32 issues record e), completing on bar_stage: each issuer adds its record's bytes
+  // to the barrier's transaction count before its copy, and thread 0 arrives once every issuer has
+  // (after the select's barriers), so the phase completes when every staged record has landed.
+  // Bulk copies leave the load units free, where 16-byte copies from host memory filled their queues
+  // and held the issuing threads back from the select.
   const int q0 = (int)((int64_t)m * crank / a.cs), q1 = (int)((int64_t)m * (crank + 1) / a.cs);
-  // 128-byte aligned (the launch adds the slack): a 16-byte copy from host memory keeps its offset
-  // within the 32-byte sector on both sides, else the copy engine splits every sector in two and
-  // the host link carries twice the bytes (measured: 32 instead of 16 sectors per 512-byte request)
+  // 128-byte aligned (the launch adds the slack), like the host records
   uint8_t* stage = (uint8_t*)(((uintptr_t)(smem + a.stage_off) + 127u) & ~(uintptr_t)127u);
   const int nstage = a.pend == nullptr ? min(q1 - q0, a.stage_recs) : 0;
   if (nstage > 0) {
     __syncthreads();  // the miss list is complete
-    const int vpr = (int)(a.rec / 16);
-    const uint64_t* row = pt_row();
-    for (int x = tid; x < nstage * vpr; x += kThreads) {
-      const int e = x / vpr, v = x - e * vpr;
-      const uint8_t* src = hs_page_row_addr(row, a.page_shift, a.rec, miss_pos[q0 + e]);
-      if (src != nullptr) cp_async16(stage + (int64_t)e * a.rec + v * 16, src + v * 16);
+    if ((tid & 31) == 0) {
+      const uint64_t* row = pt_row();
+      for (int e = tid >> 5; e < nstage; e += kWarps) {
+        const uint8_t* src = hs_page_row_addr(row, a.page_shift, a.rec, miss_pos[q0 + e]);
+        if (src != nullptr) {
+          mbar_expect(&bar_stage, (uint32_t)a.rec);
+          bulk_copy_g2s(stage + (int64_t)e * a.rec, src, (uint32_t)a.rec, &bar_stage);
+        }
+      }
     }
-    asm volatile("cp.async.commit_group;" ::: "memory");
   }
 
   HS_PHASE(hs_phase_res, 5, tid == 0);
@@ -541,6 +582,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
   const bool take_all = (m == ncand);
   uint32_t T = 0u, need_eq = 0u;
   if (m > 0 && !take_all) select_threshold(key32, flag, B, (uint32_t)m, s_klo, s_khi, wbuf, hist, sel, &T, &need_eq);
+  if (nstage > 0) {
+    __syncthreads();  // every early copy has been issued (with its bytes expected)
+    if (tid == 0) mbar_arrive1(&bar_stage);
+  }
 
   HS_PHASE(hs_phase_res, 6, tid == 0);
   // (3c) ordered compaction: the q-th victim in ascending slot order.  A slot is a victim when its
@@ -667,10 +712,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
       __syncthreads();
       fetch_misses<NV>(a, q0 + nstage, q1, s_src + nstage, victims, s_slots);
       if (nstage > 0) {
-        asm volatile("cp.async.wait_all;" ::: "memory");
-        __syncthreads();
+        // the staged records have landed (bounded: a wait that gives up flags the resolve and skips
+        // the staged records, after a second bounded wait for copies still in flight)
+        bool landed = mbar_wait_1s(&bar_stage, 0u);
+        if (!landed) {
+          atomicOr(a.err_global, (uint32_t)HS_DEVERR_TIMEOUT);
+          mbar_wait_1s(&bar_stage, 0u);
+        }
         const int vpr = (int)(a.rec / 16);
-        for (int x = tid; x < nstage * vpr; x += kThreads) {
+        for (int x = tid; landed && x < nstage * vpr; x += kThreads) {
           const int e = x / vpr, v = x - e * vpr;
           if (s_src[e] == 0ull) continue;  // page not reserved (flagged): nothing was staged
           *((uint4*)hs_slot_addr(s_slots, a.sshift, a.rec, victims[q0 + e]) + v) = *((const uint4*)(stage + (int64_t)e * a.rec) + v);
@@ -799,8 +849,13 @@ __global__ void __launch_bounds__(kAppendThreads) k_append(AppendArgs a) {
 
 // Early miss copies: 32 KB per CTA is what the host link moves in the ~10 us the victims take to
 // choose, with 64 CTAs fetching; a larger area issues more copies than the link drains and holds the
-// decision back (measured on the GQA decode workload: 16 KB +4%, 32 KB +6%, 96 KB -1% per layer-step).
-constexpr size_t kStageBytes = 32 * 1024;
+// decision back (measured on the GQA decode workload with 16-byte copies: 16 KB +4%, 32 KB +6%, 96 KB
+// -1% per layer-step; with bulk copies, whose issue waits once a few are in flight from host memory:
+// 96 KB -5% on the GQA workload, -8% on the stress batch).  HS_STAGE_KB builds another size.
+#ifndef HS_STAGE_KB
+#define HS_STAGE_KB 32
+#endif
+constexpr size_t kStageBytes = (size_t)HS_STAGE_KB * 1024;
 
 // Shared memory of the decision's arrays with a hash table of 2^bits entries.
 size_t decision_smem(const hs_config* c, int bits) {
