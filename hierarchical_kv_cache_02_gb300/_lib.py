@@ -16,13 +16,14 @@ POLICY_LRU, POLICY_FIFO, POLICY_RANDOM, POLICY_SWAP_VANILLA = 0, 1, 2, 3
 LAYOUT_MLA, LAYOUT_GQA = 0, 1
 DEVERR_RANGE, DEVERR_DUP, DEVERR_CLOCK, DEVERR_APPEND, DEVERR_LOC, DEVERR_TIMEOUT = 1, 2, 4, 8, 16, 32
 DEVERR_PAGE, DEVERR_SLOTS = 64, 128
+STALL_ATTN, STALL_RESOLVE = 1, 2  # hs_debug_stall_next (test hook for the bounded waits)
 
 # every entry point include/hisparse.h declares
 EXPORTS = ("hs_record_bytes", "hs_pool_create", "hs_pool_destroy", "hs_pool_reset", "hs_prefill_write",
            "hs_append_writethrough", "hs_resolve", "hs_sparse_attn", "hs_stats", "hs_read_state",
            "hs_read_buffer", "hs_read_history", "hs_sparse_attn_noalloc", "hs_append_resolve",
            "hs_resolve_range", "hs_sparse_attn_range", "hs_reserve", "hs_release", "hs_host_usage",
-           "hs_device_usage")
+           "hs_device_usage", "hs_debug_stall_next")
 
 
 class hs_config(ctypes.Structure):
@@ -105,6 +106,7 @@ def load(build_if_missing: bool = False):
             "hs_release": (I, [P, I]),
             "hs_host_usage": (I, [P, P, P, P]),
             "hs_device_usage": (I, [P, P, P, P]),
+            "hs_debug_stall_next": (I, [P, I]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)

@@ -63,6 +63,7 @@ struct AttnArgs {
   const hs_pending* pend;   // [R][k] host address and slot of a miss still to copy (src 0: none); null: none
   uint32_t* pend_live;      // [R]
   int L, layer;
+  int stall;                // test hook (hs_debug_stall_next): leave the first ring slot's arrival out
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -1311,7 +1312,7 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_pipe(AttnArgs a, cons
         }
       }
       HS_PHASE(hs_phase_attn, 2 + u, lane == 0 && pw == 0 && u < 18);  // load u issued
-      cp_async_arrive_noinc(&bar_full[slot]);
+      if (!(a.stall != 0 && u == 0)) cp_async_arrive_noinc(&bar_full[slot]);
       ++u;
       return true;
     };
@@ -1851,6 +1852,10 @@ int hs_launch_attn(hs_pool* p, int layer, int r0, int nreq, const void* d_q, con
   a.pend_live = (hot && p->pend_live != nullptr) ? p->pend_live + (int64_t)layer * c.num_requests : nullptr;
   a.L = c.num_layers;
   a.layer = layer;
+  if (pl.kind == 4 && (p->debug_stall & HS_STALL_ATTN) != 0) {  // test hook, consumed by this launch
+    a.stall = 1;
+    p->debug_stall &= ~HS_STALL_ATTN;
+  }
   return dispatch(c, &a, pl, st) == cudaSuccess ? HS_OK : HS_ERR_CUDA;
 }
 

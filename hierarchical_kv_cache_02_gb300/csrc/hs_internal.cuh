@@ -63,6 +63,7 @@ struct hs_pool {
   int resolve_cs;        // CTAs per request in the resolve cluster
   int attn_tickets_per_req;
   size_t attn_part_floats;
+  int debug_stall;       // HS_STALL_* bits: the next such launch leaves one barrier arrival out (test hook)
 };
 
 // ---- small device helpers -------------------------------------------------

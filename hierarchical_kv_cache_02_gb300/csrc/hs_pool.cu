@@ -568,6 +568,12 @@ extern "C" int hs_device_usage(hs_pool* pool, int64_t* pages_in_use, int64_t* pa
   return HS_OK;
 }
 
+extern "C" int hs_debug_stall_next(hs_pool* pool, int kernels) {
+  if (pool == nullptr || (kernels & ~(HS_STALL_ATTN | HS_STALL_RESOLVE)) != 0) return HS_ERR_ARG;
+  pool->debug_stall |= kernels;
+  return HS_OK;
+}
+
 extern "C" int hs_host_usage(hs_pool* pool, int64_t* pages_in_use, int64_t* pages_free, int64_t* bytes_pinned) {
   if (pool == nullptr) return HS_ERR_ARG;
   const hs_host_pages& h = *pool->host;

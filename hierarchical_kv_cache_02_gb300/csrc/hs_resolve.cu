@@ -63,6 +63,7 @@ struct ResolveArgs {
   int R, L, layer, B, k, policy, log_steps, ht_bits, cs;  // R: all requests of the pool
   int r0;  // first request of this launch: topk, locs and the append inputs are indexed from it
   int stage_off, stage_recs;  // staging area for early miss copies: byte offset in shared memory, records
+  int stall;                  // test hook (hs_debug_stall_next): leave the early copies' arrival out
 };
 
 __device__ __forceinline__ uint32_t ht_hash(int32_t p, int bits) { return ((uint32_t)p * 0x9E3779B1u) >> (32 - bits); }
@@ -584,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
   if (m > 0 && !take_all) select_threshold(key32, flag, B, (uint32_t)m, s_klo, s_khi, wbuf, hist, sel, &T, &need_eq);
   if (nstage > 0) {
     __syncthreads();  // every early copy has been issued (with its bytes expected)
-    if (tid == 0) mbar_arrive1(&bar_stage);
+    if (tid == 0 && a.stall == 0) mbar_arrive1(&bar_stage);
   }
 
   HS_PHASE(hs_phase_res, 6, tid == 0);
@@ -954,7 +955,7 @@ int hs_launch_resolve(hs_pool* p, int layer, int r0, int nreq, const int64_t* d_
                       const int32_t* d_topk, int32_t* d_locs, cudaStream_t st) {
   const hs_config& c = p->cfg;
   const int64_t R = c.num_requests, B = c.buffer_slots;
-  ResolveArgs a;
+  ResolveArgs a{};
   a.topk = d_topk;
   a.locs = d_locs;
   a.tag = p->tag + (int64_t)layer * R * B;
@@ -989,6 +990,10 @@ int hs_launch_resolve(hs_pool* p, int layer, int r0, int nreq, const int64_t* d_
   a.app_rec = (const uint8_t*)d_rec;
   a.r0 = r0;
   const size_t smem = resolve_launch_smem(&c, &a.stage_off, &a.stage_recs);
+  if (a.stage_recs > 0 && a.pend == nullptr && (p->debug_stall & HS_STALL_RESOLVE) != 0) {  // test hook
+    a.stall = 1;
+    p->debug_stall &= ~HS_STALL_RESOLVE;
+  }
   cudaError_t e;
   switch (c.io_chunk_bytes) {
     case 16: e = launch_resolve_nv<1>(&a, nreq, a.cs, smem, st); break;

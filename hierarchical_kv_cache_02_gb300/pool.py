@@ -283,6 +283,11 @@ class HsPool:
         pool) return to the free lists and its buffers are emptied; its counters stay."""
         _check("hs_release", self.lib.hs_release(self._h, int(req)))
 
+    def debug_stall_next(self, kernels: int):
+        """Test hook: the next launch of each kernel in `kernels` (STALL_ATTN, STALL_RESOLVE) leaves
+        one barrier arrival out, so its bounded wait gives up and reports DEVERR_TIMEOUT."""
+        _check("hs_debug_stall_next", self.lib.hs_debug_stall_next(self._h, int(kernels)))
+
     def device_usage(self) -> dict:
         used, free, page = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
         _check("hs_device_usage", self.lib.hs_device_usage(self._h, ctypes.byref(used), ctypes.byref(free),

@@ -328,6 +328,21 @@ int hs_reserve(hs_pool* pool, int req, int layer, int64_t end);
  */
 int hs_release(hs_pool* pool, int req);
 
+/*
+ * Test hook for the bounded waits (not for production use): the next launch of each kernel named in
+ * `kernels` leaves one mbarrier arrival out, so that the wait for it gives up after its limit (about
+ * one second) instead of completing.  The kernel then reports HS_DEVERR_TIMEOUT (hs_stats) and
+ * returns; its outputs for that launch are undefined, and the cache state of a resolve that gave up
+ * no longer matches its history (call hs_pool_reset).  The context stays usable.
+ *   HS_STALL_ATTN    : the 64-head shared-latent tensor-core attention (the producers' arrival on
+ *                      the first ring slot), consumed by the next launch of that kernel
+ *   HS_STALL_RESOLVE : the resolve (the arrival that completes the early miss copies), consumed by
+ *                      the next resolve launch that stages early copies
+ * Host-side only (takes effect at launch, also when the launch is captured).  Errors: HS_ERR_ARG.
+ */
+enum { HS_STALL_ATTN = 1, HS_STALL_RESOLVE = 2 };
+int hs_debug_stall_next(hs_pool* pool, int kernels);
+
 /* Host memory of the pool: pages mapped in some table, pages on the free list, pinned bytes held. */
 int hs_host_usage(hs_pool* pool, int64_t* pages_in_use, int64_t* pages_free, int64_t* bytes_pinned);
 
