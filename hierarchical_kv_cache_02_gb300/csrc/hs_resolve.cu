@@ -280,7 +280,31 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
   const int crank = blockIdx.x % a.cs;  // rank inside the cluster of this request
   const int tid = threadIdx.x;
   const int k = a.k, BK = a.B;              // BK: the configured B (the random key's counter)
-  const int B = min(BK, a.scap[r]);         // slots this buffer holds: all work is over [0, B)
+  const int32_t* topk = a.topk + (int64_t)(r - a.r0) * k;
+  int32_t* tag = a.tag + (int64_t)r * BK;
+  uint32_t* stamp = a.stamp + (int64_t)r * BK;
+  const uint64_t* slots_g = a.spt + (int64_t)r * a.spp;
+  // The loads that start the resolve go out together before any of them is used: the buffer's slot
+  // count, this thread's first slots' tags and stamps and top-k entries, the new position, the
+  // buffer's slot-page row, the host page-table row and the (request, layer) state.
+  constexpr int kBatch = 4;  // slots and top-k entries a thread loads up front (k <= 4 x kThreads)
+  const int cap = a.scap[r];
+  int32_t tb[kBatch], tk[kBatch];
+  uint32_t sb[kBatch];
+#pragma unroll
+  for (int u = 0; u < kBatch; ++u) {
+    const int j = tid + u * kThreads;
+    tb[u] = j < BK ? tag[j] : -1;  // slots past the buffer's B are never used
+    sb[u] = j < BK ? stamp[j] : 0u;
+    tk[u] = j < k ? topk[j] : -1;
+  }
+  const int64_t app_p = a.app_pos != nullptr ? a.app_pos[r - a.r0] : -1;
+  const uint64_t v_slots = tid < a.spp ? slots_g[tid] : 0ull;
+  const bool pt_cached = a.max_pages <= kPageRowCache;  // the row fits in shared memory
+  const uint64_t v_pt =
+      (pt_cached && tid < a.max_pages) ? a.pt[((int64_t)r * a.L + a.layer) * a.max_pages + tid] : 0ull;
+  const hs_rl_state st = a.state[r];
+  const int B = min(BK, cap);               // slots this buffer holds: all work is over [0, B)
   const int ht_size = 1 << a.ht_bits;
   int32_t* ht_key = (int32_t*)smem;                 // [ht_size]
   int32_t* ht_val = ht_key + ht_size;               // [ht_size] smallest top-k index of the key
@@ -297,12 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
   __shared__ uint32_t err_bits;
   __shared__ __align__(8) uint64_t bar_stage;  // the early miss copies (one phase per launch)
 
-  const int32_t* topk = a.topk + (int64_t)(r - a.r0) * k;
   int32_t* locs = a.locs + (int64_t)(r - a.r0) * k;
-  int32_t* tag = a.tag + (int64_t)r * BK;
-  uint32_t* stamp = a.stamp + (int64_t)r * BK;
-  const hs_rl_state st = a.state[r];
-  const uint64_t* slots_g = a.spt + (int64_t)r * a.spp;
   if (B < k) {
     // too few slots for a step (a buffer not grown): nothing changes; the locations are -1 and the
     // fused append is skipped too (same decision in every CTA of the cluster: no barrier is reached)
@@ -320,16 +339,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
     return;
   }
   __shared__ uint64_t s_slots[kMaxSlotPages];  // this buffer's page row (first used after the decision)
-  for (int i = tid; i < a.spp; i += kThreads) s_slots[i] = slots_g[i];
+  if (tid < a.spp) s_slots[tid] = v_slots;
   __shared__ int s_app_slot;
   __shared__ unsigned long long s_best[kWarps];
   __shared__ int s_found[kWarps];
   __shared__ uint64_t s_pt[kPageRowCache];
-  // this (request, layer)'s row of the host page table, cached for phase B (the decision's barriers
-  // order it before the first use; the pointer is recomputed where it is used rather than kept live)
-  hs_page_row(a.pt, a.max_pages, a.L, r, a.layer, s_pt);
+  // this (request, layer)'s row of the host page table, cached for the early copies and phase B (the
+  // decision's barriers order it before the first use; the pointer is recomputed where it is used
+  // rather than kept live)
+  if (pt_cached && tid < a.max_pages) s_pt[tid] = v_pt;
   auto pt_row = [&]() -> const uint64_t* {
-    return a.max_pages <= kPageRowCache ? s_pt : a.pt + ((int64_t)r * a.L + a.layer) * a.max_pages;
+    return pt_cached ? s_pt : a.pt + ((int64_t)r * a.L + a.layer) * a.max_pages;
   };
 
   // fetch-in-attention mode: copies a previous resolve left to an attention that never ran are
@@ -339,36 +359,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
     hs_copy_pending(a.pend + (int64_t)r * k, k, a.rec, slots_g, a.sshift, crank, a.cs);
 
   // ---------------- phase A: every CTA of the cluster computes the whole decision ----------------
-  // The loads that start it go out together: the tags and stamps of this thread's first slots, its
-  // top-k entries and, for the fused append, the new position and its host page; the hash table and
-  // the select's histograms are cleared meanwhile.  The hash is then built while the append's slot
-  // search reduces, so the two share their barriers, and the probe reuses the tags and stamps.
-  constexpr int kBatch = 4;  // slots and top-k entries a thread loads up front (k <= 4 x kThreads)
-  int32_t tb[kBatch], tk[kBatch];
-  uint32_t sb[kBatch];
-#pragma unroll
-  for (int u = 0; u < kBatch; ++u) {
-    const int j = tid + u * kThreads;
-    tb[u] = j < B ? tag[j] : -1;
-    sb[u] = j < B ? stamp[j] : 0u;
-    tk[u] = j < k ? topk[j] : -1;
-  }
+  // The hash table and the select's histograms are cleared while the first loads are in flight.  The
+  // hash is then built while the append's slot search reduces, so the two share their barriers, and
+  // the probe reuses the tags and stamps loaded at the start.
   // fused write-through append (hs_append_resolve): the new position takes the slot that already
   // holds it, else the slot with the smallest eviction key over the buffer's slots; stamp = clock, clock
   // += 1; the resolve below then sees that state
+  // The new position loaded with the rest; its host page is requested by thread 0 once the position
+  // has arrived and checked only after the hash, so no thread waits for the two loads in a row here.
   int app_slot = -1;
-  int64_t app_p = -1;
-  uint32_t app_err = 0u;
-  uint4* app_dh = nullptr;  // the append's place in the host history
-  if (a.app_pos != nullptr) {
-    app_p = a.app_pos[r - a.r0];
-    if (app_p >= a.P0 && app_p >= 0 && app_p < a.C)
-      app_dh = (uint4*)hs_page_addr(a.pt, a.max_pages, a.page_shift, a.rec, a.L, r, a.layer, app_p);
-    if (app_dh == nullptr) app_err = (uint32_t)HS_DEVERR_APPEND;  // outside [shared_prefix, capacity), or no page
-  }
+  uint4* app_dh = nullptr;  // the append's place in the host history (known after the hash)
   __shared__ uint32_t s_dups, s_klo, s_khi;
+  __shared__ unsigned long long s_app_page;
   if (tid == 0) {
-    err_bits = app_err;
+    err_bits = 0u;
     mbar_init1(&bar_stage);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     s_dups = 0u;
@@ -380,6 +384,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
     ht_val[x] = 0x7fffffff;
   }
   for (int x = tid; x < 2 * 2048; x += kThreads) hist[x >> 11][x & 2047] = 0u;
+  // the append position must lie in [shared_prefix, capacity) and on a reserved host page
+  const bool app_try = a.app_pos != nullptr && app_p >= a.P0 && app_p >= 0 && app_p < a.C;
+  unsigned long long app_page = 0ull;  // requested here, used after the hash
+  if (tid == 0 && app_try)
+    app_page = a.pt[((int64_t)r * a.L + a.layer) * a.max_pages + (app_p >> a.page_shift)];
   __syncthreads();
 
   HS_PHASE(hs_phase_res, 1, tid == 0);
@@ -409,8 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
     hit_slot[i] = state;
   }
   // the append's slot search over the tags and stamps already loaded (and the rest of the slots)
-  const bool app_on = a.app_pos != nullptr && app_dh != nullptr;
-  if (app_on) {
+  if (app_try) {
     int found = 0x7fffffff;
     unsigned long long best = ~0ull;
     auto visit = [&](int j, int32_t t, uint32_t sj) {
@@ -437,7 +445,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
     }
   }
   __syncthreads();  // the hash table and the append's per-warp results are complete
-  if (app_on && tid < 32) {  // one warp combines the warps' results
+  if (tid == 0) {
+    s_app_page = app_page;
+    if (a.app_pos != nullptr && app_page == 0ull) atomicOr(&err_bits, (uint32_t)HS_DEVERR_APPEND);
+  }
+  if (app_try && tid < 32) {  // one warp combines the warps' results
     int f = tid < kWarps ? s_found[tid] : 0x7fffffff;
     unsigned long long bb = tid < kWarps ? s_best[tid] : ~0ull;
 #pragma unroll
@@ -461,7 +473,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
     }
   }
   __syncthreads();  // the append's slot and the sorted-out repeats are known
-  if (app_on) app_slot = s_app_slot;
+  if (app_try && s_app_page != 0ull) {
+    app_dh = (uint4*)((uint8_t*)(uintptr_t)s_app_page + (app_p & ((1ll << a.page_shift) - 1)) * a.rec);
+    app_slot = s_app_slot;
+  }
   const uint32_t clock = st.clock + (app_slot >= 0 ? 1u : 0u);  // the resolve's clock
   if (tid == 0 && (uint64_t)clock + (uint64_t)k >= 0xFFFFFFFFull) atomicOr(&err_bits, (uint32_t)HS_DEVERR_CLOCK);
 
