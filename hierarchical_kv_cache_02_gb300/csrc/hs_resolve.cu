@@ -236,6 +236,7 @@ __device__ void select_threshold(const uint32_t* key32, const uint8_t* flag, int
       }
     }
     __syncthreads();
+    HS_PHASE(hs_phase_res, 14 + 2 * (pass & 1), threadIdx.x == 0 && pass < 2);  // pass's histogram complete
     // bins [BPT tid, BPT tid + BPT): find the bin where the running count reaches `need`
     constexpr int BPT = 2048 / kThreads;
     const int b0 = BPT * tid;
@@ -264,6 +265,7 @@ __device__ void select_threshold(const uint32_t* key32, const uint8_t* flag, int
       }
     }
     __syncthreads();
+    HS_PHASE(hs_phase_res, 15 + 2 * (pass & 1), threadIdx.x == 0 && pass < 2);  // pass's bin found
     prefix = (prefix << width) | sl[0];
     need = sl[1];
   }
@@ -417,6 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
     }
     hit_slot[i] = state;
   }
+  HS_PHASE(hs_phase_res, 10, tid == 0);  // this thread's hash inserts done
   // the append's slot search over the tags and stamps already loaded (and the rest of the slots)
   if (app_try) {
     int found = 0x7fffffff;
@@ -444,7 +447,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
       s_best[tid >> 5] = best;
     }
   }
+  HS_PHASE(hs_phase_res, 11, tid == 0);  // this warp's append search reduced
   __syncthreads();  // the hash table and the append's per-warp results are complete
+  HS_PHASE(hs_phase_res, 12, tid == 0);
   if (tid == 0) {
     s_app_page = app_page;
     if (a.app_pos != nullptr && app_page == 0ull) atomicOr(&err_bits, (uint32_t)HS_DEVERR_APPEND);
@@ -518,6 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
     }
     for (int j = tid + kBatch * kThreads; j < B; j += kThreads) probe_slot(j, tag[j], stamp[j]);
   }
+  HS_PHASE(hs_phase_res, 13, tid == 0);  // this thread's probes done
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     klo = min(klo, __shfl_xor_sync(0xffffffffu, klo, o));
@@ -631,6 +637,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
     }
     uint32_t tot2;
     const uint32_t pre2 = __shfl_sync(0xffffffffu, cta_exclusive_scan(lane == 0 ? cnt : 0u, wbuf, &tot2), 0);
+    HS_PHASE(hs_phase_res, 18, tid == 0);  // compaction counts scanned
     uint32_t less_b = pre2 & 0xffffu, eq_b = pre2 >> 16;
     for (int jb = j0; jb < j1; jb += 32) {
       const int j = jb + lane;
@@ -652,8 +659,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
       eq_b += (uint32_t)__popc(be);
     }
   }
+  HS_PHASE(hs_phase_res, 19, tid == 0);  // this thread's victims placed
   // every CTA of the request has read the old tags and stamps before anyone writes them
   __syncthreads();
+  HS_PHASE(hs_phase_res, 20, tid == 0);
   if (a.cs > 1) cluster_wait();
   HS_PHASE(hs_phase_res, 7, tid == 0);
 

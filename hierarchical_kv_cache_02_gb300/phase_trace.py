@@ -24,8 +24,14 @@ from . import build as _build
 _HERE = os.path.dirname(os.path.abspath(__file__))
 TRACE_LIB = os.path.join(_build.BUILD, "phase", "libhisparse_phase.so")
 
-RESOLVE = ["start", "append slot", "hash", "probe", "rank", "early copies issued", "select",
-           "compaction + cluster sync", "writes", "host fetch"]
+RESOLVE = dict(enumerate(["start", "append slot", "hash", "probe", "rank", "early copies issued", "select",
+                          "compaction + cluster sync", "writes", "host fetch"]))
+RESOLVE.update({10: "  thread 0: hash inserts done", 11: "  thread 0: append search reduced",
+                12: "  hash: first barrier passed", 13: "  thread 0: probes done",
+                14: "  select pass 0: histogram", 15: "  select pass 0: bin found",
+                16: "  select pass 1: histogram", 17: "  select pass 1: bin found",
+                18: "  compaction: counts scanned", 19: "  thread 0: victims placed",
+                20: "  compaction: barrier passed"})
 ATTN = {0: "start", 1: "setup", 38: "scores of tile 0 issued", 39: "scores of tile 1 issued",
         40: "value product of tile 0 issued", 41: "value product of tile 1 issued",
         43: "softmax: scores of tile 0 seen", 44: "softmax: scores of tile 1 seen",
@@ -51,6 +57,7 @@ def _table(tr, names):
         if len(col):
             rel = (col - t0) / 1e3
             rows.append((names[ev], len(col), float(np.median(rel)), float(rel.min()), float(rel.max())))
+    rows.sort(key=lambda row: row[2])  # in time order (median)
     return rows, int(used.sum())
 
 
@@ -114,7 +121,7 @@ def main(argv):
         st = pool.stats()
         pool.close()
         print(f"{name}: misses per (request, layer, step) {st['misses'] / (R * L * (W + 1)):.0f} of k = {k}")
-        rows, n = _table(res_tr, dict(enumerate(RESOLVE)))
+        rows, n = _table(res_tr, RESOLVE)
         print(f"  k_resolve, {n} CTAs (median / min / max over the CTAs, us from the first CTA's start)")
         for nm, cnt, med, lo, hi in rows:
             print(f"    {nm:44s} {med:7.2f} {lo:7.2f} {hi:7.2f}")
