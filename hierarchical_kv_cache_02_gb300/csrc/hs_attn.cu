@@ -1211,8 +1211,10 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 }
 
 __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_pipe(AttnArgs a, const __grid_constant__ CUtensorMap qmap) {
-  hs_pdl_enter();
-  HS_PHASE(hs_phase_attn, 0, threadIdx.x == 0);
+  // Until the grid dependency is met (programmatic dependent launch: the preceding kernel may still
+  // be running) the CTA touches only what no kernel of this library writes: its barriers, TMEM and
+  // the buffer's slot-page row (changed only by host calls between launches).  The slot indices and
+  // the queries are read after the wait.
   extern __shared__ __align__(128) uint8_t smem_raw[];
   // Q and the ring start 1024-byte aligned (the period of the 128-byte swizzle); the launch adds 1 KB
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -1255,8 +1257,15 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_pipe(AttnArgs a, cons
   }
   if (tid < 64) s_m[tid >> 5][tid & 31] = -INFINITY;
   rows_setup(a, r, s_pg);
-  const int32_t* locs = a.locs + (int64_t)(r - a.r0) * a.k + t0;
   const int64_t rows_r = rows_of(a, r);
+  if (warp == kUWarpMma) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(&s_tmem))
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  hs_pdl_enter();
+  HS_PHASE(hs_phase_attn, 0, threadIdx.x == 0);
+  const int32_t* locs = a.locs + (int64_t)(r - a.r0) * a.k + t0;
   // producers: this lane's rows of a tile are 4 (pw + kUProd e) + lane / 8; the first tile's slot
   // indices are requested before the setup barrier
   const int pw = warp - kUWarpProd, crow = lane >> 3, cch = lane & 7;
@@ -1267,11 +1276,6 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_pipe(AttnArgs a, cons
       const int q = pw + kUProd * e, x = 4 * q + crow;
       lfirst[e] = (q < 32 && x < n) ? locs[x] : -1;
     }
-  }
-  if (warp == kUWarpMma) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(&s_tmem))
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   tc_fence_before();
   __syncthreads();
