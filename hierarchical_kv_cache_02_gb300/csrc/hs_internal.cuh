@@ -181,3 +181,6 @@ bool hs_attn_can_fetch(const hs_config* cfg);  // the attention can take over th
 int hs_attn_prepare(const hs_config* cfg, int num_sms);
 int hs_resolve_prepare(hs_pool* pool);
 size_t hs_resolve_smem_bytes(const hs_config* cfg);
+// Dynamic shared memory of a resolve CTA at most: 227 KB less the kernel's static shared memory
+// (about 29 KB) and the staging area's alignment slack.
+constexpr size_t kResolveDynSmemCap = 196 * 1024;

@@ -52,7 +52,7 @@ int check_config(const hs_config* c) {
   if (!is_pow2(c->io_chunk_bytes) || c->io_chunk_bytes < 16 || c->io_chunk_bytes > 128 || rec % c->io_chunk_bytes != 0)
     return HS_ERR_CONFIG;
   if (!hs_attn_supported(c)) return HS_ERR_CONFIG;
-  if (hs_resolve_smem_bytes(c) > 200 * 1024) return HS_ERR_CONFIG;
+  if (hs_resolve_smem_bytes(c) > kResolveDynSmemCap) return HS_ERR_CONFIG;
   if (c->fetch_in_attention != 0 && (c->fetch_in_attention != 1 || !hs_attn_can_fetch(c))) return HS_ERR_CONFIG;
   if (c->host_page_tokens < 0 || c->host_page_tokens > (1 << 20) ||
       (c->host_page_tokens > 0 && !is_pow2(c->host_page_tokens)))

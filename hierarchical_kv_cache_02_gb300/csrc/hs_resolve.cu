@@ -320,6 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
   __shared__ uint32_t wbuf[kWarps];
   __shared__ uint32_t hist[2][2048];  // the victim select's histograms, zero outside the select
   __shared__ uint32_t sel[2][2];
+  __shared__ uint32_t s_cmask[kWarps][16][2];  // compaction: each warp's round masks (B <= 16384)
   __shared__ uint32_t err_bits;
   __shared__ __align__(8) uint64_t bar_stage;  // the early miss copies (one phase per launch)
 
@@ -629,31 +630,38 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
         }
       }
     };
+    // the counting pass keeps each 32-slot round's masks (below T, equal to T) for the placing pass
+    uint32_t(*masks)[2] = s_cmask[tid >> 5];
     uint32_t cnt = 0;
-    for (int jb = j0; jb < j1; jb += 32) {
+    for (int jb = j0, it = 0; jb < j1; jb += 32, ++it) {
       bool lt, eq;
       classify(jb + lane, lt, eq);
-      cnt += (uint32_t)__popc(__ballot_sync(0xffffffffu, lt)) + ((uint32_t)__popc(__ballot_sync(0xffffffffu, eq)) << 16);
+      const uint32_t bl = __ballot_sync(0xffffffffu, lt), be = __ballot_sync(0xffffffffu, eq);
+      if (lane == 0) {
+        masks[it][0] = bl;
+        masks[it][1] = be;
+      }
+      cnt += (uint32_t)__popc(bl) + ((uint32_t)__popc(be) << 16);
     }
     uint32_t tot2;
     const uint32_t pre2 = __shfl_sync(0xffffffffu, cta_exclusive_scan(lane == 0 ? cnt : 0u, wbuf, &tot2), 0);
     HS_PHASE(hs_phase_res, 18, tid == 0);  // compaction counts scanned
     uint32_t less_b = pre2 & 0xffffu, eq_b = pre2 >> 16;
-    for (int jb = j0; jb < j1; jb += 32) {
-      const int j = jb + lane;
-      bool lt, eq;
-      classify(j, lt, eq);
-      const uint32_t bl = __ballot_sync(0xffffffffu, lt), be = __ballot_sync(0xffffffffu, eq);
-      const uint32_t lb = less_b + (uint32_t)__popc(bl & below), eb = eq_b + (uint32_t)__popc(be & below);
-      int q = -1;
-      if (lt) {
-        q = (int)(lb + min(eb, need_eq));
-      } else if (eq && eb < need_eq) {
-        q = (int)(lb + eb);
-      }
-      if (q >= 0) {
-        victims[q] = j;
-        flag[j] |= 2u;
+    for (int jb = j0, it = 0; jb < j1; jb += 32, ++it) {
+      const uint32_t bl = masks[it][0], be = masks[it][1];
+      if (((bl | be) >> lane) & 1u) {
+        const uint32_t lb = less_b + (uint32_t)__popc(bl & below), eb = eq_b + (uint32_t)__popc(be & below);
+        int q = -1;
+        if ((bl >> lane) & 1u) {
+          q = (int)(lb + min(eb, need_eq));
+        } else if (eb < need_eq) {
+          q = (int)(lb + eb);
+        }
+        if (q >= 0) {
+          const int j = jb + lane;
+          victims[q] = j;
+          flag[j] |= 2u;
+        }
       }
       less_b += (uint32_t)__popc(bl);
       eq_b += (uint32_t)__popc(be);
@@ -881,6 +889,7 @@ __global__ void __launch_bounds__(kAppendThreads) k_append(AppendArgs a) {
 #define HS_STAGE_KB 32
 #endif
 constexpr size_t kStageBytes = (size_t)HS_STAGE_KB * 1024;
+constexpr size_t kDynSmemCap = kResolveDynSmemCap;
 
 // Shared memory of the decision's arrays with a hash table of 2^bits entries.
 size_t decision_smem(const hs_config* c, int bits) {
@@ -894,7 +903,7 @@ size_t decision_smem(const hs_config* c, int bits) {
 int ht_bits_for(const hs_config* c) {
   int bits = 1;
   while ((1 << bits) < 2 * c->top_k) ++bits;
-  return decision_smem(c, bits + 1) + kStageBytes <= 200 * 1024 ? bits + 1 : bits;
+  return decision_smem(c, bits + 1) + kStageBytes <= kDynSmemCap ? bits + 1 : bits;
 }
 
 }  // namespace
@@ -904,11 +913,11 @@ size_t hs_resolve_smem_bytes(const hs_config* c) { return decision_smem(c, ht_bi
 namespace {
 
 // Dynamic shared memory of a resolve launch: the decision's arrays, then (misses copied by the
-// resolve) a staging area for the early miss copies, up to kStageBytes within 200 KB in all.
+// resolve) a staging area for the early miss copies, up to kStageBytes within kDynSmemCap in all.
 size_t resolve_launch_smem(const hs_config* c, int* stage_off, int* stage_recs) {
   const size_t base = (hs_resolve_smem_bytes(c) + 127) & ~(size_t)127;
   const size_t rec = (size_t)hs_record_bytes(c);
-  size_t room = base < 200 * 1024 ? 200 * 1024 - base : 0;
+  size_t room = base < kDynSmemCap ? kDynSmemCap - base : 0;
   room = room < kStageBytes ? room : kStageBytes;
   *stage_off = (int)base;
   *stage_recs = c->fetch_in_attention ? 0 : (int)(room / rec);
