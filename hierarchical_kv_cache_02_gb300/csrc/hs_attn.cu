@@ -576,21 +576,16 @@ constexpr int kMmaTile = 16;  // tokens per stage
 // alone; with one split the CTA writes the final output, otherwise a partial that the last split of
 // the (request, KV head) combines.
 //
-// FETCH (misses copied inside the attention): the resolve only decided, and left {position, slot}
-// for every miss.  A producer loads the pending rows of its stage from the mapped host history with
-// 16-byte loads while the stage's resident rows arrive by bulk copy, stores them into the stage
-// buffer and writes them back to their hot-buffer slots (each CTA its own KV head's slice), so the
-// host-link transfer overlaps the HBM gather and the math.  The buffer's full mbarrier then takes
-// the producer's arrival only after those stores.  The last CTA of a request to finish clears the
-// request's pending flag.
+// FETCH (misses copied inside the attention): the resolve only decided, and left {host address,
+// slot} for every miss.  A producer requests a pending row of its stage straight from the mapped host
+// history by bulk copy, like the resident rows from HBM, on the same full mbarrier, so the host-link
+// transfer overlaps the HBM gather and the math; it leaves the row's hot-buffer address beside the
+// stage, and the consumer, once the stage has landed, writes the row back to that slot (each CTA its
+// own KV head's slice).  The last CTA of a request to finish clears the request's pending flag.
 constexpr int kGqaWarps = 8;           // consumer warps
 constexpr int kGqaProducers = 8;       // producer warps, one per consumer
 constexpr int kGqaStages = 3;          // buffers per consumer warp
 constexpr int kGqaRow = 512 + 16;      // staged slice (K 256 B | V 256 B) + 16 B pad for ldmatrix
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
-}
 
 __device__ __forceinline__ float fast_exp2(float x) {  // 2^x; -inf gives +0
   float y;
@@ -612,6 +607,10 @@ __global__ void __launch_bounds__((kGqaWarps + kGqaProducers) * 32, 1) k_attn_gq
   __shared__ __align__(8) uint64_t empty[NW][NS];
   __shared__ float s_m[NW][8], s_l[NW][8], s_fin[8][2];
   __shared__ uint32_t s_mask[NW][NS];  // valid tokens of the stage in each buffer (bit j: token j)
+  // FETCH: the stage's tokens copied from the host history (bit j: token j) and the hot-buffer
+  // address of each one's slice, which the consumer writes the landed row back to
+  __shared__ uint32_t s_pmask[FETCH ? NW : 1][NS];
+  __shared__ uint64_t s_pdst[FETCH ? NW : 1][NS][FETCH ? kMmaTile : 1];
   __shared__ uint32_t is_last, abort_flag, use_pend;
   __shared__ uint64_t s_pg[kMaxSlotPages];
 
@@ -671,24 +670,6 @@ __global__ void __launch_bounds__((kGqaWarps + kGqaProducers) * 32, 1) k_attn_gq
       vmask = __ballot_sync(0xffffffffu, lane < T && loc >= 0);
       pmask = FETCH ? __ballot_sync(0xffffffffu, lane < T && pp != 0ull) : 0u;
     };
-    // FETCH: up to kPre pending rows of a stage are requested from the host one stage ahead of use
-    // (deeper request windows measured slower: the link is the bound, more requests only queue)
-    constexpr int kPre = FETCH ? 8 : 1;
-    uint4 vc[kPre], vn[kPre];
-    // this lane's 16 bytes of KV head g's slice of the host record at `src`
-    auto load_row = [&](uint64_t src) -> uint4 {
-      return __ldg((const uint4*)((const uint8_t*)(uintptr_t)src + (int64_t)g * a.kstride) + lane);
-    };
-    auto request = [&](uint32_t pmask_, uint64_t pp_, uint4 (&v)[kPre]) {
-      uint32_t pm = pmask_;
-#pragma unroll
-      for (int u = 0; u < kPre; ++u) {
-        if (pm != 0u) {
-          v[u] = load_row(__shfl_sync(0xffffffffu, pp_, __ffs(pm) - 1));
-          pm &= pm - 1u;
-        }
-      }
-    };
     // the first three stages' slots are requested before the page row, so the loads overlap
     int32_t raw_l0, raw_l1, raw_l2;
     uint64_t raw_q0, raw_q1, raw_q2;
@@ -710,7 +691,6 @@ __global__ void __launch_bounds__((kGqaWarps + kGqaProducers) * 32, 1) k_attn_gq
     stage_info(raw_l0, raw_q0, loc, pp, vmask, pmask);
     raw_l0 = raw_l2;
     raw_q0 = raw_q2;
-    if (FETCH) request(pmask, pp, vc);
     for (int i = 0; i < ni; ++i) {
       const int b = i % NS;
       if (i >= NS) {
@@ -729,16 +709,19 @@ __global__ void __launch_bounds__((kGqaWarps + kGqaProducers) * 32, 1) k_attn_gq
           *(uint4*)(dst + (__ffs(zm) - 1) * RW + lane * 16) = make_uint4(0u, 0u, 0u, 0u);
         __syncwarp();
       }
-      if (!FETCH || pmask == 0u) {
-        if (lane == 0) mbar_arrive_expect_tx(&full[w][b], (uint32_t)__popc(vmask) * 512u);
+      if (FETCH) {
+        // a pending row comes straight from the host history, by bulk copy like the resident rows;
+        // the consumer writes it back to its hot-buffer slot once the stage has landed
+        if (lane == 0) s_pmask[w][b] = pmask;
+        if (pp != 0ull) s_pdst[w][b][lane] = (uint64_t)(uintptr_t)(row_addr(s_pg, a.kv_shift, rec, loc) + goff);
         __syncwarp();
-        if (loc >= 0) bulk_g2s(dst + lane * RW, row_addr(s_pg, a.kv_shift, rec, loc) + goff, 512u, &full[w][b]);
-      } else {
-        // resident rows by bulk copy; the arrival comes after the pending rows are stored, below
-        if (lane == 0) mbar_expect_tx(&full[w][b], (uint32_t)__popc(vmask & ~pmask) * 512u);
-        __syncwarp();
-        if (loc >= 0 && pp == 0ull)
-          bulk_g2s(dst + lane * RW, row_addr(s_pg, a.kv_shift, rec, loc) + goff, 512u, &full[w][b]);
+      }
+      if (lane == 0) mbar_arrive_expect_tx(&full[w][b], (uint32_t)__popc(vmask) * 512u);
+      __syncwarp();
+      if (loc >= 0) {
+        const uint8_t* src = (FETCH && pp != 0ull) ? (const uint8_t*)(uintptr_t)pp + goff
+                                                   : row_addr(s_pg, a.kv_shift, rec, loc) + goff;
+        bulk_g2s(dst + lane * RW, src, 512u, &full[w][b]);
       }
       int32_t loc2;
       uint64_t pp2;
@@ -747,28 +730,6 @@ __global__ void __launch_bounds__((kGqaWarps + kGqaProducers) * 32, 1) k_attn_gq
       raw_l1 = raw_l0;
       raw_q1 = raw_q0;
       load_raw(i + 3, raw_l0, raw_q0);
-      if (FETCH) {
-        request(pmask2, pp2, vn);  // the next stage's pending rows, before this stage's are stored
-        if (pmask != 0u) {
-          // pending rows into the stage and back to their hot-buffer slots (each CTA its KV head's slice)
-          uint32_t pm = pmask;
-#pragma unroll
-          for (int u = 0; u < kPre + 16; ++u) {  // the first kPre were requested a stage ago
-            if (pm != 0u) {
-              const int j = __ffs(pm) - 1;
-              pm &= pm - 1u;
-              const uint4 v = u < kPre ? vc[u < kPre ? u : 0] : load_row(__shfl_sync(0xffffffffu, pp, j));
-              *(uint4*)(dst + j * RW + lane * 16) = v;
-              const int32_t slot = __shfl_sync(0xffffffffu, loc, j);
-              *((uint4*)(row_addr(s_pg, a.kv_shift, rec, slot) + goff) + lane) = v;
-            }
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&full[w][b]);
-        }
-#pragma unroll
-        for (int u = 0; u < kPre; ++u) vc[u] = vn[u];
-      }
       loc = loc2;
       pp = pp2;
       vmask = vmask2;
@@ -809,6 +770,15 @@ __global__ void __launch_bounds__((kGqaWarps + kGqaProducers) * 32, 1) k_attn_gq
       }
       const uint32_t mask = s_mask[warp][b];
       const uint32_t base = ring_u + (uint32_t)(b * T * RW);
+      if (FETCH) {
+        // the stage's rows fetched from the host go back to their hot-buffer slots (each CTA its KV
+        // head's slice): 512 coalesced bytes a row
+        const uint8_t* stage_rows = smem + (size_t)(warp * NS + b) * T * RW;
+        for (uint32_t pm = s_pmask[warp][b]; pm != 0u; pm &= pm - 1u) {
+          const int j = __ffs(pm) - 1;
+          *((uint4*)(uintptr_t)s_pdst[warp][b][j] + lane) = *((const uint4*)(stage_rows + j * RW) + lane);
+        }
+      }
       // S^T = K Q^T in four independent MMA chains (k-steps s, s + 4)
       float sacc[4][4];
 #pragma unroll
