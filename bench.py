@@ -489,6 +489,10 @@ def run_ours(args, w, world, rank, local):
     if G > 1:
         # the group's resolves overlap one another and the attentions: link rate over the wall time
         link_kernel, link_s = "resolve (overlapped; whole-step wall time)", max_elapsed
+    elif M > 1 and fetch == "attention":
+        # the micro-batches' attentions move the misses one after another while the other group's
+        # resolve decides: the link's average rate over the wall time of the steps
+        link_kernel, link_s = "sparse_attn (micro-batches overlapped; whole-step wall time)", max_elapsed
     out = {
         "metric": METRIC, "value": value, "unit": "layer-steps/s", "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": max_elapsed / K * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
