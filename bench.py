@@ -773,6 +773,7 @@ def oracle_sample(w, steps, seed, budget_s, pairs_max=64):
     # one history stands in for every sampled pair: the oracle's cost does not depend on the values
     hist = inputs.normal_bf16((w["ctx0"] + steps, E), seed=seed).view(torch.int16).numpy().view(np.uint16)
     total_t, n_rl_steps, pairs = 0.0, 0, 0
+    cache_t = 0.0  # of which the cache simulation (append, resolve); the rest is the fp64 attention
     for p in range(pairs_max):
         r, l = p % R, (p * 7) % L
         # the trace of (r, l) in a batch seeded `seed` is the single trace seeded seed + r*65536 + l
@@ -781,9 +782,11 @@ def oracle_sample(w, steps, seed, budget_s, pairs_max=64):
         cache = oracle.Cache(w["B"], k, "lru", R=R, L=L, r=r, l=l, C=w["ctx0"] + steps)
         t0 = time.perf_counter()
         for t in range(steps):
+            c0 = time.perf_counter()
             if appends:
                 cache.append(w["ctx0"] + t)
             cache.resolve(tr[t])
+            cache_t += time.perf_counter() - c0
             oracle.attention(q[t], hist, tr[t], scale, kvh, w["Dqk"], w["Dv"])
             n_rl_steps += 1
             if total_t + time.perf_counter() - t0 > budget_s:
@@ -794,8 +797,11 @@ def oracle_sample(w, steps, seed, budget_s, pairs_max=64):
             break
     per = total_t / max(1, n_rl_steps)
     desc = (f"{n_rl_steps} (request, layer)-steps of {pairs} pairs, each replayed from step 0 (append, resolve, "
-            f"fp64 attention), {total_t:.1f} s on 1 core; layer-steps/s = 1 / ({R} x s per (request, layer)-step)")
-    return per, desc, n_rl_steps
+            f"fp64 attention), {total_t:.1f} s on 1 core ({cache_t:.1f} s of it the cache simulation); "
+            f"layer-steps/s = 1 / ({R} x s per (request, layer)-step)")
+    split = {"cache_us_per_layer": R * cache_t / max(1, n_rl_steps) * 1e6,
+             "attention_us_per_layer": R * (total_t - cache_t) / max(1, n_rl_steps) * 1e6}
+    return per, desc, n_rl_steps, split
 
 
 def cpu_info():
@@ -853,11 +859,16 @@ def run_reference(args, w, world, rank):
         q = inputs.normal_bf16((steps, w["Hq"], w["Dqk"]), seed=100 + p).view(torch.int16).numpy().view(np.uint16)
         pairs.append((oracle.Cache(w["B"], k, "lru", R=R, L=L, r=r, l=l, C=w["ctx0"] + steps), tr, q))
 
-    def advance(i, t):
+    cache_s = [0.0]  # time of the cache simulation (append, resolve) in the timed steps
+
+    def advance(i, t, timed=False):
         cache, tr, q = pairs[i]
+        c0 = time.perf_counter()
         if appends:
             cache.append(w["ctx0"] + t)
         cache.resolve(tr[t])
+        if timed:
+            cache_s[0] += time.perf_counter() - c0
         oracle.attention(q[t], hist, tr[t], scale, kvh, w["Dqk"], w["Dv"])
 
     # size the sample on the first warm-up step: pairs are added until the step has used its budget
@@ -872,7 +883,7 @@ def run_reference(args, w, world, rank):
     t_start = time.perf_counter()
     for t in range(W, steps):
         for i in range(P):
-            advance(i, t)
+            advance(i, t, timed=True)
     elapsed = time.perf_counter() - t_start
     per = elapsed / (P * K)  # seconds per (request, layer)-step
     value = 1.0 / (R * per)
@@ -891,7 +902,8 @@ def run_reference(args, w, world, rank):
             "config": {"workload": args.workload, "requests": R, "layers": L, "context": w["ctx0"],
                        "top_k": k, "buffer_slots": w["B"]},
             "cpu_baseline": {"value": value, "unit": "layer-steps/s", "cores": 1, "kind": "oracle", "sample": desc,
-                             **info},
+                             "cache_us_per_layer": R * cache_s[0] / (P * K) * 1e6,
+                             "attention_us_per_layer": R * (elapsed - cache_s[0]) / (P * K) * 1e6, **info},
             "e2e": {"value": value, "unit": "layer-steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -973,9 +985,10 @@ def main():
                                                 "host_link", "gpu_launches", "clocks", "errors", "config")}
         out["shared_latent"] = latent
     if rank == 0 and not args.no_cpu_baseline:
-        per, desc, n = oracle_sample(w, steps=min(16, args.warmup + args.steps), seed=99, budget_s=args.cpu_seconds)
+        per, desc, n, split = oracle_sample(w, steps=min(16, args.warmup + args.steps), seed=99,
+                                            budget_s=args.cpu_seconds)
         out["cpu_baseline"] = {"value": 1.0 / (w["R"] * per), "unit": "layer-steps/s", "cores": 1, "kind": "oracle",
-                               "sample": desc, **cpu_info()}
+                               "sample": desc, **split, **cpu_info()}
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:
