@@ -64,6 +64,10 @@ struct AttnArgs {
   uint32_t* pend_live;      // [R]
   int L, layer;
   int stall;                // test hook (hs_debug_stall_next): leave the first ring slot's arrival out
+  // set when the launch directly follows the whole-batch resolve of its layer on its stream: that
+  // resolve's [R][2] counters (launches, CTAs finished) and its CTAs per request
+  const uint32_t* res_count;
+  int res_cs;
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -593,9 +597,49 @@ __device__ __forceinline__ float fast_exp2(float x) {  // 2^x; -inf gives +0
   return y;
 }
 
+// The dependency on the resolve just before: by default the whole resolve grid (programmatic
+// dependent launch).  When the launch directly follows the whole-batch resolve of its layer
+// (a.res_count set), a CTA waits only for the resolve CTAs of its own request: every resolve CTA
+// counts itself finished after its writes (release), the resolve counts its launch for each request
+// before any CTA of this kernel may start, and thread 0 waits until the finished count reaches the
+// request's CTAs times its launches (acquire, bounded).  The resolve's CTAs are all resident before
+// this kernel starts, so the wait cannot block them.  The bulk copies then read through the async
+// proxy what the resolve wrote through the generic one, hence the proxy fence.
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void attn_enter(const AttnArgs& a, int r, uint32_t* err) {
+  if (a.res_count == nullptr) {
+    hs_pdl_enter();
+    return;
+  }
+  if (threadIdx.x == 0) {
+    const uint32_t target = (uint32_t)a.res_cs * ld_acquire_u32(&a.res_count[2 * r]);
+    uint64_t t0 = 0;
+    for (uint32_t it = 0; ld_acquire_u32(&a.res_count[2 * r + 1]) < target; ++it) {
+      __nanosleep(64);
+      if ((it & 63u) == 0u) {
+        uint64_t t;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+        if (it == 0u) {
+          t0 = t;
+        } else if (t - t0 > 1000000000ull) {
+          atomicOr(err, (uint32_t)HS_DEVERR_TIMEOUT);
+          break;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 template <int G, bool FETCH>
 __global__ void __launch_bounds__((kGqaWarps + kGqaProducers) * 32, 1) k_attn_gqa(AttnArgs a) {
-  hs_pdl_enter();
+  attn_enter(a, a.r0 + (int)blockIdx.y, a.err);
   constexpr int T = kMmaTile, D = 128, NW = kGqaWarps, NS = kGqaStages, RW = kGqaRow;
   constexpr bool kStuff = G <= 4;        // P remainders ride in columns G..2G-1 of the same MMA
   constexpr int kCols = kStuff ? 2 * G : G;
@@ -1830,6 +1874,16 @@ int hs_launch_attn(hs_pool* p, int layer, int r0, int nreq, const void* d_q, con
     a.stall = 1;
     p->debug_stall &= ~HS_STALL_ATTN;
   }
+  // directly after the whole-batch resolve of this layer on this stream (GQA kernel, misses copied by
+  // the resolve): wait for each request's own resolve CTAs rather than the whole resolve grid
+#ifndef HS_ATTN_WAIT_WHOLE_GRID  // build option: always wait for the whole resolve grid
+  if (pl.kind == 1 && !pl.fetch && kv_base == nullptr && r0 == 0 && nreq == c.num_requests &&
+      p->last_res_layer == layer && p->last_res_stream == st) {
+    a.res_count = p->res_count + (int64_t)layer * c.num_requests * 2;
+    a.res_cs = p->resolve_cs;
+  }
+#endif
+  p->last_res_layer = -1;
   return dispatch(c, &a, pl, st) == cudaSuccess ? HS_OK : HS_ERR_CUDA;
 }
 

@@ -64,6 +64,11 @@ struct hs_pool {
   int attn_tickets_per_req;
   size_t attn_part_floats;
   int debug_stall;       // HS_STALL_* bits: the next such launch leaves one barrier arrival out (test hook)
+  // [L][R][2] resolve launches and resolve CTAs finished per (layer, request): an attention that
+  // directly follows the resolve of its layer waits for its request's CTAs only (see k_attn_gqa)
+  uint32_t* res_count;
+  int last_res_layer;            // layer of the last launch if it was a whole-batch resolve, else -1
+  cudaStream_t last_res_stream;  // and its stream
 };
 
 // ---- small device helpers -------------------------------------------------

@@ -149,6 +149,7 @@ void free_pool(hs_pool* p) {
   cudaFree(p->counters);
   cudaFree(p->step_log);
   cudaFree(p->err_global);
+  cudaFree(p->res_count);
   cudaFree(p->attn_part);
   cudaFree(p->attn_ticket);
   cudaFree(p->pend);
@@ -180,6 +181,7 @@ size_t slots_total(const hs_pool* p) {
 size_t rl_total(const hs_pool* p) { return (size_t)p->cfg.num_layers * p->cfg.num_requests; }
 
 int do_reset(hs_pool* p, cudaStream_t st) {
+  p->last_res_layer = -1;
   size_t ns = slots_total(p), nrl = rl_total(p);
   int blocks = (int)std::min<size_t>((ns + 255) / 256, (size_t)p->num_sms * 8);
   k_reset<<<blocks, 256, 0, st>>>(p->tag, p->stamp, ns, p->state, nrl);
@@ -385,6 +387,7 @@ extern "C" int hs_pool_create(const hs_config* cfg, int cuda_device, hs_pool** o
   DeviceGuard guard(cuda_device);
   hs_pool* p = new hs_pool();
   memset(p, 0, sizeof(*p));
+  p->last_res_layer = -1;
   p->cfg = *cfg;
   p->device = cuda_device;
   cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, cuda_device);
@@ -443,6 +446,8 @@ extern "C" int hs_pool_create(const hs_config* cfg, int cuda_device, hs_pool** o
   if (rc == HS_OK) rc = dev_alloc(&p->counters, L * R * 4);
   if (rc == HS_OK) rc = dev_alloc(&p->step_log, (size_t)cfg->log_steps * L * R);
   if (rc == HS_OK) rc = dev_alloc(&p->err_global, 1);
+  if (rc == HS_OK) rc = dev_alloc(&p->res_count, L * R * 2);
+  if (rc == HS_OK && cudaMemset(p->res_count, 0, L * R * 2 * sizeof(uint32_t)) != cudaSuccess) rc = HS_ERR_CUDA;
   if (rc == HS_OK) {
     hs_attn_workspace(cfg, p->num_sms, &p->attn_part_floats, &p->attn_max_splits, &p->attn_tickets_per_req);
     rc = dev_alloc(&p->attn_part, p->attn_part_floats);
@@ -495,6 +500,7 @@ extern "C" int hs_prefill_write(hs_pool* pool, int req, int layer, int64_t pos0,
   if (changed && (rc = upload_tables(pool)) != HS_OK) return rc;
   const uint8_t* s = (const uint8_t*)src;
   cudaStream_t st = (cudaStream_t)stream;
+  pool->last_res_layer = -1;
   for (int64_t a = pos0; a < pos0 + n;) {  // one copy per page
     const int64_t b = std::min(pos0 + n, (a / pt + 1) * pt);
     uint8_t* dst = h.host_pt[((int64_t)req * c.num_layers + layer) * pool->max_pages + a / pt] + (a % pt) * rec;

@@ -64,6 +64,7 @@ struct ResolveArgs {
   int r0;  // first request of this launch: topk, locs and the append inputs are indexed from it
   int stage_off, stage_recs;  // staging area for early miss copies: byte offset in shared memory, records
   int stall;                  // test hook (hs_debug_stall_next): leave the early copies' arrival out
+  uint32_t* res_count;        // layer slice [R][2]: launches, CTAs finished (per request)
 };
 
 __device__ __forceinline__ uint32_t ht_hash(int32_t p, int bits) { return ((uint32_t)p * 0x9E3779B1u) >> (32 - bits); }
@@ -273,13 +274,30 @@ __device__ void select_threshold(const uint32_t* key32, const uint8_t* flag, int
   *need_out = need;
 }
 
+// A resolve CTA's last act: once every thread's writes (locs, metadata, fetched rows) are done, count
+// the CTA as finished for its request, with release ordering (an attention that waits for the count
+// then reads those writes).
+__device__ __forceinline__ void count_finished(uint32_t* res_count, int r) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(&res_count[2 * r + 1], 1u);
+  }
+}
+
 template <int NV>
 __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
-  hs_pdl_enter();
-  HS_PHASE(hs_phase_res, 0, threadIdx.x == 0);
-  extern __shared__ __align__(16) uint8_t smem[];
   const int r = a.r0 + (int)(blockIdx.x / a.cs);
   const int crank = blockIdx.x % a.cs;  // rank inside the cluster of this request
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the launch is counted for its requests before the next kernel may start
+  if (crank == 0 && threadIdx.x == 0) {
+    atomicAdd(&a.res_count[2 * r], 1u);
+    __threadfence();
+  }
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  HS_PHASE(hs_phase_res, 0, threadIdx.x == 0);
+  extern __shared__ __align__(16) uint8_t smem[];
   const int tid = threadIdx.x;
   const int k = a.k, BK = a.B;              // BK: the configured B (the random key's counter)
   const int32_t* topk = a.topk + (int64_t)(r - a.r0) * k;
@@ -339,6 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
       }
       a.state[r].err = st.err | e;
     }
+    count_finished(a.res_count, r);
     return;
   }
   __shared__ uint64_t s_slots[kMaxSlotPages];  // this buffer's page row (first used after the decision)
@@ -779,6 +798,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
       a.step_log[((int64_t)st.nres * a.L + a.layer) * a.R + r] = (uint32_t)m;
     if (a.pend != nullptr) a.pend_live[r] = 1u;
   }
+  count_finished(a.res_count, r);
 }
 
 struct AppendArgs {
@@ -1022,6 +1042,11 @@ int hs_launch_resolve(hs_pool* p, int layer, int r0, int nreq, const int64_t* d_
   a.app_pos = d_pos;
   a.app_rec = (const uint8_t*)d_rec;
   a.r0 = r0;
+  a.res_count = p->res_count + (int64_t)layer * R * 2;
+  // an attention launched right after a whole-batch resolve of its layer on the same stream may
+  // wait for its own request's resolve CTAs instead of the whole grid
+  p->last_res_layer = (r0 == 0 && nreq == R) ? layer : -1;
+  p->last_res_stream = st;
   const size_t smem = resolve_launch_smem(&c, &a.stage_off, &a.stage_recs);
   if (a.stage_recs > 0 && a.pend == nullptr && (p->debug_stall & HS_STALL_RESOLVE) != 0) {  // test hook
     a.stall = 1;
@@ -1049,6 +1074,7 @@ int hs_resolve_prepare(hs_pool* p) {
 }
 
 int hs_launch_append(hs_pool* p, int layer, const int64_t* d_pos, const void* d_rec, cudaStream_t st) {
+  p->last_res_layer = -1;
   const hs_config& c = p->cfg;
   const int64_t R = c.num_requests, B = c.buffer_slots;
   AppendArgs a;
