@@ -1277,7 +1277,7 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_mla_pipe(AttnArgs a, cons
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  hs_pdl_enter();
+  attn_enter(a, r, a.err);
   HS_PHASE(hs_phase_attn, 0, threadIdx.x == 0);
   const int32_t* locs = a.locs + (int64_t)(r - a.r0) * a.k + t0;
   // producers: this lane's rows of a tile are 4 (pw + kUProd e) + lane / 8; the first tile's slot
@@ -1874,10 +1874,11 @@ int hs_launch_attn(hs_pool* p, int layer, int r0, int nreq, const void* d_q, con
     a.stall = 1;
     p->debug_stall &= ~HS_STALL_ATTN;
   }
-  // directly after the whole-batch resolve of this layer on this stream (GQA kernel, misses copied by
-  // the resolve): wait for each request's own resolve CTAs rather than the whole resolve grid
+  // directly after the whole-batch resolve of this layer on this stream (GQA or 64-head shared-latent
+  // kernel, misses copied by the resolve): wait for each request's own resolve CTAs rather than the
+  // whole resolve grid
 #ifndef HS_ATTN_WAIT_WHOLE_GRID  // build option: always wait for the whole resolve grid
-  if (pl.kind == 1 && !pl.fetch && kv_base == nullptr && r0 == 0 && nreq == c.num_requests &&
+  if ((pl.kind == 1 || pl.kind == 4) && !pl.fetch && kv_base == nullptr && r0 == 0 && nreq == c.num_requests &&
       p->last_res_layer == layer && p->last_res_stream == st) {
     a.res_count = p->res_count + (int64_t)layer * c.num_requests * 2;
     a.res_cs = p->resolve_cs;
