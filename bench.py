@@ -61,7 +61,7 @@ DEFAULT_WORKLOAD = "gqa_b16_l32"
 # dram__bytes_read.sum + dram__bytes_write.sum of one attention launch from an ncu capture of the
 # same kernel and per-launch size (profiles/; ncu replays with cold caches, so this is the DRAM
 # traffic of a launch whose rows are not in L2); None where no capture of the current kernel exists
-ATTN_TRAFFIC = {("gqa_b16_l32", "resolve"): 138.44e6, ("mla_b8", "resolve"): 19.60e6}
+ATTN_TRAFFIC = {("gqa_b16_l32", "resolve"): 138.54e6, ("mla_b8", "resolve"): 19.60e6}
 L2_BYTES = 129e6  # GB300 L2
 
 
