@@ -218,7 +218,10 @@ int hs_append_resolve(hs_pool* pool, int layer, const int64_t* d_pos, const void
  * (fully resident KV: used to check the exactness property).  A request with no valid entry
  * gets zeros.  Entries >= rows set HS_DEVERR_LOC and are skipped.  The reduction order
  * depends only on the top-k order, so the result is bit-identical whichever slots hold the
- * records.  CAPTURABLE.
+ * records.  Enqueued directly after hs_resolve / hs_append_resolve of the same layer on the same
+ * stream (nothing of this pool in between), the attention of a request may start as soon as that
+ * request's resolve is done, before the rest of the resolve; results are the same either way.
+ * CAPTURABLE.
  */
 int hs_sparse_attn(hs_pool* pool, int layer, const void* d_q, const int32_t* d_locs, const void* kv_base,
                    int64_t kv_rows, float scale, float* d_out, void* stream);
