@@ -191,7 +191,8 @@ class Workload:
                             num_q_heads=w["Hq"], num_kv_heads=w["Hkv"], head_dim_qk=w["Dqk"], head_dim_v=w["Dv"],
                             top_k=k, buffer_slots=w["B"], policy=0, seed=seed, io_chunk_bytes=64,
                             shared_prefix=w["ctx0"] if w["shared"] else 0,
-                            fetch_in_attention=1 if fetch == "attention" else 0)
+                            fetch_in_attention=1 if fetch == "attention" else 0,
+                            early_fetch=1 if fetch == "early" else 0)
         self.appends = w.get("appends", True)
         spec = inputs.TraceSpec(ctx0=w["ctx0"], k=k, steps=steps, keep=w["keep"], recency_mean=w["mu"],
                                 appends=self.appends, burst_every=w["burst"], far_gap=int(8 * w["mu"]))
@@ -520,7 +521,7 @@ def run_ours(args, w, world, rank, local):
                          "resolve_plus_attn": float((res_ms + att_ms).mean() * 1e3)},
         "miss_rate": float(st["misses"]) / max(1.0, float(st["hits"] + st["misses"])),
         "roofline": {"kernel": "sparse_attn", "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": args.traffic if args.traffic is not None else ATTN_TRAFFIC.get((args.workload, fetch)),
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": args.traffic if args.traffic is not None else ATTN_TRAFFIC.get((args.workload, "resolve" if fetch == "early" else fetch)),
                      "peak_source": peaks["source"],
                      "bytes_per_launch": attn_bytes_per_launch(w) // M,
                      "launch_us": roof_us,
@@ -921,8 +922,10 @@ def main():
                          "the groups' resolves form one chain and their attentions another")
     ap.add_argument("--separate-append", action="store_true",
                     help="append and resolve as two launches instead of the fused hs_append_resolve")
-    ap.add_argument("--fetch", choices=["auto", "resolve", "attention"], default="auto",
-                    help="who copies the misses host -> HBM: the resolve kernel, or the attention while it gathers")
+    ap.add_argument("--fetch", choices=["auto", "resolve", "early", "attention"], default="auto",
+                    help="who copies the misses host -> HBM: the resolve kernel once it has chosen the victims, "
+                         "the resolve with fetch CTAs that start copying while the victims are chosen (early), "
+                         "or the attention while it gathers")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--index-share", type=int, default=1,
                     help="layer groups of this size share one selection; their resolves (and host fetches) "

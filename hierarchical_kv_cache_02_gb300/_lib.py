@@ -16,7 +16,7 @@ POLICY_LRU, POLICY_FIFO, POLICY_RANDOM, POLICY_SWAP_VANILLA = 0, 1, 2, 3
 LAYOUT_MLA, LAYOUT_GQA = 0, 1
 DEVERR_RANGE, DEVERR_DUP, DEVERR_CLOCK, DEVERR_APPEND, DEVERR_LOC, DEVERR_TIMEOUT = 1, 2, 4, 8, 16, 32
 DEVERR_PAGE, DEVERR_SLOTS = 64, 128
-STALL_ATTN, STALL_RESOLVE = 1, 2  # hs_debug_stall_next (test hook for the bounded waits)
+STALL_ATTN, STALL_RESOLVE, STALL_FETCH = 1, 2, 4  # hs_debug_stall_next (test hook for the bounded waits)
 
 # every entry point include/hisparse.h declares
 EXPORTS = ("hs_record_bytes", "hs_pool_create", "hs_pool_destroy", "hs_pool_reset", "hs_prefill_write",
@@ -49,6 +49,7 @@ class hs_config(ctypes.Structure):
         ("buffer_page_slots", ctypes.c_int32),
         ("device_pool_slots", ctypes.c_int64),
         ("host_to_device_ratio", ctypes.c_double),
+        ("early_fetch", ctypes.c_int32),
     ]
 
 

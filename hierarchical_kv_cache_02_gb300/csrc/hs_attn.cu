@@ -1881,7 +1881,7 @@ int hs_launch_attn(hs_pool* p, int layer, int r0, int nreq, const void* d_q, con
   if ((pl.kind == 1 || pl.kind == 4) && !pl.fetch && kv_base == nullptr && r0 == 0 && nreq == c.num_requests &&
       p->last_res_layer == layer && p->last_res_stream == st) {
     a.res_count = p->res_count + (int64_t)layer * c.num_requests * 2;
-    a.res_cs = p->resolve_cs;
+    a.res_cs = p->resolve_ctas;
   }
 #endif
   p->last_res_layer = -1;

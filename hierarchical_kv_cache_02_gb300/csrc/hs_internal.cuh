@@ -69,6 +69,16 @@ struct hs_pool {
   uint32_t* res_count;
   int last_res_layer;            // layer of the last launch if it was a whole-batch resolve, else -1
   cudaStream_t last_res_stream;  // and its stream
+  int resolve_ctas;              // resolve CTAs per request and launch: cs, or 2 cs with fetch CTAs
+  // early fetch (cfg.early_fetch = 1), else all null:
+  int32_t* pos_slot;   // [L][R][C] slot each position was last installed in (a hint: a position is
+                       // resident iff that slot is below the buffer's slot count and carries its tag)
+  uint32_t* fclaim;    // [L][R][k] claim word of each top-k entry in a launch: 0 free, 1 claimed by a
+                       // fetch CTA, (row + 1) << 2 | 2 landed in scratch row `row`, 3 claimed by a
+                       // deciding CTA; all 0 again when the launch ends
+  uint32_t* ffin;      // [L][R] CTAs of the launch finished (the last one clears the claim words)
+  uint8_t* fscratch;   // [L][R][cs x fetch_rows][rec] records fetched ahead of the decision
+  int fetch_rows;      // scratch rows of one fetch CTA
 };
 
 // ---- small device helpers -------------------------------------------------

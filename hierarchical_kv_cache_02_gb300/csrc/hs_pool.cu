@@ -65,6 +65,7 @@ int check_config(const hs_config* c) {
     return HS_ERR_CONFIG;
   if (c->device_pool_slots < 0) return HS_ERR_CONFIG;
   if (!(c->host_to_device_ratio >= 0.0) || c->host_to_device_ratio > 1e12) return HS_ERR_CONFIG;  // rejects NaN
+  if (c->early_fetch != 0 && (c->early_fetch != 1 || c->fetch_in_attention != 0)) return HS_ERR_CONFIG;
   return HS_OK;
 }
 
@@ -154,6 +155,10 @@ void free_pool(hs_pool* p) {
   cudaFree(p->attn_ticket);
   cudaFree(p->pend);
   cudaFree(p->pend_live);
+  cudaFree(p->pos_slot);
+  cudaFree(p->fclaim);
+  cudaFree(p->ffin);
+  cudaFree(p->fscratch);
   delete p;
 }
 
@@ -192,6 +197,10 @@ int do_reset(hs_pool* p, cudaStream_t st) {
   if (p->pend_live && cudaMemsetAsync(p->pend_live, 0, nrl * sizeof(uint32_t), st) != cudaSuccess) return HS_ERR_CUDA;
   if (cudaMemsetAsync(p->attn_ticket, 0, (size_t)p->cfg.num_requests * p->attn_tickets_per_req * sizeof(uint32_t), st) !=
       cudaSuccess)
+    return HS_ERR_CUDA;
+  if (p->fclaim != nullptr &&
+      (cudaMemsetAsync(p->fclaim, 0, nrl * p->cfg.top_k * sizeof(uint32_t), st) != cudaSuccess ||
+       cudaMemsetAsync(p->ffin, 0, nrl * sizeof(uint32_t), st) != cudaSuccess))
     return HS_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? HS_OK : HS_ERR_CUDA;
 }
@@ -458,6 +467,19 @@ extern "C" int hs_pool_create(const hs_config* cfg, int cuda_device, hs_pool** o
     if (rc == HS_OK) rc = dev_alloc(&p->pend_live, L * R);
   }
   if (rc == HS_OK) rc = hs_resolve_prepare(p);
+  p->resolve_ctas = p->resolve_cs;
+  if (rc == HS_OK && cfg->early_fetch) {
+    // the position -> slot map (every entry -1: no position installed yet), the claim words and
+    // finish counters (cleared by do_reset), and about top_k / 4 scratch records per (layer, request)
+    p->resolve_ctas = 2 * p->resolve_cs;
+    p->fetch_rows = (cfg->top_k + 4 * p->resolve_cs - 1) / (4 * p->resolve_cs);
+    rc = dev_alloc(&p->pos_slot, L * R * (size_t)cfg->capacity);
+    if (rc == HS_OK && cudaMemset(p->pos_slot, 0xff, L * R * (size_t)cfg->capacity * sizeof(int32_t)) != cudaSuccess)
+      rc = HS_ERR_CUDA;
+    if (rc == HS_OK) rc = dev_alloc(&p->fclaim, L * R * (size_t)cfg->top_k);
+    if (rc == HS_OK) rc = dev_alloc(&p->ffin, L * R);
+    if (rc == HS_OK) rc = dev_alloc(&p->fscratch, L * R * (size_t)p->resolve_cs * p->fetch_rows * (size_t)p->rec);
+  }
   if (rc == HS_OK) rc = hs_attn_prepare(cfg, p->num_sms);
   if (rc == HS_OK) rc = do_reset(p, 0);
   if (rc == HS_OK && cudaDeviceSynchronize() != cudaSuccess) rc = HS_ERR_CUDA;
@@ -575,7 +597,7 @@ extern "C" int hs_device_usage(hs_pool* pool, int64_t* pages_in_use, int64_t* pa
 }
 
 extern "C" int hs_debug_stall_next(hs_pool* pool, int kernels) {
-  if (pool == nullptr || (kernels & ~(HS_STALL_ATTN | HS_STALL_RESOLVE)) != 0) return HS_ERR_ARG;
+  if (pool == nullptr || (kernels & ~(HS_STALL_ATTN | HS_STALL_RESOLVE | HS_STALL_FETCH)) != 0) return HS_ERR_ARG;
   pool->debug_stall |= kernels;
   return HS_OK;
 }

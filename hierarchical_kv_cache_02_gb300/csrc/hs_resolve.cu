@@ -65,6 +65,15 @@ struct ResolveArgs {
   int stage_off, stage_recs;  // staging area for early miss copies: byte offset in shared memory, records
   int stall;                  // test hook (hs_debug_stall_next): leave the early copies' arrival out
   uint32_t* res_count;        // layer slice [R][2]: launches, CTAs finished (per request)
+  int nreq;                   // requests of this launch: CTAs [0, nreq cs) decide, the rest fetch
+  // early fetch (null when off): layer slices of the position -> slot map [R][C], the claim words
+  // [R][k], the finish counters [R] and the scratch [R][cs x fetch_rows][rec]
+  int32_t* pos_slot;
+  uint32_t* fclaim;
+  uint32_t* ffin;
+  uint8_t* fscratch;
+  int fetch_rows;
+  int fstall;                 // test hook: one claimed record is never marked as landed
 };
 
 __device__ __forceinline__ uint32_t ht_hash(int32_t p, int bits) { return ((uint32_t)p * 0x9E3779B1u) >> (32 - bits); }
@@ -276,26 +285,185 @@ __device__ void select_threshold(const uint32_t* key32, const uint8_t* flag, int
 
 // A resolve CTA's last act: once every thread's writes (locs, metadata, fetched rows) are done, count
 // the CTA as finished for its request, with release ordering (an attention that waits for the count
-// then reads those writes).
-__device__ __forceinline__ void count_finished(uint32_t* res_count, int r) {
+// then reads those writes).  With fetch CTAs, the last CTA of the request's launch to get here first
+// clears the request's claim words for the next launch: every other CTA counted itself after its
+// last use of them.
+__device__ __forceinline__ void count_finished(const ResolveArgs& a, int r) {
   __syncthreads();
+  if (a.fclaim != nullptr) {
+    __shared__ int s_last;
+    if (threadIdx.x == 0) {
+      __threadfence();
+      s_last = atomicAdd(&a.ffin[r], 1u) == (uint32_t)(2 * a.cs - 1);
+      __threadfence();
+    }
+    __syncthreads();
+    if (s_last) {
+      for (int i = threadIdx.x; i < a.k; i += kThreads) a.fclaim[(int64_t)r * a.k + i] = 0u;
+      if (threadIdx.x == 0) a.ffin[r] = 0u;
+      __syncthreads();
+    }
+  }
   if (threadIdx.x == 0) {
     __threadfence();
-    atomicAdd(&res_count[2 * r + 1], 1u);
+    atomicAdd(&a.res_count[2 * r + 1], 1u);
+  }
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// A fetch CTA (early fetch): from the launch's start, copy the missing records of its share
+// [e0, e1) of the request's top-k list from the host history into its scratch rows, while the
+// deciding CTAs work out the victims.  An entry counts as missing unless the slot its position was
+// last installed in is below the buffer's slot count and still carries the position's tag (a hit
+// slot is never rewritten by this launch, so a hit is never taken for a miss; a miss taken for a hit,
+// or an entry the decision discards, only costs a fetch nobody uses).  Each record is claimed first
+// (claim word 0 -> 1) so that it crosses the host link once, and released as landed with its row.
+// The CTA takes at most fetch_rows records; the deciding CTAs fetch the rest themselves.
+#ifndef HS_FETCH_UNROLL
+#define HS_FETCH_UNROLL 4
+#endif
+constexpr int kFetchUnroll = HS_FETCH_UNROLL;  // 16-byte loads a lane has in flight per record
+#ifndef HS_FETCH_WARPS
+#define HS_FETCH_WARPS 32
+#endif
+constexpr int kFetchWarps = HS_FETCH_WARPS;  // warps of a fetch CTA that copy records
+__device__ void early_fetch_cta(const ResolveArgs& a, int r, int crank) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  int32_t* lst = (int32_t*)smem;  // [e1 - e0]: the share's apparent misses (top-k indices)
+  __shared__ int s_n;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int k = a.k;
+  const int cap = a.scap[r];
+  if (min(a.B, cap) < k) return;  // too few slots: the deciding CTAs change nothing
+  const int e0 = (int)((int64_t)k * crank / a.cs), e1 = (int)((int64_t)k * (crank + 1) / a.cs);
+  const int32_t* topk = a.topk + (int64_t)(r - a.r0) * k;
+  const int32_t* tag = a.tag + (int64_t)r * a.B;
+  const int32_t* ps = a.pos_slot + (int64_t)r * a.C;
+  if (tid == 0) s_n = 0;
+  __syncthreads();
+  for (int ib = e0 + 32 * warp; ib < e1; ib += kThreads) {
+    const int i = ib + lane;
+    bool miss = false;
+    if (i < e1) {
+      const int32_t p = topk[i];
+      if (p >= 0 && (int64_t)p < a.C) {
+        const int32_t s = __ldcg(ps + p);
+        miss = !(s >= 0 && s < cap && __ldcg(tag + s) == p);
+      }
+    }
+    const uint32_t bm = __ballot_sync(0xffffffffu, miss);
+    int base = 0;
+    if (lane == 0 && bm != 0u) base = atomicAdd(&s_n, __popc(bm));
+    base = __shfl_sync(0xffffffffu, base, 0);
+    if (miss) lst[base + __popc(bm & ((1u << lane) - 1u))] = i;
+  }
+  __syncthreads();
+  HS_PHASE(hs_phase_res, 21, tid == 0);
+  const int n = min(s_n, a.fetch_rows);
+  const uint64_t* row = a.pt + ((int64_t)r * a.L + a.layer) * a.max_pages;
+  uint32_t* claim = a.fclaim + (int64_t)r * k;
+  const int row0 = crank * a.fetch_rows;  // this CTA's first row in the request's scratch
+  uint8_t* scratch = a.fscratch + (int64_t)r * a.cs * a.fetch_rows * a.rec;
+  const int vpr = (int)(a.rec / 16);
+  bool held = a.fstall != 0 && r == a.r0 && crank == 0 && warp == 0;  // test hook: keep one claim
+  for (int x = warp; warp < kFetchWarps && x < n; x += kFetchWarps) {
+    const int i = lst[x];
+    const uint4* src = (const uint4*)hs_page_row_addr(row, a.page_shift, a.rec, topk[i]);
+    if (src == nullptr) continue;  // not reserved: the deciding CTA flags it
+    uint32_t won = 0u;
+    if (lane == 0) won = atomicCAS(&claim[i], 0u, 1u) == 0u ? 1u : 0u;
+    if (__shfl_sync(0xffffffffu, won, 0) == 0u) continue;
+    uint4* dst = (uint4*)(scratch + (int64_t)(row0 + x) * a.rec);
+    for (int v0 = 0; v0 < vpr; v0 += 32 * kFetchUnroll) {
+      uint4 t[kFetchUnroll];
+#pragma unroll
+      for (int u = 0; u < kFetchUnroll; ++u) {
+        const int v = v0 + 32 * u + lane;
+        if (v < vpr) t[u] = ld_nc_v4(src + v);
+      }
+#pragma unroll
+      for (int u = 0; u < kFetchUnroll; ++u) {
+        const int v = v0 + 32 * u + lane;
+        if (v < vpr) dst[v] = t[u];
+      }
+    }
+    __threadfence();  // each lane's part of the row, before the release below
+    __syncwarp();
+    if (held) {
+      held = false;
+      continue;
+    }
+    if (lane == 0) st_release_gpu(&claim[i], ((uint32_t)(row0 + x + 1) << 2) | 2u);
+  }
+}
+
+// Phase B of a deciding CTA (early fetch): its misses that the fetch CTAs claimed, s_fq[0, nfq),
+// one warp per record: wait (bounded) until the record has landed, then move it from its scratch row
+// to its slot.  A wait that gives up flags the resolve and fetches the record from the host instead
+// (the same bytes).
+__device__ __forceinline__ void take_landed(const ResolveArgs& a, int r, const uint32_t* claim, const int32_t* s_fq,
+                                              int nfq, const int32_t* miss_idx, const int32_t* miss_pos,
+                                              const int32_t* victims, const uint64_t* s_slots, const uint64_t* row) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, vpr = (int)(a.rec / 16);
+  const uint8_t* scratch = a.fscratch + (int64_t)r * a.cs * a.fetch_rows * a.rec;
+  for (int x = warp; x < nfq; x += kWarps) {
+    const int q = s_fq[x];
+    const uint32_t* cw = &claim[miss_idx[q]];
+    uint32_t w = ld_acquire_gpu(cw);
+    if ((w & 3u) != 2u) {
+      const uint64_t t0 = global_ns();
+      do {
+        __nanosleep(200);
+        w = ld_acquire_gpu(cw);
+      } while ((w & 3u) != 2u && global_ns() - t0 < 1000000000ull);
+    }
+    uint4* dst = (uint4*)hs_slot_addr(s_slots, a.sshift, a.rec, victims[q]);
+    if ((w & 3u) == 2u) {
+      const uint4* src = (const uint4*)(scratch + (int64_t)((w >> 2) - 1u) * a.rec);
+      for (int v = lane; v < vpr; v += 32) dst[v] = __ldcg(src + v);
+    } else {
+      atomicOr(a.err_global, (uint32_t)HS_DEVERR_TIMEOUT);
+      const uint4* src = (const uint4*)hs_page_row_addr(row, a.page_shift, a.rec, miss_pos[q]);
+      for (int v = lane; v < vpr; v += 32) dst[v] = ld_nc_v4(src + v);
+    }
   }
 }
 
 template <int NV>
 __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
-  const int r = a.r0 + (int)(blockIdx.x / a.cs);
-  const int crank = blockIdx.x % a.cs;  // rank inside the cluster of this request
+  // CTAs [0, nreq cs) decide, one cluster per request; with early fetch, CTAs [nreq cs, 2 nreq cs)
+  // are the requests' fetch CTAs, in clusters of the same size that never use the cluster barrier
+  const bool fetcher = (int)blockIdx.x >= a.nreq * a.cs;
+  const int b = fetcher ? (int)blockIdx.x - a.nreq * a.cs : (int)blockIdx.x;
+  const int r = a.r0 + b / a.cs;
+  const int crank = b % a.cs;  // rank inside the cluster of this request
   asm volatile("griddepcontrol.wait;" ::: "memory");
   // the launch is counted for its requests before the next kernel may start
-  if (crank == 0 && threadIdx.x == 0) {
+  if (!fetcher && crank == 0 && threadIdx.x == 0) {
     atomicAdd(&a.res_count[2 * r], 1u);
     __threadfence();
   }
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (fetcher) {
+    HS_PHASE(hs_phase_res, 0, threadIdx.x == 0);
+    early_fetch_cta(a, r, crank);
+    HS_PHASE(hs_phase_res, 22, threadIdx.x == 0);
+    count_finished(a, r);
+    return;
+  }
   HS_PHASE(hs_phase_res, 0, threadIdx.x == 0);
   extern __shared__ __align__(16) uint8_t smem[];
   const int tid = threadIdx.x;
@@ -357,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
       }
       a.state[r].err = st.err | e;
     }
-    count_finished(a.res_count, r);
+    count_finished(a, r);
     return;
   }
   __shared__ uint64_t s_slots[kMaxSlotPages];  // this buffer's page row (first used after the decision)
@@ -392,12 +560,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
   int app_slot = -1;
   uint4* app_dh = nullptr;  // the append's place in the host history (known after the hash)
   __shared__ uint32_t s_dups, s_klo, s_khi;
+  __shared__ int s_nfq;  // phase B: misses taken from the fetch CTAs' scratch
   __shared__ unsigned long long s_app_page;
   if (tid == 0) {
     err_bits = 0u;
     mbar_init1(&bar_stage);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     s_dups = 0u;
+    s_nfq = 0;
     s_klo = 0xffffffffu;
     s_khi = 0u;
   }
@@ -709,6 +879,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
     for (int q = q0 + tid; q < q1; q += kThreads) {
       const int j = victims[q];
       tag[j] = miss_pos[q];
+      if (a.pos_slot != nullptr) a.pos_slot[(int64_t)r * a.C + miss_pos[q]] = j;
       stamp[j] = a.policy == HS_POLICY_FIFO ? clock + (uint32_t)q : clock + (uint32_t)h + (uint32_t)q;
       locs[miss_idx[q]] = j;
       if (a.pend != nullptr) {
@@ -746,6 +917,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
       }
       if (tid == 0 && !evicted) {
         tag[app_slot] = (int32_t)app_p;
+        if (a.pos_slot != nullptr) a.pos_slot[(int64_t)r * a.C + app_p] = app_slot;
         if (!restamped) stamp[app_slot] = st.clock;
       }
     }
@@ -760,9 +932,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
         if (src == nullptr) atomicOr(a.err_global, (uint32_t)HS_DEVERR_PAGE);
         s_src[q - q0] = (uint64_t)(uintptr_t)src;
       }
+      // early fetch: a miss the fetch CTAs have claimed (landed or in flight) comes from their
+      // scratch below; the others are claimed here and fetched from the host
+      uint32_t* claim = a.fclaim != nullptr ? a.fclaim + (int64_t)r * k : nullptr;
+      int32_t* s_fq = ht_val;  // [q1 - q0]: those misses (the hash table's values: dead by now)
+      if (claim != nullptr) {
+        for (int q = q0 + tid; q < q1; q += kThreads) {
+          if (s_src[q - q0] == 0ull) continue;  // not reserved (flagged): nothing to fetch
+          if (atomicCAS(&claim[miss_idx[q]], 0u, 3u) != 0u) {
+            s_src[q - q0] = 0ull;
+            s_fq[atomicAdd(&s_nfq, 1)] = q;
+          }
+        }
+      }
       // the rest straight from the host, then the staged ones from shared memory
       __syncthreads();
+      HS_PHASE(hs_phase_res, 23, tid == 0);
       fetch_misses<NV>(a, q0 + nstage, q1, s_src + nstage, victims, s_slots);
+      HS_PHASE(hs_phase_res, 24, tid == 0);
+      if (claim != nullptr) take_landed(a, r, claim, s_fq, s_nfq, miss_idx, miss_pos, victims, s_slots, pt_row());
       if (nstage > 0) {
         // the staged records have landed (bounded: a wait that gives up flags the resolve and skips
         // the staged records, after a second bounded wait for copies still in flight)
@@ -798,7 +986,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
       a.step_log[((int64_t)st.nres * a.L + a.layer) * a.R + r] = (uint32_t)m;
     if (a.pend != nullptr) a.pend_live[r] = 1u;
   }
-  count_finished(a.res_count, r);
+  count_finished(a, r);
 }
 
 struct AppendArgs {
@@ -817,6 +1005,7 @@ struct AppendArgs {
   uint64_t seed;
   const hs_pending* pend;  // fetch-in-attention mode: layer slice [R][k], else null
   uint32_t* pend_live;
+  int32_t* pos_slot;       // early fetch: layer slice [R][C] of the position -> slot map, else null
   int R, L, layer, B, policy, k;
 };
 
@@ -891,6 +1080,7 @@ __global__ void __launch_bounds__(kAppendThreads) k_append(AppendArgs a) {
   }
   if (tid == 0) {
     tag[slot] = (int32_t)p;
+    if (a.pos_slot != nullptr) a.pos_slot[(int64_t)r * a.C + p] = slot;
     stamp[slot] = st.clock;
     hs_rl_state ns = st;
     ns.clock = st.clock + 1u;
@@ -940,14 +1130,14 @@ size_t resolve_launch_smem(const hs_config* c, int* stage_off, int* stage_recs) 
   size_t room = base < kDynSmemCap ? kDynSmemCap - base : 0;
   room = room < kStageBytes ? room : kStageBytes;
   *stage_off = (int)base;
-  *stage_recs = c->fetch_in_attention ? 0 : (int)(room / rec);
+  *stage_recs = (c->fetch_in_attention || c->early_fetch) ? 0 : (int)(room / rec);
   return base + (size_t)*stage_recs * rec + (*stage_recs > 0 ? 128 : 0);  // + alignment slack
 }
 
 template <int NV>
 cudaError_t launch_resolve_nv(const ResolveArgs* a, int nreq, int cs, size_t smem, cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(nreq * cs), 1, 1);
+  cfg.gridDim = dim3((unsigned)(nreq * cs * (a->fclaim != nullptr ? 2 : 1)), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
@@ -1042,7 +1232,19 @@ int hs_launch_resolve(hs_pool* p, int layer, int r0, int nreq, const int64_t* d_
   a.app_pos = d_pos;
   a.app_rec = (const uint8_t*)d_rec;
   a.r0 = r0;
+  a.nreq = nreq;
   a.res_count = p->res_count + (int64_t)layer * R * 2;
+  if (p->fclaim != nullptr) {
+    a.pos_slot = p->pos_slot + (int64_t)layer * R * c.capacity;
+    a.fclaim = p->fclaim + (int64_t)layer * R * c.top_k;
+    a.ffin = p->ffin + (int64_t)layer * R;
+    a.fscratch = p->fscratch + (int64_t)layer * R * a.cs * p->fetch_rows * p->rec;
+    a.fetch_rows = p->fetch_rows;
+    if ((p->debug_stall & HS_STALL_FETCH) != 0) {  // test hook
+      a.fstall = 1;
+      p->debug_stall &= ~HS_STALL_FETCH;
+    }
+  }
   // an attention launched right after a whole-batch resolve of its layer on the same stream may
   // wait for its own request's resolve CTAs instead of the whole grid
   p->last_res_layer = (r0 == 0 && nreq == R) ? layer : -1;
@@ -1104,6 +1306,7 @@ int hs_launch_append(hs_pool* p, int layer, const int64_t* d_pos, const void* d_
   a.k = c.top_k;
   a.pend = p->pend != nullptr ? p->pend + (int64_t)layer * R * c.top_k : nullptr;
   a.pend_live = p->pend_live != nullptr ? p->pend_live + (int64_t)layer * R : nullptr;
+  a.pos_slot = p->pos_slot != nullptr ? p->pos_slot + (int64_t)layer * R * c.capacity : nullptr;
   k_append<<<c.num_requests, kAppendThreads, 0, st>>>(a);
   return cudaGetLastError() == cudaSuccess ? HS_OK : HS_ERR_CUDA;
 }

@@ -6,10 +6,11 @@ For each named workload of bench.py it runs the decode steps to a steady state, 
 of the resolve (layer 0) and, for the shared-latent workloads, one launch of the attention, and
 prints the median over the CTAs of each stamp, in microseconds from the first CTA's start.
 
-    python -m hierarchical_kv_cache_02_gb300.phase_trace gqa_b16_l32 mla_b8 stress_b16_l4
+    python -m hierarchical_kv_cache_02_gb300.phase_trace gqa_b16_l32 mla_b8 stress_b16_l4 mla_b8:early gqa_b16_l32@32
 
-Needs a GPU.  The workloads are those of bench.py (GQA with 4 of its 32 layers: one layer's steady
-state is the same).
+Needs a GPU.  The workloads are those of bench.py (GQA with 4 of its 32 layers unless NAME@L names
+the layer count: one layer's steady state is the same, but its host history spans an eighth of the
+bytes).  NAME:early runs the resolve with its fetch CTAs (early_fetch = 1).
 """
 from __future__ import annotations
 
@@ -31,7 +32,8 @@ RESOLVE.update({10: "  thread 0: hash inserts done", 11: "  thread 0: append sea
                 14: "  select pass 0: histogram", 15: "  select pass 0: bin found",
                 16: "  select pass 1: histogram", 17: "  select pass 1: bin found",
                 18: "  compaction: counts scanned", 19: "  thread 0: victims placed",
-                20: "  compaction: barrier passed"})
+                20: "  compaction: barrier passed", 21: "fetch CTAs: misses found", 22: "fetch CTAs: done",
+                23: "phase B: misses claimed", 24: "phase B: own misses fetched"})
 ATTN = {0: "start", 1: "setup", 38: "scores of tile 0 issued", 39: "scores of tile 1 issued",
         40: "value product of tile 0 issued", 41: "value product of tile 1 issued",
         43: "softmax: scores of tile 0 seen", 44: "softmax: scores of tile 1 seen",
@@ -79,11 +81,17 @@ def main(argv):
     for fn in ("hs_phase_resolve_clear", "hs_phase_attn_clear"):
         getattr(lib, fn).argtypes = []
     for name in argv or ["gqa_b16_l32", "mla_b8", "stress_b16_l4"]:
+        # NAME:early runs the resolve with fetch CTAs (early_fetch = 1); NAME@L sets the layer count
+        # (GQA: 4 of its 32 layers by default; its host history then spans an eighth of the bytes)
+        name, _, nl = name.partition("@")
+        name, _, mode = name.partition(":")
         w = dict(bench.WORKLOADS[name])
-        if name == "gqa_b16_l32":
+        if nl:
+            w["L"] = int(nl)
+        elif name == "gqa_b16_l32":
             w["L"] = 4
         W = 24
-        wl = bench.Workload(w, W + 1, "cuda", seed=bench.replica_seed(0))
+        wl = bench.Workload(w, W + 1, "cuda", seed=bench.replica_seed(0), fetch=mode or "resolve")
         pool = HsPool(wl.cfg)
         wl.prefill(pool)
         R, L, k = w["R"], w["L"], w["k"]
@@ -120,7 +128,8 @@ def main(argv):
                     lib.hs_phase_attn_read(att_tr.ctypes.data)
         st = pool.stats()
         pool.close()
-        print(f"{name}: misses per (request, layer, step) {st['misses'] / (R * L * (W + 1)):.0f} of k = {k}")
+        print(f"{name}{':' + mode if mode else ''}: misses per (request, layer, step) "
+              f"{st['misses'] / (R * L * (W + 1)):.0f} of k = {k}")
         rows, n = _table(res_tr, RESOLVE)
         print(f"  k_resolve, {n} CTAs (median / min / max over the CTAs, us from the first CTA's start)")
         for nm, cnt, med, lo, hi in rows:

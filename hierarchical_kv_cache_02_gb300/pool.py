@@ -49,6 +49,7 @@ class HsConfig:
     buffer_page_slots: int = 0
     device_pool_slots: int = 0
     host_to_device_ratio: float = 0.0
+    early_fetch: int = 0
 
     @property
     def record_bytes(self) -> int:
@@ -285,7 +286,9 @@ class HsPool:
 
     def debug_stall_next(self, kernels: int):
         """Test hook: the next launch of each kernel in `kernels` (STALL_ATTN, STALL_RESOLVE) leaves
-        one barrier arrival out, so its bounded wait gives up and reports DEVERR_TIMEOUT."""
+        one barrier arrival out, so its bounded wait gives up and reports DEVERR_TIMEOUT.
+        STALL_FETCH: one record a fetch CTA claimed is never marked as landed; the deciding CTA that
+        needs it gives up waiting, reports DEVERR_TIMEOUT and fetches it from the host itself."""
         _check("hs_debug_stall_next", self.lib.hs_debug_stall_next(self._h, int(kernels)))
 
     def device_usage(self) -> dict:

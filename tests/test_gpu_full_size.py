@@ -116,31 +116,34 @@ def test_full_mla_batch8(fused):
     run_full(cfg, ctx0, steps, spec, pairs, samples, seed=11, fused=fused)
 
 
-@pytest.mark.parametrize("fetch,fused", [(0, False), (0, True), (1, False), (1, True)])
+@pytest.mark.parametrize("fetch,fused", [(0, False), (0, True), (1, False), (1, True), (2, True)])
 def test_full_gqa_batch16_32_layers(fetch, fused):
     """Batch 16, 32 layers, 8 KV heads x (128 K + 128 V), 32 q heads, context 131072 shared by the
     requests (17 GB pinned), k=2048, B=4096, drift keep 88%, write-through append, 64 steps
-    (16 with the misses fetched inside the attention).  fused = True runs hs_append_resolve (16
-    resolve clusters with the early miss copies staged in shared memory), the call the headline
-    bench times; fetch = 1 with fused = True is the bench's two-micro-batch pass at full batch."""
+    (16 with the misses fetched inside the attention, 32 with fetch CTAs).  fused = True runs
+    hs_append_resolve (16 resolve clusters with the early miss copies staged in shared memory), the
+    call the headline bench times; fetch = 1 with fused = True is the bench's two-micro-batch pass
+    at full batch; fetch = 2 adds the fetch CTAs that copy misses while the decision runs."""
     ctx0 = 131072
-    steps = 64 if fetch == 0 else 16
+    steps = {0: 64, 1: 16, 2: 32}[fetch]
     cfg = HsConfig(num_requests=16, num_layers=32, capacity=ctx0 + steps, layout=LAYOUT_GQA, num_q_heads=32,
                    num_kv_heads=8, head_dim_qk=128, head_dim_v=128, top_k=2048, buffer_slots=4096, seed=5,
-                   shared_prefix=ctx0, fetch_in_attention=fetch)
+                   shared_prefix=ctx0, fetch_in_attention=int(fetch == 1), early_fetch=int(fetch == 2))
     spec = inputs.TraceSpec(ctx0=ctx0, k=2048, steps=steps, keep=0.88, recency_mean=2048, appends=True)
     pairs = [(3, 7), (15, 31)]
     samples = {(steps - 1, 3, 7), (steps // 2, 15, 31), (0, 15, 31)}
     run_full(cfg, ctx0, steps, spec, pairs, samples, seed=13, shared=True, fused=fused)
 
 
-def test_full_stress_bursts():
+@pytest.mark.parametrize("early", [0, 1])
+def test_full_stress_bursts(early):
     """Batch 16, 4 layers, context 262144, 576-dim latent, 64 heads, k=2048, B=8192, LRU, bursts
     (every 32 steps 40% of the top-k jumps to a far region), 128 steps with write-through append
-    fused into the resolve (the call bench.py times)."""
+    fused into the resolve (the call bench.py times); early = 1 with fetch CTAs."""
     ctx0, steps = 262144, 128
     cfg = HsConfig(num_requests=16, num_layers=4, capacity=ctx0 + steps, layout=LAYOUT_MLA, num_q_heads=64,
-                   num_kv_heads=1, head_dim_qk=576, head_dim_v=512, top_k=2048, buffer_slots=8192, seed=7)
+                   num_kv_heads=1, head_dim_qk=576, head_dim_v=512, top_k=2048, buffer_slots=8192, seed=7,
+                   early_fetch=early)
     spec = inputs.TraceSpec(ctx0=ctx0, k=2048, steps=steps, keep=0.88, recency_mean=2048, appends=True,
                             burst_every=32, burst_frac=0.4, far_gap=8 * 2048)
     pairs = [(2, 1), (11, 3)]

@@ -18,15 +18,18 @@ from hierarchical_kv_cache_02_gb300 import (DEVERR_APPEND, DEVERR_DUP, DEVERR_LO
 
 
 def _gqa(R, L, C, k, B, policy=0, kvh=8, G=4, io=64, log=0, P0=0, seed=3, fetch=0):
+    """fetch: 0 the resolve copies the misses, 1 the attention does, 2 the resolve with fetch CTAs
+    that start copying the misses before the decision ends (early_fetch)."""
     return HsConfig(num_requests=R, num_layers=L, capacity=C, layout=LAYOUT_GQA, num_q_heads=kvh * G,
                     num_kv_heads=kvh, head_dim_qk=128, head_dim_v=128, top_k=k, buffer_slots=B, policy=policy,
-                    seed=seed, io_chunk_bytes=io, log_steps=log, shared_prefix=P0, fetch_in_attention=fetch)
+                    seed=seed, io_chunk_bytes=io, log_steps=log, shared_prefix=P0, fetch_in_attention=int(fetch == 1),
+                    early_fetch=int(fetch == 2))
 
 
-def _mla(R, L, C, k, B, Hq=16, policy=0, io=64, log=0, P0=0):
+def _mla(R, L, C, k, B, Hq=16, policy=0, io=64, log=0, P0=0, early=0):
     return HsConfig(num_requests=R, num_layers=L, capacity=C, layout=LAYOUT_MLA, num_q_heads=Hq, num_kv_heads=1,
                     head_dim_qk=576, head_dim_v=512, top_k=k, buffer_slots=B, policy=policy, seed=11,
-                    io_chunk_bytes=io, log_steps=log, shared_prefix=P0)
+                    io_chunk_bytes=io, log_steps=log, shared_prefix=P0, early_fetch=early)
 
 
 def run_and_compare(sc: Scenario, attn_every=1, check_state=True, fused=False):
@@ -84,18 +87,19 @@ def test_tiny_single_request_mla():
     run_and_compare(sc)
 
 
-@pytest.mark.parametrize("fetch", [0, 1])
+@pytest.mark.parametrize("fetch", [0, 1, 2])
 @pytest.mark.parametrize("policy", [0, 1, 2, 3])
 def test_gqa_policies_ragged(policy, fetch):
     """3 requests x 2 layers, k=300 (not a multiple of the stage), B=640, every policy; misses
-    copied by the resolve (fetch=0) or by the attention while it gathers (fetch=1)."""
+    copied by the resolve (fetch=0), by the attention while it gathers (fetch=1), or by the resolve
+    with fetch CTAs that start before the decision ends (fetch=2)."""
     B = 300 if policy == 3 else 640
     sc = Scenario(_gqa(3, 2, 3000 + 12, 300, B, policy=policy, fetch=fetch), ctx0=3000, steps=12, appends=True,
                   keep=0.8, recency_mean=200, seed=policy + 1)
     run_and_compare(sc)
 
 
-@pytest.mark.parametrize("fetch", [0, 1])
+@pytest.mark.parametrize("fetch", [0, 1, 2])
 @pytest.mark.parametrize("policy", [0, 1, 2, 3])
 def test_fused_append_resolve(policy, fetch):
     """hs_append_resolve equals append then resolve: same slots, state, counters and outputs as
@@ -110,13 +114,13 @@ def test_fused_append_resolve(policy, fetch):
     for t in range(0, 10, 2):
         sc.trace[t, 0, 0][sc.trace[t, 0, 0] == 800 + t] = -1
     run_and_compare(sc, fused=True)
-    if policy == 0 and fetch == 0:
-        sc = Scenario(_mla(1, 1, 4096 + 16, 256, 512), ctx0=4096, steps=16, appends=True, keep=0.9,
-                      recency_mean=512, seed=3)
+    if policy == 0 and fetch != 1:
+        sc = Scenario(_mla(1, 1, 4096 + 16, 256, 512, early=int(fetch == 2)), ctx0=4096, steps=16, appends=True,
+                      keep=0.9, recency_mean=512, seed=3)
         run_and_compare(sc, fused=True)
 
 
-@pytest.mark.parametrize("layout", ["gqa", "gqa_fetch", "mla"])
+@pytest.mark.parametrize("layout", ["gqa", "gqa_fetch", "gqa_early", "mla"])
 def test_request_ranges_on_two_streams(layout):
     """Two micro-batches of one pool on two streams, each request's layers in order: slots, state
     and counters equal the oracle's, outputs are within the attention tolerance of its fp64
@@ -124,7 +128,7 @@ def test_request_ranges_on_two_streams(layout):
     if layout == "mla":
         cfg = _mla(4, 2, 3000 + 6, 256, 512, Hq=64)
     else:
-        cfg = _gqa(4, 2, 3000 + 6, 256, 512, fetch=1 if layout == "gqa_fetch" else 0)
+        cfg = _gqa(4, 2, 3000 + 6, 256, 512, fetch={"gqa": 0, "gqa_fetch": 1, "gqa_early": 2}[layout])
     sc = Scenario(cfg, ctx0=3000, steps=6, appends=True, seed=61)
     full, split = HsPool(cfg), HsPool(cfg)
     prefill(full, sc)
@@ -166,7 +170,7 @@ def test_request_ranges_on_two_streams(layout):
     split.close()
 
 
-@pytest.mark.parametrize("fetch", [0, 1])
+@pytest.mark.parametrize("fetch", [0, 1, 2])
 def test_layer_group_schedule_on_side_streams(fetch):
     """Layer groups sharing one selection (exact layer-group prefetch): the group's resolves run at
     once, each layer on its own stream, and the attentions follow on another stream as their
@@ -228,7 +232,7 @@ def test_layer_group_schedule_on_side_streams(fetch):
     grp.close()
 
 
-@pytest.mark.parametrize("fetch", [0, 1])
+@pytest.mark.parametrize("fetch", [0, 1, 2])
 def test_chained_microbatches_in_one_graph(fetch):
     """The bench's two-micro-batch schedule: each half on its own stream, the halves' resolves in one
     chain and their attentions in another, every step captured in one CUDA graph.  Slots, state and
@@ -352,6 +356,8 @@ def test_mla_64_heads_multi_tile_splits():
 def test_io_chunk_sizes(io):
     sc = Scenario(_gqa(2, 1, 2000 + 6, 128, 256, kvh=2, G=4, io=io), ctx0=2000, steps=6, appends=True, seed=9)
     run_and_compare(sc)
+    sc = Scenario(_gqa(2, 1, 2000 + 6, 128, 256, kvh=2, G=4, io=io, fetch=2), ctx0=2000, steps=6, appends=True, seed=9)
+    run_and_compare(sc)
 
 
 @pytest.mark.parametrize("G", [1, 2, 8])
@@ -360,7 +366,7 @@ def test_gqa_group_sizes(G):
     run_and_compare(sc)
 
 
-@pytest.mark.parametrize("fetch", [0, 1])
+@pytest.mark.parametrize("fetch", [0, 1, 2])
 def test_shared_prefix_history(fetch):
     """Requests share one prefilled history (read-only); appended tokens are private."""
     sc = Scenario(_gqa(3, 2, 2500 + 8, 200, 400, P0=2500, fetch=fetch), ctx0=2500, steps=8, appends=True, seed=21)
@@ -373,7 +379,7 @@ def test_buffer_as_large_as_context_no_misses_after_warmup():
     run_and_compare(sc)
 
 
-@pytest.mark.parametrize("fetch", [0, 1])
+@pytest.mark.parametrize("fetch", [0, 1, 2])
 def test_small_k_and_b_equal_k(fetch):
     for policy in (0, 3):
         sc = Scenario(_gqa(2, 1, 500, 1, 1, kvh=1, G=4, policy=policy, fetch=fetch), ctx0=500, steps=10,
@@ -384,11 +390,12 @@ def test_small_k_and_b_equal_k(fetch):
         run_and_compare(sc)
 
 
+@pytest.mark.parametrize("fetch", [0, 2])
 @pytest.mark.parametrize("policy", [0, 3])
-def test_repeats_of_resident_missing_and_appended_positions(policy):
+def test_repeats_of_resident_missing_and_appended_positions(policy, fetch):
     """A repeated position counts at its first occurrence only, whether the position is resident (a
     hit), missing, or the token the fused append has just written."""
-    cfg = _gqa(2, 1, 600 + 8, 64, 128, policy=policy, kvh=2)
+    cfg = _gqa(2, 1, 600 + 8, 64, 128, policy=policy, kvh=2, fetch=fetch)
     sc = Scenario(cfg, ctx0=600, steps=5, appends=True, seed=21)
     tr = sc.trace.copy()
     prev = set(tr[1, 0, 0].tolist())                   # resident after step 1 (B = 128 >= 2 k)
@@ -422,9 +429,10 @@ def test_repeats_of_resident_missing_and_appended_positions(policy):
     pool.close()
 
 
-def test_padding_duplicates_and_out_of_range():
+@pytest.mark.parametrize("fetch", [0, 2])
+def test_padding_duplicates_and_out_of_range(fetch):
     """Invalid entries are skipped like padding, flagged, and attention ignores them."""
-    cfg = _gqa(2, 1, 400, 16, 32, kvh=2)
+    cfg = _gqa(2, 1, 400, 16, 32, kvh=2, fetch=fetch)
     sc = Scenario(cfg, ctx0=400, steps=3, appends=False, seed=12)
     bad = sc.trace.copy()
     bad[1, 0, 0, 3] = -1
@@ -464,7 +472,8 @@ def test_append_out_of_range_flags():
 def test_exactness_cold_warm_resident_bit_identical():
     """Summary §3: the output over the hot buffer equals the output over fully resident KV,
     bit for bit, whatever the cache held before."""
-    for cfg in (_gqa(3, 1, 5000, 512, 1024), _gqa(3, 1, 5000, 512, 1024, fetch=1), _mla(2, 1, 5000, 512, 1024, Hq=32),
+    for cfg in (_gqa(3, 1, 5000, 512, 1024), _gqa(3, 1, 5000, 512, 1024, fetch=1),
+                _gqa(3, 1, 5000, 512, 1024, fetch=2), _mla(2, 1, 5000, 512, 1024, Hq=32),
                 _mla(2, 1, 5000, 512, 1024, Hq=64)):  # 64 heads: the tcgen05 kernel, hot slots vs resident rows
         sc = Scenario(cfg, ctx0=5000, steps=10, appends=False, keep=0.85, recency_mean=300, seed=2)
         warm = HsPool(cfg)
@@ -502,7 +511,7 @@ def test_resident_kv_bad_rows_flagged():
     pool.close()
 
 
-@pytest.mark.parametrize("fetch", [0, 1])
+@pytest.mark.parametrize("fetch", [0, 1, 2])
 def test_cuda_graph_replay_matches_eager(fetch):
     """All calls are capturable: one decode step (append, resolve, attention for every layer)
     captured once and replayed gives the eager results bit for bit."""

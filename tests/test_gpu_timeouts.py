@@ -8,6 +8,7 @@ after a cold start the same pool runs the scenario again in agreement with the o
 """
 import time
 
+import numpy as np
 import pytest
 
 from harness import OracleRun, Scenario, assert_layer_matches_oracle, assert_pool_matches_oracle, gpu_step, prefill
@@ -15,8 +16,8 @@ from harness import OracleRun, Scenario, assert_layer_matches_oracle, assert_poo
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
-from hierarchical_kv_cache_02_gb300 import DEVERR_TIMEOUT, LAYOUT_MLA, HsConfig, HsPool
-from hierarchical_kv_cache_02_gb300._lib import STALL_ATTN, STALL_RESOLVE
+from hierarchical_kv_cache_02_gb300 import DEVERR_TIMEOUT, LAYOUT_GQA, LAYOUT_MLA, HsConfig, HsPool
+from hierarchical_kv_cache_02_gb300._lib import STALL_ATTN, STALL_FETCH, STALL_RESOLVE
 
 
 def _scenario():
@@ -52,4 +53,48 @@ def test_wait_gives_up_reports_and_leaves_the_pool_usable(kernel):
         assert_layer_matches_oracle(sc, orc, ref, t, 0, locs, out, what=(kernel, t))
     assert_pool_matches_oracle(pool, orc, what=kernel)
     assert pool.stats()["error_bits"] == 0
+    pool.close()
+
+
+@pytest.mark.parametrize("layout", [LAYOUT_GQA, LAYOUT_MLA])
+def test_fetch_wait_gives_up_and_falls_back_to_the_host(layout):
+    """Early fetch: one record a fetch CTA claimed is never marked as landed.  The deciding CTA that
+    needs it waits for its limit, reports DEVERR_TIMEOUT and copies the record from the host itself,
+    so this step's outputs and the cache state still equal the oracle's, and later steps too."""
+    if layout == LAYOUT_GQA:
+        cfg = HsConfig(num_requests=3, num_layers=2, capacity=4000, layout=LAYOUT_GQA, num_q_heads=32, num_kv_heads=8,
+                       head_dim_qk=128, head_dim_v=128, top_k=512, buffer_slots=1024, seed=5, early_fetch=1)
+    else:
+        cfg = HsConfig(num_requests=2, num_layers=1, capacity=3000, layout=LAYOUT_MLA, num_q_heads=64,
+                       num_kv_heads=1, head_dim_qk=576, head_dim_v=512, top_k=512, buffer_slots=1024, seed=11,
+                       early_fetch=1)
+    # no appends: on the cold first step every selected position is a miss, so the held record is
+    # one a deciding CTA needs
+    sc = Scenario(cfg, ctx0=cfg.capacity, steps=3, appends=False, keep=0.85, recency_mean=300, seed=43)
+    pool = HsPool(cfg)
+    prefill(pool, sc)
+    orc = OracleRun(sc)
+    pool.debug_stall_next(STALL_FETCH)
+    for t in range(sc.steps):
+        t0 = time.perf_counter()
+        res = gpu_step(pool, sc, t)
+        torch.cuda.synchronize()
+        elapsed = time.perf_counter() - t0
+        ref = orc.step(t)
+        for l in range(cfg.num_layers):
+            locs, out = res[l]
+            assert_layer_matches_oracle(sc, orc, ref, t, l, locs, out, what=("fetch stall", t))
+        if t == 0:
+            assert elapsed >= 0.9, elapsed  # the wait ran for its limit (about one second)
+        assert pool.stats()["error_bits"] == DEVERR_TIMEOUT  # reported, and by the stalled step only
+    for l in range(cfg.num_layers):
+        tag, stamp, clock = pool.read_state(l)
+        for r in range(cfg.num_requests):
+            otag, ostamp = orc.caches[(r, l)].slots()
+            assert np.array_equal(tag[r], otag) and np.array_equal(stamp[r], ostamp), (r, l)
+            assert clock[r] == orc.caches[(r, l)].counters()["clock"], (r, l)
+    st = pool.stats()
+    for (r, l), cache in orc.caches.items():
+        cnt = cache.counters()
+        assert list(st["per_rl"][r, l, :3]) == [cnt["hits"], cnt["misses"], cnt["appends"]], (r, l)
     pool.close()
