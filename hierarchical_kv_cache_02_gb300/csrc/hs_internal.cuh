@@ -73,10 +73,10 @@ struct hs_pool {
   // early fetch (cfg.early_fetch = 1), else all null:
   int32_t* pos_slot;   // [L][R][C] slot each position was last installed in (a hint: a position is
                        // resident iff that slot is below the buffer's slot count and carries its tag)
-  uint32_t* fclaim;    // [L][R][k] claim word of each top-k entry in a launch: 0 free, 1 claimed by a
-                       // fetch CTA, (row + 1) << 2 | 2 landed in scratch row `row`, 3 claimed by a
-                       // deciding CTA; all 0 again when the launch ends
-  uint32_t* ffin;      // [L][R] CTAs of the launch finished (the last one clears the claim words)
+  int32_t* fslot;      // [L][R][k] slot + 1 of each missing top-k entry of a launch (0: none), written
+                       // by the deciding CTAs for the fetch CTAs; all 0 again when the launch ends
+  uint32_t* fdec;      // [L][R] deciding CTAs of the launch that have written their share
+  uint32_t* ffin;      // [L][R] CTAs of the launch finished (the last one clears fslot and fdec)
   uint8_t* fscratch;   // [L][R][cs x fetch_rows][rec] records fetched ahead of the decision
   int fetch_rows;      // scratch rows of one fetch CTA
 };

@@ -156,7 +156,8 @@ void free_pool(hs_pool* p) {
   cudaFree(p->pend);
   cudaFree(p->pend_live);
   cudaFree(p->pos_slot);
-  cudaFree(p->fclaim);
+  cudaFree(p->fslot);
+  cudaFree(p->fdec);
   cudaFree(p->ffin);
   cudaFree(p->fscratch);
   delete p;
@@ -198,8 +199,9 @@ int do_reset(hs_pool* p, cudaStream_t st) {
   if (cudaMemsetAsync(p->attn_ticket, 0, (size_t)p->cfg.num_requests * p->attn_tickets_per_req * sizeof(uint32_t), st) !=
       cudaSuccess)
     return HS_ERR_CUDA;
-  if (p->fclaim != nullptr &&
-      (cudaMemsetAsync(p->fclaim, 0, nrl * p->cfg.top_k * sizeof(uint32_t), st) != cudaSuccess ||
+  if (p->fslot != nullptr &&
+      (cudaMemsetAsync(p->fslot, 0, nrl * p->cfg.top_k * sizeof(int32_t), st) != cudaSuccess ||
+       cudaMemsetAsync(p->fdec, 0, nrl * sizeof(uint32_t), st) != cudaSuccess ||
        cudaMemsetAsync(p->ffin, 0, nrl * sizeof(uint32_t), st) != cudaSuccess))
     return HS_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? HS_OK : HS_ERR_CUDA;
@@ -469,14 +471,15 @@ extern "C" int hs_pool_create(const hs_config* cfg, int cuda_device, hs_pool** o
   if (rc == HS_OK) rc = hs_resolve_prepare(p);
   p->resolve_ctas = p->resolve_cs;
   if (rc == HS_OK && cfg->early_fetch) {
-    // the position -> slot map (every entry -1: no position installed yet), the claim words and
-    // finish counters (cleared by do_reset), and about top_k / 4 scratch records per (layer, request)
+    // the position -> slot map (every entry -1: no position installed yet), the miss slots and
+    // counters (cleared by do_reset), and about top_k / 4 scratch records per (layer, request)
     p->resolve_ctas = 2 * p->resolve_cs;
     p->fetch_rows = (cfg->top_k + 4 * p->resolve_cs - 1) / (4 * p->resolve_cs);
     rc = dev_alloc(&p->pos_slot, L * R * (size_t)cfg->capacity);
     if (rc == HS_OK && cudaMemset(p->pos_slot, 0xff, L * R * (size_t)cfg->capacity * sizeof(int32_t)) != cudaSuccess)
       rc = HS_ERR_CUDA;
-    if (rc == HS_OK) rc = dev_alloc(&p->fclaim, L * R * (size_t)cfg->top_k);
+    if (rc == HS_OK) rc = dev_alloc(&p->fslot, L * R * (size_t)cfg->top_k);
+    if (rc == HS_OK) rc = dev_alloc(&p->fdec, L * R);
     if (rc == HS_OK) rc = dev_alloc(&p->ffin, L * R);
     if (rc == HS_OK) rc = dev_alloc(&p->fscratch, L * R * (size_t)p->resolve_cs * p->fetch_rows * (size_t)p->rec);
   }

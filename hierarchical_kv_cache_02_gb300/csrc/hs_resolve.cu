@@ -66,14 +66,16 @@ struct ResolveArgs {
   int stall;                  // test hook (hs_debug_stall_next): leave the early copies' arrival out
   uint32_t* res_count;        // layer slice [R][2]: launches, CTAs finished (per request)
   int nreq;                   // requests of this launch: CTAs [0, nreq cs) decide, the rest fetch
-  // early fetch (null when off): layer slices of the position -> slot map [R][C], the claim words
-  // [R][k], the finish counters [R] and the scratch [R][cs x fetch_rows][rec]
+  // early fetch (null when off): layer slices of the position -> slot map [R][C], the slot of each
+  // missing top-k entry (+1; 0 none) [R][k], the deciding CTAs done [R], all CTAs finished [R] and
+  // the scratch [R][cs x fetch_rows][rec]
   int32_t* pos_slot;
-  uint32_t* fclaim;
+  int32_t* fslot;
+  uint32_t* fdec;
   uint32_t* ffin;
   uint8_t* fscratch;
   int fetch_rows;
-  int fstall;                 // test hook: one claimed record is never marked as landed
+  int fstall;                 // test hook: the fetch CTAs of the launch's first request do not wait
 };
 
 __device__ __forceinline__ uint32_t ht_hash(int32_t p, int bits) { return ((uint32_t)p * 0x9E3779B1u) >> (32 - bits); }
@@ -286,11 +288,11 @@ __device__ void select_threshold(const uint32_t* key32, const uint8_t* flag, int
 // A resolve CTA's last act: once every thread's writes (locs, metadata, fetched rows) are done, count
 // the CTA as finished for its request, with release ordering (an attention that waits for the count
 // then reads those writes).  With fetch CTAs, the last CTA of the request's launch to get here first
-// clears the request's claim words for the next launch: every other CTA counted itself after its
-// last use of them.
+// clears the request's miss slots and counters for the next launch: every other CTA counted itself
+// after its last use of them.
 __device__ __forceinline__ void count_finished(const ResolveArgs& a, int r) {
   __syncthreads();
-  if (a.fclaim != nullptr) {
+  if (a.fslot != nullptr) {
     __shared__ int s_last;
     if (threadIdx.x == 0) {
       __threadfence();
@@ -299,8 +301,11 @@ __device__ __forceinline__ void count_finished(const ResolveArgs& a, int r) {
     }
     __syncthreads();
     if (s_last) {
-      for (int i = threadIdx.x; i < a.k; i += kThreads) a.fclaim[(int64_t)r * a.k + i] = 0u;
-      if (threadIdx.x == 0) a.ffin[r] = 0u;
+      for (int i = threadIdx.x; i < a.k; i += kThreads) a.fslot[(int64_t)r * a.k + i] = 0;
+      if (threadIdx.x == 0) {
+        a.fdec[r] = 0u;
+        a.ffin[r] = 0u;
+      }
       __syncthreads();
     }
   }
@@ -324,36 +329,51 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 
-// A fetch CTA (early fetch): from the launch's start, copy the missing records of its share
-// [e0, e1) of the request's top-k list from the host history into its scratch rows, while the
-// deciding CTAs work out the victims.  An entry counts as missing unless the slot its position was
-// last installed in is below the buffer's slot count and still carries the position's tag (a hit
-// slot is never rewritten by this launch, so a hit is never taken for a miss; a miss taken for a hit,
-// or an entry the decision discards, only costs a fetch nobody uses).  Each record is claimed first
-// (claim word 0 -> 1) so that it crosses the host link once, and released as landed with its row.
-// The CTA takes at most fetch_rows records; the deciding CTAs fetch the rest themselves.
 #ifndef HS_FETCH_UNROLL
-#define HS_FETCH_UNROLL 4
+#define HS_FETCH_UNROLL 8
 #endif
 constexpr int kFetchUnroll = HS_FETCH_UNROLL;  // 16-byte loads a lane has in flight per record
 #ifndef HS_FETCH_WARPS
 #define HS_FETCH_WARPS 32
 #endif
-constexpr int kFetchWarps = HS_FETCH_WARPS;  // warps of a fetch CTA that copy records
+constexpr int kFetchWarps = HS_FETCH_WARPS;  // warps of a fetch CTA that copy records ahead of the decision
+
+// A fetch CTA (early fetch) does all of the miss fetch for its share [e0, e1) of the request's top-k
+// list, starting at the launch's start:
+//   (1) it lists the entries that look missing: those whose position's last slot (the position ->
+//       slot map) is not below the buffer's slot count or no longer carries the position's tag (a
+//       hint only: the decision is what counts);
+//   (2) until every deciding CTA has written its share, it copies those records from the host
+//       history into its scratch rows, at most fetch_rows of them;
+//   (3) it waits (bounded) for the deciding CTAs, reads the slot each actual miss of its share was
+//       given, and copies the record there: from its scratch row when it has it (HBM to HBM), else
+//       from the host.
+// A record it fetched that the decision did not count as a miss (a repeat, the position the fused
+// append has just installed) only costs the link transfer.  A wait that gives up flags the resolve
+// and installs nothing (the cache state then no longer matches the history).
 __device__ void early_fetch_cta(const ResolveArgs& a, int r, int crank) {
   extern __shared__ __align__(16) uint8_t smem[];
-  int32_t* lst = (int32_t*)smem;  // [e1 - e0]: the share's apparent misses (top-k indices)
-  __shared__ int s_n;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int k = a.k;
   const int cap = a.scap[r];
   if (min(a.B, cap) < k) return;  // too few slots: the deciding CTAs change nothing
-  const int e0 = (int)((int64_t)k * crank / a.cs), e1 = (int)((int64_t)k * (crank + 1) / a.cs);
+  const int e0 = (int)((int64_t)k * crank / a.cs), e1 = (int)((int64_t)k * (crank + 1) / a.cs), ne = e1 - e0;
+  int32_t* lst = (int32_t*)smem;  // [ne]: the share's apparent misses (top-k indices)
+  int32_t* srow = lst + ne;       // [ne]: scratch row holding entry e0 + x, or -1
+  int32_t* inst = srow + ne;      // [ne]: the share's actual misses (top-k indices)
+  int32_t* islot = inst + ne;     // [ne]: and their slots
+  __shared__ int s_n, s_m, s_go;
   const int32_t* topk = a.topk + (int64_t)(r - a.r0) * k;
   const int32_t* tag = a.tag + (int64_t)r * a.B;
   const int32_t* ps = a.pos_slot + (int64_t)r * a.C;
-  if (tid == 0) s_n = 0;
+  const uint32_t* dec = a.fdec + r;
+  if (tid == 0) {
+    s_n = 0;
+    s_m = 0;
+  }
+  for (int x = tid; x < ne; x += kThreads) srow[x] = -1;
   __syncthreads();
+  // (1)
   for (int ib = e0 + 32 * warp; ib < e1; ib += kThreads) {
     const int i = ib + lane;
     bool miss = false;
@@ -374,25 +394,17 @@ __device__ void early_fetch_cta(const ResolveArgs& a, int r, int crank) {
   HS_PHASE(hs_phase_res, 21, tid == 0);
   const int n = min(s_n, a.fetch_rows);
   const uint64_t* row = a.pt + ((int64_t)r * a.L + a.layer) * a.max_pages;
-  uint32_t* claim = a.fclaim + (int64_t)r * k;
   const int row0 = crank * a.fetch_rows;  // this CTA's first row in the request's scratch
   uint8_t* scratch = a.fscratch + (int64_t)r * a.cs * a.fetch_rows * a.rec;
   const int vpr = (int)(a.rec / 16);
-  bool held = a.fstall != 0 && r == a.r0 && crank == 0 && warp == 0;  // test hook: keep one claim
-  for (int x = warp; warp < kFetchWarps && x < n; x += kFetchWarps) {
-    const int i = lst[x];
-    const uint4* src = (const uint4*)hs_page_row_addr(row, a.page_shift, a.rec, topk[i]);
-    if (src == nullptr) continue;  // not reserved: the deciding CTA flags it
-    uint32_t won = 0u;
-    if (lane == 0) won = atomicCAS(&claim[i], 0u, 1u) == 0u ? 1u : 0u;
-    if (__shfl_sync(0xffffffffu, won, 0) == 0u) continue;
-    uint4* dst = (uint4*)(scratch + (int64_t)(row0 + x) * a.rec);
+  // one record -> dst by the calling warp, kFetchUnroll 16-byte loads per lane in flight
+  auto copy_rec = [&](uint4* dst, const uint4* src, bool from_host) {
     for (int v0 = 0; v0 < vpr; v0 += 32 * kFetchUnroll) {
       uint4 t[kFetchUnroll];
 #pragma unroll
       for (int u = 0; u < kFetchUnroll; ++u) {
         const int v = v0 + 32 * u + lane;
-        if (v < vpr) t[u] = ld_nc_v4(src + v);
+        if (v < vpr) t[u] = from_host ? ld_nc_v4(src + v) : __ldcg(src + v);
       }
 #pragma unroll
       for (int u = 0; u < kFetchUnroll; ++u) {
@@ -400,45 +412,58 @@ __device__ void early_fetch_cta(const ResolveArgs& a, int r, int crank) {
         if (v < vpr) dst[v] = t[u];
       }
     }
-    __threadfence();  // each lane's part of the row, before the release below
+  };
+  // (2)
+  for (int x = warp; warp < kFetchWarps && x < n; x += kFetchWarps) {
+    uint32_t decided = 0u;
+    if (lane == 0) decided = ld_acquire_gpu(dec) >= (uint32_t)a.cs ? 1u : 0u;
+    if (__shfl_sync(0xffffffffu, decided, 0) != 0u) break;
+    const int i = lst[x];
+    const uint4* src = (const uint4*)hs_page_row_addr(row, a.page_shift, a.rec, topk[i]);
+    if (src == nullptr) continue;  // not reserved: the deciding CTA flags it
+    copy_rec((uint4*)(scratch + (int64_t)(row0 + x) * a.rec), src, true);
     __syncwarp();
-    if (held) {
-      held = false;
-      continue;
-    }
-    if (lane == 0) st_release_gpu(&claim[i], ((uint32_t)(row0 + x + 1) << 2) | 2u);
+    if (lane == 0) srow[i - e0] = row0 + x;
   }
-}
-
-// Phase B of a deciding CTA (early fetch): its misses that the fetch CTAs claimed, s_fq[0, nfq),
-// one warp per record: wait (bounded) until the record has landed, then move it from its scratch row
-// to its slot.  A wait that gives up flags the resolve and fetches the record from the host instead
-// (the same bytes).
-__device__ __forceinline__ void take_landed(const ResolveArgs& a, int r, const uint32_t* claim, const int32_t* s_fq,
-                                              int nfq, const int32_t* miss_idx, const int32_t* miss_pos,
-                                              const int32_t* victims, const uint64_t* s_slots, const uint64_t* row) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, vpr = (int)(a.rec / 16);
-  const uint8_t* scratch = a.fscratch + (int64_t)r * a.cs * a.fetch_rows * a.rec;
-  for (int x = warp; x < nfq; x += kWarps) {
-    const int q = s_fq[x];
-    const uint32_t* cw = &claim[miss_idx[q]];
-    uint32_t w = ld_acquire_gpu(cw);
-    if ((w & 3u) != 2u) {
+  // (3)
+  if (tid == 0) {
+    bool ok = ld_acquire_gpu(dec) >= (uint32_t)a.cs;
+    if (!ok) {
       const uint64_t t0 = global_ns();
       do {
-        __nanosleep(200);
-        w = ld_acquire_gpu(cw);
-      } while ((w & 3u) != 2u && global_ns() - t0 < 1000000000ull);
+        __nanosleep(256);
+        ok = ld_acquire_gpu(dec) >= (uint32_t)a.cs;
+      } while (!ok && global_ns() - t0 < 1000000000ull);
     }
-    uint4* dst = (uint4*)hs_slot_addr(s_slots, a.sshift, a.rec, victims[q]);
-    if ((w & 3u) == 2u) {
-      const uint4* src = (const uint4*)(scratch + (int64_t)((w >> 2) - 1u) * a.rec);
-      for (int v = lane; v < vpr; v += 32) dst[v] = __ldcg(src + v);
-    } else {
-      atomicOr(a.err_global, (uint32_t)HS_DEVERR_TIMEOUT);
-      const uint4* src = (const uint4*)hs_page_row_addr(row, a.page_shift, a.rec, miss_pos[q]);
-      for (int v = lane; v < vpr; v += 32) dst[v] = ld_nc_v4(src + v);
+    if (!ok) atomicOr(a.err_global, (uint32_t)HS_DEVERR_TIMEOUT);
+    s_go = ok ? 1 : 0;
+  }
+  __syncthreads();
+  HS_PHASE(hs_phase_res, 23, tid == 0);
+  if (s_go == 0) return;
+  const int32_t* fs = a.fslot + (int64_t)r * k;
+  for (int ib = e0 + 32 * warp; ib < e1; ib += kThreads) {
+    const int i = ib + lane;
+    const int32_t v = i < e1 ? __ldcg(fs + i) : 0;
+    const uint32_t bm = __ballot_sync(0xffffffffu, v != 0);
+    int base = 0;
+    if (lane == 0 && bm != 0u) base = atomicAdd(&s_m, __popc(bm));
+    base = __shfl_sync(0xffffffffu, base, 0);
+    if (v != 0) {
+      const int x = base + __popc(bm & ((1u << lane) - 1u));
+      inst[x] = i;
+      islot[x] = v - 1;
     }
+  }
+  __syncthreads();
+  const uint64_t* slots = a.spt + (int64_t)r * a.spp;
+  for (int x = warp; x < s_m; x += kWarps) {
+    const int i = inst[x];
+    const int sr = srow[i - e0];
+    const uint4* src = sr >= 0 ? (const uint4*)(scratch + (int64_t)sr * a.rec)
+                               : (const uint4*)hs_page_row_addr(row, a.page_shift, a.rec, topk[i]);
+    if (src == nullptr) continue;  // not reserved (flagged by the deciding CTA)
+    copy_rec((uint4*)hs_slot_addr(slots, a.sshift, a.rec, islot[x]), src, sr < 0);
   }
 }
 
@@ -560,14 +585,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
   int app_slot = -1;
   uint4* app_dh = nullptr;  // the append's place in the host history (known after the hash)
   __shared__ uint32_t s_dups, s_klo, s_khi;
-  __shared__ int s_nfq;  // phase B: misses taken from the fetch CTAs' scratch
   __shared__ unsigned long long s_app_page;
   if (tid == 0) {
     err_bits = 0u;
     mbar_init1(&bar_stage);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     s_dups = 0u;
-    s_nfq = 0;
     s_klo = 0xffffffffu;
     s_khi = 0u;
   }
@@ -922,8 +945,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
       }
     }
     HS_PHASE(hs_phase_res, 8, tid == 0);
-    // (4) fetch this CTA's share of the misses from the host history (or leave it to the attention)
-    if (a.pend == nullptr && q1 > q0) {
+    // (4) fetch this CTA's share of the misses from the host history (or leave it to the attention,
+    // or to the fetch CTAs: they are told each miss's slot, once every deciding CTA has written its
+    // share)
+    if (a.fslot != nullptr) {
+      for (int q = q0 + tid; q < q1; q += kThreads) {
+        if (hs_page_row_addr(pt_row(), a.page_shift, a.rec, miss_pos[q]) == nullptr)
+          atomicOr(a.err_global, (uint32_t)HS_DEVERR_PAGE);
+        a.fslot[(int64_t)r * k + miss_idx[q]] = victims[q] + 1;
+      }
+      __syncthreads();
+      if (tid == 0 && !(a.fstall != 0 && r == a.r0)) {
+        __threadfence();
+        atomicAdd(&a.fdec[r], 1u);
+      }
+    } else if (a.pend == nullptr && q1 > q0) {
       // host addresses of this CTA's misses, resolved once (in the hash table's space: dead by now)
       uint64_t* s_src = (uint64_t*)ht_key;
       const uint64_t* row = pt_row();
@@ -932,25 +968,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
         if (src == nullptr) atomicOr(a.err_global, (uint32_t)HS_DEVERR_PAGE);
         s_src[q - q0] = (uint64_t)(uintptr_t)src;
       }
-      // early fetch: a miss the fetch CTAs have claimed (landed or in flight) comes from their
-      // scratch below; the others are claimed here and fetched from the host
-      uint32_t* claim = a.fclaim != nullptr ? a.fclaim + (int64_t)r * k : nullptr;
-      int32_t* s_fq = ht_val;  // [q1 - q0]: those misses (the hash table's values: dead by now)
-      if (claim != nullptr) {
-        for (int q = q0 + tid; q < q1; q += kThreads) {
-          if (s_src[q - q0] == 0ull) continue;  // not reserved (flagged): nothing to fetch
-          if (atomicCAS(&claim[miss_idx[q]], 0u, 3u) != 0u) {
-            s_src[q - q0] = 0ull;
-            s_fq[atomicAdd(&s_nfq, 1)] = q;
-          }
-        }
-      }
       // the rest straight from the host, then the staged ones from shared memory
       __syncthreads();
-      HS_PHASE(hs_phase_res, 23, tid == 0);
       fetch_misses<NV>(a, q0 + nstage, q1, s_src + nstage, victims, s_slots);
-      HS_PHASE(hs_phase_res, 24, tid == 0);
-      if (claim != nullptr) take_landed(a, r, claim, s_fq, s_nfq, miss_idx, miss_pos, victims, s_slots, pt_row());
       if (nstage > 0) {
         // the staged records have landed (bounded: a wait that gives up flags the resolve and skips
         // the staged records, after a second bounded wait for copies still in flight)
@@ -1137,7 +1157,7 @@ size_t resolve_launch_smem(const hs_config* c, int* stage_off, int* stage_recs) 
 template <int NV>
 cudaError_t launch_resolve_nv(const ResolveArgs* a, int nreq, int cs, size_t smem, cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(nreq * cs * (a->fclaim != nullptr ? 2 : 1)), 1, 1);
+  cfg.gridDim = dim3((unsigned)(nreq * cs * (a->fslot != nullptr ? 2 : 1)), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
@@ -1234,9 +1254,10 @@ int hs_launch_resolve(hs_pool* p, int layer, int r0, int nreq, const int64_t* d_
   a.r0 = r0;
   a.nreq = nreq;
   a.res_count = p->res_count + (int64_t)layer * R * 2;
-  if (p->fclaim != nullptr) {
+  if (p->fslot != nullptr) {
     a.pos_slot = p->pos_slot + (int64_t)layer * R * c.capacity;
-    a.fclaim = p->fclaim + (int64_t)layer * R * c.top_k;
+    a.fslot = p->fslot + (int64_t)layer * R * c.top_k;
+    a.fdec = p->fdec + (int64_t)layer * R;
     a.ffin = p->ffin + (int64_t)layer * R;
     a.fscratch = p->fscratch + (int64_t)layer * R * a.cs * p->fetch_rows * p->rec;
     a.fetch_rows = p->fetch_rows;

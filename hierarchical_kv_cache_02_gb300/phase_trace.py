@@ -33,7 +33,7 @@ RESOLVE.update({10: "  thread 0: hash inserts done", 11: "  thread 0: append sea
                 16: "  select pass 1: histogram", 17: "  select pass 1: bin found",
                 18: "  compaction: counts scanned", 19: "  thread 0: victims placed",
                 20: "  compaction: barrier passed", 21: "fetch CTAs: misses found", 22: "fetch CTAs: done",
-                23: "phase B: misses claimed", 24: "phase B: own misses fetched"})
+                23: "fetch CTAs: victims known"})
 ATTN = {0: "start", 1: "setup", 38: "scores of tile 0 issued", 39: "scores of tile 1 issued",
         40: "value product of tile 0 issued", 41: "value product of tile 1 issued",
         43: "softmax: scores of tile 0 seen", 44: "softmax: scores of tile 1 seen",

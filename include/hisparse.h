@@ -134,17 +134,17 @@ typedef struct {
   int32_t early_fetch;        /* summary §5 step 4 (the swap-in), started before the decision ends.
                                  0: each hs_resolve cluster fetches its misses once it has chosen
                                  the victims.  1: every hs_resolve launch also runs one cluster of
-                                 fetch CTAs per request.  They tell the misses apart from the
-                                 slot each resident position was installed in (a device map
-                                 position -> slot, confirmed by the slot's tag).  From the
-                                 launch's start they copy up to about top_k / 4 missing records
-                                 per (request, layer) from the host history into a device scratch.
-                                 The deciding CTAs then move those records from there into their
-                                 victim slots and fetch the rest themselves.  A per-entry claim
-                                 word makes each record cross the host link once.  Results are
-                                 identical to mode 0.  Extra device memory per (layer, request):
-                                 4 x capacity bytes for the map, plus the scratch and claim words
-                                 (about top_k / 4 records).  Needs fetch_in_attention = 0. */
+                                 fetch CTAs per request, which do the whole miss fetch.  From the
+                                 launch's start they copy the records that look missing (from the
+                                 slot each position was last installed in: a device map position
+                                 -> slot, confirmed by the slot's tag) from the host history into
+                                 a device scratch, up to about top_k / 4 per (request, layer).
+                                 Once the deciding CTAs have chosen the victims, the fetch CTAs
+                                 install every miss in its slot: from the scratch when they have
+                                 it, else from the host.  Results are identical to mode 0.  Extra
+                                 device memory per (layer, request): 4 x capacity bytes for the
+                                 map, the scratch (about top_k / 4 records) and 4 x top_k bytes.
+                                 Needs fetch_in_attention = 0. */
 } hs_config;
 
 /* Record size in bytes for a configuration (MLA: 2*head_dim_qk; GQA: 2*kv_heads*(qk+v)). */
@@ -355,10 +355,9 @@ int hs_release(hs_pool* pool, int req);
  *                      the first ring slot), consumed by the next launch of that kernel
  *   HS_STALL_RESOLVE : the resolve (the arrival that completes the early miss copies), consumed by
  *                      the next resolve launch that stages early copies
- *   HS_STALL_FETCH   : the resolve's fetch CTAs (early_fetch = 1): the first record one of them
- *                      claims is never marked as landed, so the deciding CTA that needs it gives
- *                      up waiting, reports HS_DEVERR_TIMEOUT and fetches that record from the host
- *                      itself (here the outputs and the cache state stay exact).  Consumed by the
+ *   HS_STALL_FETCH   : the resolve's fetch CTAs (early_fetch = 1): the deciding CTAs of the
+ *                      launch's first request never signal that the victims are chosen, so that
+ *                      request's fetch CTAs give up waiting and install nothing.  Consumed by the
  *                      next resolve launch with fetch CTAs.
  * Host-side only (takes effect at launch, also when the launch is captured).  Errors: HS_ERR_ARG.
  */
