@@ -1691,7 +1691,7 @@ bool plan_for(const hs_config* c, int num_sms, Plan* pl) {
 template <typename K>
 cudaError_t launch_kernel(K kern, const AttnArgs* a, const Plan& pl, int threads, cudaStream_t st) {
   if (a == nullptr) {  // preparation, once: the dynamic shared-memory limit and the largest carveout
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+    cudaError_t e = hs_raise_smem_limit(kern, (int)pl.smem);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
     return e;
@@ -1748,7 +1748,7 @@ cudaError_t dispatch(const hs_config& c, const AttnArgs* a, const Plan& pl, cuda
   if (pl.kind == 4) {
     cudaError_t e = cudaSuccess;
     if (a == nullptr) {  // preparation: shared-memory limit and carveout
-      e = cudaFuncSetAttribute(k_attn_mla_pipe, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+      e = hs_raise_smem_limit(k_attn_mla_pipe, (int)pl.smem);
       if (e == cudaSuccess)
         e = cudaFuncSetAttribute(k_attn_mla_pipe, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  (int)cudaSharedmemCarveoutMaxShared);

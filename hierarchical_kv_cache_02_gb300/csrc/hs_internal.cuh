@@ -163,6 +163,18 @@ __device__ __forceinline__ void hs_pdl_enter() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Raise a kernel's dynamic shared-memory limit to `bytes`, never lower it: pools of different
+// configurations in one process share the kernel's attribute, and a later pool that needs less must
+// not break the launches of an earlier one that needs more.
+template <typename K>
+inline cudaError_t hs_raise_smem_limit(K kern, int bytes) {
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, (const void*)kern);
+  if (e != cudaSuccess) return e;
+  if (fa.maxDynamicSharedSizeBytes >= bytes) return cudaSuccess;
+  return cudaFuncSetAttribute((const void*)kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
 // ---- phase stamps (built only with -DHS_PHASE_TRACE, for the phase tables of the profiles) ----
 // Thread 0 of each of the first 256 CTAs of a launch records %globaltimer at numbered points of a
 // kernel into `table` ([256][64], a device array of the kernel's translation unit, read out by its

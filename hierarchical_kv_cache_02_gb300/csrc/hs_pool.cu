@@ -473,15 +473,18 @@ extern "C" int hs_pool_create(const hs_config* cfg, int cuda_device, hs_pool** o
   if (rc == HS_OK && cfg->early_fetch) {
     // the position -> slot map (every entry -1: no position installed yet), the miss slots and
     // counters (cleared by do_reset), and about top_k / 4 scratch records per (layer, request)
-    p->resolve_ctas = 2 * p->resolve_cs;
-    p->fetch_rows = (cfg->top_k + 4 * p->resolve_cs - 1) / (4 * p->resolve_cs);
+    // fetch CTAs per request: as many as deciding CTAs (one per request measured far slower: a
+    // single SM cannot keep enough of a request's records in flight)
+    const int fpr = p->resolve_cs;
+    p->resolve_ctas = p->resolve_cs + fpr;
+    p->fetch_rows = (cfg->top_k + 4 * fpr - 1) / (4 * fpr);
     rc = dev_alloc(&p->pos_slot, L * R * (size_t)cfg->capacity);
     if (rc == HS_OK && cudaMemset(p->pos_slot, 0xff, L * R * (size_t)cfg->capacity * sizeof(int32_t)) != cudaSuccess)
       rc = HS_ERR_CUDA;
     if (rc == HS_OK) rc = dev_alloc(&p->fslot, L * R * (size_t)cfg->top_k);
     if (rc == HS_OK) rc = dev_alloc(&p->fdec, L * R);
     if (rc == HS_OK) rc = dev_alloc(&p->ffin, L * R);
-    if (rc == HS_OK) rc = dev_alloc(&p->fscratch, L * R * (size_t)p->resolve_cs * p->fetch_rows * (size_t)p->rec);
+    if (rc == HS_OK) rc = dev_alloc(&p->fscratch, L * R * (size_t)fpr * p->fetch_rows * (size_t)p->rec);
   }
   if (rc == HS_OK) rc = hs_attn_prepare(cfg, p->num_sms);
   if (rc == HS_OK) rc = do_reset(p, 0);

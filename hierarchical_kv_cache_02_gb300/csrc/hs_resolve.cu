@@ -74,7 +74,8 @@ struct ResolveArgs {
   uint32_t* fdec;
   uint32_t* ffin;
   uint8_t* fscratch;
-  int fetch_rows;
+  int fetch_rows;             // scratch rows of one fetch CTA
+  int fpr;                    // fetch CTAs per request
   int fstall;                 // test hook: the fetch CTAs of the launch's first request do not wait
 };
 
@@ -296,7 +297,7 @@ __device__ __forceinline__ void count_finished(const ResolveArgs& a, int r) {
     __shared__ int s_last;
     if (threadIdx.x == 0) {
       __threadfence();
-      s_last = atomicAdd(&a.ffin[r], 1u) == (uint32_t)(2 * a.cs - 1);
+      s_last = atomicAdd(&a.ffin[r], 1u) == (uint32_t)(a.cs + a.fpr - 1);
       __threadfence();
     }
     __syncthreads();
@@ -357,7 +358,7 @@ __device__ void early_fetch_cta(const ResolveArgs& a, int r, int crank) {
   const int k = a.k;
   const int cap = a.scap[r];
   if (min(a.B, cap) < k) return;  // too few slots: the deciding CTAs change nothing
-  const int e0 = (int)((int64_t)k * crank / a.cs), e1 = (int)((int64_t)k * (crank + 1) / a.cs), ne = e1 - e0;
+  const int e0 = (int)((int64_t)k * crank / a.fpr), e1 = (int)((int64_t)k * (crank + 1) / a.fpr), ne = e1 - e0;
   int32_t* lst = (int32_t*)smem;  // [ne]: the share's apparent misses (top-k indices)
   int32_t* srow = lst + ne;       // [ne]: scratch row holding entry e0 + x, or -1
   int32_t* inst = srow + ne;      // [ne]: the share's actual misses (top-k indices)
@@ -395,7 +396,7 @@ __device__ void early_fetch_cta(const ResolveArgs& a, int r, int crank) {
   const int n = min(s_n, a.fetch_rows);
   const uint64_t* row = a.pt + ((int64_t)r * a.L + a.layer) * a.max_pages;
   const int row0 = crank * a.fetch_rows;  // this CTA's first row in the request's scratch
-  uint8_t* scratch = a.fscratch + (int64_t)r * a.cs * a.fetch_rows * a.rec;
+  uint8_t* scratch = a.fscratch + (int64_t)r * a.fpr * a.fetch_rows * a.rec;
   const int vpr = (int)(a.rec / 16);
   // one record -> dst by the calling warp, kFetchUnroll 16-byte loads per lane in flight
   auto copy_rec = [&](uint4* dst, const uint4* src, bool from_host) {
@@ -473,8 +474,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
   // are the requests' fetch CTAs, in clusters of the same size that never use the cluster barrier
   const bool fetcher = (int)blockIdx.x >= a.nreq * a.cs;
   const int b = fetcher ? (int)blockIdx.x - a.nreq * a.cs : (int)blockIdx.x;
-  const int r = a.r0 + b / a.cs;
-  const int crank = b % a.cs;  // rank inside the cluster of this request
+  if (fetcher && b >= a.nreq * a.fpr) return;  // a cluster's padding: no request, nothing counted
+  const int r = a.r0 + (fetcher ? b / a.fpr : b / a.cs);
+  const int crank = fetcher ? b % a.fpr : b % a.cs;  // rank among the request's deciding (fetch) CTAs
   asm volatile("griddepcontrol.wait;" ::: "memory");
   // the launch is counted for its requests before the next kernel may start
   if (!fetcher && crank == 0 && threadIdx.x == 0) {
@@ -1157,7 +1159,9 @@ size_t resolve_launch_smem(const hs_config* c, int* stage_off, int* stage_recs) 
 template <int NV>
 cudaError_t launch_resolve_nv(const ResolveArgs* a, int nreq, int cs, size_t smem, cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(nreq * cs * (a->fslot != nullptr ? 2 : 1)), 1, 1);
+  // the fetch CTAs follow the deciding ones, rounded up to whole clusters
+  const int nf = a->fslot != nullptr ? (nreq * a->fpr + cs - 1) / cs * cs : 0;
+  cfg.gridDim = dim3((unsigned)(nreq * cs + nf), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
@@ -1177,8 +1181,7 @@ template <int NV>
 int prepare_nv(const hs_config* c, int num_sms, int* cs_out) {
   int stage_off, stage_recs;
   const int smem = (int)resolve_launch_smem(c, &stage_off, &stage_recs);
-  if (cudaFuncSetAttribute(k_resolve<NV>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-    return HS_ERR_CUDA;
+  if (hs_raise_smem_limit(k_resolve<NV>, smem) != cudaSuccess) return HS_ERR_CUDA;
   // the same (largest) shared-memory carveout as the attention kernels, so the SMs keep their
   // L1/shared split from one kernel of a decode step to the next
   if (cudaFuncSetAttribute(k_resolve<NV>, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -1259,7 +1262,8 @@ int hs_launch_resolve(hs_pool* p, int layer, int r0, int nreq, const int64_t* d_
     a.fslot = p->fslot + (int64_t)layer * R * c.top_k;
     a.fdec = p->fdec + (int64_t)layer * R;
     a.ffin = p->ffin + (int64_t)layer * R;
-    a.fscratch = p->fscratch + (int64_t)layer * R * a.cs * p->fetch_rows * p->rec;
+    a.fpr = p->resolve_ctas - p->resolve_cs;
+    a.fscratch = p->fscratch + (int64_t)layer * R * a.fpr * p->fetch_rows * p->rec;
     a.fetch_rows = p->fetch_rows;
     if ((p->debug_stall & HS_STALL_FETCH) != 0) {  // test hook
       a.fstall = 1;

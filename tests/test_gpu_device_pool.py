@@ -28,11 +28,13 @@ def _cfg(shape="gqa", fetch=0, pool_slots=0, B=512, k=64, C=340, R=3, L=2, polic
     lay, Hq, Hkv, Dqk, Dv = SHAPES[shape]
     return HsConfig(num_requests=R, num_layers=L, capacity=C, layout=lay, num_q_heads=Hq, num_kv_heads=Hkv,
                     head_dim_qk=Dqk, head_dim_v=Dv, top_k=k, buffer_slots=B, policy=policy, seed=11,
-                    shared_prefix=P0, fetch_in_attention=fetch, device_pool_slots=pool_slots, buffer_page_slots=16,
+                    shared_prefix=P0, fetch_in_attention=int(fetch == 1), early_fetch=int(fetch == 2),
+                    device_pool_slots=pool_slots, buffer_page_slots=16,
                     host_on_demand=host_on_demand, host_page_tokens=host_page, host_to_device_ratio=ratio)
 
 
-@pytest.mark.parametrize("shape,fetch,P0", [("gqa", 0, 0), ("gqa", 1, 256), ("mla64", 0, 0), ("mla8", 0, 256)])
+@pytest.mark.parametrize("shape,fetch,P0", [("gqa", 0, 0), ("gqa", 1, 256), ("gqa", 2, 0), ("mla64", 0, 0),
+                                            ("mla64", 2, 256), ("mla8", 0, 256)])
 def test_buffers_grown_ahead_of_the_context_match_full_buffers(shape, fetch, P0):
     """Each step the coordinator grows every buffer to cover the token it appends: caps 304 -> 336
     of B = 512, so the buffers never hold all B slots, yet everything equals the full pool's."""
@@ -67,11 +69,13 @@ def test_buffers_grown_ahead_of_the_context_match_full_buffers(shape, fetch, P0)
     grown.close()
 
 
+@pytest.mark.parametrize("fetch", [0, 2])
 @pytest.mark.parametrize("policy", [0, 2, 3])
-def test_buffer_held_below_its_context_evicts_like_the_capped_oracle(policy):
+def test_buffer_held_below_its_context_evicts_like_the_capped_oracle(policy, fetch):
     """Buffers reserved to 100 positions hold 112 slots while the traces range over 300+: the
-    kernels evict among those slots exactly as the oracle's capped buffer does."""
-    cfg = _cfg("gqa", pool_slots=3 * 2 * 512, policy=policy)
+    kernels evict among those slots exactly as the oracle's capped buffer does (fetch = 2: with the
+    resolve's fetch CTAs, whose residency hint must ignore slots past the buffer's count)."""
+    cfg = _cfg("gqa", fetch=fetch, pool_slots=3 * 2 * 512, policy=policy)
     sc = Scenario(cfg, ctx0=300, steps=16, appends=True, recency_mean=96.0, seed=43)
     pool = HsPool(cfg)
     prefill(pool, sc)
@@ -96,10 +100,11 @@ def test_buffer_held_below_its_context_evicts_like_the_capped_oracle(policy):
     pool.close()
 
 
-def test_fewer_than_k_slots_refuse_the_step():
+@pytest.mark.parametrize("fetch", [0, 2])
+def test_fewer_than_k_slots_refuse_the_step(fetch):
     """Request 1 never gets device pages: its resolves change nothing and flag HS_DEVERR_SLOTS; the
     other requests' results are those of a full pool."""
-    full_cfg, cfg = _cfg("gqa"), _cfg("gqa", pool_slots=3 * 2 * 512)
+    full_cfg, cfg = _cfg("gqa"), _cfg("gqa", fetch=fetch, pool_slots=3 * 2 * 512)
     sc = Scenario(full_cfg, ctx0=300, steps=3, appends=True, seed=45)
     full, pool = HsPool(full_cfg), HsPool(cfg)
     prefill(full, sc)

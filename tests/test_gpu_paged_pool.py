@@ -15,10 +15,11 @@ from hierarchical_kv_cache_02_gb300 import DEVERR_APPEND, DEVERR_PAGE, LAYOUT_GQ
 def _cfg(on_demand, page=0, fetch=0, P0=0, C=3000 + 8):
     return HsConfig(num_requests=3, num_layers=2, capacity=C, layout=LAYOUT_GQA, num_q_heads=32, num_kv_heads=8,
                     head_dim_qk=128, head_dim_v=128, top_k=200, buffer_slots=400, seed=5, shared_prefix=P0,
-                    fetch_in_attention=fetch, host_page_tokens=page, host_on_demand=on_demand)
+                    fetch_in_attention=int(fetch == 1), early_fetch=int(fetch == 2), host_page_tokens=page,
+                    host_on_demand=on_demand)
 
 
-@pytest.mark.parametrize("fetch", [0, 1])
+@pytest.mark.parametrize("fetch", [0, 1, 2])
 @pytest.mark.parametrize("P0", [0, 2048])
 def test_on_demand_pages_match_full_reservation(fetch, P0):
     """Small pages reserved on demand (prefill, then hs_reserve ahead of the appends) against the
@@ -72,8 +73,9 @@ def test_append_on_unreserved_page_is_flagged_and_skipped():
     pool.close()
 
 
-def test_miss_on_unreserved_page_is_flagged():
-    cfg = _cfg(1, page=64)
+@pytest.mark.parametrize("fetch", [0, 2])
+def test_miss_on_unreserved_page_is_flagged(fetch):
+    cfg = _cfg(1, page=64, fetch=fetch)
     pool = HsPool(cfg)
     R, k = cfg.num_requests, cfg.top_k
     recs = bf16_tensor(np.zeros((1000, cfg.record_elems), dtype=np.uint16), "cuda")

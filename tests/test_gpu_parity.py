@@ -569,3 +569,26 @@ def test_fault_injection_allocations(monkeypatch):
         assert e.value.status == code
     monkeypatch.delenv("HS_FAULT")
     HsPool(cfg).close()
+
+
+def test_pools_of_different_configurations_share_the_kernels():
+    """A kernel's dynamic shared-memory limit is one attribute per process, not per pool: pools of
+    different configurations (staging area or not, fetch CTAs, 64-head selections of different
+    lengths) created one after another all keep launching, and each matches the oracle."""
+    cfgs = [_gqa(2, 1, 2000 + 4, 256, 512), _gqa(2, 1, 2000 + 4, 256, 512, fetch=2),
+            _gqa(2, 1, 2000 + 4, 256, 512, fetch=1), _mla(2, 1, 2000 + 4, 512, 1024, Hq=64),
+            _mla(2, 1, 2000 + 4, 128, 256, Hq=64, early=1)]
+    scs = [Scenario(c, ctx0=2000, steps=4, appends=True, seed=71 + i) for i, c in enumerate(cfgs)]
+    pools = [HsPool(c) for c in cfgs]
+    for pool, sc in zip(pools, scs):
+        prefill(pool, sc)
+    orcs = [OracleRun(sc) for sc in scs]
+    for t in range(4):
+        for pool, sc, orc in zip(pools, scs, orcs):
+            res = gpu_step(pool, sc, t, fused=True)
+            ref = orc.step(t)
+            for l in range(sc.cfg.num_layers):
+                assert_layer_matches_oracle(sc, orc, ref, t, l, res[l][0], res[l][1], "pools side by side")
+    for pool, orc in zip(pools, orcs):
+        assert_pool_matches_oracle(pool, orc, "pools side by side")
+        pool.close()
