@@ -208,7 +208,9 @@ int hs_append_writethrough(hs_pool* pool, int layer, const int64_t* d_pos, const
  * recency stamps in place (hits to MRU in top-k order, misses after the hits), fetch each
  * missing record from the pinned host history with 16-byte loads straight into its slot,
  * and write d_locs[r][i] = slot of d_topk[r][i] (-1 for padding or invalid entries; int32
- * [R][k], device).  Updates hits/misses/host-byte counters.  CAPTURABLE.
+ * [R][k], device).  Updates hits/misses/host-byte counters.  With early_fetch = 1 a second cluster
+ * per request does the whole miss fetch, starting at the launch's start (see hs_config).
+ * CAPTURABLE.
  */
 int hs_resolve(hs_pool* pool, int layer, const int32_t* d_topk, int32_t* d_locs, void* stream);
 
