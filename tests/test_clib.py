@@ -55,6 +55,8 @@ def test_record_bytes(lib):
     dict(policy=7),
     dict(shared_prefix=11),                       # beyond capacity
     dict(num_requests=0),
+    dict(early_fetch=2),                          # not 0 or 1
+    dict(early_fetch=1, fetch_in_attention=1),    # the fetch CTAs and the attention's fetch exclude each other
 ])
 def test_bad_config_rejected_on_host(lib, change):
     base = dict(num_requests=2, num_layers=1, capacity=10, top_k=8, buffer_slots=16)
