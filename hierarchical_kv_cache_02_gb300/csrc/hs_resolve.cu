@@ -213,9 +213,9 @@ __device__ void fetch_misses(const ResolveArgs& a, int q0, int q1, const uint64_
 // candidates with key == T (lowest slots first) complete the set.  Passes alternate between two
 // histograms and two selection words, both zero on entry: each thread clears the bins it has read,
 // so a histogram is zero again two passes later and a pass needs no barrier to clear one.
-__device__ void select_threshold(const uint32_t* key32, const uint8_t* flag, int B, uint32_t m, uint32_t lo,
-                                 uint32_t hi, uint32_t* wbuf, uint32_t (*hist)[2048], uint32_t (*sel)[2],
-                                 uint32_t* T_out, uint32_t* need_out) {
+__device__ __noinline__ void select_threshold(const uint32_t* key32, const uint8_t* flag, int B, uint32_t m, uint32_t lo,
+                                             uint32_t hi, uint32_t* wbuf, uint32_t (*hist)[2048], uint32_t (*sel)[2],
+                                             uint32_t* T_out, uint32_t* need_out) {
   // lo, hi: the smallest and largest candidate key (found by the probe)
   const int tid = threadIdx.x, lane = tid & 31;
   const uint32_t range = hi - lo;
@@ -284,6 +284,101 @@ __device__ void select_threshold(const uint32_t* key32, const uint8_t* flag, int
   }
   *T_out = lo + (uint32_t)prefix;
   *need_out = need;
+}
+
+// The same threshold in one pass when the candidates' nonzero keys are all distinct: the recency
+// stamps of LRU, FIFO and swap-vanilla (every stamp a resolve or append hands out is new; 0 marks an
+// empty slot).  Each nonzero key sets bit (key - lo) of a bitmap over [lo, lo + kDenseSpan) (the
+// radix select's histograms, zero on entry); the zero keys are counted.  Then T is the
+// (m - zeros)-th set bit (need_eq = 1), found by a block scan of the words' bit counts, or T = 0 with
+// need_eq = m when the empty slots alone suffice.  Returns false, with the bitmap cleared again, when
+// a nonzero key lies outside the window: the radix select then runs.
+constexpr uint32_t kDenseSpan = 2u * 2048u * 32u;  // bits in the two histograms
+__device__ __noinline__ bool select_dense(const uint32_t* key32, const uint8_t* flag, int B, uint32_t m, uint32_t lo,
+                                          uint32_t* wbuf, uint32_t (*hist)[2048], uint32_t (*sel)[2], uint32_t* s_cnt,
+                                          uint32_t* T_out, uint32_t* need_out) {
+  // s_cnt[0]: zero keys, s_cnt[1]: keys outside the window (both 0 on entry)
+  const int tid = threadIdx.x, lane = tid & 31;
+  uint32_t* bmw = &hist[0][0];
+  constexpr int U = 4;  // slots a thread loads before it sets any bit
+  for (int base = tid & ~31; base < B; base += U * kThreads) {
+    uint32_t key[U];
+    bool cand[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int j = base + u * kThreads + lane;
+      cand[u] = j < B && !(flag[j] & 1u);
+      key[u] = cand[u] ? key32[j] : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const uint32_t d = key[u] - lo;
+      const bool zero = cand[u] && key[u] == 0u, out = cand[u] && key[u] != 0u && (key[u] < lo || d >= kDenseSpan);
+      if (cand[u] && key[u] != 0u && !out) atomicOr(&bmw[d >> 5], 1u << (d & 31u));
+      const uint32_t zb = __ballot_sync(0xffffffffu, zero), ob = __ballot_sync(0xffffffffu, out);
+      if (lane == 0 && (zb | ob) != 0u) {
+        if (zb) atomicAdd(&s_cnt[0], (uint32_t)__popc(zb));
+        if (ob) atomicAdd(&s_cnt[1], (uint32_t)__popc(ob));
+      }
+    }
+  }
+  __syncthreads();
+  HS_PHASE(hs_phase_res, 14, threadIdx.x == 0);
+  if (s_cnt[1] != 0u) {
+    for (int x = tid; x < 2 * 2048; x += kThreads) bmw[x] = 0u;
+    __syncthreads();
+    return false;
+  }
+  const uint32_t z = s_cnt[0];
+  if (m <= z) {
+    *T_out = 0u;
+    *need_out = m;
+    return true;
+  }
+  const uint32_t m2 = m - z;  // the m2-th smallest nonzero key
+  constexpr int WPT = 2 * 2048 / kThreads;  // bitmap words per thread
+  uint32_t w[WPT], c = 0u;
+#pragma unroll
+  for (int u = 0; u < WPT; ++u) {
+    w[u] = bmw[WPT * tid + u];
+    c += (uint32_t)__popc(w[u]);
+  }
+  // the thread's exclusive prefix of set bits: a warp scan, the warps' totals through wbuf, and a scan
+  // of those in every warp
+  uint32_t incl = c;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) wbuf[tid >> 5] = incl;
+  __syncthreads();
+  uint32_t wincl = lane < kWarps ? wbuf[lane] : 0u;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, wincl, o);
+    if (lane >= o) wincl += y;
+  }
+  const uint32_t wpre = __shfl_sync(0xffffffffu, wincl, tid >> 5) - wbuf[tid >> 5];  // the warps before
+  const uint32_t excl = wpre + incl - c;
+  if (excl < m2 && m2 <= excl + c) {
+    uint32_t run = excl;
+#pragma unroll
+    for (int u = 0; u < WPT; ++u) {
+      const uint32_t pc = (uint32_t)__popc(w[u]);
+      if (run < m2 && m2 <= run + pc) {
+        uint32_t x = w[u];
+        for (uint32_t t = m2 - run - 1u; t > 0u; --t) x &= x - 1u;
+        sel[0][0] = (uint32_t)(32 * (WPT * tid + u)) + (uint32_t)(__ffs(x) - 1);
+      }
+      run += pc;
+    }
+  }
+  __syncthreads();
+  HS_PHASE(hs_phase_res, 15, threadIdx.x == 0);
+  *T_out = lo + sel[0][0];
+  *need_out = 1u;
+  return true;
 }
 
 // A resolve CTA's last act: once every thread's writes (locs, metadata, fetched rows) are done, count
@@ -586,7 +681,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
   // has arrived and checked only after the hash, so no thread waits for the two loads in a row here.
   int app_slot = -1;
   uint4* app_dh = nullptr;  // the append's place in the host history (known after the hash)
-  __shared__ uint32_t s_dups, s_klo, s_khi;
+  __shared__ uint32_t s_dups, s_klo, s_khi, s_dcnt[2];
   __shared__ unsigned long long s_app_page;
   if (tid == 0) {
     err_bits = 0u;
@@ -595,6 +690,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
     s_dups = 0u;
     s_klo = 0xffffffffu;
     s_khi = 0u;
+    s_dcnt[0] = 0u;
+    s_dcnt[1] = 0u;
   }
   for (int x = tid; x < ht_size; x += kThreads) {
     ht_key[x] = -1;
@@ -818,7 +915,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_resolve(ResolveArgs a) {
   const int ncand = B - h;
   const bool take_all = (m == ncand);
   uint32_t T = 0u, need_eq = 0u;
-  if (m > 0 && !take_all) select_threshold(key32, flag, B, (uint32_t)m, s_klo, s_khi, wbuf, hist, sel, &T, &need_eq);
+  if (m > 0 && !take_all) {
+    // distinct nonzero keys (every policy but random): one bitmap pass over a window that ends at the
+    // largest key (or starts at the smallest when no slot is empty), else the radix select
+    const uint32_t lo = s_klo != 0u ? s_klo : (s_khi >= kDenseSpan ? s_khi - (kDenseSpan - 1u) : 1u);
+    const bool dense = a.policy != HS_POLICY_RANDOM && s_khi - lo < kDenseSpan &&
+                       select_dense(key32, flag, B, (uint32_t)m, lo, wbuf, hist, sel, s_dcnt, &T, &need_eq);
+    if (!dense) select_threshold(key32, flag, B, (uint32_t)m, s_klo, s_khi, wbuf, hist, sel, &T, &need_eq);
+  }
   if (nstage > 0) {
     __syncthreads();  // every early copy has been issued (with its bytes expected)
     if (tid == 0 && a.stall == 0) mbar_arrive1(&bar_stage);

@@ -29,7 +29,7 @@ RESOLVE = dict(enumerate(["start", "append slot", "hash", "probe", "rank", "earl
                           "compaction + cluster sync", "writes", "host fetch"]))
 RESOLVE.update({10: "  thread 0: hash inserts done", 11: "  thread 0: append search reduced",
                 12: "  hash: first barrier passed", 13: "  thread 0: probes done",
-                14: "  select pass 0: histogram", 15: "  select pass 0: bin found",
+                14: "  select pass 0: histogram (or the bitmap)", 15: "  select pass 0: bin (or threshold) found",
                 16: "  select pass 1: histogram", 17: "  select pass 1: bin found",
                 18: "  compaction: counts scanned", 19: "  thread 0: victims placed",
                 20: "  compaction: barrier passed", 21: "fetch CTAs: misses found", 22: "fetch CTAs: done",
