@@ -6,8 +6,9 @@
 // host copies, so the copies of one request are spread over several SMs.  The steps:
 //   (1) build a shared-memory hash table of the k selected positions;
 //   (2) probe every hot-buffer slot in parallel: hit, or a candidate for eviction;
-//   (3) parallel scans: rank hits and misses in top-k order, select the m victims (radix select
-//       on the eviction key, then an ordered compaction), update the recency stamps in place
+//   (3) parallel scans: rank hits and misses in top-k order, select the m victims (a bitmap over
+//       the eviction keys when they are distinct, else a radix select on them; then an ordered
+//       compaction), update the recency stamps in place
 //       (hits to MRU in top-k order, misses after the hits);
 //   (4) fetch the missing records straight from the pinned host history with 16-byte
 //       non-coherent vector loads into the claimed slots, a tuned number of bytes per thread.
