@@ -426,14 +426,7 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 
-#ifndef HS_FETCH_UNROLL
-#define HS_FETCH_UNROLL 8
-#endif
-constexpr int kFetchUnroll = HS_FETCH_UNROLL;  // 16-byte loads a lane has in flight per record
-#ifndef HS_FETCH_WARPS
-#define HS_FETCH_WARPS 32
-#endif
-constexpr int kFetchWarps = HS_FETCH_WARPS;  // warps of a fetch CTA that copy records ahead of the decision
+constexpr int kFetchUnroll = 8;  // 16-byte loads a lane of a fetch CTA has in flight per record
 
 // A fetch CTA (early fetch) does all of the miss fetch for its share [e0, e1) of the request's top-k
 // list, starting at the launch's start:
@@ -511,7 +504,7 @@ __device__ void early_fetch_cta(const ResolveArgs& a, int r, int crank) {
     }
   };
   // (2)
-  for (int x = warp; warp < kFetchWarps && x < n; x += kFetchWarps) {
+  for (int x = warp; x < n; x += kWarps) {
     uint32_t decided = 0u;
     if (lane == 0) decided = ld_acquire_gpu(dec) >= (uint32_t)a.cs ? 1u : 0u;
     if (__shfl_sync(0xffffffffu, decided, 0) != 0u) break;
