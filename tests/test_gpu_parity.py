@@ -592,3 +592,46 @@ def test_pools_of_different_configurations_share_the_kernels():
     for pool, orc in zip(pools, orcs):
         assert_pool_matches_oracle(pool, orc, "pools side by side")
         pool.close()
+
+
+def test_select_beyond_the_bitmap_window():
+    """The one-pass victim select covers a window of 131072 keys below the largest; older candidate
+    keys send it back to the radix select.  One request, k = 2048 in B = 4096 slots, one new position
+    per step and no appends: half the buffer stays empty while the clock passes 131072, and from about
+    step 66 on the candidates include positions dropped at the start, whose stamps lie below the
+    window (checked on the oracle's state before each step).  Slots, stamps, counters and the last
+    step's attention equal the oracle's."""
+    k, B, ctx0, steps = 2048, 4096, 20000, 80
+    cfg = _gqa(1, 1, ctx0, k, B, kvh=1, G=4)  # LRU: a hit is restamped, so the clock runs ahead
+    sc = Scenario(cfg, ctx0=ctx0, steps=steps, appends=False, seed=77)
+    rng = np.random.default_rng(77)
+    order = rng.permutation(ctx0)
+    cur, nxt = [int(x) for x in order[:k]], k
+    trace = np.empty((steps, 1, 1, k), dtype=np.int32)
+    for t in range(steps):
+        if t > 0:  # one selected position replaced by one never selected before: one miss
+            cur[int(rng.integers(k))] = int(order[nxt])
+            nxt += 1
+        trace[t, 0, 0] = cur
+    sc.trace = trace
+    pool = HsPool(cfg)
+    prefill(pool, sc)
+    orc = OracleRun(sc)
+    beyond = 0
+    for t in range(steps):
+        tag, stamp = orc.caches[(0, 0)].slots()
+        chosen = set(trace[t, 0, 0].tolist())
+        keys = [int(s) for tg, s in zip(tag.tolist(), stamp.tolist()) if tg not in chosen]
+        nz = [x for x in keys if x != 0]
+        if nz and 0 in keys:
+            beyond += any(x < max(nz) - 131071 for x in nz)
+        elif nz:
+            beyond += max(nz) - min(nz) >= 131072
+        res = gpu_step(pool, sc, t, attn=(t == steps - 1))
+        ref = orc.step(t)
+        m, locs = ref[(0, 0)]
+        assert np.array_equal(res[0][0][0], locs), t
+    assert beyond > 0  # the scenario did reach keys outside the window
+    assert_attn_close(res[0][1][0], orc.attention(steps - 1, 0, 0), tight=True)
+    assert_pool_matches_oracle(pool, orc, "select window")
+    pool.close()
