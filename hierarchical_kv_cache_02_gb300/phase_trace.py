@@ -10,7 +10,9 @@ prints the median over the CTAs of each stamp, in microseconds from the first CT
 
 Needs a GPU.  The workloads are those of bench.py (GQA with 4 of its 32 layers unless NAME@L names
 the layer count: one layer's steady state is the same, but its host history spans an eighth of the
-bytes).  NAME:early runs the resolve with its fetch CTAs (early_fetch = 1).
+bytes).  NAME:early runs the resolve with its fetch CTAs (early_fetch = 1).  With HS_PHASE_DUMP set
+to a folder, the raw stamps of every CTA ([256][64] nanoseconds, 0 = not stamped) are also saved
+there as NAME_resolve.npy and NAME_attn.npy.
 """
 from __future__ import annotations
 
@@ -130,6 +132,11 @@ def main(argv):
         pool.close()
         print(f"{name}{':' + mode if mode else ''}: misses per (request, layer, step) "
               f"{st['misses'] / (R * L * (W + 1)):.0f} of k = {k}")
+        dump = os.environ.get("HS_PHASE_DUMP")  # a folder: the raw stamps of each workload, as .npy
+        if dump:
+            os.makedirs(dump, exist_ok=True)
+            np.save(os.path.join(dump, f"{name}{'_' + mode if mode else ''}_resolve.npy"), res_tr)
+            np.save(os.path.join(dump, f"{name}{'_' + mode if mode else ''}_attn.npy"), att_tr)
         rows, n = _table(res_tr, RESOLVE)
         print(f"  k_resolve, {n} CTAs (median / min / max over the CTAs, us from the first CTA's start)")
         for nm, cnt, med, lo, hi in rows:
