@@ -983,9 +983,12 @@ def main():
         for name in ("stress_b16_l4", "mla_b8"):
             la = argparse.Namespace(**vars(args))
             la.workload, la.no_e2e = name, True
+            # at least 256 timed layer-steps: a step of these batches takes tens of microseconds, and a
+            # short timed region lets one slow step move the figure by several percent
+            la.steps = max(args.steps, 256 // WORKLOADS[name]["L"])
             res = run_ours(la, dict(WORKLOADS[name]), world, rank, local)
-            latent[name] = {k: res[k] for k in ("value", "unit", "ms_per_step", "us_per_layer", "miss_rate", "roofline",
-                                                "host_link", "gpu_launches", "clocks", "errors", "config")}
+            latent[name] = {k: res[k] for k in ("value", "unit", "steps", "ms_per_step", "us_per_layer", "miss_rate",
+                                                "roofline", "host_link", "gpu_launches", "clocks", "errors", "config")}
         out["shared_latent"] = latent
     if rank == 0 and not args.no_cpu_baseline:
         per, desc, n, split = oracle_sample(w, steps=min(16, args.warmup + args.steps), seed=99,
