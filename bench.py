@@ -539,7 +539,8 @@ def run_ours(args, w, world, rank, local):
         # the kernel that moves the misses over the host link: the resolve, or the attention when the
         # copies were left to it
         # the resolve takes most of a layer's time and is bound by the host link, a resource with no
-        # measured peak: its roofline is this object, against a pinned copy timed in this run
+        # peak in MEASURED_PEAKS.json: its roofline is this object, against a pinned copy timed in
+        # this run
         "host_link": {"kernel": link_kernel, "bound": "host link (NVLink-C2C)",
                       "miss_bytes_per_layer": miss_bytes / (K * L),
                       "achieved_gbs": miss_bytes / link_s / 1e9 if link_s > 0 else None,
